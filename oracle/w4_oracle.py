@@ -1,0 +1,225 @@
+"""CPU oracle for symmetric INT4 group-128 RTN quantisation and the W4A16 matmul.
+
+TEST INFRASTRUCTURE. Only tests/, ``__graft_entry__.smoke()`` and bench.py's
+CPU-baseline / reference leg may import this module. The product package
+(``gemm_rtn_sym_gb300``) never imports it and shares no code with it: the CUDA
+path is checked against this file, never built from it.
+
+What it computes, and from which passage
+-----------------------------------------
+Source: "Qwen3.5-4B, 작게 저장하면 무엇이 달라질까?" (Qwen3.5-4B whole-model
+quantisation study, parksieon.github.io).
+
+* §1, group-quantisation equation: q = clip(round(w/d) + z, q_min, q_max),
+  ŵ = d·(q − z).  The symmetric case has z = 0 (§1 symbol table: symmetric
+  quantisation searches no free zero point).
+* §1, paragraph under the FFN example: a group is 128 consecutive weights of one
+  row along the input direction (72 groups per row at 9216 inputs); each weight
+  keeps its own 4-bit code, only the restore scale d is shared (16 codes, §1
+  symbol table).
+* §2 settings table: RTN group 128, 4-bit weights / BF16 inputs, "minmax ·
+  symmetric" range from the group's extremes, no clipping-ratio search, no
+  calibration input.
+* §1 FFN example y = W x (2560×9216) and §2 Δy = (Ŵ − W) x: the matmul reads the
+  restored weights ŵ = d·q against BF16 inputs.
+
+Where the page is silent this module takes these readings (the library takes the
+same ones, independently):
+
+* divisor and code range: d = max|w| / 7 and q ∈ [−8, 7];
+* d is computed as an fp32 IEEE quotient max|w| / 7, rounded to bf16 with
+  round-to-nearest-even, and w is divided by that STORED bf16 d (so that
+  |ŵ − w| ≤ d/2 holds for the stored scale);
+* round() is round-half-to-even, applied to the fp32 IEEE quotient w / d;
+* an all-zero group, or one whose bf16 d rounds to zero, has d = +0 and q = 0;
+* no flush-to-zero anywhere: subnormal weights and scales are legal;
+* NaN / Inf weights are outside the contract (results unspecified);
+* storage: packed u8 [N, K/2] whose 64-byte block per (row, group) uses the
+  "P1" nibble order defined by :func:`p1_nibble_position`; scales bf16 [N, K/128];
+* the matmul reference accumulates ŵ·x in fp64 (exact products), and the
+  parity bound is |y_gpu − y_ref| ≤ 4e-3 · Σ_k |ŵ_k x_k| + ulp_bf16(y_ref).
+
+Every function below is plain numpy; nothing is blocked, fused or reordered
+beyond what the definitions state.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+GROUP = 128
+Q_MIN, Q_MAX = -8, 7
+DIVISOR = 7.0
+TOL_REL = 4e-3
+
+# P1 nibble order: inside each 32-bit word (8 consecutive k), nibble slot i
+# holds k offset P1_SLOT_K[i].  Slots i and i+4 therefore hold the pair
+# (2i, 2i+1).
+P1_SLOT_K = (0, 2, 4, 6, 1, 3, 5, 7)
+
+
+# ---------------------------------------------------------------------------
+# bf16 <-> binary32, from the IEEE 754 definition of bfloat16 as the upper half
+# of a binary32 word.
+# ---------------------------------------------------------------------------
+def bf16_bits_to_f32(bits) -> np.ndarray:
+    """Exact widening: a bf16 pattern is the high 16 bits of a binary32."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32)
+
+
+def f32_to_bf16_bits_rne(values) -> np.ndarray:
+    """Round binary32 to bfloat16, round-to-nearest, ties to even.
+
+    The 16 discarded bits are compared with half an ulp (0x8000); the kept
+    part is incremented when above half, or exactly half with an odd kept LSB.
+    NaN stays a quiet NaN.
+    """
+    f = np.ascontiguousarray(values, dtype=np.float32)
+    u = f.view(np.uint32)
+    kept = u >> np.uint32(16)
+    rest = u & np.uint32(0xFFFF)
+    round_up = (rest > 0x8000) | ((rest == 0x8000) & ((kept & np.uint32(1)) == 1))
+    out = (kept + round_up.astype(np.uint32)).astype(np.uint32)
+    nan = np.isnan(f)
+    out = np.where(nan, (kept | np.uint32(0x0040)), out)
+    return out.astype(np.uint16)
+
+
+def bf16_ulp(y) -> np.ndarray:
+    """One bf16 ulp at |y|: 2^(max(e, −126) − 7) with e = floor(log2|y|);
+    2^−133 (the smallest bf16 subnormal) at y = 0."""
+    y = np.abs(np.asarray(y, dtype=np.float64))
+    out = np.full(y.shape, 2.0 ** -133)
+    nz = y > 0
+    e = np.floor(np.log2(y[nz]))
+    out[nz] = np.exp2(np.maximum(e, -126.0) - 7.0)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# RTN quantiser (§1 equation with z = 0, §2 "minmax · symmetric", group 128).
+# ---------------------------------------------------------------------------
+def _groups(W_bits: np.ndarray, group: int) -> np.ndarray:
+    W_bits = np.asarray(W_bits, dtype=np.uint16)
+    if W_bits.ndim != 2:
+        raise ValueError("W must be 2-D [N, K]")
+    N, K = W_bits.shape
+    if group != GROUP or K % group:
+        raise ValueError("K must be a multiple of the group size 128")
+    return bf16_bits_to_f32(W_bits).reshape(N, K // group, group)
+
+
+def rtn_scales(W_bits: np.ndarray, group: int = GROUP) -> np.ndarray:
+    """Per (row, group): a = max|w|; d = bf16_rne(fp32(a / 7)).  Returns the
+    scale bit patterns, uint16 [N, K/128]."""
+    w = _groups(W_bits, group)
+    a = np.max(np.abs(w), axis=2)                       # exact
+    d32 = (a / np.float32(DIVISOR)).astype(np.float32)  # IEEE fp32 quotient, RN
+    return f32_to_bf16_bits_rne(d32)
+
+
+def rtn_codes(W_bits: np.ndarray, scale_bits: np.ndarray, group: int = GROUP) -> np.ndarray:
+    """q = clip(round_half_even(w / d), −8, 7), with w / d the fp32 IEEE
+    quotient by the stored bf16 d; q = 0 where d = 0.  int8 [N, K]."""
+    w = _groups(W_bits, group)
+    d = bf16_bits_to_f32(scale_bits)[:, :, None]
+    zero = d == 0
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = (w / np.where(zero, np.float32(1), d)).astype(np.float32)
+    q = np.clip(np.rint(r), Q_MIN, Q_MAX)
+    q = np.where(zero, 0.0, q)
+    return q.astype(np.int8).reshape(w.shape[0], -1)
+
+
+def p1_nibble_position(k_local: int) -> tuple[int, int]:
+    """Where code k_local (0..127) of a group lives inside the group's 64-byte
+    block: returns (byte offset in the block, bit shift inside that byte).
+
+    Chunk j = k_local // 32 is the 16-byte piece at byte 16j; inside it, the
+    32-bit little-endian word w = (k_local % 32) // 8 holds 8 consecutive k;
+    offset e = k_local % 8 sits in nibble slot i with P1_SLOT_K[i] = e, i.e.
+    bits 4i..4i+3 of the word.
+    """
+    j, rem = divmod(k_local, 32)
+    w, e = divmod(rem, 8)
+    i = P1_SLOT_K.index(e)
+    bit = 4 * i
+    return 16 * j + 4 * w + bit // 8, bit % 8
+
+
+def canonical_pack(q: np.ndarray) -> np.ndarray:
+    """Plain nibble packing: byte [n, k/2] holds code(k) in bits 0-3 and
+    code(k+1) in bits 4-7 (two's complement nibbles)."""
+    c = (np.asarray(q, dtype=np.int16) & 0xF).astype(np.uint8)
+    return (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+
+
+def pack_p1(q: np.ndarray) -> np.ndarray:
+    """Stored layout: packed u8 [N, K/2]; the 64-byte block of (n, g) starts
+    at byte n·K/2 + 64g and places each code by :func:`p1_nibble_position`."""
+    q = np.asarray(q, dtype=np.int8)
+    N, K = q.shape
+    G = K // GROUP
+    c = (q.astype(np.int16) & 0xF).astype(np.uint8).reshape(N, G, GROUP)
+    blocks = np.zeros((N, G, 64), dtype=np.uint8)
+    for k_local in range(GROUP):
+        byte, shift = p1_nibble_position(k_local)
+        blocks[:, :, byte] |= (c[:, :, k_local] << shift).astype(np.uint8)
+    return blocks.reshape(N, K // 2)
+
+
+def unpack_p1(packed: np.ndarray, K: int) -> np.ndarray:
+    """Inverse of :func:`pack_p1`: int8 codes [N, K], sign-extended."""
+    packed = np.asarray(packed, dtype=np.uint8)
+    N = packed.shape[0]
+    G = K // GROUP
+    blocks = packed.reshape(N, G, 64)
+    c = np.zeros((N, G, GROUP), dtype=np.int16)
+    for k_local in range(GROUP):
+        byte, shift = p1_nibble_position(k_local)
+        c[:, :, k_local] = (blocks[:, :, byte] >> shift) & 0xF
+    c = np.where(c >= 8, c - 16, c)
+    return c.reshape(N, K).astype(np.int8)
+
+
+def quantize_rtn(W_bits: np.ndarray, group: int = GROUP):
+    """RTN symmetric INT4: W bf16 bits [N, K] -> (packed u8 [N, K/2],
+    scale bits uint16 [N, K/128])."""
+    s = rtn_scales(W_bits, group)
+    q = rtn_codes(W_bits, s, group)
+    return pack_p1(q), s
+
+
+# ---------------------------------------------------------------------------
+# Matmul y = Ŵ x  (§1 FFN example; ŵ = d·q from the §1 equation).
+# ---------------------------------------------------------------------------
+def dequantize_fp64(packed: np.ndarray, scale_bits: np.ndarray, K: int) -> np.ndarray:
+    """ŵ = d·q in fp64 (exact: d has 8 significant bits, q at most 4)."""
+    q = unpack_p1(packed, K).astype(np.float64)
+    d = bf16_bits_to_f32(scale_bits).astype(np.float64)
+    N = q.shape[0]
+    return (q.reshape(N, -1, GROUP) * d[:, :, None]).reshape(N, K)
+
+
+def matmul_fp64(x: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """y[m, n] = Σ_k w[n, k] · x[m, k], fp64 (a library matmul as one step)."""
+    return np.asarray(x, dtype=np.float64) @ np.asarray(w, dtype=np.float64).T
+
+
+def gemm_reference(x_bits: np.ndarray, packed: np.ndarray, scale_bits: np.ndarray, K: int):
+    """Returns (y_ref, s_abs), both fp64 [M, N]: y_ref = Ŵ x and
+    s_abs = Σ_k |ŵ_k x_k|, the magnitude the parity bound scales with."""
+    x = bf16_bits_to_f32(np.asarray(x_bits, dtype=np.uint16)).astype(np.float64)
+    w = dequantize_fp64(packed, scale_bits, K)
+    return matmul_fp64(x, w), matmul_fp64(np.abs(x), np.abs(w))
+
+
+def parity_bound(y_ref: np.ndarray, s_abs: np.ndarray) -> np.ndarray:
+    """Allowed |y_gpu − y_ref| per element: 4e-3 · Σ|ŵx| + one bf16 ulp."""
+    return TOL_REL * s_abs + bf16_ulp(y_ref)
+
+
+def parity_excess(y_bits: np.ndarray, y_ref: np.ndarray, s_abs: np.ndarray) -> np.ndarray:
+    """|y_gpu − y_ref| / bound per element (≤ 1 passes)."""
+    y = bf16_bits_to_f32(np.asarray(y_bits, dtype=np.uint16)).astype(np.float64)
+    return np.abs(y - y_ref) / parity_bound(y_ref, s_abs)

@@ -1,0 +1,86 @@
+"""Planted mistakes: each mutant is a copy of the oracle with one plausible error
+(a wrong rounding rule, a dropped rounding of the scale, a swapped nibble, a
+transposed operand, a wrong divisor ...).  At least one pin must reject every
+mutant, otherwise the pins would not be pinning the oracle down.  The mistakes
+are planted on the CPU, in the oracle's source text; nothing here touches the
+CUDA library.
+"""
+import os
+import types
+
+import pytest
+
+import tests.test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "w4_oracle.py")
+
+MUTANTS = {
+    "round_half_away": ("q = np.clip(np.rint(r), Q_MIN, Q_MAX)",
+                        "q = np.clip(np.trunc(r + np.copysign(0.5, r)), Q_MIN, Q_MAX)"),
+    "round_down_ties": ("q = np.clip(np.rint(r), Q_MIN, Q_MAX)",
+                        "q = np.clip(np.ceil(r - 0.5), Q_MIN, Q_MAX)"),
+    "divisor_8": ("DIVISOR = 7.0", "DIVISOR = 8.0"),
+    "clip_symmetric_7": ("Q_MIN, Q_MAX = -8, 7", "Q_MIN, Q_MAX = -7, 6"),
+    "scale_truncated": ("return f32_to_bf16_bits_rne(d32)",
+                        "return (d32.view(np.uint32) >> np.uint32(16)).astype(np.uint16)"),
+    "divide_by_unrounded_scale": (
+        "d = bf16_bits_to_f32(scale_bits)[:, :, None]",
+        "d = (np.max(np.abs(w), axis=2) / np.float32(DIVISOR)).astype(np.float32)[:, :, None]"),
+    "slot_order_swapped": ("P1_SLOT_K = (0, 2, 4, 6, 1, 3, 5, 7)", "P1_SLOT_K = (0, 1, 2, 3, 4, 5, 6, 7)"),
+    "chunk_order_reversed": ("return 16 * j + 4 * w + bit // 8, bit % 8",
+                             "return 16 * (3 - j) + 4 * w + bit // 8, bit % 8"),
+    "no_sign_extension": ("c = np.where(c >= 8, c - 16, c)", "c = c"),
+    "matmul_reversed_k": ("return np.asarray(x, dtype=np.float64) @ np.asarray(w, dtype=np.float64).T",
+                          "return np.asarray(x, dtype=np.float64)[:, ::-1] @ np.asarray(w, dtype=np.float64).T"),
+    "matmul_weights_transposed": ("return np.asarray(x, dtype=np.float64) @ np.asarray(w, dtype=np.float64).T",
+                                  "return (np.asarray(w, dtype=np.float64) @ np.asarray(x, dtype=np.float64).T).T[:, ::-1]"),
+    "scale_dropped_in_dequant": ("return (q.reshape(N, -1, GROUP) * d[:, :, None]).reshape(N, K)",
+                                 "return q.reshape(N, K)"),
+    "abs_sum_signed": ("return matmul_fp64(x, w), matmul_fp64(np.abs(x), np.abs(w))",
+                       "return matmul_fp64(x, w), np.abs(matmul_fp64(x, w))"),
+    "ulp_off_by_one": ("out[nz] = np.exp2(np.maximum(e, -126.0) - 7.0)",
+                       "out[nz] = np.exp2(np.maximum(e, -126.0) - 6.0)"),
+    "bf16_round_half_up": ("round_up = (rest > 0x8000) | ((rest == 0x8000) & ((kept & np.uint32(1)) == 1))",
+                           "round_up = rest >= 0x8000"),
+}
+
+PIN_TESTS = [
+    lambda: pins.test_hand_worked_groups("A"),
+    lambda: pins.test_hand_worked_groups("B"),
+    pins.test_hand_worked_packed_bytes,
+    pins.test_hand_worked_error_is_half_step,
+    pins.test_scale_rounding_exhaustive,
+    lambda: pins.test_bruteforce_quantize_4x256("normal"),
+    lambda: pins.test_bruteforce_quantize_4x256("ties"),
+    lambda: pins.test_bruteforce_quantize_4x256("outlier"),
+    pins.test_bruteforce_matmul_3x4x256,
+    lambda: pins.test_invariants("ffn"),
+    lambda: pins.test_invariants("outlier"),
+    pins.test_special_groups,
+    pins.test_channel_scaling_identity,
+    pins.test_layout_pair_extraction,
+    pins.test_bf16_rne_against_exact,
+    pins.test_bf16_ulp,
+    pins.test_parity_bound_accepts_exact_and_rejects_offset,
+]
+
+
+def load_mutant(old: str, new: str) -> types.ModuleType:
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor not found exactly once: {old!r}"
+    mod = types.ModuleType("w4_oracle_mutant")
+    exec(compile(src.replace(old, new), "w4_oracle_mutant", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_every_mutant_is_caught(name, monkeypatch):
+    mutant = load_mutant(*MUTANTS[name])
+    monkeypatch.setattr(pins, "O", mutant)
+    caught = []
+    for t in PIN_TESTS:
+        try:
+            t()
+        except Exception as e:  # an assertion, or the mutant breaking outright
+            caught.append(type(e).__name__)
+    assert caught, f"no pin rejects the planted mistake {name!r}"
