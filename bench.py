@@ -1,0 +1,508 @@
+#!/usr/bin/env python3
+"""Benchmark of the W4A16 group-128 RTN path on GB300.
+
+One step = one pass of the whole path over one synthetic matrix: RTN-quantise a
+bf16 weight matrix (w4_quantize_rtn) and run the decode matmul (w4_gemm) on a
+quantised matrix.  The headline workload is the 2560×9216 FFN matrix with 1 %
+outlier input channels and M = 8 token rows (a speculative-verify pass of 7
+drafts + 1).  Inputs rotate over enough distinct copies that every step reads
+its inputs from HBM (the rotation set exceeds 4× the L2 size); the matmul of
+step i reads the copy quantised R/2 steps earlier, so its packed weights are
+not L2-resident either.
+
+Timing: the K timed steps are captured once into a CUDA graph and replayed
+between CUDA events on the launch stream; per-kernel durations come from
+graphs holding only that kernel's K launches, replayed right after.
+Sub-benchmarks (M = 1, M = 8, the 27B-class layer at M ∈ {1,5,7,13}, the
+70B-class layer at M = 208, the 4B-class 200-matrix stack sweep, quantiser
+alone) are reported under "sub".
+
+`--impl reference` times the CPU oracle (the only other program here that
+computes the same thing) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HEADLINE = "outlier"
+HEADLINE_M = 8
+METRIC = "W4A16 g128 GEMV/GEMM HBM GB/s (% of peak) at M=1,8,208; RTN quant GB/s"
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    p.add_argument("--no-sub", action="store_true", help="skip the sub-benchmarks")
+    p.add_argument("--no-sweep", action="store_true", help="skip the 200-matrix stack sweep")
+    p.add_argument("--only", default="", help="comma list of sub-benchmarks to run")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------- bytes / flops
+def gemm_bytes(M, N, K):
+    """Algorithmic bytes of one matmul: packed codes + scales + x + y."""
+    return N * K // 2 + N * (K // 128) * 2 + 2 * M * K + 2 * M * N
+
+
+def quant_bytes(N, K):
+    """Algorithmic bytes of one quantisation: read W, write codes + scales."""
+    return 2 * N * K + N * K // 2 + N * (K // 128) * 2
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def source_hash(name):
+    with open(os.path.join(ROOT, "gemm_rtn_sym_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:12]
+
+
+def traffic_record(kernel_file, kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    summary is missing or the kernel's source changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    h = source_hash(kernel_file)
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == workload:
+                fields = dict(p.split("=", 1) for p in parts[2:] if "=" in p)
+                if fields.get("source") == h:
+                    return float(fields["bytes_per_launch"])
+    return None
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        rows = [[c.strip() for c in l.split(",")] for l in self.lines if l.count(",") >= 8]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": float(rows[0][2]) if rows[0][2].replace(".", "").isdigit() else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())}
+
+
+# ----------------------------------------------------------------- GPU arm
+class Timer:
+    """CUDA-event timing of a callable replayed on the current stream."""
+
+    def __init__(self, torch):
+        self.torch = torch
+
+    def time(self, fn, reps=1):
+        torch = self.torch
+        s = torch.cuda.current_stream()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(s)
+        for _ in range(reps):
+            fn()
+        e1.record(s)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / reps  # seconds per call
+
+
+def capture(torch, fn):
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()  # one eager run on the capture stream before capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    g.replay()  # upload
+    torch.cuda.synchronize()
+    return g
+
+
+def n_copies(torch, bytes_per_copy, minimum=4):
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    return max(minimum, math.ceil(4 * l2 / bytes_per_copy)), l2
+
+
+def headline(torch, w4, wl, steps, warmup, pk):
+    """The timed step: quantise copy i, matmul copy i - R/2 (M = 8)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    N, K = wl.SHAPES[HEADLINE][0]
+    M = HEADLINE_M
+    W0 = wl.weight(HEADLINE, device=dev)
+    x0 = wl.activations(HEADLINE, M, K, device=dev)
+    per_copy = 2 * N * K + N * K // 2 + N * K // 64 + 2 * M * K + 2 * M * N
+    R, l2 = n_copies(torch, per_copy, minimum=8)
+    Ws = [W0.clone() for _ in range(R)]
+    xs = [x0.clone() for _ in range(R)]
+    Ps = [torch.empty((N, K // 2), dtype=torch.uint8, device=dev) for _ in range(R)]
+    Ss = [torch.empty((N, K // 128), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    Ys = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    for r in range(R):
+        w4.w4_quantize_rtn(Ws[r], packed=Ps[r], scales=Ss[r])
+    passes = (M + 15) // 16 if w4.w4_gemm_path_for(M, N, K) == w4.W4_PATH_SMALL_M else 1
+
+    def step(i):
+        a = i % R
+        b = (i + R // 2) % R
+        w4.w4_quantize_rtn(Ws[a], packed=Ps[a], scales=Ss[a])
+        w4.w4_gemm(xs[b], Ps[b], Ss[b], out=Ys[b])
+
+    for i in range(max(3, warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    g_all = capture(torch, lambda: [step(i) for i in range(steps)])
+    g_q = capture(torch, lambda: [w4.w4_quantize_rtn(Ws[i % R], packed=Ps[i % R], scales=Ss[i % R])
+                                  for i in range(steps)])
+    g_g = capture(torch, lambda: [w4.w4_gemm(xs[(i + R // 2) % R], Ps[(i + R // 2) % R],
+                                             Ss[(i + R // 2) % R], out=Ys[(i + R // 2) % R])
+                                  for i in range(steps)])
+    T = Timer(torch)
+    with ClockSampler(dev.index) as clk:
+        t_end = time.time() + 1.0
+        while time.time() < t_end:  # untimed soak so the clock record spans the load
+            g_all.replay()
+        torch.cuda.synchronize()
+        t_step = T.time(g_all.replay) / steps
+    t_q = T.time(g_q.replay) / steps
+    t_g = T.time(g_g.replay) / steps
+    torch.cuda.synchronize()
+    assert w4.w4_last_device_status() == 0
+
+    qb, gb = quant_bytes(N, K), gemm_bytes(M, N, K)
+    bytes_step = qb + gb
+    dominant = ("quantize_rtn_kernel", "w4_quantize.cu", qb, t_q) if t_q >= t_g else \
+        ("gemv_w4_kernel", "w4_gemv.cu", gb, t_g)
+    name, src, dbytes, dt = dominant
+    achieved = dbytes / dt / 1e9
+    traffic = traffic_record(src, name, f"{HEADLINE}-{N}x{K}-M{M}")
+    res = {
+        "value": bytes_step / t_step / 1e9,
+        "ms_per_step": t_step * 1e3,
+        "roofline": {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
+                     "algorithmic_bytes": dbytes, "peak_source": f"{pk['source']} hbm_gbs (burst copy)"},
+        "kernels": {
+            "quantize": {"us": t_q * 1e6, "GB/s": qb / t_q / 1e9, "frac": qb / t_q / 1e9 / pk["hbm_gbs"]},
+            "gemm_m8": {"us": t_g * 1e6, "GB/s": gb / t_g / 1e9, "frac": gb / t_g / 1e9 / pk["hbm_gbs"],
+                        "tok/s": M / t_g},
+        },
+        "clocks": clk.summary(),
+        "gpu_launches": steps * (1 + passes),
+        "rotation": {"copies": R, "bytes_per_copy": per_copy, "l2_bytes": l2},
+    }
+    # end to end through the public API with host buffers
+    Wh = W0.cpu().pin_memory()
+    xh = x0.cpu().pin_memory()
+    ph = torch.empty((N, K // 2), dtype=torch.uint8).pin_memory()
+    sh = torch.empty((N, K // 128), dtype=torch.bfloat16).pin_memory()
+    yh = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step(i):
+        a = i % R
+        b = (i + R // 2) % R
+        Ws[a].copy_(Wh, non_blocking=True)
+        xs[b].copy_(xh, non_blocking=True)
+        w4.w4_quantize_rtn(Ws[a], packed=Ps[a], scales=Ss[a])
+        w4.w4_gemm(xs[b], Ps[b], Ss[b], out=Ys[b])
+        ph.copy_(Ps[a], non_blocking=True)
+        sh.copy_(Ss[a], non_blocking=True)
+        yh.copy_(Ys[b], non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    it = iter(range(steps))
+    t_e2e = T.time(lambda: e2e_step(next(it)), reps=steps)
+    res["e2e"] = {"value": bytes_step / t_e2e / 1e9, "unit": "GB/s",
+                  "h2d_bytes_per_step": 2 * N * K + 2 * M * K,
+                  "d2h_bytes_per_step": N * K // 2 + N * (K // 128) * 2 + 2 * M * N,
+                  "ms_per_step": t_e2e * 1e3}
+    del Ws, xs, Ps, Ss, Ys
+    torch.cuda.empty_cache()
+    return res
+
+
+def gemm_set(torch, w4, wl, workload, Ms, pk, reps=20, path=None):
+    """Matmul over every matrix of a workload (one launch per matrix), per M.
+    Matrices that fit in L2 several times are rotated over copies."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    mats = []
+    shapes = wl.SHAPES[workload]
+    total_packed = sum(n * k // 2 for n, k in shapes)
+    copies = 1 if total_packed > 4 * 126e6 else n_copies(torch, total_packed)[0]
+    cache = {}
+    for i, (N, K) in enumerate(shapes):
+        key = (N, K) if workload == "stack4b" else i
+        if key not in cache:
+            W = wl.weight(workload, i, device=dev)
+            cache[key] = w4.w4_quantize_rtn(W)
+            del W
+        for c in range(copies):
+            p, s = cache[key]
+            mats.append((N, K, p.clone() if (copies > 1 or workload == "stack4b") else p,
+                         s.clone() if (copies > 1 or workload == "stack4b") else s, i))
+    cache.clear()
+    out = {}
+    T = Timer(torch)
+    for M in Ms:
+        xs = {}
+        ys = []
+        for (N, K, p, s, i) in mats:
+            if (K, i if workload != "stack4b" else 0) not in xs:
+                xs[(K, i if workload != "stack4b" else 0)] = wl.activations(workload, M, K, i, device=dev)
+            ys.append(torch.empty((M, N), dtype=torch.bfloat16, device=dev))
+
+        def run():
+            for j, (N, K, p, s, i) in enumerate(mats):
+                x = xs[(K, i if workload != "stack4b" else 0)]
+                if path is None:
+                    w4.w4_gemm(x, p, s, out=ys[j])
+                else:
+                    w4.w4_gemm_ex(x, p, s, out=ys[j], path=path)
+
+        g = capture(torch, run)
+        t = T.time(g.replay, reps=reps) / copies
+        nb = sum(gemm_bytes(M, N, K) for (N, K, _, _, _) in mats) / copies
+        fl = sum(2 * M * N * K for (N, K, _, _, _) in mats) / copies
+        t_hbm = nb / (pk["hbm_gbs"] * 1e9)
+        t_tc = fl / (pk["bf16_tflops"] * 1e12)
+        out[f"M{M}"] = {"us": t * 1e6, "GB/s": nb / t / 1e9, "TFLOP/s": fl / t / 1e12,
+                        "tok/s": M / t, "bound": "hbm" if t_hbm >= t_tc else "tensor",
+                        "frac": max(t_hbm, t_tc) / t,
+                        "path": w4.w4_gemm_path_for(M, mats[0][0], mats[0][1]) if path is None else path}
+        del g, ys, xs
+    assert w4.w4_last_device_status() == 0
+    del mats
+    torch.cuda.empty_cache()
+    return out
+
+
+def quant_set(torch, w4, wl, workload, pk, reps=10):
+    dev = torch.device("cuda", torch.cuda.current_device())
+    N, K = wl.SHAPES[workload][0]
+    W0 = wl.weight(workload, 0, device=dev)
+    R, _ = n_copies(torch, quant_bytes(N, K))
+    Ws = [W0.clone() for _ in range(R)]
+    Ps = [torch.empty((N, K // 2), dtype=torch.uint8, device=dev) for _ in range(R)]
+    Ss = [torch.empty((N, K // 128), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    g = capture(torch, lambda: [w4.w4_quantize_rtn(Ws[r], packed=Ps[r], scales=Ss[r]) for r in range(R)])
+    t = Timer(torch).time(g.replay, reps=reps) / R
+    b = quant_bytes(N, K)
+    del Ws, Ps, Ss, g
+    torch.cuda.empty_cache()
+    return {"us": t * 1e6, "GB/s": b / t / 1e9, "frac": b / t / 1e9 / pk["hbm_gbs"], "shape": [N, K]}
+
+
+def cpu_oracle_sample(wl, rows, reps_seconds=10.0, min_reps=1):
+    """Oracle quantise + matmul of `rows` rows of the headline matrix at M = 8."""
+    import numpy as np
+    import torch
+    from oracle import w4_oracle as O
+
+    N, K = wl.SHAPES[HEADLINE][0]
+    W = wl.bits(wl.weight(HEADLINE))[:rows]
+    x = wl.bits(wl.activations(HEADLINE, HEADLINE_M, K))
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        p, s = O.quantize_rtn(W)
+        O.gemm_reference(x, p, s, K)
+        n += 1
+        el = time.perf_counter() - t0
+        if n >= min_reps and el >= reps_seconds:
+            break
+    b = (quant_bytes(rows, K) + gemm_bytes(HEADLINE_M, rows, K)) * n
+    return b / el / 1e9, el, n
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def config_block(extra=None):
+    N, K = (2560, 9216)
+    c = {"workload": f"{HEADLINE}: W {N}x{K} bf16 N(0,0.02^2) with 1% input channels x8, "
+                     f"RTN sym INT4 g128, x {HEADLINE_M}x{K} bf16 N(0,1)",
+         "M": HEADLINE_M, "N": N, "K": K, "group": 128,
+         "step": "w4_quantize_rtn on one matrix copy + w4_gemm (M=8) on another",
+         "l2": "inputs rotate over copies totalling > 4x L2 (no L2 reuse between steps)"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def run_gpu(args):
+    import torch
+    import gemm_rtn_sym_gb300 as w4
+    from gemm_rtn_sym_gb300 import workloads as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    w4.load()
+    pk = peaks()
+    res = headline(torch, w4, wl, args.steps, args.warmup, pk)
+    t_step = res["ms_per_step"] / 1e3
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([t_step], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_step = float(t.item())
+        dist.barrier()
+    N, K = wl.SHAPES[HEADLINE][0]
+    bytes_step = quant_bytes(N, K) + gemm_bytes(HEADLINE_M, N, K)
+    value = world * bytes_step / t_step / 1e9
+
+    sub = {}
+    if not args.no_sub and rank == 0:
+        only = set(filter(None, args.only.split(",")))
+        want = lambda k: not only or k in only
+        if want("ffn"):
+            sub["ffn_m1"] = gemm_set(torch, w4, wl, "ffn", [1], pk)["M1"]
+        if want("outlier"):
+            sub["outlier_m8"] = gemm_set(torch, w4, wl, "outlier", [8], pk)["M8"]
+        if want("quant"):
+            sub["quant_ffn"] = quant_set(torch, w4, wl, "ffn", pk)
+        if want("layer27b"):
+            sub["layer27b"] = gemm_set(torch, w4, wl, "layer27b", wl.ROWS["layer27b"], pk, reps=10)
+        if want("layer70b"):
+            sub["layer70b"] = gemm_set(torch, w4, wl, "layer70b", wl.ROWS["layer70b"], pk, reps=5)
+        if want("stack4b") and not args.no_sweep:
+            sub["stack4b"] = gemm_set(torch, w4, wl, "stack4b", wl.ROWS["stack4b"], pk, reps=3)
+
+    if rank != 0:
+        return
+    v_cpu, el, n = cpu_oracle_sample(wl, rows=256)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 activations, int4 weights, fp32 accumulate",
+        "data": "synthetic (seeded; no model weights)",
+        "config": config_block({"parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
+        "roofline": res["roofline"], "kernels": res["kernels"], "e2e": res["e2e"],
+        "clocks": res["clocks"], "gpu_launches": res["gpu_launches"], "rotation": res["rotation"],
+        "cpu_baseline": {"value": v_cpu, "unit": "GB/s", "cores": cores(), "kind": "oracle",
+                         "sample": f"oracle quantise + fp64 matmul (M=8) of 256 of the 2560 rows, "
+                                   f"{n} reps in {el:.1f} s; elementwise numpy single-threaded, "
+                                   f"fp64 matmul in the BLAS"},
+        "peaks": pk, "sub": sub,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from gemm_rtn_sym_gb300 import workloads as wl
+    import numpy as np
+    from oracle import w4_oracle as O
+
+    N, K = wl.SHAPES[HEADLINE][0]
+    rows = 64
+    W = wl.bits(wl.weight(HEADLINE))[:rows]
+    x = wl.bits(wl.activations(HEADLINE, HEADLINE_M, K))
+    for _ in range(max(1, args.warmup)):
+        O.gemm_reference(x, *O.quantize_rtn(W), K)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        p, s = O.quantize_rtn(W)
+        O.gemm_reference(x, p, s, K)
+    el = time.perf_counter() - t0
+    b = quant_bytes(rows, K) + gemm_bytes(HEADLINE_M, rows, K)
+    v = b * args.steps / el / 1e9
+    sample = f"each step: oracle quantise + fp64 matmul (M=8) of {rows} of the {N} rows"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+        "data": "synthetic (seeded)", "config": config_block({"sample_rows": rows}),
+        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+// C ABI of the library (declared in include/w4.h): argument checks, kernel
+// choice, launches and the per-device status word of the bounded waits.
+#include <cstdint>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "w4.h"
+#include "w4_device.cuh"
+#include "w4_internal.h"
+
+namespace w4 {
+namespace {
+
+// One status word per device (written by kernels whose bounded waits ran out).
+__device__ unsigned g_status_word = 0;
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_info[kMaxDevices];
+bool g_info_ready[kMaxDevices];
+std::mutex g_info_mutex;
+
+// Smallest M that goes to the tensor-core kernel under W4_PATH_AUTO.
+constexpr int64_t kTensorMinM = INT64_MAX;  // tensor-core kernel not wired in yet
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return na != 0 && nb != 0 && pa < pb + nb && pb < pa + na;
+}
+
+int check_sizes(int64_t N, int64_t K) {
+    if (N < 0 || K < 0) return W4_ERR_INVALID_ARG;
+    if (K % 128 != 0) return W4_ERR_UNSUPPORTED;
+    if (N > 0 && K > (int64_t{1} << 62) / N) return W4_ERR_INVALID_ARG;
+    return W4_OK;
+}
+
+int to_status(cudaError_t e) { return e == cudaSuccess ? W4_OK : W4_ERR_CUDA; }
+
+}  // namespace
+
+const DeviceInfo* device_info(cudaError_t* err) {
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess) return nullptr;
+    if (dev < 0 || dev >= kMaxDevices) {
+        *err = cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_info_mutex);
+    if (!g_info_ready[dev]) {
+        DeviceInfo info;
+        if ((*err = cudaDeviceGetAttribute(&info.sm_count, cudaDevAttrMultiProcessorCount, dev)) ||
+            (*err = cudaDeviceGetAttribute(&info.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) ||
+            (*err = cudaDeviceGetAttribute(&info.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) ||
+            (*err = cudaDeviceGetAttribute(&info.max_smem_optin,
+                                           cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) ||
+            (*err = cudaGetSymbolAddress(reinterpret_cast<void**>(&info.status), g_status_word)))
+            return nullptr;
+        g_info[dev] = info;
+        g_info_ready[dev] = true;
+    }
+    *err = cudaSuccess;
+    return &g_info[dev];
+}
+
+}  // namespace w4
+
+using namespace w4;
+
+extern "C" {
+
+size_t w4_packed_bytes(int64_t N, int64_t K) {
+    if (check_sizes(N, K) != W4_OK) return 0;
+    return static_cast<size_t>(N) * static_cast<size_t>(K) / 2;
+}
+
+size_t w4_scales_bytes(int64_t N, int64_t K, int32_t group) {
+    if (group != 128 || check_sizes(N, K) != W4_OK) return 0;
+    return static_cast<size_t>(N) * static_cast<size_t>(K / 128) * 2;
+}
+
+int w4_quantize_rtn(const void* W, int64_t N, int64_t K, int32_t group, void* packed, void* scales,
+                    void* stream) {
+    if (group != 128) return W4_ERR_UNSUPPORTED;
+    if (const int s = check_sizes(N, K)) return s;
+    if (N == 0 || K == 0) return W4_OK;
+    if (!W || !packed || !scales) return W4_ERR_INVALID_ARG;
+    if (!aligned(W, 16) || !aligned(packed, 16) || !aligned(scales, 2)) return W4_ERR_MISALIGNED;
+    const size_t wb = static_cast<size_t>(N * K) * 2, pb = w4_packed_bytes(N, K),
+                 sb = w4_scales_bytes(N, K, group);
+    if (overlaps(W, wb, packed, pb) || overlaps(W, wb, scales, sb) || overlaps(packed, pb, scales, sb))
+        return W4_ERR_INVALID_ARG;
+    cudaError_t err;
+    const DeviceInfo* dev = device_info(&err);
+    if (!dev) return W4_ERR_CUDA;
+    if (dev->cc_major < 10) return W4_ERR_UNSUPPORTED;
+    return to_status(launch_quantize(W, N, K, packed, scales, *dev, static_cast<cudaStream_t>(stream)));
+}
+
+int w4_gemm_path_for(int64_t M, int64_t N, int64_t K) {
+    if (M < 0) return -W4_ERR_INVALID_ARG;
+    if (const int s = check_sizes(N, K)) return -s;
+    return M >= kTensorMinM ? W4_PATH_TENSOR : W4_PATH_SMALL_M;
+}
+
+int w4_gemm_ex(const void* x, int64_t M, int64_t N, int64_t K, const void* packed, const void* scales,
+               void* y, void* stream, int32_t path) {
+    if (M < 0) return W4_ERR_INVALID_ARG;
+    if (const int s = check_sizes(N, K)) return s;
+    if (M > 0 && K > (int64_t{1} << 62) / M) return W4_ERR_INVALID_ARG;
+    if (M > 0 && N > (int64_t{1} << 62) / M) return W4_ERR_INVALID_ARG;
+    if (path < W4_PATH_AUTO || path > W4_PATH_TENSOR) return W4_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return W4_OK;
+    if (!y) return W4_ERR_INVALID_ARG;
+    if (!aligned(y, 2)) return W4_ERR_MISALIGNED;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t yb = static_cast<size_t>(M * N) * 2;
+    if (K == 0) return to_status(cudaMemsetAsync(y, 0, yb, st));
+    if (!x || !packed || !scales) return W4_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(packed, 16) || !aligned(scales, 2)) return W4_ERR_MISALIGNED;
+    const size_t xb = static_cast<size_t>(M * K) * 2, pb = w4_packed_bytes(N, K),
+                 sb = w4_scales_bytes(N, K, 128);
+    if (overlaps(y, yb, x, xb) || overlaps(y, yb, packed, pb) || overlaps(y, yb, scales, sb))
+        return W4_ERR_INVALID_ARG;
+    cudaError_t err;
+    const DeviceInfo* dev = device_info(&err);
+    if (!dev) return W4_ERR_CUDA;
+    if (dev->cc_major < 10) return W4_ERR_UNSUPPORTED;
+    if (path == W4_PATH_AUTO) path = M >= kTensorMinM ? W4_PATH_TENSOR : W4_PATH_SMALL_M;
+    if (path == W4_PATH_TENSOR)
+        return to_status(launch_gemm_tc(x, M, N, K, packed, scales, y, *dev, st));
+    return to_status(launch_gemv(x, M, N, K, packed, scales, y, *dev, st));
+}
+
+int w4_gemm(const void* x, int64_t M, int64_t N, int64_t K, const void* packed, const void* scales,
+            void* y, void* stream) {
+    return w4_gemm_ex(x, M, N, K, packed, scales, y, stream, W4_PATH_AUTO);
+}
+
+int w4_last_device_status(void* stream) {
+    cudaError_t err;
+    const DeviceInfo* dev = device_info(&err);
+    if (!dev) return W4_ERR_CUDA;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned host = 0;
+    if (cudaMemcpyAsync(&host, dev->status, sizeof(host), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return W4_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return W4_ERR_CUDA;
+    if (host != 0) {
+        const unsigned zero = 0;
+        if (cudaMemcpyAsync(dev->status, &zero, sizeof(zero), cudaMemcpyHostToDevice, st) != cudaSuccess ||
+            cudaStreamSynchronize(st) != cudaSuccess)
+            return W4_ERR_CUDA;
+    }
+    return static_cast<int>(host);
+}
+
+int w4_wait_probe(int64_t limit_ns, int32_t arrive, void* stream) {
+    if (limit_ns < 0) return W4_ERR_INVALID_ARG;
+    cudaError_t err;
+    const DeviceInfo* dev = device_info(&err);
+    if (!dev) return W4_ERR_CUDA;
+    return to_status(launch_wait_probe(limit_ns, arrive, *dev, static_cast<cudaStream_t>(stream)));
+}
+
+const char* w4_status_string(int status) {
+    switch (status) {
+        case W4_OK: return "W4_OK";
+        case W4_ERR_INVALID_ARG: return "W4_ERR_INVALID_ARG: invalid argument";
+        case W4_ERR_UNSUPPORTED: return "W4_ERR_UNSUPPORTED: unsupported size, group or device";
+        case W4_ERR_MISALIGNED: return "W4_ERR_MISALIGNED: pointer alignment";
+        case W4_ERR_CUDA: return "W4_ERR_CUDA: CUDA runtime error";
+        case W4_ERR_TIMEOUT: return "W4_ERR_TIMEOUT: a bounded device wait ran out";
+        default: return "unknown w4 status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,110 @@
+// Device-side helpers shared by the library's kernels: status reporting,
+// bounded mbarrier waits, cache-hinted loads and bf16 nibble decoding.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+
+namespace w4 {
+
+// Mirrors w4_status in include/w4.h.
+constexpr unsigned kStatusOk = 0;
+constexpr unsigned kStatusTimeout = 5;
+
+// Default bound of every wait inside the library's kernels: about a second.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// First error wins; later ones are dropped.
+__device__ __forceinline__ void record_status(unsigned* status, unsigned code) {
+    if (status != nullptr) atomicCAS(status, kStatusOk, code);
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
+        "r"(bytes)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Waits for the phase with the given parity to complete, for at most
+// `limit_ns` nanoseconds of wall time.  Returns false when it gave up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
+    if (mbar_test(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_test(bar, parity)) {
+        if (global_ns() - t0 > limit_ns) return false;
+    }
+    return true;
+}
+
+// ------------------------------------------------------------------ loads
+// Streaming 16-byte load: read once, do not keep in L1.
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Read-only 16-byte load through L1 (data reused by other warps).
+__device__ __forceinline__ uint4 ld_cached(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
+// ------------------------------------------------------------ bf16 helpers
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// Pair i (0..3) of a stored 32-bit code word: nibble slots i and i+4 hold the
+// codes of two consecutive k.  XOR with 0x4308 turns nibble c = q & 0xF into
+// the bf16 pattern of 128 + (c ^ 8) = 136 + q; subtracting 136 (exact) leaves q.
+__device__ __forceinline__ uint32_t code_pair_bf16x2(uint32_t word, int i) {
+    const uint32_t biased = ((word >> (4 * i)) & 0x000F000Fu) ^ 0x43084308u;
+    __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&biased);
+    const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
+    __nv_bfloat162 q = __hsub2(v, off);
+    return *reinterpret_cast<uint32_t*>(&q);
+}
+
+}  // namespace w4

@@ -1,0 +1,36 @@
+// Internal declarations shared by the library's translation units (host side).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace w4 {
+
+// Device facts the launchers size their grids from (cached per device).
+struct DeviceInfo {
+    int sm_count = 0;
+    int cc_major = 0;
+    int cc_minor = 0;
+    int max_smem_optin = 0;
+    unsigned* status = nullptr;  // device address of this device's status word
+};
+
+// Returns nullptr (and sets *err) when the current device cannot be queried.
+const DeviceInfo* device_info(cudaError_t* err);
+
+// Launchers.  Arguments are already validated by the C ABI layer.
+cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, void* packed, void* scales,
+                            const DeviceInfo& dev, cudaStream_t stream);
+
+// Small-M path: any M; it runs one pass per 16 token rows.
+cudaError_t launch_gemv(const void* x, int64_t M, int64_t N, int64_t K, const void* packed,
+                        const void* scales, void* y, const DeviceInfo& dev, cudaStream_t stream);
+
+// Tensor-core path: tcgen05 MMA with TMEM accumulators, any M.
+cudaError_t launch_gemm_tc(const void* x, int64_t M, int64_t N, int64_t K, const void* packed,
+                           const void* scales, void* y, const DeviceInfo& dev, cudaStream_t stream);
+
+cudaError_t launch_wait_probe(int64_t spin_limit, int arrive, const DeviceInfo& dev,
+                              cudaStream_t stream);
+
+}  // namespace w4

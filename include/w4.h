@@ -1,0 +1,148 @@
+/*
+ * w4.h — C ABI of the GB300 (sm_103a) library for symmetric INT4, group-128,
+ * round-to-nearest weight quantisation and the decode-time W4A16 matmul.
+ *
+ * What the library computes
+ * -------------------------
+ * Source: "Qwen3.5-4B, 작게 저장하면 무엇이 달라질까?" (Qwen3.5-4B whole-model
+ * quantisation study).
+ *   §1, group-quantisation equation: q = clip(round(w/d) + z, q_min, q_max),
+ *       ŵ = d·(q − z); the symmetric case has z = 0.
+ *   §1, paragraph under the FFN example y = W x (2560×9216): a group is 128
+ *       consecutive weights of one row along the input direction (72 groups
+ *       per row at 9216 inputs); every weight keeps its own 4-bit code and the
+ *       group shares one restore scale d.
+ *   §2, settings table: RTN, group 128, 4-bit weights and BF16 inputs, range
+ *       from the group's extremes ("minmax · symmetric"), no clipping search,
+ *       no calibration data.
+ * Readings taken where the page is silent: d = bf16_rne(fp32(max|w| / 7)),
+ * q = clamp(round_half_even(fp32(w / d)), −8, 7) with the stored bf16 d, and
+ * d = +0, q = 0 for a group whose d is zero.  No flush-to-zero: subnormal
+ * weights and scales are handled.  NaN/Inf weights are outside the contract
+ * (outputs unspecified, never an out-of-bounds access).
+ *
+ * Data layout (all row-major, dense, no padding)
+ * ----------------------------------------------
+ *   W       bf16  [N, K]        weights, N = output features, K = input features
+ *   packed  u8    [N, K/2]      4-bit two's-complement codes; the 64 bytes of
+ *                               (row n, group g) start at n·K/2 + 64·g.  In that
+ *                               block, 16-byte chunk j holds k = 32j..32j+31; the
+ *                               32-bit little-endian word w of a chunk holds
+ *                               k = 8w..8w+7 (relative to the chunk), and nibble
+ *                               slot i (bits 4i..4i+3) of the word holds offset
+ *                               {0,2,4,6,1,3,5,7}[i].  So slots i and i+4 hold a
+ *                               consecutive pair, ready for a bf16x2 dequant.
+ *   scales  bf16  [N, K/128]    d of (row n, group g) at n·(K/128) + g
+ *   x       bf16  [M, K]        activations (M tokens)
+ *   y       bf16  [M, N]        y[m, n] = Σ_k ŵ[n, k] · x[m, k], rounded to bf16
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *    allocates no device memory and keeps no per-call state.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Work is enqueued asynchronously on it; nothing synchronises, except
+ *    w4_last_device_status().
+ *  - K must be a multiple of 128 and group must be 128; N, M, K ≥ 0.  Sizes
+ *    with N·K ≥ 2^62 are rejected.
+ *  - W, x and packed must be 16-byte aligned; scales and y 2-byte aligned.
+ *  - y must not overlap x, packed or scales; packed/scales must not overlap W.
+ *  - Argument errors are returned synchronously before anything is launched.
+ *    A failed launch returns W4_ERR_CUDA (the CUDA error is left readable with
+ *    cudaGetLastError()).
+ *  - Each call uses the device that is current on the calling thread.
+ */
+#ifndef W4_H_
+#define W4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum w4_status {
+    W4_OK = 0,
+    W4_ERR_INVALID_ARG = 1, /* null pointer, negative size, overlap, overflow   */
+    W4_ERR_UNSUPPORTED = 2, /* group != 128, K % 128 != 0, unsupported device    */
+    W4_ERR_MISALIGNED = 3,  /* pointer alignment below what is stated above     */
+    W4_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed       */
+    W4_ERR_TIMEOUT = 5      /* a bounded device-side wait ran out (see below)    */
+} w4_status;
+
+/* Kernel choice for w4_gemm_ex. */
+typedef enum w4_gemm_path {
+    W4_PATH_AUTO = 0,    /* what w4_gemm does: picked from M (w4_gemm_path_for)  */
+    W4_PATH_SMALL_M = 1, /* register-dequant split-K GEMV, any M (16 per pass)   */
+    W4_PATH_TENSOR = 2   /* tcgen05/TMEM tensor-core tile, any M ≥ 1             */
+} w4_gemm_path;
+
+/* Bytes of the packed code buffer: N·K/2.  0 for invalid sizes. */
+size_t w4_packed_bytes(int64_t N, int64_t K);
+
+/* Bytes of the scale buffer: N·(K/group)·2.  0 for invalid sizes. */
+size_t w4_scales_bytes(int64_t N, int64_t K, int32_t group);
+
+/*
+ * w4_quantize_rtn — RTN symmetric INT4 quantisation of W (§1 equation with
+ * z = 0; §2 settings: group 128, minmax · symmetric, no calibration).
+ *   W       in : bf16 [N, K]
+ *   packed  out: u8   [N, K/2]  (layout above)
+ *   scales  out: bf16 [N, K/128]
+ * Deterministic and bit-exact: for every group, d = bf16_rne(fp32(max|w|/7))
+ * and q = clamp(round_half_even(fp32(w/d)), −8, 7).  N = 0 or K = 0 is a no-op.
+ */
+int w4_quantize_rtn(const void* W, int64_t N, int64_t K, int32_t group,
+                    void* packed, void* scales, void* stream);
+
+/*
+ * w4_gemm — y = Ŵ x with ŵ = d·q (§1 FFN example y = W x; §2: 4-bit weights,
+ * BF16 inputs).  M is the number of token rows: 1 for plain decode, K+1 for a
+ * speculative-verify pass with K drafts.
+ *   x       in : bf16 [M, K]
+ *   packed  in : u8   [N, K/2]   as written by w4_quantize_rtn
+ *   scales  in : bf16 [N, K/128]
+ *   y       out: bf16 [M, N]
+ * Accuracy: |y − Σ_k ŵ x| ≤ 4e-3 · Σ_k |ŵ x| + 1 bf16 ulp per element
+ * (fp32 accumulation; the tensor-core path rounds d·q to bf16 first).
+ * K = 0 writes zeros to y; M = 0 or N = 0 is a no-op.
+ */
+int w4_gemm(const void* x, int64_t M, int64_t N, int64_t K,
+            const void* packed, const void* scales, void* y, void* stream);
+
+/* w4_gemm with an explicit kernel choice (w4_gemm_path); same contract. */
+int w4_gemm_ex(const void* x, int64_t M, int64_t N, int64_t K,
+               const void* packed, const void* scales, void* y, void* stream,
+               int32_t path);
+
+/* The kernel W4_PATH_AUTO picks for these sizes (W4_PATH_SMALL_M or
+ * W4_PATH_TENSOR), or a negative w4_status for invalid sizes. */
+int w4_gemm_path_for(int64_t M, int64_t N, int64_t K);
+
+/*
+ * Every wait inside the library's kernels (mbarrier phases, TMA completion)
+ * is bounded.  A wait that runs out records W4_ERR_TIMEOUT in a per-device
+ * status word and the kernel returns early (its outputs are then undefined).
+ * w4_last_device_status synchronises `stream`, returns the recorded status
+ * (W4_OK if none) and clears it.  Returns W4_ERR_CUDA if synchronisation fails.
+ */
+int w4_last_device_status(void* stream);
+
+/*
+ * Diagnostic for the bounded-wait machinery: launches one CTA that waits on an
+ * mbarrier.  With arrive = 1 the barrier is completed and the wait succeeds;
+ * with arrive = 0 nothing ever completes it and the wait gives up after
+ * `limit_ns` nanoseconds, records W4_ERR_TIMEOUT and exits normally.  Read
+ * the outcome with w4_last_device_status.
+ */
+int w4_wait_probe(int64_t limit_ns, int32_t arrive, void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* w4_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4_H_ */

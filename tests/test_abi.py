@@ -1,0 +1,110 @@
+"""C-ABI library checks that need no GPU: every symbol include/w4.h declares is
+exported, and argument errors are rejected on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gemm_rtn_sym_gb300 as w4
+from gemm_rtn_sym_gb300 import build as b
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(w4.library_path()):
+        b.build()
+    return w4.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "w4.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(w4_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("w4_quantize_rtn", "w4_gemm", "w4_packed_bytes", "w4_scales_bytes",
+                     "w4_last_device_status", "w4_status_string"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in w4.h but not exported"
+        assert name in w4._SIGNATURES, f"{name} has no binding"
+
+
+def test_size_helpers(lib):
+    assert lib.w4_packed_bytes(2560, 9216) == 2560 * 9216 // 2
+    assert lib.w4_scales_bytes(2560, 9216, 128) == 2560 * 72 * 2
+    assert lib.w4_scales_bytes(2560, 9216, 64) == 0
+    assert lib.w4_packed_bytes(4, 100) == 0
+    assert lib.w4_packed_bytes(-1, 128) == 0
+    # packed + scales = 0.515625 bytes per weight
+    assert lib.w4_packed_bytes(7, 384) + lib.w4_scales_bytes(7, 384, 128) == 0.515625 * 7 * 384
+
+
+def test_path_choice(lib):
+    assert lib.w4_gemm_path_for(1, 2560, 9216) == w4.W4_PATH_SMALL_M
+    assert lib.w4_gemm_path_for(16, 2560, 9216) == w4.W4_PATH_SMALL_M
+    assert lib.w4_gemm_path_for(-1, 2560, 9216) == -w4.W4_ERR_INVALID_ARG
+    assert lib.w4_gemm_path_for(1, 2560, 100) == -w4.W4_ERR_UNSUPPORTED
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert lib.w4_status_string(s).decode().startswith("W4_")
+    assert b"unknown" in lib.w4_status_string(99)
+
+
+A16 = 0x10000  # fake, never dereferenced: every case below fails its checks first
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((A16, 4, 256, 64, A16, A16, None), w4.W4_ERR_UNSUPPORTED),        # group 64
+    ((A16, 4, 200, 128, A16, A16, None), w4.W4_ERR_UNSUPPORTED),       # K % 128
+    ((A16, -4, 256, 128, A16, A16, None), w4.W4_ERR_INVALID_ARG),      # negative N
+    ((None, 4, 256, 128, A16, A16, None), w4.W4_ERR_INVALID_ARG),      # null W
+    ((A16 + 8, 4, 256, 128, A16 * 4, A16 * 8, None), w4.W4_ERR_MISALIGNED),
+    ((A16, 4, 256, 128, A16 + 512, A16 * 8, None), w4.W4_ERR_INVALID_ARG),  # packed inside W
+    ((A16, 1 << 40, 1 << 30, 128, A16 * 4, A16 * 8, None), w4.W4_ERR_INVALID_ARG),  # overflow
+])
+def test_quantize_rejects(lib, args, expect):
+    assert lib.w4_quantize_rtn(*args) == expect
+
+
+def test_quantize_empty_is_noop(lib):
+    assert lib.w4_quantize_rtn(None, 0, 256, 128, None, None, None) == w4.W4_OK
+    assert lib.w4_quantize_rtn(None, 4, 0, 128, None, None, None) == w4.W4_OK
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((A16, 1, 4, 200, A16 * 2, A16 * 4, A16 * 8, None, 0), w4.W4_ERR_UNSUPPORTED),
+    ((A16, -1, 4, 256, A16 * 2, A16 * 4, A16 * 8, None, 0), w4.W4_ERR_INVALID_ARG),
+    ((A16, 1, 4, 256, A16 * 2, A16 * 4, A16 * 8, None, 7), w4.W4_ERR_INVALID_ARG),   # bad path
+    ((None, 1, 4, 256, A16 * 2, A16 * 4, A16 * 8, None, 0), w4.W4_ERR_INVALID_ARG),
+    ((A16, 1, 4, 256, A16 * 2, A16 * 4, None, None, 0), w4.W4_ERR_INVALID_ARG),
+    ((A16 + 4, 1, 4, 256, A16 * 2, A16 * 4, A16 * 8, None, 0), w4.W4_ERR_MISALIGNED),
+    ((A16, 1, 4, 256, A16 * 2 + 1, A16 * 4, A16 * 8, None, 0), w4.W4_ERR_MISALIGNED),
+    ((A16, 1, 4, 256, A16 * 2, A16 * 4, A16 * 8 + 1, None, 0), w4.W4_ERR_MISALIGNED),
+    ((A16, 4, 4, 256, A16 * 2, A16 * 4, A16, None, 0), w4.W4_ERR_INVALID_ARG),       # y aliases x
+    ((A16, 1, 4, 256, A16 * 2, A16 * 4, A16 * 2 + 2, None, 0), w4.W4_ERR_INVALID_ARG),  # y in packed
+])
+def test_gemm_rejects(lib, args, expect):
+    assert lib.w4_gemm_ex(*args) == expect
+
+
+def test_gemm_empty_is_noop(lib):
+    assert lib.w4_gemm(None, 0, 4, 256, None, None, None, None) == w4.W4_OK
+    assert lib.w4_gemm(None, 3, 0, 256, None, None, None, None) == w4.W4_OK
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(w4, "_lib", None)
+    monkeypatch.setattr(w4, "library_path", lambda: str(tmp_path / "libw4.so"))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        w4.load()
