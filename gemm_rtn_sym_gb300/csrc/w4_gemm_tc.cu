@@ -1,12 +1,399 @@
-// Tensor-core W4A16 matmul (tcgen05 / TMEM).  Not built yet.
+// Tensor-core W4A16 matmul for larger M: tcgen05.mma (kind::f16, BF16 × BF16 →
+// FP32 in TMEM), weights dequantised into shared memory.
+//
+// Source: Qwen3.5-4B quantisation study, §1 FFN example y = W x with ŵ = d·q
+// (one d per 128 consecutive inputs) and §2 settings (4-bit weights, BF16
+// inputs).  The kernel multiplies bf16_rn(d·q), so its error per weight is at
+// most 2^-9 relative; with fp32 accumulation and the final bf16 rounding the
+// result stays inside 4e-3·Σ|ŵx| + 1 ulp.
+//
+// Tile: 128 weight rows (the MMA's M) × up to 256 tokens (the MMA's N; the
+// token count is rounded up to a multiple of 16, padding rows of x read as
+// zeros) per CTA, K streamed in blocks of 64 through a 4-stage ring:
+//   warp 0      : TMA loads of x tiles (128-byte swizzle) into the ring;
+//   warp 1      : allocates TMEM, one lane issues 4 MMAs (K = 16 each) per
+//                 stage and commits each stage back to its "empty" barrier;
+//   warps 2..5  : one weight row per thread — load 32 bytes of codes (kept two
+//                 stages ahead in registers), decode nibble pairs to bf16 q,
+//                 multiply by d (bf16, round-to-nearest), and store the 128-byte
+//                 row into the stage's A tile in the same 128-byte swizzle the
+//                 MMA descriptor names; then, after the last stage, read the
+//                 accumulator back from TMEM and store y.
+// Every mbarrier wait is bounded; a wait that runs out records a timeout in
+// the status word and the CTA winds down (draining its own TMA copies and
+// MMAs before freeing TMEM).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "w4_device.cuh"
 #include "w4_internal.h"
 
 namespace w4 {
+namespace {
 
-cudaError_t launch_gemm_tc(const void*, int64_t, int64_t, int64_t, const void*, const void*, void*,
-                           const DeviceInfo&, cudaStream_t) {
-    return cudaErrorNotSupported;
+constexpr int kBN = 128;            // weight rows per CTA = MMA M
+constexpr int kBK = 64;             // k per stage: one 128-byte swizzle row of bf16
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr int kDequantWarp0 = 2;
+constexpr int kATileBytes = kBN * kBK * 2;  // 16 KB
+constexpr int kMaxBM = 256;
+constexpr int kPrefetch = 2;        // stages of codes held in registers ahead of use
+
+struct TcArgs {
+    const uint8_t* packed;
+    const uint16_t* scales;
+    __nv_bfloat16* y;
+    int64_t M, N, K;
+    int bm;
+    unsigned* status;
+};
+
+// ------------------------------------------------------------- tcgen05 PTX
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+        "%12, %13, %14, %15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+          "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3}], [%4];" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, groups of 8 rows 1024 bytes apart (stride byte offset); the
+// leading byte offset is unused for this layout.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFF) >> 4);   // start address, bits 0-13
+    d |= static_cast<uint64_t>(1) << 16;                  // leading byte offset (16 B, unused)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;          // stride byte offset
+    d |= static_cast<uint64_t>(1) << 46;                  // descriptor version for tcgen05
+    d |= static_cast<uint64_t>(2) << 61;                  // swizzle mode: 128-byte
+    return d;
+}
+
+// Instruction descriptor for kind::f16: FP32 accumulator, BF16 A and B, both
+// K-major, MMA shape M = 128, N = n.
+__device__ __forceinline__ uint32_t idesc_bf16(int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+           (static_cast<uint32_t>(kBN >> 4) << 24);
+}
+
+// Byte offset of 16-byte chunk c of row r in a 128-byte-swizzled tile.
+__device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
+    return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// q·d for the pair i of a code word, as bf16x2 (exact q, one rounding).
+__device__ __forceinline__ uint32_t deq_pair(uint32_t word, int i, __nv_bfloat162 d2) {
+    const uint32_t q = code_pair_bf16x2(word, i);
+    __nv_bfloat162 v = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&q), d2);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+
+    const int bm = args.bm;
+    const uint32_t b_tile_bytes = static_cast<uint32_t>(bm) * 128u;
+    const uint32_t a_base = base;
+    const uint32_t b_base = base + kStages * kATileBytes;
+    const uint32_t bar_base = b_base + kStages * b_tile_bytes;
+    auto full_a = [&](int s) { return bar_base + 8u * s; };
+    auto full_b = [&](int s) { return bar_base + 8u * (kStages + s); };
+    auto empty = [&](int s) { return bar_base + 8u * (2 * kStages + s); };
+    const uint32_t accum_bar = bar_base + 8u * (3 * kStages);
+    const uint32_t tmem_slot = accum_bar + 8u;
+    volatile uint32_t* tmem_slot_ptr =
+        reinterpret_cast<volatile uint32_t*>(gbase + (tmem_slot - base));
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kBN;
+    const int64_t m0 = static_cast<int64_t>(blockIdx.y) * bm;
+    const int nkb = static_cast<int>(args.K / kBK);
+    const int64_t G = args.K >> 7;
+    uint32_t tmem_cols = 32;
+    while (tmem_cols < static_cast<uint32_t>(bm)) tmem_cols <<= 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_a(s), 128);
+            mbar_init(full_b(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        mbar_init(accum_bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_async_smem();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, tmem_cols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_d = *tmem_slot_ptr;
+
+    bool ok = true;
+    if (warp == 0) {
+        // ------------------------------------------------ x tiles via TMA
+        if (lane == 0) {
+            int issued = 0;
+            for (int kb = 0; kb < nkb && ok; ++kb) {
+                const int s = kb % kStages;
+                const uint32_t r = static_cast<uint32_t>(kb / kStages);
+                if (!mbar_wait(empty(s), (r & 1u) ^ 1u)) { ok = false; break; }
+                mbar_arrive_expect_tx(full_b(s), b_tile_bytes);
+                tma_load_2d(b_base + s * b_tile_bytes, &tmap_x, kb * kBK, static_cast<int>(m0), full_b(s));
+                issued = kb + 1;
+            }
+            if (!ok) {
+                record_status(args.status, kStatusTimeout);
+                // Drain: every issued copy lands before the CTA may exit.
+                for (int kb = (issued > kStages ? issued - kStages : 0); kb < issued; ++kb)
+                    mbar_wait(full_b(kb % kStages), static_cast<uint32_t>(kb / kStages) & 1u);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issue
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(bm);
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int s = kb % kStages;
+                const uint32_t par = static_cast<uint32_t>(kb / kStages) & 1u;
+                if (!mbar_wait(full_b(s), par) || !mbar_wait(full_a(s), par)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t a_s = a_base + s * kATileBytes;
+                const uint32_t b_s = b_base + s * b_tile_bytes;
+#pragma unroll
+                for (int ks = 0; ks < kBK / 16; ++ks)
+                    mma_bf16(tmem_d, sw128_desc(a_s + ks * 32), sw128_desc(b_s + ks * 32), idesc,
+                             (kb | ks) != 0 ? 1u : 0u);
+                mma_commit(empty(s));
+            }
+            mma_commit(accum_bar);  // also tracks MMAs issued before an abort
+            if (!ok) record_status(args.status, kStatusTimeout);
+        }
+    } else {
+        // ------------------------------------------------ dequant producers
+        const int t = threadIdx.x - 32 * kDequantWarp0;  // weight row within the tile
+        const int64_t n = n0 + t;
+        const bool valid = n < args.N;
+        const uint8_t* row = args.packed + (valid ? n : 0) * (args.K >> 1);
+        const uint16_t* srow = args.scales + (valid ? n : 0) * G;
+
+        struct Codes {
+            uint4 lo, hi;
+            uint32_t d;
+        };
+        auto fetch = [&](int kb) {
+            Codes c;
+            if (valid && kb < nkb) {
+                const uint8_t* p = row + (kb >> 1) * 64 + (kb & 1) * 32;
+                c.lo = ld_stream(p);
+                c.hi = ld_stream(p + 16);
+                c.d = __ldg(srow + (kb >> 1));
+            } else {
+                c.lo = make_uint4(0, 0, 0, 0);
+                c.hi = make_uint4(0, 0, 0, 0);
+                c.d = 0;
+            }
+            return c;
+        };
+        Codes ring[kPrefetch];
+#pragma unroll
+        for (int i = 0; i < kPrefetch; ++i) ring[i] = fetch(i);
+
+        for (int kb0 = 0; kb0 < nkb && ok; kb0 += kPrefetch) {
+#pragma unroll
+            for (int i = 0; i < kPrefetch; ++i) {
+                const int kb = kb0 + i;
+                if (kb < nkb && ok) {
+                    const int s = kb % kStages;
+                    const uint32_t r = static_cast<uint32_t>(kb / kStages);
+                    const Codes cur = ring[i];
+                    ring[i] = fetch(kb + kPrefetch);
+                    if (!mbar_wait(empty(s), (r & 1u) ^ 1u)) {
+                        ok = false;
+                    } else {
+                        const uint32_t d2bits = cur.d | (cur.d << 16);
+                        const __nv_bfloat162 d2 = *reinterpret_cast<const __nv_bfloat162*>(&d2bits);
+                        const uint32_t words[8] = {cur.lo.x, cur.lo.y, cur.lo.z, cur.lo.w,
+                                                   cur.hi.x, cur.hi.y, cur.hi.z, cur.hi.w};
+                        uint8_t* a_row = gbase + (a_base - base) + s * kATileBytes;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            uint4 v;
+                            v.x = deq_pair(words[c], 0, d2);
+                            v.y = deq_pair(words[c], 1, d2);
+                            v.z = deq_pair(words[c], 2, d2);
+                            v.w = deq_pair(words[c], 3, d2);
+                            *reinterpret_cast<uint4*>(a_row + sw128_offset(t, c)) = v;
+                        }
+                        fence_async_smem();
+                        mbar_arrive(full_a(s));
+                    }
+                }
+            }
+        }
+        if (!ok) record_status(args.status, kStatusTimeout);
+
+        // ------------------------------------------------ epilogue
+        // tcgen05.ld is warp-collective: decide per warp, not per thread.
+        ok = __all_sync(0xffffffffu, ok);
+        const bool acc_ready = ok && __all_sync(0xffffffffu, mbar_wait(accum_bar, 0));
+        if (acc_ready) {
+            tc_fence_after();
+            const int q = warp & 3;  // TMEM lane quarter this warp may access
+            const int64_t ny = n0 + q * 32 + lane;
+            const uint32_t taddr = tmem_d + (static_cast<uint32_t>(q * 32) << 16);
+            for (int c0 = 0; c0 < bm; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld16(taddr + c0, v);
+                if (ny < args.N) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int64_t m = m0 + c0 + j;
+                        if (m < args.M) args.y[m * args.N + ny] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                    }
+                }
+            }
+        } else if (ok) {
+            record_status(args.status, kStatusTimeout);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        // MMAs still in flight (after an abort) must finish before TMEM is freed.
+        if (lane == 0) mbar_wait(accum_bar, 0);
+        __syncwarp();
+        tmem_dealloc(tmem_d, tmem_cols);
+    }
+}
+
+// ------------------------------------------------------------------- host
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+std::mutex g_attr_mutex;
+bool g_attr_set[64];
+
+cudaError_t get_encoder() {
+    std::call_once(g_encode_once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode ? cudaSuccess : cudaErrorNotSupported;
+}
+
+int smem_bytes(int bm) { return kStages * (kATileBytes + bm * 128) + 8 * (3 * kStages + 2) + 1024; }
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const void* x, int64_t M, int64_t N, int64_t K, const void* packed,
+                           const void* scales, void* y, const DeviceInfo& dev, cudaStream_t stream) {
+    if (cudaError_t e = get_encoder()) return e;
+    const int64_t m_tiles = (M + kMaxBM - 1) / kMaxBM;
+    int64_t bm = (M + m_tiles - 1) / m_tiles;
+    bm = (bm + 15) / 16 * 16;
+    const int64_t n_tiles = (N + kBN - 1) / kBN;
+    if (n_tiles > 0x7fffffffLL || m_tiles > 65535 || M > 0x7fffffffLL || K > 0x7fffffffLL)
+        return cudaErrorInvalidConfiguration;
+    const int smem = smem_bytes(static_cast<int>(bm));
+    if (smem > dev.max_smem_optin) return cudaErrorInvalidConfiguration;
+
+    CUtensorMap tmap;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(bm)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (g_encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+
+    int device = 0;
+    if (cudaError_t e = cudaGetDevice(&device)) return e;
+    {
+        std::lock_guard<std::mutex> lock(g_attr_mutex);
+        if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+        if (!g_attr_set[device]) {
+            if (cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     smem_bytes(kMaxBM)))
+                return e;
+            g_attr_set[device] = true;
+        }
+    }
+    TcArgs args;
+    args.packed = static_cast<const uint8_t*>(packed);
+    args.scales = static_cast<const uint16_t*>(scales);
+    args.y = static_cast<__nv_bfloat16*>(y);
+    args.M = M;
+    args.N = N;
+    args.K = K;
+    args.bm = static_cast<int>(bm);
+    args.status = dev.status;
+    dim3 grid(static_cast<unsigned>(n_tiles), static_cast<unsigned>(m_tiles));
+    gemm_tc_kernel<<<grid, kThreads, smem, stream>>>(tmap, args);
+    return cudaGetLastError();
 }
 
 }  // namespace w4

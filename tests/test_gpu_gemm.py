@@ -11,7 +11,8 @@ from tests.helpers import check_gemm, check_quantize, gemm_gpu, quantize_gpu, sa
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-PATHS = [w4.W4_PATH_SMALL_M]
+PATHS = [pytest.param(w4.W4_PATH_SMALL_M, id="small"), pytest.param(w4.W4_PATH_TENSOR, id="tensor")]
+PATH_VALUES = [w4.W4_PATH_SMALL_M, w4.W4_PATH_TENSOR]
 
 
 def run(cuda_lib, W, M, path, seed=0, x=None):
@@ -112,7 +113,7 @@ def test_index_probe(cuda_lib):
     x = torch.zeros((len(ks), K), dtype=torch.bfloat16)
     for i, k in enumerate(ks):
         x[i, k] = 1.0
-    for path in PATHS:
+    for path in PATH_VALUES:
         y = gemm_gpu(cuda_lib, x.to(DEV), packed, scales, path).float().cpu().numpy()
         for i, k in enumerate(ks):
             expect = what[:, k].astype(np.float32)
