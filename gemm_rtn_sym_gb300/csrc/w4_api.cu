@@ -21,7 +21,7 @@ bool g_info_ready[kMaxDevices];
 std::mutex g_info_mutex;
 
 // Smallest M that goes to the tensor-core kernel under W4_PATH_AUTO.
-constexpr int64_t kTensorMinM = INT64_MAX;  // tensor-core kernel not wired in yet
+constexpr int64_t kTensorMinM = 17;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
