@@ -5,16 +5,20 @@
 // §2 settings (4-bit weights, BF16 inputs).
 //
 // Design (HBM-bound at M ≤ 16):
-//  * One warp owns 16 output rows and a contiguous range of groups; the CTA's
-//    warps split the row tile's groups (split-K) and their fp32 partials are
+//  * One warp owns RT tiles of 16 output rows and a contiguous range of groups;
+//    the CTA's warps split the groups (split-K) and their fp32 partials are
 //    summed in shared memory in a fixed order, so results are deterministic.
 //  * Each lane streams one 16-byte chunk (32 codes) per row per group straight
 //    from HBM into registers, `kDepth` groups ahead of use.  The stored nibble
 //    order makes every 32-bit word yield four bf16x2 pairs with one shift, one
 //    LOP3 and one exact bf16x2 subtract each, with no shuffles.
+//  * The activations of the same groups are staged `kDepth` groups ahead into a
+//    per-warp shared-memory ring with cp.async (no registers held while in
+//    flight); token rows beyond M are zeroed once and never copied.  The row
+//    pitch and chunk order of the ring make the fragment loads conflict-free.
 //  * The products q·x go through the legacy tensor-core MMA (m16n8k16, bf16 in,
 //    fp32 accumulate) from registers: the 16 rows are the MMA's M, up to 8 tokens
-//    its N.  At 2 B per weight-pair of HBM traffic the SM must consume about 45
+//    its N.  At 0.5 B per weight of HBM traffic the SM must consume about 45
 //    weights per clock; one fp32 FMA per weight and token plus the decode would
 //    exceed the SM's 128 lanes already at M ≈ 2, while the MMA retires 2048
 //    multiply-adds per instruction.  The tensor pipe is therefore used as an ALU
@@ -26,6 +30,8 @@
 //    32·tig + 4s + {2,3} (MMA k = 2tig+8, 2tig+9) for both A (weights) and B (x).
 //    Any consistent permutation of k leaves the sum unchanged; this one makes a
 //    thread's weights one 16-byte chunk and its activations 64 contiguous bytes.
+#include <mutex>
+
 #include "w4_device.cuh"
 #include "w4_internal.h"
 
@@ -33,7 +39,13 @@ namespace w4 {
 namespace {
 
 constexpr int kGemvMaxWarps = 8;
-constexpr int kDepth = 4;  // groups of weights in flight per thread
+constexpr int kDepth = 4;       // groups in flight per warp (weights in registers, x in shared memory)
+constexpr int kXPitch = 272;    // bytes per staged token row of one group: 256 + 16 of padding
+
+// Position of 16-byte chunk ch (0..15) of a staged x row.  With the 272-byte
+// pitch this places the eight chunks one load instruction phase reads (two
+// token rows x four quads) in eight different bank groups.
+__device__ __forceinline__ int x_phys_chunk(int ch) { return ch ^ ((ch >> 3) << 1); }
 
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                                uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -44,18 +56,22 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint3
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+template <int RT>
 struct Slot {
-    uint4 wa, wb;        // 16-byte code chunks of rows gid and gid+8
-    uint32_t da, db;     // their bf16 scale bits (low 16 bits)
+    uint4 w[RT][2];        // 16-byte code chunks of rows gid and gid+8 of each row tile
+    uint32_t d[RT][2];     // their bf16 scale bits (low 16 bits)
 };
 
-// MT: token tiles of 8 (1: M ≤ 8, 2: M ≤ 16).
-template <int MT>
+// MT: token tiles of 8 (1: M <= 8, 2: M <= 16).  RT: 16-row tiles per warp.
+template <int MT, int RT>
 __global__ void __launch_bounds__(32 * kGemvMaxWarps)
 gemv_w4_kernel(const __nv_bfloat16* __restrict__ x, int M, int64_t N, int64_t K,
                const uint8_t* __restrict__ packed, const __nv_bfloat16* __restrict__ scales,
                __nv_bfloat16* __restrict__ y) {
-    __shared__ float red[kGemvMaxWarps][MT][4][32];
+    extern __shared__ __align__(16) uint8_t xs_raw[];
+    __shared__ float red[kGemvMaxWarps][RT][MT][4][32];
+    constexpr int XR = MT * 8;                 // staged token rows
+    constexpr int kSlot = XR * kXPitch;        // bytes of one staged group
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -64,149 +80,212 @@ gemv_w4_kernel(const __nv_bfloat16* __restrict__ x, int M, int64_t N, int64_t K,
     const int tig = lane & 3;
     const int64_t G = K >> 7;
     const int64_t half_k = K >> 1;
-
-    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * 16;
-    const int64_t na = n0 + gid;
-    const int64_t nb = na + 8;
-    const bool va = na < N;
-    const bool vb = nb < N;
+    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * 16 * RT;
 
     const int64_t g0 = (warp * G) / n_warps;
     const int64_t g1 = ((warp + 1) * G) / n_warps;
-    const int64_t ng = g1 - g0;
+    const int ng = static_cast<int>(g1 - g0);
 
-    const uint8_t* pa = packed + (va ? na : 0) * half_k + tig * 16;
-    const uint8_t* pb = packed + (vb ? nb : 0) * half_k + tig * 16;
-    const uint16_t* sa = reinterpret_cast<const uint16_t*>(scales) + (va ? na : 0) * G;
-    const uint16_t* sb = reinterpret_cast<const uint16_t*>(scales) + (vb ? nb : 0) * G;
-
-    const __nv_bfloat16* xr[MT];
-    bool xv[MT];
+    const uint8_t* pa[RT];
+    const uint8_t* pb[RT];
+    const uint16_t* sa[RT];
+    const uint16_t* sb[RT];
+    bool va[RT], vb[RT];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-        const int m = mt * 8 + gid;
-        xv[mt] = m < M;
-        xr[mt] = x + static_cast<int64_t>(xv[mt] ? m : 0) * K + tig * 32;
+    for (int rt = 0; rt < RT; ++rt) {
+        const int64_t na = n0 + rt * 16 + gid, nb = na + 8;
+        va[rt] = na < N;
+        vb[rt] = nb < N;
+        pa[rt] = packed + (va[rt] ? na : 0) * half_k + (g0 * 64 + tig * 16);
+        pb[rt] = packed + (vb[rt] ? nb : 0) * half_k + (g0 * 64 + tig * 16);
+        sa[rt] = reinterpret_cast<const uint16_t*>(scales) + (va[rt] ? na : 0) * G + g0;
+        sb[rt] = reinterpret_cast<const uint16_t*>(scales) + (vb[rt] ? nb : 0) * G + g0;
     }
 
-    auto load_slot = [&](Slot& s, int64_t g) {
-        s.wa = va ? ld_stream(pa + g * 64) : make_uint4(0, 0, 0, 0);
-        s.wb = vb ? ld_stream(pb + g * 64) : make_uint4(0, 0, 0, 0);
-        s.da = va ? __ldg(sa + g) : 0u;
-        s.db = vb ? __ldg(sb + g) : 0u;
+    // Per-warp ring of staged x groups.  Token rows >= M stay zero.
+    const uint32_t xbase = smem_addr(xs_raw) + static_cast<uint32_t>(warp * kDepth * kSlot);
+    const int m_real = M < XR ? M : XR;
+    for (int i = lane; i < kDepth * (XR - m_real) * 17; i += 32) {
+        const int per_slot = (XR - m_real) * 17;
+        const int slot = i / per_slot, rest = i % per_slot;
+        sts128(xbase + slot * kSlot + (m_real + rest / 17) * kXPitch + (rest % 17) * 16, make_uint4(0, 0, 0, 0));
+    }
+    __syncwarp();
+    const __nv_bfloat16* xg = x + g0 * 128;
+    auto issue_x = [&](int slot, int gi) {
+        for (int p = lane; p < m_real * 16; p += 32) {
+            const int r = p >> 4, ch = p & 15;
+            cp_async16(xbase + slot * kSlot + r * kXPitch + x_phys_chunk(ch) * 16,
+                       xg + static_cast<int64_t>(r) * K + gi * 128 + ch * 8);
+        }
+    };
+    auto load_w = [&](Slot<RT>& s, int gi) {
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-            if (xv[mt]) prefetch_l1(xr[mt] + g * 128);
+        for (int rt = 0; rt < RT; ++rt) {
+            s.w[rt][0] = va[rt] ? ld_stream(pa[rt] + gi * 64) : make_uint4(0, 0, 0, 0);
+            s.w[rt][1] = vb[rt] ? ld_stream(pb[rt] + gi * 64) : make_uint4(0, 0, 0, 0);
+            s.d[rt][0] = va[rt] ? __ldg(sa[rt] + gi) : 0u;
+            s.d[rt][1] = vb[rt] ? __ldg(sb[rt] + gi) : 0u;
+        }
     };
 
-    float acc[MT][4];
+    float acc[RT][MT][4];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
+    for (int rt = 0; rt < RT; ++rt)
 #pragma unroll
-        for (int r = 0; r < 4; ++r) acc[mt][r] = 0.0f;
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[rt][mt][r] = 0.0f;
 
-    Slot ring[kDepth];
+    Slot<RT> ring[kDepth];
 #pragma unroll
-    for (int i = 0; i < kDepth; ++i)
-        if (i < ng) load_slot(ring[i], g0 + i);
+    for (int i = 0; i < kDepth; ++i) {
+        if (i < ng) {
+            load_w(ring[i], i);
+            issue_x(i, i);
+        }
+        cp_async_commit();
+    }
 
-    for (int64_t it = 0; it < ng; it += kDepth) {
+    for (int it = 0; it < ng; it += kDepth) {
 #pragma unroll
         for (int i = 0; i < kDepth; ++i) {
-            const int64_t gi = it + i;
+            const int gi = it + i;
             if (gi < ng) {
-                const Slot cur = ring[i];
-                if (gi + kDepth < ng) load_slot(ring[i], g0 + gi + kDepth);
-                const int64_t g = g0 + gi;
-
+                const Slot<RT> cur = ring[i];
+                cp_async_wait<kDepth - 1>();
+                __syncwarp();
                 uint32_t xw[MT][16];
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt) {
+                    const uint32_t row = xbase + i * kSlot + (mt * 8 + gid) * kXPitch;
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
-                        const uint4 t = xv[mt] ? ld_cached(xr[mt] + g * 128 + v * 8)
-                                               : make_uint4(0, 0, 0, 0);
+                        const uint4 t = lds128(row + x_phys_chunk(4 * tig + v) * 16);
                         xw[mt][4 * v + 0] = t.x;
                         xw[mt][4 * v + 1] = t.y;
                         xw[mt][4 * v + 2] = t.z;
                         xw[mt][4 * v + 3] = t.w;
                     }
                 }
+                __syncwarp();
+                if (gi + kDepth < ng) {
+                    load_w(ring[i], gi + kDepth);
+                    issue_x(i, gi + kDepth);
+                }
+                cp_async_commit();
 
-                float cg[MT][4];
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) cg[mt][r] = 0.0f;
-
-                const uint32_t wa[4] = {cur.wa.x, cur.wa.y, cur.wa.z, cur.wa.w};
-                const uint32_t wb[4] = {cur.wb.x, cur.wb.y, cur.wb.z, cur.wb.w};
-#pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    const int w = s >> 1;
-                    const int h = s & 1;
-                    const uint32_t a0 = code_pair_bf16x2(wa[w], 2 * h);
-                    const uint32_t a2 = code_pair_bf16x2(wa[w], 2 * h + 1);
-                    const uint32_t a1 = code_pair_bf16x2(wb[w], 2 * h);
-                    const uint32_t a3 = code_pair_bf16x2(wb[w], 2 * h + 1);
+                for (int rt = 0; rt < RT; ++rt) {
+                    float cg[MT][4];
 #pragma unroll
                     for (int mt = 0; mt < MT; ++mt)
-                        mma_bf16_16816(cg[mt], a0, a1, a2, a3, xw[mt][2 * s], xw[mt][2 * s + 1]);
-                }
-                const float da = bf16_lo(cur.da);
-                const float db = bf16_lo(cur.db);
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    acc[mt][0] = fmaf(da, cg[mt][0], acc[mt][0]);
-                    acc[mt][1] = fmaf(da, cg[mt][1], acc[mt][1]);
-                    acc[mt][2] = fmaf(db, cg[mt][2], acc[mt][2]);
-                    acc[mt][3] = fmaf(db, cg[mt][3], acc[mt][3]);
+                        for (int r = 0; r < 4; ++r) cg[mt][r] = 0.0f;
+                    const uint32_t wa[4] = {cur.w[rt][0].x, cur.w[rt][0].y, cur.w[rt][0].z, cur.w[rt][0].w};
+                    const uint32_t wb[4] = {cur.w[rt][1].x, cur.w[rt][1].y, cur.w[rt][1].z, cur.w[rt][1].w};
+#pragma unroll
+                    for (int s = 0; s < 8; ++s) {
+                        const int w = s >> 1;
+                        const int h = s & 1;
+                        const uint32_t a0 = code_pair_bf16x2(wa[w], 2 * h);
+                        const uint32_t a2 = code_pair_bf16x2(wa[w], 2 * h + 1);
+                        const uint32_t a1 = code_pair_bf16x2(wb[w], 2 * h);
+                        const uint32_t a3 = code_pair_bf16x2(wb[w], 2 * h + 1);
+#pragma unroll
+                        for (int mt = 0; mt < MT; ++mt)
+                            mma_bf16_16816(cg[mt], a0, a1, a2, a3, xw[mt][2 * s], xw[mt][2 * s + 1]);
+                    }
+                    const float da = bf16_lo(cur.d[rt][0]);
+                    const float db = bf16_lo(cur.d[rt][1]);
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt) {
+                        acc[rt][mt][0] = fmaf(da, cg[mt][0], acc[rt][mt][0]);
+                        acc[rt][mt][1] = fmaf(da, cg[mt][1], acc[rt][mt][1]);
+                        acc[rt][mt][2] = fmaf(db, cg[mt][2], acc[rt][mt][2]);
+                        acc[rt][mt][3] = fmaf(db, cg[mt][3], acc[rt][mt][3]);
+                    }
                 }
             }
         }
     }
+    cp_async_wait<0>();
 
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
+    for (int rt = 0; rt < RT; ++rt)
 #pragma unroll
-        for (int r = 0; r < 4; ++r) red[warp][mt][r][lane] = acc[mt][r];
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) red[warp][rt][mt][r][lane] = acc[rt][mt][r];
     __syncthreads();
 
-    for (int e = threadIdx.x; e < MT * 4 * 32; e += blockDim.x) {
-        const int mt = e / 128;
+    for (int e = threadIdx.x; e < RT * MT * 4 * 32; e += blockDim.x) {
+        const int rt = e / (MT * 128);
+        const int mt = (e / 128) % MT;
         const int r = (e / 32) & 3;
         const int l = e & 31;
         float v = 0.0f;
-        for (int w = 0; w < n_warps; ++w) v += red[w][mt][r][l];
-        const int64_t n = n0 + (l >> 2) + (r >= 2 ? 8 : 0);
+        for (int w = 0; w < n_warps; ++w) v += red[w][rt][mt][r][l];
+        const int64_t n = n0 + rt * 16 + (l >> 2) + (r >= 2 ? 8 : 0);
         const int m = mt * 8 + 2 * (l & 3) + (r & 1);
         if (n < N && m < M) y[static_cast<int64_t>(m) * N + n] = __float2bfloat16_rn(v);
     }
+}
+
+template <int MT, int RT>
+int gemv_smem_bytes(int warps) {
+    return warps * kDepth * MT * 8 * kXPitch;
+}
+
+std::mutex g_attr_mutex;
+bool g_attr_set[64][4];
+
+template <int MT, int RT>
+cudaError_t launch_one(const __nv_bfloat16* x, int mp, int64_t N, int64_t K, const uint8_t* packed,
+                       const __nv_bfloat16* scales, __nv_bfloat16* y, int warps, cudaStream_t stream) {
+    int device = 0;
+    if (cudaError_t e = cudaGetDevice(&device)) return e;
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    const int variant = (MT - 1) * 2 + (RT - 1);
+    {
+        std::lock_guard<std::mutex> lock(g_attr_mutex);
+        if (!g_attr_set[device][variant]) {
+            if (cudaError_t e = cudaFuncSetAttribute(gemv_w4_kernel<MT, RT>,
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     gemv_smem_bytes<MT, RT>(kGemvMaxWarps)))
+                return e;
+            g_attr_set[device][variant] = true;
+        }
+    }
+    const int64_t blocks = (N + 16 * RT - 1) / (16 * RT);
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    gemv_w4_kernel<MT, RT><<<static_cast<unsigned>(blocks), 32 * warps, gemv_smem_bytes<MT, RT>(warps),
+                             stream>>>(x, mp, N, K, packed, scales, y);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_gemv(const void* x, int64_t M, int64_t N, int64_t K, const void* packed,
                         const void* scales, void* y, const DeviceInfo& dev, cudaStream_t stream) {
-    (void)dev;
     const int64_t G = K / 128;
     const int warps = static_cast<int>(G < kGemvMaxWarps ? G : kGemvMaxWarps);
-    const int64_t blocks = (N + 15) / 16;
-    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    // Two row tiles per warp halve the x traffic per weight when there are
+    // still at least two CTAs per SM.
+    const bool two_tiles = (N + 31) / 32 >= 2 * static_cast<int64_t>(dev.sm_count);
     const auto* xb = static_cast<const __nv_bfloat16*>(x);
+    const auto* pk = static_cast<const uint8_t*>(packed);
+    const auto* sc = static_cast<const __nv_bfloat16*>(scales);
     auto* yb = static_cast<__nv_bfloat16*>(y);
     for (int64_t m0 = 0; m0 < M; m0 += 16) {
         const int mp = static_cast<int>(M - m0 < 16 ? M - m0 : 16);
-        if (mp <= 8) {
-            gemv_w4_kernel<1><<<static_cast<unsigned>(blocks), 32 * warps, 0, stream>>>(
-                xb + m0 * K, mp, N, K, static_cast<const uint8_t*>(packed),
-                static_cast<const __nv_bfloat16*>(scales), yb + m0 * N);
-        } else {
-            gemv_w4_kernel<2><<<static_cast<unsigned>(blocks), 32 * warps, 0, stream>>>(
-                xb + m0 * K, mp, N, K, static_cast<const uint8_t*>(packed),
-                static_cast<const __nv_bfloat16*>(scales), yb + m0 * N);
-        }
-        const cudaError_t e = cudaGetLastError();
+        cudaError_t e;
+        if (mp <= 8)
+            e = two_tiles ? launch_one<1, 2>(xb + m0 * K, mp, N, K, pk, sc, yb + m0 * N, warps, stream)
+                          : launch_one<1, 1>(xb + m0 * K, mp, N, K, pk, sc, yb + m0 * N, warps, stream);
+        else
+            e = two_tiles ? launch_one<2, 2>(xb + m0 * K, mp, N, K, pk, sc, yb + m0 * N, warps, stream)
+                          : launch_one<2, 1>(xb + m0 * K, mp, N, K, pk, sc, yb + m0 * N, warps, stream);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
