@@ -10,8 +10,11 @@
 //    summed in shared memory in a fixed order, so results are deterministic.
 //  * Each lane streams one 16-byte chunk (32 codes) per row per group straight
 //    from HBM into registers, `kDepth` groups ahead of use.  The stored nibble
-//    order makes every 32-bit word yield four bf16x2 pairs with one shift, one
-//    LOP3 and one exact bf16x2 subtract each, with no shuffles.
+//    order makes every 32-bit word yield four bf16x2 pairs (136 + q) with one
+//    shift and one LOP3 each, with no shuffles.  The 136·Σx offset is removed
+//    exactly enough (fp32, products exact) by starting each group's
+//    accumulator at −136·Σx, which one extra MMA chain per group computes for
+//    all rows at once.
 //  * The activations of the same groups are staged `kDepth` groups ahead into a
 //    per-warp shared-memory ring with cp.async (no registers held while in
 //    flight); token rows beyond M are zeroed once and never copied.  The row
@@ -23,8 +26,10 @@
 //    exceed the SM's 128 lanes already at M ≈ 2, while the MMA retires 2048
 //    multiply-adds per instruction.  The tensor pipe is therefore used as an ALU
 //    offload here; the kernel stays bound by HBM.
-//  * q is exact in bf16 and q·x is exact in fp32, so each group's partial sum is
-//    the exact-product fp32 sum; it is then scaled by d in fp32.
+//  * 136 + q is exact in bf16 and (136 + q)·x is exact in fp32, so each group's
+//    partial sum is an fp32 sum of exact products; it is then scaled by d in
+//    fp32.  Cancelling the offset costs about 2^-22·143·Σ|x| per group, three
+//    orders of magnitude inside the 4e-3·Σ|ŵx| bound.
 //  * Mapping of the MMA's k index: thread `tig` of a quad feeds, at k-step s,
 //    actual group offsets 32·tig + 4s + {0,1} (MMA k = 2tig, 2tig+1) and
 //    32·tig + 4s + {2,3} (MMA k = 2tig+8, 2tig+9) for both A (weights) and B (x).
@@ -39,7 +44,6 @@ namespace w4 {
 namespace {
 
 constexpr int kGemvMaxWarps = 8;
-constexpr int kDepth = 4;       // groups in flight per warp (weights in registers, x in shared memory)
 constexpr int kXPitch = 272;    // bytes per staged token row of one group: 256 + 16 of padding
 
 // Position of 16-byte chunk ch (0..15) of a staged x row.  With the 272-byte
@@ -56,6 +60,15 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint3
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Pair i (0..3) of a stored code word as the bf16x2 value (136 + q_lo, 136 + q_hi):
+// one shift and one LOP3, no subtract.  The 136·Σx offset this adds to every
+// group sum is removed by starting the group's accumulator at −136·Σx.
+__device__ __forceinline__ uint32_t biased_pair(uint32_t word, int i) {
+    return ((word >> (4 * i)) & 0x000F000Fu) ^ 0x43084308u;
+}
+
+constexpr uint32_t kMinus136x2 = 0xC308C308u;  // bf16x2 (−136, −136)
+
 template <int RT>
 struct Slot {
     uint4 w[RT][2];        // 16-byte code chunks of rows gid and gid+8 of each row tile
@@ -63,8 +76,10 @@ struct Slot {
 };
 
 // MT: token tiles of 8 (1: M <= 8, 2: M <= 16).  RT: 16-row tiles per warp.
-template <int MT, int RT>
-__global__ void __launch_bounds__(32 * kGemvMaxWarps)
+// kDepth: groups in flight per warp (weights in registers, x in shared memory).
+// MINB: CTAs per SM the register allocation must allow.
+template <int MT, int RT, int kDepth, int MINB>
+__global__ void __launch_bounds__(32 * kGemvMaxWarps, MINB)
 gemv_w4_kernel(const __nv_bfloat16* __restrict__ x, int M, int64_t N, int64_t K,
                const uint8_t* __restrict__ packed, const __nv_bfloat16* __restrict__ scales,
                __nv_bfloat16* __restrict__ y) {
@@ -175,23 +190,34 @@ gemv_w4_kernel(const __nv_bfloat16* __restrict__ x, int M, int64_t N, int64_t K,
                 }
                 cp_async_commit();
 
+                // −136·Σ_k x[m, k] over this group, identical for every row.
+                float corr[MT][4];
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) corr[mt][r] = 0.0f;
+#pragma unroll
+                    for (int s = 0; s < 8; ++s)
+                        mma_bf16_16816(corr[mt], kMinus136x2, kMinus136x2, kMinus136x2, kMinus136x2,
+                                       xw[mt][2 * s], xw[mt][2 * s + 1]);
+                }
 #pragma unroll
                 for (int rt = 0; rt < RT; ++rt) {
                     float cg[MT][4];
 #pragma unroll
                     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-                        for (int r = 0; r < 4; ++r) cg[mt][r] = 0.0f;
+                        for (int r = 0; r < 4; ++r) cg[mt][r] = corr[mt][r];
                     const uint32_t wa[4] = {cur.w[rt][0].x, cur.w[rt][0].y, cur.w[rt][0].z, cur.w[rt][0].w};
                     const uint32_t wb[4] = {cur.w[rt][1].x, cur.w[rt][1].y, cur.w[rt][1].z, cur.w[rt][1].w};
 #pragma unroll
                     for (int s = 0; s < 8; ++s) {
                         const int w = s >> 1;
                         const int h = s & 1;
-                        const uint32_t a0 = code_pair_bf16x2(wa[w], 2 * h);
-                        const uint32_t a2 = code_pair_bf16x2(wa[w], 2 * h + 1);
-                        const uint32_t a1 = code_pair_bf16x2(wb[w], 2 * h);
-                        const uint32_t a3 = code_pair_bf16x2(wb[w], 2 * h + 1);
+                        const uint32_t a0 = biased_pair(wa[w], 2 * h);
+                        const uint32_t a2 = biased_pair(wa[w], 2 * h + 1);
+                        const uint32_t a1 = biased_pair(wb[w], 2 * h);
+                        const uint32_t a3 = biased_pair(wb[w], 2 * h + 1);
 #pragma unroll
                         for (int mt = 0; mt < MT; ++mt)
                             mma_bf16_16816(cg[mt], a0, a1, a2, a3, xw[mt][2 * s], xw[mt][2 * s + 1]);
@@ -232,35 +258,35 @@ gemv_w4_kernel(const __nv_bfloat16* __restrict__ x, int M, int64_t N, int64_t K,
     }
 }
 
-template <int MT, int RT>
+template <int MT, int kDepth>
 int gemv_smem_bytes(int warps) {
     return warps * kDepth * MT * 8 * kXPitch;
 }
 
 std::mutex g_attr_mutex;
-bool g_attr_set[64][4];
 
-template <int MT, int RT>
+template <int MT, int RT, int kDepth, int MINB>
 cudaError_t launch_one(const __nv_bfloat16* x, int mp, int64_t N, int64_t K, const uint8_t* packed,
                        const __nv_bfloat16* scales, __nv_bfloat16* y, int warps, cudaStream_t stream) {
+    static bool attr_set[64];
     int device = 0;
     if (cudaError_t e = cudaGetDevice(&device)) return e;
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
-    const int variant = (MT - 1) * 2 + (RT - 1);
     {
         std::lock_guard<std::mutex> lock(g_attr_mutex);
-        if (!g_attr_set[device][variant]) {
-            if (cudaError_t e = cudaFuncSetAttribute(gemv_w4_kernel<MT, RT>,
+        if (!attr_set[device]) {
+            if (cudaError_t e = cudaFuncSetAttribute(gemv_w4_kernel<MT, RT, kDepth, MINB>,
                                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     gemv_smem_bytes<MT, RT>(kGemvMaxWarps)))
+                                                     gemv_smem_bytes<MT, kDepth>(kGemvMaxWarps)))
                 return e;
-            g_attr_set[device][variant] = true;
+            attr_set[device] = true;
         }
     }
     const int64_t blocks = (N + 16 * RT - 1) / (16 * RT);
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    gemv_w4_kernel<MT, RT><<<static_cast<unsigned>(blocks), 32 * warps, gemv_smem_bytes<MT, RT>(warps),
-                             stream>>>(x, mp, N, K, packed, scales, y);
+    gemv_w4_kernel<MT, RT, kDepth, MINB>
+        <<<static_cast<unsigned>(blocks), 32 * warps, gemv_smem_bytes<MT, kDepth>(warps), stream>>>(
+            x, mp, N, K, packed, scales, y);
     return cudaGetLastError();
 }
 
@@ -281,11 +307,11 @@ cudaError_t launch_gemv(const void* x, int64_t M, int64_t N, int64_t K, const vo
         const int mp = static_cast<int>(M - m0 < 16 ? M - m0 : 16);
         cudaError_t e;
         if (mp <= 8)
-            e = two_tiles ? launch_one<1, 2>(xb + m0 * K, mp, N, K, pk, sc, yb + m0 * N, warps, stream)
-                          : launch_one<1, 1>(xb + m0 * K, mp, N, K, pk, sc, yb + m0 * N, warps, stream);
+            e = two_tiles ? launch_one<1, 2, 4, 1>(xb + m0 * K, mp, N, K, pk, sc, yb + m0 * N, warps, stream)
+                          : launch_one<1, 1, 4, 1>(xb + m0 * K, mp, N, K, pk, sc, yb + m0 * N, warps, stream);
         else
-            e = two_tiles ? launch_one<2, 2>(xb + m0 * K, mp, N, K, pk, sc, yb + m0 * N, warps, stream)
-                          : launch_one<2, 1>(xb + m0 * K, mp, N, K, pk, sc, yb + m0 * N, warps, stream);
+            e = two_tiles ? launch_one<2, 2, 4, 1>(xb + m0 * K, mp, N, K, pk, sc, yb + m0 * N, warps, stream)
+                          : launch_one<2, 1, 4, 1>(xb + m0 * K, mp, N, K, pk, sc, yb + m0 * N, warps, stream);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -25,38 +25,83 @@ constexpr int kQuantUnroll = 4;  // chunks in flight per thread
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: x + kRoundMagic rounds x to an integer (ties to even)
 constexpr int kRoundMagicBits = 0x4B400000;
 
-// Codes of the two weights of one bf16x2 word, as the pair (slot j, slot j+4)
-// of the stored word: bits 0-3 and 16-19 before the caller shifts by 4j.
-//
 // round_half_even(w / d) without a per-weight division.  With ρ = 1/d
 // correctly rounded (CUDA's __frcp_rn), w·ρ differs from w/d by at most
-// |w/d|·2^-23 < 2^-20.  Both w and d carry 8-bit significands, so a quotient
+// |w/d|·2^-23 < 2^-19.  Both w and d carry 8-bit significands, so a quotient
 // that is not exactly a half-integer lies at least 1/512 away from every
 // half-integer; rounding w·ρ to the nearest integer therefore gives
 // round(w/d) everywhere except at exact ties.  Ties are found exactly: with
-// q' the rounded value, e = w − q'·d is computed exactly by one FMA (q'·d has
-// at most 12 significant bits and |e| ≤ d/2 + tiny), and |e| = d/2 holds
-// precisely at a tie, where the even neighbour is then chosen.  The result is
-// clamped to [-8, 7] only on the subnormal-scale path, where d's rounding can
-// leave max|w|/d above 7.5; for d ≥ 2^-64 it never exceeds 7·(1 + 2^-8).
+// q' the rounded value, e = w − q'·d is exact (one FMA; q'·d has at most 12
+// significant bits and |e| ≤ d/2 + tiny), and |e| = d/2 holds precisely at a
+// tie.  The rare chunks that contain a tie are redone with the even neighbour
+// chosen.  The result is clamped to [-8, 7] only on the subnormal-scale path,
+// where d's rounding can leave max|w|/d above 7.5; for d ≥ 2^-64 it never
+// exceeds 7·(1 + 2^-8).
+//
+// rounded(): the integer nearest to r, as the low bits of the binary32
+// pattern of r + 1.5·2^23 (two's complement, valid for |r| < 2^22).
 template <bool kTiny>
-__device__ __forceinline__ uint32_t code_pair(uint32_t two, float d, float rcp, float half_d) {
-    float w[2] = {bf16_lo(two), bf16_hi(two)};
-    int t[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        float x = kTiny ? w[h] * 0x1p64f : w[h];
+struct Rounder {
+    float d, rcp, half_d;
+    __device__ __forceinline__ explicit Rounder(float d_) {
+        d = kTiny ? d_ * 0x1p64f : d_;  // exact: power-of-two scaling of a tiny scale
+        rcp = __frcp_rn(d);
+        half_d = 0.5f * d;
+    }
+    __device__ __forceinline__ float scaled(float w) const { return kTiny ? w * 0x1p64f : w; }
+    // Nearest integer of x/d (ties unresolved) as rounded-magic bits; sets *tie
+    // when x/d is exactly a half-integer.
+    __device__ __forceinline__ int round_bits(float x, bool* tie) const {
         float r = x * rcp;
         if (kTiny) r = fminf(fmaxf(r, -8.0f), 7.0f);
         const float tf = r + kRoundMagic;
-        const float qf = tf - kRoundMagic;
-        const float e = fmaf(-qf, d, x);
+        const float e = fmaf(-(tf - kRoundMagic), d, x);
+        *tie = *tie || fabsf(e) == half_d;
+        return __float_as_int(tf);
+    }
+    // Same, resolving a tie to the even neighbour.
+    __device__ __forceinline__ int round_bits_even(float x) const {
+        float r = x * rcp;
+        if (kTiny) r = fminf(fmaxf(r, -8.0f), 7.0f);
+        const float tf = r + kRoundMagic;
+        const float e = fmaf(-(tf - kRoundMagic), d, x);
         int tb = __float_as_int(tf);
         if (fabsf(e) == half_d && (tb & 1)) tb += e > 0.0f ? 1 : -1;
-        if (kTiny) tb = min(max(tb, kRoundMagicBits - 8), kRoundMagicBits + 7);
-        t[h] = tb;
+        return tb;
     }
-    return __byte_perm(t[0], t[1], 0x5410) & 0x000F000Fu;
+};
+
+// Two rounded-magic patterns -> the nibble pair (bits 0-3 and 16-19) for slots
+// j and j+4 of the stored word.
+__device__ __forceinline__ uint32_t pair_bits(int lo, int hi, bool tiny) {
+    if (tiny) {
+        lo = min(max(lo, kRoundMagicBits - 8), kRoundMagicBits + 7);
+        hi = min(max(hi, kRoundMagicBits - 8), kRoundMagicBits + 7);
+    }
+    return __byte_perm(lo, hi, 0x5410) & 0x000F000Fu;
+}
+
+template <bool kTiny>
+__device__ __forceinline__ uint32_t quantize_chunk_t(const uint32_t (&h)[4], float d) {
+    const Rounder<kTiny> R(d);
+    uint32_t word = 0;
+    bool tie = false;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int lo = R.round_bits(R.scaled(bf16_lo(h[j])), &tie);
+        const int hi = R.round_bits(R.scaled(bf16_hi(h[j])), &tie);
+        word |= pair_bits(lo, hi, kTiny) << (4 * j);
+    }
+    if (tie) {
+        word = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int lo = R.round_bits_even(R.scaled(bf16_lo(h[j])));
+            const int hi = R.round_bits_even(R.scaled(bf16_hi(h[j])));
+            word |= pair_bits(lo, hi, kTiny) << (4 * j);
+        }
+    }
+    return word;
 }
 
 // Packs the 8 weights of one 16-byte chunk into the stored 32-bit code word:
@@ -64,20 +109,15 @@ __device__ __forceinline__ uint32_t code_pair(uint32_t two, float d, float rcp, 
 __device__ __forceinline__ uint32_t quantize_chunk(const uint4 v, const float d) {
     if (d == 0.0f) return 0u;
     const uint32_t h[4] = {v.x, v.y, v.z, v.w};
-    uint32_t word = 0;
-    if (d >= 0x1p-64f) {
-        const float rcp = __frcp_rn(d);
-        const float half_d = 0.5f * d;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) word |= code_pair<false>(h[j], d, rcp, half_d) << (4 * j);
-    } else {
-        const float ds = d * 0x1p64f;  // exact: power-of-two scaling of a tiny scale
-        const float rcp = __frcp_rn(ds);
-        const float half_d = 0.5f * ds;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) word |= code_pair<true>(h[j], ds, rcp, half_d) << (4 * j);
-    }
-    return word;
+    return d >= 0x1p-64f ? quantize_chunk_t<false>(h, d) : quantize_chunk_t<true>(h, d);
+}
+
+// d = bf16_rne(max|w| / 7).  a/7 is never within 1/14 of a bf16 spacing of a
+// bf16 rounding midpoint (2·a/7 is an integer multiple of the spacing divided
+// by 7), so rounding the fp32 product a·fl(1/7), whose error is below 2^-22
+// relative, to bf16 gives the same d as rounding the exact quotient.
+__device__ __forceinline__ __nv_bfloat16 group_scale(float a) {
+    return __float2bfloat16_rn(a * (1.0f / 7.0f));
 }
 
 // max|w| of the chunk as a bf16 bit pattern: for non-negative finite bf16,
@@ -110,7 +150,7 @@ quantize_rtn_kernel(const uint4* __restrict__ W, uint32_t* __restrict__ packed,
             uint32_t a = chunk_absmax_bits(v[u]);
 #pragma unroll
             for (int off = 1; off < 16; off <<= 1) a = max(a, __shfl_xor_sync(0xffffffffu, a, off));
-            const __nv_bfloat16 d16 = __float2bfloat16_rn(__fdiv_rn(bf16_lo(a), 7.0f));
+            const __nv_bfloat16 d16 = group_scale(bf16_lo(a));
             const float d = __bfloat162float(d16);
             const uint32_t word = quantize_chunk(v[u], d);
             if (c < n_chunks) {
