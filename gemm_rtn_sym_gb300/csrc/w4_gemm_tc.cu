@@ -29,6 +29,7 @@
 
 #include "w4_device.cuh"
 #include "w4_internal.h"
+#include "w4_tcgen05.cuh"
 
 namespace w4 {
 namespace {
@@ -50,89 +51,6 @@ struct TcArgs {
     int bm;
     unsigned* status;
 };
-
-// ------------------------------------------------------------- tcgen05 PTX
-__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
-                 "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-        "%12, %13, %14, %15}, [%16];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-          "=r"(v[14]), "=r"(v[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-        "%3}], [%4];" ::"r"(dst),
-        "l"(map), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void fence_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
-// 128 bytes, groups of 8 rows 1024 bytes apart (stride byte offset); the
-// leading byte offset is unused for this layout.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr & 0x3FFFF) >> 4);   // start address, bits 0-13
-    d |= static_cast<uint64_t>(1) << 16;                  // leading byte offset (16 B, unused)
-    d |= static_cast<uint64_t>(1024 >> 4) << 32;          // stride byte offset
-    d |= static_cast<uint64_t>(1) << 46;                  // descriptor version for tcgen05
-    d |= static_cast<uint64_t>(2) << 61;                  // swizzle mode: 128-byte
-    return d;
-}
-
-// Instruction descriptor for kind::f16: FP32 accumulator, BF16 A and B, both
-// K-major, MMA shape M = 128, N = n.
-__device__ __forceinline__ uint32_t idesc_bf16(int n) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
-           (static_cast<uint32_t>(kBN >> 4) << 24);
-}
-
-// Byte offset of 16-byte chunk c of row r in a 128-byte-swizzled tile.
-__device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
-    return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
-}
 
 // q·d for the pair i of a code word, as bf16x2 (exact q, one rounding).
 __device__ __forceinline__ uint32_t deq_pair(uint32_t word, int i, __nv_bfloat162 d2) {
@@ -344,13 +262,29 @@ cudaError_t get_encoder() {
     return g_encode ? cudaSuccess : cudaErrorNotSupported;
 }
 
+}  // namespace
+
+cudaError_t encode_x_map(CUtensorMap* map, const void* x, int64_t M, int64_t K, int box_rows) {
+    if (cudaError_t e = get_encoder()) return e;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    return cudaSuccess;
+}
+
+namespace {
+
 int smem_bytes(int bm) { return kStages * (kATileBytes + bm * 128) + 8 * (3 * kStages + 2) + 1024; }
 
 }  // namespace
 
 cudaError_t launch_gemm_tc(const void* x, int64_t M, int64_t N, int64_t K, const void* packed,
                            const void* scales, void* y, const DeviceInfo& dev, cudaStream_t stream) {
-    if (cudaError_t e = get_encoder()) return e;
     const int64_t m_tiles = (M + kMaxBM - 1) / kMaxBM;
     int64_t bm = (M + m_tiles - 1) / m_tiles;
     bm = (bm + 15) / 16 * 16;
@@ -361,14 +295,7 @@ cudaError_t launch_gemm_tc(const void* x, int64_t M, int64_t N, int64_t K, const
     if (smem > dev.max_smem_optin) return cudaErrorInvalidConfiguration;
 
     CUtensorMap tmap;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(bm)};
-    const cuuint32_t estr[2] = {1, 1};
-    if (g_encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
-                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
+    if (cudaError_t e = encode_x_map(&tmap, x, M, K, static_cast<int>(bm))) return e;
 
     int device = 0;
     if (cudaError_t e = cudaGetDevice(&device)) return e;

@@ -8,17 +8,17 @@
 //  * One warp owns RT tiles of 16 output rows and a contiguous range of groups;
 //    the CTA's warps split the groups (split-K) and their fp32 partials are
 //    summed in shared memory in a fixed order, so results are deterministic.
-//  * Each lane streams one 16-byte chunk (32 codes) per row per group straight
-//    from HBM into registers, `kDepth` groups ahead of use.  The stored nibble
+//  * Each lane copies one 16-byte chunk (32 codes) per row per group from HBM
+//    into a per-warp shared-memory ring with cp.async, `kDepth` groups ahead of
+//    use, so nothing in flight occupies registers and several CTAs fit per SM.  The stored nibble
 //    order makes every 32-bit word yield four bf16x2 pairs (136 + q) with one
 //    shift and one LOP3 each, with no shuffles.  The 136·Σx offset is removed
 //    exactly enough (fp32, products exact) by starting each group's
 //    accumulator at −136·Σx, which one extra MMA chain per group computes for
 //    all rows at once.
-//  * The activations of the same groups are staged `kDepth` groups ahead into a
-//    per-warp shared-memory ring with cp.async (no registers held while in
-//    flight); token rows beyond M are zeroed once and never copied.  The row
-//    pitch and chunk order of the ring make the fragment loads conflict-free.
+//  * The activations of the same groups go into the same ring (only the M real
+//    token rows; lanes of padding tokens use zero fragments).  The row pitch
+//    and chunk order make the fragment loads conflict-free.
 //  * The products q·x go through the legacy tensor-core MMA (m16n8k16, bf16 in,
 //    fp32 accumulate) from registers: the 16 rows are the MMA's M, up to 8 tokens
 //    its N.  At 0.5 B per weight of HBM traffic the SM must consume about 45
@@ -60,33 +60,39 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint3
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Right shifts by 4, 8 and 12 bits written as the high word of a product with
+// 2^28, 2^24, 2^20.  The multipliers live in constant memory, so they reach the
+// integer multiply-add unit (which shares the FMA pipe) instead of becoming
+// shifts on the ALU pipe, which the LOP3 decode already keeps busy.
+__constant__ uint32_t kShiftMul[4] = {0u, 1u << 28, 1u << 24, 1u << 20};
+
 // Pair i (0..3) of a stored code word as the bf16x2 value (136 + q_lo, 136 + q_hi):
 // one shift and one LOP3, no subtract.  The 136·Σx offset this adds to every
 // group sum is removed by starting the group's accumulator at −136·Σx.
 __device__ __forceinline__ uint32_t biased_pair(uint32_t word, int i) {
-    return ((word >> (4 * i)) & 0x000F000Fu) ^ 0x43084308u;
+    const uint32_t shifted = i == 0 ? word : __umulhi(word, kShiftMul[i]);
+    return (shifted & 0x000F000Fu) ^ 0x43084308u;
 }
 
 constexpr uint32_t kMinus136x2 = 0xC308C308u;  // bf16x2 (−136, −136)
 
+// Shared-memory ring of one warp, per stage (one group):
+//   [RT tiles][16 rows][64 bytes of codes]   then   [m_real token rows][272 bytes of x]
+// Codes: lane (gid, tig) reads 16 bytes at row gid and row gid+8, chunk tig; one
+// load phase covers two rows x 64 contiguous bytes, so reads are conflict-free.
 template <int RT>
-struct Slot {
-    uint4 w[RT][2];        // 16-byte code chunks of rows gid and gid+8 of each row tile
-    uint32_t d[RT][2];     // their bf16 scale bits (low 16 bits)
-};
+__host__ __device__ constexpr int w_stage_bytes() { return RT * 16 * 64; }
 
 // MT: token tiles of 8 (1: M <= 8, 2: M <= 16).  RT: 16-row tiles per warp.
-// kDepth: groups in flight per warp (weights in registers, x in shared memory).
-// MINB: CTAs per SM the register allocation must allow.
+// kDepth: groups in flight per warp.  MINB: CTAs per SM the register allocation
+// must allow.
 template <int MT, int RT, int kDepth, int MINB>
 __global__ void __launch_bounds__(32 * kGemvMaxWarps, MINB)
 gemv_w4_kernel(const __nv_bfloat16* __restrict__ x, int M, int64_t N, int64_t K,
                const uint8_t* __restrict__ packed, const __nv_bfloat16* __restrict__ scales,
                __nv_bfloat16* __restrict__ y) {
-    extern __shared__ __align__(16) uint8_t xs_raw[];
+    extern __shared__ __align__(16) uint8_t ring_raw[];
     __shared__ float red[kGemvMaxWarps][RT][MT][4][32];
-    constexpr int XR = MT * 8;                 // staged token rows
-    constexpr int kSlot = XR * kXPitch;        // bytes of one staged group
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -96,51 +102,45 @@ gemv_w4_kernel(const __nv_bfloat16* __restrict__ x, int M, int64_t N, int64_t K,
     const int64_t G = K >> 7;
     const int64_t half_k = K >> 1;
     const int64_t n0 = static_cast<int64_t>(blockIdx.x) * 16 * RT;
+    const int m_real = M < MT * 8 ? M : MT * 8;
 
     const int64_t g0 = (warp * G) / n_warps;
     const int64_t g1 = ((warp + 1) * G) / n_warps;
     const int ng = static_cast<int>(g1 - g0);
 
+    const int stage = w_stage_bytes<RT>() + m_real * kXPitch;
+    const uint32_t wbase = smem_addr(ring_raw) + static_cast<uint32_t>(warp * kDepth * stage);
+    const uint32_t xoff = w_stage_bytes<RT>();
+
+    // Rows past N are clamped to row N-1 (valid memory); their outputs are dropped.
     const uint8_t* pa[RT];
     const uint8_t* pb[RT];
     const uint16_t* sa[RT];
     const uint16_t* sb[RT];
-    bool va[RT], vb[RT];
 #pragma unroll
     for (int rt = 0; rt < RT; ++rt) {
-        const int64_t na = n0 + rt * 16 + gid, nb = na + 8;
-        va[rt] = na < N;
-        vb[rt] = nb < N;
-        pa[rt] = packed + (va[rt] ? na : 0) * half_k + (g0 * 64 + tig * 16);
-        pb[rt] = packed + (vb[rt] ? nb : 0) * half_k + (g0 * 64 + tig * 16);
-        sa[rt] = reinterpret_cast<const uint16_t*>(scales) + (va[rt] ? na : 0) * G + g0;
-        sb[rt] = reinterpret_cast<const uint16_t*>(scales) + (vb[rt] ? nb : 0) * G + g0;
+        int64_t na = n0 + rt * 16 + gid, nb = na + 8;
+        na = na < N ? na : N - 1;
+        nb = nb < N ? nb : N - 1;
+        pa[rt] = packed + na * half_k + (g0 * 64 + tig * 16);
+        pb[rt] = packed + nb * half_k + (g0 * 64 + tig * 16);
+        sa[rt] = reinterpret_cast<const uint16_t*>(scales) + na * G + g0;
+        sb[rt] = reinterpret_cast<const uint16_t*>(scales) + nb * G + g0;
     }
-
-    // Per-warp ring of staged x groups.  Token rows >= M stay zero.
-    const uint32_t xbase = smem_addr(xs_raw) + static_cast<uint32_t>(warp * kDepth * kSlot);
-    const int m_real = M < XR ? M : XR;
-    for (int i = lane; i < kDepth * (XR - m_real) * 17; i += 32) {
-        const int per_slot = (XR - m_real) * 17;
-        const int slot = i / per_slot, rest = i % per_slot;
-        sts128(xbase + slot * kSlot + (m_real + rest / 17) * kXPitch + (rest % 17) * 16, make_uint4(0, 0, 0, 0));
-    }
-    __syncwarp();
     const __nv_bfloat16* xg = x + g0 * 128;
-    auto issue_x = [&](int slot, int gi) {
-        for (int p = lane; p < m_real * 16; p += 32) {
-            const int r = p >> 4, ch = p & 15;
-            cp_async16(xbase + slot * kSlot + r * kXPitch + x_phys_chunk(ch) * 16,
-                       xg + static_cast<int64_t>(r) * K + gi * 128 + ch * 8);
-        }
-    };
-    auto load_w = [&](Slot<RT>& s, int gi) {
+
+    // Stage group gi of this warp's range into ring slot `slot`.
+    auto issue = [&](int slot, int gi) {
+        const uint32_t st = wbase + slot * stage;
 #pragma unroll
         for (int rt = 0; rt < RT; ++rt) {
-            s.w[rt][0] = va[rt] ? ld_stream(pa[rt] + gi * 64) : make_uint4(0, 0, 0, 0);
-            s.w[rt][1] = vb[rt] ? ld_stream(pb[rt] + gi * 64) : make_uint4(0, 0, 0, 0);
-            s.d[rt][0] = va[rt] ? __ldg(sa[rt] + gi) : 0u;
-            s.d[rt][1] = vb[rt] ? __ldg(sb[rt] + gi) : 0u;
+            cp_async16(st + (rt * 16 + gid) * 64 + tig * 16, pa[rt] + gi * 64);
+            cp_async16(st + (rt * 16 + gid + 8) * 64 + tig * 16, pb[rt] + gi * 64);
+        }
+        for (int q = lane; q < m_real * 16; q += 32) {
+            const int r = q >> 4, ch = q & 15;
+            cp_async16(st + xoff + r * kXPitch + x_phys_chunk(ch) * 16,
+                       xg + static_cast<int64_t>(r) * K + gi * 128 + ch * 8);
         }
     };
 
@@ -152,86 +152,111 @@ gemv_w4_kernel(const __nv_bfloat16* __restrict__ x, int M, int64_t N, int64_t K,
 #pragma unroll
             for (int r = 0; r < 4; ++r) acc[rt][mt][r] = 0.0f;
 
-    Slot<RT> ring[kDepth];
 #pragma unroll
     for (int i = 0; i < kDepth; ++i) {
-        if (i < ng) {
-            load_w(ring[i], i);
-            issue_x(i, i);
-        }
+        if (i < ng) issue(i, i);
         cp_async_commit();
     }
-
-    for (int it = 0; it < ng; it += kDepth) {
+    // Scales one group ahead in registers.
+    uint32_t d_next[RT][2];
 #pragma unroll
-        for (int i = 0; i < kDepth; ++i) {
-            const int gi = it + i;
-            if (gi < ng) {
-                const Slot<RT> cur = ring[i];
-                cp_async_wait<kDepth - 1>();
-                __syncwarp();
-                uint32_t xw[MT][16];
+    for (int rt = 0; rt < RT; ++rt) {
+        d_next[rt][0] = ng > 0 ? __ldg(sa[rt]) : 0u;
+        d_next[rt][1] = ng > 0 ? __ldg(sb[rt]) : 0u;
+    }
+
+    for (int gi = 0; gi < ng; ++gi) {
+        const int slot = gi % kDepth;
+        const uint32_t st = wbase + slot * stage;
+        uint32_t d_cur[RT][2];
+#pragma unroll
+        for (int rt = 0; rt < RT; ++rt) {
+            d_cur[rt][0] = d_next[rt][0];
+            d_cur[rt][1] = d_next[rt][1];
+            if (gi + 1 < ng) {
+                d_next[rt][0] = __ldg(sa[rt] + gi + 1);
+                d_next[rt][1] = __ldg(sb[rt] + gi + 1);
+            }
+        }
+        cp_async_wait<kDepth - 1>();
+        __syncwarp();
+        uint4 wv[RT][2];
+#pragma unroll
+        for (int rt = 0; rt < RT; ++rt) {
+            wv[rt][0] = lds128(st + (rt * 16 + gid) * 64 + tig * 16);
+            wv[rt][1] = lds128(st + (rt * 16 + gid + 8) * 64 + tig * 16);
+        }
+        uint32_t xw[MT][16];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            const int row = mt * 8 + gid;
+            if (row < m_real) {
+                const uint32_t xr = st + xoff + row * kXPitch;
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const uint4 t = lds128(xr + x_phys_chunk(4 * tig + v) * 16);
+                    xw[mt][4 * v + 0] = t.x;
+                    xw[mt][4 * v + 1] = t.y;
+                    xw[mt][4 * v + 2] = t.z;
+                    xw[mt][4 * v + 3] = t.w;
+                }
+            } else {
+#pragma unroll
+                for (int v = 0; v < 16; ++v) xw[mt][v] = 0u;
+            }
+        }
+        __syncwarp();
+        if (gi + kDepth < ng) issue(slot, gi + kDepth);
+        cp_async_commit();
+
+        // −136·Σ_k x[m, k] over this group, identical for every row.
+        float corr[MT][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) corr[mt][r] = 0.0f;
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                mma_bf16_16816(corr[mt], kMinus136x2, kMinus136x2, kMinus136x2, kMinus136x2,
+                               xw[mt][2 * s], xw[mt][2 * s + 1]);
+        }
+#pragma unroll
+        for (int rt = 0; rt < RT; ++rt) {
+            // Two independent MMA chains (even and odd k-steps) per tile.
+            float ce[MT][4], co[MT][4];
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    ce[mt][r] = corr[mt][r];
+                    co[mt][r] = 0.0f;
+                }
+            const uint32_t wa[4] = {wv[rt][0].x, wv[rt][0].y, wv[rt][0].z, wv[rt][0].w};
+            const uint32_t wb[4] = {wv[rt][1].x, wv[rt][1].y, wv[rt][1].z, wv[rt][1].w};
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const int w = s >> 1;
+                const int h = s & 1;
+                const uint32_t a0 = biased_pair(wa[w], 2 * h);
+                const uint32_t a2 = biased_pair(wa[w], 2 * h + 1);
+                const uint32_t a1 = biased_pair(wb[w], 2 * h);
+                const uint32_t a3 = biased_pair(wb[w], 2 * h + 1);
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt) {
-                    const uint32_t row = xbase + i * kSlot + (mt * 8 + gid) * kXPitch;
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const uint4 t = lds128(row + x_phys_chunk(4 * tig + v) * 16);
-                        xw[mt][4 * v + 0] = t.x;
-                        xw[mt][4 * v + 1] = t.y;
-                        xw[mt][4 * v + 2] = t.z;
-                        xw[mt][4 * v + 3] = t.w;
-                    }
+                    if (h == 0)
+                        mma_bf16_16816(ce[mt], a0, a1, a2, a3, xw[mt][2 * s], xw[mt][2 * s + 1]);
+                    else
+                        mma_bf16_16816(co[mt], a0, a1, a2, a3, xw[mt][2 * s], xw[mt][2 * s + 1]);
                 }
-                __syncwarp();
-                if (gi + kDepth < ng) {
-                    load_w(ring[i], gi + kDepth);
-                    issue_x(i, gi + kDepth);
-                }
-                cp_async_commit();
-
-                // −136·Σ_k x[m, k] over this group, identical for every row.
-                float corr[MT][4];
+            }
+            const float da = bf16_lo(d_cur[rt][0]);
+            const float db = bf16_lo(d_cur[rt][1]);
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) corr[mt][r] = 0.0f;
-#pragma unroll
-                    for (int s = 0; s < 8; ++s)
-                        mma_bf16_16816(corr[mt], kMinus136x2, kMinus136x2, kMinus136x2, kMinus136x2,
-                                       xw[mt][2 * s], xw[mt][2 * s + 1]);
-                }
-#pragma unroll
-                for (int rt = 0; rt < RT; ++rt) {
-                    float cg[MT][4];
-#pragma unroll
-                    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                        for (int r = 0; r < 4; ++r) cg[mt][r] = corr[mt][r];
-                    const uint32_t wa[4] = {cur.w[rt][0].x, cur.w[rt][0].y, cur.w[rt][0].z, cur.w[rt][0].w};
-                    const uint32_t wb[4] = {cur.w[rt][1].x, cur.w[rt][1].y, cur.w[rt][1].z, cur.w[rt][1].w};
-#pragma unroll
-                    for (int s = 0; s < 8; ++s) {
-                        const int w = s >> 1;
-                        const int h = s & 1;
-                        const uint32_t a0 = biased_pair(wa[w], 2 * h);
-                        const uint32_t a2 = biased_pair(wa[w], 2 * h + 1);
-                        const uint32_t a1 = biased_pair(wb[w], 2 * h);
-                        const uint32_t a3 = biased_pair(wb[w], 2 * h + 1);
-#pragma unroll
-                        for (int mt = 0; mt < MT; ++mt)
-                            mma_bf16_16816(cg[mt], a0, a1, a2, a3, xw[mt][2 * s], xw[mt][2 * s + 1]);
-                    }
-                    const float da = bf16_lo(cur.d[rt][0]);
-                    const float db = bf16_lo(cur.d[rt][1]);
-#pragma unroll
-                    for (int mt = 0; mt < MT; ++mt) {
-                        acc[rt][mt][0] = fmaf(da, cg[mt][0], acc[rt][mt][0]);
-                        acc[rt][mt][1] = fmaf(da, cg[mt][1], acc[rt][mt][1]);
-                        acc[rt][mt][2] = fmaf(db, cg[mt][2], acc[rt][mt][2]);
-                        acc[rt][mt][3] = fmaf(db, cg[mt][3], acc[rt][mt][3]);
-                    }
-                }
+            for (int mt = 0; mt < MT; ++mt) {
+                acc[rt][mt][0] = fmaf(da, ce[mt][0] + co[mt][0], acc[rt][mt][0]);
+                acc[rt][mt][1] = fmaf(da, ce[mt][1] + co[mt][1], acc[rt][mt][1]);
+                acc[rt][mt][2] = fmaf(db, ce[mt][2] + co[mt][2], acc[rt][mt][2]);
+                acc[rt][mt][3] = fmaf(db, ce[mt][3] + co[mt][3], acc[rt][mt][3]);
             }
         }
     }
@@ -258,9 +283,9 @@ gemv_w4_kernel(const __nv_bfloat16* __restrict__ x, int M, int64_t N, int64_t K,
     }
 }
 
-template <int MT, int kDepth>
-int gemv_smem_bytes(int warps) {
-    return warps * kDepth * MT * 8 * kXPitch;
+template <int MT, int RT, int kDepth>
+int gemv_smem_bytes(int warps, int m_real) {
+    return warps * kDepth * (w_stage_bytes<RT>() + m_real * kXPitch);
 }
 
 std::mutex g_attr_mutex;
@@ -277,16 +302,17 @@ cudaError_t launch_one(const __nv_bfloat16* x, int mp, int64_t N, int64_t K, con
         if (!attr_set[device]) {
             if (cudaError_t e = cudaFuncSetAttribute(gemv_w4_kernel<MT, RT, kDepth, MINB>,
                                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     gemv_smem_bytes<MT, kDepth>(kGemvMaxWarps)))
+                                                     gemv_smem_bytes<MT, RT, kDepth>(kGemvMaxWarps, MT * 8)))
                 return e;
             attr_set[device] = true;
         }
     }
     const int64_t blocks = (N + 16 * RT - 1) / (16 * RT);
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    gemv_w4_kernel<MT, RT, kDepth, MINB>
-        <<<static_cast<unsigned>(blocks), 32 * warps, gemv_smem_bytes<MT, kDepth>(warps), stream>>>(
-            x, mp, N, K, packed, scales, y);
+    const int m_real = mp < MT * 8 ? mp : MT * 8;
+    gemv_w4_kernel<MT, RT, kDepth, MINB><<<static_cast<unsigned>(blocks), 32 * warps,
+                                           gemv_smem_bytes<MT, RT, kDepth>(warps, m_real), stream>>>(
+        x, mp, N, K, packed, scales, y);
     return cudaGetLastError();
 }
 

@@ -1,0 +1,399 @@
+// Small-M W4A16 matmul on the tcgen05 tensor cores, weights as the A operand
+// in tensor memory:  y[m, n] = Σ_g d[n, g] · Σ_{k∈g} q[n, k] · x[m, k].
+//
+// Source: Qwen3.5-4B quantisation study, §1 FFN example y = W x with the
+// group-quantisation equation (ŵ = d·q, one d per 128 consecutive inputs) and
+// §2 settings (4-bit weights, BF16 inputs).
+//
+// Why this shape: at M ≤ 16 the matmul is bound by HBM (0.5 byte per weight),
+// so every SM must decode about 45 weights per clock.  The decode itself (one
+// shift and one LOP3 per pair of weights) is the floor of the instruction
+// stream; everything else is moved off the SM's issue slots:
+//  * each of 128 decoder threads owns one weight row; it loads its row's
+//    64-byte group block (kept kCodePrefetch groups ahead in registers), turns
+//    the 128 nibbles into 64 bf16x2 values 136 + q and writes them with two
+//    tcgen05.st into tensor memory, where they are the MMA's A operand
+//    (128 lanes = rows, one 32-bit column = one pair along K);
+//  * the activations of the group (16 token rows, rows ≥ M read as zeros)
+//    arrive by TMA in a 128-byte-swizzled shared-memory tile, the B operand;
+//  * one thread issues per group 8 MMAs of 128×16×16 with the decoded A, plus
+//    8 more with a constant A tile of −136 that cancels the bias, so the fp32
+//    accumulator of the group holds Σ q·x exactly up to fp32 rounding;
+//  * the group accumulator (double-buffered in TMEM) is read back with one
+//    tcgen05.ld per thread and scaled by d in fp32 registers.
+// Split-K: the CTAs of a thread-block cluster (1 × S) take disjoint group
+// ranges of the same 128 rows and sum their partials through distributed
+// shared memory in a fixed rank order, so results are deterministic and no
+// global scratch is used.
+//
+// Every mbarrier wait is bounded; a wait that runs out records a timeout in
+// the status word and the CTA winds down, draining its TMA copies and MMAs
+// before it frees tensor memory.
+#include <mutex>
+
+#include "w4_device.cuh"
+#include "w4_internal.h"
+#include "w4_tcgen05.cuh"
+
+namespace w4 {
+namespace {
+
+constexpr int kRows = 128;          // weight rows per CTA = MMA M
+constexpr int kTok = 16;            // token rows per pass = MMA N
+constexpr int kThreads = 192;       // warp 0: TMA, warp 1: TMEM + MMA, warps 2..5: decode + epilogue
+constexpr int kSlots = 2;           // groups staged at once (A in TMEM, B in shared memory)
+constexpr int kCodePrefetch = 3;    // groups of codes held in registers ahead of use
+constexpr int kMaxSplit = 8;
+constexpr int kBSlotBytes = 2 * kTok * 128;  // two 64-k boxes of 16 rows x 128 bytes
+
+// Tensor memory columns.
+constexpr uint32_t kColD0 = 0;       // group accumulator, even groups (16 fp32 columns)
+constexpr uint32_t kColD1 = 32;      // odd groups
+constexpr uint32_t kColConst = 64;   // 8 columns of bf16x2 (−136, −136): K = 16 of constant A
+constexpr uint32_t kColA = 128;      // + 64·slot: decoded weights of one group
+constexpr uint32_t kTmemCols = 256;
+// Shared memory per CTA is padded to this size so that at most two CTAs share
+// an SM, which keeps the tensor-memory allocations (2 x 256 columns) within
+// the SM's 512 columns: no allocation ever waits.
+constexpr int kSmemBytes = 80 * 1024;
+
+constexpr uint32_t kMinus136x2 = 0xC308C308u;
+
+struct TmemArgs {
+    const uint8_t* packed;
+    const uint16_t* scales;
+    __nv_bfloat16* y;
+    int M;  // token rows of this pass, 1..16
+    int64_t N, K;
+    int split;
+    unsigned* status;
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                     "memory");
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t local_addr, uint32_t rank) {
+    uint32_t remote;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+// Pair i (0..3) of a stored code word as the bf16x2 value (136 + q_lo, 136 + q_hi).
+__device__ __forceinline__ uint32_t biased_pair(uint32_t word, int i) {
+    return ((word >> (4 * i)) & 0x000F000Fu) ^ 0x43084308u;
+}
+
+struct Codes {
+    uint4 c[4];   // the row's 64-byte group block
+    uint32_t d;   // bf16 scale bits
+};
+
+__global__ void __launch_bounds__(kThreads, 2)
+gemv_tmem_kernel(const __grid_constant__ CUtensorMap tmap_x, const TmemArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+
+    const uint32_t b_base = base;                                // kSlots x 4 KB
+    const uint32_t red_base = b_base + kSlots * kBSlotBytes;     // 16 x 128 fp32
+    const uint32_t bar_base = red_base + kTok * kRows * 4;
+    auto a_full = [&](int s) { return bar_base + 8u * s; };
+    auto b_full = [&](int s) { return bar_base + 8u * (kSlots + s); };
+    auto slot_empty = [&](int s) { return bar_base + 8u * (2 * kSlots + s); };
+    auto d_full = [&](int b) { return bar_base + 8u * (3 * kSlots + b); };
+    auto d_empty = [&](int b) { return bar_base + 8u * (3 * kSlots + 2 + b); };
+    const uint32_t done_bar = bar_base + 8u * (3 * kSlots + 4);
+    const uint32_t tmem_slot = done_bar + 8u;
+    volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(gbase + (tmem_slot - base));
+    float* red = reinterpret_cast<float*>(gbase + (red_base - base));
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kRows;
+    const int64_t G = args.K >> 7;
+    const int split = args.split;
+    const uint32_t rank = split > 1 ? cluster_rank() : 0u;
+    const int64_t gs = (static_cast<int64_t>(rank) * G) / split;
+    const int64_t ge = (static_cast<int64_t>(rank + 1) * G) / split;
+    const int nj = static_cast<int>(ge - gs);
+    const int M = args.M;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(a_full(s), 128);
+            mbar_init(b_full(s), 1);
+            mbar_init(slot_empty(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(d_full(b), 1);
+            mbar_init(d_empty(b), 128);
+        }
+        mbar_init(done_bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_async_smem();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot_ptr;
+
+    // Decoder threads own TMEM lanes 32·(warp % 4) .. +31 (the lanes a warp may access).
+    const bool decoder = warp >= 2;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    if (decoder) {
+        tmem_st8(lane_base + kColConst, kMinus136x2);
+        tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    bool ok = true;
+    if (warp == 0) {
+        // -------------------------------------------------- activations via TMA
+        if (lane == 0) {
+            int issued = 0;
+            for (int j = 0; j < nj; ++j) {
+                const int s = j % kSlots;
+                const uint32_t rs = static_cast<uint32_t>(j / kSlots);
+                if (!mbar_wait(slot_empty(s), (rs & 1u) ^ 1u)) { ok = false; break; }
+                mbar_arrive_expect_tx(b_full(s), kBSlotBytes);
+                const int k0 = static_cast<int>((gs + j) * 128);
+                tma_load_2d(b_base + s * kBSlotBytes, &tmap_x, k0, 0, b_full(s));
+                tma_load_2d(b_base + s * kBSlotBytes + kBSlotBytes / 2, &tmap_x, k0 + 64, 0, b_full(s));
+                issued = j + 1;
+            }
+            if (!ok) {
+                record_status(args.status, kStatusTimeout);
+                for (int j = issued > kSlots ? issued - kSlots : 0; j < issued; ++j)
+                    mbar_wait(b_full(j % kSlots), static_cast<uint32_t>(j / kSlots) & 1u);
+            }
+        }
+    } else if (warp == 1) {
+        // -------------------------------------------------- MMA issue
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(kTok);
+            for (int j = 0; j < nj; ++j) {
+                const int s = j % kSlots;
+                const uint32_t rs = static_cast<uint32_t>(j / kSlots) & 1u;
+                const int b = j & 1;
+                if (!mbar_wait(b_full(s), rs) || !mbar_wait(a_full(s), rs)) { ok = false; break; }
+                if (j >= 2 && !mbar_wait(d_empty(b), static_cast<uint32_t>((j >> 1) - 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + (b ? kColD1 : kColD0);
+                const uint32_t a = tmem + kColA + 64u * s;
+                const uint32_t bs = b_base + s * kBSlotBytes;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint64_t bd = sw128_desc(bs + (ks >> 2) * (kBSlotBytes / 2) + (ks & 3) * 32);
+                    mma_bf16_tmem_a(d, a + 8u * ks, bd, idesc, ks > 0 ? 1u : 0u);
+                    mma_bf16_tmem_a(d, tmem + kColConst, bd, idesc, 1u);
+                }
+                mma_commit(slot_empty(s));
+                mma_commit(d_full(b));
+            }
+            mma_commit(done_bar);  // also tracks MMAs issued before an abort
+            if (!ok) record_status(args.status, kStatusTimeout);
+        }
+    } else {
+        // -------------------------------------------------- decode + epilogue
+        int64_t n = n0 + row;
+        if (n >= args.N) n = args.N - 1;  // padding rows read valid memory; outputs dropped
+        const uint8_t* prow = args.packed + n * (args.K >> 1) + gs * 64;
+        const uint16_t* srow = args.scales + n * G + gs;
+        auto fetch = [&](int j) {
+            Codes c;
+            if (j < nj) {
+                const uint8_t* p = prow + static_cast<int64_t>(j) * 64;
+                c.c[0] = ld_stream(p);
+                c.c[1] = ld_stream(p + 16);
+                c.c[2] = ld_stream(p + 32);
+                c.c[3] = ld_stream(p + 48);
+                c.d = __ldg(srow + j);
+            } else {
+                c.c[0] = c.c[1] = c.c[2] = c.c[3] = make_uint4(0, 0, 0, 0);
+                c.d = 0;
+            }
+            return c;
+        };
+        float acc[kTok];
+#pragma unroll
+        for (int m = 0; m < kTok; ++m) acc[m] = 0.0f;
+
+        // Reads group i's accumulator, scales it into acc and frees the buffer.
+        auto retire = [&](int i, uint32_t dbits) {
+            const int b = i & 1;
+            const bool got = mbar_wait(d_full(b), static_cast<uint32_t>(i >> 1) & 1u);
+            if (!__all_sync(0xffffffffu, got)) return false;
+            tc_fence_after();
+            uint32_t v[16];
+            tmem_ld16(lane_base + (b ? kColD1 : kColD0), v);
+            tc_fence_before();
+            mbar_arrive(d_empty(b));
+            const float d = bf16_lo(dbits);
+#pragma unroll
+            for (int m = 0; m < kTok; ++m)
+                if (m < M) acc[m] = fmaf(d, __uint_as_float(v[m]), acc[m]);
+            return true;
+        };
+
+        Codes ring[kCodePrefetch];
+#pragma unroll
+        for (int i = 0; i < kCodePrefetch; ++i) ring[i] = fetch(i);
+        uint32_t d_prev = 0;
+        for (int j0 = 0; j0 < nj && ok; j0 += kCodePrefetch) {
+#pragma unroll
+            for (int i = 0; i < kCodePrefetch; ++i) {
+                const int j = j0 + i;
+                if (j < nj && ok) {
+                    const Codes cur = ring[i];
+                    ring[i] = fetch(j + kCodePrefetch);
+                    const int s = j % kSlots;
+                    const uint32_t rs = static_cast<uint32_t>(j / kSlots);
+                    const bool free_slot = mbar_wait(slot_empty(s), (rs & 1u) ^ 1u);
+                    if (!__all_sync(0xffffffffu, free_slot)) {
+                        ok = false;
+                    } else {
+                        tc_fence_after();
+                        const uint32_t words[16] = {cur.c[0].x, cur.c[0].y, cur.c[0].z, cur.c[0].w,
+                                                    cur.c[1].x, cur.c[1].y, cur.c[1].z, cur.c[1].w,
+                                                    cur.c[2].x, cur.c[2].y, cur.c[2].z, cur.c[2].w,
+                                                    cur.c[3].x, cur.c[3].y, cur.c[3].z, cur.c[3].w};
+                        const uint32_t a_addr = lane_base + kColA + 64u * s;
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            uint32_t v[32];
+#pragma unroll
+                            for (int w = 0; w < 8; ++w)
+#pragma unroll
+                                for (int p = 0; p < 4; ++p) v[4 * w + p] = biased_pair(words[8 * half + w], p);
+                            tmem_st32(a_addr + 32u * half, v);
+                        }
+                        tmem_wait_st();
+                        tc_fence_before();
+                        mbar_arrive(a_full(s));
+                        if (j >= 1 && !retire(j - 1, d_prev)) ok = false;
+                        d_prev = cur.d;
+                    }
+                }
+            }
+        }
+        if (ok && nj > 0 && !retire(nj - 1, d_prev)) ok = false;
+        if (!ok) record_status(args.status, kStatusTimeout);
+
+        if (split == 1) {
+            const int64_t ny = n0 + row;
+            if (ny < args.N)
+                for (int m = 0; m < M; ++m) args.y[static_cast<int64_t>(m) * args.N + ny] = __float2bfloat16_rn(acc[m]);
+        } else {
+#pragma unroll
+            for (int m = 0; m < kTok; ++m) red[m * kRows + row] = acc[m];
+        }
+    }
+
+    // Split-K partials: rank 0 of the cluster sums them in rank order.
+    if (split > 1) {
+        cluster_sync();
+        if (rank == 0 && decoder) {
+            const int64_t ny = n0 + row;
+            if (ny < args.N) {
+                for (int m = 0; m < M; ++m) {
+                    const uint32_t addr = red_base + static_cast<uint32_t>((m * kRows + row) * 4);
+                    float v = 0.0f;
+                    for (int r = 0; r < split; ++r) v += ld_cluster_f32(addr, static_cast<uint32_t>(r));
+                    args.y[static_cast<int64_t>(m) * args.N + ny] = __float2bfloat16_rn(v);
+                }
+            }
+        }
+        cluster_sync();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        if (lane == 0) mbar_wait(done_bar, 0);  // MMAs in flight finish before TMEM is freed
+        __syncwarp();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+std::mutex g_attr_mutex;
+bool g_attr_set[64];
+
+}  // namespace
+
+cudaError_t launch_gemv_tmem(const void* x, int64_t M, int64_t N, int64_t K, const void* packed,
+                             const void* scales, void* y, const DeviceInfo& dev, cudaStream_t stream) {
+    const int64_t G = K / 128;
+    const int64_t row_blocks = (N + kRows - 1) / kRows;
+    if (row_blocks > 0x7fffffffLL || K > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    // Enough CTAs for two per SM, at most 8 per cluster, at least one group each.
+    int64_t split = (2 * static_cast<int64_t>(dev.sm_count) + row_blocks - 1) / row_blocks;
+    if (split > kMaxSplit) split = kMaxSplit;
+    if (split > G) split = G;
+    if (split < 1) split = 1;
+
+    int device = 0;
+    if (cudaError_t e = cudaGetDevice(&device)) return e;
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(g_attr_mutex);
+        if (!g_attr_set[device]) {
+            if (cudaError_t e = cudaFuncSetAttribute(gemv_tmem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     kSmemBytes))
+                return e;
+            g_attr_set[device] = true;
+        }
+    }
+    const auto* xb = static_cast<const __nv_bfloat16*>(x);
+    auto* yb = static_cast<__nv_bfloat16*>(y);
+    for (int64_t m0 = 0; m0 < M; m0 += kTok) {
+        const int mp = static_cast<int>(M - m0 < kTok ? M - m0 : kTok);
+        CUtensorMap tmap;
+        if (cudaError_t e = encode_x_map(&tmap, xb + m0 * K, mp, K, kTok)) return e;
+        TmemArgs args;
+        args.packed = static_cast<const uint8_t*>(packed);
+        args.scales = static_cast<const uint16_t*>(scales);
+        args.y = yb + m0 * N;
+        args.M = mp;
+        args.N = N;
+        args.K = K;
+        args.split = static_cast<int>(split);
+        args.status = dev.status;
+
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(row_blocks), static_cast<unsigned>(split), 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = static_cast<unsigned>(split);
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_tmem_kernel, tmap, args)) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace w4

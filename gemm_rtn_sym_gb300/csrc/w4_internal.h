@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace w4 {
@@ -29,6 +30,15 @@ cudaError_t launch_gemv(const void* x, int64_t M, int64_t N, int64_t K, const vo
 // Tensor-core path: tcgen05 MMA with TMEM accumulators, any M.
 cudaError_t launch_gemm_tc(const void* x, int64_t M, int64_t N, int64_t K, const void* packed,
                            const void* scales, void* y, const DeviceInfo& dev, cudaStream_t stream);
+
+// Small-M path on the tensor cores: dequantised weights written to TMEM as the
+// MMA's A operand, M <= 16 per pass.
+cudaError_t launch_gemv_tmem(const void* x, int64_t M, int64_t N, int64_t K, const void* packed,
+                             const void* scales, void* y, const DeviceInfo& dev, cudaStream_t stream);
+
+// 2-D tensor map over x bf16 [M, K]: boxes of 64 k x box_rows rows, 128-byte
+// swizzle, rows past M read as zeros.
+cudaError_t encode_x_map(CUtensorMap* map, const void* x, int64_t M, int64_t K, int box_rows);
 
 cudaError_t launch_wait_probe(int64_t spin_limit, int arrive, const DeviceInfo& dev,
                               cudaStream_t stream);
