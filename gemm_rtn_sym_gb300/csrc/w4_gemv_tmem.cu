@@ -9,18 +9,21 @@
 // so every SM must decode about 45 weights per clock.  The decode itself (one
 // shift and one LOP3 per pair of weights) is the floor of the instruction
 // stream; everything else is moved off the SM's issue slots:
-//  * each of 128 decoder threads owns one weight row; it loads its row's
-//    64-byte group block (kept kCodePrefetch groups ahead in registers), turns
-//    the 128 nibbles into 64 bf16x2 values 136 + q and writes them with two
-//    tcgen05.st into tensor memory, where they are the MMA's A operand
-//    (128 lanes = rows, one 32-bit column = one pair along K);
+//  * one thread streams, by TMA, each group's code tile (128 rows x 64 bytes,
+//    64-byte swizzle) and activation tile into a 4-deep shared-memory ring;
+//  * each of 128 decoder threads owns one weight row; it reads its row's 64
+//    bytes (conflict-free thanks to the swizzle), turns the 128 nibbles into
+//    64 bf16x2 values 136 + q and writes them with two tcgen05.st into tensor
+//    memory, where they are the MMA's A operand (128 lanes = rows, one 32-bit
+//    column = one pair along K);
 //  * the activations of the group (16 token rows, rows ≥ M read as zeros)
 //    arrive by TMA in a 128-byte-swizzled shared-memory tile, the B operand;
 //  * one thread issues per group 8 MMAs of 128×16×16 with the decoded A, plus
 //    8 more with a constant A tile of −136 that cancels the bias, so the fp32
 //    accumulator of the group holds Σ q·x exactly up to fp32 rounding;
-//  * the group accumulator (double-buffered in TMEM) is read back with one
-//    tcgen05.ld per thread and scaled by d in fp32 registers.
+//  * the group accumulators (three buffers in TMEM) are read back two groups
+//    behind with one tcgen05.ld per thread and scaled by d in fp32 registers;
+//  * waiting threads sleep in mbarrier try_wait instead of spinning.
 // Split-K: the CTAs of a thread-block cluster (1 × S) take disjoint group
 // ranges of the same 128 rows and sum their partials through distributed
 // shared memory in a fixed rank order, so results are deterministic and no
@@ -41,15 +44,16 @@ namespace {
 constexpr int kRows = 128;          // weight rows per CTA = MMA M
 constexpr int kTok = 16;            // token rows per pass = MMA N
 constexpr int kThreads = 192;       // warp 0: TMA, warp 1: TMEM + MMA, warps 2..5: decode + epilogue
-constexpr int kSlots = 2;           // groups staged at once (A in TMEM, B in shared memory)
-constexpr int kCodePrefetch = 3;    // groups of codes held in registers ahead of use
+constexpr int kInSlots = 4;         // groups of codes + activations in flight (shared memory)
+constexpr int kASlots = 2;          // decoded groups in TMEM
+constexpr int kDBufs = 3;           // group accumulators in TMEM: read back two groups behind
 constexpr int kMaxSplit = 8;
-constexpr int kBSlotBytes = 2 * kTok * 128;  // two 64-k boxes of 16 rows x 128 bytes
+constexpr int kCodeSlotBytes = kRows * 64;   // one group of 128 rows, 64-byte swizzle
+constexpr int kXSlotBytes = 2 * kTok * 128;  // two 64-k boxes of 16 rows x 128 bytes
 
 // Tensor memory columns.
-constexpr uint32_t kColD0 = 0;       // group accumulator, even groups (16 fp32 columns)
-constexpr uint32_t kColD1 = 32;      // odd groups
-constexpr uint32_t kColConst = 64;   // 8 columns of bf16x2 (−136, −136): K = 16 of constant A
+constexpr uint32_t kColD = 0;        // + 32·b: group accumulators (16 fp32 columns each)
+constexpr uint32_t kColConst = 96;   // 8 columns of bf16x2 (−136, −136): K = 16 of constant A
 constexpr uint32_t kColA = 128;      // + 64·slot: decoded weights of one group
 constexpr uint32_t kTmemCols = 256;
 // Shared memory per CTA is padded to this size so that at most two CTAs share
@@ -60,7 +64,6 @@ constexpr int kSmemBytes = 80 * 1024;
 constexpr uint32_t kMinus136x2 = 0xC308C308u;
 
 struct TmemArgs {
-    const uint8_t* packed;
     const uint16_t* scales;
     __nv_bfloat16* y;
     int M;  // token rows of this pass, 1..16
@@ -93,27 +96,25 @@ __device__ __forceinline__ uint32_t biased_pair(uint32_t word, int i) {
     return ((word >> (4 * i)) & 0x000F000Fu) ^ 0x43084308u;
 }
 
-struct Codes {
-    uint4 c[4];   // the row's 64-byte group block
-    uint32_t d;   // bf16 scale bits
-};
-
 __global__ void __launch_bounds__(kThreads, 2)
-gemv_tmem_kernel(const __grid_constant__ CUtensorMap tmap_x, const TmemArgs args) {
+gemv_tmem_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_codes,
+                 const TmemArgs args) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
 
-    const uint32_t b_base = base;                                // kSlots x 4 KB
-    const uint32_t red_base = b_base + kSlots * kBSlotBytes;     // 16 x 128 fp32
+    const uint32_t code_base = base;                                  // kInSlots x 8 KB
+    const uint32_t x_base = code_base + kInSlots * kCodeSlotBytes;    // kInSlots x 4 KB
+    const uint32_t red_base = x_base + kInSlots * kXSlotBytes;        // 16 x 128 fp32
     const uint32_t bar_base = red_base + kTok * kRows * 4;
-    auto a_full = [&](int s) { return bar_base + 8u * s; };
-    auto b_full = [&](int s) { return bar_base + 8u * (kSlots + s); };
-    auto slot_empty = [&](int s) { return bar_base + 8u * (2 * kSlots + s); };
-    auto d_full = [&](int b) { return bar_base + 8u * (3 * kSlots + b); };
-    auto d_empty = [&](int b) { return bar_base + 8u * (3 * kSlots + 2 + b); };
-    const uint32_t done_bar = bar_base + 8u * (3 * kSlots + 4);
+    auto in_full = [&](int c) { return bar_base + 8u * c; };
+    auto in_empty = [&](int c) { return bar_base + 8u * (kInSlots + c); };
+    auto a_full = [&](int s) { return bar_base + 8u * (2 * kInSlots + s); };
+    auto a_empty = [&](int s) { return bar_base + 8u * (2 * kInSlots + kASlots + s); };
+    auto d_full = [&](int b) { return bar_base + 8u * (2 * kInSlots + 2 * kASlots + b); };
+    auto d_empty = [&](int b) { return bar_base + 8u * (2 * kInSlots + 2 * kASlots + kDBufs + b); };
+    const uint32_t done_bar = bar_base + 8u * (2 * kInSlots + 2 * kASlots + 2 * kDBufs);
     const uint32_t tmem_slot = done_bar + 8u;
     volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(gbase + (tmem_slot - base));
     float* red = reinterpret_cast<float*>(gbase + (red_base - base));
@@ -130,12 +131,15 @@ gemv_tmem_kernel(const __grid_constant__ CUtensorMap tmap_x, const TmemArgs args
     const int M = args.M;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kSlots; ++s) {
-            mbar_init(a_full(s), 128);
-            mbar_init(b_full(s), 1);
-            mbar_init(slot_empty(s), 1);
+        for (int c = 0; c < kInSlots; ++c) {
+            mbar_init(in_full(c), 1);
+            mbar_init(in_empty(c), 128 + 1);  // decoders have read the codes, MMAs have read x
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int s = 0; s < kASlots; ++s) {
+            mbar_init(a_full(s), 128);
+            mbar_init(a_empty(s), 1);
+        }
+        for (int b = 0; b < kDBufs; ++b) {
             mbar_init(d_full(b), 1);
             mbar_init(d_empty(b), 128);
         }
@@ -164,23 +168,24 @@ gemv_tmem_kernel(const __grid_constant__ CUtensorMap tmap_x, const TmemArgs args
 
     bool ok = true;
     if (warp == 0) {
-        // -------------------------------------------------- activations via TMA
+        // -------------------------------------------------- codes + activations via TMA
         if (lane == 0) {
             int issued = 0;
             for (int j = 0; j < nj; ++j) {
-                const int s = j % kSlots;
-                const uint32_t rs = static_cast<uint32_t>(j / kSlots);
-                if (!mbar_wait(slot_empty(s), (rs & 1u) ^ 1u)) { ok = false; break; }
-                mbar_arrive_expect_tx(b_full(s), kBSlotBytes);
-                const int k0 = static_cast<int>((gs + j) * 128);
-                tma_load_2d(b_base + s * kBSlotBytes, &tmap_x, k0, 0, b_full(s));
-                tma_load_2d(b_base + s * kBSlotBytes + kBSlotBytes / 2, &tmap_x, k0 + 64, 0, b_full(s));
+                const int c = j % kInSlots;
+                const uint32_t rc = static_cast<uint32_t>(j / kInSlots);
+                if (!mbar_wait(in_empty(c), (rc & 1u) ^ 1u)) { ok = false; break; }
+                mbar_arrive_expect_tx(in_full(c), kCodeSlotBytes + kXSlotBytes);
+                const int g = static_cast<int>(gs + j);
+                tma_load_2d(code_base + c * kCodeSlotBytes, &tmap_codes, g * 64, static_cast<int>(n0), in_full(c));
+                tma_load_2d(x_base + c * kXSlotBytes, &tmap_x, g * 128, 0, in_full(c));
+                tma_load_2d(x_base + c * kXSlotBytes + kXSlotBytes / 2, &tmap_x, g * 128 + 64, 0, in_full(c));
                 issued = j + 1;
             }
             if (!ok) {
                 record_status(args.status, kStatusTimeout);
-                for (int j = issued > kSlots ? issued - kSlots : 0; j < issued; ++j)
-                    mbar_wait(b_full(j % kSlots), static_cast<uint32_t>(j / kSlots) & 1u);
+                for (int j = issued > kInSlots ? issued - kInSlots : 0; j < issued; ++j)
+                    mbar_wait(in_full(j % kInSlots), static_cast<uint32_t>(j / kInSlots) & 1u);
             }
         }
     } else if (warp == 1) {
@@ -188,25 +193,27 @@ gemv_tmem_kernel(const __grid_constant__ CUtensorMap tmap_x, const TmemArgs args
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16(kTok);
             for (int j = 0; j < nj; ++j) {
-                const int s = j % kSlots;
-                const uint32_t rs = static_cast<uint32_t>(j / kSlots) & 1u;
-                const int b = j & 1;
-                if (!mbar_wait(b_full(s), rs) || !mbar_wait(a_full(s), rs)) { ok = false; break; }
-                if (j >= 2 && !mbar_wait(d_empty(b), static_cast<uint32_t>((j >> 1) - 1) & 1u)) {
+                const int c = j % kInSlots;
+                const int s = j % kASlots;
+                const int b = j % kDBufs;
+                if (!mbar_wait(in_full(c), static_cast<uint32_t>(j / kInSlots) & 1u) ||
+                    !mbar_wait(a_full(s), static_cast<uint32_t>(j / kASlots) & 1u) ||
+                    (j >= kDBufs && !mbar_wait(d_empty(b), static_cast<uint32_t>(j / kDBufs - 1) & 1u))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d = tmem + (b ? kColD1 : kColD0);
+                const uint32_t d = tmem + kColD + 32u * b;
                 const uint32_t a = tmem + kColA + 64u * s;
-                const uint32_t bs = b_base + s * kBSlotBytes;
+                const uint32_t xs = x_base + c * kXSlotBytes;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    const uint64_t bd = sw128_desc(bs + (ks >> 2) * (kBSlotBytes / 2) + (ks & 3) * 32);
+                    const uint64_t bd = sw128_desc(xs + (ks >> 2) * (kXSlotBytes / 2) + (ks & 3) * 32);
                     mma_bf16_tmem_a(d, a + 8u * ks, bd, idesc, ks > 0 ? 1u : 0u);
                     mma_bf16_tmem_a(d, tmem + kColConst, bd, idesc, 1u);
                 }
-                mma_commit(slot_empty(s));
+                mma_commit(a_empty(s));
+                mma_commit(in_empty(c));
                 mma_commit(d_full(b));
             }
             mma_commit(done_bar);  // also tracks MMAs issued before an abort
@@ -215,36 +222,20 @@ gemv_tmem_kernel(const __grid_constant__ CUtensorMap tmap_x, const TmemArgs args
     } else {
         // -------------------------------------------------- decode + epilogue
         int64_t n = n0 + row;
-        if (n >= args.N) n = args.N - 1;  // padding rows read valid memory; outputs dropped
-        const uint8_t* prow = args.packed + n * (args.K >> 1) + gs * 64;
+        if (n >= args.N) n = args.N - 1;  // padding rows: codes arrive as zeros, scale of a valid row
         const uint16_t* srow = args.scales + n * G + gs;
-        auto fetch = [&](int j) {
-            Codes c;
-            if (j < nj) {
-                const uint8_t* p = prow + static_cast<int64_t>(j) * 64;
-                c.c[0] = ld_stream(p);
-                c.c[1] = ld_stream(p + 16);
-                c.c[2] = ld_stream(p + 32);
-                c.c[3] = ld_stream(p + 48);
-                c.d = __ldg(srow + j);
-            } else {
-                c.c[0] = c.c[1] = c.c[2] = c.c[3] = make_uint4(0, 0, 0, 0);
-                c.d = 0;
-            }
-            return c;
-        };
         float acc[kTok];
 #pragma unroll
         for (int m = 0; m < kTok; ++m) acc[m] = 0.0f;
 
         // Reads group i's accumulator, scales it into acc and frees the buffer.
         auto retire = [&](int i, uint32_t dbits) {
-            const int b = i & 1;
-            const bool got = mbar_wait(d_full(b), static_cast<uint32_t>(i >> 1) & 1u);
+            const int b = i % kDBufs;
+            const bool got = mbar_wait(d_full(b), static_cast<uint32_t>(i / kDBufs) & 1u);
             if (!__all_sync(0xffffffffu, got)) return false;
             tc_fence_after();
             uint32_t v[16];
-            tmem_ld16(lane_base + (b ? kColD1 : kColD0), v);
+            tmem_ld16(lane_base + kColD + 32u * b, v);
             tc_fence_before();
             mbar_arrive(d_empty(b));
             const float d = bf16_lo(dbits);
@@ -254,48 +245,51 @@ gemv_tmem_kernel(const __grid_constant__ CUtensorMap tmap_x, const TmemArgs args
             return true;
         };
 
-        Codes ring[kCodePrefetch];
+        // Byte offset of 16-byte chunk q of this thread's row in a code slot
+        // (64-byte swizzle: chunk bits 4-5 XOR address bits 7-8).
+        const uint32_t row_off = static_cast<uint32_t>(row * 64);
+        const uint32_t sw = static_cast<uint32_t>((row >> 1) & 3);
+
+        uint32_t d_hist[3] = {0, 0, 0};  // scales of groups j-2, j-1, j
+        uint32_t d_next = nj > 0 ? __ldg(srow) : 0u;
+        for (int j = 0; j < nj && ok; ++j) {
+            const int c = j % kInSlots;
+            const int s = j % kASlots;
+            d_hist[0] = d_hist[1];
+            d_hist[1] = d_hist[2];
+            d_hist[2] = d_next;
+            if (j + 1 < nj) d_next = __ldg(srow + j + 1);
+
+            const bool have = mbar_wait(in_full(c), static_cast<uint32_t>(j / kInSlots) & 1u);
+            if (!__all_sync(0xffffffffu, have)) { ok = false; break; }
+            uint4 q[4];
+            const uint32_t slot = code_base + c * kCodeSlotBytes + row_off;
 #pragma unroll
-        for (int i = 0; i < kCodePrefetch; ++i) ring[i] = fetch(i);
-        uint32_t d_prev = 0;
-        for (int j0 = 0; j0 < nj && ok; j0 += kCodePrefetch) {
+            for (int ch = 0; ch < 4; ++ch) q[ch] = lds128(slot + ((static_cast<uint32_t>(ch) ^ sw) << 4));
+            mbar_arrive(in_empty(c));
+
+            const bool free_a = mbar_wait(a_empty(s), (static_cast<uint32_t>(j / kASlots) & 1u) ^ 1u);
+            if (!__all_sync(0xffffffffu, free_a)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t words[16] = {q[0].x, q[0].y, q[0].z, q[0].w, q[1].x, q[1].y, q[1].z, q[1].w,
+                                        q[2].x, q[2].y, q[2].z, q[2].w, q[3].x, q[3].y, q[3].z, q[3].w};
+            const uint32_t a_addr = lane_base + kColA + 64u * s;
 #pragma unroll
-            for (int i = 0; i < kCodePrefetch; ++i) {
-                const int j = j0 + i;
-                if (j < nj && ok) {
-                    const Codes cur = ring[i];
-                    ring[i] = fetch(j + kCodePrefetch);
-                    const int s = j % kSlots;
-                    const uint32_t rs = static_cast<uint32_t>(j / kSlots);
-                    const bool free_slot = mbar_wait(slot_empty(s), (rs & 1u) ^ 1u);
-                    if (!__all_sync(0xffffffffu, free_slot)) {
-                        ok = false;
-                    } else {
-                        tc_fence_after();
-                        const uint32_t words[16] = {cur.c[0].x, cur.c[0].y, cur.c[0].z, cur.c[0].w,
-                                                    cur.c[1].x, cur.c[1].y, cur.c[1].z, cur.c[1].w,
-                                                    cur.c[2].x, cur.c[2].y, cur.c[2].z, cur.c[2].w,
-                                                    cur.c[3].x, cur.c[3].y, cur.c[3].z, cur.c[3].w};
-                        const uint32_t a_addr = lane_base + kColA + 64u * s;
+            for (int half = 0; half < 2; ++half) {
+                uint32_t v[32];
 #pragma unroll
-                        for (int half = 0; half < 2; ++half) {
-                            uint32_t v[32];
+                for (int w = 0; w < 8; ++w)
 #pragma unroll
-                            for (int w = 0; w < 8; ++w)
-#pragma unroll
-                                for (int p = 0; p < 4; ++p) v[4 * w + p] = biased_pair(words[8 * half + w], p);
-                            tmem_st32(a_addr + 32u * half, v);
-                        }
-                        tmem_wait_st();
-                        tc_fence_before();
-                        mbar_arrive(a_full(s));
-                        if (j >= 1 && !retire(j - 1, d_prev)) ok = false;
-                        d_prev = cur.d;
-                    }
-                }
+                    for (int p = 0; p < 4; ++p) v[4 * w + p] = biased_pair(words[8 * half + w], p);
+                tmem_st32(a_addr + 32u * half, v);
             }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(a_full(s));
+            if (j >= 2 && !retire(j - 2, d_hist[0])) ok = false;
         }
-        if (ok && nj > 0 && !retire(nj - 1, d_prev)) ok = false;
+        if (ok && nj >= 2 && !retire(nj - 2, d_hist[1])) ok = false;
+        if (ok && nj >= 1 && !retire(nj - 1, d_hist[2])) ok = false;
         if (!ok) record_status(args.status, kStatusTimeout);
 
         if (split == 1) {
@@ -344,7 +338,7 @@ cudaError_t launch_gemv_tmem(const void* x, int64_t M, int64_t N, int64_t K, con
                              const void* scales, void* y, const DeviceInfo& dev, cudaStream_t stream) {
     const int64_t G = K / 128;
     const int64_t row_blocks = (N + kRows - 1) / kRows;
-    if (row_blocks > 0x7fffffffLL || K > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if (row_blocks > 0x7fffffffLL || K > 0x7fffffffLL || N > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     // Enough CTAs for two per SM, at most 8 per cluster, at least one group each.
     int64_t split = (2 * static_cast<int64_t>(dev.sm_count) + row_blocks - 1) / row_blocks;
     if (split > kMaxSplit) split = kMaxSplit;
@@ -363,14 +357,15 @@ cudaError_t launch_gemv_tmem(const void* x, int64_t M, int64_t N, int64_t K, con
             g_attr_set[device] = true;
         }
     }
+    CUtensorMap tmap_codes;
+    if (cudaError_t e = encode_codes_map(&tmap_codes, packed, N, K)) return e;
     const auto* xb = static_cast<const __nv_bfloat16*>(x);
     auto* yb = static_cast<__nv_bfloat16*>(y);
     for (int64_t m0 = 0; m0 < M; m0 += kTok) {
         const int mp = static_cast<int>(M - m0 < kTok ? M - m0 : kTok);
-        CUtensorMap tmap;
-        if (cudaError_t e = encode_x_map(&tmap, xb + m0 * K, mp, K, kTok)) return e;
+        CUtensorMap tmap_x;
+        if (cudaError_t e = encode_x_map(&tmap_x, xb + m0 * K, mp, K, kTok)) return e;
         TmemArgs args;
-        args.packed = static_cast<const uint8_t*>(packed);
         args.scales = static_cast<const uint16_t*>(scales);
         args.y = yb + m0 * N;
         args.M = mp;
@@ -391,7 +386,7 @@ cudaError_t launch_gemv_tmem(const void* x, int64_t M, int64_t N, int64_t K, con
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_tmem_kernel, tmap, args)) return e;
+        if (cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_tmem_kernel, tmap_x, tmap_codes, args)) return e;
     }
     return cudaSuccess;
 }
