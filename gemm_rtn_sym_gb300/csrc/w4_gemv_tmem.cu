@@ -10,10 +10,12 @@
 // shift and one LOP3 per pair of weights) is the floor of the instruction
 // stream; everything else is moved off the SM's issue slots:
 //  * one thread streams, by TMA, each group's code tile (128 rows x 64 bytes,
-//    64-byte swizzle) and activation tile into a 4-deep shared-memory ring;
-//  * each of 128 decoder threads owns one weight row; it reads its row's 64
-//    bytes (conflict-free thanks to the swizzle), turns the 128 nibbles into
-//    64 bf16x2 values 136 + q and writes them with two tcgen05.st into tensor
+//    64-byte swizzle) into a 20-deep shared-memory ring (160 KB: at the loaded
+//    HBM latency every SM needs well over 100 KB in flight), another the
+//    group's activation tile into a 4-deep ring;
+//  * 256 decoder threads, two per weight row, each read 32 bytes of their
+//    row (conflict-free thanks to the swizzle), turn the 64 nibbles into 32
+//    bf16x2 values 136 + q and write them with one tcgen05.st into tensor
 //    memory, where they are the MMA's A operand (128 lanes = rows, one 32-bit
 //    column = one pair along K);
 //  * the activations of the group (16 token rows, rows ≥ M read as zeros)
@@ -21,8 +23,8 @@
 //  * one thread issues per group 8 MMAs of 128×16×16 with the decoded A, plus
 //    8 more with a constant A tile of −136 that cancels the bias, so the fp32
 //    accumulator of the group holds Σ q·x exactly up to fp32 rounding;
-//  * the group accumulators (three buffers in TMEM) are read back two groups
-//    behind with one tcgen05.ld per thread and scaled by d in fp32 registers;
+//  * the group accumulators (four buffers in TMEM) are read back three groups
+//    behind with one tcgen05.ld per row and scaled by d in fp32 registers;
 //  * waiting threads sleep in mbarrier try_wait instead of spinning.
 // Split-K: the CTAs of a thread-block cluster (1 × S) take disjoint group
 // ranges of the same 128 rows and sum their partials through distributed
@@ -43,23 +45,25 @@ namespace {
 
 constexpr int kRows = 128;          // weight rows per CTA = MMA M
 constexpr int kTok = 16;            // token rows per pass = MMA N
-constexpr int kThreads = 192;       // warp 0: TMA, warp 1: TMEM + MMA, warps 2..5: decode + epilogue
-constexpr int kInSlots = 4;         // groups of codes + activations in flight (shared memory)
-constexpr int kASlots = 2;          // decoded groups in TMEM
-constexpr int kDBufs = 3;           // group accumulators in TMEM: read back two groups behind
+// Warps: 0 code TMA, 1 TMEM + MMA, 2 activation TMA, 3..10 decoders (two per
+// TMEM lane quarter, each decoding half of a group's k range).
+constexpr int kDecoderWarp0 = 3;
+constexpr int kDecoders = 256;
+constexpr int kThreads = 32 * kDecoderWarp0 + kDecoders;
+constexpr int kCodeSlots = 20;      // groups of codes in flight: 160 KB, most of shared memory
+constexpr int kXSlots = 4;          // activation groups (L2-resident) in flight
+constexpr int kASlots = 4;          // decoded groups in TMEM
+constexpr int kDBufs = 4;           // group accumulators in TMEM: read back kDBufs-1 groups behind
 constexpr int kMaxSplit = 8;
 constexpr int kCodeSlotBytes = kRows * 64;   // one group of 128 rows, 64-byte swizzle
 constexpr int kXSlotBytes = 2 * kTok * 128;  // two 64-k boxes of 16 rows x 128 bytes
 
-// Tensor memory columns.
+// Tensor memory columns (one CTA per SM: the whole 512-column TMEM).
 constexpr uint32_t kColD = 0;        // + 32·b: group accumulators (16 fp32 columns each)
-constexpr uint32_t kColConst = 96;   // 8 columns of bf16x2 (−136, −136): K = 16 of constant A
-constexpr uint32_t kColA = 128;      // + 64·slot: decoded weights of one group
-constexpr uint32_t kTmemCols = 256;
-// Shared memory per CTA is padded to this size so that at most two CTAs share
-// an SM, which keeps the tensor-memory allocations (2 x 256 columns) within
-// the SM's 512 columns: no allocation ever waits.
-constexpr int kSmemBytes = 80 * 1024;
+constexpr uint32_t kColConst = 128;  // 8 columns of bf16x2 (−136, −136): K = 16 of constant A
+constexpr uint32_t kColA = 256;      // + 64·slot: decoded weights of one group
+constexpr uint32_t kTmemCols = 512;
+constexpr int kSmemBytes = kCodeSlots * kCodeSlotBytes + kXSlots * kXSlotBytes + kTok * kRows * 4 + 1024 + 1024;
 
 constexpr uint32_t kMinus136x2 = 0xC308C308u;
 
@@ -96,7 +100,7 @@ __device__ __forceinline__ uint32_t biased_pair(uint32_t word, int i) {
     return ((word >> (4 * i)) & 0x000F000Fu) ^ 0x43084308u;
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
 gemv_tmem_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_codes,
                  const TmemArgs args) {
     extern __shared__ uint8_t smem_raw[];
@@ -104,17 +108,22 @@ gemv_tmem_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
 
-    const uint32_t code_base = base;                                  // kInSlots x 8 KB
-    const uint32_t x_base = code_base + kInSlots * kCodeSlotBytes;    // kInSlots x 4 KB
-    const uint32_t red_base = x_base + kInSlots * kXSlotBytes;        // 16 x 128 fp32
+    const uint32_t code_base = base;                                  // kCodeSlots x 8 KB
+    const uint32_t x_base = code_base + kCodeSlots * kCodeSlotBytes;  // kXSlots x 4 KB
+    const uint32_t red_base = x_base + kXSlots * kXSlotBytes;         // 16 x 128 fp32
     const uint32_t bar_base = red_base + kTok * kRows * 4;
-    auto in_full = [&](int c) { return bar_base + 8u * c; };
-    auto in_empty = [&](int c) { return bar_base + 8u * (kInSlots + c); };
-    auto a_full = [&](int s) { return bar_base + 8u * (2 * kInSlots + s); };
-    auto a_empty = [&](int s) { return bar_base + 8u * (2 * kInSlots + kASlots + s); };
-    auto d_full = [&](int b) { return bar_base + 8u * (2 * kInSlots + 2 * kASlots + b); };
-    auto d_empty = [&](int b) { return bar_base + 8u * (2 * kInSlots + 2 * kASlots + kDBufs + b); };
-    const uint32_t done_bar = bar_base + 8u * (2 * kInSlots + 2 * kASlots + 2 * kDBufs);
+    auto code_full = [&](int c) { return bar_base + 8u * c; };
+    auto code_empty = [&](int c) { return bar_base + 8u * (kCodeSlots + c); };
+    constexpr int kB1 = 2 * kCodeSlots;
+    auto x_full = [&](int c) { return bar_base + 8u * (kB1 + c); };
+    auto x_empty = [&](int c) { return bar_base + 8u * (kB1 + kXSlots + c); };
+    constexpr int kB2 = kB1 + 2 * kXSlots;
+    auto a_full = [&](int s) { return bar_base + 8u * (kB2 + s); };
+    auto a_empty = [&](int s) { return bar_base + 8u * (kB2 + kASlots + s); };
+    constexpr int kB3 = kB2 + 2 * kASlots;
+    auto d_full = [&](int b) { return bar_base + 8u * (kB3 + b); };
+    auto d_empty = [&](int b) { return bar_base + 8u * (kB3 + kDBufs + b); };
+    const uint32_t done_bar = bar_base + 8u * (kB3 + 2 * kDBufs);
     const uint32_t tmem_slot = done_bar + 8u;
     volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(gbase + (tmem_slot - base));
     float* red = reinterpret_cast<float*>(gbase + (red_base - base));
@@ -131,17 +140,21 @@ gemv_tmem_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
     const int M = args.M;
 
     if (threadIdx.x == 0) {
-        for (int c = 0; c < kInSlots; ++c) {
-            mbar_init(in_full(c), 1);
-            mbar_init(in_empty(c), 128 + 1);  // decoders have read the codes, MMAs have read x
+        for (int c = 0; c < kCodeSlots; ++c) {
+            mbar_init(code_full(c), 1);
+            mbar_init(code_empty(c), kDecoders);
+        }
+        for (int c = 0; c < kXSlots; ++c) {
+            mbar_init(x_full(c), 1);
+            mbar_init(x_empty(c), 1);
         }
         for (int s = 0; s < kASlots; ++s) {
-            mbar_init(a_full(s), 128);
+            mbar_init(a_full(s), kDecoders);
             mbar_init(a_empty(s), 1);
         }
         for (int b = 0; b < kDBufs; ++b) {
             mbar_init(d_full(b), 1);
-            mbar_init(d_empty(b), 128);
+            mbar_init(d_empty(b), kRows);
         }
         mbar_init(done_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -153,12 +166,15 @@ gemv_tmem_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
     tc_fence_after();
     const uint32_t tmem = *tmem_slot_ptr;
 
-    // Decoder threads own TMEM lanes 32·(warp % 4) .. +31 (the lanes a warp may access).
-    const bool decoder = warp >= 2;
+    // Decoder threads: TMEM lane quarter warp % 4 (the lanes a warp may access),
+    // k half `half` of every group.
+    const bool decoder = warp >= kDecoderWarp0;
     const int quarter = warp & 3;
+    const int half = (warp - kDecoderWarp0) >> 2;
     const int row = quarter * 32 + lane;
+    const bool owner = decoder && half == 0;  // keeps the row's accumulator
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    if (decoder) {
+    if (owner) {
         tmem_st8(lane_base + kColConst, kMinus136x2);
         tmem_wait_st();
     }
@@ -168,24 +184,46 @@ gemv_tmem_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
 
     bool ok = true;
     if (warp == 0) {
-        // -------------------------------------------------- codes + activations via TMA
+        // -------------------------------------------------- codes via TMA
         if (lane == 0) {
             int issued = 0;
             for (int j = 0; j < nj; ++j) {
-                const int c = j % kInSlots;
-                const uint32_t rc = static_cast<uint32_t>(j / kInSlots);
-                if (!mbar_wait(in_empty(c), (rc & 1u) ^ 1u)) { ok = false; break; }
-                mbar_arrive_expect_tx(in_full(c), kCodeSlotBytes + kXSlotBytes);
-                const int g = static_cast<int>(gs + j);
-                tma_load_2d(code_base + c * kCodeSlotBytes, &tmap_codes, g * 64, static_cast<int>(n0), in_full(c));
-                tma_load_2d(x_base + c * kXSlotBytes, &tmap_x, g * 128, 0, in_full(c));
-                tma_load_2d(x_base + c * kXSlotBytes + kXSlotBytes / 2, &tmap_x, g * 128 + 64, 0, in_full(c));
+                const int c = j % kCodeSlots;
+                if (!mbar_wait(code_empty(c), (static_cast<uint32_t>(j / kCodeSlots) & 1u) ^ 1u)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(code_full(c), kCodeSlotBytes);
+                tma_load_2d(code_base + c * kCodeSlotBytes, &tmap_codes, static_cast<int>((gs + j) * 64),
+                            static_cast<int>(n0), code_full(c));
                 issued = j + 1;
             }
             if (!ok) {
                 record_status(args.status, kStatusTimeout);
-                for (int j = issued > kInSlots ? issued - kInSlots : 0; j < issued; ++j)
-                    mbar_wait(in_full(j % kInSlots), static_cast<uint32_t>(j / kInSlots) & 1u);
+                for (int j = issued > kCodeSlots ? issued - kCodeSlots : 0; j < issued; ++j)
+                    mbar_wait(code_full(j % kCodeSlots), static_cast<uint32_t>(j / kCodeSlots) & 1u);
+            }
+        }
+    } else if (warp == 2) {
+        // -------------------------------------------------- activations via TMA
+        if (lane == 0) {
+            int issued = 0;
+            for (int j = 0; j < nj; ++j) {
+                const int c = j % kXSlots;
+                if (!mbar_wait(x_empty(c), (static_cast<uint32_t>(j / kXSlots) & 1u) ^ 1u)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(x_full(c), kXSlotBytes);
+                const int k0 = static_cast<int>((gs + j) * 128);
+                tma_load_2d(x_base + c * kXSlotBytes, &tmap_x, k0, 0, x_full(c));
+                tma_load_2d(x_base + c * kXSlotBytes + kXSlotBytes / 2, &tmap_x, k0 + 64, 0, x_full(c));
+                issued = j + 1;
+            }
+            if (!ok) {
+                record_status(args.status, kStatusTimeout);
+                for (int j = issued > kXSlots ? issued - kXSlots : 0; j < issued; ++j)
+                    mbar_wait(x_full(j % kXSlots), static_cast<uint32_t>(j / kXSlots) & 1u);
             }
         }
     } else if (warp == 1) {
@@ -193,10 +231,10 @@ gemv_tmem_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16(kTok);
             for (int j = 0; j < nj; ++j) {
-                const int c = j % kInSlots;
+                const int c = j % kXSlots;
                 const int s = j % kASlots;
                 const int b = j % kDBufs;
-                if (!mbar_wait(in_full(c), static_cast<uint32_t>(j / kInSlots) & 1u) ||
+                if (!mbar_wait(x_full(c), static_cast<uint32_t>(j / kXSlots) & 1u) ||
                     !mbar_wait(a_full(s), static_cast<uint32_t>(j / kASlots) & 1u) ||
                     (j >= kDBufs && !mbar_wait(d_empty(b), static_cast<uint32_t>(j / kDBufs - 1) & 1u))) {
                     ok = false;
@@ -213,7 +251,7 @@ gemv_tmem_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
                     mma_bf16_tmem_a(d, tmem + kColConst, bd, idesc, 1u);
                 }
                 mma_commit(a_empty(s));
-                mma_commit(in_empty(c));
+                mma_commit(x_empty(c));
                 mma_commit(d_full(b));
             }
             mma_commit(done_bar);  // also tracks MMAs issued before an abort
@@ -245,67 +283,73 @@ gemv_tmem_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
             return true;
         };
 
-        // Byte offset of 16-byte chunk q of this thread's row in a code slot
+        // This thread's two 16-byte chunks (k half) of its row in a code slot
         // (64-byte swizzle: chunk bits 4-5 XOR address bits 7-8).
         const uint32_t row_off = static_cast<uint32_t>(row * 64);
         const uint32_t sw = static_cast<uint32_t>((row >> 1) & 3);
+        const uint32_t ch0 = static_cast<uint32_t>(2 * half);
+        const uint32_t off0 = row_off + ((ch0 ^ sw) << 4);
+        const uint32_t off1 = row_off + (((ch0 + 1) ^ sw) << 4);
 
-        uint32_t d_hist[3] = {0, 0, 0};  // scales of groups j-2, j-1, j
-        uint32_t d_next = nj > 0 ? __ldg(srow) : 0u;
-        for (int j = 0; j < nj && ok; ++j) {
-            const int c = j % kInSlots;
-            const int s = j % kASlots;
-            d_hist[0] = d_hist[1];
-            d_hist[1] = d_hist[2];
-            d_hist[2] = d_next;
-            if (j + 1 < nj) d_next = __ldg(srow + j + 1);
-
-            const bool have = mbar_wait(in_full(c), static_cast<uint32_t>(j / kInSlots) & 1u);
-            if (!__all_sync(0xffffffffu, have)) { ok = false; break; }
-            uint4 q[4];
-            const uint32_t slot = code_base + c * kCodeSlotBytes + row_off;
+        constexpr int kLag = kDBufs - 1;
+        uint32_t d_hist[kLag + 1];  // scales of groups j-kLag .. j
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) q[ch] = lds128(slot + ((static_cast<uint32_t>(ch) ^ sw) << 4));
-            mbar_arrive(in_empty(c));
+        for (int i = 0; i <= kLag; ++i) d_hist[i] = 0;
+        uint32_t d_next = (owner && nj > 0) ? __ldg(srow) : 0u;
+        for (int j = 0; j < nj && ok; ++j) {
+            const int c = j % kCodeSlots;
+            const int s = j % kASlots;
+            if (owner) {
+#pragma unroll
+                for (int i = 0; i < kLag; ++i) d_hist[i] = d_hist[i + 1];
+                d_hist[kLag] = d_next;
+                if (j + 1 < nj) d_next = __ldg(srow + j + 1);
+            }
+            const bool have = mbar_wait(code_full(c), static_cast<uint32_t>(j / kCodeSlots) & 1u);
+            if (!__all_sync(0xffffffffu, have)) { ok = false; break; }
+            const uint32_t slot = code_base + c * kCodeSlotBytes;
+            const uint4 q0 = lds128(slot + off0);
+            const uint4 q1 = lds128(slot + off1);
+            mbar_arrive(code_empty(c));
 
             const bool free_a = mbar_wait(a_empty(s), (static_cast<uint32_t>(j / kASlots) & 1u) ^ 1u);
             if (!__all_sync(0xffffffffu, free_a)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t words[16] = {q[0].x, q[0].y, q[0].z, q[0].w, q[1].x, q[1].y, q[1].z, q[1].w,
-                                        q[2].x, q[2].y, q[2].z, q[2].w, q[3].x, q[3].y, q[3].z, q[3].w};
-            const uint32_t a_addr = lane_base + kColA + 64u * s;
+            const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+            uint32_t v[32];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t v[32];
+            for (int w = 0; w < 8; ++w)
 #pragma unroll
-                for (int w = 0; w < 8; ++w)
-#pragma unroll
-                    for (int p = 0; p < 4; ++p) v[4 * w + p] = biased_pair(words[8 * half + w], p);
-                tmem_st32(a_addr + 32u * half, v);
-            }
+                for (int p = 0; p < 4; ++p) v[4 * w + p] = biased_pair(words[w], p);
+            tmem_st32(lane_base + kColA + 64u * s + 32u * half, v);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(a_full(s));
-            if (j >= 2 && !retire(j - 2, d_hist[0])) ok = false;
+            if (owner && j >= kLag && !retire(j - kLag, d_hist[0])) ok = false;
         }
-        if (ok && nj >= 2 && !retire(nj - 2, d_hist[1])) ok = false;
-        if (ok && nj >= 1 && !retire(nj - 1, d_hist[2])) ok = false;
+        if (owner && ok) {
+            for (int i = nj - kLag < 0 ? 0 : nj - kLag; i < nj && ok; ++i)
+                if (!retire(i, d_hist[kLag - (nj - 1 - i)])) ok = false;
+        }
         if (!ok) record_status(args.status, kStatusTimeout);
 
-        if (split == 1) {
-            const int64_t ny = n0 + row;
-            if (ny < args.N)
-                for (int m = 0; m < M; ++m) args.y[static_cast<int64_t>(m) * args.N + ny] = __float2bfloat16_rn(acc[m]);
-        } else {
+        if (owner) {
+            if (split == 1) {
+                const int64_t ny = n0 + row;
+                if (ny < args.N)
+                    for (int m = 0; m < M; ++m)
+                        args.y[static_cast<int64_t>(m) * args.N + ny] = __float2bfloat16_rn(acc[m]);
+            } else {
 #pragma unroll
-            for (int m = 0; m < kTok; ++m) red[m * kRows + row] = acc[m];
+                for (int m = 0; m < kTok; ++m) red[m * kRows + row] = acc[m];
+            }
         }
     }
 
     // Split-K partials: rank 0 of the cluster sums them in rank order.
     if (split > 1) {
         cluster_sync();
-        if (rank == 0 && decoder) {
+        if (rank == 0 && owner) {
             const int64_t ny = n0 + row;
             if (ny < args.N) {
                 for (int m = 0; m < M; ++m) {
@@ -339,12 +383,6 @@ cudaError_t launch_gemv_tmem(const void* x, int64_t M, int64_t N, int64_t K, con
     const int64_t G = K / 128;
     const int64_t row_blocks = (N + kRows - 1) / kRows;
     if (row_blocks > 0x7fffffffLL || K > 0x7fffffffLL || N > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    // Enough CTAs for two per SM, at most 8 per cluster, at least one group each.
-    int64_t split = (2 * static_cast<int64_t>(dev.sm_count) + row_blocks - 1) / row_blocks;
-    if (split > kMaxSplit) split = kMaxSplit;
-    if (split > G) split = G;
-    if (split < 1) split = 1;
-
     int device = 0;
     if (cudaError_t e = cudaGetDevice(&device)) return e;
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
@@ -357,6 +395,38 @@ cudaError_t launch_gemv_tmem(const void* x, int64_t M, int64_t N, int64_t K, con
             g_attr_set[device] = true;
         }
     }
+    // Split-K factor: the cluster size (1..8, at most G) that finishes the
+    // row blocks in the fewest rounds of group work, counting how many clusters
+    // of that size can be resident at once (one CTA per SM).
+    int64_t split = 1;
+    {
+        double best = 0.0;
+        for (int s = 1; s <= kMaxSplit && s <= G; ++s) {
+            cudaLaunchConfig_t q = {};
+            q.gridDim = dim3(static_cast<unsigned>(row_blocks), static_cast<unsigned>(s), 1);
+            q.blockDim = dim3(kThreads, 1, 1);
+            q.dynamicSmemBytes = kSmemBytes;
+            cudaLaunchAttribute qa[1];
+            qa[0].id = cudaLaunchAttributeClusterDimension;
+            qa[0].val.clusterDim.x = 1;
+            qa[0].val.clusterDim.y = static_cast<unsigned>(s);
+            qa[0].val.clusterDim.z = 1;
+            q.attrs = qa;
+            q.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, gemv_tmem_kernel, &q) != cudaSuccess || clusters < 1) {
+                cudaGetLastError();
+                continue;
+            }
+            const int64_t waves = (row_blocks + clusters - 1) / clusters;
+            const double cost = static_cast<double>(waves) * static_cast<double>((G + s - 1) / s);
+            if (best == 0.0 || cost < best) {
+                best = cost;
+                split = s;
+            }
+        }
+    }
+
     CUtensorMap tmap_codes;
     if (cudaError_t e = encode_codes_map(&tmap_codes, packed, N, K)) return e;
     const auto* xb = static_cast<const __nv_bfloat16*>(x);
