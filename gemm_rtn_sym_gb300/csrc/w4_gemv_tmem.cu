@@ -9,10 +9,10 @@
 // so every SM must decode about 45 weights per clock.  The decode itself (one
 // shift and one LOP3 per pair of weights) is the floor of the instruction
 // stream; everything else is moved off the SM's issue slots:
-//  * one thread streams, by TMA, each group's code tile (128 rows x 64 bytes,
-//    64-byte swizzle) into a 20-deep shared-memory ring (160 KB: at the loaded
-//    HBM latency every SM needs well over 100 KB in flight), another the
-//    group's activation tile into a 4-deep ring;
+//  * one thread streams, by TMA, code tiles of two groups (128 rows x 128
+//    bytes, 128-byte swizzle, 16 KB per copy) into an 8-deep shared-memory
+//    ring (128 KB: at the loaded HBM latency every SM needs well over 100 KB
+//    in flight), another thread the matching activation tiles;
 //  * 256 decoder threads, two per weight row, each read 32 bytes of their
 //    row (conflict-free thanks to the swizzle), turn the 64 nibbles into 32
 //    bf16x2 values 136 + q and write them with one tcgen05.st into tensor
@@ -50,13 +50,17 @@ constexpr int kTok = 16;            // token rows per pass = MMA N
 constexpr int kDecoderWarp0 = 3;
 constexpr int kDecoders = 256;
 constexpr int kThreads = 32 * kDecoderWarp0 + kDecoders;
-constexpr int kCodeSlots = 20;      // groups of codes in flight: 160 KB, most of shared memory
-constexpr int kXSlots = 4;          // activation groups (L2-resident) in flight
+// A TMA copy of only 8 KB per instruction caps one issuing thread well below
+// the HBM rate; 16 KB copies reach it.  So codes and activations move in
+// stages of two groups (256 k): one 16 KB code copy (128 rows x 128 bytes,
+// 128-byte swizzle) and one 8 KB activation copy per stage.
+constexpr int kCodeSlots = 8;       // stages of codes in flight: 128 KB, most of shared memory
+constexpr int kXSlots = 4;          // stages of activations (L2-resident) in flight
 constexpr int kASlots = 4;          // decoded groups in TMEM
 constexpr int kDBufs = 4;           // group accumulators in TMEM: read back kDBufs-1 groups behind
 constexpr int kMaxSplit = 8;
-constexpr int kCodeSlotBytes = kRows * 64;   // one group of 128 rows, 64-byte swizzle
-constexpr int kXSlotBytes = 2 * kTok * 128;  // two 64-k boxes of 16 rows x 128 bytes
+constexpr int kCodeSlotBytes = kRows * 128;      // two groups of 128 rows, 128-byte swizzle
+constexpr int kXSlotBytes = 4 * kTok * 128;      // four 64-k blocks of 16 rows x 128 bytes
 
 // Tensor memory columns (one CTA per SM: the whole 512-column TMEM).
 constexpr uint32_t kColD = 0;        // + 32·b: group accumulators (16 fp32 columns each)
@@ -142,11 +146,11 @@ gemv_tmem_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
     if (threadIdx.x == 0) {
         for (int c = 0; c < kCodeSlots; ++c) {
             mbar_init(code_full(c), 1);
-            mbar_init(code_empty(c), kDecoders);
+            mbar_init(code_empty(c), 2 * kDecoders);  // every decoder, once per group of the stage
         }
         for (int c = 0; c < kXSlots; ++c) {
             mbar_init(x_full(c), 1);
-            mbar_init(x_empty(c), 1);
+            mbar_init(x_empty(c), 2);  // one MMA commit per group of the stage
         }
         for (int s = 0; s < kASlots; ++s) {
             mbar_init(a_full(s), kDecoders);
@@ -186,44 +190,44 @@ gemv_tmem_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
     if (warp == 0) {
         // -------------------------------------------------- codes via TMA
         if (lane == 0) {
+            const int nt = (nj + 1) / 2;
             int issued = 0;
-            for (int j = 0; j < nj; ++j) {
-                const int c = j % kCodeSlots;
-                if (!mbar_wait(code_empty(c), (static_cast<uint32_t>(j / kCodeSlots) & 1u) ^ 1u)) {
+            for (int t = 0; t < nt; ++t) {
+                const int c = t % kCodeSlots;
+                if (!mbar_wait(code_empty(c), (static_cast<uint32_t>(t / kCodeSlots) & 1u) ^ 1u)) {
                     ok = false;
                     break;
                 }
                 mbar_arrive_expect_tx(code_full(c), kCodeSlotBytes);
-                tma_load_2d(code_base + c * kCodeSlotBytes, &tmap_codes, static_cast<int>((gs + j) * 64),
+                tma_load_2d(code_base + c * kCodeSlotBytes, &tmap_codes, static_cast<int>((gs + 2 * t) * 64),
                             static_cast<int>(n0), code_full(c));
-                issued = j + 1;
+                issued = t + 1;
             }
             if (!ok) {
                 record_status(args.status, kStatusTimeout);
-                for (int j = issued > kCodeSlots ? issued - kCodeSlots : 0; j < issued; ++j)
-                    mbar_wait(code_full(j % kCodeSlots), static_cast<uint32_t>(j / kCodeSlots) & 1u);
+                for (int t = issued > kCodeSlots ? issued - kCodeSlots : 0; t < issued; ++t)
+                    mbar_wait(code_full(t % kCodeSlots), static_cast<uint32_t>(t / kCodeSlots) & 1u);
             }
         }
     } else if (warp == 2) {
         // -------------------------------------------------- activations via TMA
         if (lane == 0) {
+            const int nt = (nj + 1) / 2;
             int issued = 0;
-            for (int j = 0; j < nj; ++j) {
-                const int c = j % kXSlots;
-                if (!mbar_wait(x_empty(c), (static_cast<uint32_t>(j / kXSlots) & 1u) ^ 1u)) {
+            for (int t = 0; t < nt; ++t) {
+                const int c = t % kXSlots;
+                if (!mbar_wait(x_empty(c), (static_cast<uint32_t>(t / kXSlots) & 1u) ^ 1u)) {
                     ok = false;
                     break;
                 }
                 mbar_arrive_expect_tx(x_full(c), kXSlotBytes);
-                const int k0 = static_cast<int>((gs + j) * 128);
-                tma_load_2d(x_base + c * kXSlotBytes, &tmap_x, k0, 0, x_full(c));
-                tma_load_2d(x_base + c * kXSlotBytes + kXSlotBytes / 2, &tmap_x, k0 + 64, 0, x_full(c));
-                issued = j + 1;
+                tma_load_3d(x_base + c * kXSlotBytes, &tmap_x, 0, 0, static_cast<int>((gs + 2 * t) * 2), x_full(c));
+                issued = t + 1;
             }
             if (!ok) {
                 record_status(args.status, kStatusTimeout);
-                for (int j = issued > kXSlots ? issued - kXSlots : 0; j < issued; ++j)
-                    mbar_wait(x_full(j % kXSlots), static_cast<uint32_t>(j / kXSlots) & 1u);
+                for (int t = issued > kXSlots ? issued - kXSlots : 0; t < issued; ++t)
+                    mbar_wait(x_full(t % kXSlots), static_cast<uint32_t>(t / kXSlots) & 1u);
             }
         }
     } else if (warp == 1) {
@@ -231,10 +235,11 @@ gemv_tmem_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16(kTok);
             for (int j = 0; j < nj; ++j) {
-                const int c = j % kXSlots;
+                const int t = j >> 1;
+                const int c = t % kXSlots;
                 const int s = j % kASlots;
                 const int b = j % kDBufs;
-                if (!mbar_wait(x_full(c), static_cast<uint32_t>(j / kXSlots) & 1u) ||
+                if (!mbar_wait(x_full(c), static_cast<uint32_t>(t / kXSlots) & 1u) ||
                     !mbar_wait(a_full(s), static_cast<uint32_t>(j / kASlots) & 1u) ||
                     (j >= kDBufs && !mbar_wait(d_empty(b), static_cast<uint32_t>(j / kDBufs - 1) & 1u))) {
                     ok = false;
@@ -243,10 +248,10 @@ gemv_tmem_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
                 tc_fence_after();
                 const uint32_t d = tmem + kColD + 32u * b;
                 const uint32_t a = tmem + kColA + 64u * s;
-                const uint32_t xs = x_base + c * kXSlotBytes;
+                const uint32_t xs = x_base + c * kXSlotBytes + (j & 1) * (kXSlotBytes / 2);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    const uint64_t bd = sw128_desc(xs + (ks >> 2) * (kXSlotBytes / 2) + (ks & 3) * 32);
+                    const uint64_t bd = sw128_desc(xs + (ks >> 2) * (kTok * 128) + (ks & 3) * 32);
                     mma_bf16_tmem_a(d, a + 8u * ks, bd, idesc, ks > 0 ? 1u : 0u);
                     mma_bf16_tmem_a(d, tmem + kColConst, bd, idesc, 1u);
                 }
@@ -283,13 +288,13 @@ gemv_tmem_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
             return true;
         };
 
-        // This thread's two 16-byte chunks (k half) of its row in a code slot
-        // (64-byte swizzle: chunk bits 4-5 XOR address bits 7-8).
-        const uint32_t row_off = static_cast<uint32_t>(row * 64);
-        const uint32_t sw = static_cast<uint32_t>((row >> 1) & 3);
-        const uint32_t ch0 = static_cast<uint32_t>(2 * half);
-        const uint32_t off0 = row_off + ((ch0 ^ sw) << 4);
-        const uint32_t off1 = row_off + (((ch0 + 1) ^ sw) << 4);
+        // This thread's two 16-byte chunks (its k half of one group) in a code
+        // stage: row pitch 128 bytes, 128-byte swizzle (chunk index XOR row % 8).
+        const uint32_t row_off = static_cast<uint32_t>(row * 128);
+        const uint32_t sw = static_cast<uint32_t>(row & 7);
+        auto chunk_off = [&](int sub, int i) {
+            return row_off + ((static_cast<uint32_t>(4 * sub + 2 * half + i) ^ sw) << 4);
+        };
 
         constexpr int kLag = kDBufs - 1;
         uint32_t d_hist[kLag + 1];  // scales of groups j-kLag .. j
@@ -297,7 +302,7 @@ gemv_tmem_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
         for (int i = 0; i <= kLag; ++i) d_hist[i] = 0;
         uint32_t d_next = (owner && nj > 0) ? __ldg(srow) : 0u;
         for (int j = 0; j < nj && ok; ++j) {
-            const int c = j % kCodeSlots;
+            const int c = (j >> 1) % kCodeSlots;
             const int s = j % kASlots;
             if (owner) {
 #pragma unroll
@@ -305,11 +310,11 @@ gemv_tmem_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
                 d_hist[kLag] = d_next;
                 if (j + 1 < nj) d_next = __ldg(srow + j + 1);
             }
-            const bool have = mbar_wait(code_full(c), static_cast<uint32_t>(j / kCodeSlots) & 1u);
+            const bool have = mbar_wait(code_full(c), static_cast<uint32_t>((j >> 1) / kCodeSlots) & 1u);
             if (!__all_sync(0xffffffffu, have)) { ok = false; break; }
             const uint32_t slot = code_base + c * kCodeSlotBytes;
-            const uint4 q0 = lds128(slot + off0);
-            const uint4 q1 = lds128(slot + off1);
+            const uint4 q0 = lds128(slot + chunk_off(j & 1, 0));
+            const uint4 q1 = lds128(slot + chunk_off(j & 1, 1));
             mbar_arrive(code_empty(c));
 
             const bool free_a = mbar_wait(a_empty(s), (static_cast<uint32_t>(j / kASlots) & 1u) ^ 1u);
@@ -429,12 +434,15 @@ cudaError_t launch_gemv_tmem(const void* x, int64_t M, int64_t N, int64_t K, con
 
     CUtensorMap tmap_codes;
     if (cudaError_t e = encode_codes_map(&tmap_codes, packed, N, K)) return e;
+    // With an odd group count the last stage of a range reaches one group past
+    // it; that copy reads valid memory (or the zero fill past K) and is never
+    // consumed.
     const auto* xb = static_cast<const __nv_bfloat16*>(x);
     auto* yb = static_cast<__nv_bfloat16*>(y);
     for (int64_t m0 = 0; m0 < M; m0 += kTok) {
         const int mp = static_cast<int>(M - m0 < kTok ? M - m0 : kTok);
         CUtensorMap tmap_x;
-        if (cudaError_t e = encode_x_map(&tmap_x, xb + m0 * K, mp, K, kTok)) return e;
+        if (cudaError_t e = encode_x_stage_map(&tmap_x, xb + m0 * K, mp, K)) return e;
         TmemArgs args;
         args.scales = static_cast<const uint16_t*>(scales);
         args.y = yb + m0 * N;

@@ -40,9 +40,13 @@ cudaError_t launch_gemv_tmem(const void* x, int64_t M, int64_t N, int64_t K, con
 // swizzle, rows past M read as zeros.
 cudaError_t encode_x_map(CUtensorMap* map, const void* x, int64_t M, int64_t K, int box_rows);
 
-// 2-D tensor map over packed codes u8 [N, K/2]: boxes of one group (64 bytes)
-// x 128 rows, 64-byte swizzle, rows past N read as zeros.
+// 2-D tensor map over packed codes u8 [N, K/2]: boxes of two groups (128
+// bytes) x 128 rows, 128-byte swizzle, rows past N read as zeros.
 cudaError_t encode_codes_map(CUtensorMap* map, const void* packed, int64_t N, int64_t K);
+
+// 3-D tensor map over x bf16 [M, K] seen as [K/64][M][64]: boxes of four 64-k
+// blocks x 16 rows, 128-byte swizzle, rows past M read as zeros.
+cudaError_t encode_x_stage_map(CUtensorMap* map, const void* x, int64_t M, int64_t K);
 
 cudaError_t launch_wait_probe(int64_t spin_limit, int arrive, const DeviceInfo& dev,
                               cudaStream_t stream);
