@@ -46,29 +46,33 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
         : "memory");
 }
 
-// try_wait may suspend the thread until the phase completes or the hint (ns)
-// runs out, so waiting threads do not spin on the issue slots.
+// Non-blocking test of the phase with the given parity.
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
-        : "r"(bar), "r"(parity), "r"(200000u)
+        : "r"(bar), "r"(parity)
         : "memory");
     return done != 0;
 }
 
 // Waits for the phase with the given parity to complete, for at most
-// `limit_ns` nanoseconds of wall time.  Returns false when it gave up.
+// `limit_ns` nanoseconds of wall time; returns false when it gave up.  The
+// thread polls with a short sleep between tests: suspending in try_wait until
+// the phase completes was measured to wake far too late for a pipeline whose
+// stages last well under a microsecond, and a bare spin takes issue slots
+// from the warps doing the work.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = global_ns();
-    while (!mbar_test(bar, parity)) {
-        if (global_ns() - t0 > limit_ns) return false;
+    for (uint32_t i = 1;; ++i) {
+        __nanosleep(20);
+        if (mbar_test(bar, parity)) return true;
+        if ((i & 63u) == 0 && global_ns() - t0 > limit_ns) return false;
     }
-    return true;
 }
 
 // ------------------------------------------------------------------ loads
