@@ -290,12 +290,27 @@ cudaError_t encode_codes_map(CUtensorMap* map, const void* packed, int64_t N, in
     return cudaSuccess;
 }
 
-cudaError_t encode_x_stage_map(CUtensorMap* map, const void* x, int64_t M, int64_t K) {
+cudaError_t encode_codes_stage_map(CUtensorMap* map, const void* packed, int64_t N, int64_t K, int rows,
+                                   int groups) {
+    if (cudaError_t e = get_encoder()) return e;
+    // codes viewed as [G groups][N rows][64 bytes]: byte (b, n, g) at n*K/2 + g*64 + b.
+    const cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K / 128)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K / 2), 64u};
+    const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(rows), static_cast<cuuint32_t>(groups)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(packed), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    return cudaSuccess;
+}
+
+cudaError_t encode_x_stage_map(CUtensorMap* map, const void* x, int64_t M, int64_t K, int rows, int blocks) {
     if (cudaError_t e = get_encoder()) return e;
     // x viewed as [K/64 blocks][M rows][64 k]: element (k, m, b) at m*2K + b*128 + 2k bytes.
     const cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128u};
-    const cuuint32_t box[3] = {64u, 16u, 4u};
+    const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(rows), static_cast<cuuint32_t>(blocks)};
     const cuuint32_t estr[3] = {1, 1, 1};
     if (g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), dims, strides, box, estr,
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

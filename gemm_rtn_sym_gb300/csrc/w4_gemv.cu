@@ -5,27 +5,31 @@
 // §2 settings (4-bit weights, BF16 inputs).
 //
 // Design (HBM-bound at M ≤ 16):
-//  * One warp owns RT tiles of 16 output rows and a contiguous range of groups;
-//    the CTA's warps split the groups (split-K) and their fp32 partials are
-//    summed in shared memory in a fixed order, so results are deterministic.
-//  * Each lane copies one 16-byte chunk (32 codes) per row per group from HBM
-//    into a per-warp shared-memory ring with cp.async, `kDepth` groups ahead of
-//    use, so nothing in flight occupies registers and several CTAs fit per SM.  The stored nibble
-//    order makes every 32-bit word yield four bf16x2 pairs (136 + q) with one
-//    shift and one LOP3 each, with no shuffles.  The 136·Σx offset is removed
-//    exactly enough (fp32, products exact) by starting each group's
-//    accumulator at −136·Σx, which one extra MMA chain per group computes for
-//    all rows at once.
-//  * The activations of the same groups go into the same ring (only the M real
-//    token rows; lanes of padding tokens use zero fragments).  The row pitch
-//    and chunk order make the fragment loads conflict-free.
-//  * The products q·x go through the legacy tensor-core MMA (m16n8k16, bf16 in,
-//    fp32 accumulate) from registers: the 16 rows are the MMA's M, up to 8 tokens
-//    its N.  At 0.5 B per weight of HBM traffic the SM must consume about 45
-//    weights per clock; one fp32 FMA per weight and token plus the decode would
-//    exceed the SM's 128 lanes already at M ≈ 2, while the MMA retires 2048
-//    multiply-adds per instruction.  The tensor pipe is therefore used as an ALU
-//    offload here; the kernel stays bound by HBM.
+//  * A CTA owns 64 output rows (four 16-row tiles) and a range of groups.  One
+//    producer thread streams, by TMA, stages of four groups: a 16 KB code tile
+//    ([group][row][64 B], from a 3-D view of the packed matrix) and the
+//    matching activation tile (16-row boxes of 64-k blocks, 128-byte swizzle;
+//    token rows >= M read as zeros), into a 3-4 deep shared-memory ring.  Two
+//    CTAs share an SM, so two threads per SM keep the copies flowing.
+//  * Four consumer warps each take one group of every stage for all four row
+//    tiles, so the activation fragments are loaded once per group and reused
+//    for 64 rows; the warps' fp32 partials are summed in shared memory in a
+//    fixed order at the end.  Small matrices are split along K over the CTAs
+//    of a thread-block cluster, whose partials rank 0 adds through
+//    distributed shared memory in rank order: deterministic, no global scratch.
+//  * The stored nibble order makes every 32-bit word yield four bf16x2 pairs
+//    (136 + q) with one shift and one LOP3 each, with no shuffles; the
+//    136·Σx offset is removed by starting each group's accumulator at −136·Σx,
+//    which one extra MMA chain per group computes for all rows at once.
+//  * The products go through the legacy tensor-core MMA (m16n8k16, bf16 in,
+//    fp32 accumulate) from registers: the 16 rows are the MMA's M, up to 8
+//    tokens its N.  At 0.5 B per weight of HBM traffic each SM must consume
+//    about 45 weights per clock; one fp32 FMA per weight and token plus the
+//    decode would exceed the SM's lanes already at M ≈ 2.  The tcgen05 MMA is
+//    no help at this size: one 128 x N x 16 instruction costs at least about
+//    46 cycles for any N <= 64 (measured), i.e. at most ~44 weights per clock
+//    per SM before any other work.  The legacy MMA from registers is used as
+//    an ALU offload here; the kernel stays bound by HBM.
 //  * 136 + q is exact in bf16 and (136 + q)·x is exact in fp32, so each group's
 //    partial sum is an fp32 sum of exact products; it is then scaled by d in
 //    fp32.  Cancelling the offset costs about 2^-22·143·Σ|x| per group, three
@@ -39,17 +43,29 @@
 
 #include "w4_device.cuh"
 #include "w4_internal.h"
+#include "w4_tcgen05.cuh"
 
 namespace w4 {
 namespace {
 
-constexpr int kGemvMaxWarps = 8;
-constexpr int kXPitch = 272;    // bytes per staged token row of one group: 256 + 16 of padding
+constexpr int kTiles = 4;                // 16-row tiles per CTA (and per consumer warp)
+constexpr int kRowsCta = 16 * kTiles;    // 64 weight rows per CTA
+constexpr int kConsumers = 4;            // consumer warps; warp c takes group c of every stage
+constexpr int kStageGroups = kConsumers; // groups per stage
+constexpr int kThreads = 32 * (1 + kConsumers);
+constexpr int kMaxSplit = 8;
+constexpr int kCodeStageBytes = kStageGroups * kRowsCta * 64;  // 16 KB: [group][row][64 B]
 
-// Position of 16-byte chunk ch (0..15) of a staged x row.  With the 272-byte
-// pitch this places the eight chunks one load instruction phase reads (two
-// token rows x four quads) in eight different bank groups.
-__device__ __forceinline__ int x_phys_chunk(int ch) { return ch ^ ((ch >> 3) << 1); }
+template <int MT>
+struct Cfg {
+    static constexpr int kXRows = 8 * MT;                               // token rows staged
+    static constexpr int kXStageBytes = 2 * kStageGroups * kXRows * 128;  // [k-block][row][128 B]
+    static constexpr int kStages = MT == 1 ? 4 : 3;
+    static constexpr int kStageBytes = kCodeStageBytes + kXStageBytes;
+    // Two CTAs per SM, each with its own TMA producer (one issuing thread per
+    // SM does not reach the HBM rate with copies of this size).
+    static constexpr int kSmemBytes = kStages * kStageBytes + 2048;
+};
 
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                                uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -60,239 +76,284 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint3
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Right shifts by 4, 8 and 12 bits written as the high word of a product with
-// 2^28, 2^24, 2^20.  The multipliers live in constant memory, so they reach the
-// integer multiply-add unit (which shares the FMA pipe) instead of becoming
-// shifts on the ALU pipe, which the LOP3 decode already keeps busy.
-__constant__ uint32_t kShiftMul[4] = {0u, 1u << 28, 1u << 24, 1u << 20};
-
 // Pair i (0..3) of a stored code word as the bf16x2 value (136 + q_lo, 136 + q_hi):
 // one shift and one LOP3, no subtract.  The 136·Σx offset this adds to every
 // group sum is removed by starting the group's accumulator at −136·Σx.
 __device__ __forceinline__ uint32_t biased_pair(uint32_t word, int i) {
-    const uint32_t shifted = i == 0 ? word : __umulhi(word, kShiftMul[i]);
-    return (shifted & 0x000F000Fu) ^ 0x43084308u;
+    return ((word >> (4 * i)) & 0x000F000Fu) ^ 0x43084308u;
 }
 
 constexpr uint32_t kMinus136x2 = 0xC308C308u;  // bf16x2 (−136, −136)
 
-// Shared-memory ring of one warp, per stage (one group):
-//   [RT tiles][16 rows][64 bytes of codes]   then   [m_real token rows][272 bytes of x]
-// Codes: lane (gid, tig) reads 16 bytes at row gid and row gid+8, chunk tig; one
-// load phase covers two rows x 64 contiguous bytes, so reads are conflict-free.
-template <int RT>
-__host__ __device__ constexpr int w_stage_bytes() { return RT * 16 * 64; }
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
 
-// MT: token tiles of 8 (1: M <= 8, 2: M <= 16).  RT: 16-row tiles per warp.
-// kDepth: groups in flight per warp.  MINB: CTAs per SM the register allocation
-// must allow.
-template <int MT, int RT, int kDepth, int MINB>
-__global__ void __launch_bounds__(32 * kGemvMaxWarps, MINB)
-gemv_w4_kernel(const __nv_bfloat16* __restrict__ x, int M, int64_t N, int64_t K,
-               const uint8_t* __restrict__ packed, const __nv_bfloat16* __restrict__ scales,
-               __nv_bfloat16* __restrict__ y) {
-    extern __shared__ __align__(16) uint8_t ring_raw[];
-    __shared__ float red[kGemvMaxWarps][RT][MT][4][32];
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                     "memory");
+}
 
-    const int lane = threadIdx.x & 31;
+__device__ __forceinline__ float ld_cluster_f32(uint32_t local_addr, uint32_t rank) {
+    uint32_t remote;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+struct GemvArgs {
+    const uint16_t* scales;
+    __nv_bfloat16* y;
+    int M;  // token rows of this pass, 1..16
+    int64_t N, K;
+    int split;
+    unsigned* status;
+};
+
+// MT: token tiles of 8 (1: M <= 8, 2: M <= 16).
+template <int MT>
+__global__ void __launch_bounds__(kThreads, 2)
+gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_constant__ CUtensorMap tmap_x,
+               const GemvArgs args) {
+    using C = Cfg<MT>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const uint32_t bar_base = base + C::kStages * C::kStageBytes;
+    auto full = [&](int s) { return bar_base + 8u * s; };
+    auto empty = [&](int s) { return bar_base + 8u * (C::kStages + s); };
+
     const int warp = threadIdx.x >> 5;
-    const int n_warps = blockDim.x >> 5;
+    const int lane = threadIdx.x & 31;
     const int gid = lane >> 2;
     const int tig = lane & 3;
-    const int64_t G = K >> 7;
-    const int64_t half_k = K >> 1;
-    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * 16 * RT;
-    const int m_real = M < MT * 8 ? M : MT * 8;
+    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kRowsCta;
+    const int64_t G = args.K >> 7;
+    const int split = args.split;
+    const uint32_t rank = split > 1 ? cluster_rank() : 0u;
+    const int64_t gs = (static_cast<int64_t>(rank) * G) / split;
+    const int64_t ge = (static_cast<int64_t>(rank + 1) * G) / split;
+    const int ng = static_cast<int>(ge - gs);
+    const int nt = (ng + kStageGroups - 1) / kStageGroups;
+    const int M = args.M;
 
-    const int64_t g0 = (warp * G) / n_warps;
-    const int64_t g1 = ((warp + 1) * G) / n_warps;
-    const int ng = static_cast<int>(g1 - g0);
-
-    const int stage = w_stage_bytes<RT>() + m_real * kXPitch;
-    const uint32_t wbase = smem_addr(ring_raw) + static_cast<uint32_t>(warp * kDepth * stage);
-    const uint32_t xoff = w_stage_bytes<RT>();
-
-    // Rows past N are clamped to row N-1 (valid memory); their outputs are dropped.
-    const uint8_t* pa[RT];
-    const uint8_t* pb[RT];
-    const uint16_t* sa[RT];
-    const uint16_t* sb[RT];
-#pragma unroll
-    for (int rt = 0; rt < RT; ++rt) {
-        int64_t na = n0 + rt * 16 + gid, nb = na + 8;
-        na = na < N ? na : N - 1;
-        nb = nb < N ? nb : N - 1;
-        pa[rt] = packed + na * half_k + (g0 * 64 + tig * 16);
-        pb[rt] = packed + nb * half_k + (g0 * 64 + tig * 16);
-        sa[rt] = reinterpret_cast<const uint16_t*>(scales) + na * G + g0;
-        sb[rt] = reinterpret_cast<const uint16_t*>(scales) + nb * G + g0;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 32 * kConsumers);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_async_smem();
     }
-    const __nv_bfloat16* xg = x + g0 * 128;
+    __syncthreads();
 
-    // Stage group gi of this warp's range into ring slot `slot`.
-    auto issue = [&](int slot, int gi) {
-        const uint32_t st = wbase + slot * stage;
+    bool ok = true;
+    float acc[kTiles][MT][4];
 #pragma unroll
-        for (int rt = 0; rt < RT; ++rt) {
-            cp_async16(st + (rt * 16 + gid) * 64 + tig * 16, pa[rt] + gi * 64);
-            cp_async16(st + (rt * 16 + gid + 8) * 64 + tig * 16, pb[rt] + gi * 64);
-        }
-        for (int q = lane; q < m_real * 16; q += 32) {
-            const int r = q >> 4, ch = q & 15;
-            cp_async16(st + xoff + r * kXPitch + x_phys_chunk(ch) * 16,
-                       xg + static_cast<int64_t>(r) * K + gi * 128 + ch * 8);
-        }
-    };
-
-    float acc[RT][MT][4];
-#pragma unroll
-    for (int rt = 0; rt < RT; ++rt)
+    for (int rt = 0; rt < kTiles; ++rt)
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int r = 0; r < 4; ++r) acc[rt][mt][r] = 0.0f;
 
-#pragma unroll
-    for (int i = 0; i < kDepth; ++i) {
-        if (i < ng) issue(i, i);
-        cp_async_commit();
-    }
-    // Scales one group ahead in registers.
-    uint32_t d_next[RT][2];
-#pragma unroll
-    for (int rt = 0; rt < RT; ++rt) {
-        d_next[rt][0] = ng > 0 ? __ldg(sa[rt]) : 0u;
-        d_next[rt][1] = ng > 0 ? __ldg(sb[rt]) : 0u;
-    }
-
-    for (int gi = 0; gi < ng; ++gi) {
-        const int slot = gi % kDepth;
-        const uint32_t st = wbase + slot * stage;
-        uint32_t d_cur[RT][2];
-#pragma unroll
-        for (int rt = 0; rt < RT; ++rt) {
-            d_cur[rt][0] = d_next[rt][0];
-            d_cur[rt][1] = d_next[rt][1];
-            if (gi + 1 < ng) {
-                d_next[rt][0] = __ldg(sa[rt] + gi + 1);
-                d_next[rt][1] = __ldg(sb[rt] + gi + 1);
-            }
-        }
-        cp_async_wait<kDepth - 1>();
-        __syncwarp();
-        uint4 wv[RT][2];
-#pragma unroll
-        for (int rt = 0; rt < RT; ++rt) {
-            wv[rt][0] = lds128(st + (rt * 16 + gid) * 64 + tig * 16);
-            wv[rt][1] = lds128(st + (rt * 16 + gid + 8) * 64 + tig * 16);
-        }
-        uint32_t xw[MT][16];
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-            const int row = mt * 8 + gid;
-            if (row < m_real) {
-                const uint32_t xr = st + xoff + row * kXPitch;
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const uint4 t = lds128(xr + x_phys_chunk(4 * tig + v) * 16);
-                    xw[mt][4 * v + 0] = t.x;
-                    xw[mt][4 * v + 1] = t.y;
-                    xw[mt][4 * v + 2] = t.z;
-                    xw[mt][4 * v + 3] = t.w;
+    if (warp == 0) {
+        // -------------------------------------------------- producer: one thread, two copies per stage
+        if (lane == 0) {
+            int issued = 0;
+            for (int t = 0; t < nt; ++t) {
+                const int s = t % C::kStages;
+                if (!mbar_wait(empty(s), (static_cast<uint32_t>(t / C::kStages) & 1u) ^ 1u)) {
+                    ok = false;
+                    break;
                 }
-            } else {
-#pragma unroll
-                for (int v = 0; v < 16; ++v) xw[mt][v] = 0u;
+                const uint32_t st = base + s * C::kStageBytes;
+                const int g = static_cast<int>(gs + t * kStageGroups);
+                mbar_arrive_expect_tx(full(s), C::kStageBytes);
+                tma_load_3d(st, &tmap_codes, 0, static_cast<int>(n0), g, full(s));
+                tma_load_3d(st + kCodeStageBytes, &tmap_x, 0, 0, 2 * g, full(s));
+                issued = t + 1;
+            }
+            if (!ok) {
+                record_status(args.status, kStatusTimeout);
+                for (int t = issued > C::kStages ? issued - C::kStages : 0; t < issued; ++t)
+                    mbar_wait(full(t % C::kStages), static_cast<uint32_t>(t / C::kStages) & 1u);
             }
         }
-        __syncwarp();
-        if (gi + kDepth < ng) issue(slot, gi + kDepth);
-        cp_async_commit();
+    } else {
+        // -------------------------------------------------- consumers: decode + legacy MMA
+        const int cw = warp - 1;  // this warp's group within every stage
+        // Scales of rows gid / gid+8 of each tile, for this warp's group of a stage.
+        const uint16_t* srow[kTiles][2];
+#pragma unroll
+        for (int rt = 0; rt < kTiles; ++rt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                int64_t n = n0 + rt * 16 + gid + 8 * h;
+                if (n >= args.N) n = args.N - 1;
+                srow[rt][h] = args.scales + n * G;
+            }
+        auto load_scales = [&](uint32_t (&d)[kTiles][2], int t) {
+            const int64_t g = gs + t * kStageGroups + cw;
+#pragma unroll
+            for (int rt = 0; rt < kTiles; ++rt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) d[rt][h] = (t < nt && g < ge) ? __ldg(srow[rt][h] + g) : 0u;
+        };
+        uint32_t d_cur[kTiles][2], d_nxt[kTiles][2];
+        load_scales(d_nxt, 0);
 
-        // −136·Σ_k x[m, k] over this group, identical for every row.
-        float corr[MT][4];
+        // Byte offsets inside a stage.
+        const uint32_t w_off = static_cast<uint32_t>(cw * kRowsCta * 64 + gid * 64 + tig * 16);
+        const uint32_t x_blk = static_cast<uint32_t>(kCodeStageBytes + (2 * cw + (tig >> 1)) * C::kXRows * 128);
+
+        for (int t = 0; t < nt; ++t) {
+            const int s = t % C::kStages;
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
+            for (int rt = 0; rt < kTiles; ++rt) {
+                d_cur[rt][0] = d_nxt[rt][0];
+                d_cur[rt][1] = d_nxt[rt][1];
+            }
+            load_scales(d_nxt, t + 1);
+            const bool have = mbar_wait(full(s), static_cast<uint32_t>(t / C::kStages) & 1u);
+            if (!__all_sync(0xffffffffu, have)) {
+                ok = false;
+                break;
+            }
+            const bool active = gs + t * kStageGroups + cw < ge;  // warp-uniform
+            const uint32_t st = base + s * C::kStageBytes;
+            uint32_t xw[MT][16];
+            uint4 wv[kTiles][2];
+            if (active) {
 #pragma unroll
-            for (int r = 0; r < 4; ++r) corr[mt][r] = 0.0f;
+                for (int mt = 0; mt < MT; ++mt) {
+                    const int r = mt * 8 + gid;
+                    const uint32_t rowa = st + x_blk + r * 128;
 #pragma unroll
-            for (int s = 0; s < 8; ++s)
-                mma_bf16_16816(corr[mt], kMinus136x2, kMinus136x2, kMinus136x2, kMinus136x2,
-                               xw[mt][2 * s], xw[mt][2 * s + 1]);
+                    for (int v = 0; v < 4; ++v) {
+                        const uint32_t c = static_cast<uint32_t>(4 * (tig & 1) + v);
+                        const uint4 q = lds128(rowa + ((c ^ static_cast<uint32_t>(r & 7)) << 4));
+                        xw[mt][4 * v + 0] = q.x;
+                        xw[mt][4 * v + 1] = q.y;
+                        xw[mt][4 * v + 2] = q.z;
+                        xw[mt][4 * v + 3] = q.w;
+                    }
+                }
+#pragma unroll
+                for (int rt = 0; rt < kTiles; ++rt) {
+                    wv[rt][0] = lds128(st + w_off + rt * 16 * 64);
+                    wv[rt][1] = lds128(st + w_off + rt * 16 * 64 + 8 * 64);
+                }
+            }
+            mbar_arrive(empty(s));
+            if (!active) continue;
+
+            // −136·Σ_k x[m, k] over this group, identical for every row.
+            float corr[MT][4];
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) corr[mt][r] = 0.0f;
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mma_bf16_16816(corr[mt], kMinus136x2, kMinus136x2, kMinus136x2, kMinus136x2,
+                                   xw[mt][2 * k], xw[mt][2 * k + 1]);
+            }
+#pragma unroll
+            for (int rt = 0; rt < kTiles; ++rt) {
+                float cg[MT][4];
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) cg[mt][r] = corr[mt][r];
+                const uint32_t wa[4] = {wv[rt][0].x, wv[rt][0].y, wv[rt][0].z, wv[rt][0].w};
+                const uint32_t wb[4] = {wv[rt][1].x, wv[rt][1].y, wv[rt][1].z, wv[rt][1].w};
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int w = k >> 1;
+                    const int h = k & 1;
+                    const uint32_t a0 = biased_pair(wa[w], 2 * h);
+                    const uint32_t a2 = biased_pair(wa[w], 2 * h + 1);
+                    const uint32_t a1 = biased_pair(wb[w], 2 * h);
+                    const uint32_t a3 = biased_pair(wb[w], 2 * h + 1);
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt)
+                        mma_bf16_16816(cg[mt], a0, a1, a2, a3, xw[mt][2 * k], xw[mt][2 * k + 1]);
+                }
+                const float da = bf16_lo(d_cur[rt][0]);
+                const float db = bf16_lo(d_cur[rt][1]);
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    acc[rt][mt][0] = fmaf(da, cg[mt][0], acc[rt][mt][0]);
+                    acc[rt][mt][1] = fmaf(da, cg[mt][1], acc[rt][mt][1]);
+                    acc[rt][mt][2] = fmaf(db, cg[mt][2], acc[rt][mt][2]);
+                    acc[rt][mt][3] = fmaf(db, cg[mt][3], acc[rt][mt][3]);
+                }
+            }
         }
+        if (!ok) record_status(args.status, kStatusTimeout);
+    }
+
+    // ------------------------------------------------------ reduction
+    // Every stage was consumed, so the stage memory is free: partials of the
+    // consumer warps go there as red[warp][tile][mt][r][lane], then the CTA's
+    // sum as part[m][row].
+    __syncthreads();
+    float* red = reinterpret_cast<float*>(gbase);
+    float* part = red + kConsumers * kTiles * MT * 4 * 32;
+    if (warp >= 1) {
 #pragma unroll
-        for (int rt = 0; rt < RT; ++rt) {
-            // Two independent MMA chains (even and odd k-steps) per tile.
-            float ce[MT][4], co[MT][4];
+        for (int rt = 0; rt < kTiles; ++rt)
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    ce[mt][r] = corr[mt][r];
-                    co[mt][r] = 0.0f;
-                }
-            const uint32_t wa[4] = {wv[rt][0].x, wv[rt][0].y, wv[rt][0].z, wv[rt][0].w};
-            const uint32_t wb[4] = {wv[rt][1].x, wv[rt][1].y, wv[rt][1].z, wv[rt][1].w};
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const int w = s >> 1;
-                const int h = s & 1;
-                const uint32_t a0 = biased_pair(wa[w], 2 * h);
-                const uint32_t a2 = biased_pair(wa[w], 2 * h + 1);
-                const uint32_t a1 = biased_pair(wb[w], 2 * h);
-                const uint32_t a3 = biased_pair(wb[w], 2 * h + 1);
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    if (h == 0)
-                        mma_bf16_16816(ce[mt], a0, a1, a2, a3, xw[mt][2 * s], xw[mt][2 * s + 1]);
-                    else
-                        mma_bf16_16816(co[mt], a0, a1, a2, a3, xw[mt][2 * s], xw[mt][2 * s + 1]);
-                }
-            }
-            const float da = bf16_lo(d_cur[rt][0]);
-            const float db = bf16_lo(d_cur[rt][1]);
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                acc[rt][mt][0] = fmaf(da, ce[mt][0] + co[mt][0], acc[rt][mt][0]);
-                acc[rt][mt][1] = fmaf(da, ce[mt][1] + co[mt][1], acc[rt][mt][1]);
-                acc[rt][mt][2] = fmaf(db, ce[mt][2] + co[mt][2], acc[rt][mt][2]);
-                acc[rt][mt][3] = fmaf(db, ce[mt][3] + co[mt][3], acc[rt][mt][3]);
-            }
+                for (int r = 0; r < 4; ++r)
+                    red[((((warp - 1) * kTiles + rt) * MT + mt) * 4 + r) * 32 + lane] = acc[rt][mt][r];
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < kTiles * MT * 4 * 32; e += kThreads) {
+        const int l = e & 31;
+        const int r = (e >> 5) & 3;
+        const int mt = (e >> 7) % MT;
+        const int rt = e / (MT * 128);
+        float v = 0.0f;
+        for (int w = 0; w < kConsumers; ++w) v += red[(((w * kTiles + rt) * MT + mt) * 4 + r) * 32 + l];
+        const int rowc = rt * 16 + (l >> 2) + (r >= 2 ? 8 : 0);
+        const int m = mt * 8 + 2 * (l & 3) + (r & 1);
+        if (split == 1) {
+            const int64_t n = n0 + rowc;
+            if (n < args.N && m < M) args.y[static_cast<int64_t>(m) * args.N + n] = __float2bfloat16_rn(v);
+        } else {
+            part[m * kRowsCta + rowc] = v;
         }
     }
-    cp_async_wait<0>();
-
-#pragma unroll
-    for (int rt = 0; rt < RT; ++rt)
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) red[warp][rt][mt][r][lane] = acc[rt][mt][r];
-    __syncthreads();
-
-    for (int e = threadIdx.x; e < RT * MT * 4 * 32; e += blockDim.x) {
-        const int rt = e / (MT * 128);
-        const int mt = (e / 128) % MT;
-        const int r = (e / 32) & 3;
-        const int l = e & 31;
-        float v = 0.0f;
-        for (int w = 0; w < n_warps; ++w) v += red[w][rt][mt][r][l];
-        const int64_t n = n0 + rt * 16 + (l >> 2) + (r >= 2 ? 8 : 0);
-        const int m = mt * 8 + 2 * (l & 3) + (r & 1);
-        if (n < N && m < M) y[static_cast<int64_t>(m) * N + n] = __float2bfloat16_rn(v);
+    if (split > 1) {
+        // Split-K partials: rank 0 of the cluster sums them in rank order.
+        cluster_sync();
+        if (rank == 0) {
+            const uint32_t part_addr = smem_addr(part);
+            for (int e = threadIdx.x; e < kRowsCta * M; e += kThreads) {
+                const int rowc = e % kRowsCta, m = e / kRowsCta;
+                const int64_t n = n0 + rowc;
+                float v = 0.0f;
+                for (int r = 0; r < split; ++r)
+                    v += ld_cluster_f32(part_addr + static_cast<uint32_t>((m * kRowsCta + rowc) * 4), static_cast<uint32_t>(r));
+                if (n < args.N) args.y[static_cast<int64_t>(m) * args.N + n] = __float2bfloat16_rn(v);
+            }
+        }
+        cluster_sync();
     }
-}
-
-template <int MT, int RT, int kDepth>
-int gemv_smem_bytes(int warps, int m_real) {
-    return warps * kDepth * (w_stage_bytes<RT>() + m_real * kXPitch);
 }
 
 std::mutex g_attr_mutex;
 
-template <int MT, int RT, int kDepth, int MINB>
-cudaError_t launch_one(const __nv_bfloat16* x, int mp, int64_t N, int64_t K, const uint8_t* packed,
-                       const __nv_bfloat16* scales, __nv_bfloat16* y, int warps, cudaStream_t stream) {
+template <int MT>
+cudaError_t launch_mt(const __nv_bfloat16* x, int mp, int64_t N, int64_t K, const CUtensorMap& tmap_codes,
+                      const uint16_t* scales, __nv_bfloat16* y, const DeviceInfo& dev, cudaStream_t stream) {
+    using C = Cfg<MT>;
     static bool attr_set[64];
     int device = 0;
     if (cudaError_t e = cudaGetDevice(&device)) return e;
@@ -300,44 +361,85 @@ cudaError_t launch_one(const __nv_bfloat16* x, int mp, int64_t N, int64_t K, con
     {
         std::lock_guard<std::mutex> lock(g_attr_mutex);
         if (!attr_set[device]) {
-            if (cudaError_t e = cudaFuncSetAttribute(gemv_w4_kernel<MT, RT, kDepth, MINB>,
-                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     gemv_smem_bytes<MT, RT, kDepth>(kGemvMaxWarps, MT * 8)))
+            if (cudaError_t e = cudaFuncSetAttribute(gemv_w4_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     C::kSmemBytes))
                 return e;
             attr_set[device] = true;
         }
     }
-    const int64_t blocks = (N + 16 * RT - 1) / (16 * RT);
-    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    const int m_real = mp < MT * 8 ? mp : MT * 8;
-    gemv_w4_kernel<MT, RT, kDepth, MINB><<<static_cast<unsigned>(blocks), 32 * warps,
-                                           gemv_smem_bytes<MT, RT, kDepth>(warps, m_real), stream>>>(
-        x, mp, N, K, packed, scales, y);
-    return cudaGetLastError();
+    const int64_t G = K / 128;
+    const int64_t row_blocks = (N + kRowsCta - 1) / kRowsCta;
+    if (row_blocks > 0x7fffffffLL || K > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+
+    // Split-K factor: the cluster size (1..8, at most G) that finishes the row
+    // blocks in the fewest rounds of stage work, given how many clusters of
+    // that size can be resident at once.
+    int64_t split = 1;
+    double best = 0.0;
+    for (int s = 1; s <= kMaxSplit && s <= G; ++s) {
+        cudaLaunchConfig_t q = {};
+        q.gridDim = dim3(static_cast<unsigned>(row_blocks), static_cast<unsigned>(s), 1);
+        q.blockDim = dim3(kThreads, 1, 1);
+        q.dynamicSmemBytes = C::kSmemBytes;
+        cudaLaunchAttribute qa[1];
+        qa[0].id = cudaLaunchAttributeClusterDimension;
+        qa[0].val.clusterDim.x = 1;
+        qa[0].val.clusterDim.y = static_cast<unsigned>(s);
+        qa[0].val.clusterDim.z = 1;
+        q.attrs = qa;
+        q.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, gemv_w4_kernel<MT>, &q) != cudaSuccess || clusters < 1) {
+            cudaGetLastError();
+            continue;
+        }
+        const int64_t waves = (row_blocks + clusters - 1) / clusters;
+        const int64_t stages = ((G + s - 1) / s + kStageGroups - 1) / kStageGroups;
+        const double cost = static_cast<double>(waves) * static_cast<double>(stages);
+        if (best == 0.0 || cost < best) {
+            best = cost;
+            split = s;
+        }
+    }
+
+    CUtensorMap tmap_x;
+    if (cudaError_t e = encode_x_stage_map(&tmap_x, x, mp, K, C::kXRows, 2 * kStageGroups)) return e;
+    GemvArgs args;
+    args.scales = scales;
+    args.y = y;
+    args.M = mp;
+    args.N = N;
+    args.K = K;
+    args.split = static_cast<int>(split);
+    args.status = dev.status;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(row_blocks), static_cast<unsigned>(split), 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = static_cast<unsigned>(split);
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemv_w4_kernel<MT>, tmap_codes, tmap_x, args);
 }
 
 }  // namespace
 
 cudaError_t launch_gemv(const void* x, int64_t M, int64_t N, int64_t K, const void* packed,
                         const void* scales, void* y, const DeviceInfo& dev, cudaStream_t stream) {
-    const int64_t G = K / 128;
-    const int warps = static_cast<int>(G < kGemvMaxWarps ? G : kGemvMaxWarps);
-    // Two row tiles per warp halve the x traffic per weight when there are
-    // still at least two CTAs per SM.
-    const bool two_tiles = (N + 31) / 32 >= 2 * static_cast<int64_t>(dev.sm_count);
+    CUtensorMap tmap_codes;
+    if (cudaError_t e = encode_codes_stage_map(&tmap_codes, packed, N, K, kRowsCta, kStageGroups)) return e;
     const auto* xb = static_cast<const __nv_bfloat16*>(x);
-    const auto* pk = static_cast<const uint8_t*>(packed);
-    const auto* sc = static_cast<const __nv_bfloat16*>(scales);
+    const auto* sc = static_cast<const uint16_t*>(scales);
     auto* yb = static_cast<__nv_bfloat16*>(y);
     for (int64_t m0 = 0; m0 < M; m0 += 16) {
         const int mp = static_cast<int>(M - m0 < 16 ? M - m0 : 16);
-        cudaError_t e;
-        if (mp <= 8)
-            e = two_tiles ? launch_one<1, 2, 4, 1>(xb + m0 * K, mp, N, K, pk, sc, yb + m0 * N, warps, stream)
-                          : launch_one<1, 1, 4, 1>(xb + m0 * K, mp, N, K, pk, sc, yb + m0 * N, warps, stream);
-        else
-            e = two_tiles ? launch_one<2, 2, 4, 1>(xb + m0 * K, mp, N, K, pk, sc, yb + m0 * N, warps, stream)
-                          : launch_one<2, 1, 4, 1>(xb + m0 * K, mp, N, K, pk, sc, yb + m0 * N, warps, stream);
+        const cudaError_t e = mp <= 8 ? launch_mt<1>(xb + m0 * K, mp, N, K, tmap_codes, sc, yb + m0 * N, dev, stream)
+                                      : launch_mt<2>(xb + m0 * K, mp, N, K, tmap_codes, sc, yb + m0 * N, dev, stream);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -442,7 +442,7 @@ cudaError_t launch_gemv_tmem(const void* x, int64_t M, int64_t N, int64_t K, con
     for (int64_t m0 = 0; m0 < M; m0 += kTok) {
         const int mp = static_cast<int>(M - m0 < kTok ? M - m0 : kTok);
         CUtensorMap tmap_x;
-        if (cudaError_t e = encode_x_stage_map(&tmap_x, xb + m0 * K, mp, K)) return e;
+        if (cudaError_t e = encode_x_stage_map(&tmap_x, xb + m0 * K, mp, K, kTok, 4)) return e;
         TmemArgs args;
         args.scales = static_cast<const uint16_t*>(scales);
         args.y = yb + m0 * N;
