@@ -19,13 +19,12 @@ __all__ = [
     "load", "library_path", "W4Error",
     "w4_quantize_rtn", "w4_gemm", "w4_gemm_ex", "w4_gemm_path_for",
     "w4_packed_bytes", "w4_scales_bytes", "w4_last_device_status", "w4_wait_probe",
-    "w4_status_string", "W4_PATH_AUTO", "W4_PATH_SMALL_M", "W4_PATH_TENSOR", "W4_PATH_SMALL_M_TMEM",
-    "GROUP",
+    "w4_status_string", "W4_PATH_AUTO", "W4_PATH_SMALL_M", "W4_PATH_TENSOR", "GROUP",
 ]
 
 GROUP = 128
 W4_OK, W4_ERR_INVALID_ARG, W4_ERR_UNSUPPORTED, W4_ERR_MISALIGNED, W4_ERR_CUDA, W4_ERR_TIMEOUT = range(6)
-W4_PATH_AUTO, W4_PATH_SMALL_M, W4_PATH_TENSOR, W4_PATH_SMALL_M_TMEM = 0, 1, 2, 3
+W4_PATH_AUTO, W4_PATH_SMALL_M, W4_PATH_TENSOR = 0, 1, 2
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _lib = None

@@ -112,7 +112,7 @@ int w4_gemm_ex(const void* x, int64_t M, int64_t N, int64_t K, const void* packe
     if (const int s = check_sizes(N, K)) return s;
     if (M > 0 && K > (int64_t{1} << 62) / M) return W4_ERR_INVALID_ARG;
     if (M > 0 && N > (int64_t{1} << 62) / M) return W4_ERR_INVALID_ARG;
-    if (path < W4_PATH_AUTO || path > W4_PATH_SMALL_M_TMEM) return W4_ERR_INVALID_ARG;
+    if (path < W4_PATH_AUTO || path > W4_PATH_TENSOR) return W4_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return W4_OK;
     if (!y) return W4_ERR_INVALID_ARG;
     if (!aligned(y, 2)) return W4_ERR_MISALIGNED;
@@ -132,8 +132,6 @@ int w4_gemm_ex(const void* x, int64_t M, int64_t N, int64_t K, const void* packe
     if (path == W4_PATH_AUTO) path = M >= kTensorMinM ? W4_PATH_TENSOR : W4_PATH_SMALL_M;
     if (path == W4_PATH_TENSOR)
         return to_status(launch_gemm_tc(x, M, N, K, packed, scales, y, *dev, st));
-    if (path == W4_PATH_SMALL_M_TMEM)
-        return to_status(launch_gemv_tmem(x, M, N, K, packed, scales, y, *dev, st));
     return to_status(launch_gemv(x, M, N, K, packed, scales, y, *dev, st));
 }
 

@@ -277,19 +277,6 @@ cudaError_t encode_x_map(CUtensorMap* map, const void* x, int64_t M, int64_t K, 
     return cudaSuccess;
 }
 
-cudaError_t encode_codes_map(CUtensorMap* map, const void* packed, int64_t N, int64_t K) {
-    if (cudaError_t e = get_encoder()) return e;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(N)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
-    const cuuint32_t box[2] = {128u, 128u};
-    const cuuint32_t estr[2] = {1, 1};
-    if (g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(packed), dims, strides, box, estr,
-                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
-    return cudaSuccess;
-}
-
 cudaError_t encode_codes_stage_map(CUtensorMap* map, const void* packed, int64_t N, int64_t K, int rows,
                                    int groups) {
     if (cudaError_t e = get_encoder()) return e;

@@ -23,7 +23,7 @@ const DeviceInfo* device_info(cudaError_t* err);
 cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, void* packed, void* scales,
                             const DeviceInfo& dev, cudaStream_t stream);
 
-// Small-M path: any M; it runs one pass per 16 token rows.
+// Small-M path (TMA-fed GEMV on the legacy MMA): any M, one pass per 16 token rows.
 cudaError_t launch_gemv(const void* x, int64_t M, int64_t N, int64_t K, const void* packed,
                         const void* scales, void* y, const DeviceInfo& dev, cudaStream_t stream);
 
@@ -31,18 +31,9 @@ cudaError_t launch_gemv(const void* x, int64_t M, int64_t N, int64_t K, const vo
 cudaError_t launch_gemm_tc(const void* x, int64_t M, int64_t N, int64_t K, const void* packed,
                            const void* scales, void* y, const DeviceInfo& dev, cudaStream_t stream);
 
-// Small-M path on the tensor cores: dequantised weights written to TMEM as the
-// MMA's A operand, M <= 16 per pass.
-cudaError_t launch_gemv_tmem(const void* x, int64_t M, int64_t N, int64_t K, const void* packed,
-                             const void* scales, void* y, const DeviceInfo& dev, cudaStream_t stream);
-
 // 2-D tensor map over x bf16 [M, K]: boxes of 64 k x box_rows rows, 128-byte
 // swizzle, rows past M read as zeros.
 cudaError_t encode_x_map(CUtensorMap* map, const void* x, int64_t M, int64_t K, int box_rows);
-
-// 2-D tensor map over packed codes u8 [N, K/2]: boxes of two groups (128
-// bytes) x 128 rows, 128-byte swizzle, rows past N read as zeros.
-cudaError_t encode_codes_map(CUtensorMap* map, const void* packed, int64_t N, int64_t K);
 
 // 3-D tensor map over x bf16 [M, K] seen as [K/64][M][64]: boxes of `blocks`
 // 64-k blocks x `rows` rows, 128-byte swizzle, rows past M read as zeros.

@@ -74,12 +74,10 @@ typedef enum w4_status {
 /* Kernel choice for w4_gemm_ex. */
 typedef enum w4_gemm_path {
     W4_PATH_AUTO = 0,    /* what w4_gemm does: picked from M (w4_gemm_path_for)  */
-    W4_PATH_SMALL_M = 1, /* register-dequant split-K GEMV on the legacy MMA,
-                            any M (16 per pass)                                 */
-    W4_PATH_TENSOR = 2,  /* tcgen05 tile, weights dequantised into shared
-                            memory, TMEM accumulators, any M ≥ 1                */
-    W4_PATH_SMALL_M_TMEM = 3 /* tcgen05 GEMV, weights decoded into TMEM as the
-                            MMA's A operand, cluster split-K, any M (16 per pass) */
+    W4_PATH_SMALL_M = 1, /* TMA-fed GEMV: register nibble decode, legacy MMA,
+                            cluster split-K; any M (16 token rows per pass)     */
+    W4_PATH_TENSOR = 2   /* tcgen05 tile: weights dequantised into shared
+                            memory, TMEM accumulators; any M ≥ 1                */
 } w4_gemm_path;
 
 /* Bytes of the packed code buffer: N·K/2.  0 for invalid sizes. */

@@ -87,7 +87,7 @@ def test_quantize_empty_is_noop(lib):
 @pytest.mark.parametrize("args,expect", [
     ((A16, 1, 4, 200, A16 * 2, A16 * 4, A16 * 8, None, 0), w4.W4_ERR_UNSUPPORTED),
     ((A16, -1, 4, 256, A16 * 2, A16 * 4, A16 * 8, None, 0), w4.W4_ERR_INVALID_ARG),
-    ((A16, 1, 4, 256, A16 * 2, A16 * 4, A16 * 8, None, 7), w4.W4_ERR_INVALID_ARG),   # bad path
+    ((A16, 1, 4, 256, A16 * 2, A16 * 4, A16 * 8, None, 3), w4.W4_ERR_INVALID_ARG),   # bad path
     ((A16, 1, 4, 256, A16 * 2, A16 * 4, A16 * 8, None, -1), w4.W4_ERR_INVALID_ARG),
     ((None, 1, 4, 256, A16 * 2, A16 * 4, A16 * 8, None, 0), w4.W4_ERR_INVALID_ARG),
     ((A16, 1, 4, 256, A16 * 2, A16 * 4, None, None, 0), w4.W4_ERR_INVALID_ARG),

@@ -11,9 +11,8 @@ from tests.helpers import check_gemm, check_quantize, gemm_gpu, quantize_gpu, sa
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-PATHS = [pytest.param(w4.W4_PATH_SMALL_M, id="small"), pytest.param(w4.W4_PATH_TENSOR, id="tensor"),
-         pytest.param(w4.W4_PATH_SMALL_M_TMEM, id="tmem")]
-PATH_VALUES = [w4.W4_PATH_SMALL_M, w4.W4_PATH_TENSOR, w4.W4_PATH_SMALL_M_TMEM]
+PATHS = [pytest.param(w4.W4_PATH_SMALL_M, id="small"), pytest.param(w4.W4_PATH_TENSOR, id="tensor")]
+PATH_VALUES = [w4.W4_PATH_SMALL_M, w4.W4_PATH_TENSOR]
 
 
 def run(cuda_lib, W, M, path, seed=0, x=None):
