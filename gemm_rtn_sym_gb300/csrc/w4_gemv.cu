@@ -79,8 +79,13 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint3
 // Pair i (0..3) of a stored code word as the bf16x2 value (136 + q_lo, 136 + q_hi):
 // one shift and one LOP3, no subtract.  The 136·Σx offset this adds to every
 // group sum is removed by starting the group's accumulator at −136·Σx.
-__device__ __forceinline__ uint32_t biased_pair(uint32_t word, int i) {
-    return ((word >> (4 * i)) & 0x000F000Fu) ^ 0x43084308u;
+template <int I>
+__device__ __forceinline__ uint32_t biased_pair(uint32_t word) {
+    uint32_t r, t = word;
+    if (I != 0) asm("shr.b32 %0, %1, %2;" : "=r"(t) : "r"(word), "n"(4 * I));
+    // (t & 0x000F000F) ^ 0x43084308 as one three-input logic op (LUT 0x6A = (a & b) ^ c).
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(r) : "r"(t), "n"(0x000F000F), "r"(0x43084308u));
+    return r;
 }
 
 constexpr uint32_t kMinus136x2 = 0xC308C308u;  // bf16x2 (−136, −136)
@@ -272,16 +277,17 @@ gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_cons
                 const uint32_t wa[4] = {wv[rt][0].x, wv[rt][0].y, wv[rt][0].z, wv[rt][0].w};
                 const uint32_t wb[4] = {wv[rt][1].x, wv[rt][1].y, wv[rt][1].z, wv[rt][1].w};
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int w = k >> 1;
-                    const int h = k & 1;
-                    const uint32_t a0 = biased_pair(wa[w], 2 * h);
-                    const uint32_t a2 = biased_pair(wa[w], 2 * h + 1);
-                    const uint32_t a1 = biased_pair(wb[w], 2 * h);
-                    const uint32_t a3 = biased_pair(wb[w], 2 * h + 1);
+                for (int w = 0; w < 4; ++w) {
+                    // k-steps 2w (pairs 0, 1 of word w) and 2w+1 (pairs 2, 3).
+                    const uint32_t a0 = biased_pair<0>(wa[w]), a2 = biased_pair<1>(wa[w]);
+                    const uint32_t a1 = biased_pair<0>(wb[w]), a3 = biased_pair<1>(wb[w]);
+                    const uint32_t b0 = biased_pair<2>(wa[w]), b2 = biased_pair<3>(wa[w]);
+                    const uint32_t b1 = biased_pair<2>(wb[w]), b3 = biased_pair<3>(wb[w]);
 #pragma unroll
-                    for (int mt = 0; mt < MT; ++mt)
-                        mma_bf16_16816(cg[mt], a0, a1, a2, a3, xw[mt][2 * k], xw[mt][2 * k + 1]);
+                    for (int mt = 0; mt < MT; ++mt) {
+                        mma_bf16_16816(cg[mt], a0, a1, a2, a3, xw[mt][4 * w], xw[mt][4 * w + 1]);
+                        mma_bf16_16816(cg[mt], b0, b1, b2, b3, xw[mt][4 * w + 2], xw[mt][4 * w + 3]);
+                    }
                 }
                 const float da = bf16_lo(d_cur[rt][0]);
                 const float db = bf16_lo(d_cur[rt][1]);

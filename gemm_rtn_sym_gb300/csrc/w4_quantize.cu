@@ -81,6 +81,23 @@ __device__ __forceinline__ uint32_t pair_bits(int lo, int hi, bool tiny) {
     return __byte_perm(lo, hi, 0x5410) & 0x000F000Fu;
 }
 
+// The chunk again, resolving ties to the even neighbour: taken only for the
+// rare chunks that contain an exact tie, kept out of line so the common path
+// carries none of its instructions.
+template <bool kTiny>
+__device__ __noinline__ uint32_t quantize_chunk_ties(uint32_t h0, uint32_t h1, uint32_t h2, uint32_t h3, float d) {
+    const Rounder<kTiny> R(d);
+    const uint32_t h[4] = {h0, h1, h2, h3};
+    uint32_t word = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int lo = R.round_bits_even(R.scaled(bf16_lo(h[j])));
+        const int hi = R.round_bits_even(R.scaled(bf16_hi(h[j])));
+        word |= pair_bits(lo, hi, kTiny) << (4 * j);
+    }
+    return word;
+}
+
 template <bool kTiny>
 __device__ __forceinline__ uint32_t quantize_chunk_t(const uint32_t (&h)[4], float d) {
     const Rounder<kTiny> R(d);
@@ -92,15 +109,7 @@ __device__ __forceinline__ uint32_t quantize_chunk_t(const uint32_t (&h)[4], flo
         const int hi = R.round_bits(R.scaled(bf16_hi(h[j])), &tie);
         word |= pair_bits(lo, hi, kTiny) << (4 * j);
     }
-    if (tie) {
-        word = 0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int lo = R.round_bits_even(R.scaled(bf16_lo(h[j])));
-            const int hi = R.round_bits_even(R.scaled(bf16_hi(h[j])));
-            word |= pair_bits(lo, hi, kTiny) << (4 * j);
-        }
-    }
+    if (tie) word = quantize_chunk_ties<kTiny>(h[0], h[1], h[2], h[3], d);
     return word;
 }
 
