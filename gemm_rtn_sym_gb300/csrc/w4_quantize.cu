@@ -23,93 +23,55 @@ constexpr int kQuantThreads = 256;
 constexpr int kQuantUnroll = 4;  // chunks in flight per thread
 
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: x + kRoundMagic rounds x to an integer (ties to even)
-constexpr int kRoundMagicBits = 0x4B400000;
 
-// round_half_even(w / d) without a per-weight division.  With ρ = 1/d
-// correctly rounded (CUDA's __frcp_rn), w·ρ differs from w/d by at most
-// |w/d|·2^-23 < 2^-19.  Both w and d carry 8-bit significands, so a quotient
-// that is not exactly a half-integer lies at least 1/512 away from every
-// half-integer; rounding w·ρ to the nearest integer therefore gives
-// round(w/d) everywhere except at exact ties.  Ties are found exactly: with
-// q' the rounded value, e = w − q'·d is exact (one FMA; q'·d has at most 12
-// significant bits and |e| ≤ d/2 + tiny), and |e| = d/2 holds precisely at a
-// tie.  The rare chunks that contain a tie are redone with the even neighbour
-// chosen.  The result is clamped to [-8, 7] only on the subnormal-scale path,
-// where d's rounding can leave max|w|/d above 7.5; for d ≥ 2^-64 it never
-// exceeds 7·(1 + 2^-8).
-//
-// rounded(): the integer nearest to r, as the low bits of the binary32
-// pattern of r + 1.5·2^23 (two's complement, valid for |r| < 2^22).
+// round_half_even(w / d) without a per-weight division and without a tie
+// branch.  With ρ = 1/d correctly rounded (CUDA's __frcp_rn):
+//   q0 = fl(w·ρ),  e = fma(−q0, d, w),  q1 = fma(e, ρ, q0)
+// is one residual-correction step of the quotient (P. Markstein, "Computation
+// of elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990).  Properties used, for bf16 w and d (8-bit significands):
+//  * at an exact tie w = (n + ½)·d, the real value q0 + e·ρ differs from n + ½
+//    by at most |n + ½ − q0|·2^-24 < 2^-44, far below half an ulp of n + ½, so
+//    q1 = n + ½ exactly, and rounding it half-to-even gives the even neighbour;
+//  * otherwise w/d lies at least 1/512 from every half-integer (2w − (2n+1)·d
+//    is a nonzero multiple of the coarser of the two grids), while q1 is within
+//    an ulp of w/d, so rounding q1 gives round(w/d).
+// Rounding uses x + 1.5·2^23: the low bits of that sum's binary32 pattern are
+// the nearest integer (ties to even) in two's complement, for |x| < 2^22.
+// The result is clamped to [-8, 7] only on the subnormal-scale path, where
+// d's rounding can leave max|w|/d above 7.5; for d ≥ 2^-64 it never exceeds
+// 7·(1 + 2^-8).
 template <bool kTiny>
 struct Rounder {
-    float d, rcp, half_d;
+    float d, rcp;
     __device__ __forceinline__ explicit Rounder(float d_) {
         d = kTiny ? d_ * 0x1p64f : d_;  // exact: power-of-two scaling of a tiny scale
         rcp = __frcp_rn(d);
-        half_d = 0.5f * d;
     }
-    __device__ __forceinline__ float scaled(float w) const { return kTiny ? w * 0x1p64f : w; }
-    // Nearest integer of x/d (ties unresolved) as rounded-magic bits; sets *tie
-    // when x/d is exactly a half-integer.
-    __device__ __forceinline__ int round_bits(float x, bool* tie) const {
-        float r = x * rcp;
-        if (kTiny) r = fminf(fmaxf(r, -8.0f), 7.0f);
-        const float tf = r + kRoundMagic;
-        const float e = fmaf(-(tf - kRoundMagic), d, x);
-        *tie = *tie || fabsf(e) == half_d;
-        return __float_as_int(tf);
-    }
-    // Same, resolving a tie to the even neighbour.
-    __device__ __forceinline__ int round_bits_even(float x) const {
-        float r = x * rcp;
-        if (kTiny) r = fminf(fmaxf(r, -8.0f), 7.0f);
-        const float tf = r + kRoundMagic;
-        const float e = fmaf(-(tf - kRoundMagic), d, x);
-        int tb = __float_as_int(tf);
-        if (fabsf(e) == half_d && (tb & 1)) tb += e > 0.0f ? 1 : -1;
-        return tb;
+    // round_half_even(w / d) as the rounded-magic bit pattern.
+    __device__ __forceinline__ int round_bits(float w) const {
+        const float x = kTiny ? w * 0x1p64f : w;
+        const float q0 = __fmul_rn(x, rcp);
+        const float e = __fmaf_rn(-q0, d, x);
+        float q1 = __fmaf_rn(e, rcp, q0);
+        if (kTiny) q1 = fminf(fmaxf(q1, -8.0f), 7.0f);
+        return __float_as_int(__fadd_rn(q1, kRoundMagic));
     }
 };
 
 // Two rounded-magic patterns -> the nibble pair (bits 0-3 and 16-19) for slots
 // j and j+4 of the stored word.
-__device__ __forceinline__ uint32_t pair_bits(int lo, int hi, bool tiny) {
-    if (tiny) {
-        lo = min(max(lo, kRoundMagicBits - 8), kRoundMagicBits + 7);
-        hi = min(max(hi, kRoundMagicBits - 8), kRoundMagicBits + 7);
-    }
+__device__ __forceinline__ uint32_t pair_bits(int lo, int hi) {
     return __byte_perm(lo, hi, 0x5410) & 0x000F000Fu;
-}
-
-// The chunk again, resolving ties to the even neighbour: taken only for the
-// rare chunks that contain an exact tie, kept out of line so the common path
-// carries none of its instructions.
-template <bool kTiny>
-__device__ __noinline__ uint32_t quantize_chunk_ties(uint32_t h0, uint32_t h1, uint32_t h2, uint32_t h3, float d) {
-    const Rounder<kTiny> R(d);
-    const uint32_t h[4] = {h0, h1, h2, h3};
-    uint32_t word = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int lo = R.round_bits_even(R.scaled(bf16_lo(h[j])));
-        const int hi = R.round_bits_even(R.scaled(bf16_hi(h[j])));
-        word |= pair_bits(lo, hi, kTiny) << (4 * j);
-    }
-    return word;
 }
 
 template <bool kTiny>
 __device__ __forceinline__ uint32_t quantize_chunk_t(const uint32_t (&h)[4], float d) {
     const Rounder<kTiny> R(d);
     uint32_t word = 0;
-    bool tie = false;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int lo = R.round_bits(R.scaled(bf16_lo(h[j])), &tie);
-        const int hi = R.round_bits(R.scaled(bf16_hi(h[j])), &tie);
-        word |= pair_bits(lo, hi, kTiny) << (4 * j);
-    }
-    if (tie) word = quantize_chunk_ties<kTiny>(h[0], h[1], h[2], h[3], d);
+    for (int j = 0; j < 4; ++j)
+        word |= pair_bits(R.round_bits(bf16_lo(h[j])), R.round_bits(bf16_hi(h[j]))) << (4 * j);
     return word;
 }
 
