@@ -48,12 +48,19 @@
 namespace w4 {
 namespace {
 
-constexpr int kTiles = 4;                // 16-row tiles per CTA (and per consumer warp)
+constexpr int kTiles = 4;                // 16-row tiles per CTA
 constexpr int kRowsCta = 16 * kTiles;    // 64 weight rows per CTA
-constexpr int kConsumers = 4;            // consumer warps; warp c takes group c of every stage
-constexpr int kStageGroups = kConsumers; // groups per stage
-constexpr int kThreads = 32 * (1 + kConsumers);
+constexpr int kStageGroups = 4;          // groups per stage
 constexpr int kMaxSplit = 8;
+constexpr int kTpw = 2;
+
+// TPW: row tiles per consumer warp.  Consumer warp c takes group c % 4 of every
+// stage for tiles (c / 4)·TPW .. +TPW-1, so 16 / TPW consumer warps per CTA.
+template <int TPW>
+struct Warps {
+    static constexpr int kConsumers = kStageGroups * (kTiles / TPW);
+    static constexpr int kThreads = 32 * (1 + kConsumers);
+};
 constexpr int kCodeStageBytes = kStageGroups * kRowsCta * 64;  // 16 KB: [group][row][64 B]
 
 template <int MT>
@@ -119,11 +126,13 @@ struct GemvArgs {
 };
 
 // MT: token tiles of 8 (1: M <= 8, 2: M <= 16).
-template <int MT>
-__global__ void __launch_bounds__(kThreads, 2)
+template <int MT, int TPW>
+__global__ void __launch_bounds__(Warps<TPW>::kThreads, 2)
 gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_constant__ CUtensorMap tmap_x,
                const GemvArgs args) {
     using C = Cfg<MT>;
+    constexpr int kConsumers = Warps<TPW>::kConsumers;
+    constexpr int kThreads = Warps<TPW>::kThreads;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -157,9 +166,9 @@ gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_cons
     __syncthreads();
 
     bool ok = true;
-    float acc[kTiles][MT][4];
+    float acc[TPW][MT][4];
 #pragma unroll
-    for (int rt = 0; rt < kTiles; ++rt)
+    for (int rt = 0; rt < TPW; ++rt)
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -190,35 +199,36 @@ gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_cons
         }
     } else {
         // -------------------------------------------------- consumers: decode + legacy MMA
-        const int cw = warp - 1;  // this warp's group within every stage
+        const int cw = (warp - 1) % kStageGroups;          // this warp's group within every stage
+        const int tile0 = ((warp - 1) / kStageGroups) * TPW;  // first of its row tiles
         // Scales of rows gid / gid+8 of each tile, for this warp's group of a stage.
-        const uint16_t* srow[kTiles][2];
+        const uint16_t* srow[TPW][2];
 #pragma unroll
-        for (int rt = 0; rt < kTiles; ++rt)
+        for (int rt = 0; rt < TPW; ++rt)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                int64_t n = n0 + rt * 16 + gid + 8 * h;
+                int64_t n = n0 + (tile0 + rt) * 16 + gid + 8 * h;
                 if (n >= args.N) n = args.N - 1;
                 srow[rt][h] = args.scales + n * G;
             }
-        auto load_scales = [&](uint32_t (&d)[kTiles][2], int t) {
+        auto load_scales = [&](uint32_t (&d)[TPW][2], int t) {
             const int64_t g = gs + t * kStageGroups + cw;
 #pragma unroll
-            for (int rt = 0; rt < kTiles; ++rt)
+            for (int rt = 0; rt < TPW; ++rt)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) d[rt][h] = (t < nt && g < ge) ? __ldg(srow[rt][h] + g) : 0u;
         };
-        uint32_t d_cur[kTiles][2], d_nxt[kTiles][2];
+        uint32_t d_cur[TPW][2], d_nxt[TPW][2];
         load_scales(d_nxt, 0);
 
         // Byte offsets inside a stage.
-        const uint32_t w_off = static_cast<uint32_t>(cw * kRowsCta * 64 + gid * 64 + tig * 16);
+        const uint32_t w_off = static_cast<uint32_t>(cw * kRowsCta * 64 + (tile0 * 16 + gid) * 64 + tig * 16);
         const uint32_t x_blk = static_cast<uint32_t>(kCodeStageBytes + (2 * cw + (tig >> 1)) * C::kXRows * 128);
 
         for (int t = 0; t < nt; ++t) {
             const int s = t % C::kStages;
 #pragma unroll
-            for (int rt = 0; rt < kTiles; ++rt) {
+            for (int rt = 0; rt < TPW; ++rt) {
                 d_cur[rt][0] = d_nxt[rt][0];
                 d_cur[rt][1] = d_nxt[rt][1];
             }
@@ -231,7 +241,7 @@ gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_cons
             const bool active = gs + t * kStageGroups + cw < ge;  // warp-uniform
             const uint32_t st = base + s * C::kStageBytes;
             uint32_t xw[MT][16];
-            uint4 wv[kTiles][2];
+            uint4 wv[TPW][2];
             if (active) {
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt) {
@@ -248,7 +258,7 @@ gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_cons
                     }
                 }
 #pragma unroll
-                for (int rt = 0; rt < kTiles; ++rt) {
+                for (int rt = 0; rt < TPW; ++rt) {
                     wv[rt][0] = lds128(st + w_off + rt * 16 * 64);
                     wv[rt][1] = lds128(st + w_off + rt * 16 * 64 + 8 * 64);
                 }
@@ -268,7 +278,7 @@ gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_cons
                                    xw[mt][2 * k], xw[mt][2 * k + 1]);
             }
 #pragma unroll
-            for (int rt = 0; rt < kTiles; ++rt) {
+            for (int rt = 0; rt < TPW; ++rt) {
                 float cg[MT][4];
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt)
@@ -308,16 +318,18 @@ gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_cons
     // consumer warps go there as red[warp][tile][mt][r][lane], then the CTA's
     // sum as part[m][row].
     __syncthreads();
-    float* red = reinterpret_cast<float*>(gbase);
-    float* part = red + kConsumers * kTiles * MT * 4 * 32;
+    float* red = reinterpret_cast<float*>(gbase);  // [group][tile][mt][r][lane]
+    float* part = red + kStageGroups * kTiles * MT * 4 * 32;
     if (warp >= 1) {
+        const int cw = (warp - 1) % kStageGroups;
+        const int tile0 = ((warp - 1) / kStageGroups) * TPW;
 #pragma unroll
-        for (int rt = 0; rt < kTiles; ++rt)
+        for (int rt = 0; rt < TPW; ++rt)
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
                 for (int r = 0; r < 4; ++r)
-                    red[((((warp - 1) * kTiles + rt) * MT + mt) * 4 + r) * 32 + lane] = acc[rt][mt][r];
+                    red[(((cw * kTiles + tile0 + rt) * MT + mt) * 4 + r) * 32 + lane] = acc[rt][mt][r];
     }
     __syncthreads();
     for (int e = threadIdx.x; e < kTiles * MT * 4 * 32; e += kThreads) {
@@ -326,7 +338,7 @@ gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_cons
         const int mt = (e >> 7) % MT;
         const int rt = e / (MT * 128);
         float v = 0.0f;
-        for (int w = 0; w < kConsumers; ++w) v += red[(((w * kTiles + rt) * MT + mt) * 4 + r) * 32 + l];
+        for (int w = 0; w < kStageGroups; ++w) v += red[(((w * kTiles + rt) * MT + mt) * 4 + r) * 32 + l];
         const int rowc = rt * 16 + (l >> 2) + (r >= 2 ? 8 : 0);
         const int m = mt * 8 + 2 * (l & 3) + (r & 1);
         if (split == 1) {
@@ -356,10 +368,11 @@ gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_cons
 
 std::mutex g_attr_mutex;
 
-template <int MT>
+template <int MT, int TPW>
 cudaError_t launch_mt(const __nv_bfloat16* x, int mp, int64_t N, int64_t K, const CUtensorMap& tmap_codes,
                       const uint16_t* scales, __nv_bfloat16* y, const DeviceInfo& dev, cudaStream_t stream) {
     using C = Cfg<MT>;
+    constexpr int kThreads = Warps<TPW>::kThreads;
     static bool attr_set[64];
     int device = 0;
     if (cudaError_t e = cudaGetDevice(&device)) return e;
@@ -367,7 +380,7 @@ cudaError_t launch_mt(const __nv_bfloat16* x, int mp, int64_t N, int64_t K, cons
     {
         std::lock_guard<std::mutex> lock(g_attr_mutex);
         if (!attr_set[device]) {
-            if (cudaError_t e = cudaFuncSetAttribute(gemv_w4_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaError_t e = cudaFuncSetAttribute(gemv_w4_kernel<MT, TPW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                      C::kSmemBytes))
                 return e;
             attr_set[device] = true;
@@ -395,7 +408,7 @@ cudaError_t launch_mt(const __nv_bfloat16* x, int mp, int64_t N, int64_t K, cons
         q.attrs = qa;
         q.numAttrs = 1;
         int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, gemv_w4_kernel<MT>, &q) != cudaSuccess || clusters < 1) {
+        if (cudaOccupancyMaxActiveClusters(&clusters, gemv_w4_kernel<MT, TPW>, &q) != cudaSuccess || clusters < 1) {
             cudaGetLastError();
             continue;
         }
@@ -430,7 +443,7 @@ cudaError_t launch_mt(const __nv_bfloat16* x, int mp, int64_t N, int64_t K, cons
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_w4_kernel<MT>, tmap_codes, tmap_x, args);
+    return cudaLaunchKernelEx(&cfg, gemv_w4_kernel<MT, TPW>, tmap_codes, tmap_x, args);
 }
 
 }  // namespace
@@ -444,8 +457,8 @@ cudaError_t launch_gemv(const void* x, int64_t M, int64_t N, int64_t K, const vo
     auto* yb = static_cast<__nv_bfloat16*>(y);
     for (int64_t m0 = 0; m0 < M; m0 += 16) {
         const int mp = static_cast<int>(M - m0 < 16 ? M - m0 : 16);
-        const cudaError_t e = mp <= 8 ? launch_mt<1>(xb + m0 * K, mp, N, K, tmap_codes, sc, yb + m0 * N, dev, stream)
-                                      : launch_mt<2>(xb + m0 * K, mp, N, K, tmap_codes, sc, yb + m0 * N, dev, stream);
+        const cudaError_t e = mp <= 8 ? launch_mt<1, kTpw>(xb + m0 * K, mp, N, K, tmap_codes, sc, yb + m0 * N, dev, stream)
+                                      : launch_mt<2, kTpw>(xb + m0 * K, mp, N, K, tmap_codes, sc, yb + m0 * N, dev, stream);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
