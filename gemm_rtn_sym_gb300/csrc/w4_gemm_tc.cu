@@ -49,6 +49,7 @@ struct TcArgs {
     __nv_bfloat16* y;
     int64_t M, N, K;
     int bm;
+    int split;  // CTAs of a cluster splitting K (1 = no split)
     unsigned* status;
 };
 
@@ -83,7 +84,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs args) {
     const int lane = threadIdx.x & 31;
     const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kBN;
     const int64_t m0 = static_cast<int64_t>(blockIdx.y) * bm;
-    const int nkb = static_cast<int>(args.K / kBK);
+    const int split = args.split;
+    const uint32_t rank = split > 1 ? cluster_rank() : 0u;
+    const int nkb_all = static_cast<int>(args.K / kBK);
+    const int kb_lo = static_cast<int>((static_cast<int64_t>(rank) * nkb_all) / split);
+    const int nkb = static_cast<int>((static_cast<int64_t>(rank + 1) * nkb_all) / split) - kb_lo;
     const int64_t G = args.K >> 7;
     uint32_t tmem_cols = 32;
     while (tmem_cols < static_cast<uint32_t>(bm)) tmem_cols <<= 1;
@@ -114,7 +119,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs args) {
                 const uint32_t r = static_cast<uint32_t>(kb / kStages);
                 if (!mbar_wait(empty(s), (r & 1u) ^ 1u)) { ok = false; break; }
                 mbar_arrive_expect_tx(full_b(s), b_tile_bytes);
-                tma_load_2d(b_base + s * b_tile_bytes, &tmap_x, kb * kBK, static_cast<int>(m0), full_b(s));
+                tma_load_2d(b_base + s * b_tile_bytes, &tmap_x, (kb_lo + kb) * kBK, static_cast<int>(m0), full_b(s));
                 issued = kb + 1;
             }
             if (!ok) {
@@ -159,10 +164,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs args) {
         auto fetch = [&](int kb) {
             Codes c;
             if (valid && kb < nkb) {
-                const uint8_t* p = row + (kb >> 1) * 64 + (kb & 1) * 32;
+                const int kg = kb_lo + kb;
+                const uint8_t* p = row + (kg >> 1) * 64 + (kg & 1) * 32;
                 c.lo = ld_stream(p);
                 c.hi = ld_stream(p + 16);
-                c.d = __ldg(srow + (kb >> 1));
+                c.d = __ldg(srow + (kg >> 1));
             } else {
                 c.lo = make_uint4(0, 0, 0, 0);
                 c.hi = make_uint4(0, 0, 0, 0);
@@ -215,12 +221,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs args) {
         if (acc_ready) {
             tc_fence_after();
             const int q = warp & 3;  // TMEM lane quarter this warp may access
-            const int64_t ny = n0 + q * 32 + lane;
+            const int rowt = q * 32 + lane;
+            const int64_t ny = n0 + rowt;
             const uint32_t taddr = tmem_d + (static_cast<uint32_t>(q * 32) << 16);
+            // With a split, the fp32 partial goes to shared memory (the ring is
+            // idle now) as red[column][row], for the cluster reduction below.
+            float* red = reinterpret_cast<float*>(gbase);
             for (int c0 = 0; c0 < bm; c0 += 16) {
                 uint32_t v[16];
                 tmem_ld16(taddr + c0, v);
-                if (ny < args.N) {
+                if (split > 1) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) red[(c0 + j) * kBN + rowt] = __uint_as_float(v[j]);
+                } else if (ny < args.N) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int64_t m = m0 + c0 + j;
@@ -231,6 +244,27 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs args) {
         } else if (ok) {
             record_status(args.status, kStatusTimeout);
         }
+    }
+
+    if (split > 1) {
+        // Split-K: CTA `rank` sums rows [rank*128/split, (rank+1)*128/split) of
+        // every CTA's partial, in rank order, and stores them.
+        cluster_sync();
+        const int r0 = (static_cast<int>(rank) * kBN) / split;
+        const int r1 = (static_cast<int>(rank + 1) * kBN) / split;
+        const int rows = r1 - r0;
+        const uint32_t red_addr = base;
+        for (int e = threadIdx.x; e < rows * bm; e += kThreads) {
+            const int rowt = r0 + e % rows;
+            const int c = e / rows;
+            const int64_t ny = n0 + rowt;
+            const int64_t m = m0 + c;
+            float v = 0.0f;
+            for (int r = 0; r < split; ++r)
+                v += ld_cluster_f32(red_addr + static_cast<uint32_t>((c * kBN + rowt) * 4), static_cast<uint32_t>(r));
+            if (ny < args.N && m < args.M) args.y[m * args.N + ny] = __float2bfloat16_rn(v);
+        }
+        cluster_sync();
     }
 
     tc_fence_before();
@@ -338,6 +372,40 @@ cudaError_t launch_gemm_tc(const void* x, int64_t M, int64_t N, int64_t K, const
             g_attr_set[device] = true;
         }
     }
+    // Split-K over a cluster when the tiles alone leave SMs idle: pick the
+    // cluster size (1..8, at least 4 k-blocks per CTA) that needs the fewest
+    // rounds of k-block work, given how many such clusters fit at once.
+    const int64_t nkb_all = K / kBK;
+    int split = 1;
+    {
+        double best = 0.0;
+        for (int s = 1; s <= 8 && s * 4 <= nkb_all; ++s) {
+            cudaLaunchConfig_t q = {};
+            q.gridDim = dim3(static_cast<unsigned>(n_tiles), static_cast<unsigned>(m_tiles), static_cast<unsigned>(s));
+            q.blockDim = dim3(kThreads, 1, 1);
+            q.dynamicSmemBytes = smem;
+            cudaLaunchAttribute qa[1];
+            qa[0].id = cudaLaunchAttributeClusterDimension;
+            qa[0].val.clusterDim.x = 1;
+            qa[0].val.clusterDim.y = 1;
+            qa[0].val.clusterDim.z = static_cast<unsigned>(s);
+            q.attrs = qa;
+            q.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tc_kernel, &q) != cudaSuccess || clusters < 1) {
+                cudaGetLastError();
+                continue;
+            }
+            const int64_t waves = (n_tiles * m_tiles + clusters - 1) / clusters;
+            const double cost = static_cast<double>(waves) * static_cast<double>((nkb_all + s - 1) / s) +
+                                (s > 1 ? 2.0 : 0.0);  // the reduction costs about two k-blocks
+            if (best == 0.0 || cost < best) {
+                best = cost;
+                split = s;
+            }
+        }
+    }
+
     TcArgs args;
     args.packed = static_cast<const uint8_t*>(packed);
     args.scales = static_cast<const uint16_t*>(scales);
@@ -346,10 +414,21 @@ cudaError_t launch_gemm_tc(const void* x, int64_t M, int64_t N, int64_t K, const
     args.N = N;
     args.K = K;
     args.bm = static_cast<int>(bm);
+    args.split = split;
     args.status = dev.status;
-    dim3 grid(static_cast<unsigned>(n_tiles), static_cast<unsigned>(m_tiles));
-    gemm_tc_kernel<<<grid, kThreads, smem, stream>>>(tmap, args);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(n_tiles), static_cast<unsigned>(m_tiles), static_cast<unsigned>(split));
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = static_cast<unsigned>(split);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, tmap, args);
 }
 
 }  // namespace w4

@@ -52,7 +52,7 @@ constexpr int kTiles = 4;                // 16-row tiles per CTA
 constexpr int kRowsCta = 16 * kTiles;    // 64 weight rows per CTA
 constexpr int kStageGroups = 4;          // groups per stage
 constexpr int kMaxSplit = 8;
-constexpr int kTpw = 2;
+constexpr int kTpw = 2;  // row tiles per consumer warp at M <= 8 (4 at M <= 16: fewer x fragments per tile)
 
 // TPW: row tiles per consumer warp.  Consumer warp c takes group c % 4 of every
 // stage for tiles (c / 4)·TPW .. +TPW-1, so 16 / TPW consumer warps per CTA.
@@ -96,25 +96,6 @@ __device__ __forceinline__ uint32_t biased_pair(uint32_t word) {
 }
 
 constexpr uint32_t kMinus136x2 = 0xC308C308u;  // bf16x2 (−136, −136)
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
-                     "memory");
-}
-
-__device__ __forceinline__ float ld_cluster_f32(uint32_t local_addr, uint32_t rank) {
-    uint32_t remote;
-    float v;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
-}
 
 struct GemvArgs {
     const uint16_t* scales;
@@ -458,7 +439,7 @@ cudaError_t launch_gemv(const void* x, int64_t M, int64_t N, int64_t K, const vo
     for (int64_t m0 = 0; m0 < M; m0 += 16) {
         const int mp = static_cast<int>(M - m0 < 16 ? M - m0 : 16);
         const cudaError_t e = mp <= 8 ? launch_mt<1, kTpw>(xb + m0 * K, mp, N, K, tmap_codes, sc, yb + m0 * N, dev, stream)
-                                      : launch_mt<2, kTpw>(xb + m0 * K, mp, N, K, tmap_codes, sc, yb + m0 * N, dev, stream);
+                                      : launch_mt<2, 4>(xb + m0 * K, mp, N, K, tmap_codes, sc, yb + m0 * N, dev, stream);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
