@@ -36,12 +36,15 @@ namespace {
 
 constexpr int kBN = 128;            // weight rows per CTA = MMA M
 constexpr int kBK = 64;             // k per stage: one 128-byte swizzle row of bf16
-constexpr int kStages = 4;
-constexpr int kThreads = 192;
+constexpr int kStages = 3;          // A (dequantised) + B (activation) stages
+constexpr int kCodeStages = 4;      // code stages of two groups (4 k-blocks) each: 16 k-blocks ahead
+constexpr int kCodeStageBytes = 2 * kBN * 64;  // 16 KB: [group][row][64 B], 64-byte swizzle
+// Warps: 0 activation TMA, 1 TMEM + MMA, 2..5 dequantise + epilogue, 6 code TMA.
+constexpr int kThreads = 224;
 constexpr int kDequantWarp0 = 2;
+constexpr int kCodeWarp = 6;
 constexpr int kATileBytes = kBN * kBK * 2;  // 16 KB
 constexpr int kMaxBM = 256;
-constexpr int kPrefetch = 2;        // stages of codes held in registers ahead of use
 
 struct TcArgs {
     const uint8_t* packed;
@@ -61,7 +64,8 @@ __device__ __forceinline__ uint32_t deq_pair(uint32_t word, int i, __nv_bfloat16
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs args) {
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_codes,
+               const TcArgs args) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -71,11 +75,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs args) {
     const uint32_t b_tile_bytes = static_cast<uint32_t>(bm) * 128u;
     const uint32_t a_base = base;
     const uint32_t b_base = base + kStages * kATileBytes;
-    const uint32_t bar_base = b_base + kStages * b_tile_bytes;
+    const uint32_t code_base = b_base + kStages * b_tile_bytes;
+    const uint32_t bar_base = code_base + kCodeStages * kCodeStageBytes;
     auto full_a = [&](int s) { return bar_base + 8u * s; };
     auto full_b = [&](int s) { return bar_base + 8u * (kStages + s); };
     auto empty = [&](int s) { return bar_base + 8u * (2 * kStages + s); };
-    const uint32_t accum_bar = bar_base + 8u * (3 * kStages);
+    auto code_full = [&](int c) { return bar_base + 8u * (3 * kStages + c); };
+    auto code_empty = [&](int c) { return bar_base + 8u * (3 * kStages + kCodeStages + c); };
+    const uint32_t accum_bar = bar_base + 8u * (3 * kStages + 2 * kCodeStages);
     const uint32_t tmem_slot = accum_bar + 8u;
     volatile uint32_t* tmem_slot_ptr =
         reinterpret_cast<volatile uint32_t*>(gbase + (tmem_slot - base));
@@ -86,10 +93,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs args) {
     const int64_t m0 = static_cast<int64_t>(blockIdx.y) * bm;
     const int split = args.split;
     const uint32_t rank = split > 1 ? cluster_rank() : 0u;
-    const int nkb_all = static_cast<int>(args.K / kBK);
-    const int kb_lo = static_cast<int>((static_cast<int64_t>(rank) * nkb_all) / split);
-    const int nkb = static_cast<int>((static_cast<int64_t>(rank + 1) * nkb_all) / split) - kb_lo;
     const int64_t G = args.K >> 7;
+    // K range of this CTA, in whole groups (a code stage holds two groups).
+    const int64_t g_lo = (static_cast<int64_t>(rank) * G) / split;
+    const int64_t g_hi = (static_cast<int64_t>(rank + 1) * G) / split;
+    const int kb_lo = static_cast<int>(2 * g_lo);
+    const int nkb = static_cast<int>(2 * (g_hi - g_lo));
     uint32_t tmem_cols = 32;
     while (tmem_cols < static_cast<uint32_t>(bm)) tmem_cols <<= 1;
 
@@ -98,6 +107,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs args) {
             mbar_init(full_a(s), 128);
             mbar_init(full_b(s), 1);
             mbar_init(empty(s), 1);
+        }
+        for (int c = 0; c < kCodeStages; ++c) {
+            mbar_init(code_full(c), 1);
+            mbar_init(code_empty(c), 128 * 4);  // every dequantiser, once per k-block of the stage
         }
         mbar_init(accum_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -129,6 +142,28 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs args) {
                     mbar_wait(full_b(kb % kStages), static_cast<uint32_t>(kb / kStages) & 1u);
             }
         }
+    } else if (warp == kCodeWarp) {
+        // ------------------------------------------------ codes via TMA
+        if (lane == 0) {
+            const int nst = (nkb + 3) / 4;
+            int issued = 0;
+            for (int t = 0; t < nst; ++t) {
+                const int c = t % kCodeStages;
+                if (!mbar_wait(code_empty(c), (static_cast<uint32_t>(t / kCodeStages) & 1u) ^ 1u)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(code_full(c), kCodeStageBytes);
+                tma_load_3d(code_base + c * kCodeStageBytes, &tmap_codes, 0, static_cast<int>(n0),
+                            static_cast<int>(g_lo + 2 * t), code_full(c));
+                issued = t + 1;
+            }
+            if (!ok) {
+                record_status(args.status, kStatusTimeout);
+                for (int t = issued > kCodeStages ? issued - kCodeStages : 0; t < issued; ++t)
+                    mbar_wait(code_full(t % kCodeStages), static_cast<uint32_t>(t / kCodeStages) & 1u);
+            }
+        }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issue
         if (lane == 0) {
@@ -152,65 +187,47 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs args) {
     } else {
         // ------------------------------------------------ dequant producers
         const int t = threadIdx.x - 32 * kDequantWarp0;  // weight row within the tile
-        const int64_t n = n0 + t;
-        const bool valid = n < args.N;
-        const uint8_t* row = args.packed + (valid ? n : 0) * (args.K >> 1);
-        const uint16_t* srow = args.scales + (valid ? n : 0) * G;
-
-        struct Codes {
-            uint4 lo, hi;
-            uint32_t d;
-        };
-        auto fetch = [&](int kb) {
-            Codes c;
-            if (valid && kb < nkb) {
-                const int kg = kb_lo + kb;
-                const uint8_t* p = row + (kg >> 1) * 64 + (kg & 1) * 32;
-                c.lo = ld_stream(p);
-                c.hi = ld_stream(p + 16);
-                c.d = __ldg(srow + (kg >> 1));
-            } else {
-                c.lo = make_uint4(0, 0, 0, 0);
-                c.hi = make_uint4(0, 0, 0, 0);
-                c.d = 0;
+        const int64_t n = n0 + t < args.N ? n0 + t : args.N - 1;  // padding rows: zero codes, valid scale
+        const uint16_t* srow = args.scales + n * G;
+        // Row t of a code stage: 64 bytes per group, 16-byte chunk c at c ^ ((t >> 1) & 3).
+        const uint32_t row_off = static_cast<uint32_t>(t * 64);
+        const uint32_t sw = static_cast<uint32_t>((t >> 1) & 3);
+        uint32_t d_next = nkb > 0 ? __ldg(srow + (kb_lo >> 1)) : 0u;
+        for (int kb = 0; kb < nkb && ok; ++kb) {
+            const int s = kb % kStages;
+            const uint32_t r = static_cast<uint32_t>(kb / kStages);
+            const int cst = (kb >> 2) % kCodeStages;
+            const int sub = kb & 3;  // k-block within the code stage
+            const uint32_t dbits = d_next;
+            if (kb + 1 < nkb) d_next = __ldg(srow + ((kb_lo + kb + 1) >> 1));
+            if (!mbar_wait(code_full(cst), static_cast<uint32_t>((kb >> 2) / kCodeStages) & 1u)) {
+                ok = false;
+                break;
             }
-            return c;
-        };
-        Codes ring[kPrefetch];
-#pragma unroll
-        for (int i = 0; i < kPrefetch; ++i) ring[i] = fetch(i);
-
-        for (int kb0 = 0; kb0 < nkb && ok; kb0 += kPrefetch) {
-#pragma unroll
-            for (int i = 0; i < kPrefetch; ++i) {
-                const int kb = kb0 + i;
-                if (kb < nkb && ok) {
-                    const int s = kb % kStages;
-                    const uint32_t r = static_cast<uint32_t>(kb / kStages);
-                    const Codes cur = ring[i];
-                    ring[i] = fetch(kb + kPrefetch);
-                    if (!mbar_wait(empty(s), (r & 1u) ^ 1u)) {
-                        ok = false;
-                    } else {
-                        const uint32_t d2bits = cur.d | (cur.d << 16);
-                        const __nv_bfloat162 d2 = *reinterpret_cast<const __nv_bfloat162*>(&d2bits);
-                        const uint32_t words[8] = {cur.lo.x, cur.lo.y, cur.lo.z, cur.lo.w,
-                                                   cur.hi.x, cur.hi.y, cur.hi.z, cur.hi.w};
-                        uint8_t* a_row = gbase + (a_base - base) + s * kATileBytes;
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            uint4 v;
-                            v.x = deq_pair(words[c], 0, d2);
-                            v.y = deq_pair(words[c], 1, d2);
-                            v.z = deq_pair(words[c], 2, d2);
-                            v.w = deq_pair(words[c], 3, d2);
-                            *reinterpret_cast<uint4*>(a_row + sw128_offset(t, c)) = v;
-                        }
-                        fence_async_smem();
-                        mbar_arrive(full_a(s));
-                    }
-                }
+            const uint32_t slot = code_base + cst * kCodeStageBytes + (sub >> 1) * (kBN * 64) + row_off;
+            const uint32_t c0 = static_cast<uint32_t>(2 * (sub & 1));
+            const uint4 lo = lds128(slot + ((c0 ^ sw) << 4));
+            const uint4 hi = lds128(slot + (((c0 + 1) ^ sw) << 4));
+            mbar_arrive(code_empty(cst));
+            if (!mbar_wait(empty(s), (r & 1u) ^ 1u)) {
+                ok = false;
+                break;
             }
+            const uint32_t d2bits = dbits | (dbits << 16);
+            const __nv_bfloat162 d2 = *reinterpret_cast<const __nv_bfloat162*>(&d2bits);
+            const uint32_t words[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+            uint8_t* a_row = gbase + (a_base - base) + s * kATileBytes;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint4 v;
+                v.x = deq_pair(words[c], 0, d2);
+                v.y = deq_pair(words[c], 1, d2);
+                v.z = deq_pair(words[c], 2, d2);
+                v.w = deq_pair(words[c], 3, d2);
+                *reinterpret_cast<uint4*>(a_row + sw128_offset(t, c)) = v;
+            }
+            fence_async_smem();
+            mbar_arrive(full_a(s));
         }
         if (!ok) record_status(args.status, kStatusTimeout);
 
@@ -312,7 +329,7 @@ cudaError_t encode_x_map(CUtensorMap* map, const void* x, int64_t M, int64_t K, 
 }
 
 cudaError_t encode_codes_stage_map(CUtensorMap* map, const void* packed, int64_t N, int64_t K, int rows,
-                                   int groups) {
+                                   int groups, CUtensorMapSwizzle swizzle) {
     if (cudaError_t e = get_encoder()) return e;
     // codes viewed as [G groups][N rows][64 bytes]: byte (b, n, g) at n*K/2 + g*64 + b.
     const cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K / 128)};
@@ -320,7 +337,7 @@ cudaError_t encode_codes_stage_map(CUtensorMap* map, const void* packed, int64_t
     const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(rows), static_cast<cuuint32_t>(groups)};
     const cuuint32_t estr[3] = {1, 1, 1};
     if (g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(packed), dims, strides, box, estr,
-                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     return cudaSuccess;
@@ -342,7 +359,10 @@ cudaError_t encode_x_stage_map(CUtensorMap* map, const void* x, int64_t M, int64
 
 namespace {
 
-int smem_bytes(int bm) { return kStages * (kATileBytes + bm * 128) + 8 * (3 * kStages + 2) + 1024; }
+int smem_bytes(int bm) {
+    return kStages * (kATileBytes + bm * 128) + kCodeStages * kCodeStageBytes + 8 * (3 * kStages + 2 * kCodeStages + 2) +
+           1024;
+}
 
 }  // namespace
 
@@ -359,6 +379,9 @@ cudaError_t launch_gemm_tc(const void* x, int64_t M, int64_t N, int64_t K, const
 
     CUtensorMap tmap;
     if (cudaError_t e = encode_x_map(&tmap, x, M, K, static_cast<int>(bm))) return e;
+    CUtensorMap tmap_codes;
+    if (cudaError_t e = encode_codes_stage_map(&tmap_codes, packed, N, K, kBN, 2, CU_TENSOR_MAP_SWIZZLE_64B))
+        return e;
 
     int device = 0;
     if (cudaError_t e = cudaGetDevice(&device)) return e;
@@ -379,7 +402,7 @@ cudaError_t launch_gemm_tc(const void* x, int64_t M, int64_t N, int64_t K, const
     int split = 1;
     {
         double best = 0.0;
-        for (int s = 1; s <= 8 && s * 4 <= nkb_all; ++s) {
+        for (int s = 1; s <= 8 && s * 2 <= K / 128; ++s) {
             cudaLaunchConfig_t q = {};
             q.gridDim = dim3(static_cast<unsigned>(n_tiles), static_cast<unsigned>(m_tiles), static_cast<unsigned>(s));
             q.blockDim = dim3(kThreads, 1, 1);
@@ -428,7 +451,7 @@ cudaError_t launch_gemm_tc(const void* x, int64_t M, int64_t N, int64_t K, const
     attr[0].val.clusterDim.z = static_cast<unsigned>(split);
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, tmap, args);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, tmap, tmap_codes, args);
 }
 
 }  // namespace w4

@@ -432,7 +432,8 @@ cudaError_t launch_mt(const __nv_bfloat16* x, int mp, int64_t N, int64_t K, cons
 cudaError_t launch_gemv(const void* x, int64_t M, int64_t N, int64_t K, const void* packed,
                         const void* scales, void* y, const DeviceInfo& dev, cudaStream_t stream) {
     CUtensorMap tmap_codes;
-    if (cudaError_t e = encode_codes_stage_map(&tmap_codes, packed, N, K, kRowsCta, kStageGroups)) return e;
+    if (cudaError_t e = encode_codes_stage_map(&tmap_codes, packed, N, K, kRowsCta, kStageGroups, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return e;
     const auto* xb = static_cast<const __nv_bfloat16*>(x);
     const auto* sc = static_cast<const uint16_t*>(scales);
     auto* yb = static_cast<__nv_bfloat16*>(y);

@@ -40,10 +40,10 @@ cudaError_t encode_x_map(CUtensorMap* map, const void* x, int64_t M, int64_t K, 
 cudaError_t encode_x_stage_map(CUtensorMap* map, const void* x, int64_t M, int64_t K, int rows, int blocks);
 
 // 3-D tensor map over packed codes u8 [N, K/2] seen as [G][N][64]: boxes of
-// `groups` groups x `rows` rows x 64 bytes (dense, no swizzle); rows past N and
-// groups past G read as zeros.
+// `groups` groups x `rows` rows x 64 bytes; rows past N and groups past G read
+// as zeros.
 cudaError_t encode_codes_stage_map(CUtensorMap* map, const void* packed, int64_t N, int64_t K, int rows,
-                                   int groups);
+                                   int groups, CUtensorMapSwizzle swizzle);
 
 cudaError_t launch_wait_probe(int64_t spin_limit, int arrive, const DeviceInfo& dev,
                               cudaStream_t stream);
