@@ -1,5 +1,6 @@
 // Tensor-core W4A16 matmul for larger M: tcgen05.mma (kind::f16, BF16 × BF16 →
-// FP32 in TMEM), weights dequantised into shared memory.
+// FP32 in TMEM), weights dequantised straight into tensor memory as the MMA's
+// A operand.
 //
 // Source: Qwen3.5-4B quantisation study, §1 FFN example y = W x with ŵ = d·q
 // (one d per 128 consecutive inputs) and §2 settings (4-bit weights, BF16
@@ -9,16 +10,21 @@
 //
 // Tile: 128 weight rows (the MMA's M) × up to 256 tokens (the MMA's N; the
 // token count is rounded up to a multiple of 16, padding rows of x read as
-// zeros) per CTA, K streamed in blocks of 64 through a 4-stage ring:
+// zeros) per CTA, K streamed in blocks of 64 through a 4-stage ring; a cluster
+// of up to 8 CTAs may split K (whole groups each) and sum its fp32 partials
+// over distributed shared memory.
 //   warp 0      : TMA loads of x tiles (128-byte swizzle) into the ring;
 //   warp 1      : allocates TMEM, one lane issues 4 MMAs (K = 16 each) per
-//                 stage and commits each stage back to its "empty" barrier;
-//   warps 2..5  : one weight row per thread — load 32 bytes of codes (kept two
-//                 stages ahead in registers), decode nibble pairs to bf16 q,
-//                 multiply by d (bf16, round-to-nearest), and store the 128-byte
-//                 row into the stage's A tile in the same 128-byte swizzle the
-//                 MMA descriptor names; then, after the last stage, read the
-//                 accumulator back from TMEM and store y.
+//                 stage with A read from TMEM, B from shared memory, and
+//                 commits each stage back to its "empty" barrier;
+//   warps 2..9  : one weight row and 32 k per thread — read 16 bytes of codes
+//                 from the code ring, decode nibble pairs to bf16 q, multiply
+//                 by d (bf16, round-to-nearest) and store the 16 columns into
+//                 the stage's A slot with tcgen05.st; after the last stage,
+//                 read the accumulator back and store y (or the partial);
+//   warp 10     : TMA loads of codes, two groups × 128 rows per copy.
+// Keeping A out of shared memory leaves the shared-memory port to the MMA's
+// B reads and the code ring, which at 200+ tokens is what bounds the tile.
 // Every mbarrier wait is bounded; a wait that runs out records a timeout in
 // the status word and the CTA winds down (draining its own TMA copies and
 // MMAs before freeing TMEM).
@@ -35,19 +41,25 @@ namespace w4 {
 namespace {
 
 constexpr int kBN = 128;            // weight rows per CTA = MMA M
-constexpr int kBK = 64;             // k per stage: one 128-byte swizzle row of bf16
-constexpr int kStages = 3;          // A (dequantised) + B (activation) stages
+constexpr int kBK = 64;             // k per stage
+constexpr int kStages = 4;          // A (decoded, in TMEM) + B (activation, shared memory) stages
 constexpr int kCodeStages = 4;      // code stages of two groups (4 k-blocks) each: 16 k-blocks ahead
 constexpr int kCodeStageBytes = 2 * kBN * 64;  // 16 KB: [group][row][64 B], 64-byte swizzle
-// Warps: 0 activation TMA, 1 TMEM + MMA, 2..5 dequantise + epilogue, 6 code TMA.
-constexpr int kThreads = 224;
+// Warps: 0 activation TMA, 1 TMEM + MMA, 2..9 dequantise + epilogue (two per
+// TMEM lane quarter, each one half of the k-block), 10 code TMA.
 constexpr int kDequantWarp0 = 2;
-constexpr int kCodeWarp = 6;
-constexpr int kATileBytes = kBN * kBK * 2;  // 16 KB
+constexpr int kDequantWarps = 8;
+constexpr int kCodeWarp = kDequantWarp0 + kDequantWarps;
+constexpr int kThreads = 32 * (kCodeWarp + 1);
 constexpr int kMaxBM = 256;
+// Tensor memory: accumulator in columns [0, 256), decoded A stages of 32
+// columns (64 k of bf16 pairs) from column 256.  The whole 512 columns are
+// taken, so the shared memory request below keeps one CTA per SM.
+constexpr uint32_t kColA = 256;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kMinSmemBytes = 120 * 1024;
 
 struct TcArgs {
-    const uint8_t* packed;
     const uint16_t* scales;
     __nv_bfloat16* y;
     int64_t M, N, K;
@@ -73,8 +85,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
 
     const int bm = args.bm;
     const uint32_t b_tile_bytes = static_cast<uint32_t>(bm) * 128u;
-    const uint32_t a_base = base;
-    const uint32_t b_base = base + kStages * kATileBytes;
+    const uint32_t b_base = base;
     const uint32_t code_base = b_base + kStages * b_tile_bytes;
     const uint32_t bar_base = code_base + kCodeStages * kCodeStageBytes;
     auto full_a = [&](int s) { return bar_base + 8u * s; };
@@ -99,24 +110,22 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
     const int64_t g_hi = (static_cast<int64_t>(rank + 1) * G) / split;
     const int kb_lo = static_cast<int>(2 * g_lo);
     const int nkb = static_cast<int>(2 * (g_hi - g_lo));
-    uint32_t tmem_cols = 32;
-    while (tmem_cols < static_cast<uint32_t>(bm)) tmem_cols <<= 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(full_a(s), 128);
+            mbar_init(full_a(s), 32 * kDequantWarps);
             mbar_init(full_b(s), 1);
             mbar_init(empty(s), 1);
         }
         for (int c = 0; c < kCodeStages; ++c) {
             mbar_init(code_full(c), 1);
-            mbar_init(code_empty(c), 128 * 4);  // every dequantiser, once per k-block of the stage
+            mbar_init(code_empty(c), 32 * kDequantWarps * 4);  // every dequantiser, once per k-block
         }
         mbar_init(accum_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_async_smem();
     }
-    if (warp == 1) tmem_alloc(tmem_slot, tmem_cols);
+    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -173,20 +182,23 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
                 const uint32_t par = static_cast<uint32_t>(kb / kStages) & 1u;
                 if (!mbar_wait(full_b(s), par) || !mbar_wait(full_a(s), par)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t a_s = a_base + s * kATileBytes;
+                const uint32_t a_s = tmem_d + kColA + 32u * s;
                 const uint32_t b_s = b_base + s * b_tile_bytes;
 #pragma unroll
                 for (int ks = 0; ks < kBK / 16; ++ks)
-                    mma_bf16(tmem_d, sw128_desc(a_s + ks * 32), sw128_desc(b_s + ks * 32), idesc,
-                             (kb | ks) != 0 ? 1u : 0u);
+                    mma_bf16_tmem_a(tmem_d, a_s + 8u * ks, sw128_desc(b_s + ks * 32), idesc,
+                                    (kb | ks) != 0 ? 1u : 0u);
                 mma_commit(empty(s));
             }
             mma_commit(accum_bar);  // also tracks MMAs issued before an abort
             if (!ok) record_status(args.status, kStatusTimeout);
         }
     } else {
-        // ------------------------------------------------ dequant producers
-        const int t = threadIdx.x - 32 * kDequantWarp0;  // weight row within the tile
+        // ------------------------------------------------ dequantisers
+        const int quarter = warp & 3;               // TMEM lane quarter this warp may access
+        const int half = (warp - kDequantWarp0) >> 2;  // which 32 k of each 64-k block
+        const int t = quarter * 32 + lane;          // weight row within the tile
+        const uint32_t lane_base = tmem_d + (static_cast<uint32_t>(quarter * 32) << 16);
         const int64_t n = n0 + t < args.N ? n0 + t : args.N - 1;  // padding rows: zero codes, valid scale
         const uint16_t* srow = args.scales + n * G;
         // Row t of a code stage: 64 bytes per group, 16-byte chunk c at c ^ ((t >> 1) & 3).
@@ -200,33 +212,26 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             const int sub = kb & 3;  // k-block within the code stage
             const uint32_t dbits = d_next;
             if (kb + 1 < nkb) d_next = __ldg(srow + ((kb_lo + kb + 1) >> 1));
-            if (!mbar_wait(code_full(cst), static_cast<uint32_t>((kb >> 2) / kCodeStages) & 1u)) {
-                ok = false;
-                break;
-            }
-            const uint32_t slot = code_base + cst * kCodeStageBytes + (sub >> 1) * (kBN * 64) + row_off;
-            const uint32_t c0 = static_cast<uint32_t>(2 * (sub & 1));
-            const uint4 lo = lds128(slot + ((c0 ^ sw) << 4));
-            const uint4 hi = lds128(slot + (((c0 + 1) ^ sw) << 4));
+            const bool have = mbar_wait(code_full(cst), static_cast<uint32_t>((kb >> 2) / kCodeStages) & 1u);
+            if (!__all_sync(0xffffffffu, have)) { ok = false; break; }
+            const uint32_t chunk = static_cast<uint32_t>(2 * (sub & 1) + half);
+            const uint4 q = lds128(code_base + cst * kCodeStageBytes + (sub >> 1) * (kBN * 64) + row_off +
+                                   ((chunk ^ sw) << 4));
             mbar_arrive(code_empty(cst));
-            if (!mbar_wait(empty(s), (r & 1u) ^ 1u)) {
-                ok = false;
-                break;
-            }
+            const bool free_stage = mbar_wait(empty(s), (r & 1u) ^ 1u);
+            if (!__all_sync(0xffffffffu, free_stage)) { ok = false; break; }
+            tc_fence_after();
             const uint32_t d2bits = dbits | (dbits << 16);
             const __nv_bfloat162 d2 = *reinterpret_cast<const __nv_bfloat162*>(&d2bits);
-            const uint32_t words[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-            uint8_t* a_row = gbase + (a_base - base) + s * kATileBytes;
+            const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+            uint32_t v[16];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint4 v;
-                v.x = deq_pair(words[c], 0, d2);
-                v.y = deq_pair(words[c], 1, d2);
-                v.z = deq_pair(words[c], 2, d2);
-                v.w = deq_pair(words[c], 3, d2);
-                *reinterpret_cast<uint4*>(a_row + sw128_offset(t, c)) = v;
-            }
-            fence_async_smem();
+            for (int w = 0; w < 4; ++w)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) v[4 * w + i] = deq_pair(words[w], i, d2);
+            tmem_st16(lane_base + kColA + 32u * s + 16u * half, v);
+            tmem_wait_st();
+            tc_fence_before();
             mbar_arrive(full_a(s));
         }
         if (!ok) record_status(args.status, kStatusTimeout);
@@ -237,24 +242,26 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
         const bool acc_ready = ok && __all_sync(0xffffffffu, mbar_wait(accum_bar, 0));
         if (acc_ready) {
             tc_fence_after();
-            const int q = warp & 3;  // TMEM lane quarter this warp may access
-            const int rowt = q * 32 + lane;
-            const int64_t ny = n0 + rowt;
-            const uint32_t taddr = tmem_d + (static_cast<uint32_t>(q * 32) << 16);
-            // With a split, the fp32 partial goes to shared memory (the ring is
-            // idle now) as red[column][row], for the cluster reduction below.
+            const int64_t ny = n0 + t;
+            // With a split, the fp32 partial goes to shared memory (the rings
+            // are idle now) as red[column][row], for the cluster reduction below.
             float* red = reinterpret_cast<float*>(gbase);
-            for (int c0 = 0; c0 < bm; c0 += 16) {
+            // The two warps of a lane quarter take the columns below / from cmid.
+            const int cmid = (bm >> 5) << 4;
+            const int cbeg = half == 0 ? 0 : cmid;
+            const int cend = half == 0 ? cmid : bm;
+            for (int c0 = cbeg; c0 < cend; c0 += 16) {
                 uint32_t v[16];
-                tmem_ld16(taddr + c0, v);
+                tmem_ld16(lane_base + static_cast<uint32_t>(c0), v);
                 if (split > 1) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) red[(c0 + j) * kBN + rowt] = __uint_as_float(v[j]);
+                    for (int j = 0; j < 16; ++j) red[(c0 + j) * kBN + t] = __uint_as_float(v[j]);
                 } else if (ny < args.N) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int64_t m = m0 + c0 + j;
-                        if (m < args.M) args.y[m * args.N + ny] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                        if (m < args.M)
+                            args.y[m * args.N + ny] = __float2bfloat16_rn(__uint_as_float(v[j]));
                     }
                 }
             }
@@ -291,7 +298,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
         // MMAs still in flight (after an abort) must finish before TMEM is freed.
         if (lane == 0) mbar_wait(accum_bar, 0);
         __syncwarp();
-        tmem_dealloc(tmem_d, tmem_cols);
+        tmem_dealloc(tmem_d, kTmemCols);
     }
 }
 
@@ -360,8 +367,10 @@ cudaError_t encode_x_stage_map(CUtensorMap* map, const void* x, int64_t M, int64
 namespace {
 
 int smem_bytes(int bm) {
-    return kStages * (kATileBytes + bm * 128) + kCodeStages * kCodeStageBytes + 8 * (3 * kStages + 2 * kCodeStages + 2) +
-           1024;
+    const int need = kStages * bm * 128 + kCodeStages * kCodeStageBytes + 8 * (3 * kStages + 2 * kCodeStages + 2) + 1024;
+    const int red = bm * kBN * 4 + 1024;  // split-K partials reuse the rings
+    const int n = need > red ? need : red;
+    return n > kMinSmemBytes ? n : kMinSmemBytes;
 }
 
 }  // namespace
@@ -430,7 +439,6 @@ cudaError_t launch_gemm_tc(const void* x, int64_t M, int64_t N, int64_t K, const
     }
 
     TcArgs args;
-    args.packed = static_cast<const uint8_t*>(packed);
     args.scales = static_cast<const uint16_t*>(scales);
     args.y = static_cast<__nv_bfloat16*>(y);
     args.M = M;
