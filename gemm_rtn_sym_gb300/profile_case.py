@@ -1,0 +1,63 @@
+"""Run one small, self-checking case of a single kernel, for a profiler.
+
+    python -m gemm_rtn_sym_gb300.profile_case quantize --workload outlier
+    python -m gemm_rtn_sym_gb300.profile_case gemm --workload outlier --M 8
+    python -m gemm_rtn_sym_gb300.profile_case gemm --workload layer70b --matrix 2 --M 208
+
+The inputs are the seeded synthetic matrices of ``workloads``.  For ``gemm`` the
+weights are quantised first (one quantiser launch), then the matmul runs
+``--launches`` times on the same inputs.  The case checks the device status
+word at the end and exits non-zero if any wait timed out.  It times nothing:
+numbers taken under a profiler are not benchmark results.
+"""
+from __future__ import annotations
+
+import argparse
+import sys
+
+import torch
+
+from . import W4_PATH_AUTO, W4_PATH_SMALL_M, W4_PATH_TENSOR
+from . import load, w4_gemm_ex, w4_last_device_status, w4_quantize_rtn
+from . import workloads as wl
+
+PATHS = {"auto": W4_PATH_AUTO, "small": W4_PATH_SMALL_M, "tensor": W4_PATH_TENSOR}
+
+
+def main(argv=None) -> int:
+    p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    p.add_argument("kernel", choices=["quantize", "gemm"])
+    p.add_argument("--workload", default="outlier", choices=sorted(wl.SHAPES))
+    p.add_argument("--matrix", type=int, default=0, help="index into the workload's matrices")
+    p.add_argument("--M", type=int, default=8, help="token rows of x (gemm)")
+    p.add_argument("--path", default="auto", choices=sorted(PATHS))
+    p.add_argument("--launches", type=int, default=3)
+    a = p.parse_args(argv)
+
+    load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    N, K = wl.SHAPES[a.workload][a.matrix]
+    W = wl.weight(a.workload, a.matrix, device=dev)
+    packed = torch.empty((N, K // 2), dtype=torch.uint8, device=dev)
+    scales = torch.empty((N, K // 128), dtype=torch.bfloat16, device=dev)
+    if a.kernel == "quantize":
+        for _ in range(a.launches):
+            w4_quantize_rtn(W, packed=packed, scales=scales)
+        what = f"quantize {a.workload}[{a.matrix}] {N}x{K}"
+    else:
+        w4_quantize_rtn(W, packed=packed, scales=scales)
+        del W
+        x = wl.activations(a.workload, a.M, K, a.matrix, device=dev)
+        y = torch.empty((a.M, N), dtype=torch.bfloat16, device=dev)
+        for _ in range(a.launches):
+            w4_gemm_ex(x, packed, scales, out=y, path=PATHS[a.path])
+        what = f"gemm {a.workload}[{a.matrix}] M={a.M} N={N} K={K} path={a.path}"
+    torch.cuda.synchronize()
+    status = w4_last_device_status(dev)
+    print(f"{what}: {a.launches} launches, device status {status}")
+    return 0 if status == 0 else 1
+
+
+if __name__ == "__main__":
+    sys.exit(main())
