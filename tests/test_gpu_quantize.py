@@ -56,6 +56,20 @@ def test_every_quotient_and_tie(cuda_lib):
     check_quantize(Wc, packed, scales)
 
 
+@pytest.mark.parametrize("offset_elems", [8, 16])
+def test_input_alignment_variants(cuda_lib, offset_elems):
+    """W at a 16-byte (not 32-byte) offset takes the 16-byte-load variant; both
+    variants must give the oracle's bytes, on the tie/range matrix too."""
+    for W in (wl.random_bf16((129, 1152), 0.02, seed=7, device=DEV), tie_and_range_matrix().to(DEV)):
+        N, K = W.shape
+        flat = torch.empty(N * K + 64, dtype=torch.bfloat16, device=DEV)
+        Wv = flat[offset_elems:offset_elems + N * K].view(N, K)
+        Wv.copy_(W)
+        assert Wv.data_ptr() % 16 == 0
+        packed, scales = quantize_gpu(cuda_lib, Wv)
+        check_quantize(W.cpu(), packed, scales)
+
+
 def test_special_groups(cuda_lib):
     W = torch.zeros((6, 256), dtype=torch.float32)
     W[1, :] = -0.375                       # all equal
