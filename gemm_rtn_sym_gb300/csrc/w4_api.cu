@@ -106,13 +106,17 @@ int w4_gemm_path_for(int64_t M, int64_t N, int64_t K) {
     return M >= kTensorMinM ? W4_PATH_TENSOR : W4_PATH_SMALL_M;
 }
 
-int w4_gemm_ex(const void* x, int64_t M, int64_t N, int64_t K, const void* packed, const void* scales,
-               void* y, void* stream, int32_t path) {
+namespace {
+
+int gemm_impl(const void* x, int64_t M, int64_t N, int64_t K, const void* packed, const void* scales, void* y,
+              void* stream, int32_t path) {
     if (M < 0) return W4_ERR_INVALID_ARG;
     if (const int s = check_sizes(N, K)) return s;
     if (M > 0 && K > (int64_t{1} << 62) / M) return W4_ERR_INVALID_ARG;
     if (M > 0 && N > (int64_t{1} << 62) / M) return W4_ERR_INVALID_ARG;
     if (path < W4_PATH_AUTO || path > W4_PATH_TENSOR) return W4_ERR_INVALID_ARG;
+    // Tensor-map coordinates are 32-bit.
+    if (N > INT32_MAX || K > INT32_MAX || M > INT32_MAX) return W4_ERR_UNSUPPORTED;
     if (M == 0 || N == 0) return W4_OK;
     if (!y) return W4_ERR_INVALID_ARG;
     if (!aligned(y, 2)) return W4_ERR_MISALIGNED;
@@ -135,9 +139,16 @@ int w4_gemm_ex(const void* x, int64_t M, int64_t N, int64_t K, const void* packe
     return to_status(launch_gemv(x, M, N, K, packed, scales, y, *dev, st));
 }
 
+}  // namespace
+
+int w4_gemm_ex(const void* x, int64_t M, int64_t N, int64_t K, const void* packed, const void* scales,
+               void* y, void* stream, int32_t path) {
+    return gemm_impl(x, M, N, K, packed, scales, y, stream, path);
+}
+
 int w4_gemm(const void* x, int64_t M, int64_t N, int64_t K, const void* packed, const void* scales,
             void* y, void* stream) {
-    return w4_gemm_ex(x, M, N, K, packed, scales, y, stream, W4_PATH_AUTO);
+    return gemm_impl(x, M, N, K, packed, scales, y, stream, W4_PATH_AUTO);
 }
 
 int w4_last_device_status(void* stream) {

@@ -109,6 +109,15 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
 }
 
 // ------------------------------------------------------------ bf16 helpers
+// Programmatic dependent launch: let the next kernel on the stream start its
+// prologue now, and wait until the previous one has finished (and its writes
+// are visible) before touching global memory.  No-ops without the launch
+// attribute.
+__device__ __forceinline__ void pdl_start() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 

@@ -129,6 +129,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_start();
     const uint32_t tmem_d = *tmem_slot_ptr;
 
     bool ok = true;
@@ -217,10 +218,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             const uint32_t chunk = static_cast<uint32_t>(2 * (sub & 1) + half);
             const uint4 q = lds128(code_base + cst * kCodeStageBytes + (sub >> 1) * (kBN * 64) + row_off +
                                    ((chunk ^ sw) << 4));
-            mbar_arrive(code_empty(cst));
-            const bool free_stage = mbar_wait(empty(s), (r & 1u) ^ 1u);
-            if (!__all_sync(0xffffffffu, free_stage)) { ok = false; break; }
-            tc_fence_after();
             const uint32_t d2bits = dbits | (dbits << 16);
             const __nv_bfloat162 d2 = *reinterpret_cast<const __nv_bfloat162*>(&d2bits);
             const uint32_t words[4] = {q.x, q.y, q.z, q.w};
@@ -229,6 +226,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             for (int w = 0; w < 4; ++w)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) v[4 * w + i] = deq_pair(words[w], i, d2);
+            // The code slot is released only once its words have been used: the
+            // shared-memory load may still be pending when an arrive executes,
+            // and the next TMA copy into the slot must not overtake it.
+            mbar_arrive(code_empty(cst));
+            const bool free_stage = mbar_wait(empty(s), (r & 1u) ^ 1u);
+            if (!__all_sync(0xffffffffu, free_stage)) { ok = false; break; }
+            tc_fence_after();
             tmem_st16(lane_base + kColA + 32u * s + 16u * half, v);
             tmem_wait_st();
             tc_fence_before();
@@ -452,13 +456,15 @@ cudaError_t launch_gemm_tc(const void* x, int64_t M, int64_t N, int64_t K, const
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = static_cast<unsigned>(split);
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, tmap, tmap_codes, args);
 }
 

@@ -97,6 +97,76 @@ __device__ __forceinline__ uint32_t biased_pair(uint32_t word) {
 
 constexpr uint32_t kMinus136x2 = 0xC308C308u;  // bf16x2 (−136, −136)
 
+// Activation fragments of one stage: token rows mt·8 + gid, the 64 contiguous
+// bytes (32 k) of this lane's part of the group, from the 128-byte-swizzled
+// [k-block][row][128 B] tile.
+template <int MT, int kXRows>
+__device__ __forceinline__ void load_x_frags(uint32_t (&xw)[MT][16], uint32_t st_x_blk, int gid, int tig) {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+        const int r = mt * 8 + gid;
+        const uint32_t rowa = st_x_blk + r * 128;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const uint32_t c = static_cast<uint32_t>(4 * (tig & 1) + v);
+            const uint4 q = lds128(rowa + ((c ^ static_cast<uint32_t>(r & 7)) << 4));
+            xw[mt][4 * v + 0] = q.x;
+            xw[mt][4 * v + 1] = q.y;
+            xw[mt][4 * v + 2] = q.z;
+            xw[mt][4 * v + 3] = q.w;
+        }
+    }
+}
+
+// One group of one stage for TPW row tiles: acc += d · (Σ (136 + q)·x − 136·Σx).
+template <int MT, int TPW>
+__device__ __forceinline__ void group_math(float (&acc)[TPW][MT][4], const uint32_t (&xw)[MT][16],
+                                           const uint4 (&wv)[TPW][2], const uint32_t (&dbits)[TPW][2]) {
+    // −136·Σ_k x[m, k] over this group, identical for every row.
+    float corr[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) corr[mt][r] = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            mma_bf16_16816(corr[mt], kMinus136x2, kMinus136x2, kMinus136x2, kMinus136x2, xw[mt][2 * k],
+                           xw[mt][2 * k + 1]);
+    }
+#pragma unroll
+    for (int rt = 0; rt < TPW; ++rt) {
+        float cg[MT][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) cg[mt][r] = corr[mt][r];
+        const uint32_t wa[4] = {wv[rt][0].x, wv[rt][0].y, wv[rt][0].z, wv[rt][0].w};
+        const uint32_t wb[4] = {wv[rt][1].x, wv[rt][1].y, wv[rt][1].z, wv[rt][1].w};
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            // k-steps 2w (pairs 0, 1 of word w) and 2w+1 (pairs 2, 3).
+            const uint32_t a0 = biased_pair<0>(wa[w]), a2 = biased_pair<1>(wa[w]);
+            const uint32_t a1 = biased_pair<0>(wb[w]), a3 = biased_pair<1>(wb[w]);
+            const uint32_t b0 = biased_pair<2>(wa[w]), b2 = biased_pair<3>(wa[w]);
+            const uint32_t b1 = biased_pair<2>(wb[w]), b3 = biased_pair<3>(wb[w]);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                mma_bf16_16816(cg[mt], a0, a1, a2, a3, xw[mt][4 * w], xw[mt][4 * w + 1]);
+                mma_bf16_16816(cg[mt], b0, b1, b2, b3, xw[mt][4 * w + 2], xw[mt][4 * w + 3]);
+            }
+        }
+        const float da = bf16_lo(dbits[rt][0]);
+        const float db = bf16_lo(dbits[rt][1]);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            acc[rt][mt][0] = fmaf(da, cg[mt][0], acc[rt][mt][0]);
+            acc[rt][mt][1] = fmaf(da, cg[mt][1], acc[rt][mt][1]);
+            acc[rt][mt][2] = fmaf(db, cg[mt][2], acc[rt][mt][2]);
+            acc[rt][mt][3] = fmaf(db, cg[mt][3], acc[rt][mt][3]);
+        }
+    }
+}
+
 struct GemvArgs {
     const uint16_t* scales;
     __nv_bfloat16* y;
@@ -145,6 +215,7 @@ gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_cons
         fence_async_smem();
     }
     __syncthreads();
+    pdl_start();
 
     bool ok = true;
     float acc[TPW][MT][4];
@@ -224,72 +295,19 @@ gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_cons
             uint32_t xw[MT][16];
             uint4 wv[TPW][2];
             if (active) {
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    const int r = mt * 8 + gid;
-                    const uint32_t rowa = st + x_blk + r * 128;
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const uint32_t c = static_cast<uint32_t>(4 * (tig & 1) + v);
-                        const uint4 q = lds128(rowa + ((c ^ static_cast<uint32_t>(r & 7)) << 4));
-                        xw[mt][4 * v + 0] = q.x;
-                        xw[mt][4 * v + 1] = q.y;
-                        xw[mt][4 * v + 2] = q.z;
-                        xw[mt][4 * v + 3] = q.w;
-                    }
-                }
+                load_x_frags<MT, C::kXRows>(xw, st + x_blk, gid, tig);
 #pragma unroll
                 for (int rt = 0; rt < TPW; ++rt) {
                     wv[rt][0] = lds128(st + w_off + rt * 16 * 64);
                     wv[rt][1] = lds128(st + w_off + rt * 16 * 64 + 8 * 64);
                 }
             }
+            // Release the stage only after its fragments have been used: the
+            // shared-memory loads may still be pending when an arrive executes,
+            // and the next TMA copy into this stage must not overtake them
+            // (releasing right after the loads gave rare corrupted fragments).
+            if (active) group_math<MT, TPW>(acc, xw, wv, d_cur);
             mbar_arrive(empty(s));
-            if (!active) continue;
-
-            // −136·Σ_k x[m, k] over this group, identical for every row.
-            float corr[MT][4];
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-                for (int r = 0; r < 4; ++r) corr[mt][r] = 0.0f;
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    mma_bf16_16816(corr[mt], kMinus136x2, kMinus136x2, kMinus136x2, kMinus136x2,
-                                   xw[mt][2 * k], xw[mt][2 * k + 1]);
-            }
-#pragma unroll
-            for (int rt = 0; rt < TPW; ++rt) {
-                float cg[MT][4];
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) cg[mt][r] = corr[mt][r];
-                const uint32_t wa[4] = {wv[rt][0].x, wv[rt][0].y, wv[rt][0].z, wv[rt][0].w};
-                const uint32_t wb[4] = {wv[rt][1].x, wv[rt][1].y, wv[rt][1].z, wv[rt][1].w};
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    // k-steps 2w (pairs 0, 1 of word w) and 2w+1 (pairs 2, 3).
-                    const uint32_t a0 = biased_pair<0>(wa[w]), a2 = biased_pair<1>(wa[w]);
-                    const uint32_t a1 = biased_pair<0>(wb[w]), a3 = biased_pair<1>(wb[w]);
-                    const uint32_t b0 = biased_pair<2>(wa[w]), b2 = biased_pair<3>(wa[w]);
-                    const uint32_t b1 = biased_pair<2>(wb[w]), b3 = biased_pair<3>(wb[w]);
-#pragma unroll
-                    for (int mt = 0; mt < MT; ++mt) {
-                        mma_bf16_16816(cg[mt], a0, a1, a2, a3, xw[mt][4 * w], xw[mt][4 * w + 1]);
-                        mma_bf16_16816(cg[mt], b0, b1, b2, b3, xw[mt][4 * w + 2], xw[mt][4 * w + 3]);
-                    }
-                }
-                const float da = bf16_lo(d_cur[rt][0]);
-                const float db = bf16_lo(d_cur[rt][1]);
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    acc[rt][mt][0] = fmaf(da, cg[mt][0], acc[rt][mt][0]);
-                    acc[rt][mt][1] = fmaf(da, cg[mt][1], acc[rt][mt][1]);
-                    acc[rt][mt][2] = fmaf(db, cg[mt][2], acc[rt][mt][2]);
-                    acc[rt][mt][3] = fmaf(db, cg[mt][3], acc[rt][mt][3]);
-                }
-            }
         }
         if (!ok) record_status(args.status, kStatusTimeout);
     }
@@ -371,9 +389,9 @@ cudaError_t launch_mt(const __nv_bfloat16* x, int mp, int64_t N, int64_t K, cons
     const int64_t row_blocks = (N + kRowsCta - 1) / kRowsCta;
     if (row_blocks > 0x7fffffffLL || K > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
 
-    // Split-K factor: the cluster size (1..8, at most G) that finishes the row
-    // blocks in the fewest rounds of stage work, given how many clusters of
-    // that size can be resident at once.
+    // Split-K factor: the cluster size (1..8, at most G) with the least
+    // modelled time, given how many clusters of that size can be resident at
+    // once.
     int64_t split = 1;
     double best = 0.0;
     for (int s = 1; s <= kMaxSplit && s <= G; ++s) {
@@ -395,7 +413,10 @@ cudaError_t launch_mt(const __nv_bfloat16* x, int mp, int64_t N, int64_t K, cons
         }
         const int64_t waves = (row_blocks + clusters - 1) / clusters;
         const int64_t stages = ((G + s - 1) / s + kStageGroups - 1) / kStageGroups;
-        const double cost = static_cast<double>(waves) * static_cast<double>(stages);
+        // Per CTA: its stages plus a fixed part (pipeline fill, epilogue) that
+        // grows with the cluster reduction; fitted to timings of the layer
+        // shapes on GB300 (in units of one stage, about 1.1 us).
+        const double cost = static_cast<double>(waves) * (static_cast<double>(stages) + 0.5 + 0.6 * (s - 1));
         if (best == 0.0 || cost < best) {
             best = cost;
             split = s;
@@ -417,13 +438,15 @@ cudaError_t launch_mt(const __nv_bfloat16* x, int mp, int64_t N, int64_t K, cons
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = static_cast<unsigned>(split);
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, gemv_w4_kernel<MT, TPW>, tmap_codes, tmap_x, args);
 }
 

@@ -234,6 +234,7 @@ quantize_rtn_kernel(const uint8_t* __restrict__ W, uint4* __restrict__ packed,
     // l's quarter group, chunks c..c+3 with c = 128·unit + 4·l, is in range for
     // all four lanes of its group or for none (n_chunks is a multiple of 16).
     const int64_t n_units = (n_chunks + 127) >> 7;
+    pdl_start();
     int64_t u = warp;
     if (u >= n_units) return;
     const int64_t stride = n_warps << 7;  // chunks between a warp's units
@@ -276,9 +277,17 @@ cudaError_t launch_quantize_t(const void* W, int64_t n_chunks, void* packed, voi
     const int64_t cap = static_cast<int64_t>(dev.sm_count) * occ;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    quantize_rtn_kernel<kWide><<<static_cast<unsigned>(blocks), kQuantThreads, 0, stream>>>(
-        static_cast<const uint8_t*>(W), static_cast<uint4*>(packed), static_cast<__nv_bfloat16*>(scales), n_chunks);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+    cfg.blockDim = dim3(kQuantThreads, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, quantize_rtn_kernel<kWide>, static_cast<const uint8_t*>(W),
+                              static_cast<uint4*>(packed), static_cast<__nv_bfloat16*>(scales), n_chunks);
 }
 
 }  // namespace

@@ -44,7 +44,8 @@
  *    Work is enqueued asynchronously on it; nothing synchronises, except
  *    w4_last_device_status().
  *  - K must be a multiple of 128 and group must be 128; N, M, K ≥ 0.  Sizes
- *    with N·K ≥ 2^62 are rejected.
+ *    with N·K ≥ 2^62 are rejected; the matmul also needs N, M, K < 2^31
+ *    (W4_ERR_UNSUPPORTED otherwise).
  *  - W, x and packed must be 16-byte aligned; scales and y 2-byte aligned.
  *  - y must not overlap x, packed or scales; packed/scales must not overlap W.
  *  - Argument errors are returned synchronously before anything is launched.
@@ -76,8 +77,9 @@ typedef enum w4_gemm_path {
     W4_PATH_AUTO = 0,    /* what w4_gemm does: picked from M (w4_gemm_path_for)  */
     W4_PATH_SMALL_M = 1, /* TMA-fed GEMV: register nibble decode, legacy MMA,
                             cluster split-K; any M (16 token rows per pass)     */
-    W4_PATH_TENSOR = 2   /* tcgen05 tile: weights dequantised into shared
-                            memory, TMEM accumulators; any M ≥ 1                */
+    W4_PATH_TENSOR = 2   /* tcgen05 tile: weights dequantised into tensor
+                            memory as the A operand, TMEM accumulators, cluster
+                            split-K; any M ≥ 1                                  */
 } w4_gemm_path;
 
 /* Bytes of the packed code buffer: N·K/2.  0 for invalid sizes. */

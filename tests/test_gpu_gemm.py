@@ -71,12 +71,37 @@ def test_auto_path_matches_explicit(cuda_lib):
 def test_deterministic(cuda_lib):
     W = wl.random_bf16((512, 4096), 0.02, seed=3, device=DEV)
     packed, scales = quantize_gpu(cuda_lib, W)
-    for M in (1, 8, 64):
+    for M in (1, 8, 13, 64):
         x = wl.random_bf16((M, 4096), 1.0, seed=M, device=DEV)
-        ys = [w4.w4_gemm(x, packed, scales) for _ in range(3)]
+        ys = [w4.w4_gemm(x, packed, scales) for _ in range(5)]
         torch.cuda.synchronize()
         for y in ys[1:]:
             assert torch.equal(y.view(torch.int16), ys[0].view(torch.int16))
+
+
+@pytest.mark.parametrize("N,K", [(1280, 8192), (2000, 2560), (4160, 1152), (96, 30720), (10240, 384)])
+@pytest.mark.parametrize("M", [1, 5, 13])
+def test_split_shapes(cuda_lib, N, K, M):
+    """Shapes whose split-K choice ranges from none to eight-CTA clusters,
+    with ragged row blocks and groups per CTA."""
+    W = wl.random_bf16((N, K), 0.02, seed=N + K, device=DEV)
+    x, y, _, _ = run(cuda_lib, W, M, w4.W4_PATH_SMALL_M, seed=M)
+    check_gemm(W, x, y)
+
+
+def test_repeat_is_bit_identical_mid_m(cuda_lib):
+    """Many repeats of a 16-token pass on a matrix whose row blocks are split
+    over cluster CTAs: a stage released before its fragments were read would
+    show up as an occasional difference."""
+    W = wl.random_bf16((10240, 2048), 0.02, seed=11, device=DEV)
+    packed, scales = quantize_gpu(cuda_lib, W)
+    for M in (13, 16):
+        x = wl.random_bf16((M, 2048), 1.0, seed=M, device=DEV)
+        ref = w4.w4_gemm_ex(x, packed, scales, path=w4.W4_PATH_SMALL_M)
+        ys = [w4.w4_gemm_ex(x, packed, scales, path=w4.W4_PATH_SMALL_M) for _ in range(40)]
+        torch.cuda.synchronize()
+        for y in ys:
+            assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
 
 
 def test_empty_and_degenerate(cuda_lib):
