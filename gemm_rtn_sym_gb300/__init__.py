@@ -20,6 +20,7 @@ __all__ = [
     "w4_quantize_rtn", "w4_gemm", "w4_gemm_ex", "w4_gemm_path_for",
     "w4_packed_bytes", "w4_scales_bytes", "w4_last_device_status", "w4_wait_probe",
     "w4_status_string", "W4_PATH_AUTO", "W4_PATH_SMALL_M", "W4_PATH_TENSOR", "GROUP",
+    "GroupedPlan", "w4_grouped_plan", "w4_gemm_grouped",
 ]
 
 GROUP = 128
@@ -31,6 +32,18 @@ _lib = None
 _lock = threading.Lock()
 
 _i64, _i32, _vp, _sz = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t
+
+
+class _Problem(ctypes.Structure):
+    """w4_gemm_problem of include/w4.h."""
+    _fields_ = [("x", _vp), ("M", _i64), ("N", _i64), ("K", _i64), ("packed", _vp), ("scales", _vp), ("y", _vp)]
+
+
+class _Plan(ctypes.Structure):
+    """w4_grouped_plan of include/w4.h."""
+    _fields_ = [("device_plan", _vp), ("bytes", _sz), ("count", _i32), ("items", _i32), ("ctas", _i32),
+                ("token_tiles", _i32), ("device", _i32)]
+
 _SIGNATURES = {
     "w4_packed_bytes": (_sz, [_i64, _i64]),
     "w4_scales_bytes": (_sz, [_i64, _i64, _i32]),
@@ -41,6 +54,9 @@ _SIGNATURES = {
     "w4_last_device_status": (ctypes.c_int, [_vp]),
     "w4_wait_probe": (ctypes.c_int, [_i64, _i32, _vp]),
     "w4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "w4_grouped_plan_bytes": (_sz, [_i32, ctypes.POINTER(_Problem)]),
+    "w4_grouped_plan_init": (ctypes.c_int, [ctypes.POINTER(_Plan), _vp, _sz, _i32, ctypes.POINTER(_Problem)]),
+    "w4_gemm_grouped": (ctypes.c_int, [ctypes.POINTER(_Plan), _vp]),
 }
 
 
@@ -154,6 +170,66 @@ def w4_gemm_ex(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
 def w4_gemm(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
             out: torch.Tensor | None = None) -> torch.Tensor:
     return w4_gemm_ex(x, packed, scales, out, W4_PATH_AUTO)
+
+
+class GroupedPlan:
+    """A built grouped-matmul plan: the device memory holding it (a torch
+    tensor) and the C descriptor.  Keeps the problems' tensors referenced, since
+    the plan records their addresses."""
+
+    def __init__(self, memory: torch.Tensor, plan: _Plan, tensors: list):
+        self.memory = memory
+        self.plan = plan
+        self.tensors = tensors
+
+    @property
+    def items(self) -> int:
+        return self.plan.items
+
+
+def w4_grouped_plan(problems) -> GroupedPlan:
+    """Plan for many small-M matmuls y_i = Ŵ_i x_i run by one w4_gemm_grouped
+    launch.  problems: sequence of (x, packed, scales, y) CUDA tensors with the
+    shapes of w4_gemm (1 ≤ M ≤ 16), all on one device."""
+    problems = list(problems)
+    if not problems:
+        raise ValueError("no problems")
+    arr = (_Problem * len(problems))()
+    tensors = []
+    device = problems[0][0].device
+    for i, (x, packed, scales, y) in enumerate(problems):
+        _cuda_tensor(x, "x", torch.bfloat16, 2)
+        _cuda_tensor(packed, "packed", torch.uint8, 2)
+        _cuda_tensor(scales, "scales", torch.bfloat16, 2)
+        _cuda_tensor(y, "y", torch.bfloat16, 2)
+        M, K = x.shape
+        N = packed.shape[0]
+        if tuple(packed.shape) != (N, K // 2) or tuple(scales.shape) != (N, K // GROUP) or tuple(y.shape) != (M, N):
+            raise ValueError(f"problem {i}: x / packed / scales / y shapes disagree")
+        if x.device != device or packed.device != device or scales.device != device or y.device != device:
+            raise ValueError("all tensors of a plan must be on one device")
+        arr[i] = _Problem(x.data_ptr(), M, N, K, packed.data_ptr(), scales.data_ptr(), y.data_ptr())
+        tensors += [x, packed, scales, y]
+    with torch.cuda.device(device):
+        nbytes = load().w4_grouped_plan_bytes(len(problems), arr)
+        if nbytes == 0:  # some problem is invalid: let plan_init name the reason
+            probe = torch.empty(256, dtype=torch.uint8, device=device)
+            status = load().w4_grouped_plan_init(ctypes.byref(_Plan()), probe.data_ptr() + (-probe.data_ptr()) % 128,
+                                                 128, len(problems), arr)
+            raise W4Error(status if status != W4_OK else W4_ERR_INVALID_ARG, "w4_grouped_plan")
+        memory = torch.empty(nbytes + 128, dtype=torch.uint8, device=device)
+        off = (-memory.data_ptr()) % 128
+        plan = _Plan()
+        _check(load().w4_grouped_plan_init(ctypes.byref(plan), memory.data_ptr() + off, nbytes, len(problems), arr),
+               "w4_grouped_plan_init")
+    return GroupedPlan(memory, plan, tensors)
+
+
+def w4_gemm_grouped(plan: GroupedPlan) -> None:
+    """Runs every problem of the plan on the current stream of its device."""
+    device = torch.device("cuda", plan.plan.device)
+    with torch.cuda.device(device):
+        _check(load().w4_gemm_grouped(ctypes.byref(plan.plan), _stream(device)), "w4_gemm_grouped")
 
 
 def w4_last_device_status(device=None) -> int:

@@ -2,6 +2,7 @@
 // choice, launches and the per-device status word of the bounded waits.
 #include <cstdint>
 #include <mutex>
+#include <vector>
 
 #include <cuda_runtime.h>
 
@@ -149,6 +150,105 @@ int w4_gemm_ex(const void* x, int64_t M, int64_t N, int64_t K, const void* packe
 int w4_gemm(const void* x, int64_t M, int64_t N, int64_t K, const void* packed, const void* scales,
             void* y, void* stream) {
     return gemm_impl(x, M, N, K, packed, scales, y, stream, W4_PATH_AUTO);
+}
+
+namespace {
+
+// Checks one grouped problem like w4_gemm does; small-M only (1 ≤ M ≤ 16).
+int check_grouped_problem(const w4_gemm_problem& p) {
+    if (p.M < 1 || p.N < 1 || p.K < 128) return W4_ERR_INVALID_ARG;
+    if (const int s = check_sizes(p.N, p.K)) return s;
+    if (p.M > 16) return W4_ERR_UNSUPPORTED;
+    if (p.N > INT32_MAX || p.K > INT32_MAX || p.K > (int64_t{1} << 62) / p.M || p.N > (int64_t{1} << 62) / p.M)
+        return W4_ERR_UNSUPPORTED;
+    if (!p.x || !p.packed || !p.scales || !p.y) return W4_ERR_INVALID_ARG;
+    if (!aligned(p.x, 16) || !aligned(p.packed, 16) || !aligned(p.scales, 2) || !aligned(p.y, 2))
+        return W4_ERR_MISALIGNED;
+    return W4_OK;
+}
+
+size_t out_bytes(const w4_gemm_problem& p) { return static_cast<size_t>(p.M * p.N) * 2; }
+
+}  // namespace
+
+size_t w4_grouped_plan_bytes(int32_t count, const w4_gemm_problem* problems) {
+    if (count < 1 || !problems) return 0;
+    int64_t items = 0;
+    for (int32_t i = 0; i < count; ++i) {
+        if (check_grouped_problem(problems[i]) != W4_OK) return 0;
+        items += (problems[i].N + 63) / 64;
+    }
+    if (items > INT32_MAX) return 0;
+    // Sized for the largest grid a plan can use (one CTA per item), so that
+    // the answer does not depend on the device.
+    return grouped_plan_bytes(count, items, static_cast<int32_t>(items));
+}
+
+int w4_grouped_plan_init(w4_grouped_plan* plan, void* device_memory, size_t bytes, int32_t count,
+                         const w4_gemm_problem* problems) {
+    if (!plan || !device_memory || count < 1 || !problems) return W4_ERR_INVALID_ARG;
+    if (!aligned(device_memory, 128)) return W4_ERR_MISALIGNED;
+    int token_tiles = 1;
+    for (int32_t i = 0; i < count; ++i) {
+        const w4_gemm_problem& p = problems[i];
+        if (const int s = check_grouped_problem(p)) return s;
+        if (p.M > 8) token_tiles = 2;
+        const size_t yb = out_bytes(p);
+        for (int32_t j = 0; j < count; ++j) {
+            const w4_gemm_problem& q = problems[j];
+            const size_t xb = static_cast<size_t>(q.M * q.K) * 2, pb = w4_packed_bytes(q.N, q.K),
+                         sb = w4_scales_bytes(q.N, q.K, 128);
+            if (overlaps(p.y, yb, q.x, xb) || overlaps(p.y, yb, q.packed, pb) || overlaps(p.y, yb, q.scales, sb))
+                return W4_ERR_INVALID_ARG;
+            if (j != i && overlaps(p.y, yb, q.y, out_bytes(q))) return W4_ERR_INVALID_ARG;
+            if (overlaps(device_memory, bytes, q.x, xb) || overlaps(device_memory, bytes, q.packed, pb) ||
+                overlaps(device_memory, bytes, q.scales, sb) || overlaps(device_memory, bytes, q.y, out_bytes(q)))
+                return W4_ERR_INVALID_ARG;
+        }
+    }
+    cudaError_t err;
+    const DeviceInfo* dev = device_info(&err);
+    if (!dev) return W4_ERR_CUDA;
+    if (dev->cc_major < 10) return W4_ERR_UNSUPPORTED;
+    std::vector<GroupedSpec> specs(static_cast<size_t>(count));
+    for (int32_t i = 0; i < count; ++i) {
+        const w4_gemm_problem& p = problems[i];
+        specs[i] = GroupedSpec{p.x, p.M, p.N, p.K, p.packed, p.scales, p.y};
+    }
+    const int ctas = grouped_ctas(token_tiles, *dev);
+    if (ctas < 1) return W4_ERR_CUDA;
+    std::vector<uint8_t> image;
+    int64_t n_items = 0;
+    int32_t n_ctas = 0;
+    if (grouped_plan_build(specs.data(), count, token_tiles, ctas, &image, &n_items, &n_ctas) != cudaSuccess)
+        return W4_ERR_CUDA;
+    if (bytes < image.size()) return W4_ERR_INVALID_ARG;
+    if (cudaMemcpy(device_memory, image.data(), image.size(), cudaMemcpyHostToDevice) != cudaSuccess)
+        return W4_ERR_CUDA;
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return W4_ERR_CUDA;
+    plan->device_plan = device_memory;
+    plan->bytes = image.size();
+    plan->count = count;
+    plan->items = static_cast<int32_t>(n_items);
+    plan->ctas = n_ctas;
+    plan->token_tiles = token_tiles;
+    plan->device = device;
+    return W4_OK;
+}
+
+int w4_gemm_grouped(const w4_grouped_plan* plan, void* stream) {
+    if (!plan || !plan->device_plan || plan->items < 1 || plan->ctas < 1 || plan->ctas > plan->items ||
+        (plan->token_tiles != 1 && plan->token_tiles != 2))
+        return W4_ERR_INVALID_ARG;
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return W4_ERR_CUDA;
+    if (device != plan->device) return W4_ERR_INVALID_ARG;
+    cudaError_t err;
+    const DeviceInfo* dev = device_info(&err);
+    if (!dev) return W4_ERR_CUDA;
+    return to_status(launch_grouped(plan->device_plan, plan->ctas, plan->token_tiles, *dev,
+                                    static_cast<cudaStream_t>(stream)));
 }
 
 int w4_last_device_status(void* stream) {

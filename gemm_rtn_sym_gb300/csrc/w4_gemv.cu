@@ -42,130 +42,14 @@
 #include <mutex>
 
 #include "w4_device.cuh"
+#include "w4_gemv_common.cuh"
 #include "w4_internal.h"
 #include "w4_tcgen05.cuh"
 
 namespace w4 {
 namespace {
 
-constexpr int kTiles = 4;                // 16-row tiles per CTA
-constexpr int kRowsCta = 16 * kTiles;    // 64 weight rows per CTA
-constexpr int kStageGroups = 4;          // groups per stage
-constexpr int kMaxSplit = 8;
-constexpr int kTpw = 2;  // row tiles per consumer warp at M <= 8 (4 at M <= 16: fewer x fragments per tile)
-
-// TPW: row tiles per consumer warp.  Consumer warp c takes group c % 4 of every
-// stage for tiles (c / 4)·TPW .. +TPW-1, so 16 / TPW consumer warps per CTA.
-template <int TPW>
-struct Warps {
-    static constexpr int kConsumers = kStageGroups * (kTiles / TPW);
-    static constexpr int kThreads = 32 * (1 + kConsumers);
-};
-constexpr int kCodeStageBytes = kStageGroups * kRowsCta * 64;  // 16 KB: [group][row][64 B]
-
-template <int MT>
-struct Cfg {
-    static constexpr int kXRows = 8 * MT;                               // token rows staged
-    static constexpr int kXStageBytes = 2 * kStageGroups * kXRows * 128;  // [k-block][row][128 B]
-    static constexpr int kStages = MT == 1 ? 4 : 3;
-    static constexpr int kStageBytes = kCodeStageBytes + kXStageBytes;
-    // Two CTAs per SM, each with its own TMA producer (one issuing thread per
-    // SM does not reach the HBM rate with copies of this size).
-    static constexpr int kSmemBytes = kStages * kStageBytes + 2048;
-};
-
-__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                               uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// Pair i (0..3) of a stored code word as the bf16x2 value (136 + q_lo, 136 + q_hi):
-// one shift and one LOP3, no subtract.  The 136·Σx offset this adds to every
-// group sum is removed by starting the group's accumulator at −136·Σx.
-template <int I>
-__device__ __forceinline__ uint32_t biased_pair(uint32_t word) {
-    uint32_t r, t = word;
-    if (I != 0) asm("shr.b32 %0, %1, %2;" : "=r"(t) : "r"(word), "n"(4 * I));
-    // (t & 0x000F000F) ^ 0x43084308 as one three-input logic op (LUT 0x6A = (a & b) ^ c).
-    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(r) : "r"(t), "n"(0x000F000F), "r"(0x43084308u));
-    return r;
-}
-
-constexpr uint32_t kMinus136x2 = 0xC308C308u;  // bf16x2 (−136, −136)
-
-// Activation fragments of one stage: token rows mt·8 + gid, the 64 contiguous
-// bytes (32 k) of this lane's part of the group, from the 128-byte-swizzled
-// [k-block][row][128 B] tile.
-template <int MT, int kXRows>
-__device__ __forceinline__ void load_x_frags(uint32_t (&xw)[MT][16], uint32_t st_x_blk, int gid, int tig) {
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-        const int r = mt * 8 + gid;
-        const uint32_t rowa = st_x_blk + r * 128;
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            const uint32_t c = static_cast<uint32_t>(4 * (tig & 1) + v);
-            const uint4 q = lds128(rowa + ((c ^ static_cast<uint32_t>(r & 7)) << 4));
-            xw[mt][4 * v + 0] = q.x;
-            xw[mt][4 * v + 1] = q.y;
-            xw[mt][4 * v + 2] = q.z;
-            xw[mt][4 * v + 3] = q.w;
-        }
-    }
-}
-
-// One group of one stage for TPW row tiles: acc += d · (Σ (136 + q)·x − 136·Σx).
-template <int MT, int TPW>
-__device__ __forceinline__ void group_math(float (&acc)[TPW][MT][4], const uint32_t (&xw)[MT][16],
-                                           const uint4 (&wv)[TPW][2], const uint32_t (&dbits)[TPW][2]) {
-    // −136·Σ_k x[m, k] over this group, identical for every row.
-    float corr[MT][4];
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r) corr[mt][r] = 0.0f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            mma_bf16_16816(corr[mt], kMinus136x2, kMinus136x2, kMinus136x2, kMinus136x2, xw[mt][2 * k],
-                           xw[mt][2 * k + 1]);
-    }
-#pragma unroll
-    for (int rt = 0; rt < TPW; ++rt) {
-        float cg[MT][4];
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) cg[mt][r] = corr[mt][r];
-        const uint32_t wa[4] = {wv[rt][0].x, wv[rt][0].y, wv[rt][0].z, wv[rt][0].w};
-        const uint32_t wb[4] = {wv[rt][1].x, wv[rt][1].y, wv[rt][1].z, wv[rt][1].w};
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            // k-steps 2w (pairs 0, 1 of word w) and 2w+1 (pairs 2, 3).
-            const uint32_t a0 = biased_pair<0>(wa[w]), a2 = biased_pair<1>(wa[w]);
-            const uint32_t a1 = biased_pair<0>(wb[w]), a3 = biased_pair<1>(wb[w]);
-            const uint32_t b0 = biased_pair<2>(wa[w]), b2 = biased_pair<3>(wa[w]);
-            const uint32_t b1 = biased_pair<2>(wb[w]), b3 = biased_pair<3>(wb[w]);
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                mma_bf16_16816(cg[mt], a0, a1, a2, a3, xw[mt][4 * w], xw[mt][4 * w + 1]);
-                mma_bf16_16816(cg[mt], b0, b1, b2, b3, xw[mt][4 * w + 2], xw[mt][4 * w + 3]);
-            }
-        }
-        const float da = bf16_lo(dbits[rt][0]);
-        const float db = bf16_lo(dbits[rt][1]);
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-            acc[rt][mt][0] = fmaf(da, cg[mt][0], acc[rt][mt][0]);
-            acc[rt][mt][1] = fmaf(da, cg[mt][1], acc[rt][mt][1]);
-            acc[rt][mt][2] = fmaf(db, cg[mt][2], acc[rt][mt][2]);
-            acc[rt][mt][3] = fmaf(db, cg[mt][3], acc[rt][mt][3]);
-        }
-    }
-}
+using namespace gemv;
 
 struct GemvArgs {
     const uint16_t* scales;

@@ -1,0 +1,396 @@
+// Grouped small-M W4A16 matmul: many independent problems y_i = Ŵ_i x_i
+// (for example the four matrices of a transformer layer, or every matrix of a
+// stack) in one persistent launch.
+//
+// Source: Qwen3.5-4B quantisation study, §1 FFN example y = W x with ŵ = d·q
+// (one d per 128 consecutive inputs) and §2 settings (4-bit weights, BF16
+// inputs); a model applies it to every linear layer (§2: 200 quantised
+// matrices).  Each problem is computed exactly as by the single-matrix kernel
+// in w4_gemv.cu (same decode, same MMA, same per-group fp32 scaling), so the
+// results are within the same bound.
+//
+// Why: a small matrix takes only a few microseconds of streaming, and a launch
+// of its own adds the launch gap, the pipeline fill (one DRAM latency) and a
+// split-K reduction each time.  Here the work is a list of items, one per
+// (problem, 64-row block), each covering the block's whole K, so no split-K
+// is needed.  The plan fixes the grid (two CTAs per SM) and assigns the items
+// longest first, each to the CTA with the least work so far (LPT).
+// The producer warp streams the stages of a CTA's items back to back through
+// one shared-memory ring, so the pipeline fills once per CTA, not once per
+// matrix.  At the end of an item the consumer warps sum their fp32 partials in
+// shared memory in a fixed order and store y: results are deterministic.
+//
+// The plan (built once on the host, copied to device memory the caller owns)
+// holds a TMA descriptor pair per problem and the item list; the kernel reads
+// descriptors from global memory after a tensormap-proxy acquire fence.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <queue>
+#include <vector>
+
+#include "w4_device.cuh"
+#include "w4_gemv_common.cuh"
+#include "w4_internal.h"
+#include "w4_tcgen05.cuh"
+
+namespace w4 {
+namespace {
+
+using namespace gemv;
+
+// Device layout of a plan:
+//   GroupedHeader (128 B) | GroupedProblem[count] (384 B each) |
+//   int32 first[n_ctas + 1] (padded to 8 B) | uint2 items[n_items]
+// CTA c runs items[first[c] .. first[c + 1]).  Tensor maps stay 128-byte
+// aligned when the plan is.
+struct alignas(128) GroupedHeader {
+    int32_t count;
+    int32_t n_items;
+    int32_t token_tiles;  // MT: 1 (all M <= 8) or 2 (some M in 9..16)
+    int32_t n_ctas;       // the grid the plan was scheduled for
+    int32_t reserved[28];
+};
+
+struct alignas(128) GroupedProblem {
+    CUtensorMap codes;  // [G][N][64 B], boxes of 4 groups × 64 rows
+    CUtensorMap x;      // [K/64][M][64], boxes of 8 blocks × 8·MT rows, 128-byte swizzle
+    const uint16_t* scales;
+    __nv_bfloat16* y;
+    int64_t N;
+    int32_t M;
+    int32_t G;
+    int32_t T;  // stages per item
+    int32_t reserved[23];
+};
+static_assert(sizeof(GroupedHeader) == 128, "plan header");
+static_assert(sizeof(GroupedProblem) == 384, "plan problem record");
+
+__device__ __forceinline__ void tensormap_acquire(const void* map) {
+    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
+}
+
+__device__ __forceinline__ void consumer_sync(int n_threads) {
+    asm volatile("bar.sync 1, %0;" ::"r"(n_threads) : "memory");
+}
+
+template <int MT, int TPW>
+__global__ void __launch_bounds__(Warps<TPW>::kThreads, 2)
+gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
+    using C = Cfg<MT>;
+    constexpr int kConsumers = Warps<TPW>::kConsumers;
+    constexpr int kCThreads = 32 * kConsumers;
+    constexpr int kRedFloats = kStageGroups * kTiles * 4 * 32;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    float* red = reinterpret_cast<float*>(gbase + C::kStages * C::kStageBytes);
+    const uint32_t bar_base = base + C::kStages * C::kStageBytes + kRedFloats * 4;
+    auto full = [&](int s) { return bar_base + 8u * s; };
+    auto empty = [&](int s) { return bar_base + 8u * (C::kStages + s); };
+
+    const GroupedHeader* hdr = reinterpret_cast<const GroupedHeader*>(plan);
+    const GroupedProblem* probs = reinterpret_cast<const GroupedProblem*>(plan + sizeof(GroupedHeader));
+    const int count = hdr->count;
+    const int32_t* first = reinterpret_cast<const int32_t*>(plan + sizeof(GroupedHeader) + sizeof(GroupedProblem) * count);
+    const uint2* items = reinterpret_cast<const uint2*>(first + ((hdr->n_ctas + 2) & ~1));
+    const int i_begin = first[blockIdx.x];
+    const int i_end = first[blockIdx.x + 1];
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int gid = lane >> 2;
+    const int tig = lane & 3;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 32 * kConsumers);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_async_smem();
+    }
+    __syncthreads();
+    pdl_start();
+
+    if (warp == 0) {
+        // -------------------------------------------------- producer: stages of every item, back to back
+        if (lane == 0) {
+            int s = 0;
+            uint32_t phase = 0;
+            int issued = 0;  // stages issued
+            bool ok = true;
+            for (int i = i_begin; i < i_end && ok; ++i) {
+                const uint2 it = items[i];
+                const GroupedProblem* pr = probs + it.x;
+                tensormap_acquire(&pr->codes);
+                tensormap_acquire(&pr->x);
+                const int row = static_cast<int>(it.y) * kRowsCta;
+                for (int t = 0; t < pr->T; ++t) {
+                    if (!mbar_wait(empty(s), phase ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t st = base + s * C::kStageBytes;
+                    mbar_arrive_expect_tx(full(s), C::kStageBytes);
+                    tma_load_3d(st, &pr->codes, 0, row, t * kStageGroups, full(s));
+                    tma_load_3d(st + kCodeStageBytes, &pr->x, 0, 0, 2 * kStageGroups * t, full(s));
+                    ++issued;
+                    if (++s == C::kStages) {
+                        s = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                record_status(status, kStatusTimeout);
+                // Drain: every issued copy lands before the CTA may exit.
+                for (int j = issued > C::kStages ? issued - C::kStages : 0; j < issued; ++j)
+                    mbar_wait(full(j % C::kStages), static_cast<uint32_t>(j / C::kStages) & 1u);
+            }
+        }
+        return;
+    }
+
+    // ------------------------------------------------------ consumers
+    // Every consumer warp runs the same sequence of items, stages and named
+    // barriers; after a timed-out wait a warp only skips work.
+    const int ctid = threadIdx.x - 32;
+    const int cw = (warp - 1) % kStageGroups;
+    const int tile0 = ((warp - 1) / kStageGroups) * TPW;
+    const uint32_t w_off = static_cast<uint32_t>(cw * kRowsCta * 64 + (tile0 * 16 + gid) * 64 + tig * 16);
+    const uint32_t x_blk = static_cast<uint32_t>(kCodeStageBytes + (2 * cw + (tig >> 1)) * C::kXRows * 128);
+
+    int s = 0;
+    uint32_t phase = 0;
+    bool aborted = false;
+    for (int i = i_begin; i < i_end; ++i) {
+        const uint2 it = items[i];
+        const GroupedProblem* pr = probs + it.x;
+        const int T = pr->T;
+        const int G = pr->G;
+        const int64_t N = pr->N;
+        const int M = pr->M;
+        const int64_t row0 = static_cast<int64_t>(it.y) * kRowsCta;
+        // Scale rows gid / gid+8 of each tile (clamped: rows past N have zero codes).
+        const uint16_t* srow[TPW][2];
+#pragma unroll
+        for (int rt = 0; rt < TPW; ++rt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                int64_t n = row0 + (tile0 + rt) * 16 + gid + 8 * h;
+                if (n >= N) n = N - 1;
+                srow[rt][h] = pr->scales + n * G;
+            }
+        float acc[TPW][MT][4];
+#pragma unroll
+        for (int rt = 0; rt < TPW; ++rt)
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) acc[rt][mt][r] = 0.0f;
+        uint32_t d_nxt[TPW][2];
+        auto load_scales = [&](int t) {
+            const int g = t * kStageGroups + cw;
+#pragma unroll
+            for (int rt = 0; rt < TPW; ++rt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) d_nxt[rt][h] = (t < T && g < G) ? __ldg(srow[rt][h] + g) : 0u;
+        };
+        load_scales(0);
+        for (int t = 0; t < T; ++t) {
+            uint32_t d_cur[TPW][2];
+#pragma unroll
+            for (int rt = 0; rt < TPW; ++rt) {
+                d_cur[rt][0] = d_nxt[rt][0];
+                d_cur[rt][1] = d_nxt[rt][1];
+            }
+            load_scales(t + 1);
+            if (!aborted) {
+                aborted = !__all_sync(0xffffffffu, mbar_wait(full(s), phase));
+                if (aborted && lane == 0) record_status(status, kStatusTimeout);
+            }
+            if (!aborted) {
+                const bool active = t * kStageGroups + cw < G;  // warp-uniform
+                if (active) {
+                    const uint32_t st = base + s * C::kStageBytes;
+                    uint32_t xw[MT][16];
+                    uint4 wv[TPW][2];
+                    load_x_frags<MT, C::kXRows>(xw, st + x_blk, gid, tig);
+#pragma unroll
+                    for (int rt = 0; rt < TPW; ++rt) {
+                        wv[rt][0] = lds128(st + w_off + rt * 16 * 64);
+                        wv[rt][1] = lds128(st + w_off + rt * 16 * 64 + 8 * 64);
+                    }
+                    // Release the stage only after its fragments have been used
+                    // (shared-memory loads may still be pending when an arrive
+                    // executes; the next TMA copy must not overtake them).
+                    group_math<MT, TPW>(acc, xw, wv, d_cur);
+                }
+                mbar_arrive(empty(s));
+            }
+            if (++s == C::kStages) {
+                s = 0;
+                phase ^= 1u;
+            }
+        }
+        // The item's sum: warp partials through shared memory, added in warp order.
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            consumer_sync(kCThreads);  // the previous readers of red are done
+#pragma unroll
+            for (int rt = 0; rt < TPW; ++rt)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) red[((cw * kTiles + tile0 + rt) * 4 + r) * 32 + lane] = acc[rt][mt][r];
+            consumer_sync(kCThreads);
+            for (int e = ctid; e < kTiles * 4 * 32; e += kCThreads) {
+                const int l = e & 31;
+                const int r = (e >> 5) & 3;
+                const int rt = e >> 7;
+                float v = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kStageGroups; ++w) v += red[((w * kTiles + rt) * 4 + r) * 32 + l];
+                const int m = mt * 8 + 2 * (l & 3) + (r & 1);
+                const int64_t n = row0 + rt * 16 + (l >> 2) + (r >= 2 ? 8 : 0);
+                if (!aborted && n < N && m < M) pr->y[static_cast<int64_t>(m) * N + n] = __float2bfloat16_rn(v);
+            }
+        }
+    }
+}
+
+template <int MT, int TPW>
+constexpr int grouped_smem_bytes() {
+    return Cfg<MT>::kStages * Cfg<MT>::kStageBytes + kStageGroups * kTiles * 4 * 32 * 4 + 16 * Cfg<MT>::kStages +
+           1024;
+}
+
+std::mutex g_grouped_mutex;
+
+template <int MT, int TPW>
+int grouped_ctas_per_sm(int device) {
+    static int per_device[64];
+    std::lock_guard<std::mutex> lock(g_grouped_mutex);
+    if (device < 0 || device >= 64) return 0;
+    if (per_device[device] == 0) {
+        int v = 0;
+        if (cudaFuncSetAttribute(gemv_grouped_kernel<MT, TPW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 grouped_smem_bytes<MT, TPW>()) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, gemv_grouped_kernel<MT, TPW>, Warps<TPW>::kThreads,
+                                                          grouped_smem_bytes<MT, TPW>()) != cudaSuccess ||
+            v < 1) {
+            cudaGetLastError();
+            return 0;
+        }
+        per_device[device] = v;
+    }
+    return per_device[device];
+}
+
+template <int MT, int TPW>
+cudaError_t launch_grouped_t(const void* plan, int32_t n_ctas, const DeviceInfo& dev, cudaStream_t stream) {
+    int device = 0;
+    if (cudaError_t e = cudaGetDevice(&device)) return e;
+    if (grouped_ctas_per_sm<MT, TPW>(device) < 1) return cudaErrorInvalidConfiguration;  // sets the smem attribute
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(n_ctas), 1, 1);
+    cfg.blockDim = dim3(Warps<TPW>::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = grouped_smem_bytes<MT, TPW>();
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    (void)dev;
+    return cudaLaunchKernelEx(&cfg, gemv_grouped_kernel<MT, TPW>, static_cast<const uint8_t*>(plan), dev.status);
+}
+
+}  // namespace
+
+size_t grouped_plan_bytes(int32_t count, int64_t n_items, int32_t n_ctas) {
+    return sizeof(GroupedHeader) + sizeof(GroupedProblem) * static_cast<size_t>(count) +
+           sizeof(int32_t) * static_cast<size_t>((n_ctas + 2) & ~1) + sizeof(uint2) * static_cast<size_t>(n_items);
+}
+
+int grouped_ctas(int token_tiles, const DeviceInfo& dev) {
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return 0;
+    const int per_sm = token_tiles == 1 ? grouped_ctas_per_sm<1, kTpw>(device) : grouped_ctas_per_sm<2, 4>(device);
+    return per_sm * dev.sm_count;
+}
+
+cudaError_t grouped_plan_build(const GroupedSpec* specs, int32_t count, int token_tiles, int32_t n_ctas,
+                               std::vector<uint8_t>* out, int64_t* n_items_out, int32_t* n_ctas_out) {
+    int64_t n_items = 0;
+    for (int32_t i = 0; i < count; ++i) n_items += (specs[i].N + kRowsCta - 1) / kRowsCta;
+    if (n_items > 0x7fffffffLL || n_ctas < 1) return cudaErrorInvalidValue;
+    if (n_ctas > n_items) n_ctas = static_cast<int32_t>(n_items);
+    out->assign(grouped_plan_bytes(count, n_items, n_ctas), 0);
+    GroupedHeader hdr = {};
+    hdr.count = count;
+    hdr.n_items = static_cast<int32_t>(n_items);
+    hdr.token_tiles = token_tiles;
+    hdr.n_ctas = n_ctas;
+    std::memcpy(out->data(), &hdr, sizeof(hdr));
+    struct Item {
+        int32_t stages;
+        uint2 id;
+    };
+    std::vector<Item> list;
+    list.reserve(static_cast<size_t>(n_items));
+    for (int32_t i = 0; i < count; ++i) {
+        const GroupedSpec& sp = specs[i];
+        GroupedProblem pr;
+        std::memset(&pr, 0, sizeof(pr));
+        if (cudaError_t e = encode_codes_stage_map(&pr.codes, sp.packed, sp.N, sp.K, kRowsCta, kStageGroups,
+                                                   CU_TENSOR_MAP_SWIZZLE_NONE))
+            return e;
+        if (cudaError_t e = encode_x_stage_map(&pr.x, sp.x, sp.M, sp.K, 8 * token_tiles, 2 * kStageGroups)) return e;
+        pr.scales = static_cast<const uint16_t*>(sp.scales);
+        pr.y = static_cast<__nv_bfloat16*>(sp.y);
+        pr.N = sp.N;
+        pr.M = static_cast<int32_t>(sp.M);
+        pr.G = static_cast<int32_t>(sp.K / 128);
+        pr.T = (pr.G + kStageGroups - 1) / kStageGroups;
+        std::memcpy(out->data() + sizeof(GroupedHeader) + sizeof(GroupedProblem) * i, &pr, sizeof(pr));
+        const int64_t rbs = (sp.N + kRowsCta - 1) / kRowsCta;
+        for (int64_t rb = 0; rb < rbs; ++rb)
+            list.push_back({pr.T, make_uint2(static_cast<unsigned>(i), static_cast<unsigned>(rb))});
+    }
+    // Longest processing time first: items by cost (stages, plus one for the
+    // item's epilogue) in decreasing order, each to the least-loaded CTA
+    // (lowest index among equals).  Deterministic.
+    std::stable_sort(list.begin(), list.end(), [](const Item& a, const Item& b) { return a.stages > b.stages; });
+    using Load = std::pair<int64_t, int32_t>;  // (work so far, CTA)
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+    for (int32_t c = 0; c < n_ctas; ++c) heap.push({0, c});
+    std::vector<std::vector<uint2>> per_cta(static_cast<size_t>(n_ctas));
+    for (const Item& it : list) {
+        Load l = heap.top();
+        heap.pop();
+        per_cta[static_cast<size_t>(l.second)].push_back(it.id);
+        l.first += it.stages + 1;
+        heap.push(l);
+    }
+    int32_t* first = reinterpret_cast<int32_t*>(out->data() + sizeof(GroupedHeader) + sizeof(GroupedProblem) * count);
+    uint2* items = reinterpret_cast<uint2*>(first + ((n_ctas + 2) & ~1));
+    int32_t k = 0;
+    for (int32_t c = 0; c < n_ctas; ++c) {
+        first[c] = k;
+        for (const uint2& id : per_cta[static_cast<size_t>(c)]) items[k++] = id;
+    }
+    first[n_ctas] = k;
+    *n_items_out = n_items;
+    *n_ctas_out = n_ctas;
+    return cudaSuccess;
+}
+
+cudaError_t launch_grouped(const void* plan, int32_t n_ctas, int token_tiles, const DeviceInfo& dev,
+                           cudaStream_t stream) {
+    if (n_ctas < 1) return cudaSuccess;
+    return token_tiles == 1 ? launch_grouped_t<1, kTpw>(plan, n_ctas, dev, stream)
+                            : launch_grouped_t<2, 4>(plan, n_ctas, dev, stream);
+}
+
+}  // namespace w4

@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <vector>
 
 namespace w4 {
 
@@ -44,6 +45,27 @@ cudaError_t encode_x_stage_map(CUtensorMap* map, const void* x, int64_t M, int64
 // as zeros.
 cudaError_t encode_codes_stage_map(CUtensorMap* map, const void* packed, int64_t N, int64_t K, int rows,
                                    int groups, CUtensorMapSwizzle swizzle);
+
+// One problem of a grouped matmul (validated by the C ABI layer).
+struct GroupedSpec {
+    const void* x;
+    int64_t M, N, K;
+    const void* packed;
+    const void* scales;
+    void* y;
+};
+// Plan bytes for `count` problems with `n_items` 64-row blocks in total,
+// scheduled over `n_ctas` CTAs.
+size_t grouped_plan_bytes(int32_t count, int64_t n_items, int32_t n_ctas);
+// CTAs the grouped kernel runs with on this device (resident at once).
+int grouped_ctas(int token_tiles, const DeviceInfo& dev);
+// Host image of a grouped plan: tensor maps, and the items assigned to
+// min(n_ctas, items) CTAs longest first.
+cudaError_t grouped_plan_build(const GroupedSpec* specs, int32_t count, int token_tiles, int32_t n_ctas,
+                               std::vector<uint8_t>* out, int64_t* n_items, int32_t* n_ctas_used);
+// Runs a plan already copied to device memory.
+cudaError_t launch_grouped(const void* plan, int32_t n_ctas, int token_tiles, const DeviceInfo& dev,
+                           cudaStream_t stream);
 
 cudaError_t launch_wait_probe(int64_t spin_limit, int arrive, const DeviceInfo& dev,
                               cudaStream_t stream);

@@ -125,6 +125,58 @@ int w4_gemm_ex(const void* x, int64_t M, int64_t N, int64_t K,
 int w4_gemm_path_for(int64_t M, int64_t N, int64_t K);
 
 /*
+ * Grouped matmul — many independent small-M problems y_i = Ŵ_i x_i in one
+ * launch (the matrices of a layer, or of a whole model step).  Each problem
+ * is computed exactly as by w4_gemm's small-M kernel (same per-element
+ * results contract, K not split, deterministic).  Work items are (problem,
+ * 64-row block) pairs, assigned at plan time longest first to the least
+ * loaded of a fixed grid of two CTAs per SM; each CTA streams its items back
+ * to back through one TMA pipeline.
+ *
+ * A plan is built once (host work plus one synchronous copy) and may then be
+ * run any number of times, including inside CUDA graphs; it records the
+ * problems' pointers, so their buffers must stay allocated and in place, but
+ * their contents may change between runs.
+ */
+typedef struct w4_gemm_problem {
+    const void* x;      /* bf16 [M, K]  (16-byte aligned)                       */
+    int64_t M;          /* token rows, 1..16                                     */
+    int64_t N;          /* output features, ≥ 1                                  */
+    int64_t K;          /* input features, multiple of 128, ≥ 128                */
+    const void* packed; /* u8 [N, K/2]  as written by w4_quantize_rtn (16-B al.) */
+    const void* scales; /* bf16 [N, K/128]                                       */
+    void* y;            /* bf16 [M, N]; must not overlap any other problem's    */
+                        /* inputs or output                                      */
+} w4_gemm_problem;
+
+typedef struct w4_grouped_plan {
+    void* device_plan;   /* the caller's device memory holding the plan           */
+    size_t bytes;        /* bytes of it in use                                    */
+    int32_t count;       /* problems                                              */
+    int32_t items;       /* (problem, 64-row block) work items                    */
+    int32_t ctas;        /* CTAs the items were scheduled over (the launch grid)  */
+    int32_t token_tiles; /* 1 when every M ≤ 8, else 2                            */
+    int32_t device;      /* CUDA device the plan was built on                     */
+} w4_grouped_plan;
+
+/* Device bytes a plan for these problems needs (0 if any problem is invalid):
+ * at most 128 + 384 per problem + 12 per 64-row block (+4). */
+size_t w4_grouped_plan_bytes(int32_t count, const w4_gemm_problem* problems);
+
+/* Validates the problems (as w4_gemm would, plus 1 ≤ M ≤ 16 → else
+ * W4_ERR_UNSUPPORTED; outputs overlapping any input or other output →
+ * W4_ERR_INVALID_ARG), encodes the plan and copies it synchronously into
+ * `device_memory` (128-byte aligned, at least w4_grouped_plan_bytes bytes, on
+ * the current device), and fills *plan.  The library keeps no reference to
+ * `problems` afterwards. */
+int w4_grouped_plan_init(w4_grouped_plan* plan, void* device_memory, size_t bytes,
+                         int32_t count, const w4_gemm_problem* problems);
+
+/* Runs every problem of the plan on `stream` (the device must be the one the
+ * plan was built on).  Asynchronous; no allocation. */
+int w4_gemm_grouped(const w4_grouped_plan* plan, void* stream);
+
+/*
  * Every wait inside the library's kernels (mbarrier phases, TMA completion)
  * is bounded.  A wait that runs out records W4_ERR_TIMEOUT in a per-device
  * status word and the kernel returns early (its outputs are then undefined).

@@ -101,6 +101,19 @@ def test_gemm_rejects(lib, args, expect):
     assert lib.w4_gemm_ex(*args) == expect
 
 
+def test_grouped_rejects_without_gpu(lib):
+    probs = (w4._Problem * 2)()
+    probs[0] = w4._Problem(A16, 1, 4, 256, A16 * 2, A16 * 4, A16 * 8)
+    probs[1] = w4._Problem(A16, 17, 4, 256, A16 * 2, A16 * 4, A16 * 16)  # M > 16
+    assert lib.w4_grouped_plan_bytes(1, probs) == 128 + 384 + 4 * 2 + 8
+    assert lib.w4_grouped_plan_bytes(2, probs) == 0
+    assert lib.w4_grouped_plan_bytes(0, probs) == 0
+    plan = w4._Plan()
+    assert lib.w4_grouped_plan_init(plan, A16 * 32 + 64, 4096, 1, probs) == w4.W4_ERR_MISALIGNED
+    assert lib.w4_grouped_plan_init(plan, A16 * 32, 4096, 2, probs) == w4.W4_ERR_UNSUPPORTED
+    assert lib.w4_gemm_grouped(None, None) == w4.W4_ERR_INVALID_ARG
+
+
 def test_gemm_empty_is_noop(lib):
     assert lib.w4_gemm(None, 0, 4, 256, None, None, None, None) == w4.W4_OK
     assert lib.w4_gemm(None, 3, 0, 256, None, None, None, None) == w4.W4_OK

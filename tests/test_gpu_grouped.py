@@ -1,0 +1,121 @@
+"""GPU parity of the grouped matmul (w4_gemm_grouped) against the CPU oracle:
+every problem of a plan element by element within 4e-3·Σ|ŵx| + 1 bf16 ulp,
+outputs guarded, runs deterministic, plans reusable and graph-capturable."""
+import pytest
+import torch
+
+import gemm_rtn_sym_gb300 as w4
+from gemm_rtn_sym_gb300 import workloads as wl
+from tests.helpers import check_gemm, guarded, guards_intact, quantize_gpu, sample_rows
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def make_problems(cuda_lib, shapes, Ms, seed=0):
+    Ws, probs, bufs = [], [], []
+    for i, ((N, K), M) in enumerate(zip(shapes, Ms)):
+        W = wl.random_bf16((N, K), 0.02, seed=seed + 31 * i + N, device=DEV)
+        packed, scales = quantize_gpu(cuda_lib, W)
+        x = wl.random_bf16((M, K), 1.0, seed=seed + 17 * i + M, device=DEV)
+        y, ybuf = guarded((M, N), torch.bfloat16, DEV)
+        Ws.append(W)
+        probs.append((x, packed, scales, y))
+        bufs.append(ybuf)
+    return Ws, probs, bufs
+
+
+SHAPES = [(1, 128), (7, 256), (129, 1152), (200, 4096), (64, 384), (2560, 512), (96, 30720)]
+
+
+@pytest.mark.parametrize("Ms", [[1, 2, 3, 5, 8, 1, 4], [9, 1, 13, 16, 8, 12, 11]])
+def test_grouped_small_problems(cuda_lib, Ms):
+    Ws, probs, bufs = make_problems(cuda_lib, SHAPES, Ms, seed=len(Ms) * Ms[0])
+    plan = w4.w4_grouped_plan(probs)
+    w4.w4_gemm_grouped(plan)
+    torch.cuda.synchronize()
+    assert w4.w4_last_device_status() == 0
+    for W, (x, _, _, y), b in zip(Ws, probs, bufs):
+        assert guards_intact(b), "grouped matmul wrote outside an output"
+        check_gemm(W, x, y)
+    # deterministic, and the plan is reusable
+    first = [p[3].clone() for p in probs]
+    for _ in range(3):
+        w4.w4_gemm_grouped(plan)
+    torch.cuda.synchronize()
+    for f, p in zip(first, probs):
+        assert torch.equal(f.view(torch.int16), p[3].view(torch.int16))
+
+
+def test_grouped_new_inputs_and_graph_replay(cuda_lib):
+    Ws, probs, _ = make_problems(cuda_lib, SHAPES[:5], [1, 4, 8, 2, 3], seed=5)
+    plan = w4.w4_grouped_plan(probs)
+    g = torch.cuda.CUDAGraph()
+    w4.w4_gemm_grouped(plan)  # warm-up outside capture
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        w4.w4_gemm_grouped(plan)
+    for rep in range(2):
+        for i, (x, _, _, _) in enumerate(probs):  # new activations in the same buffers
+            x.copy_(wl.random_bf16(tuple(x.shape), 1.0, seed=1000 + 10 * rep + i, device=DEV))
+        g.replay()
+        torch.cuda.synchronize()
+        for W, (x, _, _, y) in zip(Ws, probs):
+            check_gemm(W, x, y)
+
+
+def test_grouped_rejects(cuda_lib):
+    _, probs, _ = make_problems(cuda_lib, [(64, 256), (64, 256)], [4, 4], seed=9)
+    x, p, s, y = probs[0]
+    with pytest.raises(w4.W4Error) as e:  # M = 17 is not small-M
+        x17 = wl.random_bf16((17, 256), 1.0, seed=1, device=DEV)
+        w4.w4_grouped_plan([(x17, p, s, torch.empty((17, 64), dtype=torch.bfloat16, device=DEV))])
+    assert e.value.status == w4.W4_ERR_UNSUPPORTED
+    with pytest.raises(w4.W4Error) as e:  # two problems writing the same output
+        w4.w4_grouped_plan([(x, p, s, y), (probs[1][0], probs[1][1], probs[1][2], y)])
+    assert e.value.status == w4.W4_ERR_INVALID_ARG
+    x1, p1, s1, y1 = probs[1]
+    with pytest.raises(w4.W4Error) as e:  # output overlapping another problem's input
+        w4.w4_grouped_plan([(x, p, s, x1.view(-1)[:256].view(4, 64)), (x1, p1, s1, y1)])
+    assert e.value.status == w4.W4_ERR_INVALID_ARG
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("M", [1, 5, 13])
+def test_grouped_layer27b_sampled(cuda_lib, M):
+    shapes = wl.SHAPES["layer27b"]
+    Ws, probs = [], []
+    for i, (N, K) in enumerate(shapes):
+        W = wl.weight("layer27b", i, device=DEV)
+        packed, scales = quantize_gpu(cuda_lib, W)
+        x = wl.activations("layer27b", M, K, i, device=DEV)
+        Ws.append(W)
+        probs.append((x, packed, scales, torch.empty((M, N), dtype=torch.bfloat16, device=DEV)))
+    plan = w4.w4_grouped_plan(probs)
+    w4.w4_gemm_grouped(plan)
+    torch.cuda.synchronize()
+    assert w4.w4_last_device_status() == 0
+    for i, (W, (x, _, _, y)) in enumerate(zip(Ws, probs)):
+        rows = torch.from_numpy(sample_rows(W.shape[0], 64, seed=i)).to(DEV)
+        check_gemm(W[rows].cpu(), x, y[:, rows])
+
+
+@pytest.mark.slow
+def test_grouped_stack_subset(cuda_lib):
+    """Two matrices of each stack shape (8 problems, 4 shapes) in one plan."""
+    shapes = wl.SHAPES["stack4b"]
+    pick = [0, 1, 56, 57, 112, 113, 156, 157]
+    Ws, probs = [], []
+    for j, i in enumerate(pick):
+        N, K = shapes[i]
+        W = wl.weight("stack4b", i, device=DEV)
+        packed, scales = quantize_gpu(cuda_lib, W)
+        x = wl.activations("stack4b", 8, K, i, device=DEV)
+        Ws.append(W)
+        probs.append((x, packed, scales, torch.empty((8, N), dtype=torch.bfloat16, device=DEV)))
+    plan = w4.w4_grouped_plan(probs)
+    w4.w4_gemm_grouped(plan)
+    torch.cuda.synchronize()
+    for j, (W, (x, _, _, y)) in enumerate(zip(Ws, probs)):
+        rows = torch.from_numpy(sample_rows(W.shape[0], 48, seed=j)).to(DEV)
+        check_gemm(W[rows].cpu(), x, y[:, rows])
