@@ -288,9 +288,10 @@ def headline(torch, w4, wl, steps, warmup, pk):
     return res
 
 
-def gemm_set(torch, w4, wl, workload, Ms, pk, reps=20, path=None):
-    """Matmul over every matrix of a workload (one launch per matrix), per M.
-    Matrices that fit in L2 several times are rotated over copies."""
+def gemm_set(torch, w4, wl, workload, Ms, pk, reps=20, path=None, grouped=False):
+    """Matmul over every matrix of a workload (one launch per matrix, or one
+    grouped launch over all of them), per M.  Matrices that fit in L2 several
+    times are rotated over copies."""
     dev = torch.device("cuda", torch.cuda.current_device())
     mats = []
     shapes = wl.SHAPES[workload]
@@ -318,13 +319,20 @@ def gemm_set(torch, w4, wl, workload, Ms, pk, reps=20, path=None):
                 xs[(K, i if workload != "stack4b" else 0)] = wl.activations(workload, M, K, i, device=dev)
             ys.append(torch.empty((M, N), dtype=torch.bfloat16, device=dev))
 
-        def run():
-            for j, (N, K, p, s, i) in enumerate(mats):
-                x = xs[(K, i if workload != "stack4b" else 0)]
-                if path is None:
-                    w4.w4_gemm(x, p, s, out=ys[j])
-                else:
-                    w4.w4_gemm_ex(x, p, s, out=ys[j], path=path)
+        if grouped:
+            plan = w4.w4_grouped_plan([(xs[(K, i if workload != "stack4b" else 0)], p, s, ys[j])
+                                       for j, (N, K, p, s, i) in enumerate(mats)])
+
+            def run():
+                w4.w4_gemm_grouped(plan)
+        else:
+            def run():
+                for j, (N, K, p, s, i) in enumerate(mats):
+                    x = xs[(K, i if workload != "stack4b" else 0)]
+                    if path is None:
+                        w4.w4_gemm(x, p, s, out=ys[j])
+                    else:
+                        w4.w4_gemm_ex(x, p, s, out=ys[j], path=path)
 
         g = capture(torch, run)
         t = T.time(g.replay, reps=reps) / copies
@@ -335,7 +343,11 @@ def gemm_set(torch, w4, wl, workload, Ms, pk, reps=20, path=None):
         out[f"M{M}"] = {"us": t * 1e6, "GB/s": nb / t / 1e9, "TFLOP/s": fl / t / 1e12,
                         "tok/s": M / t, "bound": "hbm" if t_hbm >= t_tc else "tensor",
                         "frac": max(t_hbm, t_tc) / t,
-                        "path": w4.w4_gemm_path_for(M, mats[0][0], mats[0][1]) if path is None else path}
+                        "path": "grouped" if grouped else
+                        (w4.w4_gemm_path_for(M, mats[0][0], mats[0][1]) if path is None else path)}
+        if grouped:
+            out[f"M{M}"]["launches"] = 1
+            del plan
         del g, ys, xs
     assert w4.w4_last_device_status() == 0
     del mats
@@ -440,8 +452,16 @@ def run_gpu(args):
             sub["layer27b"] = gemm_set(torch, w4, wl, "layer27b", wl.ROWS["layer27b"], pk, reps=10)
         if want("layer70b"):
             sub["layer70b"] = gemm_set(torch, w4, wl, "layer70b", wl.ROWS["layer70b"], pk, reps=5)
+        if want("layer27b_grouped"):
+            sub["layer27b_grouped"] = gemm_set(torch, w4, wl, "layer27b", wl.ROWS["layer27b"], pk, reps=10,
+                                               grouped=True)
         if want("stack4b") and not args.no_sweep:
             sub["stack4b"] = gemm_set(torch, w4, wl, "stack4b", wl.ROWS["stack4b"], pk, reps=3)
+        if want("layer70b_grouped"):
+            sub["layer70b_grouped"] = gemm_set(torch, w4, wl, "layer70b", wl.ROWS["layer70b"], pk, reps=5,
+                                               grouped=True)
+        if want("stack4b_grouped") and not args.no_sweep:
+            sub["stack4b_grouped"] = gemm_set(torch, w4, wl, "stack4b", wl.ROWS["stack4b"], pk, reps=3, grouped=True)
 
     if rank != 0:
         return

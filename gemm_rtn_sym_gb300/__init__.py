@@ -41,8 +41,9 @@ class _Problem(ctypes.Structure):
 
 class _Plan(ctypes.Structure):
     """w4_grouped_plan of include/w4.h."""
-    _fields_ = [("device_plan", _vp), ("bytes", _sz), ("count", _i32), ("items", _i32), ("ctas", _i32),
-                ("token_tiles", _i32), ("device", _i32)]
+    _fields_ = [("device_plan", _vp), ("bytes", _sz), ("count", _i32), ("device", _i32), ("items", _i32),
+                ("ctas", _i32), ("token_tiles", _i32), ("tc_items", _i32), ("tc_ctas", _i32), ("tc_max_bm", _i32),
+                ("tc_offset", _sz)]
 
 _SIGNATURES = {
     "w4_packed_bytes": (_sz, [_i64, _i64]),
@@ -184,13 +185,13 @@ class GroupedPlan:
 
     @property
     def items(self) -> int:
-        return self.plan.items
+        return self.plan.items + self.plan.tc_items
 
 
 def w4_grouped_plan(problems) -> GroupedPlan:
-    """Plan for many small-M matmuls y_i = Ŵ_i x_i run by one w4_gemm_grouped
-    launch.  problems: sequence of (x, packed, scales, y) CUDA tensors with the
-    shapes of w4_gemm (1 ≤ M ≤ 16), all on one device."""
+    """Plan for many matmuls y_i = Ŵ_i x_i run by one w4_gemm_grouped call.
+    problems: sequence of (x, packed, scales, y) CUDA tensors with the shapes
+    of w4_gemm, all on one device."""
     problems = list(problems)
     if not problems:
         raise ValueError("no problems")

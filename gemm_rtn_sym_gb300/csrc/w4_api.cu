@@ -1,6 +1,7 @@
 // C ABI of the library (declared in include/w4.h): argument checks, kernel
 // choice, launches and the per-device status word of the bounded waits.
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 #include <vector>
 
@@ -154,12 +155,12 @@ int w4_gemm(const void* x, int64_t M, int64_t N, int64_t K, const void* packed, 
 
 namespace {
 
-// Checks one grouped problem like w4_gemm does; small-M only (1 ≤ M ≤ 16).
+// Checks one grouped problem like w4_gemm does.
 int check_grouped_problem(const w4_gemm_problem& p) {
     if (p.M < 1 || p.N < 1 || p.K < 128) return W4_ERR_INVALID_ARG;
     if (const int s = check_sizes(p.N, p.K)) return s;
-    if (p.M > 16) return W4_ERR_UNSUPPORTED;
-    if (p.N > INT32_MAX || p.K > INT32_MAX || p.K > (int64_t{1} << 62) / p.M || p.N > (int64_t{1} << 62) / p.M)
+    if (p.N > INT32_MAX || p.K > INT32_MAX || p.M > INT32_MAX || p.K > (int64_t{1} << 62) / p.M ||
+        p.N > (int64_t{1} << 62) / p.M)
         return W4_ERR_UNSUPPORTED;
     if (!p.x || !p.packed || !p.scales || !p.y) return W4_ERR_INVALID_ARG;
     if (!aligned(p.x, 16) || !aligned(p.packed, 16) || !aligned(p.scales, 2) || !aligned(p.y, 2))
@@ -169,19 +170,34 @@ int check_grouped_problem(const w4_gemm_problem& p) {
 
 size_t out_bytes(const w4_gemm_problem& p) { return static_cast<size_t>(p.M * p.N) * 2; }
 
+bool is_tensor(const w4_gemm_problem& p) { return p.M >= kTensorMinM; }
+
+size_t round128(size_t v) { return (v + 127) / 128 * 128; }
+
 }  // namespace
 
 size_t w4_grouped_plan_bytes(int32_t count, const w4_gemm_problem* problems) {
     if (count < 1 || !problems) return 0;
-    int64_t items = 0;
+    int64_t small_items = 0, tc_items = 0;
+    int32_t n_small = 0, n_tc = 0;
     for (int32_t i = 0; i < count; ++i) {
-        if (check_grouped_problem(problems[i]) != W4_OK) return 0;
-        items += (problems[i].N + 63) / 64;
+        const w4_gemm_problem& p = problems[i];
+        if (check_grouped_problem(p) != W4_OK) return 0;
+        if (is_tensor(p)) {
+            ++n_tc;
+            tc_items += tc_grouped_items(GroupedSpec{p.x, p.M, p.N, p.K, p.packed, p.scales, p.y});
+        } else {
+            ++n_small;
+            small_items += (p.N + 63) / 64;
+        }
     }
-    if (items > INT32_MAX) return 0;
-    // Sized for the largest grid a plan can use (one CTA per item), so that
+    if (small_items > INT32_MAX || tc_items > INT32_MAX) return 0;
+    // Sized for the largest grids a plan can use (one CTA per item), so that
     // the answer does not depend on the device.
-    return grouped_plan_bytes(count, items, static_cast<int32_t>(items));
+    size_t bytes = 0;
+    if (n_small) bytes += round128(grouped_plan_bytes(n_small, small_items, static_cast<int32_t>(small_items)));
+    if (n_tc) bytes += tc_grouped_plan_bytes(n_tc, tc_items, static_cast<int32_t>(tc_items));
+    return bytes;
 }
 
 int w4_grouped_plan_init(w4_grouped_plan* plan, void* device_memory, size_t bytes, int32_t count,
@@ -189,10 +205,10 @@ int w4_grouped_plan_init(w4_grouped_plan* plan, void* device_memory, size_t byte
     if (!plan || !device_memory || count < 1 || !problems) return W4_ERR_INVALID_ARG;
     if (!aligned(device_memory, 128)) return W4_ERR_MISALIGNED;
     int token_tiles = 1;
+    std::vector<GroupedSpec> small, tc;
     for (int32_t i = 0; i < count; ++i) {
         const w4_gemm_problem& p = problems[i];
         if (const int s = check_grouped_problem(p)) return s;
-        if (p.M > 8) token_tiles = 2;
         const size_t yb = out_bytes(p);
         for (int32_t j = 0; j < count; ++j) {
             const w4_gemm_problem& q = problems[j];
@@ -205,41 +221,66 @@ int w4_grouped_plan_init(w4_grouped_plan* plan, void* device_memory, size_t byte
                 overlaps(device_memory, bytes, q.scales, sb) || overlaps(device_memory, bytes, q.y, out_bytes(q)))
                 return W4_ERR_INVALID_ARG;
         }
+        const GroupedSpec sp{p.x, p.M, p.N, p.K, p.packed, p.scales, p.y};
+        if (is_tensor(p)) {
+            tc.push_back(sp);
+        } else {
+            small.push_back(sp);
+            if (p.M > 8) token_tiles = 2;
+        }
     }
     cudaError_t err;
     const DeviceInfo* dev = device_info(&err);
     if (!dev) return W4_ERR_CUDA;
     if (dev->cc_major < 10) return W4_ERR_UNSUPPORTED;
-    std::vector<GroupedSpec> specs(static_cast<size_t>(count));
-    for (int32_t i = 0; i < count; ++i) {
-        const w4_gemm_problem& p = problems[i];
-        specs[i] = GroupedSpec{p.x, p.M, p.N, p.K, p.packed, p.scales, p.y};
+    std::vector<uint8_t> image, tc_image;
+    int64_t n_items = 0, n_tc_items = 0;
+    int32_t n_ctas = 0, n_tc_ctas = 0;
+    if (!small.empty()) {
+        const int ctas = grouped_ctas(token_tiles, *dev);
+        if (ctas < 1) return W4_ERR_CUDA;
+        if (grouped_plan_build(small.data(), static_cast<int32_t>(small.size()), token_tiles, ctas, &image, &n_items,
+                               &n_ctas) != cudaSuccess)
+            return W4_ERR_CUDA;
+        image.resize(round128(image.size()), 0);
     }
-    const int ctas = grouped_ctas(token_tiles, *dev);
-    if (ctas < 1) return W4_ERR_CUDA;
-    std::vector<uint8_t> image;
-    int64_t n_items = 0;
-    int32_t n_ctas = 0;
-    if (grouped_plan_build(specs.data(), count, token_tiles, ctas, &image, &n_items, &n_ctas) != cudaSuccess)
-        return W4_ERR_CUDA;
+    const size_t tc_offset = image.size();
+    if (!tc.empty()) {
+        if (tc_grouped_plan_build(tc.data(), static_cast<int32_t>(tc.size()), dev->sm_count, &tc_image, &n_tc_items,
+                                  &n_tc_ctas) != cudaSuccess)
+            return W4_ERR_CUDA;
+        image.insert(image.end(), tc_image.begin(), tc_image.end());
+    }
     if (bytes < image.size()) return W4_ERR_INVALID_ARG;
     if (cudaMemcpy(device_memory, image.data(), image.size(), cudaMemcpyHostToDevice) != cudaSuccess)
         return W4_ERR_CUDA;
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess) return W4_ERR_CUDA;
+    int max_bm = 0;
+    if (!tc.empty()) std::memcpy(&max_bm, tc_image.data() + 12, sizeof(int));  // TcHeader::max_bm
     plan->device_plan = device_memory;
     plan->bytes = image.size();
     plan->count = count;
+    plan->device = device;
     plan->items = static_cast<int32_t>(n_items);
     plan->ctas = n_ctas;
-    plan->token_tiles = token_tiles;
-    plan->device = device;
+    plan->token_tiles = small.empty() ? 0 : token_tiles;
+    plan->tc_items = static_cast<int32_t>(n_tc_items);
+    plan->tc_ctas = n_tc_ctas;
+    plan->tc_max_bm = max_bm;
+    plan->tc_offset = tc_offset;
     return W4_OK;
 }
 
 int w4_gemm_grouped(const w4_grouped_plan* plan, void* stream) {
-    if (!plan || !plan->device_plan || plan->items < 1 || plan->ctas < 1 || plan->ctas > plan->items ||
-        (plan->token_tiles != 1 && plan->token_tiles != 2))
+    if (!plan || !plan->device_plan) return W4_ERR_INVALID_ARG;
+    const bool has_small = plan->items > 0, has_tc = plan->tc_items > 0;
+    if (!has_small && !has_tc) return W4_ERR_INVALID_ARG;
+    if (has_small && (plan->ctas < 1 || plan->ctas > plan->items ||
+                      (plan->token_tiles != 1 && plan->token_tiles != 2)))
+        return W4_ERR_INVALID_ARG;
+    if (has_tc && (plan->tc_ctas < 1 || plan->tc_ctas > plan->tc_items || plan->tc_max_bm < 16 ||
+                   plan->tc_max_bm > 256 || plan->tc_offset % 128 != 0 || plan->tc_offset >= plan->bytes))
         return W4_ERR_INVALID_ARG;
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess) return W4_ERR_CUDA;
@@ -247,8 +288,13 @@ int w4_gemm_grouped(const w4_grouped_plan* plan, void* stream) {
     cudaError_t err;
     const DeviceInfo* dev = device_info(&err);
     if (!dev) return W4_ERR_CUDA;
-    return to_status(launch_grouped(plan->device_plan, plan->ctas, plan->token_tiles, *dev,
-                                    static_cast<cudaStream_t>(stream)));
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (has_small)
+        if (const int s = to_status(launch_grouped(plan->device_plan, plan->ctas, plan->token_tiles, *dev, st))) return s;
+    if (has_tc)
+        return to_status(launch_tc_grouped(static_cast<const uint8_t*>(plan->device_plan) + plan->tc_offset,
+                                           plan->tc_ctas, plan->tc_max_bm, *dev, st));
+    return W4_OK;
 }
 
 int w4_last_device_status(void* stream) {

@@ -375,6 +375,8 @@ cudaError_t grouped_plan_build(const GroupedSpec* specs, int32_t count, int toke
     }
     int32_t* first = reinterpret_cast<int32_t*>(out->data() + sizeof(GroupedHeader) + sizeof(GroupedProblem) * count);
     uint2* items = reinterpret_cast<uint2*>(first + ((n_ctas + 2) & ~1));
+    // The kernel loads items with 8-byte loads from a 128-byte aligned plan.
+    if ((reinterpret_cast<uint8_t*>(items) - out->data()) % 8 != 0) return cudaErrorMisalignedAddress;
     int32_t k = 0;
     for (int32_t c = 0; c < n_ctas; ++c) {
         first[c] = k;

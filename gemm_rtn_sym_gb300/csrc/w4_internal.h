@@ -67,6 +67,15 @@ cudaError_t grouped_plan_build(const GroupedSpec* specs, int32_t count, int toke
 cudaError_t launch_grouped(const void* plan, int32_t n_ctas, int token_tiles, const DeviceInfo& dev,
                            cudaStream_t stream);
 
+// Tensor-core grouped plan (problems with M ≥ 17): (problem, 128-row tile,
+// token tile) items scheduled longest first over one CTA per SM.
+size_t tc_grouped_plan_bytes(int32_t count, int64_t n_items, int32_t n_ctas);
+int64_t tc_grouped_items(const GroupedSpec& sp);
+cudaError_t tc_grouped_plan_build(const GroupedSpec* specs, int32_t count, int32_t n_ctas, std::vector<uint8_t>* out,
+                                  int64_t* n_items, int32_t* n_ctas_used);
+cudaError_t launch_tc_grouped(const void* plan, int32_t n_ctas, int max_bm, const DeviceInfo& dev,
+                              cudaStream_t stream);
+
 cudaError_t launch_wait_probe(int64_t spin_limit, int arrive, const DeviceInfo& dev,
                               cudaStream_t stream);
 

@@ -125,13 +125,16 @@ int w4_gemm_ex(const void* x, int64_t M, int64_t N, int64_t K,
 int w4_gemm_path_for(int64_t M, int64_t N, int64_t K);
 
 /*
- * Grouped matmul — many independent small-M problems y_i = Ŵ_i x_i in one
- * launch (the matrices of a layer, or of a whole model step).  Each problem
- * is computed exactly as by w4_gemm's small-M kernel (same per-element
- * results contract, K not split, deterministic).  Work items are (problem,
- * 64-row block) pairs, assigned at plan time longest first to the least
- * loaded of a fixed grid of two CTAs per SM; each CTA streams its items back
- * to back through one TMA pipeline.
+ * Grouped matmul — many independent problems y_i = Ŵ_i x_i in one call (the
+ * matrices of a layer, or of a whole model step).  Each problem is computed
+ * as by w4_gemm's kernel for its M (same per-element results contract, K not
+ * split, deterministic): problems with M ≤ 16 by the small-M kernel, whose
+ * work items are (problem, 64-row block) pairs on a fixed grid of two CTAs
+ * per SM; problems with M ≥ 17 by the tensor-core kernel, whose items are
+ * (problem, 128-row tile, token tile) on one CTA per SM.  Items are assigned
+ * at plan time longest first to the least-loaded CTA, and each CTA streams
+ * its items back to back through its TMA pipelines.  A plan with both kinds
+ * launches two kernels, one after the other, on the stream.
  *
  * A plan is built once (host work plus one synchronous copy) and may then be
  * run any number of times, including inside CUDA graphs; it records the
@@ -140,7 +143,7 @@ int w4_gemm_path_for(int64_t M, int64_t N, int64_t K);
  */
 typedef struct w4_gemm_problem {
     const void* x;      /* bf16 [M, K]  (16-byte aligned)                       */
-    int64_t M;          /* token rows, 1..16                                     */
+    int64_t M;          /* token rows, ≥ 1                                       */
     int64_t N;          /* output features, ≥ 1                                  */
     int64_t K;          /* input features, multiple of 128, ≥ 128                */
     const void* packed; /* u8 [N, K/2]  as written by w4_quantize_rtn (16-B al.) */
@@ -153,22 +156,25 @@ typedef struct w4_grouped_plan {
     void* device_plan;   /* the caller's device memory holding the plan           */
     size_t bytes;        /* bytes of it in use                                    */
     int32_t count;       /* problems                                              */
-    int32_t items;       /* (problem, 64-row block) work items                    */
-    int32_t ctas;        /* CTAs the items were scheduled over (the launch grid)  */
-    int32_t token_tiles; /* 1 when every M ≤ 8, else 2                            */
     int32_t device;      /* CUDA device the plan was built on                     */
+    int32_t items;       /* small-M work items (0: no problem with M ≤ 16)        */
+    int32_t ctas;        /* CTAs they were scheduled over (the launch grid)       */
+    int32_t token_tiles; /* small-M kernel variant: 1 when every M ≤ 8, else 2    */
+    int32_t tc_items;    /* tensor-core work items (0: no problem with M ≥ 17)    */
+    int32_t tc_ctas;     /* CTAs they were scheduled over                         */
+    int32_t tc_max_bm;   /* widest token tile                                     */
+    size_t tc_offset;    /* byte offset of the tensor-core part of the plan       */
 } w4_grouped_plan;
 
-/* Device bytes a plan for these problems needs (0 if any problem is invalid):
- * at most 128 + 384 per problem + 12 per 64-row block (+4). */
+/* Device bytes a plan for these problems needs (0 if any problem is invalid);
+ * an upper bound that does not depend on the device. */
 size_t w4_grouped_plan_bytes(int32_t count, const w4_gemm_problem* problems);
 
-/* Validates the problems (as w4_gemm would, plus 1 ≤ M ≤ 16 → else
- * W4_ERR_UNSUPPORTED; outputs overlapping any input or other output →
- * W4_ERR_INVALID_ARG), encodes the plan and copies it synchronously into
- * `device_memory` (128-byte aligned, at least w4_grouped_plan_bytes bytes, on
- * the current device), and fills *plan.  The library keeps no reference to
- * `problems` afterwards. */
+/* Validates the problems (as w4_gemm would; an output overlapping any input
+ * or other output → W4_ERR_INVALID_ARG), encodes the plan and copies it
+ * synchronously into `device_memory` (128-byte aligned, at least
+ * w4_grouped_plan_bytes bytes, on the current device), and fills *plan.  The
+ * library keeps no reference to `problems` afterwards. */
 int w4_grouped_plan_init(w4_grouped_plan* plan, void* device_memory, size_t bytes,
                          int32_t count, const w4_gemm_problem* problems);
 

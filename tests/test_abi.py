@@ -104,8 +104,8 @@ def test_gemm_rejects(lib, args, expect):
 def test_grouped_rejects_without_gpu(lib):
     probs = (w4._Problem * 2)()
     probs[0] = w4._Problem(A16, 1, 4, 256, A16 * 2, A16 * 4, A16 * 8)
-    probs[1] = w4._Problem(A16, 17, 4, 256, A16 * 2, A16 * 4, A16 * 16)  # M > 16
-    assert lib.w4_grouped_plan_bytes(1, probs) == 128 + 384 + 4 * 2 + 8
+    probs[1] = w4._Problem(A16, 4, 4, 200, A16 * 2, A16 * 4, A16 * 16)  # K % 128 != 0
+    assert lib.w4_grouped_plan_bytes(1, probs) == 640  # 128 + 384 + 4·2 + 8, rounded to 128
     assert lib.w4_grouped_plan_bytes(2, probs) == 0
     assert lib.w4_grouped_plan_bytes(0, probs) == 0
     plan = w4._Plan()

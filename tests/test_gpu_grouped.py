@@ -64,13 +64,30 @@ def test_grouped_new_inputs_and_graph_replay(cuda_lib):
             check_gemm(W, x, y)
 
 
+@pytest.mark.parametrize("Ms", [[17, 33, 64, 208, 100, 257, 19], [1, 40, 13, 208, 8, 24, 2]])
+def test_grouped_tensor_and_mixed(cuda_lib, Ms):
+    """Problems with M ≥ 17 take the tensor-core grouped kernel; a plan mixing
+    both kinds runs both kernels."""
+    Ws, probs, bufs = make_problems(cuda_lib, SHAPES, Ms, seed=3 + Ms[1])
+    plan = w4.w4_grouped_plan(probs)
+    assert plan.plan.tc_items > 0
+    w4.w4_gemm_grouped(plan)
+    torch.cuda.synchronize()
+    assert w4.w4_last_device_status() == 0
+    for W, (x, _, _, y), b in zip(Ws, probs, bufs):
+        assert guards_intact(b), "grouped matmul wrote outside an output"
+        check_gemm(W, x, y)
+    first = [p[3].clone() for p in probs]
+    for _ in range(2):
+        w4.w4_gemm_grouped(plan)
+    torch.cuda.synchronize()
+    for f, p in zip(first, probs):
+        assert torch.equal(f.view(torch.int16), p[3].view(torch.int16))
+
+
 def test_grouped_rejects(cuda_lib):
     _, probs, _ = make_problems(cuda_lib, [(64, 256), (64, 256)], [4, 4], seed=9)
     x, p, s, y = probs[0]
-    with pytest.raises(w4.W4Error) as e:  # M = 17 is not small-M
-        x17 = wl.random_bf16((17, 256), 1.0, seed=1, device=DEV)
-        w4.w4_grouped_plan([(x17, p, s, torch.empty((17, 64), dtype=torch.bfloat16, device=DEV))])
-    assert e.value.status == w4.W4_ERR_UNSUPPORTED
     with pytest.raises(w4.W4Error) as e:  # two problems writing the same output
         w4.w4_grouped_plan([(x, p, s, y), (probs[1][0], probs[1][1], probs[1][2], y)])
     assert e.value.status == w4.W4_ERR_INVALID_ARG
@@ -118,4 +135,23 @@ def test_grouped_stack_subset(cuda_lib):
     torch.cuda.synchronize()
     for j, (W, (x, _, _, y)) in enumerate(zip(Ws, probs)):
         rows = torch.from_numpy(sample_rows(W.shape[0], 48, seed=j)).to(DEV)
+        check_gemm(W[rows].cpu(), x, y[:, rows])
+
+
+@pytest.mark.slow
+def test_grouped_layer70b_m208_sampled(cuda_lib):
+    shapes = wl.SHAPES["layer70b"]
+    Ws, probs = [], []
+    for i, (N, K) in enumerate(shapes):
+        W = wl.weight("layer70b", i, device=DEV)
+        packed, scales = quantize_gpu(cuda_lib, W)
+        x = wl.activations("layer70b", 208, K, i, device=DEV)
+        Ws.append(W)
+        probs.append((x, packed, scales, torch.empty((208, N), dtype=torch.bfloat16, device=DEV)))
+    plan = w4.w4_grouped_plan(probs)
+    w4.w4_gemm_grouped(plan)
+    torch.cuda.synchronize()
+    assert w4.w4_last_device_status() == 0
+    for i, (W, (x, _, _, y)) in enumerate(zip(Ws, probs)):
+        rows = torch.from_numpy(sample_rows(W.shape[0], 32, seed=i)).to(DEV)
         check_gemm(W[rows].cpu(), x, y[:, rows])
