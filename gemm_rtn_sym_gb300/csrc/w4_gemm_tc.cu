@@ -10,16 +10,18 @@
 //
 // Tile: 128 weight rows (the MMA's M) × up to 256 tokens (the MMA's N; the
 // token count is rounded up to a multiple of 16, padding rows of x read as
-// zeros) per CTA, K streamed in blocks of 64 through a 4-stage ring; a cluster
-// of up to 8 CTAs may split K (whole groups each) and sum its fp32 partials
-// over distributed shared memory.
+// zeros) per CTA, K streamed one group (128) per stage through a 3-stage ring;
+// a cluster of up to 8 CTAs may split K (whole groups each) and sum its fp32
+// partials over distributed shared memory.
 //   warp 0      : TMA loads of x tiles (128-byte swizzle) into the ring;
-//   warp 1      : allocates TMEM, one lane issues 4 MMAs (K = 16 each) per
+//   warp 1      : allocates TMEM, one lane issues 8 MMAs (K = 16 each) per
 //                 stage with A read from TMEM, B from shared memory, and
-//                 commits each stage back to its "empty" barrier;
-//   warps 2..9  : one weight row and 32 k per thread — read 16 bytes of codes
+//                 commits each stage back to its "empty" barrier (a 64-k stage
+//                 left the issuing thread's barrier and commit overhead per
+//                 stage as large as the MMAs' own time at N ≈ 200);
+//   warps 2..9  : one weight row and 64 k per thread — read 32 bytes of codes
 //                 from the code ring, decode nibble pairs to bf16 q, multiply
-//                 by d (bf16, round-to-nearest) and store the 16 columns into
+//                 by d (bf16, round-to-nearest) and store the 32 columns into
 //                 the stage's A slot with tcgen05.st; after the last stage,
 //                 read the accumulator back and store y (or the partial);
 //   warp 10     : TMA loads of codes, two groups × 128 rows per copy.
@@ -41,9 +43,9 @@ namespace w4 {
 namespace {
 
 constexpr int kBN = 128;            // weight rows per CTA = MMA M
-constexpr int kBK = 64;             // k per stage
-constexpr int kStages = 4;          // A (decoded, in TMEM) + B (activation, shared memory) stages
-constexpr int kCodeStages = 4;      // code stages of two groups (4 k-blocks) each: 16 k-blocks ahead
+constexpr int kBK = 128;            // k per stage: one group
+constexpr int kStages = 3;          // A (decoded, in TMEM) + B (activation, shared memory) stages
+constexpr int kCodeStages = 2;      // code stages of two groups (two k stages) each
 constexpr int kCodeStageBytes = 2 * kBN * 64;  // 16 KB: [group][row][64 B], 64-byte swizzle
 // Warps: 0 activation TMA, 1 TMEM + MMA, 2..9 dequantise + epilogue (two per
 // TMEM lane quarter, each one half of the k-block), 10 code TMA.
@@ -52,8 +54,8 @@ constexpr int kDequantWarps = 8;
 constexpr int kCodeWarp = kDequantWarp0 + kDequantWarps;
 constexpr int kThreads = 32 * (kCodeWarp + 1);
 constexpr int kMaxBM = 256;
-// Tensor memory: accumulator in columns [0, 256), decoded A stages of 32
-// columns (64 k of bf16 pairs) from column 256.  The whole 512 columns are
+// Tensor memory: accumulator in columns [0, 256), decoded A stages of 64
+// columns (128 k of bf16 pairs) from column 256.  The whole 512 columns are
 // taken, so the shared memory request below keeps one CTA per SM.
 constexpr uint32_t kColA = 256;
 constexpr uint32_t kTmemCols = 512;
@@ -84,7 +86,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
     uint8_t* gbase = smem_raw + (base - raw);
 
     const int bm = args.bm;
-    const uint32_t b_tile_bytes = static_cast<uint32_t>(bm) * 128u;
+    const uint32_t b_half_bytes = static_cast<uint32_t>(bm) * 128u;  // one 64-k sub-tile
+    const uint32_t b_tile_bytes = 2u * b_half_bytes;
     const uint32_t b_base = base;
     const uint32_t code_base = b_base + kStages * b_tile_bytes;
     const uint32_t bar_base = code_base + kCodeStages * kCodeStageBytes;
@@ -108,8 +111,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
     // K range of this CTA, in whole groups (a code stage holds two groups).
     const int64_t g_lo = (static_cast<int64_t>(rank) * G) / split;
     const int64_t g_hi = (static_cast<int64_t>(rank + 1) * G) / split;
-    const int kb_lo = static_cast<int>(2 * g_lo);
-    const int nkb = static_cast<int>(2 * (g_hi - g_lo));
+    const int kb_lo = static_cast<int>(g_lo);  // stages are groups
+    const int nkb = static_cast<int>(g_hi - g_lo);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -119,7 +122,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
         }
         for (int c = 0; c < kCodeStages; ++c) {
             mbar_init(code_full(c), 1);
-            mbar_init(code_empty(c), 32 * kDequantWarps * 4);  // every dequantiser, once per k-block
+            mbar_init(code_empty(c), 32 * kDequantWarps * 2);  // every dequantiser, once per k stage
         }
         mbar_init(accum_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -143,6 +146,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
                 if (!mbar_wait(empty(s), (r & 1u) ^ 1u)) { ok = false; break; }
                 mbar_arrive_expect_tx(full_b(s), b_tile_bytes);
                 tma_load_2d(b_base + s * b_tile_bytes, &tmap_x, (kb_lo + kb) * kBK, static_cast<int>(m0), full_b(s));
+                tma_load_2d(b_base + s * b_tile_bytes + b_half_bytes, &tmap_x, (kb_lo + kb) * kBK + 64,
+                            static_cast<int>(m0), full_b(s));
                 issued = kb + 1;
             }
             if (!ok) {
@@ -155,7 +160,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
     } else if (warp == kCodeWarp) {
         // ------------------------------------------------ codes via TMA
         if (lane == 0) {
-            const int nst = (nkb + 3) / 4;
+            const int nst = (nkb + 1) / 2;
             int issued = 0;
             for (int t = 0; t < nst; ++t) {
                 const int c = t % kCodeStages;
@@ -165,7 +170,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
                 }
                 mbar_arrive_expect_tx(code_full(c), kCodeStageBytes);
                 tma_load_3d(code_base + c * kCodeStageBytes, &tmap_codes, 0, static_cast<int>(n0),
-                            static_cast<int>(g_lo + 2 * t), code_full(c));
+                            static_cast<int>(g_lo + 2 * t), code_full(c));  // groups beyond g_hi are not read by this CTA
                 issued = t + 1;
             }
             if (!ok) {
@@ -183,11 +188,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
                 const uint32_t par = static_cast<uint32_t>(kb / kStages) & 1u;
                 if (!mbar_wait(full_b(s), par) || !mbar_wait(full_a(s), par)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t a_s = tmem_d + kColA + 32u * s;
+                const uint32_t a_s = tmem_d + kColA + 64u * s;
                 const uint32_t b_s = b_base + s * b_tile_bytes;
 #pragma unroll
                 for (int ks = 0; ks < kBK / 16; ++ks)
-                    mma_bf16_tmem_a(tmem_d, a_s + 8u * ks, sw128_desc(b_s + ks * 32), idesc,
+                    mma_bf16_tmem_a(tmem_d, a_s + 8u * ks,
+                                    sw128_desc(b_s + (ks >> 2) * b_half_bytes + (ks & 3) * 32), idesc,
                                     (kb | ks) != 0 ? 1u : 0u);
                 mma_commit(empty(s));
             }
@@ -197,7 +203,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
     } else {
         // ------------------------------------------------ dequantisers
         const int quarter = warp & 3;               // TMEM lane quarter this warp may access
-        const int half = (warp - kDequantWarp0) >> 2;  // which 32 k of each 64-k block
+        const int half = (warp - kDequantWarp0) >> 2;  // which 64 k of each group
         const int t = quarter * 32 + lane;          // weight row within the tile
         const uint32_t lane_base = tmem_d + (static_cast<uint32_t>(quarter * 32) << 16);
         const int64_t n = n0 + t < args.N ? n0 + t : args.N - 1;  // padding rows: zero codes, valid scale
@@ -205,25 +211,25 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
         // Row t of a code stage: 64 bytes per group, 16-byte chunk c at c ^ ((t >> 1) & 3).
         const uint32_t row_off = static_cast<uint32_t>(t * 64);
         const uint32_t sw = static_cast<uint32_t>((t >> 1) & 3);
-        uint32_t d_next = nkb > 0 ? __ldg(srow + (kb_lo >> 1)) : 0u;
+        uint32_t d_next = nkb > 0 ? __ldg(srow + kb_lo) : 0u;
         for (int kb = 0; kb < nkb && ok; ++kb) {
             const int s = kb % kStages;
             const uint32_t r = static_cast<uint32_t>(kb / kStages);
-            const int cst = (kb >> 2) % kCodeStages;
-            const int sub = kb & 3;  // k-block within the code stage
+            const int cst = (kb >> 1) % kCodeStages;
+            const int sub = kb & 1;  // group within the code stage
             const uint32_t dbits = d_next;
-            if (kb + 1 < nkb) d_next = __ldg(srow + ((kb_lo + kb + 1) >> 1));
-            const bool have = mbar_wait(code_full(cst), static_cast<uint32_t>((kb >> 2) / kCodeStages) & 1u);
+            if (kb + 1 < nkb) d_next = __ldg(srow + kb_lo + kb + 1);
+            const bool have = mbar_wait(code_full(cst), static_cast<uint32_t>((kb >> 1) / kCodeStages) & 1u);
             if (!__all_sync(0xffffffffu, have)) { ok = false; break; }
-            const uint32_t chunk = static_cast<uint32_t>(2 * (sub & 1) + half);
-            const uint4 q = lds128(code_base + cst * kCodeStageBytes + (sub >> 1) * (kBN * 64) + row_off +
-                                   ((chunk ^ sw) << 4));
+            const uint32_t grp = code_base + cst * kCodeStageBytes + sub * (kBN * 64) + row_off;
+            const uint4 q0 = lds128(grp + (((2u * half) ^ sw) << 4));
+            const uint4 q1 = lds128(grp + (((2u * half + 1u) ^ sw) << 4));
             const uint32_t d2bits = dbits | (dbits << 16);
             const __nv_bfloat162 d2 = *reinterpret_cast<const __nv_bfloat162*>(&d2bits);
-            const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-            uint32_t v[16];
+            const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+            uint32_t v[32];  // column 4w + i of this thread's 32: pair i of word w
 #pragma unroll
-            for (int w = 0; w < 4; ++w)
+            for (int w = 0; w < 8; ++w)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) v[4 * w + i] = deq_pair(words[w], i, d2);
             // The code slot is released only once its words have been used: the
@@ -233,7 +239,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             const bool free_stage = mbar_wait(empty(s), (r & 1u) ^ 1u);
             if (!__all_sync(0xffffffffu, free_stage)) { ok = false; break; }
             tc_fence_after();
-            tmem_st16(lane_base + kColA + 32u * s + 16u * half, v);
+            tmem_st32(lane_base + kColA + 64u * s + 32u * half, v);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(full_a(s));
@@ -371,7 +377,7 @@ cudaError_t encode_x_stage_map(CUtensorMap* map, const void* x, int64_t M, int64
 namespace {
 
 int smem_bytes(int bm) {
-    const int need = kStages * bm * 128 + kCodeStages * kCodeStageBytes + 8 * (3 * kStages + 2 * kCodeStages + 2) + 1024;
+    const int need = kStages * bm * 256 + kCodeStages * kCodeStageBytes + 8 * (3 * kStages + 2 * kCodeStages + 2) + 1024;
     const int red = bm * kBN * 4 + 1024;  // split-K partials reuse the rings
     const int n = need > red ? need : red;
     return n > kMinSmemBytes ? n : kMinSmemBytes;
@@ -409,8 +415,8 @@ cudaError_t launch_gemm_tc(const void* x, int64_t M, int64_t N, int64_t K, const
         }
     }
     // Split-K over a cluster when the tiles alone leave SMs idle: pick the
-    // cluster size (1..8, at least 4 k-blocks per CTA) that needs the fewest
-    // rounds of k-block work, given how many such clusters fit at once.
+    // cluster size (1..8, at least 2 groups per CTA) that needs the fewest
+    // rounds of k-stage work, given how many such clusters fit at once.
     const int64_t nkb_all = K / kBK;
     int split = 1;
     {
@@ -434,7 +440,7 @@ cudaError_t launch_gemm_tc(const void* x, int64_t M, int64_t N, int64_t K, const
             }
             const int64_t waves = (n_tiles * m_tiles + clusters - 1) / clusters;
             const double cost = static_cast<double>(waves) * static_cast<double>((nkb_all + s - 1) / s) +
-                                (s > 1 ? 2.0 : 0.0);  // the reduction costs about two k-blocks
+                                (s > 1 ? 1.0 : 0.0);  // the reduction costs about one k stage
             if (best == 0.0 || cost < best) {
                 best = cost;
                 split = s;
