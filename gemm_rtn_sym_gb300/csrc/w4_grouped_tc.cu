@@ -29,9 +29,9 @@ namespace w4 {
 namespace {
 
 constexpr int kBN = 128;            // weight rows per tile = MMA M
-constexpr int kBK = 64;             // k per stage
-constexpr int kStages = 4;          // A (TMEM) + B (shared memory) stages
-constexpr int kCodeStages = 4;      // code stages of two groups (4 k-blocks) each
+constexpr int kBK = 128;            // k per stage: one group
+constexpr int kStages = 3;          // A (TMEM) + B (shared memory) stages
+constexpr int kCodeStages = 2;      // code stages of two groups (two k stages) each
 constexpr int kCodeStageBytes = 2 * kBN * 64;
 constexpr int kDequantWarp0 = 2;
 constexpr int kDequantWarps = 8;
@@ -60,7 +60,7 @@ struct alignas(128) TcProblem {
     int64_t M;
     int64_t N;
     int32_t G;
-    int32_t nkb;  // 64-k blocks
+    int32_t nkb;  // k stages (groups)
     int32_t bm;   // token rows per tile (multiple of 16, ≤ 256)
     int32_t reserved[21];
 };
@@ -91,7 +91,7 @@ gemm_tc_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
     const int i_begin = first[blockIdx.x];
     const int i_end = first[blockIdx.x + 1];
 
-    const uint32_t b_slot = static_cast<uint32_t>(hdr->max_bm) * 128u;
+    const uint32_t b_slot = static_cast<uint32_t>(hdr->max_bm) * 256u;  // two 64-k sub-tiles
     const uint32_t b_base = base;
     const uint32_t code_base = b_base + kStages * b_slot;
     const uint32_t bar_base = code_base + kCodeStages * kCodeStageBytes;
@@ -117,7 +117,7 @@ gemm_tc_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
         }
         for (int c = 0; c < kCodeStages; ++c) {
             mbar_init(code_full(c), 1);
-            mbar_init(code_empty(c), 32 * kDequantWarps * 4);  // every dequantiser, once per k-block
+            mbar_init(code_empty(c), 32 * kDequantWarps * 2);  // every dequantiser, once per k stage
         }
         mbar_init(accum_bar, 1);
         mbar_init(acc_empty, 32 * kDequantWarps);
@@ -143,14 +143,15 @@ gemm_tc_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
                 const TcProblem* pr = probs + items[i].x;
                 tensormap_acquire(&pr->x);
                 const int m0 = static_cast<int>(items[i].z) * pr->bm;
-                const uint32_t bytes = static_cast<uint32_t>(pr->bm) * 128u;
+                const uint32_t half_bytes = static_cast<uint32_t>(pr->bm) * 128u;
                 for (int kb = 0; kb < pr->nkb; ++kb) {
                     if (!mbar_wait(empty(s), ph ^ 1u)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(full_b(s), bytes);
+                    mbar_arrive_expect_tx(full_b(s), 2u * half_bytes);
                     tma_load_2d(b_base + s * b_slot, &pr->x, kb * kBK, m0, full_b(s));
+                    tma_load_2d(b_base + s * b_slot + half_bytes, &pr->x, kb * kBK + 64, m0, full_b(s));
                     ++issued;
                     if (++s == kStages) {
                         s = 0;
@@ -175,7 +176,7 @@ gemm_tc_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
                 const TcProblem* pr = probs + items[i].x;
                 tensormap_acquire(&pr->codes);
                 const int n0 = static_cast<int>(items[i].y) * kBN;
-                const int nst = (pr->nkb + 3) / 4;
+                const int nst = (pr->nkb + 1) / 2;
                 for (int t = 0; t < nst; ++t) {
                     if (!mbar_wait(code_empty(c), ph ^ 1u)) {
                         ok = false;
@@ -206,8 +207,7 @@ gemm_tc_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
             for (int i = i_begin; i < i_end && ok; ++i) {
                 const TcProblem* pr = probs + items[i].x;
                 const uint32_t idesc = idesc_bf16(pr->bm);
-                const uint32_t bytes = static_cast<uint32_t>(pr->bm) * 128u;
-                (void)bytes;
+                const uint32_t half_bytes = static_cast<uint32_t>(pr->bm) * 128u;
                 // The previous item's accumulator must have been read out.
                 if (!mbar_wait(acc_empty, acc_ph ^ 1u)) {
                     ok = false;
@@ -221,12 +221,12 @@ gemm_tc_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_s = tmem_d + kColA + 32u * s;
+                    const uint32_t a_s = tmem_d + kColA + 64u * s;
                     const uint32_t b_s = b_base + s * b_slot;
 #pragma unroll
                     for (int ks = 0; ks < kBK / 16; ++ks)
-                        mma_bf16_tmem_a(tmem_d, a_s + 8u * ks, sw128_desc(b_s + ks * 32), idesc,
-                                        (kb | ks) != 0 ? 1u : 0u);
+                        mma_bf16_tmem_a(tmem_d, a_s + 8u * ks, sw128_desc(b_s + (ks >> 2) * half_bytes + (ks & 3) * 32),
+                                        idesc, (kb | ks) != 0 ? 1u : 0u);
                     mma_commit(empty(s));
                     if (++s == kStages) {
                         s = 0;
@@ -265,34 +265,31 @@ gemm_tc_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
             if (ok) {
                 uint32_t d_next = __ldg(srow);
                 for (int kb = 0; kb < nkb; ++kb) {
-                    const int sub = kb & 3;  // k-block within the code stage
+                    const int sub = kb & 1;  // group within the code stage
                     const uint32_t dbits = d_next;
-                    if (kb + 1 < nkb) d_next = __ldg(srow + ((kb + 1) >> 1));
+                    if (kb + 1 < nkb) d_next = __ldg(srow + kb + 1);
                     const bool have = mbar_wait(code_full(c), cph);
                     if (!__all_sync(0xffffffffu, have)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t chunk = static_cast<uint32_t>(2 * (sub & 1) + half);
-                    const uint4 q = lds128(code_base + c * kCodeStageBytes + (sub >> 1) * (kBN * 64) + row_off +
-                                           ((chunk ^ sw) << 4));
+                    const uint32_t grp = code_base + c * kCodeStageBytes + sub * (kBN * 64) + row_off;
+                    const uint4 q0 = lds128(grp + (((2u * half) ^ sw) << 4));
+                    const uint4 q1 = lds128(grp + (((2u * half + 1u) ^ sw) << 4));
                     const uint32_t d2bits = dbits | (dbits << 16);
                     const __nv_bfloat162 d2 = *reinterpret_cast<const __nv_bfloat162*>(&d2bits);
-                    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-                    uint32_t v[16];
+                    const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                    uint32_t v[32];
 #pragma unroll
-                    for (int w = 0; w < 4; ++w)
+                    for (int w = 0; w < 8; ++w)
 #pragma unroll
                         for (int p = 0; p < 4; ++p) v[4 * w + p] = deq_pair(words[w], p, d2);
                     // Release the code slot only after its words have been used
                     // (the shared-memory load may still be pending at an arrive).
                     mbar_arrive(code_empty(c));
-                    if (sub == 3 || kb + 1 == nkb) {
-                        // A last stage with two k-blocks still owes two arrivals.
-                        if (sub == 1) {
-                            mbar_arrive(code_empty(c));
-                            mbar_arrive(code_empty(c));
-                        }
+                    if (sub == 1 || kb + 1 == nkb) {
+                        // A last stage holding one group still owes one arrival.
+                        if (sub == 0) mbar_arrive(code_empty(c));
                         if (++c == kCodeStages) {
                             c = 0;
                             cph ^= 1u;
@@ -304,7 +301,7 @@ gemm_tc_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
                         break;
                     }
                     tc_fence_after();
-                    tmem_st16(lane_base + kColA + 32u * s + 16u * half, v);
+                    tmem_st32(lane_base + kColA + 64u * s + 32u * half, v);
                     tmem_wait_st();
                     tc_fence_before();
                     mbar_arrive(full_a(s));
@@ -353,7 +350,7 @@ gemm_tc_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
 }
 
 int tc_grouped_smem_bytes(int max_bm) {
-    const int need = kStages * max_bm * 128 + kCodeStages * kCodeStageBytes + 8 * (3 * kStages + 2 * kCodeStages + 4) +
+    const int need = kStages * max_bm * 256 + kCodeStages * kCodeStageBytes + 8 * (3 * kStages + 2 * kCodeStages + 4) +
                      1024;
     return need > kMinSmemBytes ? need : kMinSmemBytes;
 }
@@ -407,12 +404,12 @@ cudaError_t tc_grouped_plan_build(const GroupedSpec* specs, int32_t count, int32
         pr.M = sp.M;
         pr.N = sp.N;
         pr.G = static_cast<int32_t>(sp.K / 128);
-        pr.nkb = static_cast<int32_t>(sp.K / kBK);
+        pr.nkb = static_cast<int32_t>(sp.K / kBK);  // groups
         pr.bm = static_cast<int32_t>(bm);
         std::memcpy(out->data() + sizeof(TcHeader) + sizeof(TcProblem) * i, &pr, sizeof(pr));
         const int64_t n_tiles = (sp.N + kBN - 1) / kBN;
-        // Cost of a tile: its k-blocks, each an MMA of N = bm (plus its epilogue).
-        const int32_t cost = static_cast<int32_t>(pr.nkb * (bm + 32) / 32 + bm / 8);
+        // Cost of a tile: its k stages, each 8 MMAs of N = bm, plus its epilogue.
+        const int32_t cost = static_cast<int32_t>(pr.nkb * (bm + 32) / 16 + bm / 8);
         for (int64_t mt = 0; mt < m_tiles; ++mt)
             for (int64_t nt = 0; nt < n_tiles; ++nt)
                 list.push_back({cost, make_uint4(static_cast<unsigned>(i), static_cast<unsigned>(nt),
