@@ -320,11 +320,19 @@ def gemm_set(torch, w4, wl, workload, Ms, pk, reps=20, path=None, grouped=False)
             ys.append(torch.empty((M, N), dtype=torch.bfloat16, device=dev))
 
         if grouped:
-            plan = w4.w4_grouped_plan([(xs[(K, i if workload != "stack4b" else 0)], p, s, ys[j])
-                                       for j, (N, K, p, s, i) in enumerate(mats)])
+            # One plan per copy of the workload (a layer, or the whole stack):
+            # copies exist only to rotate inputs through L2, and must not
+            # enlarge the group a launch balances its work over.
+            n_per = len(mats) // copies
+            plans = [w4.w4_grouped_plan([(xs[(K, i if workload != "stack4b" else 0)], p, s, ys[j])
+                                         for j, (N, K, p, s, i) in enumerate(mats)
+                                         if j % copies == c])
+                     for c in range(copies)]
+            assert all(len(pl.tensors) == 4 * n_per for pl in plans)
 
             def run():
-                w4.w4_gemm_grouped(plan)
+                for pl in plans:
+                    w4.w4_gemm_grouped(pl)
         else:
             def run():
                 for j, (N, K, p, s, i) in enumerate(mats):
@@ -346,8 +354,8 @@ def gemm_set(torch, w4, wl, workload, Ms, pk, reps=20, path=None, grouped=False)
                         "path": "grouped" if grouped else
                         (w4.w4_gemm_path_for(M, mats[0][0], mats[0][1]) if path is None else path)}
         if grouped:
-            out[f"M{M}"]["launches"] = 1
-            del plan
+            out[f"M{M}"]["launches_per_set"] = 1
+            del plans
         del g, ys, xs
     assert w4.w4_last_device_status() == 0
     del mats

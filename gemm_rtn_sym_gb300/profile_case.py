@@ -3,10 +3,12 @@
     python -m gemm_rtn_sym_gb300.profile_case quantize --workload outlier
     python -m gemm_rtn_sym_gb300.profile_case gemm --workload outlier --M 8
     python -m gemm_rtn_sym_gb300.profile_case gemm --workload layer70b --matrix 2 --M 208
+    python -m gemm_rtn_sym_gb300.profile_case grouped --workload layer27b --M 1
 
 The inputs are the seeded synthetic matrices of ``workloads``.  For ``gemm`` the
 weights are quantised first (one quantiser launch), then the matmul runs
-``--launches`` times on the same inputs.  The case checks the device status
+``--launches`` times on the same inputs.  ``grouped`` quantises every matrix
+of the workload and runs one grouped plan over all of them.  The case checks the device status
 word at the end and exits non-zero if any wait timed out.  It times nothing:
 numbers taken under a profiler are not benchmark results.
 """
@@ -18,7 +20,7 @@ import sys
 import torch
 
 from . import W4_PATH_AUTO, W4_PATH_SMALL_M, W4_PATH_TENSOR
-from . import load, w4_gemm_ex, w4_last_device_status, w4_quantize_rtn
+from . import load, w4_gemm_ex, w4_gemm_grouped, w4_grouped_plan, w4_last_device_status, w4_quantize_rtn
 from . import workloads as wl
 
 PATHS = {"auto": W4_PATH_AUTO, "small": W4_PATH_SMALL_M, "tensor": W4_PATH_TENSOR}
@@ -26,7 +28,7 @@ PATHS = {"auto": W4_PATH_AUTO, "small": W4_PATH_SMALL_M, "tensor": W4_PATH_TENSO
 
 def main(argv=None) -> int:
     p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
-    p.add_argument("kernel", choices=["quantize", "gemm"])
+    p.add_argument("kernel", choices=["quantize", "gemm", "grouped"])
     p.add_argument("--workload", default="outlier", choices=sorted(wl.SHAPES))
     p.add_argument("--matrix", type=int, default=0, help="index into the workload's matrices")
     p.add_argument("--M", type=int, default=8, help="token rows of x (gemm)")
@@ -37,6 +39,22 @@ def main(argv=None) -> int:
     load()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
+    if a.kernel == "grouped":
+        problems = []
+        for i, (N, K) in enumerate(wl.SHAPES[a.workload]):
+            W = wl.weight(a.workload, i, device=dev)
+            packed, scales = w4_quantize_rtn(W)
+            del W
+            x = wl.activations(a.workload, a.M, K, i, device=dev)
+            problems.append((x, packed, scales, torch.empty((a.M, N), dtype=torch.bfloat16, device=dev)))
+        plan = w4_grouped_plan(problems)
+        for _ in range(a.launches):
+            w4_gemm_grouped(plan)
+        torch.cuda.synchronize()
+        status = w4_last_device_status(dev)
+        print(f"grouped {a.workload} M={a.M}: {len(problems)} problems, {plan.items} items, "
+              f"{a.launches} launches, device status {status}")
+        return 0 if status == 0 else 1
     N, K = wl.SHAPES[a.workload][a.matrix]
     W = wl.weight(a.workload, a.matrix, device=dev)
     packed = torch.empty((N, K // 2), dtype=torch.uint8, device=dev)
