@@ -200,10 +200,13 @@ size_t w4_grouped_plan_bytes(int32_t count, const w4_gemm_problem* problems) {
     return bytes;
 }
 
-int w4_grouped_plan_init(w4_grouped_plan* plan, void* device_memory, size_t bytes, int32_t count,
-                         const w4_gemm_problem* problems) {
-    if (!plan || !device_memory || count < 1 || !problems) return W4_ERR_INVALID_ARG;
-    if (!aligned(device_memory, 128)) return W4_ERR_MISALIGNED;
+namespace {
+
+// Validates the problems (against each other and, when device_memory is not
+// NULL, against the plan memory), builds the plan image and fills every field
+// of *plan except device_plan.
+int grouped_prepare(const void* device_memory, size_t bytes, int32_t count, const w4_gemm_problem* problems,
+                    std::vector<uint8_t>* image, w4_grouped_plan* plan) {
     int token_tiles = 1;
     std::vector<GroupedSpec> small, tc;
     for (int32_t i = 0; i < count; ++i) {
@@ -217,8 +220,9 @@ int w4_grouped_plan_init(w4_grouped_plan* plan, void* device_memory, size_t byte
             if (overlaps(p.y, yb, q.x, xb) || overlaps(p.y, yb, q.packed, pb) || overlaps(p.y, yb, q.scales, sb))
                 return W4_ERR_INVALID_ARG;
             if (j != i && overlaps(p.y, yb, q.y, out_bytes(q))) return W4_ERR_INVALID_ARG;
-            if (overlaps(device_memory, bytes, q.x, xb) || overlaps(device_memory, bytes, q.packed, pb) ||
-                overlaps(device_memory, bytes, q.scales, sb) || overlaps(device_memory, bytes, q.y, out_bytes(q)))
+            if (device_memory &&
+                (overlaps(device_memory, bytes, q.x, xb) || overlaps(device_memory, bytes, q.packed, pb) ||
+                 overlaps(device_memory, bytes, q.scales, sb) || overlaps(device_memory, bytes, q.y, out_bytes(q))))
                 return W4_ERR_INVALID_ARG;
         }
         const GroupedSpec sp{p.x, p.M, p.N, p.K, p.packed, p.scales, p.y};
@@ -233,33 +237,31 @@ int w4_grouped_plan_init(w4_grouped_plan* plan, void* device_memory, size_t byte
     const DeviceInfo* dev = device_info(&err);
     if (!dev) return W4_ERR_CUDA;
     if (dev->cc_major < 10) return W4_ERR_UNSUPPORTED;
-    std::vector<uint8_t> image, tc_image;
+    std::vector<uint8_t> tc_image;
     int64_t n_items = 0, n_tc_items = 0;
     int32_t n_ctas = 0, n_tc_ctas = 0;
+    image->clear();
     if (!small.empty()) {
         const int ctas = grouped_ctas(token_tiles, *dev);
         if (ctas < 1) return W4_ERR_CUDA;
-        if (grouped_plan_build(small.data(), static_cast<int32_t>(small.size()), token_tiles, ctas, &image, &n_items,
+        if (grouped_plan_build(small.data(), static_cast<int32_t>(small.size()), token_tiles, ctas, image, &n_items,
                                &n_ctas) != cudaSuccess)
             return W4_ERR_CUDA;
-        image.resize(round128(image.size()), 0);
+        image->resize(round128(image->size()), 0);
     }
-    const size_t tc_offset = image.size();
+    const size_t tc_offset = image->size();
     if (!tc.empty()) {
         if (tc_grouped_plan_build(tc.data(), static_cast<int32_t>(tc.size()), dev->sm_count, &tc_image, &n_tc_items,
                                   &n_tc_ctas) != cudaSuccess)
             return W4_ERR_CUDA;
-        image.insert(image.end(), tc_image.begin(), tc_image.end());
+        image->insert(image->end(), tc_image.begin(), tc_image.end());
     }
-    if (bytes < image.size()) return W4_ERR_INVALID_ARG;
-    if (cudaMemcpy(device_memory, image.data(), image.size(), cudaMemcpyHostToDevice) != cudaSuccess)
-        return W4_ERR_CUDA;
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess) return W4_ERR_CUDA;
     int max_bm = 0;
     if (!tc.empty()) std::memcpy(&max_bm, tc_image.data() + 12, sizeof(int));  // TcHeader::max_bm
-    plan->device_plan = device_memory;
-    plan->bytes = image.size();
+    plan->device_plan = nullptr;
+    plan->bytes = image->size();
     plan->count = count;
     plan->device = device;
     plan->items = static_cast<int32_t>(n_items);
@@ -269,6 +271,23 @@ int w4_grouped_plan_init(w4_grouped_plan* plan, void* device_memory, size_t byte
     plan->tc_ctas = n_tc_ctas;
     plan->tc_max_bm = max_bm;
     plan->tc_offset = tc_offset;
+    return W4_OK;
+}
+
+}  // namespace
+
+int w4_grouped_plan_init(w4_grouped_plan* plan, void* device_memory, size_t bytes, int32_t count,
+                         const w4_gemm_problem* problems) {
+    if (!plan || !device_memory || count < 1 || !problems) return W4_ERR_INVALID_ARG;
+    if (!aligned(device_memory, 128)) return W4_ERR_MISALIGNED;
+    std::vector<uint8_t> image;
+    w4_grouped_plan p;
+    if (const int s = grouped_prepare(device_memory, bytes, count, problems, &image, &p)) return s;
+    if (bytes < image.size()) return W4_ERR_INVALID_ARG;
+    if (cudaMemcpy(device_memory, image.data(), image.size(), cudaMemcpyHostToDevice) != cudaSuccess)
+        return W4_ERR_CUDA;
+    p.device_plan = device_memory;
+    *plan = p;
     return W4_OK;
 }
 
