@@ -20,7 +20,7 @@ __all__ = [
     "w4_quantize_rtn", "w4_gemm", "w4_gemm_ex", "w4_gemm_path_for",
     "w4_packed_bytes", "w4_scales_bytes", "w4_last_device_status", "w4_wait_probe",
     "w4_status_string", "W4_PATH_AUTO", "W4_PATH_SMALL_M", "W4_PATH_TENSOR", "GROUP",
-    "GroupedPlan", "w4_grouped_plan", "w4_gemm_grouped",
+    "GroupedPlan", "w4_grouped_plan", "w4_gemm_grouped", "w4_gemm_grouped_noalloc",
 ]
 
 GROUP = 128
@@ -58,6 +58,7 @@ _SIGNATURES = {
     "w4_grouped_plan_bytes": (_sz, [_i32, ctypes.POINTER(_Problem)]),
     "w4_grouped_plan_init": (ctypes.c_int, [ctypes.POINTER(_Plan), _vp, _sz, _i32, ctypes.POINTER(_Problem)]),
     "w4_gemm_grouped": (ctypes.c_int, [ctypes.POINTER(_Plan), _vp]),
+    "w4_gemm_grouped_noalloc": (ctypes.c_int, [_i32, ctypes.POINTER(_Problem), _vp]),
 }
 
 
@@ -224,6 +225,35 @@ def w4_grouped_plan(problems) -> GroupedPlan:
         _check(load().w4_grouped_plan_init(ctypes.byref(plan), memory.data_ptr() + off, nbytes, len(problems), arr),
                "w4_grouped_plan_init")
     return GroupedPlan(memory, plan, tensors)
+
+
+def _problem_array(problems):
+    problems = list(problems)
+    if not problems:
+        raise ValueError("no problems")
+    arr = (_Problem * len(problems))()
+    device = problems[0][0].device
+    for i, (x, packed, scales, y) in enumerate(problems):
+        _cuda_tensor(x, "x", torch.bfloat16, 2)
+        _cuda_tensor(packed, "packed", torch.uint8, 2)
+        _cuda_tensor(scales, "scales", torch.bfloat16, 2)
+        _cuda_tensor(y, "y", torch.bfloat16, 2)
+        M, K = x.shape
+        N = packed.shape[0]
+        if tuple(packed.shape) != (N, K // 2) or tuple(scales.shape) != (N, K // GROUP) or tuple(y.shape) != (M, N):
+            raise ValueError(f"problem {i}: x / packed / scales / y shapes disagree")
+        if x.device != device or packed.device != device or scales.device != device or y.device != device:
+            raise ValueError("all tensors must be on one device")
+        arr[i] = _Problem(x.data_ptr(), M, N, K, packed.data_ptr(), scales.data_ptr(), y.data_ptr())
+    return arr, len(problems), device
+
+
+def w4_gemm_grouped_noalloc(problems) -> None:
+    """Every problem (x, packed, scales, y) through the library's static plan
+    buffer (no caller memory, no allocation; see w4.h for its race rules)."""
+    arr, n, device = _problem_array(problems)
+    with torch.cuda.device(device):
+        _check(load().w4_gemm_grouped_noalloc(n, arr, _stream(device)), "w4_gemm_grouped_noalloc")
 
 
 def w4_gemm_grouped(plan: GroupedPlan) -> None:

@@ -316,6 +316,25 @@ int w4_gemm_grouped(const w4_grouped_plan* plan, void* stream) {
     return W4_OK;
 }
 
+int w4_gemm_grouped_noalloc(int32_t count, const w4_gemm_problem* problems, void* stream) {
+    if (count < 1 || !problems) return W4_ERR_INVALID_ARG;
+    std::vector<uint8_t> image;
+    w4_grouped_plan p;
+    if (const int s = grouped_prepare(nullptr, 0, count, problems, &image, &p)) return s;
+    void* mem = nullptr;
+    size_t cap = 0;
+    if (static_plan_memory(&mem, &cap) != cudaSuccess) return W4_ERR_CUDA;
+    if (image.size() > cap) return W4_ERR_UNSUPPORTED;
+    // A pageable source: the copy waits for the stream's earlier work (so a
+    // previous call's kernels no longer read the buffer) and has been staged
+    // when it returns, so `image` may be released.
+    if (cudaMemcpyAsync(mem, image.data(), image.size(), cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return W4_ERR_CUDA;
+    p.device_plan = mem;
+    return w4_gemm_grouped(&p, stream);
+}
+
 int w4_last_device_status(void* stream) {
     cudaError_t err;
     const DeviceInfo* dev = device_info(&err);

@@ -39,6 +39,12 @@ namespace {
 
 using namespace gemv;
 
+// Plan memory of w4_gemm_grouped_noalloc: a file-scope device array, so that
+// entry point allocates nothing.  Shared by every call on a device (see the
+// race note in w4.h).
+constexpr size_t kStaticPlanBytes = size_t{2} << 20;
+static __device__ __align__(256) uint8_t g_static_plan[kStaticPlanBytes];
+
 // Device layout of a plan:
 //   GroupedHeader (128 B) | GroupedProblem[count] (384 B each) |
 //   int32 first[n_ctas + 1] (padded to 8 B) | uint2 items[n_items]
@@ -307,6 +313,22 @@ cudaError_t launch_grouped_t(const void* plan, int32_t n_ctas, const DeviceInfo&
 }
 
 }  // namespace
+
+cudaError_t static_plan_memory(void** ptr, size_t* bytes) {
+    static void* per_device[64];
+    int device = 0;
+    if (cudaError_t e = cudaGetDevice(&device)) return e;
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_grouped_mutex);
+    if (!per_device[device]) {
+        void* p = nullptr;
+        if (cudaError_t e = cudaGetSymbolAddress(&p, g_static_plan)) return e;
+        per_device[device] = p;
+    }
+    *ptr = per_device[device];
+    *bytes = kStaticPlanBytes;
+    return cudaSuccess;
+}
 
 size_t grouped_plan_bytes(int32_t count, int64_t n_items, int32_t n_ctas) {
     return sizeof(GroupedHeader) + sizeof(GroupedProblem) * static_cast<size_t>(count) +

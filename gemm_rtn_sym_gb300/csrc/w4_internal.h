@@ -63,6 +63,9 @@ int grouped_ctas(int token_tiles, const DeviceInfo& dev);
 // min(n_ctas, items) CTAs longest first.
 cudaError_t grouped_plan_build(const GroupedSpec* specs, int32_t count, int token_tiles, int32_t n_ctas,
                                std::vector<uint8_t>* out, int64_t* n_items, int32_t* n_ctas_used);
+// The device address and size of the library's static plan buffer on the
+// current device (w4_gemm_grouped_noalloc).
+cudaError_t static_plan_memory(void** ptr, size_t* bytes);
 // Runs a plan already copied to device memory.
 cudaError_t launch_grouped(const void* plan, int32_t n_ctas, int token_tiles, const DeviceInfo& dev,
                            cudaStream_t stream);

@@ -183,6 +183,27 @@ int w4_grouped_plan_init(w4_grouped_plan* plan, void* device_memory, size_t byte
 int w4_gemm_grouped(const w4_grouped_plan* plan, void* stream);
 
 /*
+ * w4_gemm_grouped_noalloc — the grouped matmul without caller memory for the
+ * plan: the plan is built on every call and copied into a 2 MB device array
+ * compiled into the library (found once per device with
+ * cudaGetSymbolAddress), then run on `stream`.  No device memory is
+ * allocated.  An implementation convenience with no counterpart in the pages:
+ * they describe the computation, not how its work lists are stored.
+ *   W4_ERR_UNSUPPORTED  the plan for these problems exceeds the 2 MB array
+ *                       (about 5000 problems, or about 250000 64-row blocks);
+ *   otherwise the checks and results of w4_grouped_plan_init + w4_gemm_grouped.
+ * Races: the array is shared by every call on a device.  Calls in order on
+ * one stream are safe (the plan copy waits for the stream's earlier work);
+ * calls that may overlap — other streams, other host threads, or a CUDA
+ * graph replaying a captured call while another call runs — can overwrite a
+ * plan a running kernel is reading, and give wrong results.  The host thread
+ * blocks until the stream's earlier work is done (pageable-memory copy), and
+ * the call cannot be captured into a CUDA graph; use w4_grouped_plan_init +
+ * w4_gemm_grouped for either.
+ */
+int w4_gemm_grouped_noalloc(int32_t count, const w4_gemm_problem* problems, void* stream);
+
+/*
  * Every wait inside the library's kernels (mbarrier phases, TMA completion)
  * is bounded.  A wait that runs out records W4_ERR_TIMEOUT in a per-device
  * status word and the kernel returns early (its outputs are then undefined).
