@@ -20,6 +20,10 @@ quantisation study, parksieon.github.io).
 * §2 settings table: RTN group 128, 4-bit weights / BF16 inputs, "minmax ·
   symmetric" range from the group's extremes, no clipping-ratio search, no
   calibration input.
+* §2 AWQ equation: scaling input channel j of W by s_j and of x by 1/s_j keeps
+  W'x' = Wx; the channel scale s_j is not the group scale d and is not limited
+  to powers of two (§2, paragraph after the equation).  W' is then quantised
+  like any other weight matrix.
 * §1 FFN example y = W x (2560×9216) and §2 Δy = (Ŵ − W) x: the matmul reads the
   restored weights ŵ = d·q against BF16 inputs.
 
@@ -36,6 +40,10 @@ same ones, independently):
 * NaN / Inf weights are outside the contract (results unspecified);
 * storage: packed u8 [N, K/2] whose 64-byte block per (row, group) uses the
   "P1" nibble order defined by :func:`p1_nibble_position`; scales bf16 [N, K/128];
+* AWQ channel scaling (§2 AWQ equation): s is a caller-supplied fp32 vector
+  of K finite positive scales; W' = bf16_rne(fp32(w·s_k)) is quantised by the
+  same RTN, and x' = bf16_rne(fp32(x / s_k)); results where w·s_k overflows
+  are unspecified, like Inf weights;
 * the matmul reference accumulates ŵ·x in fp64 (exact products), and the
   parity bound is |y_gpu − y_ref| ≤ 4e-3 · Σ_k |ŵ_k x_k| + ulp_bf16(y_ref).
 
@@ -188,6 +196,43 @@ def quantize_rtn(W_bits: np.ndarray, group: int = GROUP):
     s = rtn_scales(W_bits, group)
     q = rtn_codes(W_bits, s, group)
     return pack_p1(q), s
+
+
+# ---------------------------------------------------------------------------
+# AWQ-style channel scaling (§2 AWQ equation: W'_ij = W_ij·s_j, x'_j = x_j/s_j,
+# so that W'x' = Wx).  The caller supplies s; how s is searched (the §2 grid of
+# exponents over calibration statistics) is not part of this module.
+# ---------------------------------------------------------------------------
+def _channel_scales(s, K: int) -> np.ndarray:
+    s = np.asarray(s, dtype=np.float32)
+    if s.shape != (K,):
+        raise ValueError("s must be a vector of K channel scales")
+    if not np.all(np.isfinite(s)) or np.any(s <= 0):
+        raise ValueError("channel scales must be finite and positive")
+    return s
+
+
+def awq_scale_weights(W_bits: np.ndarray, s) -> np.ndarray:
+    """W'[n, k] = bf16_rne(fp32(w[n, k] · s[k])): the fp32 IEEE product of the
+    bf16 weight and the fp32 scale of its input channel k, rounded to bf16 with
+    ties to even.  uint16 [N, K]."""
+    w = bf16_bits_to_f32(np.asarray(W_bits, dtype=np.uint16))
+    s = _channel_scales(s, w.shape[1])
+    return f32_to_bf16_bits_rne((w * s[None, :]).astype(np.float32))
+
+
+def awq_scale_activations(x_bits: np.ndarray, s) -> np.ndarray:
+    """x'[m, k] = bf16_rne(fp32(x[m, k] / s[k])), the fp32 IEEE quotient.
+    uint16 [M, K]."""
+    x = bf16_bits_to_f32(np.asarray(x_bits, dtype=np.uint16))
+    s = _channel_scales(s, x.shape[1])
+    return f32_to_bf16_bits_rne((x / s[None, :]).astype(np.float32))
+
+
+def quantize_rtn_scaled(W_bits: np.ndarray, s, group: int = GROUP):
+    """RTN of the channel-scaled weights: quantize_rtn(W') with W' from
+    :func:`awq_scale_weights`.  Same storage as :func:`quantize_rtn`."""
+    return quantize_rtn(awq_scale_weights(W_bits, s), group)
 
 
 # ---------------------------------------------------------------------------

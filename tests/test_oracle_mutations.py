@@ -42,6 +42,16 @@ MUTANTS = {
                        "out[nz] = np.exp2(np.maximum(e, -126.0) - 6.0)"),
     "bf16_round_half_up": ("round_up = (rest > 0x8000) | ((rest == 0x8000) & ((kept & np.uint32(1)) == 1))",
                            "round_up = rest >= 0x8000"),
+    "awq_weights_divided": ("return f32_to_bf16_bits_rne((w * s[None, :]).astype(np.float32))",
+                            "return f32_to_bf16_bits_rne((w / s[None, :]).astype(np.float32))"),
+    "awq_channels_reversed": ("return f32_to_bf16_bits_rne((w * s[None, :]).astype(np.float32))",
+                              "return f32_to_bf16_bits_rne((w * s[None, ::-1]).astype(np.float32))"),
+    "awq_weights_truncated": ("return f32_to_bf16_bits_rne((w * s[None, :]).astype(np.float32))",
+                              "return ((w * s[None, :]).astype(np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)"),
+    "awq_inputs_multiplied": ("return f32_to_bf16_bits_rne((x / s[None, :]).astype(np.float32))",
+                              "return f32_to_bf16_bits_rne((x * s[None, :]).astype(np.float32))"),
+    "awq_scale_ignored": ("return quantize_rtn(awq_scale_weights(W_bits, s), group)",
+                          "return quantize_rtn(W_bits, group)"),
 }
 
 PIN_TESTS = [
@@ -62,6 +72,10 @@ PIN_TESTS = [
     pins.test_bf16_rne_against_exact,
     pins.test_bf16_ulp,
     pins.test_parity_bound_accepts_exact_and_rejects_offset,
+    pins.test_awq_unit_scale_is_plain_rtn,
+    lambda: pins.test_awq_bruteforce_4x256(71),
+    pins.test_awq_rounds_through_fp32,
+    pins.test_awq_power_of_two_group_scales,
 ]
 
 

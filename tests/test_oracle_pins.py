@@ -4,7 +4,7 @@ never against the oracle's own formulas retyped.
 Definition: Qwen3.5-4B quantisation study (parksieon.github.io), §1 group
 quantisation equation with z = 0, §1 group-of-128 paragraph (72 groups per row
 at 9216 inputs), §2 settings table (RTN minmax · symmetric, 4-bit weights /
-BF16 inputs), §2 AWQ identity W'x' = Wx.
+BF16 inputs), §2 AWQ equation W'_ij = W_ij·s_j, x'_j = x_j/s_j, W'x' = Wx.
 """
 import math
 import os
@@ -274,6 +274,126 @@ def test_channel_scaling_identity():
     loop = np.array([[math.fsum(W[n, k] * x[m, k] for k in range(384)) for n in range(24)]
                      for m in range(5)])
     assert np.allclose(y, loop, rtol=1e-12, atol=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# P4: AWQ channel scaling applied before RTN (§2 AWQ equation), against exact
+# rational arithmetic.  Reading: W' = bf16_rne(fp32(w·s_k)) and
+# x' = bf16_rne(fp32(x / s_k)), both rounded twice (fp32, then bf16).
+# ---------------------------------------------------------------------------
+def float_rne(v: Fraction, p: int, emin: int) -> Fraction:
+    """Nearest binary float with p significant bits and minimum normal exponent
+    emin to a rational (ties to even); no overflow."""
+    if v == 0:
+        return Fraction(0)
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    ulp = Fraction(2) ** (max(e, emin) - (p - 1))
+    r = round_half_even(a / ulp) * ulp
+    return r if v > 0 else -r
+
+
+def fp32_then_bf16_bits(v: Fraction, negative: bool) -> int:
+    return bf16_rne_bits(abs(float_rne(v, 24, -126))) | (0x8000 if negative else 0)
+
+
+def exact_scaled_weight(w_bits: int, s: float) -> int:
+    return fp32_then_bf16_bits(bf16_exact(w_bits) * Fraction(float(s)), bool(w_bits & 0x8000))
+
+
+def exact_scaled_input(x_bits: int, s: float) -> int:
+    return fp32_then_bf16_bits(bf16_exact(x_bits) / Fraction(float(s)), bool(x_bits & 0x8000))
+
+
+def test_awq_unit_scale_is_plain_rtn():
+    W = wl.bits(wl.random_bf16((5, 384), 0.02, seed=61))
+    x = wl.bits(wl.random_bf16((3, 384), 1.0, seed=62))
+    ones = np.ones(384, dtype=np.float32)
+    p0, d0 = O.quantize_rtn(W)
+    p1, d1 = O.quantize_rtn_scaled(W, ones)
+    assert np.array_equal(p0, p1) and np.array_equal(d0, d1)
+    assert np.array_equal(O.awq_scale_activations(x, ones), x)
+
+
+@pytest.mark.parametrize("seed", [71, 72])
+def test_awq_bruteforce_4x256(seed):
+    rng = np.random.default_rng(seed)
+    W = wl.bits(wl.random_bf16((4, 256), 0.02, seed=seed))
+    x = wl.bits(wl.random_bf16((3, 256), 1.0, seed=seed + 100))
+    s = np.exp2(rng.uniform(-3, 3, size=256)).astype(np.float32)
+    assert np.mean(np.log2(s) == np.round(np.log2(s))) < 0.01  # not powers of two
+    Wp = O.awq_scale_weights(W, s)
+    packed, d = O.quantize_rtn_scaled(W, s)
+    q = O.unpack_p1(packed, 256)
+    for n in range(4):
+        wp = [exact_scaled_weight(W[n, k], s[k]) for k in range(256)]
+        assert list(Wp[n]) == wp
+        for g in range(2):
+            d_bits, q_exact = exact_rtn_group(wp[128 * g: 128 * g + 128])
+            assert d[n, g] == d_bits
+            assert list(q[n, 128 * g: 128 * g + 128]) == q_exact
+    xp = O.awq_scale_activations(x, s)
+    for m in range(3):
+        assert list(xp[m]) == [exact_scaled_input(x[m, k], s[k]) for k in range(256)]
+
+
+def double_rounding_cases():
+    """(w bits, s) pairs whose exact product rounds to a bf16 tie in fp32, so
+    that rounding once (exact -> bf16) and twice (exact -> fp32 -> bf16) give
+    different bf16 results."""
+    out = []
+    for j in range(1, 128, 2):
+        w = Fraction(128 + j, 128)
+        for m in range(0, 128, 9):
+            tie = Fraction(256 + 2 * m + 1, 256)  # halfway between two bf16 in [1, 2)
+            s = float_rne(tie / w, 24, -126)
+            p = w * s
+            if p == tie or float_rne(p, 24, -126) != tie:
+                continue
+            if bf16_rne_bits(p) != bf16_rne_bits(tie):
+                out.append((bf16_rne_bits(w), float(s)))
+    return out
+
+
+def test_awq_rounds_through_fp32():
+    cases = double_rounding_cases()
+    assert len(cases) >= 50
+    W = np.array([[w for w, _ in cases]], dtype=np.uint16)
+    s = np.array([s for _, s in cases], dtype=np.float32)
+    Wp = O.awq_scale_weights(W, s)
+    for k, (w, sk) in enumerate(cases):
+        assert Wp[0, k] == exact_scaled_weight(w, sk)
+        assert Wp[0, k] != bf16_rne_bits(bf16_exact(w) * Fraction(float(sk)))
+
+
+def test_awq_power_of_two_group_scales():
+    """s constant 2^e over each group: W' = W·2^e exactly, so the codes are the
+    unscaled codes and every group scale is multiplied by 2^e exactly."""
+    W = wl.bits(wl.random_bf16((6, 512), 0.02, seed=81))
+    x = wl.bits(wl.random_bf16((2, 512), 1.0, seed=82))
+    e = np.array([-3.0, 0.0, 2.0, 5.0])
+    s = np.repeat(np.exp2(e), 128).astype(np.float32)
+    p0, d0 = O.quantize_rtn(W)
+    p1, d1 = O.quantize_rtn_scaled(W, s)
+    assert np.array_equal(p0, p1)
+    f0 = O.bf16_bits_to_f32(d0).astype(np.float64)
+    f1 = O.bf16_bits_to_f32(d1).astype(np.float64)
+    assert np.array_equal(f1, f0 * np.exp2(e)[None, :])
+    xf = O.bf16_bits_to_f32(x).astype(np.float64)
+    xs = O.bf16_bits_to_f32(O.awq_scale_activations(x, s)).astype(np.float64)
+    assert np.array_equal(xs, xf / s[None, :])
+
+
+def test_awq_rejects_bad_scales():
+    W = wl.bits(wl.random_bf16((2, 256), 0.02, seed=91))
+    for bad in (np.ones(128, np.float32), -np.ones(256, np.float32),
+                np.full(256, np.inf, np.float32), np.zeros(256, np.float32)):
+        with pytest.raises(ValueError):
+            O.quantize_rtn_scaled(W, bad)
 
 
 # ---------------------------------------------------------------------------
