@@ -15,7 +15,8 @@ between CUDA events on the launch stream; per-kernel durations come from
 graphs holding only that kernel's K launches, replayed right after.
 Sub-benchmarks (M = 1, M = 8, the 27B-class layer at M ∈ {1,5,7,13}, the
 70B-class layer at M = 208, the 4B-class 200-matrix stack sweep, quantiser
-alone) are reported under "sub".
+alone, the AWQ-style channel-scaled quantiser and activation scaling) are
+reported under "sub".
 
 `--impl reference` times the CPU oracle (the only other program here that
 computes the same thing) on a bounded sample of the same workload.
@@ -363,7 +364,9 @@ def gemm_set(torch, w4, wl, workload, Ms, pk, reps=20, path=None, grouped=False)
     return out
 
 
-def quant_set(torch, w4, wl, workload, pk, reps=10):
+def quant_set(torch, w4, wl, workload, pk, reps=10, scaled=False):
+    """The quantiser alone over rotating copies; with ``scaled``, the
+    channel-scaled variant (AWQ-style s, fp32 [K], read once per launch)."""
     dev = torch.device("cuda", torch.cuda.current_device())
     N, K = wl.SHAPES[workload][0]
     W0 = wl.weight(workload, 0, device=dev)
@@ -371,12 +374,35 @@ def quant_set(torch, w4, wl, workload, pk, reps=10):
     Ws = [W0.clone() for _ in range(R)]
     Ps = [torch.empty((N, K // 2), dtype=torch.uint8, device=dev) for _ in range(R)]
     Ss = [torch.empty((N, K // 128), dtype=torch.bfloat16, device=dev) for _ in range(R)]
-    g = capture(torch, lambda: [w4.w4_quantize_rtn(Ws[r], packed=Ps[r], scales=Ss[r]) for r in range(R)])
+    if scaled:
+        s = wl.workload_channel_scales(workload, device=dev)
+        g = capture(torch, lambda: [w4.w4_quantize_rtn_scaled(Ws[r], s, packed=Ps[r], scales=Ss[r])
+                                    for r in range(R)])
+    else:
+        g = capture(torch, lambda: [w4.w4_quantize_rtn(Ws[r], packed=Ps[r], scales=Ss[r]) for r in range(R)])
     t = Timer(torch).time(g.replay, reps=reps) / R
-    b = quant_bytes(N, K)
+    b = quant_bytes(N, K) + (4 * K if scaled else 0)
     del Ws, Ps, Ss, g
     torch.cuda.empty_cache()
     return {"us": t * 1e6, "GB/s": b / t / 1e9, "frac": b / t / 1e9 / pk["hbm_gbs"], "shape": [N, K]}
+
+
+def scale_act_set(torch, w4, wl, workload, M, pk, reps=20):
+    """x' = x / s (w4_scale_activations) on M rows of the workload's first K,
+    over rotating copies of x; bytes = x read + x' written + s read."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    K = wl.SHAPES[workload][0][1]
+    b = 4 * M * K + 4 * K
+    R, _ = n_copies(torch, b)
+    x0 = wl.activations(workload, M, K, device=dev)
+    s = wl.workload_channel_scales(workload, device=dev)
+    xs = [x0.clone() for _ in range(R)]
+    outs = [torch.empty_like(x0) for _ in range(R)]
+    g = capture(torch, lambda: [w4.w4_scale_activations(xs[r], s, out=outs[r]) for r in range(R)])
+    t = Timer(torch).time(g.replay, reps=reps) / R
+    del xs, outs, g
+    torch.cuda.empty_cache()
+    return {"us": t * 1e6, "GB/s": b / t / 1e9, "frac": b / t / 1e9 / pk["hbm_gbs"], "shape": [M, K]}
 
 
 def cpu_oracle_sample(wl, rows, reps_seconds=10.0, min_reps=1):
@@ -456,6 +482,10 @@ def run_gpu(args):
             sub["outlier_m8"] = gemm_set(torch, w4, wl, "outlier", [8], pk)["M8"]
         if want("quant"):
             sub["quant_ffn"] = quant_set(torch, w4, wl, "ffn", pk)
+        if want("awq"):
+            sub["quant_scaled_outlier"] = quant_set(torch, w4, wl, "outlier", pk, scaled=True)
+            sub["scale_act_m8"] = scale_act_set(torch, w4, wl, "outlier", 8, pk)
+            sub["scale_act_m208"] = scale_act_set(torch, w4, wl, "layer70b", 208, pk)
         if want("layer27b"):
             sub["layer27b"] = gemm_set(torch, w4, wl, "layer27b", wl.ROWS["layer27b"], pk, reps=10)
         if want("layer70b"):

@@ -17,7 +17,8 @@ import torch
 
 __all__ = [
     "load", "library_path", "W4Error",
-    "w4_quantize_rtn", "w4_gemm", "w4_gemm_ex", "w4_gemm_path_for",
+    "w4_quantize_rtn", "w4_quantize_rtn_scaled", "w4_scale_activations",
+    "w4_gemm", "w4_gemm_ex", "w4_gemm_path_for",
     "w4_packed_bytes", "w4_scales_bytes", "w4_last_device_status", "w4_wait_probe",
     "w4_status_string", "W4_PATH_AUTO", "W4_PATH_SMALL_M", "W4_PATH_TENSOR", "GROUP",
     "GroupedPlan", "w4_grouped_plan", "w4_gemm_grouped", "w4_gemm_grouped_noalloc",
@@ -49,6 +50,8 @@ _SIGNATURES = {
     "w4_packed_bytes": (_sz, [_i64, _i64]),
     "w4_scales_bytes": (_sz, [_i64, _i64, _i32]),
     "w4_quantize_rtn": (ctypes.c_int, [_vp, _i64, _i64, _i32, _vp, _vp, _vp]),
+    "w4_quantize_rtn_scaled": (ctypes.c_int, [_vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp]),
+    "w4_scale_activations": (ctypes.c_int, [_vp, _i64, _i64, _vp, _vp, _vp]),
     "w4_gemm": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp]),
     "w4_gemm_ex": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _i32]),
     "w4_gemm_path_for": (ctypes.c_int, [_i64, _i64, _i64]),
@@ -146,6 +149,51 @@ def w4_quantize_rtn(W: torch.Tensor, group: int = GROUP, packed: torch.Tensor | 
         _check(load().w4_quantize_rtn(W.data_ptr(), N, K, group, packed.data_ptr(),
                                       scales.data_ptr(), _stream(W.device)), "w4_quantize_rtn")
     return packed, scales
+
+
+def _channel_scales(s: torch.Tensor, K: int) -> None:
+    _cuda_tensor(s, "s", torch.float32, 1)
+    if s.shape[0] != K:
+        raise ValueError("s must hold one scale per input channel (K)")
+
+
+def w4_quantize_rtn_scaled(W: torch.Tensor, s: torch.Tensor, group: int = GROUP,
+                           packed: torch.Tensor | None = None, scales: torch.Tensor | None = None):
+    """RTN of the channel-scaled weights W' = bf16(W · s) (s fp32 [K], finite, > 0)
+    -> (packed u8 [N, K/2], scales bf16 [N, K/128])."""
+    _cuda_tensor(W, "W", torch.bfloat16, 2)
+    N, K = W.shape
+    _channel_scales(s, K)
+    if group != GROUP or K % GROUP:
+        raise W4Error(W4_ERR_UNSUPPORTED, "w4_quantize_rtn_scaled")
+    if packed is None:
+        packed = torch.empty((N, K // 2), dtype=torch.uint8, device=W.device)
+    if scales is None:
+        scales = torch.empty((N, K // GROUP), dtype=torch.bfloat16, device=W.device)
+    _cuda_tensor(packed, "packed", torch.uint8, 2)
+    _cuda_tensor(scales, "scales", torch.bfloat16, 2)
+    if tuple(packed.shape) != (N, K // 2) or tuple(scales.shape) != (N, K // GROUP):
+        raise ValueError("packed / scales have the wrong shape")
+    with torch.cuda.device(W.device):
+        _check(load().w4_quantize_rtn_scaled(W.data_ptr(), N, K, group, s.data_ptr(), packed.data_ptr(),
+                                             scales.data_ptr(), _stream(W.device)), "w4_quantize_rtn_scaled")
+    return packed, scales
+
+
+def w4_scale_activations(x: torch.Tensor, s: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """x' = bf16(x / s): x bf16 [M, K], s fp32 [K] -> bf16 [M, K]; out may be x (in place)."""
+    _cuda_tensor(x, "x", torch.bfloat16, 2)
+    M, K = x.shape
+    _channel_scales(s, K)
+    if out is None:
+        out = torch.empty_like(x)
+    _cuda_tensor(out, "out", torch.bfloat16, 2)
+    if tuple(out.shape) != (M, K):
+        raise ValueError("out has the wrong shape")
+    with torch.cuda.device(x.device):
+        _check(load().w4_scale_activations(x.data_ptr(), M, K, s.data_ptr(), out.data_ptr(),
+                                           _stream(x.device)), "w4_scale_activations")
+    return out
 
 
 def w4_gemm_ex(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,

@@ -84,22 +84,60 @@ size_t w4_scales_bytes(int64_t N, int64_t K, int32_t group) {
     return static_cast<size_t>(N) * static_cast<size_t>(K / 128) * 2;
 }
 
-int w4_quantize_rtn(const void* W, int64_t N, int64_t K, int32_t group, void* packed, void* scales,
-                    void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Plain RTN (channel_scales == nullptr) or RTN of the channel-scaled weights.
+int quantize_impl(const void* W, int64_t N, int64_t K, int32_t group, const float* channel_scales,
+                  bool scaled, void* packed, void* scales, void* stream) {
     if (group != 128) return W4_ERR_UNSUPPORTED;
     if (const int s = check_sizes(N, K)) return s;
     if (N == 0 || K == 0) return W4_OK;
-    if (!W || !packed || !scales) return W4_ERR_INVALID_ARG;
-    if (!aligned(W, 16) || !aligned(packed, 16) || !aligned(scales, 2)) return W4_ERR_MISALIGNED;
+    if (!W || !packed || !scales || (scaled && !channel_scales)) return W4_ERR_INVALID_ARG;
+    if (!aligned(W, 16) || !aligned(packed, 16) || !aligned(scales, 2) ||
+        (scaled && !aligned(channel_scales, 16)))
+        return W4_ERR_MISALIGNED;
     const size_t wb = static_cast<size_t>(N * K) * 2, pb = w4_packed_bytes(N, K),
-                 sb = w4_scales_bytes(N, K, group);
-    if (overlaps(W, wb, packed, pb) || overlaps(W, wb, scales, sb) || overlaps(packed, pb, scales, sb))
+                 sb = w4_scales_bytes(N, K, group), cb = scaled ? static_cast<size_t>(K) * 4 : 0;
+    if (overlaps(W, wb, packed, pb) || overlaps(W, wb, scales, sb) || overlaps(packed, pb, scales, sb) ||
+        overlaps(channel_scales, cb, packed, pb) || overlaps(channel_scales, cb, scales, sb))
         return W4_ERR_INVALID_ARG;
     cudaError_t err;
     const DeviceInfo* dev = device_info(&err);
     if (!dev) return W4_ERR_CUDA;
     if (dev->cc_major < 10) return W4_ERR_UNSUPPORTED;
-    return to_status(launch_quantize(W, N, K, packed, scales, *dev, static_cast<cudaStream_t>(stream)));
+    return to_status(launch_quantize(W, N, K, packed, scales, scaled ? channel_scales : nullptr, *dev,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int w4_quantize_rtn(const void* W, int64_t N, int64_t K, int32_t group, void* packed, void* scales,
+                    void* stream) {
+    return quantize_impl(W, N, K, group, nullptr, false, packed, scales, stream);
+}
+
+int w4_quantize_rtn_scaled(const void* W, int64_t N, int64_t K, int32_t group, const float* s, void* packed,
+                           void* scales, void* stream) {
+    return quantize_impl(W, N, K, group, s, true, packed, scales, stream);
+}
+
+int w4_scale_activations(const void* x, int64_t M, int64_t K, const float* s, void* x_out, void* stream) {
+    if (M < 0) return W4_ERR_INVALID_ARG;
+    if (const int st = check_sizes(M, K)) return st;
+    if (M == 0 || K == 0) return W4_OK;
+    if (!x || !s || !x_out) return W4_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(s, 16) || !aligned(x_out, 16)) return W4_ERR_MISALIGNED;
+    const size_t xb = static_cast<size_t>(M * K) * 2, cb = static_cast<size_t>(K) * 4;
+    if ((x != x_out && overlaps(x, xb, x_out, xb)) || overlaps(s, cb, x_out, xb)) return W4_ERR_INVALID_ARG;
+    cudaError_t err;
+    const DeviceInfo* dev = device_info(&err);
+    if (!dev) return W4_ERR_CUDA;
+    if (dev->cc_major < 10) return W4_ERR_UNSUPPORTED;
+    return to_status(launch_scale_activations(x, M, K, s, x_out, *dev, static_cast<cudaStream_t>(stream)));
 }
 
 int w4_gemm_path_for(int64_t M, int64_t N, int64_t K) {

@@ -21,8 +21,13 @@ struct DeviceInfo {
 const DeviceInfo* device_info(cudaError_t* err);
 
 // Launchers.  Arguments are already validated by the C ABI layer.
-cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, void* packed, void* scales,
+// s == nullptr: plain RTN; otherwise RTN of bf16_rne(fp32(w·s_k)) (s fp32 [K]).
+cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, void* packed, void* scales, const float* s,
                             const DeviceInfo& dev, cudaStream_t stream);
+
+// x' = bf16_rne(fp32(x / s_k)) over x bf16 [M, K]; out may be x itself.
+cudaError_t launch_scale_activations(const void* x, int64_t M, int64_t K, const float* s, void* out,
+                                     const DeviceInfo& dev, cudaStream_t stream);
 
 // Small-M path (TMA-fed GEMV on the legacy MMA): any M, one pass per 16 token rows.
 cudaError_t launch_gemv(const void* x, int64_t M, int64_t N, int64_t K, const void* packed,

@@ -18,6 +18,16 @@
 //   Instruction budget: at the HBM roofline an SM must retire about 8.6 weights
 //   per clock, i.e. at most 15 warp-lane instructions per weight; the packed
 //   two-lane fp32 arithmetic below keeps the kernel near 5.
+//
+// Channel-scaled variant (same study, §2 AWQ equation W'_ij = W_ij·s_j): each
+// loaded weight is first replaced by W' = bf16_rne(fp32(w·s_k)), with s_k the
+// fp32 scale of its input channel, and W' is quantised as above.  s (K·4 bytes
+// for the whole matrix) is read through L1; that kernel maps chunks to lanes
+// differently (see quantize_rtn_scaled_kernel) so that the s reads coalesce.
+//
+// Also here: the input-side half of that equation, x'_j = x_j / s_j, as a
+// streaming elementwise pass, x' = bf16_rne(fp32(x / s_k)) with the IEEE
+// quotient.
 #include "w4_device.cuh"
 #include "w4_internal.h"
 
@@ -255,25 +265,154 @@ quantize_rtn_kernel(const uint8_t* __restrict__ W, uint4* __restrict__ packed,
     }
 }
 
-template <bool kWide>
-int resident_ctas_per_sm() {
+// ---------------------------------------------------------------------------
+// Channel-scaled variant.  Same units of 128 chunks and the same four lanes
+// per group (lanes 4g..4g+3 take group g of the unit), but lane q = l mod 4 of
+// a group takes its chunks q, q+4, q+8, q+12 instead of 4q..4q+3.  Then each
+// warp load instruction reads, per group, 64 contiguous bytes of W and the 128
+// contiguous bytes of s that belong to them (the 8 fp32 channel scales of each
+// of 4 chunks), so an s read from L1 costs one wavefront per group rather than
+// one per lane.  A group never crosses a row, so chunk q + 4i of the group is
+// at row offset r0 + 4i, with r0 that of chunk q.
+// ---------------------------------------------------------------------------
+// The 8 fp32 channel scales of one chunk (32 bytes; 32-byte loads when s is
+// 32-byte aligned, which makes every chunk's scales 32-byte aligned).
+template <bool kWideS>
+__device__ __forceinline__ void load_chunk_scales(const float* p, float (&sv)[8]) {
+    if (kWideS) {
+        uint32_t r[8];
+        asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                       "=r"(r[7])
+                     : "l"(p));
+#pragma unroll
+        for (int j = 0; j < 8; ++j) sv[j] = __uint_as_float(r[j]);
+    } else {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+        const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+        sv[0] = a.x; sv[1] = a.y; sv[2] = a.z; sv[3] = a.w;
+        sv[4] = b.x; sv[5] = b.y; sv[6] = b.z; sv[7] = b.w;
+    }
+}
+
+// One chunk h[0..3] (h[j] holds weights 2j and 2j+1) <- bf16_rne(fp32(w·s_k)).
+__device__ __forceinline__ void scale_chunk(uint32_t* h, const float (&sv)[8]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint64_t P = f2_mul(f2_pack(bf16_lo(h[j]), bf16_hi(h[j])), f2_pack(sv[2 * j], sv[2 * j + 1]));
+        float lo, hi;
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(P));
+        const __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
+        h[j] = *reinterpret_cast<const uint32_t*>(&r);
+    }
+}
+
+// The lane's chunks c0 + 4i, i = 0..3 (zeros when its group is out of range).
+__device__ __forceinline__ void load_strided_or_zero(const uint4* __restrict__ W, int64_t c0, int64_t n_chunks,
+                                                     uint32_t (&h)[16]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint4 v = c0 < n_chunks ? ld_stream(W + c0 + 4 * i) : make_uint4(0u, 0u, 0u, 0u);
+        h[4 * i] = v.x;
+        h[4 * i + 1] = v.y;
+        h[4 * i + 2] = v.z;
+        h[4 * i + 3] = v.w;
+    }
+}
+
+// Scales, quantises and stores the lane's chunks c0 + 4i (row offset r0 + 4i).
+// Warp-collective.  A group's chunks are all in range or all out of range
+// (n_chunks is a multiple of 16), and the scale reads stay inside s even for
+// a group out of range (r0 + 12 < row_chunks).
+template <bool kWideS>
+__device__ __forceinline__ void quantize_group_scaled(uint32_t (&h)[16], int64_t c0, int64_t r0, bool valid,
+                                                      int lane, uint32_t* __restrict__ packed,
+                                                      __nv_bfloat16* __restrict__ scales,
+                                                      const float* __restrict__ s) {
+    const float* sp = s + 8 * r0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float sv[8];
+        load_chunk_scales<kWideS>(sp + 32 * i, sv);
+        scale_chunk(&h[4 * i], sv);
+    }
+    const uint32_t a = group_absmax_bits(h);
+    const __nv_bfloat16 d16 = group_scale(bf16_lo(a));
+    const float d = __bfloat162float(d16);
+    uint32_t word[4];
+    if (d >= 0x1p-64f) {
+        const float rho = rcp_approx(d);
+        const uint64_t R = f2_pack(rho, rho);
+        const uint64_t ND = f2_pack(-d, -d);
+        const uint64_t MG = f2_pack(kBiasedMagic, kBiasedMagic);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) word[k] = chunk_word_normal(&h[4 * k], R, ND, MG);
+    } else {
+        const float ds = d == 0.0f ? 1.0f : d * 0x1p64f;
+        const float rho = rcp_approx(ds);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) word[k] = chunk_word_tiny(&h[4 * k], ds, rho);
+    }
+    if (valid) {
+        uint32_t* out = packed + c0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) out[4 * k] = word[k];
+        if ((lane & 3) == 0) scales[c0 >> 4] = d16;
+    }
+}
+
+template <bool kWideS>
+__global__ void __launch_bounds__(kQuantThreads)
+quantize_rtn_scaled_kernel(const uint4* __restrict__ W, uint32_t* __restrict__ packed,
+                           __nv_bfloat16* __restrict__ scales, int64_t n_chunks, const float* __restrict__ s,
+                           int64_t row_chunks) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t n_units = (n_chunks + 127) >> 7;
+    pdl_start();
+    int64_t u = warp;
+    if (u >= n_units) return;
+    const int64_t stride = n_warps << 7;
+    // Chunk q of group g = l/4 of unit u: c0 = 128·u + 16·g + q, q = l mod 4.
+    int64_t c = (u << 7) + 16 * (lane >> 2) + (lane & 3);
+    // c mod row_chunks, kept up to date without a division per unit.
+    int64_t r = c % row_chunks;
+    const int64_t stride_r = stride % row_chunks;
+    uint32_t A[16], B[16];
+    load_strided_or_zero(W, c, n_chunks, A);
+    while (true) {  // u < n_units here, so the whole warp runs each body
+        if (u + n_warps < n_units) load_strided_or_zero(W, c + stride, n_chunks, B);
+        quantize_group_scaled<kWideS>(A, c, r, c < n_chunks, lane, packed, scales, s);
+        u += n_warps;
+        c += stride;
+        if ((r += stride_r) >= row_chunks) r -= row_chunks;
+        if (u >= n_units) break;
+        if (u + n_warps < n_units) load_strided_or_zero(W, c + stride, n_chunks, A);
+        quantize_group_scaled<kWideS>(B, c, r, c < n_chunks, lane, packed, scales, s);
+        u += n_warps;
+        c += stride;
+        if ((r += stride_r) >= row_chunks) r -= row_chunks;
+        if (u >= n_units) break;
+    }
+}
+
+template <typename Kernel>
+int resident_ctas_per_sm(Kernel kernel) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_rtn_kernel<kWide>, kQuantThreads, 0) !=
-            cudaSuccess ||
-        n < 1) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kQuantThreads, 0) != cudaSuccess || n < 1) {
         cudaGetLastError();
         n = 1;
     }
     return n;
 }
 
-template <bool kWide>
-cudaError_t launch_quantize_t(const void* W, int64_t n_chunks, void* packed, void* scales, const DeviceInfo& dev,
-                              cudaStream_t stream) {
+// One wave of resident CTAs (occ per SM), each looping over its share of units.
+template <typename Kernel, typename... Args>
+cudaError_t launch_one_wave(Kernel kernel, int occ, int64_t n_chunks, const DeviceInfo& dev, cudaStream_t stream,
+                            Args... args) {
     const int64_t per_cta = static_cast<int64_t>(kQuantThreads / 32) * 128 * 2;
     int64_t blocks = (n_chunks + per_cta - 1) / per_cta;
-    // One wave of resident CTAs, each looping over its share.
-    static const int occ = resident_ctas_per_sm<kWide>();
     const int64_t cap = static_cast<int64_t>(dev.sm_count) * occ;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
@@ -286,18 +425,86 @@ cudaError_t launch_quantize_t(const void* W, int64_t n_chunks, void* packed, voi
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, quantize_rtn_kernel<kWide>, static_cast<const uint8_t*>(W),
-                              static_cast<uint4*>(packed), static_cast<__nv_bfloat16*>(scales), n_chunks);
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+template <bool kWide>
+cudaError_t launch_quantize_t(const void* W, int64_t n_chunks, void* packed, void* scales, const DeviceInfo& dev,
+                              cudaStream_t stream) {
+    static const int occ = resident_ctas_per_sm(quantize_rtn_kernel<kWide>);
+    return launch_one_wave(quantize_rtn_kernel<kWide>, occ, n_chunks, dev, stream, static_cast<const uint8_t*>(W),
+                           static_cast<uint4*>(packed), static_cast<__nv_bfloat16*>(scales), n_chunks);
+}
+
+template <bool kWideS>
+cudaError_t launch_quantize_scaled_t(const void* W, int64_t n_chunks, void* packed, void* scales, const float* s,
+                                     int64_t row_chunks, const DeviceInfo& dev, cudaStream_t stream) {
+    static const int occ = resident_ctas_per_sm(quantize_rtn_scaled_kernel<kWideS>);
+    return launch_one_wave(quantize_rtn_scaled_kernel<kWideS>, occ, n_chunks, dev, stream,
+                           static_cast<const uint4*>(W), static_cast<uint32_t*>(packed),
+                           static_cast<__nv_bfloat16*>(scales), n_chunks, s, row_chunks);
+}
+
+// x' = bf16_rne(fp32(x / s_k)) over x bf16 [M, K] seen as n8 vectors of 8
+// consecutive k (K is a multiple of 8, so a vector never crosses a row).
+constexpr int kScaleThreads = 256;
+
+__global__ void __launch_bounds__(kScaleThreads)
+scale_activations_kernel(const uint4* x, const float* __restrict__ s, uint4* out, int64_t n8, int64_t row_vecs) {
+    // x and out may be the same buffer: each vector is read, then written, by one thread.
+    pdl_start();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
+        const uint4 v = x[i];
+        const float4* sp = reinterpret_cast<const float4*>(s + 8 * (i % row_vecs));
+        const float4 s0 = __ldg(sp), s1 = __ldg(sp + 1);
+        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+        const float sk[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __nv_bfloat162 r = __floats2bfloat162_rn(__fdiv_rn(bf16_lo(in[j]), sk[2 * j]),
+                                                           __fdiv_rn(bf16_hi(in[j]), sk[2 * j + 1]));
+            o[j] = *reinterpret_cast<const uint32_t*>(&r);
+        }
+        out[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
 }
 
 }  // namespace
 
-cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, void* packed, void* scales,
+cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, void* packed, void* scales, const float* s,
                             const DeviceInfo& dev, cudaStream_t stream) {
-    const int64_t n_chunks = N * K / 8;
+    const int64_t n_chunks = N * K / 8, row_chunks = K / 8;
+    if (s) {
+        if ((reinterpret_cast<uintptr_t>(s) & 31u) == 0)
+            return launch_quantize_scaled_t<true>(W, n_chunks, packed, scales, s, row_chunks, dev, stream);
+        return launch_quantize_scaled_t<false>(W, n_chunks, packed, scales, s, row_chunks, dev, stream);
+    }
     // 32-byte loads need a 32-byte aligned base; the ABI promises 16.
-    if ((reinterpret_cast<uintptr_t>(W) & 31u) == 0) return launch_quantize_t<true>(W, n_chunks, packed, scales, dev, stream);
+    if ((reinterpret_cast<uintptr_t>(W) & 31u) == 0)
+        return launch_quantize_t<true>(W, n_chunks, packed, scales, dev, stream);
     return launch_quantize_t<false>(W, n_chunks, packed, scales, dev, stream);
+}
+
+cudaError_t launch_scale_activations(const void* x, int64_t M, int64_t K, const float* s, void* out,
+                                     const DeviceInfo& dev, cudaStream_t stream) {
+    const int64_t n8 = M * K / 8;
+    int64_t blocks = (n8 + kScaleThreads - 1) / kScaleThreads;
+    const int64_t cap = static_cast<int64_t>(dev.sm_count) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+    cfg.blockDim = dim3(kScaleThreads, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, scale_activations_kernel, static_cast<const uint4*>(x), s,
+                              static_cast<uint4*>(out), n8, K / 8);
 }
 
 }  // namespace w4

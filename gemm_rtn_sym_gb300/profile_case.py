@@ -1,6 +1,7 @@
 """Run one small, self-checking case of a single kernel, for a profiler.
 
     python -m gemm_rtn_sym_gb300.profile_case quantize --workload outlier
+    python -m gemm_rtn_sym_gb300.profile_case quantize_scaled --workload outlier
     python -m gemm_rtn_sym_gb300.profile_case gemm --workload outlier --M 8
     python -m gemm_rtn_sym_gb300.profile_case gemm --workload layer70b --matrix 2 --M 208
     python -m gemm_rtn_sym_gb300.profile_case grouped --workload layer27b --M 1
@@ -21,6 +22,7 @@ import torch
 
 from . import W4_PATH_AUTO, W4_PATH_SMALL_M, W4_PATH_TENSOR
 from . import load, w4_gemm_ex, w4_gemm_grouped, w4_grouped_plan, w4_last_device_status, w4_quantize_rtn
+from . import w4_quantize_rtn_scaled
 from . import workloads as wl
 
 PATHS = {"auto": W4_PATH_AUTO, "small": W4_PATH_SMALL_M, "tensor": W4_PATH_TENSOR}
@@ -28,7 +30,7 @@ PATHS = {"auto": W4_PATH_AUTO, "small": W4_PATH_SMALL_M, "tensor": W4_PATH_TENSO
 
 def main(argv=None) -> int:
     p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
-    p.add_argument("kernel", choices=["quantize", "gemm", "grouped"])
+    p.add_argument("kernel", choices=["quantize", "quantize_scaled", "gemm", "grouped"])
     p.add_argument("--workload", default="outlier", choices=sorted(wl.SHAPES))
     p.add_argument("--matrix", type=int, default=0, help="index into the workload's matrices")
     p.add_argument("--M", type=int, default=8, help="token rows of x (gemm)")
@@ -63,6 +65,11 @@ def main(argv=None) -> int:
         for _ in range(a.launches):
             w4_quantize_rtn(W, packed=packed, scales=scales)
         what = f"quantize {a.workload}[{a.matrix}] {N}x{K}"
+    elif a.kernel == "quantize_scaled":
+        s = wl.workload_channel_scales(a.workload, a.matrix, device=dev)
+        for _ in range(a.launches):
+            w4_quantize_rtn_scaled(W, s, packed=packed, scales=scales)
+        what = f"quantize_scaled {a.workload}[{a.matrix}] {N}x{K}"
     else:
         w4_quantize_rtn(W, packed=packed, scales=scales)
         del W

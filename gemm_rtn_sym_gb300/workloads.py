@@ -20,7 +20,14 @@ the format on (Qwen3.5-4B whole-model quantisation study, §1 FFN example
 * ``stack4b``  — 56×(2560×9216) + 56×(9216×2560) + 44×(2560×4096) +
   44×(4096×2560) = 3,565,158,400 weights, N(0, 0.02²).
 
-Seeds: 1000·workload_id + 10·matrix_index + {0: W, 1: x, 2: aux}.
+Channel scales for the AWQ-style scaled quantiser (§2 AWQ equation and the
+paragraph after it: s_j ∝ (mean|x_j|)^α, α = k/19): :func:`channel_scales`
+draws synthetic per-channel input magnitudes m_j (log-normal, with the same
+1 % of channels ×8 as ``outlier``), raises them to α = 10/19 and divides by
+their geometric mean.  No calibration activations exist here, and the search
+over α is not part of the library; the scales are only inputs.
+
+Seeds: 1000·workload_id + 10·matrix_index + {0: W, 1: x, 2: aux, 3: s}.
 Each draw is fp32 from a seeded ``torch.Generator`` on the requested device,
 then converted to bf16 with round-to-nearest-even.
 """
@@ -83,6 +90,28 @@ def outlier_channels(K: int, seed: int, device="cpu") -> torch.Tensor:
     g = _gen(seed, device)
     n = int(round(OUTLIER_FRACTION * K))
     return torch.randperm(K, generator=g, device=device)[:n]
+
+
+AWQ_ALPHA = 10 / 19
+CHANNEL_LOG_STD = 0.5
+
+
+def channel_scales(K: int, seed: int, alpha: float = AWQ_ALPHA, device="cpu") -> torch.Tensor:
+    """fp32 [K] channel scales s_j = (m_j)^α / geomean(m^α), with synthetic
+    magnitudes m_j = exp(N(0, 0.5²)) and 1 % of the channels ×8.  Drawn on the
+    CPU (the same values for every device), then moved to ``device``."""
+    g = _gen(seed, "cpu")
+    m = torch.exp(torch.randn(K, generator=g, dtype=torch.float64) * CHANNEL_LOG_STD)
+    m[outlier_channels(K, seed + 1)] *= OUTLIER_FACTOR
+    p = m ** alpha
+    s = p / torch.exp(torch.log(p).mean())
+    return s.to(torch.float32).to(device)
+
+
+def workload_channel_scales(workload: str, matrix_index: int = 0, device="cpu") -> torch.Tensor:
+    """The channel scales of one matrix of a workload (K of that matrix)."""
+    K = SHAPES[workload][matrix_index][1]
+    return channel_scales(K, seed_for(workload, matrix_index, 3), device=device)
 
 
 def weight(workload: str, matrix_index: int = 0, device="cpu", shape=None) -> torch.Tensor:

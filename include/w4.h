@@ -101,6 +101,43 @@ int w4_quantize_rtn(const void* W, int64_t N, int64_t K, int32_t group,
                     void* packed, void* scales, void* stream);
 
 /*
+ * AWQ-style channel scaling (§2 AWQ equation: W'_ij = W_ij·s_j and
+ * x'_j = x_j/s_j leave the product unchanged, W'x' = Wx; s_j is a per-input-
+ * channel factor, distinct from the group scale d and not limited to powers of
+ * two).  The caller supplies s; searching for it (the study's grid of
+ * exponents over calibration statistics) is not part of this library.
+ *
+ * w4_quantize_rtn_scaled — quantises W' = bf16_rne(fp32(W[n,k] · s[k])) exactly
+ * as w4_quantize_rtn quantises W (same d and q rules, same outputs); W' itself
+ * is never stored.
+ *   W       in : bf16 [N, K]
+ *   s       in : fp32 [K], device, 16-byte aligned; every entry finite and > 0
+ *                (not checked: other values give unspecified codes, never an
+ *                out-of-bounds access).  Where W·s overflows bf16 the codes of
+ *                that group are unspecified, as for Inf weights.
+ *   packed  out: u8   [N, K/2]
+ *   scales  out: bf16 [N, K/128]
+ * s must not overlap packed or scales.
+ */
+int w4_quantize_rtn_scaled(const void* W, int64_t N, int64_t K, int32_t group,
+                           const float* s, void* packed, void* scales, void* stream);
+
+/*
+ * w4_scale_activations — the input side: x'[m,k] = bf16_rne(fp32(x[m,k] / s[k]))
+ * with the IEEE fp32 quotient, so that w4_gemm(x', packed', scales') computes
+ * Ŵ'x' ≈ Wx for the outputs of w4_quantize_rtn_scaled.  With M = 1 it also
+ * folds 1/s into a per-channel vector, such as the weight of the normalisation
+ * that produces x.  A streaming elementwise pass (HBM-bound).
+ *   x       in : bf16 [M, K], 16-byte aligned
+ *   s       in : fp32 [K], 16-byte aligned, finite and > 0 (as above)
+ *   x_out   out: bf16 [M, K], 16-byte aligned; x_out == x (in place) is allowed,
+ *                any other overlap with x, or any overlap with s, is rejected.
+ * K must be a multiple of 128; M = 0 or K = 0 is a no-op.
+ */
+int w4_scale_activations(const void* x, int64_t M, int64_t K, const float* s,
+                         void* x_out, void* stream);
+
+/*
  * w4_gemm — y = Ŵ x with ŵ = d·q (§1 FFN example y = W x; §2: 4-bit weights,
  * BF16 inputs).  M is the number of token rows: 1 for plain decode, K+1 for a
  * speculative-verify pass with K drafts.

@@ -79,6 +79,37 @@ def test_quantize_rejects(lib, args, expect):
     assert lib.w4_quantize_rtn(*args) == expect
 
 
+@pytest.mark.parametrize("args,expect", [
+    ((A16, 4, 256, 128, None, A16 * 4, A16 * 8, None), w4.W4_ERR_INVALID_ARG),           # null s
+    ((A16, 4, 256, 128, A16 * 12 + 4, A16 * 4, A16 * 8, None), w4.W4_ERR_MISALIGNED),    # s at 4 B
+    ((A16, 4, 256, 128, A16 * 8, A16 * 4, A16 * 8, None), w4.W4_ERR_INVALID_ARG),        # s on scales
+    ((A16, 4, 256, 128, A16 * 4 + 256, A16 * 4, A16 * 8, None), w4.W4_ERR_INVALID_ARG),  # s in packed
+    ((A16, 4, 256, 64, A16 * 12, A16 * 4, A16 * 8, None), w4.W4_ERR_UNSUPPORTED),        # group 64
+])
+def test_quantize_scaled_rejects(lib, args, expect):
+    assert lib.w4_quantize_rtn_scaled(*args) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((A16, 2, 200, A16 * 4, A16 * 8, None), w4.W4_ERR_UNSUPPORTED),       # K % 128
+    ((A16, -2, 256, A16 * 4, A16 * 8, None), w4.W4_ERR_INVALID_ARG),
+    ((None, 2, 256, A16 * 4, A16 * 8, None), w4.W4_ERR_INVALID_ARG),
+    ((A16, 2, 256, None, A16 * 8, None), w4.W4_ERR_INVALID_ARG),
+    ((A16, 2, 256, A16 * 4 + 8, A16 * 8, None), w4.W4_ERR_MISALIGNED),
+    ((A16, 2, 256, A16 * 4, A16 * 8 + 2, None), w4.W4_ERR_MISALIGNED),
+    ((A16, 2, 256, A16 * 4, A16 + 16, None), w4.W4_ERR_INVALID_ARG),     # out overlaps x, not equal
+    ((A16, 2, 256, A16 * 4, A16 * 4 + 512, None), w4.W4_ERR_INVALID_ARG),  # out overlaps s
+])
+def test_scale_activations_rejects(lib, args, expect):
+    assert lib.w4_scale_activations(*args) == expect
+
+
+def test_awq_empty_is_noop(lib):
+    assert lib.w4_quantize_rtn_scaled(None, 0, 256, 128, None, None, None, None) == w4.W4_OK
+    assert lib.w4_scale_activations(None, 0, 256, None, None, None) == w4.W4_OK
+    assert lib.w4_scale_activations(None, 3, 0, None, None, None) == w4.W4_OK
+
+
 def test_quantize_empty_is_noop(lib):
     assert lib.w4_quantize_rtn(None, 0, 256, 128, None, None, None) == w4.W4_OK
     assert lib.w4_quantize_rtn(None, 4, 0, 128, None, None, None) == w4.W4_OK
