@@ -44,6 +44,15 @@ same ones, independently):
   of K finite positive scales; W' = bf16_rne(fp32(w·s_k)) is quantised by the
   same RTN, and x' = bf16_rne(fp32(x / s_k)); results where w·s_k overflows
   are unspecified, like Inf weights;
+* group sizes 32 and 64 (§2 settings table: a smaller group follows the range
+  more closely at the cost of more scales) use the same rules per group; the
+  packed code layout stays per 128 inputs, scales are [N, K/group];
+* asymmetric (§1 equation with z ≠ 0; z is the code of real zero, §1 symbol
+  table): lo = min(0, min w), hi = max(0, max w), d = bf16_rne(fp32(fp32(hi −
+  lo) / 15)), z = clip(round_half_even(fp32(−lo / d)), 0, 15),
+  q = clip(round_half_even(fp32(w / d)) + z, 0, 15); where d = 0, z = 8 and
+  q = z.  Stored: the nibble q − 8 in the same layout and an int8 zero z − 8
+  per group, so ŵ = d·(stored code − stored zero);
 * the matmul reference accumulates ŵ·x in fp64 (exact products), and the
   parity bound is |y_gpu − y_ref| ≤ 4e-3 · Σ_k |ŵ_k x_k| + ulp_bf16(y_ref).
 
@@ -55,8 +64,13 @@ from __future__ import annotations
 import numpy as np
 
 GROUP = 128
+GROUPS = (32, 64, 128)
 Q_MIN, Q_MAX = -8, 7
 DIVISOR = 7.0
+# Asymmetric (z != 0) codes are unsigned, 0..15; the stored nibble is q - 8.
+QA_MIN, QA_MAX = 0, 15
+DIVISOR_ASYM = 15.0
+ZERO_OF_EMPTY = 8
 TOL_REL = 4e-3
 
 # P1 nibble order: inside each 32-bit word (8 consecutive k), nibble slot i
@@ -112,8 +126,10 @@ def _groups(W_bits: np.ndarray, group: int) -> np.ndarray:
     if W_bits.ndim != 2:
         raise ValueError("W must be 2-D [N, K]")
     N, K = W_bits.shape
-    if group != GROUP or K % group:
-        raise ValueError("K must be a multiple of the group size 128")
+    if group not in GROUPS:
+        raise ValueError("group must be 32, 64 or 128")
+    if K % GROUP:
+        raise ValueError("K must be a multiple of 128 (the packed block)")
     return bf16_bits_to_f32(W_bits).reshape(N, K // group, group)
 
 
@@ -192,10 +208,59 @@ def unpack_p1(packed: np.ndarray, K: int) -> np.ndarray:
 
 def quantize_rtn(W_bits: np.ndarray, group: int = GROUP):
     """RTN symmetric INT4: W bf16 bits [N, K] -> (packed u8 [N, K/2],
-    scale bits uint16 [N, K/128])."""
+    scale bits uint16 [N, K/group]).  The packed layout does not depend on the
+    group size."""
     s = rtn_scales(W_bits, group)
     q = rtn_codes(W_bits, s, group)
     return pack_p1(q), s
+
+
+# ---------------------------------------------------------------------------
+# Asymmetric RTN: the §1 equation with a free zero point z (the position of
+# real zero on the code grid, §1 symbol table), q in 0..15.
+# ---------------------------------------------------------------------------
+def asym_params(W_bits: np.ndarray, group: int = GROUP):
+    """Per (row, group): lo = min(0, min w), hi = max(0, max w) (so that real 0
+    lies on the grid); d = bf16_rne(fp32(fp32(hi − lo) / 15));
+    z = clip(round_half_even(fp32(−lo / d)), 0, 15), and z = 8 where d = 0.
+    Returns (scale bits uint16 [N, K/group], z int8 [N, K/group])."""
+    w = _groups(W_bits, group)
+    lo = np.minimum(np.min(w, axis=2), np.float32(0)).astype(np.float32)
+    hi = np.maximum(np.max(w, axis=2), np.float32(0)).astype(np.float32)
+    span = (hi - lo).astype(np.float32)                        # fp32 IEEE, RN
+    d32 = (span / np.float32(DIVISOR_ASYM)).astype(np.float32)  # fp32 IEEE quotient, RN
+    d_bits = f32_to_bf16_bits_rne(d32)
+    d = bf16_bits_to_f32(d_bits)
+    zero = d == 0
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = (-lo / np.where(zero, np.float32(1), d)).astype(np.float32)
+    z = np.clip(np.rint(r), QA_MIN, QA_MAX)
+    z = np.where(zero, ZERO_OF_EMPTY, z)
+    return d_bits, z.astype(np.int8)
+
+
+def asym_codes(W_bits: np.ndarray, scale_bits: np.ndarray, z: np.ndarray, group: int = GROUP) -> np.ndarray:
+    """q = clip(round_half_even(fp32(w / d)) + z, 0, 15), with the stored bf16
+    d; q = z where d = 0 (so ŵ = 0).  int16 [N, K]."""
+    w = _groups(W_bits, group)
+    d = bf16_bits_to_f32(scale_bits)[:, :, None]
+    zz = np.asarray(z, dtype=np.int16)[:, :, None]
+    zero = d == 0
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = (w / np.where(zero, np.float32(1), d)).astype(np.float32)
+    n = np.where(zero, 0.0, np.rint(r)).astype(np.int64)
+    q = np.clip(n + zz, QA_MIN, QA_MAX)
+    return q.astype(np.int16).reshape(w.shape[0], -1)
+
+
+def quantize_rtn_asym(W_bits: np.ndarray, group: int = GROUP):
+    """RTN asymmetric INT4 -> (packed u8 [N, K/2] holding q − 8 in the same
+    nibble layout, scale bits uint16 [N, K/group], zeros int8 [N, K/group]
+    holding z − 8).  Then ŵ = d·(q − z) = d·(stored code − stored zero), and
+    the symmetric format is the case stored zero = 0."""
+    d_bits, z = asym_params(W_bits, group)
+    q = asym_codes(W_bits, d_bits, z, group)
+    return pack_p1((q - 8).astype(np.int8)), d_bits, (z.astype(np.int16) - 8).astype(np.int8)
 
 
 # ---------------------------------------------------------------------------
@@ -238,12 +303,18 @@ def quantize_rtn_scaled(W_bits: np.ndarray, s, group: int = GROUP):
 # ---------------------------------------------------------------------------
 # Matmul y = Ŵ x  (§1 FFN example; ŵ = d·q from the §1 equation).
 # ---------------------------------------------------------------------------
-def dequantize_fp64(packed: np.ndarray, scale_bits: np.ndarray, K: int) -> np.ndarray:
-    """ŵ = d·q in fp64 (exact: d has 8 significant bits, q at most 4)."""
-    q = unpack_p1(packed, K).astype(np.float64)
+def dequantize_fp64(packed: np.ndarray, scale_bits: np.ndarray, K: int, group: int = GROUP,
+                    zeros: np.ndarray | None = None) -> np.ndarray:
+    """ŵ = d·(c − z') in fp64, c the stored code and z' the stored zero (0 when
+    ``zeros`` is None, the symmetric case).  Exact: d has 8 significant bits,
+    c − z' at most 5."""
+    c = unpack_p1(packed, K).astype(np.float64)
     d = bf16_bits_to_f32(scale_bits).astype(np.float64)
-    N = q.shape[0]
-    return (q.reshape(N, -1, GROUP) * d[:, :, None]).reshape(N, K)
+    N = c.shape[0]
+    c = c.reshape(N, K // group, group)
+    if zeros is not None:
+        c = c - np.asarray(zeros, dtype=np.float64)[:, :, None]
+    return (c * d[:, :, None]).reshape(N, K)
 
 
 def matmul_fp64(x: np.ndarray, w: np.ndarray) -> np.ndarray:
@@ -251,11 +322,12 @@ def matmul_fp64(x: np.ndarray, w: np.ndarray) -> np.ndarray:
     return np.asarray(x, dtype=np.float64) @ np.asarray(w, dtype=np.float64).T
 
 
-def gemm_reference(x_bits: np.ndarray, packed: np.ndarray, scale_bits: np.ndarray, K: int):
+def gemm_reference(x_bits: np.ndarray, packed: np.ndarray, scale_bits: np.ndarray, K: int,
+                   group: int = GROUP, zeros: np.ndarray | None = None):
     """Returns (y_ref, s_abs), both fp64 [M, N]: y_ref = Ŵ x and
     s_abs = Σ_k |ŵ_k x_k|, the magnitude the parity bound scales with."""
     x = bf16_bits_to_f32(np.asarray(x_bits, dtype=np.uint16)).astype(np.float64)
-    w = dequantize_fp64(packed, scale_bits, K)
+    w = dequantize_fp64(packed, scale_bits, K, group, zeros)
     return matmul_fp64(x, w), matmul_fp64(np.abs(x), np.abs(w))
 
 

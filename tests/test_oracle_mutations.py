@@ -24,8 +24,8 @@ MUTANTS = {
     "scale_truncated": ("return f32_to_bf16_bits_rne(d32)",
                         "return (d32.view(np.uint32) >> np.uint32(16)).astype(np.uint16)"),
     "divide_by_unrounded_scale": (
-        "d = bf16_bits_to_f32(scale_bits)[:, :, None]",
-        "d = (np.max(np.abs(w), axis=2) / np.float32(DIVISOR)).astype(np.float32)[:, :, None]"),
+        "d = bf16_bits_to_f32(scale_bits)[:, :, None]\n    zero = d == 0",
+        "d = (np.max(np.abs(w), axis=2) / np.float32(DIVISOR)).astype(np.float32)[:, :, None]\n    zero = d == 0"),
     "slot_order_swapped": ("P1_SLOT_K = (0, 2, 4, 6, 1, 3, 5, 7)", "P1_SLOT_K = (0, 1, 2, 3, 4, 5, 6, 7)"),
     "chunk_order_reversed": ("return 16 * j + 4 * w + bit // 8, bit % 8",
                              "return 16 * (3 - j) + 4 * w + bit // 8, bit % 8"),
@@ -34,8 +34,8 @@ MUTANTS = {
                           "return np.asarray(x, dtype=np.float64)[:, ::-1] @ np.asarray(w, dtype=np.float64).T"),
     "matmul_weights_transposed": ("return np.asarray(x, dtype=np.float64) @ np.asarray(w, dtype=np.float64).T",
                                   "return (np.asarray(w, dtype=np.float64) @ np.asarray(x, dtype=np.float64).T).T[:, ::-1]"),
-    "scale_dropped_in_dequant": ("return (q.reshape(N, -1, GROUP) * d[:, :, None]).reshape(N, K)",
-                                 "return q.reshape(N, K)"),
+    "scale_dropped_in_dequant": ("return (c * d[:, :, None]).reshape(N, K)",
+                                 "return c.reshape(N, K)"),
     "abs_sum_signed": ("return matmul_fp64(x, w), matmul_fp64(np.abs(x), np.abs(w))",
                        "return matmul_fp64(x, w), np.abs(matmul_fp64(x, w))"),
     "ulp_off_by_one": ("out[nz] = np.exp2(np.maximum(e, -126.0) - 7.0)",
@@ -52,6 +52,21 @@ MUTANTS = {
                               "return f32_to_bf16_bits_rne((x * s[None, :]).astype(np.float32))"),
     "awq_scale_ignored": ("return quantize_rtn(awq_scale_weights(W_bits, s), group)",
                           "return quantize_rtn(W_bits, group)"),
+    "asym_divisor_16": ("DIVISOR_ASYM = 15.0", "DIVISOR_ASYM = 16.0"),
+    "asym_range_without_zero": (
+        "lo = np.minimum(np.min(w, axis=2), np.float32(0)).astype(np.float32)",
+        "lo = np.min(w, axis=2).astype(np.float32)"),
+    "asym_zero_added_before_rounding": (
+        "n = np.where(zero, 0.0, np.rint(r)).astype(np.int64)\n    q = np.clip(n + zz, QA_MIN, QA_MAX)",
+        "n = np.where(zero, 0.0, r).astype(np.float64)\n    q = np.clip(np.rint(n + zz), QA_MIN, QA_MAX).astype(np.int64)"),
+    "asym_zero_point_unclipped": ("z = np.clip(np.rint(r), QA_MIN, QA_MAX)", "z = np.rint(r)"),
+    "asym_zeros_ignored_in_dequant": ("c = c - np.asarray(zeros, dtype=np.float64)[:, :, None]", "c = c"),
+    "asym_zero_sign_flipped": ("c = c - np.asarray(zeros, dtype=np.float64)[:, :, None]",
+                               "c = c + np.asarray(zeros, dtype=np.float64)[:, :, None]"),
+    "asym_empty_zero_0": ("ZERO_OF_EMPTY = 8", "ZERO_OF_EMPTY = 0"),
+    "asym_codes_unshifted": ("return pack_p1((q - 8).astype(np.int8)), d_bits",
+                             "return pack_p1(q.astype(np.int8)), d_bits"),
+    "dequant_group_fixed_128": ("c = c.reshape(N, K // group, group)", "c = c.reshape(N, K // GROUP, GROUP)"),
 }
 
 PIN_TESTS = [
@@ -76,6 +91,14 @@ PIN_TESTS = [
     lambda: pins.test_awq_bruteforce_4x256(71),
     pins.test_awq_rounds_through_fp32,
     pins.test_awq_power_of_two_group_scales,
+    lambda: pins.test_hand_worked_asym_groups("C"),
+    lambda: pins.test_hand_worked_asym_groups("D"),
+    lambda: pins.test_bruteforce_asym("ties", 32),
+    lambda: pins.test_bruteforce_asym("skewed", 128),
+    lambda: pins.test_bruteforce_small_groups("normal", 64),
+    lambda: pins.test_asym_matmul_bruteforce(32),
+    lambda: pins.test_asym_invariants("ffn", 64),
+    pins.test_asym_special_groups,
 ]
 
 

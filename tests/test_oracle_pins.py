@@ -4,7 +4,8 @@ never against the oracle's own formulas retyped.
 Definition: Qwen3.5-4B quantisation study (parksieon.github.io), §1 group
 quantisation equation with z = 0, §1 group-of-128 paragraph (72 groups per row
 at 9216 inputs), §2 settings table (RTN minmax · symmetric, 4-bit weights /
-BF16 inputs), §2 AWQ equation W'_ij = W_ij·s_j, x'_j = x_j/s_j, W'x' = Wx.
+BF16 inputs; smaller groups), §2 AWQ equation W'_ij = W_ij·s_j, x'_j = x_j/s_j,
+W'x' = Wx, and the §1 equation with a free zero point z (asymmetric).
 """
 import math
 import os
@@ -82,6 +83,40 @@ def exact_rtn_group(w_bits):
     if d == 0:
         return d_bits, [0] * len(w)
     return d_bits, [min(7, max(-8, round_half_even(v / d))) for v in w]
+
+
+def float_rne(v: Fraction, p: int, emin: int) -> Fraction:
+    """Nearest binary float with p significant bits and minimum normal exponent
+    emin to a rational (ties to even); no overflow."""
+    if v == 0:
+        return Fraction(0)
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    ulp = Fraction(2) ** (max(e, emin) - (p - 1))
+    r = round_half_even(a / ulp) * ulp
+    return r if v > 0 else -r
+
+
+def fp32(v: Fraction) -> Fraction:
+    return float_rne(v, 24, -126)
+
+
+def exact_asym_group(w_bits):
+    """Exact-rational asymmetric RTN of one group, each fp32 step rounded as
+    the reading states: (d bits, z, q list)."""
+    w = [bf16_exact(b) for b in w_bits]
+    lo = min(min(w), Fraction(0))
+    hi = max(max(w), Fraction(0))
+    d_bits = bf16_rne_bits(fp32(fp32(hi - lo) / 15))
+    d = bf16_exact(d_bits)
+    if d == 0:
+        return d_bits, 8, [8] * len(w)
+    z = min(15, max(0, round_half_even(fp32(-lo / d))))
+    return d_bits, z, [min(15, max(0, round_half_even(fp32(v / d)) + z)) for v in w]
 
 
 def read_golden():
@@ -281,22 +316,6 @@ def test_channel_scaling_identity():
 # rational arithmetic.  Reading: W' = bf16_rne(fp32(w·s_k)) and
 # x' = bf16_rne(fp32(x / s_k)), both rounded twice (fp32, then bf16).
 # ---------------------------------------------------------------------------
-def float_rne(v: Fraction, p: int, emin: int) -> Fraction:
-    """Nearest binary float with p significant bits and minimum normal exponent
-    emin to a rational (ties to even); no overflow."""
-    if v == 0:
-        return Fraction(0)
-    a = abs(v)
-    e = a.numerator.bit_length() - a.denominator.bit_length()
-    while Fraction(2) ** e > a:
-        e -= 1
-    while Fraction(2) ** (e + 1) <= a:
-        e += 1
-    ulp = Fraction(2) ** (max(e, emin) - (p - 1))
-    r = round_half_even(a / ulp) * ulp
-    return r if v > 0 else -r
-
-
 def fp32_then_bf16_bits(v: Fraction, negative: bool) -> int:
     return bf16_rne_bits(abs(float_rne(v, 24, -126))) | (0x8000 if negative else 0)
 
@@ -394,6 +413,146 @@ def test_awq_rejects_bad_scales():
                 np.full(256, np.inf, np.float32), np.zeros(256, np.float32)):
         with pytest.raises(ValueError):
             O.quantize_rtn_scaled(W, bad)
+
+
+# ---------------------------------------------------------------------------
+# P7: group sizes 32 / 64 and the asymmetric quantiser (§1 equation with a
+# free zero point; §2 settings table on smaller groups).
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("name", ["C", "D"])
+def test_hand_worked_asym_groups(name):
+    w_s, d_s, z_s, q_s, sum_s = read_golden()[name]
+    w = [float(v) for v in w_s.split()]
+    packed, s, zeros = O.quantize_rtn_asym(one_group_matrix(w))
+    assert O.bf16_bits_to_f32(s)[0, 0] == float(d_s)
+    assert int(zeros[0, 0]) == int(z_s) - 8
+    c = O.unpack_p1(packed, 128)[0].astype(int)
+    expect = [int(v) for v in q_s.split()]
+    assert list(c[: len(expect)] + 8) == expect
+    assert np.all(c[len(expect):] + 8 == int(z_s))
+    x_ones = f_to_bf16_bits(np.ones((1, 128), dtype=np.float32))
+    y, _ = O.gemm_reference(x_ones, packed, s, 128, 128, zeros)
+    assert y[0, 0] == float(sum_s)
+
+
+def asym_rows(kind, n_rows=4, K=256):
+    if kind == "normal":
+        return wl.bits(wl.random_bf16((n_rows, K), 0.02, seed=13))
+    if kind == "ties":
+        return tie_heavy_rows(n_rows)
+    if kind == "skewed":  # one-signed groups, some with a single outlier
+        W = np.abs(O.bf16_bits_to_f32(wl.bits(wl.random_bf16((n_rows, K), 0.02, seed=14))))
+        W[1] = -W[1]
+        W[2, 40] = 1.5
+        W[3, 100:164] = 0.0
+        return f_to_bf16_bits(W.astype(np.float32))
+    raise ValueError(kind)
+
+
+@pytest.mark.parametrize("group", [32, 64, 128])
+@pytest.mark.parametrize("kind", ["normal", "ties", "skewed"])
+def test_bruteforce_asym(kind, group):
+    W = asym_rows(kind)
+    packed, s, zeros = O.quantize_rtn_asym(W, group)
+    c = O.unpack_p1(packed, W.shape[1]).astype(int)
+    for n in range(W.shape[0]):
+        for g in range(W.shape[1] // group):
+            d_bits, z, q = exact_asym_group(W[n, group * g: group * g + group])
+            assert s[n, g] == d_bits
+            assert int(zeros[n, g]) == z - 8
+            assert list(c[n, group * g: group * g + group] + 8) == q
+
+
+@pytest.mark.parametrize("group", [32, 64])
+@pytest.mark.parametrize("kind", ["normal", "ties", "outlier"])
+def test_bruteforce_small_groups(kind, group):
+    if kind == "outlier":
+        W = wl.bits(wl.random_bf16((4, 256), 0.02, seed=12)).copy()
+        W[:, 3] = f_to_bf16_bits(O.bf16_bits_to_f32(W[:, 3]) * 8)
+    else:
+        W = asym_rows(kind)
+    packed, s = O.quantize_rtn(W, group)
+    assert s.shape == (4, 256 // group)
+    q = O.unpack_p1(packed, 256)
+    for n in range(4):
+        for g in range(256 // group):
+            d_bits, q_exact = exact_rtn_group(W[n, group * g: group * g + group])
+            assert s[n, g] == d_bits
+            assert list(q[n, group * g: group * g + group]) == q_exact
+
+
+@pytest.mark.parametrize("group", [32, 64, 128])
+def test_asym_matmul_bruteforce(group):
+    W = wl.bits(wl.random_bf16((3, 256), 0.02, seed=23))
+    x = wl.bits(wl.random_bf16((2, 256), 1.0, seed=24))
+    packed, s, zeros = O.quantize_rtn_asym(W, group)
+    y, sabs = O.gemm_reference(x, packed, s, 256, group, zeros)
+    for n in range(3):
+        what = []
+        for g in range(256 // group):
+            d_bits, z, q = exact_asym_group(W[n, group * g: group * g + group])
+            what += [bf16_exact(d_bits) * (qv - z) for qv in q]
+        for m in range(2):
+            xs = [bf16_exact(b) for b in x[m]]
+            exact = sum(a * b for a, b in zip(what, xs))
+            exact_abs = sum(abs(a * b) for a, b in zip(what, xs))
+            assert abs(y[m, n] - float(exact)) <= 1e-12 * float(exact_abs)
+            assert abs(sabs[m, n] - float(exact_abs)) <= 1e-12 * float(exact_abs)
+
+
+@pytest.mark.parametrize("group", [32, 64, 128])
+@pytest.mark.parametrize("workload", ["ffn", "outlier", "layer70b"])
+def test_asym_invariants(workload, group):
+    """Real zero is exact; the error is at most half a step (plus the clamp's
+    margin from rounding d); d·z' is within half a step of lo."""
+    N, K = wl.SHAPES[workload][0]
+    W = wl.bits(wl.weight(workload, shape=(96, K)))
+    packed, s, zeros = O.quantize_rtn_asym(W, group)
+    w = O.bf16_bits_to_f32(W).astype(np.float64)
+    what = O.dequantize_fp64(packed, s, K, group, zeros)
+    d = np.repeat(O.bf16_bits_to_f32(s).astype(np.float64), group, axis=1)
+    assert np.all(what[w == 0] == 0)
+    assert np.all(np.abs(what - w) <= 0.5625 * d)
+    lo = np.minimum(w.reshape(96, -1, group).min(axis=2), 0)
+    dg = O.bf16_bits_to_f32(s).astype(np.float64)
+    zq = zeros.astype(np.float64) + 8
+    assert np.all(np.abs(-dg * zq - lo) <= 0.5 * dg + 1e-30)
+
+
+def test_asym_special_groups():
+    K = 512
+    W = np.zeros((5, K), dtype=np.float32)
+    W[1, :128] = 0.25 + np.arange(128) / 512        # all positive: z = 0
+    W[2, :128] = -(0.25 + np.arange(128) / 512)     # all negative: z = 15
+    W[3, :128] = 0.75                               # constant: q = 15
+    W[4, :128] = -0.75                              # constant negative: q = 0
+    Wb = np.concatenate([f_to_bf16_bits(W), np.zeros((1, K), dtype=np.uint16)])
+    # Subnormal all-negative group: d = bf16(31·2^-133 / 15) = 2^-132 rounds
+    # down so far that −lo/d = 15.5 rounds to 16, which the clip brings to 15.
+    Wb[5, :128] = 0x801F
+    packed, s, zeros = O.quantize_rtn_asym(Wb)
+    c = O.unpack_p1(packed, K).astype(int)
+    d_bits, z, q = exact_asym_group(Wb[5, :128])
+    assert (d_bits, z) == (0x0002, 15) and s[5, 0] == 0x0002 and zeros[5, 0] == 7
+    assert np.all(c[5, :128] == -8) and q == [0] * 128
+    assert not s[0].any() and not zeros[0].any() and not packed[0].any()  # all-zero groups
+    assert zeros[1, 0] == -8 and zeros[2, 0] == 7
+    assert np.all(c[3, :128] == 7) and zeros[3, 0] == -8
+    assert np.all(c[4, :128] == -8) and zeros[4, 0] == 7
+    what = O.dequantize_fp64(packed, s, K, 128, zeros)
+    d3 = float(O.bf16_bits_to_f32(s)[3, 0])
+    assert what[3, 0] == 15 * d3 and abs(what[3, 0] - 0.75) <= d3 / 2
+
+
+def test_group_size_rejects():
+    W = wl.bits(wl.random_bf16((2, 256), 0.02, seed=3))
+    for g in (16, 96, 256):
+        with pytest.raises(ValueError):
+            O.quantize_rtn(W, g)
+        with pytest.raises(ValueError):
+            O.quantize_rtn_asym(W, g)
+    with pytest.raises(ValueError):
+        O.quantize_rtn(wl.bits(wl.random_bf16((2, 96), 0.02, seed=3)), 32)
 
 
 # ---------------------------------------------------------------------------
