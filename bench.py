@@ -15,8 +15,8 @@ between CUDA events on the launch stream; per-kernel durations come from
 graphs holding only that kernel's K launches, replayed right after.
 Sub-benchmarks (M = 1, M = 8, the 27B-class layer at M ∈ {1,5,7,13}, the
 70B-class layer at M = 208, the 4B-class 200-matrix stack sweep, quantiser
-alone, the AWQ-style channel-scaled quantiser and activation scaling) are
-reported under "sub".
+alone, the AWQ-style channel-scaled quantiser and activation scaling, the
+asymmetric and group-32/64 formats) are reported under "sub".
 
 `--impl reference` times the CPU oracle (the only other program here that
 computes the same thing) on a bounded sample of the same workload.
@@ -405,6 +405,60 @@ def scale_act_set(torch, w4, wl, workload, M, pk, reps=20):
     return {"us": t * 1e6, "GB/s": b / t / 1e9, "frac": b / t / 1e9 / pk["hbm_gbs"], "shape": [M, K]}
 
 
+def affine_bytes(M, N, K, group, asym):
+    """Algorithmic bytes of one affine-format matmul: codes + scales (+ zeros) + x + y."""
+    return N * K // 2 + N * (K // group) * (3 if asym else 2) + 2 * M * K + 2 * M * N
+
+
+def affine_set(torch, w4, wl, workload, matrix, Ms, group, asym, pk, reps=10):
+    """Quantiser (group, asym) and w4_gemm_affine on one matrix of a workload,
+    over rotating copies of its inputs."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    N, K = wl.SHAPES[workload][matrix]
+    W0 = wl.weight(workload, matrix, device=dev)
+    qb = 2 * N * K + N * K // 2 + N * (K // group) * (3 if asym else 2)
+    R, _ = n_copies(torch, qb)
+    Ws = [W0.clone() for _ in range(R)]
+    outs = [(torch.empty((N, K // 2), dtype=torch.uint8, device=dev),
+             torch.empty((N, K // group), dtype=torch.bfloat16, device=dev),
+             torch.empty((N, K // group), dtype=torch.int8, device=dev) if asym else None) for _ in range(R)]
+    del W0
+
+    def quant():
+        for r in range(R):
+            p, s, z = outs[r]
+            if asym:
+                w4.w4_quantize_rtn_asym(Ws[r], group, packed=p, scales=s, zeros=z)
+            else:
+                w4.w4_quantize_rtn(Ws[r], group, packed=p, scales=s)
+    g = capture(torch, quant)
+    t = Timer(torch).time(g.replay, reps=reps) / R
+    res = {"format": f"g{group} {'asym' if asym else 'sym'}", "shape": [N, K],
+           "quant": {"us": t * 1e6, "GB/s": qb / t / 1e9, "frac": qb / t / 1e9 / pk["hbm_gbs"]}}
+    del Ws, g
+    torch.cuda.empty_cache()
+    for M in Ms:
+        x = wl.activations(workload, M, K, matrix, device=dev)
+        ys = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+
+        def mm():
+            for r in range(R):
+                p, s, z = outs[r]
+                w4.w4_gemm_affine(x, p, s, z, group=group, out=ys[r])
+        g = capture(torch, mm)
+        t = Timer(torch).time(g.replay, reps=reps) / R
+        b = affine_bytes(M, N, K, group, asym)
+        fl = 2 * M * N * K
+        t_hbm, t_tc = b / (pk["hbm_gbs"] * 1e9), fl / (pk["bf16_tflops"] * 1e12)
+        res[f"M{M}"] = {"us": t * 1e6, "GB/s": b / t / 1e9, "TFLOP/s": fl / t / 1e12,
+                        "bound": "hbm" if t_hbm >= t_tc else "tensor", "frac": max(t_hbm, t_tc) / t}
+        del g, ys
+    assert w4.w4_last_device_status() == 0
+    del outs
+    torch.cuda.empty_cache()
+    return res
+
+
 def cpu_oracle_sample(wl, rows, reps_seconds=10.0, min_reps=1):
     """Oracle quantise + matmul of `rows` rows of the headline matrix at M = 8."""
     import numpy as np
@@ -482,6 +536,11 @@ def run_gpu(args):
             sub["outlier_m8"] = gemm_set(torch, w4, wl, "outlier", [8], pk)["M8"]
         if want("quant"):
             sub["quant_ffn"] = quant_set(torch, w4, wl, "ffn", pk)
+        if want("affine"):
+            for group, asym in ((128, True), (64, True), (32, True), (32, False)):
+                key = f"affine_g{group}_{'asym' if asym else 'sym'}"
+                sub[key + "_outlier"] = affine_set(torch, w4, wl, "outlier", 0, [1, 8], group, asym, pk)
+                sub[key + "_gateup70b"] = affine_set(torch, w4, wl, "layer70b", 2, [208], group, asym, pk, reps=5)
         if want("awq"):
             sub["quant_scaled_outlier"] = quant_set(torch, w4, wl, "outlier", pk, scaled=True)
             sub["scale_act_m8"] = scale_act_set(torch, w4, wl, "outlier", 8, pk)

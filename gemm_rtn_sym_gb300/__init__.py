@@ -17,14 +17,15 @@ import torch
 
 __all__ = [
     "load", "library_path", "W4Error",
-    "w4_quantize_rtn", "w4_quantize_rtn_scaled", "w4_scale_activations",
-    "w4_gemm", "w4_gemm_ex", "w4_gemm_path_for",
+    "w4_quantize_rtn", "w4_quantize_rtn_scaled", "w4_scale_activations", "w4_quantize_rtn_asym",
+    "w4_gemm", "w4_gemm_ex", "w4_gemm_affine", "w4_gemm_path_for", "w4_zeros_bytes", "GROUPS",
     "w4_packed_bytes", "w4_scales_bytes", "w4_last_device_status", "w4_wait_probe",
     "w4_status_string", "W4_PATH_AUTO", "W4_PATH_SMALL_M", "W4_PATH_TENSOR", "GROUP",
     "GroupedPlan", "w4_grouped_plan", "w4_gemm_grouped", "w4_gemm_grouped_noalloc",
 ]
 
 GROUP = 128
+GROUPS = (32, 64, 128)
 W4_OK, W4_ERR_INVALID_ARG, W4_ERR_UNSUPPORTED, W4_ERR_MISALIGNED, W4_ERR_CUDA, W4_ERR_TIMEOUT = range(6)
 W4_PATH_AUTO, W4_PATH_SMALL_M, W4_PATH_TENSOR = 0, 1, 2
 
@@ -51,6 +52,9 @@ _SIGNATURES = {
     "w4_scales_bytes": (_sz, [_i64, _i64, _i32]),
     "w4_quantize_rtn": (ctypes.c_int, [_vp, _i64, _i64, _i32, _vp, _vp, _vp]),
     "w4_quantize_rtn_scaled": (ctypes.c_int, [_vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp]),
+    "w4_quantize_rtn_asym": (ctypes.c_int, [_vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp]),
+    "w4_zeros_bytes": (_sz, [_i64, _i64, _i32]),
+    "w4_gemm_affine": (ctypes.c_int, [_vp, _i64, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _i32]),
     "w4_scale_activations": (ctypes.c_int, [_vp, _i64, _i64, _vp, _vp, _vp]),
     "w4_gemm": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp]),
     "w4_gemm_ex": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _i32]),
@@ -123,6 +127,10 @@ def w4_scales_bytes(N: int, K: int, group: int = GROUP) -> int:
     return load().w4_scales_bytes(N, K, group)
 
 
+def w4_zeros_bytes(N: int, K: int, group: int = GROUP) -> int:
+    return load().w4_zeros_bytes(N, K, group)
+
+
 def w4_gemm_path_for(M: int, N: int, K: int) -> int:
     r = load().w4_gemm_path_for(M, N, K)
     if r < 0:
@@ -130,25 +138,46 @@ def w4_gemm_path_for(M: int, N: int, K: int) -> int:
     return r
 
 
-def w4_quantize_rtn(W: torch.Tensor, group: int = GROUP, packed: torch.Tensor | None = None,
-                    scales: torch.Tensor | None = None):
-    """RTN symmetric INT4 of W (bf16 [N, K]) -> (packed u8 [N, K/2], scales bf16 [N, K/128])."""
+def _quant_outputs(W, group, packed, scales, where):
     _cuda_tensor(W, "W", torch.bfloat16, 2)
     N, K = W.shape
-    if group != GROUP or K % GROUP:
-        raise W4Error(W4_ERR_UNSUPPORTED, "w4_quantize_rtn")
+    if group not in GROUPS or K % GROUP:
+        raise W4Error(W4_ERR_UNSUPPORTED, where)
     if packed is None:
         packed = torch.empty((N, K // 2), dtype=torch.uint8, device=W.device)
     if scales is None:
-        scales = torch.empty((N, K // GROUP), dtype=torch.bfloat16, device=W.device)
+        scales = torch.empty((N, K // group), dtype=torch.bfloat16, device=W.device)
     _cuda_tensor(packed, "packed", torch.uint8, 2)
     _cuda_tensor(scales, "scales", torch.bfloat16, 2)
-    if tuple(packed.shape) != (N, K // 2) or tuple(scales.shape) != (N, K // GROUP):
+    if tuple(packed.shape) != (N, K // 2) or tuple(scales.shape) != (N, K // group):
         raise ValueError("packed / scales have the wrong shape")
+    return N, K, packed, scales
+
+
+def w4_quantize_rtn(W: torch.Tensor, group: int = GROUP, packed: torch.Tensor | None = None,
+                    scales: torch.Tensor | None = None):
+    """RTN symmetric INT4 of W (bf16 [N, K]) -> (packed u8 [N, K/2], scales bf16 [N, K/group])."""
+    N, K, packed, scales = _quant_outputs(W, group, packed, scales, "w4_quantize_rtn")
     with torch.cuda.device(W.device):
         _check(load().w4_quantize_rtn(W.data_ptr(), N, K, group, packed.data_ptr(),
                                       scales.data_ptr(), _stream(W.device)), "w4_quantize_rtn")
     return packed, scales
+
+
+def w4_quantize_rtn_asym(W: torch.Tensor, group: int = GROUP, packed: torch.Tensor | None = None,
+                         scales: torch.Tensor | None = None, zeros: torch.Tensor | None = None):
+    """RTN asymmetric INT4 of W -> (packed u8 [N, K/2], scales bf16 [N, K/group],
+    zeros int8 [N, K/group])."""
+    N, K, packed, scales = _quant_outputs(W, group, packed, scales, "w4_quantize_rtn_asym")
+    if zeros is None:
+        zeros = torch.empty((N, K // group), dtype=torch.int8, device=W.device)
+    _cuda_tensor(zeros, "zeros", torch.int8, 2)
+    if tuple(zeros.shape) != (N, K // group):
+        raise ValueError("zeros has the wrong shape")
+    with torch.cuda.device(W.device):
+        _check(load().w4_quantize_rtn_asym(W.data_ptr(), N, K, group, packed.data_ptr(), scales.data_ptr(),
+                                           zeros.data_ptr(), _stream(W.device)), "w4_quantize_rtn_asym")
+    return packed, scales, zeros
 
 
 def _channel_scales(s: torch.Tensor, K: int) -> None:
@@ -220,6 +249,34 @@ def w4_gemm_ex(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
 def w4_gemm(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
             out: torch.Tensor | None = None) -> torch.Tensor:
     return w4_gemm_ex(x, packed, scales, out, W4_PATH_AUTO)
+
+
+def w4_gemm_affine(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor | None = None,
+                   group: int = GROUP, out: torch.Tensor | None = None, path: int = W4_PATH_AUTO) -> torch.Tensor:
+    """y = Ŵ x with ŵ = d·(code − zero) per group of ``group`` (zeros int8 [N, K/group] or None)."""
+    _cuda_tensor(x, "x", torch.bfloat16, 2)
+    _cuda_tensor(packed, "packed", torch.uint8, 2)
+    _cuda_tensor(scales, "scales", torch.bfloat16, 2)
+    M, K = x.shape
+    N = packed.shape[0]
+    if group not in GROUPS:
+        raise W4Error(W4_ERR_UNSUPPORTED, "w4_gemm_affine")
+    if tuple(packed.shape) != (N, K // 2) or K % GROUP or tuple(scales.shape) != (N, K // group):
+        raise ValueError("x / packed / scales shapes disagree")
+    if zeros is not None:
+        _cuda_tensor(zeros, "zeros", torch.int8, 2)
+        if tuple(zeros.shape) != (N, K // group):
+            raise ValueError("zeros has the wrong shape")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _cuda_tensor(out, "out", torch.bfloat16, 2)
+    if tuple(out.shape) != (M, N):
+        raise ValueError("out has the wrong shape")
+    with torch.cuda.device(x.device):
+        _check(load().w4_gemm_affine(x.data_ptr(), M, N, K, group, packed.data_ptr(), scales.data_ptr(),
+                                     zeros.data_ptr() if zeros is not None else None, out.data_ptr(),
+                                     _stream(x.device), path), "w4_gemm_affine")
+    return out
 
 
 class GroupedPlan:

@@ -41,6 +41,8 @@ int check_sizes(int64_t N, int64_t K) {
 
 int to_status(cudaError_t e) { return e == cudaSuccess ? W4_OK : W4_ERR_CUDA; }
 
+bool valid_group(int32_t group) { return group == 32 || group == 64 || group == 128; }
+
 }  // namespace
 
 const DeviceInfo* device_info(cudaError_t* err) {
@@ -80,35 +82,43 @@ size_t w4_packed_bytes(int64_t N, int64_t K) {
 }
 
 size_t w4_scales_bytes(int64_t N, int64_t K, int32_t group) {
-    if (group != 128 || check_sizes(N, K) != W4_OK) return 0;
-    return static_cast<size_t>(N) * static_cast<size_t>(K / 128) * 2;
+    if (!valid_group(group) || check_sizes(N, K) != W4_OK) return 0;
+    return static_cast<size_t>(N) * static_cast<size_t>(K / group) * 2;
+}
+
+size_t w4_zeros_bytes(int64_t N, int64_t K, int32_t group) {
+    if (!valid_group(group) || check_sizes(N, K) != W4_OK) return 0;
+    return static_cast<size_t>(N) * static_cast<size_t>(K / group);
 }
 
 }  // extern "C"
 
 namespace {
 
-// Plain RTN (channel_scales == nullptr) or RTN of the channel-scaled weights.
+// Symmetric RTN (asym false), asymmetric RTN (zeros written), or symmetric
+// RTN of the channel-scaled weights (scaled, group 128 only).
 int quantize_impl(const void* W, int64_t N, int64_t K, int32_t group, const float* channel_scales,
-                  bool scaled, void* packed, void* scales, void* stream) {
-    if (group != 128) return W4_ERR_UNSUPPORTED;
+                  bool scaled, bool asym, void* packed, void* scales, void* zeros, void* stream) {
+    if (!valid_group(group) || (scaled && group != 128)) return W4_ERR_UNSUPPORTED;
     if (const int s = check_sizes(N, K)) return s;
     if (N == 0 || K == 0) return W4_OK;
-    if (!W || !packed || !scales || (scaled && !channel_scales)) return W4_ERR_INVALID_ARG;
+    if (!W || !packed || !scales || (scaled && !channel_scales) || (asym && !zeros)) return W4_ERR_INVALID_ARG;
     if (!aligned(W, 16) || !aligned(packed, 16) || !aligned(scales, 2) ||
         (scaled && !aligned(channel_scales, 16)))
         return W4_ERR_MISALIGNED;
     const size_t wb = static_cast<size_t>(N * K) * 2, pb = w4_packed_bytes(N, K),
-                 sb = w4_scales_bytes(N, K, group), cb = scaled ? static_cast<size_t>(K) * 4 : 0;
+                 sb = w4_scales_bytes(N, K, group), cb = scaled ? static_cast<size_t>(K) * 4 : 0,
+                 zb = asym ? w4_zeros_bytes(N, K, group) : 0;
     if (overlaps(W, wb, packed, pb) || overlaps(W, wb, scales, sb) || overlaps(packed, pb, scales, sb) ||
-        overlaps(channel_scales, cb, packed, pb) || overlaps(channel_scales, cb, scales, sb))
+        overlaps(channel_scales, cb, packed, pb) || overlaps(channel_scales, cb, scales, sb) ||
+        overlaps(zeros, zb, W, wb) || overlaps(zeros, zb, packed, pb) || overlaps(zeros, zb, scales, sb))
         return W4_ERR_INVALID_ARG;
     cudaError_t err;
     const DeviceInfo* dev = device_info(&err);
     if (!dev) return W4_ERR_CUDA;
     if (dev->cc_major < 10) return W4_ERR_UNSUPPORTED;
-    return to_status(launch_quantize(W, N, K, packed, scales, scaled ? channel_scales : nullptr, *dev,
-                                     static_cast<cudaStream_t>(stream)));
+    return to_status(launch_quantize(W, N, K, group, packed, scales, asym ? zeros : nullptr,
+                                     scaled ? channel_scales : nullptr, *dev, static_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace
@@ -117,12 +127,17 @@ extern "C" {
 
 int w4_quantize_rtn(const void* W, int64_t N, int64_t K, int32_t group, void* packed, void* scales,
                     void* stream) {
-    return quantize_impl(W, N, K, group, nullptr, false, packed, scales, stream);
+    return quantize_impl(W, N, K, group, nullptr, false, false, packed, scales, nullptr, stream);
+}
+
+int w4_quantize_rtn_asym(const void* W, int64_t N, int64_t K, int32_t group, void* packed, void* scales,
+                         void* zeros, void* stream) {
+    return quantize_impl(W, N, K, group, nullptr, false, true, packed, scales, zeros, stream);
 }
 
 int w4_quantize_rtn_scaled(const void* W, int64_t N, int64_t K, int32_t group, const float* s, void* packed,
                            void* scales, void* stream) {
-    return quantize_impl(W, N, K, group, s, true, packed, scales, stream);
+    return quantize_impl(W, N, K, group, s, true, false, packed, scales, nullptr, stream);
 }
 
 int w4_scale_activations(const void* x, int64_t M, int64_t K, const float* s, void* x_out, void* stream) {
@@ -148,8 +163,11 @@ int w4_gemm_path_for(int64_t M, int64_t N, int64_t K) {
 
 namespace {
 
-int gemm_impl(const void* x, int64_t M, int64_t N, int64_t K, const void* packed, const void* scales, void* y,
-              void* stream, int32_t path) {
+// affine: the w4_gemm_affine formats (group 32/64/128, zeros or nullptr);
+// otherwise the symmetric group-128 format.
+int gemm_impl(const void* x, int64_t M, int64_t N, int64_t K, int32_t group, const void* packed,
+              const void* scales, const void* zeros, void* y, void* stream, int32_t path, bool affine) {
+    if (affine && !valid_group(group)) return W4_ERR_UNSUPPORTED;
     if (M < 0) return W4_ERR_INVALID_ARG;
     if (const int s = check_sizes(N, K)) return s;
     if (M > 0 && K > (int64_t{1} << 62) / M) return W4_ERR_INVALID_ARG;
@@ -166,14 +184,23 @@ int gemm_impl(const void* x, int64_t M, int64_t N, int64_t K, const void* packed
     if (!x || !packed || !scales) return W4_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(packed, 16) || !aligned(scales, 2)) return W4_ERR_MISALIGNED;
     const size_t xb = static_cast<size_t>(M * K) * 2, pb = w4_packed_bytes(N, K),
-                 sb = w4_scales_bytes(N, K, 128);
-    if (overlaps(y, yb, x, xb) || overlaps(y, yb, packed, pb) || overlaps(y, yb, scales, sb))
+                 sb = w4_scales_bytes(N, K, affine ? group : 128),
+                 zb = affine && zeros ? w4_zeros_bytes(N, K, group) : 0;
+    if (overlaps(y, yb, x, xb) || overlaps(y, yb, packed, pb) || overlaps(y, yb, scales, sb) ||
+        overlaps(y, yb, zeros, zb))
         return W4_ERR_INVALID_ARG;
     cudaError_t err;
     const DeviceInfo* dev = device_info(&err);
     if (!dev) return W4_ERR_CUDA;
     if (dev->cc_major < 10) return W4_ERR_UNSUPPORTED;
     if (path == W4_PATH_AUTO) path = M >= kTensorMinM ? W4_PATH_TENSOR : W4_PATH_SMALL_M;
+    // The symmetric group-128 format has its own kernels (offset MMA chain in
+    // the small-M path); w4_gemm_affine with group 128 and no zeros uses them.
+    if (affine && (group != 128 || zeros)) {
+        if (path == W4_PATH_TENSOR)
+            return to_status(launch_gemm_tc_affine(x, M, N, K, group, packed, scales, zeros, y, *dev, st));
+        return to_status(launch_gemv_affine(x, M, N, K, group, packed, scales, zeros, y, *dev, st));
+    }
     if (path == W4_PATH_TENSOR)
         return to_status(launch_gemm_tc(x, M, N, K, packed, scales, y, *dev, st));
     return to_status(launch_gemv(x, M, N, K, packed, scales, y, *dev, st));
@@ -183,12 +210,17 @@ int gemm_impl(const void* x, int64_t M, int64_t N, int64_t K, const void* packed
 
 int w4_gemm_ex(const void* x, int64_t M, int64_t N, int64_t K, const void* packed, const void* scales,
                void* y, void* stream, int32_t path) {
-    return gemm_impl(x, M, N, K, packed, scales, y, stream, path);
+    return gemm_impl(x, M, N, K, 128, packed, scales, nullptr, y, stream, path, false);
 }
 
 int w4_gemm(const void* x, int64_t M, int64_t N, int64_t K, const void* packed, const void* scales,
             void* y, void* stream) {
-    return gemm_impl(x, M, N, K, packed, scales, y, stream, W4_PATH_AUTO);
+    return gemm_impl(x, M, N, K, 128, packed, scales, nullptr, y, stream, W4_PATH_AUTO, false);
+}
+
+int w4_gemm_affine(const void* x, int64_t M, int64_t N, int64_t K, int32_t group, const void* packed,
+                   const void* scales, const void* zeros, void* y, void* stream, int32_t path) {
+    return gemm_impl(x, M, N, K, group, packed, scales, zeros, y, stream, path, true);
 }
 
 namespace {

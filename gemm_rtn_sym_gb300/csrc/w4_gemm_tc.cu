@@ -63,6 +63,8 @@ constexpr int kMinSmemBytes = 120 * 1024;
 
 struct TcArgs {
     const uint16_t* scales;
+    const int8_t* zeros;  // affine formats only; nullptr: symmetric
+    int64_t row_groups;   // scales (and zeros) per row: K / group
     __nv_bfloat16* y;
     int64_t M, N, K;
     int bm;
@@ -70,13 +72,20 @@ struct TcArgs {
     unsigned* status;
 };
 
-// q·d for the pair i of a code word, as bf16x2 (exact q, one rounding).
-__device__ __forceinline__ uint32_t deq_pair(uint32_t word, int i, __nv_bfloat162 d2) {
-    const uint32_t q = code_pair_bf16x2(word, i);
-    __nv_bfloat162 v = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&q), d2);
-    return *reinterpret_cast<uint32_t*>(&v);
+// d·(c − z') for the pair i of a code word, as bf16x2: (136 + c) − (136 + z') is
+// exact, the product rounds once.  off2 = bf16x2(136 + z'), d2 = bf16x2(d).
+__device__ __forceinline__ uint32_t deq_pair(uint32_t word, int i, uint32_t off2, uint32_t d2) {
+    const uint32_t biased = ((word >> (4 * i)) & 0x000F000Fu) ^ 0x43084308u;
+    uint32_t r;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(biased), "r"(off2));
+    asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(r) : "r"(d2));
+    return r;
 }
 
+// QG: 0 for the symmetric group-128 format; 32, 64 or 128 for the affine
+// formats (group size QG, zero points when args.zeros is set).  Only the
+// dequantisers' scale (and zero) reads differ.
+template <int QG>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_codes,
                const TcArgs args) {
@@ -207,31 +216,48 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
         const int t = quarter * 32 + lane;          // weight row within the tile
         const uint32_t lane_base = tmem_d + (static_cast<uint32_t>(quarter * 32) << 16);
         const int64_t n = n0 + t < args.N ? n0 + t : args.N - 1;  // padding rows: zero codes, valid scale
-        const uint16_t* srow = args.scales + n * G;
+        const int64_t rg = QG == 0 ? G : args.row_groups;
+        const uint16_t* srow = args.scales + n * rg;
+        const int8_t* zrow = QG != 0 && args.zeros ? args.zeros + n * rg : nullptr;
+        // (d, 136 + z') of the two 32-k chunks this thread dequantises in k
+        // stage kb, as bf16x2: {d2 of chunk 2·half, of chunk 2·half + 1,
+        // off2 of the first, of the second}.
+        auto load_dz = [&](int kb, uint32_t (&o)[4]) {
+            const int64_t gk = kb_lo + kb;
+            int64_t ia = gk, ib = gk;
+            if (QG == 64) ia = ib = 2 * gk + half;
+            if (QG == 32) ia = 4 * gk + 2 * half, ib = ia + 1;
+            const uint32_t da = __ldg(srow + ia), db = QG == 32 ? __ldg(srow + ib) : da;
+            const uint32_t za = zrow ? static_cast<uint32_t>(0x4308 + __ldg(zrow + ia)) : 0x4308u;
+            const uint32_t zb = zrow && QG == 32 ? static_cast<uint32_t>(0x4308 + __ldg(zrow + ib)) : za;
+            o[0] = da | (da << 16);
+            o[1] = db | (db << 16);
+            o[2] = za | (za << 16);
+            o[3] = zb | (zb << 16);
+        };
         // Row t of a code stage: 64 bytes per group, 16-byte chunk c at c ^ ((t >> 1) & 3).
         const uint32_t row_off = static_cast<uint32_t>(t * 64);
         const uint32_t sw = static_cast<uint32_t>((t >> 1) & 3);
-        uint32_t d_next = nkb > 0 ? __ldg(srow + kb_lo) : 0u;
+        uint32_t dz_next[4] = {0u, 0u, 0x43084308u, 0x43084308u};
+        if (nkb > 0) load_dz(0, dz_next);
         for (int kb = 0; kb < nkb && ok; ++kb) {
             const int s = kb % kStages;
             const uint32_t r = static_cast<uint32_t>(kb / kStages);
             const int cst = (kb >> 1) % kCodeStages;
             const int sub = kb & 1;  // group within the code stage
-            const uint32_t dbits = d_next;
-            if (kb + 1 < nkb) d_next = __ldg(srow + kb_lo + kb + 1);
+            const uint32_t dz[4] = {dz_next[0], dz_next[1], dz_next[2], dz_next[3]};
+            if (kb + 1 < nkb) load_dz(kb + 1, dz_next);
             const bool have = mbar_wait(code_full(cst), static_cast<uint32_t>((kb >> 1) / kCodeStages) & 1u);
             if (!__all_sync(0xffffffffu, have)) { ok = false; break; }
             const uint32_t grp = code_base + cst * kCodeStageBytes + sub * (kBN * 64) + row_off;
             const uint4 q0 = lds128(grp + (((2u * half) ^ sw) << 4));
             const uint4 q1 = lds128(grp + (((2u * half + 1u) ^ sw) << 4));
-            const uint32_t d2bits = dbits | (dbits << 16);
-            const __nv_bfloat162 d2 = *reinterpret_cast<const __nv_bfloat162*>(&d2bits);
             const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
             uint32_t v[32];  // column 4w + i of this thread's 32: pair i of word w
 #pragma unroll
             for (int w = 0; w < 8; ++w)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) v[4 * w + i] = deq_pair(words[w], i, d2);
+                for (int i = 0; i < 4; ++i) v[4 * w + i] = deq_pair(words[w], i, dz[2 + (w >> 2)], dz[w >> 2]);
             // The code slot is released only once its words have been used: the
             // shared-memory load may still be pending when an arrive executes,
             // and the next TMA copy into the slot must not overtake it.
@@ -316,7 +342,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 std::mutex g_attr_mutex;
-bool g_attr_set[64];
 
 cudaError_t get_encoder() {
     std::call_once(g_encode_once, [] {
@@ -383,10 +408,11 @@ int smem_bytes(int bm) {
     return n > kMinSmemBytes ? n : kMinSmemBytes;
 }
 
-}  // namespace
-
-cudaError_t launch_gemm_tc(const void* x, int64_t M, int64_t N, int64_t K, const void* packed,
-                           const void* scales, void* y, const DeviceInfo& dev, cudaStream_t stream) {
+template <int QG>
+cudaError_t launch_gemm_tc_q(const void* x, int64_t M, int64_t N, int64_t K, const void* packed,
+                             const void* scales, const void* zeros, void* y, const DeviceInfo& dev,
+                             cudaStream_t stream) {
+    static bool attr_set[64];
     const int64_t m_tiles = (M + kMaxBM - 1) / kMaxBM;
     int64_t bm = (M + m_tiles - 1) / m_tiles;
     bm = (bm + 15) / 16 * 16;
@@ -407,11 +433,11 @@ cudaError_t launch_gemm_tc(const void* x, int64_t M, int64_t N, int64_t K, const
     {
         std::lock_guard<std::mutex> lock(g_attr_mutex);
         if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
-        if (!g_attr_set[device]) {
-            if (cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (!attr_set[device]) {
+            if (cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<QG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                      smem_bytes(kMaxBM)))
                 return e;
-            g_attr_set[device] = true;
+            attr_set[device] = true;
         }
     }
     // Split-K over a cluster when the tiles alone leave SMs idle: pick the
@@ -434,7 +460,7 @@ cudaError_t launch_gemm_tc(const void* x, int64_t M, int64_t N, int64_t K, const
             q.attrs = qa;
             q.numAttrs = 1;
             int clusters = 0;
-            if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tc_kernel, &q) != cudaSuccess || clusters < 1) {
+            if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tc_kernel<QG>, &q) != cudaSuccess || clusters < 1) {
                 cudaGetLastError();
                 continue;
             }
@@ -450,6 +476,8 @@ cudaError_t launch_gemm_tc(const void* x, int64_t M, int64_t N, int64_t K, const
 
     TcArgs args;
     args.scales = static_cast<const uint16_t*>(scales);
+    args.zeros = static_cast<const int8_t*>(zeros);
+    args.row_groups = QG == 0 ? K / 128 : K / QG;
     args.y = static_cast<__nv_bfloat16*>(y);
     args.M = M;
     args.N = N;
@@ -471,7 +499,24 @@ cudaError_t launch_gemm_tc(const void* x, int64_t M, int64_t N, int64_t K, const
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, tmap, tmap_codes, args);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<QG>, tmap, tmap_codes, args);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const void* x, int64_t M, int64_t N, int64_t K, const void* packed,
+                           const void* scales, void* y, const DeviceInfo& dev, cudaStream_t stream) {
+    return launch_gemm_tc_q<0>(x, M, N, K, packed, scales, nullptr, y, dev, stream);
+}
+
+cudaError_t launch_gemm_tc_affine(const void* x, int64_t M, int64_t N, int64_t K, int group, const void* packed,
+                                  const void* scales, const void* zeros, void* y, const DeviceInfo& dev,
+                                  cudaStream_t stream) {
+    switch (group) {
+        case 32: return launch_gemm_tc_q<32>(x, M, N, K, packed, scales, zeros, y, dev, stream);
+        case 64: return launch_gemm_tc_q<64>(x, M, N, K, packed, scales, zeros, y, dev, stream);
+        default: return launch_gemm_tc_q<128>(x, M, N, K, packed, scales, zeros, y, dev, stream);
+    }
 }
 
 }  // namespace w4

@@ -53,6 +53,8 @@ using namespace gemv;
 
 struct GemvArgs {
     const uint16_t* scales;
+    const int8_t* zeros;  // affine variant only; nullptr: symmetric
+    int64_t row_groups;   // affine variant: scales (and zeros) per row, K / group
     __nv_bfloat16* y;
     int M;  // token rows of this pass, 1..16
     int64_t N, K;
@@ -60,8 +62,10 @@ struct GemvArgs {
     unsigned* status;
 };
 
-// MT: token tiles of 8 (1: M <= 8, 2: M <= 16).
-template <int MT, int TPW>
+// MT: token tiles of 8 (1: M <= 8, 2: M <= 16).  QG: 0 for the symmetric
+// group-128 format (offset MMA chain, one fp32 scaling per group); 32, 64 or
+// 128 for the affine variant (group size QG, optional zero points).
+template <int MT, int TPW, int QG>
 __global__ void __launch_bounds__(Warps<TPW>::kThreads, 2)
 gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_constant__ CUtensorMap tmap_x,
                const GemvArgs args) {
@@ -138,24 +142,39 @@ gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_cons
         const int cw = (warp - 1) % kStageGroups;          // this warp's group within every stage
         const int tile0 = ((warp - 1) / kStageGroups) * TPW;  // first of its row tiles
         // Scales of rows gid / gid+8 of each tile, for this warp's group of a stage.
+        // Affine variant: the group of size QG holding this thread's chunk
+        // (k 32·tig .. 32·tig + 31 of the 128-k block) is 128/QG·g + sub.
+        constexpr int kSub = QG == 0 ? 1 : 128 / QG;
+        const int sub = QG == 32 ? tig : (QG == 64 ? (tig >> 1) : 0);
+        const int64_t rg = QG == 0 ? G : args.row_groups;
         const uint16_t* srow[TPW][2];
+        const int8_t* zrow[TPW][2];
 #pragma unroll
         for (int rt = 0; rt < TPW; ++rt)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 int64_t n = n0 + (tile0 + rt) * 16 + gid + 8 * h;
                 if (n >= args.N) n = args.N - 1;
-                srow[rt][h] = args.scales + n * G;
+                srow[rt][h] = args.scales + n * rg + (QG == 0 ? 0 : sub);
+                zrow[rt][h] = QG != 0 && args.zeros ? args.zeros + n * rg + sub : nullptr;
             }
-        auto load_scales = [&](uint32_t (&d)[TPW][2], int t) {
+        // d: scale bits; for the affine variant also z: bf16 bits of 136 + z'.
+        auto load_scales = [&](uint32_t (&d)[TPW][2], uint32_t (&z)[TPW][2], int t) {
             const int64_t g = gs + t * kStageGroups + cw;
+            const bool in = t < nt && g < ge;
 #pragma unroll
             for (int rt = 0; rt < TPW; ++rt)
 #pragma unroll
-                for (int h = 0; h < 2; ++h) d[rt][h] = (t < nt && g < ge) ? __ldg(srow[rt][h] + g) : 0u;
+                for (int h = 0; h < 2; ++h) {
+                    d[rt][h] = in ? __ldg(srow[rt][h] + g * kSub) : 0u;
+                    if (QG != 0) {
+                        const int zq = in && zrow[rt][h] ? __ldg(zrow[rt][h] + g * kSub) : 0;
+                        z[rt][h] = static_cast<uint32_t>(0x4308 + zq);  // bf16(136 + z'), z' in [-8, 7]
+                    }
+                }
         };
-        uint32_t d_cur[TPW][2], d_nxt[TPW][2];
-        load_scales(d_nxt, 0);
+        uint32_t d_cur[TPW][2], d_nxt[TPW][2], z_cur[TPW][2], z_nxt[TPW][2];
+        load_scales(d_nxt, z_nxt, 0);
 
         // Byte offsets inside a stage.
         const uint32_t w_off = static_cast<uint32_t>(cw * kRowsCta * 64 + (tile0 * 16 + gid) * 64 + tig * 16);
@@ -167,8 +186,10 @@ gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_cons
             for (int rt = 0; rt < TPW; ++rt) {
                 d_cur[rt][0] = d_nxt[rt][0];
                 d_cur[rt][1] = d_nxt[rt][1];
+                z_cur[rt][0] = z_nxt[rt][0];
+                z_cur[rt][1] = z_nxt[rt][1];
             }
-            load_scales(d_nxt, t + 1);
+            load_scales(d_nxt, z_nxt, t + 1);
             const bool have = mbar_wait(full(s), static_cast<uint32_t>(t / C::kStages) & 1u);
             if (!__all_sync(0xffffffffu, have)) {
                 ok = false;
@@ -190,7 +211,21 @@ gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_cons
             // shared-memory loads may still be pending when an arrive executes,
             // and the next TMA copy into this stage must not overtake them
             // (releasing right after the loads gave rare corrupted fragments).
-            if (active) group_math<MT, TPW>(acc, xw, wv, d_cur);
+            if (active) {
+                if (QG == 0) {
+                    group_math<MT, TPW>(acc, xw, wv, d_cur);
+                } else {
+                    uint32_t d2[TPW][2], o2[TPW][2];
+#pragma unroll
+                    for (int rt = 0; rt < TPW; ++rt)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            d2[rt][h] = d_cur[rt][h] | (d_cur[rt][h] << 16);
+                            o2[rt][h] = z_cur[rt][h] | (z_cur[rt][h] << 16);
+                        }
+                    group_math_affine<MT, TPW>(acc, xw, wv, d2, o2);
+                }
+            }
             mbar_arrive(empty(s));
         }
         if (!ok) record_status(args.status, kStatusTimeout);
@@ -251,9 +286,10 @@ gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_cons
 
 std::mutex g_attr_mutex;
 
-template <int MT, int TPW>
+template <int MT, int TPW, int QG>
 cudaError_t launch_mt(const __nv_bfloat16* x, int mp, int64_t N, int64_t K, const CUtensorMap& tmap_codes,
-                      const uint16_t* scales, __nv_bfloat16* y, const DeviceInfo& dev, cudaStream_t stream) {
+                      const uint16_t* scales, const int8_t* zeros, __nv_bfloat16* y, const DeviceInfo& dev,
+                      cudaStream_t stream) {
     using C = Cfg<MT>;
     constexpr int kThreads = Warps<TPW>::kThreads;
     static bool attr_set[64];
@@ -263,7 +299,7 @@ cudaError_t launch_mt(const __nv_bfloat16* x, int mp, int64_t N, int64_t K, cons
     {
         std::lock_guard<std::mutex> lock(g_attr_mutex);
         if (!attr_set[device]) {
-            if (cudaError_t e = cudaFuncSetAttribute(gemv_w4_kernel<MT, TPW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaError_t e = cudaFuncSetAttribute(gemv_w4_kernel<MT, TPW, QG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                      C::kSmemBytes))
                 return e;
             attr_set[device] = true;
@@ -291,7 +327,7 @@ cudaError_t launch_mt(const __nv_bfloat16* x, int mp, int64_t N, int64_t K, cons
         q.attrs = qa;
         q.numAttrs = 1;
         int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, gemv_w4_kernel<MT, TPW>, &q) != cudaSuccess || clusters < 1) {
+        if (cudaOccupancyMaxActiveClusters(&clusters, gemv_w4_kernel<MT, TPW, QG>, &q) != cudaSuccess || clusters < 1) {
             cudaGetLastError();
             continue;
         }
@@ -311,6 +347,8 @@ cudaError_t launch_mt(const __nv_bfloat16* x, int mp, int64_t N, int64_t K, cons
     if (cudaError_t e = encode_x_stage_map(&tmap_x, x, mp, K, C::kXRows, 2 * kStageGroups)) return e;
     GemvArgs args;
     args.scales = scales;
+    args.zeros = zeros;
+    args.row_groups = QG == 0 ? K / 128 : K / QG;
     args.y = y;
     args.M = mp;
     args.N = N;
@@ -331,26 +369,44 @@ cudaError_t launch_mt(const __nv_bfloat16* x, int mp, int64_t N, int64_t K, cons
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, gemv_w4_kernel<MT, TPW>, tmap_codes, tmap_x, args);
+    return cudaLaunchKernelEx(&cfg, gemv_w4_kernel<MT, TPW, QG>, tmap_codes, tmap_x, args);
 }
 
-}  // namespace
-
-cudaError_t launch_gemv(const void* x, int64_t M, int64_t N, int64_t K, const void* packed,
-                        const void* scales, void* y, const DeviceInfo& dev, cudaStream_t stream) {
+template <int QG>
+cudaError_t launch_gemv_q(const void* x, int64_t M, int64_t N, int64_t K, const void* packed, const void* scales,
+                          const void* zeros, void* y, const DeviceInfo& dev, cudaStream_t stream) {
     CUtensorMap tmap_codes;
     if (cudaError_t e = encode_codes_stage_map(&tmap_codes, packed, N, K, kRowsCta, kStageGroups, CU_TENSOR_MAP_SWIZZLE_NONE))
         return e;
     const auto* xb = static_cast<const __nv_bfloat16*>(x);
     const auto* sc = static_cast<const uint16_t*>(scales);
+    const auto* zp = static_cast<const int8_t*>(zeros);
     auto* yb = static_cast<__nv_bfloat16*>(y);
     for (int64_t m0 = 0; m0 < M; m0 += 16) {
         const int mp = static_cast<int>(M - m0 < 16 ? M - m0 : 16);
-        const cudaError_t e = mp <= 8 ? launch_mt<1, kTpw>(xb + m0 * K, mp, N, K, tmap_codes, sc, yb + m0 * N, dev, stream)
-                                      : launch_mt<2, 4>(xb + m0 * K, mp, N, K, tmap_codes, sc, yb + m0 * N, dev, stream);
+        const cudaError_t e =
+            mp <= 8 ? launch_mt<1, kTpw, QG>(xb + m0 * K, mp, N, K, tmap_codes, sc, zp, yb + m0 * N, dev, stream)
+                    : launch_mt<2, 4, QG>(xb + m0 * K, mp, N, K, tmap_codes, sc, zp, yb + m0 * N, dev, stream);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_gemv(const void* x, int64_t M, int64_t N, int64_t K, const void* packed, const void* scales,
+                        void* y, const DeviceInfo& dev, cudaStream_t stream) {
+    return launch_gemv_q<0>(x, M, N, K, packed, scales, nullptr, y, dev, stream);
+}
+
+cudaError_t launch_gemv_affine(const void* x, int64_t M, int64_t N, int64_t K, int group, const void* packed,
+                               const void* scales, const void* zeros, void* y, const DeviceInfo& dev,
+                               cudaStream_t stream) {
+    switch (group) {
+        case 32: return launch_gemv_q<32>(x, M, N, K, packed, scales, zeros, y, dev, stream);
+        case 64: return launch_gemv_q<64>(x, M, N, K, packed, scales, zeros, y, dev, stream);
+        default: return launch_gemv_q<128>(x, M, N, K, packed, scales, zeros, y, dev, stream);
+    }
 }
 
 }  // namespace w4

@@ -128,5 +128,48 @@ __device__ __forceinline__ void group_math(float (&acc)[TPW][MT][4], const uint3
     }
 }
 
+// Affine variant (group sizes 32 / 64 / 128, optional zero points): every A
+// operand is dequantised, ŵ = bf16(d·((136 + c) − (136 + z'))) with c the
+// stored code and z' the stored zero: the subtraction is exact, the product
+// rounds once, as in the tensor-core path.  A thread's 32 codes of a group
+// (one 16-byte chunk) always lie inside one group of 32 or 64, so each thread
+// needs one (d, 136 + z') pair per row: d2[rt][h] and off2[rt][h] hold them as
+// bf16x2 for rows gid (h = 0) and gid + 8 (h = 1).  No offset MMA chain and no
+// per-group scaling: the MMA accumulates straight into acc.
+__device__ __forceinline__ uint32_t affine_pair(uint32_t biased, uint32_t off2, uint32_t d2) {
+    uint32_t r;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(biased), "r"(off2));
+    asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(r) : "r"(d2));
+    return r;
+}
+
+template <int MT, int TPW>
+__device__ __forceinline__ void group_math_affine(float (&acc)[TPW][MT][4], const uint32_t (&xw)[MT][16],
+                                                  const uint4 (&wv)[TPW][2], const uint32_t (&d2)[TPW][2],
+                                                  const uint32_t (&off2)[TPW][2]) {
+#pragma unroll
+    for (int rt = 0; rt < TPW; ++rt) {
+        const uint32_t wa[4] = {wv[rt][0].x, wv[rt][0].y, wv[rt][0].z, wv[rt][0].w};
+        const uint32_t wb[4] = {wv[rt][1].x, wv[rt][1].y, wv[rt][1].z, wv[rt][1].w};
+        const uint32_t da = d2[rt][0], db = d2[rt][1], oa = off2[rt][0], ob = off2[rt][1];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const uint32_t a0 = affine_pair(biased_pair<0>(wa[w]), oa, da);
+            const uint32_t a2 = affine_pair(biased_pair<1>(wa[w]), oa, da);
+            const uint32_t a1 = affine_pair(biased_pair<0>(wb[w]), ob, db);
+            const uint32_t a3 = affine_pair(biased_pair<1>(wb[w]), ob, db);
+            const uint32_t b0 = affine_pair(biased_pair<2>(wa[w]), oa, da);
+            const uint32_t b2 = affine_pair(biased_pair<3>(wa[w]), oa, da);
+            const uint32_t b1 = affine_pair(biased_pair<2>(wb[w]), ob, db);
+            const uint32_t b3 = affine_pair(biased_pair<3>(wb[w]), ob, db);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                mma_bf16_16816(acc[rt][mt], a0, a1, a2, a3, xw[mt][4 * w], xw[mt][4 * w + 1]);
+                mma_bf16_16816(acc[rt][mt], b0, b1, b2, b3, xw[mt][4 * w + 2], xw[mt][4 * w + 3]);
+            }
+        }
+    }
+}
+
 }  // namespace gemv
 }  // namespace w4

@@ -21,9 +21,10 @@ struct DeviceInfo {
 const DeviceInfo* device_info(cudaError_t* err);
 
 // Launchers.  Arguments are already validated by the C ABI layer.
-// s == nullptr: plain RTN; otherwise RTN of bf16_rne(fp32(w·s_k)) (s fp32 [K]).
-cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, void* packed, void* scales, const float* s,
-                            const DeviceInfo& dev, cudaStream_t stream);
+// group 32/64/128; zeros == nullptr: symmetric, else asymmetric (int8 z − 8 per
+// group).  s != nullptr (group 128, symmetric only): RTN of bf16_rne(fp32(w·s_k)).
+cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, int group, void* packed, void* scales, void* zeros,
+                            const float* s, const DeviceInfo& dev, cudaStream_t stream);
 
 // x' = bf16_rne(fp32(x / s_k)) over x bf16 [M, K]; out may be x itself.
 cudaError_t launch_scale_activations(const void* x, int64_t M, int64_t K, const float* s, void* out,
@@ -33,9 +34,20 @@ cudaError_t launch_scale_activations(const void* x, int64_t M, int64_t K, const 
 cudaError_t launch_gemv(const void* x, int64_t M, int64_t N, int64_t K, const void* packed,
                         const void* scales, void* y, const DeviceInfo& dev, cudaStream_t stream);
 
+// Small-M path for the affine formats: group 32/64/128, zeros (int8 z − 8 per
+// group) or nullptr for symmetric codes; weights dequantised to bf16 first.
+cudaError_t launch_gemv_affine(const void* x, int64_t M, int64_t N, int64_t K, int group, const void* packed,
+                               const void* scales, const void* zeros, void* y, const DeviceInfo& dev,
+                               cudaStream_t stream);
+
 // Tensor-core path: tcgen05 MMA with TMEM accumulators, any M.
 cudaError_t launch_gemm_tc(const void* x, int64_t M, int64_t N, int64_t K, const void* packed,
                            const void* scales, void* y, const DeviceInfo& dev, cudaStream_t stream);
+
+// Tensor-core path for the affine formats (group 32/64/128, zeros or nullptr).
+cudaError_t launch_gemm_tc_affine(const void* x, int64_t M, int64_t N, int64_t K, int group, const void* packed,
+                                  const void* scales, const void* zeros, void* y, const DeviceInfo& dev,
+                                  cudaStream_t stream);
 
 // 2-D tensor map over x bf16 [M, K]: boxes of 64 k x box_rows rows, 128-byte
 // swizzle, rows past M read as zeros.

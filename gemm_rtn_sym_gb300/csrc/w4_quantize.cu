@@ -148,8 +148,9 @@ __device__ __forceinline__ uint32_t max_abs2(uint32_t a, uint32_t b) {
     return r;
 }
 
-// max|w| over a lane's 32 weights, then over the 4 lanes of its group, as a
-// bf16 bit pattern (in both halves).
+// max|w| over a lane's 32 weights, then over the G/32 lanes of its group, as
+// a bf16 bit pattern (in both halves).
+template <int G = 128>
 __device__ __forceinline__ uint32_t group_absmax_bits(const uint32_t (&h)[16]) {
     uint32_t t[8];
 #pragma unroll
@@ -158,9 +159,116 @@ __device__ __forceinline__ uint32_t group_absmax_bits(const uint32_t (&h)[16]) {
     for (int i = 0; i < 4; ++i) t[i] = max_abs2(t[2 * i], t[2 * i + 1]);
     uint32_t a = max_abs2(max_abs2(t[0], t[1]), max_abs2(t[2], t[3]));
     a = max_abs2(a, __byte_perm(a, 0, 0x1032));  // both halves: max over the lane
-    a = max_abs2(a, __shfl_xor_sync(0xffffffffu, a, 1));
-    a = max_abs2(a, __shfl_xor_sync(0xffffffffu, a, 2));
+    if (G >= 64) a = max_abs2(a, __shfl_xor_sync(0xffffffffu, a, 1));
+    if (G >= 128) a = max_abs2(a, __shfl_xor_sync(0xffffffffu, a, 2));
     return a & 0x7FFF7FFFu;
+}
+
+// ---------------------------------------------------------------------------
+// Asymmetric codes (the §1 equation with a free zero point z, the code of real
+// zero): lo = min(0, min w), hi = max(0, max w), d = bf16_rne(fp32(fp32(hi −
+// lo) / 15)) with IEEE fp32 subtraction and division, z = clamp(round(fp32(−lo
+// / d)), 0, 15) (z = 8 where d = 0), q = clamp(round(w / d) + z, 0, 15), stored
+// as the nibble q − 8 with the int8 zero z − 8.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t min2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("min.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// lo = min(0, min w) and hi = max(0, max w) over the group (G/32 lanes).
+template <int G>
+__device__ __forceinline__ void group_range(const uint32_t (&h)[16], float& lo, float& hi) {
+    uint32_t mx[8], mn[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        mx[i] = max2(h[2 * i], h[2 * i + 1]);
+        mn[i] = min2(h[2 * i], h[2 * i + 1]);
+    }
+#pragma unroll
+    for (int s = 4; s >= 1; s >>= 1)
+#pragma unroll
+        for (int i = 0; i < s; ++i) {
+            mx[i] = max2(mx[2 * i], mx[2 * i + 1]);
+            mn[i] = min2(mn[2 * i], mn[2 * i + 1]);
+        }
+    uint32_t a = max2(mx[0], __byte_perm(mx[0], 0, 0x1032));
+    uint32_t b = min2(mn[0], __byte_perm(mn[0], 0, 0x1032));
+    if (G >= 64) {
+        a = max2(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        b = min2(b, __shfl_xor_sync(0xffffffffu, b, 1));
+    }
+    if (G >= 128) {
+        a = max2(a, __shfl_xor_sync(0xffffffffu, a, 2));
+        b = min2(b, __shfl_xor_sync(0xffffffffu, b, 2));
+    }
+    hi = fmaxf(bf16_lo(a), 0.0f);
+    lo = fminf(bf16_lo(b), 0.0f);
+}
+
+// x + kBiasedMagic24, for |x| < 2^22, has low 16 bits round_half_even(x) + 24
+// (the bias is even, so ties still go to the even neighbour).  With d ≥ 2^-64
+// a normal bf16, |w/d| ≤ 15·(1 + 2^-8)/(1 − 2^-8) < 15.5, so those bits lie in
+// [9, 39] and, after adding z ≤ 15, in [9, 54]: no carry between the halves.
+constexpr float kBiasedMagic24 = 12582936.0f;  // 1.5 * 2^23 + 24
+// Σ_j 24·16^j in both halves: removes the +24 of every nibble after packing.
+constexpr uint32_t kPackBias24 = (24u * 0x1111u) * 0x00010001u;
+
+// Pair (round(w/d) + 24) in both halves -> (q + 24), q = clamp(round + z, 0, 15).
+__device__ __forceinline__ uint32_t asym_pair(uint32_t biased, uint32_t zz) {
+    uint32_t v = biased + zz;
+    asm("max.u16x2 %0, %0, %1;" : "+r"(v) : "r"(0x00180018u));
+    asm("min.u16x2 %0, %0, %1;" : "+r"(v) : "r"(0x00270027u));
+    return v;
+}
+
+// Pairs m[j] = (q(2j+1) + 24) << 16 | (q(2j) + 24) -> the stored word of nibbles
+// q − 8 (two's complement), by linearity of the packing sum modulo 2^32.
+__device__ __forceinline__ uint32_t pack_word_24(const uint32_t (&m)[4]) {
+    const uint32_t w = ((m[3] * 16u + m[2]) * 16u + m[1]) * 16u + m[0];
+    return (w - kPackBias24) ^ 0x88888888u;
+}
+
+// d ≥ 2^-64: the asymmetric code word of chunk h[0..3], zz = z in both halves.
+__device__ __forceinline__ uint32_t chunk_word_asym(const uint32_t* h, uint64_t R, uint64_t ND, uint64_t MG,
+                                                    uint32_t zz) {
+    uint32_t m[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint64_t X = f2_pack(bf16_lo(h[j]), bf16_hi(h[j]));
+        const uint64_t Q0 = f2_mul(X, R);
+        const uint64_t E = f2_fma(Q0, ND, X);
+        const uint64_t Q1 = f2_fma(E, R, Q0);
+        m[j] = asym_pair(f2_biased_pair(f2_add(Q1, MG)), zz);
+    }
+    return pack_word_24(m);
+}
+
+// d < 2^-64 (or zero, replaced by 1): weights and scale scaled by 2^64 (exact).
+// The quotient is clamped to [-16, 16] first, which leaves clamp(round + z,
+// 0, 15) unchanged for any z in [0, 15].
+__device__ __forceinline__ uint32_t chunk_word_asym_tiny(const uint32_t* h, float ds, float rho, uint32_t zz) {
+    uint32_t m[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t b[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float x = (i == 0 ? bf16_lo(h[j]) : bf16_hi(h[j])) * 0x1p64f;
+            const float q0 = __fmul_rn(x, rho);
+            const float e = __fmaf_rn(-q0, ds, x);
+            const float q1 = fminf(fmaxf(__fmaf_rn(e, rho, q0), -16.0f), 16.0f);
+            b[i] = __float_as_uint(__fadd_rn(q1, kBiasedMagic24));
+        }
+        m[j] = asym_pair(__byte_perm(b[0], b[1], 0x5410), zz);
+    }
+    return pack_word_24(m);
 }
 
 // d = bf16_rne(max|w| / 7).  a/7 is never within 1/14 of a bf16 spacing of a
@@ -203,38 +311,70 @@ __device__ __forceinline__ void load_quarter_or_zero(const uint8_t* W, int64_t c
     }
 }
 
-// Quantises the lane's quarter group h (chunks c..c+3) and, if valid, stores
-// its code words and, from the group's first lane, its scale.  Warp-collective
-// (the group max is reduced with shuffles): every lane of the warp calls it.
+// Quantises the lane's 32 weights h (chunks c..c+3, in one group of G) and,
+// if valid, stores its code words and, from the group's first lane, its scale
+// (and zero).  Warp-collective (group reductions use shuffles): every lane of
+// the warp calls it.
+template <int G, bool kAsym>
 __device__ __forceinline__ void quantize_quarter(const uint32_t (&h)[16], int64_t c, bool valid, int lane,
-                                                 uint4* __restrict__ packed, __nv_bfloat16* __restrict__ scales) {
-    const uint32_t a = group_absmax_bits(h);
-    const __nv_bfloat16 d16 = group_scale(bf16_lo(a));
-    const float d = __bfloat162float(d16);
+                                                 uint4* __restrict__ packed, __nv_bfloat16* __restrict__ scales,
+                                                 int8_t* __restrict__ zeros) {
+    __nv_bfloat16 d16;
+    float d;
     uint32_t word[4];
-    if (d >= 0x1p-64f) {
-        const float rho = rcp_approx(d);
-        const uint64_t R = f2_pack(rho, rho);
-        const uint64_t ND = f2_pack(-d, -d);
-        const uint64_t MG = f2_pack(kBiasedMagic, kBiasedMagic);
+    int z = 0;
+    if (kAsym) {
+        float lo, hi;
+        group_range<G>(h, lo, hi);
+        d16 = __float2bfloat16_rn(__fdiv_rn(__fsub_rn(hi, lo), 15.0f));
+        d = __bfloat162float(d16);
+        z = d == 0.0f ? 8 : min(15, max(0, __float2int_rn(__fdiv_rn(-lo, d))));
+        const uint32_t zz = static_cast<uint32_t>(z) * 0x00010001u;
+        if (d >= 0x1p-64f) {
+            const float rho = rcp_approx(d);
+            const uint64_t R = f2_pack(rho, rho);
+            const uint64_t ND = f2_pack(-d, -d);
+            const uint64_t MG = f2_pack(kBiasedMagic24, kBiasedMagic24);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) word[k] = chunk_word_normal(&h[4 * k], R, ND, MG);
+            for (int k = 0; k < 4; ++k) word[k] = chunk_word_asym(&h[4 * k], R, ND, MG, zz);
+        } else {
+            const float ds = d == 0.0f ? 1.0f : d * 0x1p64f;
+            const float rho = rcp_approx(ds);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) word[k] = chunk_word_asym_tiny(&h[4 * k], ds, rho, zz);
+        }
     } else {
-        const float ds = d == 0.0f ? 1.0f : d * 0x1p64f;
-        const float rho = rcp_approx(ds);
+        const uint32_t a = group_absmax_bits<G>(h);
+        d16 = group_scale(bf16_lo(a));
+        d = __bfloat162float(d16);
+        if (d >= 0x1p-64f) {
+            const float rho = rcp_approx(d);
+            const uint64_t R = f2_pack(rho, rho);
+            const uint64_t ND = f2_pack(-d, -d);
+            const uint64_t MG = f2_pack(kBiasedMagic, kBiasedMagic);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) word[k] = chunk_word_tiny(&h[4 * k], ds, rho);
+            for (int k = 0; k < 4; ++k) word[k] = chunk_word_normal(&h[4 * k], R, ND, MG);
+        } else {
+            const float ds = d == 0.0f ? 1.0f : d * 0x1p64f;
+            const float rho = rcp_approx(ds);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) word[k] = chunk_word_tiny(&h[4 * k], ds, rho);
+        }
     }
     if (valid) {
         packed[c >> 2] = make_uint4(word[0], word[1], word[2], word[3]);
-        if ((lane & 3) == 0) scales[c >> 4] = d16;
+        if ((lane & (G / 32 - 1)) == 0) {
+            const int64_t g = c / (G / 8);  // 8 weights per chunk
+            scales[g] = d16;
+            if (kAsym) zeros[g] = static_cast<int8_t>(z - 8);
+        }
     }
 }
 
-template <bool kWide>
+template <bool kWide, int G, bool kAsym>
 __global__ void __launch_bounds__(kQuantThreads)
 quantize_rtn_kernel(const uint8_t* __restrict__ W, uint4* __restrict__ packed,
-                    __nv_bfloat16* __restrict__ scales, int64_t n_chunks) {
+                    __nv_bfloat16* __restrict__ scales, int8_t* __restrict__ zeros, int64_t n_chunks) {
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -253,12 +393,12 @@ quantize_rtn_kernel(const uint8_t* __restrict__ W, uint4* __restrict__ packed,
     load_quarter_or_zero<kWide>(W, c, n_chunks, A);
     while (true) {  // u < n_units here, so the whole warp runs each body
         if (u + n_warps < n_units) load_quarter_or_zero<kWide>(W, c + stride, n_chunks, B);
-        quantize_quarter(A, c, c < n_chunks, lane, packed, scales);
+        quantize_quarter<G, kAsym>(A, c, c < n_chunks, lane, packed, scales, zeros);
         u += n_warps;
         c += stride;
         if (u >= n_units) break;
         if (u + n_warps < n_units) load_quarter_or_zero<kWide>(W, c + stride, n_chunks, A);
-        quantize_quarter(B, c, c < n_chunks, lane, packed, scales);
+        quantize_quarter<G, kAsym>(B, c, c < n_chunks, lane, packed, scales, zeros);
         u += n_warps;
         c += stride;
         if (u >= n_units) break;
@@ -428,12 +568,30 @@ cudaError_t launch_one_wave(Kernel kernel, int occ, int64_t n_chunks, const Devi
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+template <bool kWide, int G, bool kAsym>
+cudaError_t launch_quantize_t(const void* W, int64_t n_chunks, void* packed, void* scales, void* zeros,
+                              const DeviceInfo& dev, cudaStream_t stream) {
+    static const int occ = resident_ctas_per_sm(quantize_rtn_kernel<kWide, G, kAsym>);
+    return launch_one_wave(quantize_rtn_kernel<kWide, G, kAsym>, occ, n_chunks, dev, stream,
+                           static_cast<const uint8_t*>(W), static_cast<uint4*>(packed),
+                           static_cast<__nv_bfloat16*>(scales), static_cast<int8_t*>(zeros), n_chunks);
+}
+
 template <bool kWide>
-cudaError_t launch_quantize_t(const void* W, int64_t n_chunks, void* packed, void* scales, const DeviceInfo& dev,
-                              cudaStream_t stream) {
-    static const int occ = resident_ctas_per_sm(quantize_rtn_kernel<kWide>);
-    return launch_one_wave(quantize_rtn_kernel<kWide>, occ, n_chunks, dev, stream, static_cast<const uint8_t*>(W),
-                           static_cast<uint4*>(packed), static_cast<__nv_bfloat16*>(scales), n_chunks);
+cudaError_t launch_quantize_g(const void* W, int64_t n_chunks, int group, void* packed, void* scales, void* zeros,
+                              const DeviceInfo& dev, cudaStream_t stream) {
+    const bool asym = zeros != nullptr;
+    switch (group) {
+        case 32:
+            return asym ? launch_quantize_t<kWide, 32, true>(W, n_chunks, packed, scales, zeros, dev, stream)
+                        : launch_quantize_t<kWide, 32, false>(W, n_chunks, packed, scales, zeros, dev, stream);
+        case 64:
+            return asym ? launch_quantize_t<kWide, 64, true>(W, n_chunks, packed, scales, zeros, dev, stream)
+                        : launch_quantize_t<kWide, 64, false>(W, n_chunks, packed, scales, zeros, dev, stream);
+        default:
+            return asym ? launch_quantize_t<kWide, 128, true>(W, n_chunks, packed, scales, zeros, dev, stream)
+                        : launch_quantize_t<kWide, 128, false>(W, n_chunks, packed, scales, zeros, dev, stream);
+    }
 }
 
 template <bool kWideS>
@@ -473,8 +631,8 @@ scale_activations_kernel(const uint4* x, const float* __restrict__ s, uint4* out
 
 }  // namespace
 
-cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, void* packed, void* scales, const float* s,
-                            const DeviceInfo& dev, cudaStream_t stream) {
+cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, int group, void* packed, void* scales, void* zeros,
+                            const float* s, const DeviceInfo& dev, cudaStream_t stream) {
     const int64_t n_chunks = N * K / 8, row_chunks = K / 8;
     if (s) {
         if ((reinterpret_cast<uintptr_t>(s) & 31u) == 0)
@@ -483,8 +641,8 @@ cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, void* packed, v
     }
     // 32-byte loads need a 32-byte aligned base; the ABI promises 16.
     if ((reinterpret_cast<uintptr_t>(W) & 31u) == 0)
-        return launch_quantize_t<true>(W, n_chunks, packed, scales, dev, stream);
-    return launch_quantize_t<false>(W, n_chunks, packed, scales, dev, stream);
+        return launch_quantize_g<true>(W, n_chunks, group, packed, scales, zeros, dev, stream);
+    return launch_quantize_g<false>(W, n_chunks, group, packed, scales, zeros, dev, stream);
 }
 
 cudaError_t launch_scale_activations(const void* x, int64_t M, int64_t K, const float* s, void* out,

@@ -43,7 +43,9 @@
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    Work is enqueued asynchronously on it; nothing synchronises, except
  *    w4_last_device_status().
- *  - K must be a multiple of 128 and group must be 128; N, M, K ≥ 0.  Sizes
+ *  - K must be a multiple of 128; group is 128 except where an entry point
+ *    says otherwise (32, 64 or 128 for the quantisers and w4_gemm_affine);
+ *    N, M, K ≥ 0.  Sizes
  *    with N·K ≥ 2^62 are rejected; the matmul also needs N, M, K < 2^31
  *    (W4_ERR_UNSUPPORTED otherwise).
  *  - W, x and packed must be 16-byte aligned; scales and y 2-byte aligned.
@@ -85,20 +87,49 @@ typedef enum w4_gemm_path {
 /* Bytes of the packed code buffer: N·K/2.  0 for invalid sizes. */
 size_t w4_packed_bytes(int64_t N, int64_t K);
 
-/* Bytes of the scale buffer: N·(K/group)·2.  0 for invalid sizes. */
+/* Bytes of the scale buffer: N·(K/group)·2 (group 32, 64 or 128).  0 for
+ * invalid sizes. */
 size_t w4_scales_bytes(int64_t N, int64_t K, int32_t group);
+
+/* Bytes of the zero-point buffer of the asymmetric format: N·(K/group).  0 for
+ * invalid sizes. */
+size_t w4_zeros_bytes(int64_t N, int64_t K, int32_t group);
 
 /*
  * w4_quantize_rtn — RTN symmetric INT4 quantisation of W (§1 equation with
- * z = 0; §2 settings: group 128, minmax · symmetric, no calibration).
+ * z = 0; §2 settings: group 128, minmax · symmetric, no calibration).  Groups
+ * of 32 or 64 (§2 settings table: smaller groups follow the range more closely
+ * at the cost of more scales) apply the same rules per group.
  *   W       in : bf16 [N, K]
- *   packed  out: u8   [N, K/2]  (layout above)
- *   scales  out: bf16 [N, K/128]
+ *   group   in : 128 (the study's setting), 64 or 32
+ *   packed  out: u8   [N, K/2]  (layout above; the same for every group size)
+ *   scales  out: bf16 [N, K/group]
  * Deterministic and bit-exact: for every group, d = bf16_rne(fp32(max|w|/7))
  * and q = clamp(round_half_even(fp32(w/d)), −8, 7).  N = 0 or K = 0 is a no-op.
+ * Only group 128 is read by w4_gemm; w4_gemm_affine reads every group size.
  */
 int w4_quantize_rtn(const void* W, int64_t N, int64_t K, int32_t group,
                     void* packed, void* scales, void* stream);
+
+/*
+ * w4_quantize_rtn_asym — RTN asymmetric INT4 (§1 equation with a free zero
+ * point z, the code of real zero in the §1 symbol table), per group of 32, 64
+ * or 128:
+ *   lo = min(0, min w), hi = max(0, max w),
+ *   d  = bf16_rne(fp32(fp32(hi − lo) / 15))          (IEEE fp32 steps),
+ *   z  = clamp(round_half_even(fp32(−lo / d)), 0, 15) (z = 8 where d = 0),
+ *   q  = clamp(round_half_even(fp32(w / d)) + z, 0, 15),
+ * so ŵ = d·(q − z).  Stored: the nibble q − 8 in the packed layout above and
+ * the int8 z − 8 per group; ŵ = d·(stored code − stored zero).  (The symmetric
+ * format is the case stored zero = 0.)
+ *   W       in : bf16 [N, K]
+ *   packed  out: u8   [N, K/2]
+ *   scales  out: bf16 [N, K/group]
+ *   zeros   out: int8 [N, K/group], any alignment
+ * Bit-exact and deterministic.  N = 0 or K = 0 is a no-op.
+ */
+int w4_quantize_rtn_asym(const void* W, int64_t N, int64_t K, int32_t group,
+                         void* packed, void* scales, void* zeros, void* stream);
 
 /*
  * AWQ-style channel scaling (§2 AWQ equation: W'_ij = W_ij·s_j and
@@ -156,6 +187,21 @@ int w4_gemm(const void* x, int64_t M, int64_t N, int64_t K,
 int w4_gemm_ex(const void* x, int64_t M, int64_t N, int64_t K,
                const void* packed, const void* scales, void* y, void* stream,
                int32_t path);
+
+/*
+ * w4_gemm_affine — y = Ŵ x for every stored format: ŵ = d·(c − z') with c the
+ * stored code, d the scale and z' the stored zero of its group (z' = 0 when
+ * zeros is NULL, the symmetric format).
+ *   group   in : 32, 64 or 128 (the group size the weights were quantised with)
+ *   scales  in : bf16 [N, K/group]
+ *   zeros   in : int8 [N, K/group] from w4_quantize_rtn_asym, or NULL
+ * Same kernels, paths, accuracy and argument rules as w4_gemm_ex; group 128
+ * with zeros NULL is w4_gemm_ex itself.  Other formats dequantise each weight
+ * to bf16(d·(c − z')) (one rounding) before the products.
+ */
+int w4_gemm_affine(const void* x, int64_t M, int64_t N, int64_t K, int32_t group,
+                   const void* packed, const void* scales, const void* zeros,
+                   void* y, void* stream, int32_t path);
 
 /* The kernel W4_PATH_AUTO picks for these sizes (W4_PATH_SMALL_M or
  * W4_PATH_TENSOR), or a negative w4_status for invalid sizes. */

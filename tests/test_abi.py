@@ -41,7 +41,13 @@ def test_every_declared_symbol_is_exported(lib):
 def test_size_helpers(lib):
     assert lib.w4_packed_bytes(2560, 9216) == 2560 * 9216 // 2
     assert lib.w4_scales_bytes(2560, 9216, 128) == 2560 * 72 * 2
-    assert lib.w4_scales_bytes(2560, 9216, 64) == 0
+    assert lib.w4_scales_bytes(2560, 9216, 64) == 2560 * 144 * 2
+    assert lib.w4_scales_bytes(2560, 9216, 32) == 2560 * 288 * 2
+    assert lib.w4_scales_bytes(2560, 9216, 96) == 0
+    assert lib.w4_zeros_bytes(2560, 9216, 128) == 2560 * 72
+    assert lib.w4_zeros_bytes(2560, 9216, 32) == 2560 * 288
+    assert lib.w4_zeros_bytes(2560, 9216, 16) == 0
+    assert lib.w4_zeros_bytes(4, 100, 32) == 0
     assert lib.w4_packed_bytes(4, 100) == 0
     assert lib.w4_packed_bytes(-1, 128) == 0
     # packed + scales = 0.515625 bytes per weight
@@ -67,7 +73,8 @@ A16 = 0x10000  # fake, never dereferenced: every case below fails its checks fir
 
 
 @pytest.mark.parametrize("args,expect", [
-    ((A16, 4, 256, 64, A16, A16, None), w4.W4_ERR_UNSUPPORTED),        # group 64
+    ((A16, 4, 256, 96, A16, A16, None), w4.W4_ERR_UNSUPPORTED),        # group 96
+    ((A16, 4, 256, 16, A16, A16, None), w4.W4_ERR_UNSUPPORTED),        # group 16
     ((A16, 4, 200, 128, A16, A16, None), w4.W4_ERR_UNSUPPORTED),       # K % 128
     ((A16, -4, 256, 128, A16, A16, None), w4.W4_ERR_INVALID_ARG),      # negative N
     ((None, 4, 256, 128, A16, A16, None), w4.W4_ERR_INVALID_ARG),      # null W
@@ -108,6 +115,32 @@ def test_awq_empty_is_noop(lib):
     assert lib.w4_quantize_rtn_scaled(None, 0, 256, 128, None, None, None, None) == w4.W4_OK
     assert lib.w4_scale_activations(None, 0, 256, None, None, None) == w4.W4_OK
     assert lib.w4_scale_activations(None, 3, 0, None, None, None) == w4.W4_OK
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((A16, 4, 256, 96, A16 * 4, A16 * 8, A16 * 12, None), w4.W4_ERR_UNSUPPORTED),      # group 96
+    ((A16, 4, 256, 32, A16 * 4, A16 * 8, None, None), w4.W4_ERR_INVALID_ARG),          # null zeros
+    ((A16, 4, 256, 32, A16 * 4, A16 * 8, A16 * 8 + 8, None), w4.W4_ERR_INVALID_ARG),   # zeros in scales
+    ((A16, 4, 256, 32, A16 * 4, A16 * 8, A16 + 100, None), w4.W4_ERR_INVALID_ARG),     # zeros in W
+    ((A16, 4, 256, 64, A16 * 4 + 8, A16 * 8, A16 * 12, None), w4.W4_ERR_MISALIGNED),   # packed at 8 B
+])
+def test_quantize_asym_rejects(lib, args, expect):
+    assert lib.w4_quantize_rtn_asym(*args) == expect
+
+
+def test_quantize_scaled_needs_group_128(lib):
+    assert lib.w4_quantize_rtn_scaled(A16, 4, 256, 64, A16 * 12, A16 * 4, A16 * 8, None) == w4.W4_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((A16, 1, 4, 256, 96, A16 * 2, A16 * 4, None, A16 * 8, None, 0), w4.W4_ERR_UNSUPPORTED),  # group 96
+    ((A16, 1, 4, 200, 32, A16 * 2, A16 * 4, None, A16 * 8, None, 0), w4.W4_ERR_UNSUPPORTED),  # K % 128
+    ((A16, 1, 4, 256, 32, A16 * 2, A16 * 4, None, A16 * 8, None, 5), w4.W4_ERR_INVALID_ARG),  # bad path
+    ((A16, 1, 4, 256, 32, A16 * 2, A16 * 4, A16 * 8, A16 * 8, None, 0), w4.W4_ERR_INVALID_ARG),  # y on zeros
+    ((A16, 1, 4, 256, 64, A16 * 2 + 4, A16 * 4, None, A16 * 8, None, 0), w4.W4_ERR_MISALIGNED),
+])
+def test_gemm_affine_rejects(lib, args, expect):
+    assert lib.w4_gemm_affine(*args) == expect
 
 
 def test_quantize_empty_is_noop(lib):

@@ -1,0 +1,163 @@
+"""GPU parity of the affine formats (Qwen3.5-4B quantisation study, §1
+group-quantisation equation with a free zero point z; §2 settings table on
+smaller groups) against the CPU oracle: w4_quantize_rtn at groups 32/64 and
+w4_quantize_rtn_asym at 32/64/128 must give the oracle's packed bytes, scale
+bits and zeros exactly; w4_gemm_affine must stay within the parity bound on
+both kernel paths."""
+import numpy as np
+import pytest
+import torch
+
+from gemm_rtn_sym_gb300 import W4_PATH_SMALL_M, W4_PATH_TENSOR
+from gemm_rtn_sym_gb300 import workloads as wl
+from oracle import w4_oracle as O
+from tests.helpers import guarded, guards_intact
+from tests.test_gpu_quantize import tie_and_range_matrix
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def quantize_gpu(w4, W, group, asym):
+    N, K = W.shape
+    packed, pbuf = guarded((N, K // 2), torch.uint8, W.device)
+    scales, sbuf = guarded((N, K // group), torch.bfloat16, W.device)
+    if asym:
+        zeros, zbuf = guarded((N, K // group), torch.uint8, W.device)
+        zeros = zeros.view(torch.int8)
+        w4.w4_quantize_rtn_asym(W, group, packed=packed, scales=scales, zeros=zeros)
+    else:
+        zeros, zbuf = None, None
+        w4.w4_quantize_rtn(W, group, packed=packed, scales=scales)
+    torch.cuda.synchronize()
+    assert guards_intact(pbuf) and guards_intact(sbuf), "quantiser wrote outside its outputs"
+    if zbuf is not None:
+        assert guards_intact(zbuf), "quantiser wrote outside the zeros"
+    return packed, scales, zeros
+
+
+def check(W, group, asym, packed, scales, zeros):
+    Wb = wl.bits(W)
+    if asym:
+        p_ref, s_ref, z_ref = O.quantize_rtn_asym(Wb, group)
+        zg = zeros.cpu().numpy()
+        assert np.array_equal(zg, z_ref), f"zeros differ in {np.count_nonzero(zg != z_ref)} places"
+    else:
+        p_ref, s_ref = O.quantize_rtn(Wb, group)
+    sg, pg = wl.bits(scales), packed.cpu().numpy()
+    assert np.array_equal(sg, s_ref), f"scale bits differ in {np.count_nonzero(sg != s_ref)} places"
+    assert np.array_equal(pg, p_ref), f"packed bytes differ in {np.count_nonzero(pg != p_ref)} places"
+
+
+FORMATS = [(32, False), (64, False), (32, True), (64, True), (128, True)]
+
+
+@pytest.mark.parametrize("group,asym", FORMATS)
+@pytest.mark.parametrize("N,K", [(1, 128), (7, 256), (129, 1152), (300, 9216), (33, 2560)])
+def test_quantize_small_shapes(cuda_lib, N, K, group, asym):
+    W = wl.random_bf16((N, K), 0.02, seed=N * 1000 + K + group, device=DEV)
+    check(W, group, asym, *quantize_gpu(cuda_lib, W, group, asym))
+
+
+@pytest.mark.parametrize("group,asym", FORMATS)
+def test_quantize_full_outlier(cuda_lib, group, asym):
+    W = wl.weight("outlier", device=DEV)
+    check(W, group, asym, *quantize_gpu(cuda_lib, W, group, asym))
+
+
+@pytest.mark.parametrize("group,asym", FORMATS)
+def test_quantize_every_quotient_and_tie(cuda_lib, group, asym):
+    """Normal, tiny and subnormal groups, exact ties, signed mixes."""
+    Wc = tie_and_range_matrix()
+    check(Wc, group, asym, *quantize_gpu(cuda_lib, Wc.to(DEV), group, asym))
+
+
+@pytest.mark.parametrize("group,asym", FORMATS)
+def test_quantize_16_byte_aligned_input(cuda_lib, group, asym):
+    W = wl.random_bf16((129, 1152), 0.02, seed=7 + group, device=DEV)
+    N, K = W.shape
+    flat = torch.empty(N * K + 64, dtype=torch.bfloat16, device=DEV)
+    Wv = flat[8:8 + N * K].view(N, K)
+    Wv.copy_(W)
+    check(W, group, asym, *quantize_gpu(cuda_lib, Wv, group, asym))
+
+
+def test_asym_special_groups(cuda_lib):
+    K = 512
+    W = torch.zeros((7, K), dtype=torch.float32)
+    W[1, :128] = 0.25 + torch.arange(128) / 512      # all positive
+    W[2, :128] = -(0.25 + torch.arange(128) / 512)   # all negative
+    W[3, :128] = 0.75                                # constant
+    W[4, 128:256] = torch.linspace(-1e-38, 3e-38, 128)
+    W[5, 256:] = 3e-39
+    Wb = W.to(torch.bfloat16)
+    Wb.view(torch.int16)[6, :128] = -32737          # 0x801F: subnormal, clipped zero point
+    Wb.view(torch.int16)[6, 130] = 1
+    for group in (32, 64, 128):
+        check(Wb, group, True, *quantize_gpu(cuda_lib, Wb.to(DEV), group, True))
+
+
+@pytest.mark.parametrize("group,asym", FORMATS + [(128, False)])
+@pytest.mark.parametrize("M", [1, 5, 8, 16, 17, 33, 208])
+def test_gemm_affine_parity(cuda_lib, group, asym, M):
+    N, K = 300, 1152
+    W = wl.random_bf16((N, K), 0.02, seed=11 + group, device=DEV)
+    x = wl.random_bf16((M, K), 1.0, seed=M, device=DEV)
+    packed, scales, zeros = quantize_gpu(cuda_lib, W, group, asym)
+    Wb = wl.bits(W)
+    if asym:
+        p_ref, s_ref, z_ref = O.quantize_rtn_asym(Wb, group)
+    else:
+        (p_ref, s_ref), z_ref = O.quantize_rtn(Wb, group), None
+    y_ref, s_abs = O.gemm_reference(wl.bits(x), p_ref, s_ref, K, group, z_ref)
+    for path in (W4_PATH_SMALL_M, W4_PATH_TENSOR):
+        y, ybuf = guarded((M, N), torch.bfloat16, x.device)
+        cuda_lib.w4_gemm_affine(x, packed, scales, zeros, group=group, out=y, path=path)
+        torch.cuda.synchronize()
+        assert guards_intact(ybuf), "matmul wrote outside y"
+        assert cuda_lib.w4_last_device_status() == 0
+        excess = O.parity_excess(wl.bits(y), y_ref, s_abs)
+        assert float(excess.max()) <= 1.0, (path, float(excess.max()))
+
+
+@pytest.mark.parametrize("group,asym", FORMATS)
+@pytest.mark.parametrize("M", [1, 8, 208])
+def test_gemm_affine_full_outlier_sampled(cuda_lib, group, asym, M):
+    W = wl.weight("outlier", device=DEV)
+    N, K = W.shape
+    x = wl.activations("outlier", M, K, device=DEV)
+    packed, scales, zeros = quantize_gpu(cuda_lib, W, group, asym)
+    y = cuda_lib.w4_gemm_affine(x, packed, scales, zeros, group=group)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([np.arange(8), np.arange(N - 8, N),
+                                     np.random.default_rng(group + M).choice(N, 96, replace=False)]))
+    Wb = wl.bits(W)[rows]
+    if asym:
+        p_ref, s_ref, z_ref = O.quantize_rtn_asym(Wb, group)
+    else:
+        (p_ref, s_ref), z_ref = O.quantize_rtn(Wb, group), None
+    y_ref, s_abs = O.gemm_reference(wl.bits(x), p_ref, s_ref, K, group, z_ref)
+    excess = O.parity_excess(wl.bits(y)[:, rows], y_ref, s_abs)
+    assert float(excess.max()) <= 1.0
+
+
+def test_affine_group128_symmetric_is_w4_gemm(cuda_lib):
+    W = wl.random_bf16((256, 2048), 0.02, seed=3, device=DEV)
+    packed, scales = cuda_lib.w4_quantize_rtn(W)
+    for M in (1, 8, 40):
+        x = wl.random_bf16((M, 2048), 1.0, seed=M + 1, device=DEV)
+        a = cuda_lib.w4_gemm_ex(x, packed, scales)
+        b = cuda_lib.w4_gemm_affine(x, packed, scales, None, group=128)
+        torch.cuda.synchronize()
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("group", [32, 64, 128])
+def test_gemm_affine_repeat_is_bit_identical(cuda_lib, group):
+    W = wl.random_bf16((512, 4096), 0.02, seed=5, device=DEV)
+    packed, scales, zeros = quantize_gpu(cuda_lib, W, group, True)
+    for M in (3, 13, 64):
+        x = wl.random_bf16((M, 4096), 1.0, seed=M, device=DEV)
+        ys = [cuda_lib.w4_gemm_affine(x, packed, scales, zeros, group=group) for _ in range(5)]
+        torch.cuda.synchronize()
+        assert all(torch.equal(ys[0].view(torch.int16), v.view(torch.int16)) for v in ys[1:])
