@@ -53,6 +53,13 @@ same ones, independently):
   q = clip(round_half_even(fp32(w / d)) + z, 0, 15); where d = 0, z = 8 and
   q = z.  Stored: the nibble q − 8 in the same layout and an int8 zero z − 8
   per group, so ŵ = d·(stored code − stored zero);
+* GPTQ (§2 settings table and H' equation; the update rule of the published
+  GPTQ algorithm): fp64 throughout; λ = 0.01·mean(diag H); columns in their
+  original order; blocks of 128 columns; each group's scale is taken at the
+  group's first column from its current (corrected) weights, d =
+  bf16_rne(fp32(max|w|/7)) with the quotient in fp64, and q =
+  clip(round_half_even(w/d), −8, 7) in fp64; H is an input (the study's
+  calibration statistic; there is no calibration data here);
 * the matmul reference accumulates ŵ·x in fp64 (exact products), and the
   parity bound is |y_gpu − y_ref| ≤ 4e-3 · Σ_k |ŵ_k x_k| + ulp_bf16(y_ref).
 
@@ -298,6 +305,91 @@ def quantize_rtn_scaled(W_bits: np.ndarray, s, group: int = GROUP):
     """RTN of the channel-scaled weights: quantize_rtn(W') with W' from
     :func:`awq_scale_weights`.  Same storage as :func:`quantize_rtn`."""
     return quantize_rtn(awq_scale_weights(W_bits, s), group)
+
+
+# ---------------------------------------------------------------------------
+# GPTQ into the same storage (§2 settings table: GPTQ, same storage as RTN,
+# damping 0.01, no reordering, 128-column blocks; §2 H' = H + λI with
+# λ = 0.01·mean(diag H); §2 method table: quantise one column, then correct
+# the remaining weights).  The update rule is the published GPTQ algorithm
+# (Frantar et al., "GPTQ: Accurate Post-Training Quantization for Generative
+# Pre-trained Transformers", 2022, Algorithm 1), restated in fp64.
+# ---------------------------------------------------------------------------
+GPTQ_DAMP = 0.01
+GPTQ_BLOCK = 128
+
+
+def gptq_damped(H, damp: float = GPTQ_DAMP) -> np.ndarray:
+    """H' = H + λI with λ = damp·mean(diag H), fp64."""
+    H = np.asarray(H, dtype=np.float64)
+    K = H.shape[0]
+    return H + damp * np.mean(np.diag(H)) * np.eye(K)
+
+
+def gptq_inverse_factor(H, damp: float = GPTQ_DAMP) -> np.ndarray:
+    """Upper-triangular U with Uᵀ U = (H')⁻¹ (library inverse and Cholesky)."""
+    Hinv = np.linalg.inv(gptq_damped(H, damp))
+    L = np.linalg.cholesky((Hinv + Hinv.T) / 2)  # lower: Hinv = L Lᵀ
+    return L.T
+
+
+def gptq_group_scale(w: np.ndarray) -> np.ndarray:
+    """Scale bits of groups of real-valued weights (last axis): d =
+    bf16_rne(fp32(max|w| / 7)), the quotient taken in fp64 then rounded to fp32
+    (for bf16 weights this is the RTN scale exactly)."""
+    a = np.max(np.abs(np.asarray(w, dtype=np.float64)), axis=-1)
+    return f32_to_bf16_bits_rne((a / DIVISOR).astype(np.float32))
+
+
+def gptq_round(w: np.ndarray, d: np.ndarray) -> np.ndarray:
+    """q = clip(round_half_even(w / d), −8, 7) in fp64, q = 0 where d = 0."""
+    zero = d == 0
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = np.where(zero, 0.0, w / np.where(zero, 1.0, d))
+    return np.clip(np.rint(r), Q_MIN, Q_MAX)
+
+
+def gptq_quantize(W_bits: np.ndarray, H, group: int = GROUP, block: int = GPTQ_BLOCK,
+                  damp: float = GPTQ_DAMP):
+    """GPTQ of W (bf16 bits [N, K]) with the calibration statistic H ([K, K],
+    symmetric positive semi-definite) -> (packed u8 [N, K/2], scale bits
+    [N, K/group]), the RTN storage.
+
+    Columns are taken in their original order in blocks of ``block``.  At the
+    first column of each group the group's scale comes from its current
+    (already corrected) weights.  Column c is rounded with that scale; its
+    error, divided by U[c, c], corrects the later columns of the block at once
+    (row c of U) and the columns after the block when the block ends."""
+    W = bf16_bits_to_f32(np.asarray(W_bits, dtype=np.uint16)).astype(np.float64)
+    N, K = W.shape
+    if group not in GROUPS or K % GROUP:
+        raise ValueError("group must be 32, 64 or 128 and K a multiple of 128")
+    if block % group and group % block:
+        raise ValueError("block and group sizes must divide one another")
+    U = gptq_inverse_factor(H, damp)
+    q = np.zeros((N, K), dtype=np.int8)
+    s = np.zeros((N, K // group), dtype=np.uint16)
+    d = np.zeros(N)
+    for i1 in range(0, K, block):
+        i2 = min(i1 + block, K)
+        W1 = W[:, i1:i2].copy()
+        E1 = np.zeros_like(W1)
+        for j in range(i2 - i1):
+            c = i1 + j
+            if c % group == 0:
+                # Current weights of the group: inside the block they carry the
+                # block's corrections so far; a group longer than the block
+                # starts at a block start, where W is already current.
+                cur = W1[:, j:j + group] if j + group <= i2 - i1 else W[:, c:c + group]
+                s[:, c // group] = gptq_group_scale(cur)
+                d = bf16_bits_to_f32(s[:, c // group]).astype(np.float64)
+            qc = gptq_round(W1[:, j], d)
+            q[:, c] = qc.astype(np.int8)
+            err = (W1[:, j] - d * qc) / U[c, c]
+            W1[:, j:] -= np.outer(err, U[c, c:i2])
+            E1[:, j] = err
+        W[:, i2:] -= E1 @ U[i1:i2, i2:]
+    return pack_p1(q), s
 
 
 # ---------------------------------------------------------------------------

@@ -10,6 +10,7 @@ import types
 
 import pytest
 
+import tests.test_oracle_gptq as gptq
 import tests.test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "w4_oracle.py")
@@ -67,6 +68,15 @@ MUTANTS = {
     "asym_codes_unshifted": ("return pack_p1((q - 8).astype(np.int8)), d_bits",
                              "return pack_p1(q.astype(np.int8)), d_bits"),
     "dequant_group_fixed_128": ("c = c.reshape(N, K // group, group)", "c = c.reshape(N, K // GROUP, GROUP)"),
+    "gptq_lower_factor": ("    return L.T\n", "    return L\n"),
+    "gptq_absolute_damping": ("return H + damp * np.mean(np.diag(H)) * np.eye(K)", "return H + damp * np.eye(K)"),
+    "gptq_no_damping": ("return H + damp * np.mean(np.diag(H)) * np.eye(K)", "return H + 0.0 * np.eye(K)"),
+    "gptq_error_unscaled": ("err = (W1[:, j] - d * qc) / U[c, c]", "err = (W1[:, j] - d * qc)"),
+    "gptq_no_block_carry": ("W[:, i2:] -= E1 @ U[i1:i2, i2:]", "W[:, i2:] -= 0.0"),
+    "gptq_column_not_row": ("W1[:, j:] -= np.outer(err, U[c, c:i2])", "W1[:, j:] -= np.outer(err, U[c:i2, c])"),
+    "gptq_scale_from_original": (
+        "cur = W1[:, j:j + group] if j + group <= i2 - i1 else W[:, c:c + group]",
+        "cur = bf16_bits_to_f32(np.asarray(W_bits, dtype=np.uint16))[:, c:c + group]"),
 }
 
 PIN_TESTS = [
@@ -99,6 +109,12 @@ PIN_TESTS = [
     lambda: pins.test_asym_matmul_bruteforce(32),
     lambda: pins.test_asym_invariants("ffn", 64),
     pins.test_asym_special_groups,
+    gptq.test_gptq_matches_obs_route,
+    gptq.test_gptq_diagonal_h_is_rtn,
+    lambda: gptq.test_gptq_block_size_does_not_change_the_result(32),
+    gptq.test_gptq_scale_invariant_in_h,
+    gptq.test_gptq_first_group_scale_is_rtn,
+    gptq.test_gptq_singular_h,
 ]
 
 
@@ -114,6 +130,7 @@ def load_mutant(old: str, new: str) -> types.ModuleType:
 def test_every_mutant_is_caught(name, monkeypatch):
     mutant = load_mutant(*MUTANTS[name])
     monkeypatch.setattr(pins, "O", mutant)
+    monkeypatch.setattr(gptq, "O", mutant)
     caught = []
     for t in PIN_TESTS:
         try:
