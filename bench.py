@@ -16,7 +16,7 @@ graphs holding only that kernel's K launches, replayed right after.
 Sub-benchmarks (M = 1, M = 8, the 27B-class layer at M ∈ {1,5,7,13}, the
 70B-class layer at M = 208, the 4B-class 200-matrix stack sweep, quantiser
 alone, the AWQ-style channel-scaled quantiser and activation scaling, the
-asymmetric and group-32/64 formats) are reported under "sub".
+asymmetric and group-32/64 formats, GPTQ) are reported under "sub".
 
 `--impl reference` times the CPU oracle (the only other program here that
 computes the same thing) on a bounded sample of the same workload.
@@ -459,6 +459,38 @@ def affine_set(torch, w4, wl, workload, matrix, Ms, group, asym, pk, reps=10):
     return res
 
 
+FP64_NOMINAL_TFLOPS = 1.25  # GB300 dense fp64, nominal (no measured figure in MEASURED_PEAKS.json)
+
+
+def gptq_set(torch, w4, wl, workload, pk, T=4096, reps=3):
+    """GPTQ of one matrix of a workload: the factor of its input's calibration
+    statistic (once per input) and the per-matrix quantisation, both fp64."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    N, K = wl.SHAPES[workload][0]
+    W = wl.weight(workload, 0, device=dev)
+    H = wl.calibration_hessian(K, T, seed=wl.seed_for(workload, 0, 4), device=dev)
+    U = torch.empty((K, K), dtype=torch.float64, device=dev)
+    fws = torch.empty(w4.w4_gptq_factor_workspace_bytes(K), dtype=torch.uint8, device=dev)
+    qws = torch.empty(w4.w4_gptq_workspace_bytes(N, K), dtype=torch.uint8, device=dev)
+    packed = torch.empty((N, K // 2), dtype=torch.uint8, device=dev)
+    scales = torch.empty((N, K // 128), dtype=torch.bfloat16, device=dev)
+    w4.w4_gptq_factor(H, U=U, workspace=fws)
+    w4.w4_gptq_quantize(W, U, packed=packed, scales=scales, workspace=qws)
+    T_ = Timer(torch)
+    t_f = T_.time(lambda: w4.w4_gptq_factor(H, U=U, workspace=fws), reps=reps)
+    t_q = T_.time(lambda: w4.w4_gptq_quantize(W, U, packed=packed, scales=scales, workspace=qws), reps=reps)
+    assert w4.w4_last_device_status() == 0
+    f_f = 4.0 / 3.0 * K ** 3
+    f_q = 2.0 * N * 128 * sum(K - i2 for i2 in range(128, K, 128)) + N * K * 128
+    del W, H, U, fws, qws, packed, scales
+    torch.cuda.empty_cache()
+    return {"shape": [N, K], "calibration_rows": T,
+            "factor": {"ms": t_f * 1e3, "GFLOP/s": f_f / t_f / 1e9, "bound": "fp64",
+                       "frac": f_f / t_f / 1e12 / FP64_NOMINAL_TFLOPS, "peak": "nominal 1.25 TFLOP/s fp64"},
+            "quantize": {"ms": t_q * 1e3, "GFLOP/s": f_q / t_q / 1e9, "bound": "fp64",
+                         "frac": f_q / t_q / 1e12 / FP64_NOMINAL_TFLOPS, "peak": "nominal 1.25 TFLOP/s fp64"}}
+
+
 def cpu_oracle_sample(wl, rows, reps_seconds=10.0, min_reps=1):
     """Oracle quantise + matmul of `rows` rows of the headline matrix at M = 8."""
     import numpy as np
@@ -536,6 +568,8 @@ def run_gpu(args):
             sub["outlier_m8"] = gemm_set(torch, w4, wl, "outlier", [8], pk)["M8"]
         if want("quant"):
             sub["quant_ffn"] = quant_set(torch, w4, wl, "ffn", pk)
+        if want("gptq"):
+            sub["gptq_ffn"] = gptq_set(torch, w4, wl, "ffn", pk)
         if want("affine"):
             for group, asym in ((128, True), (64, True), (32, True), (32, False)):
                 key = f"affine_g{group}_{'asym' if asym else 'sym'}"

@@ -19,6 +19,8 @@ __all__ = [
     "load", "library_path", "W4Error",
     "w4_quantize_rtn", "w4_quantize_rtn_scaled", "w4_scale_activations", "w4_quantize_rtn_asym",
     "w4_gemm", "w4_gemm_ex", "w4_gemm_affine", "w4_gemm_path_for", "w4_zeros_bytes", "GROUPS",
+    "w4_gptq_factor", "w4_gptq_quantize", "w4_gptq_workspace_bytes", "w4_gptq_factor_workspace_bytes",
+    "W4_ERR_NUMERIC",
     "w4_packed_bytes", "w4_scales_bytes", "w4_last_device_status", "w4_wait_probe",
     "w4_status_string", "W4_PATH_AUTO", "W4_PATH_SMALL_M", "W4_PATH_TENSOR", "GROUP",
     "GroupedPlan", "w4_grouped_plan", "w4_gemm_grouped", "w4_gemm_grouped_noalloc",
@@ -26,7 +28,7 @@ __all__ = [
 
 GROUP = 128
 GROUPS = (32, 64, 128)
-W4_OK, W4_ERR_INVALID_ARG, W4_ERR_UNSUPPORTED, W4_ERR_MISALIGNED, W4_ERR_CUDA, W4_ERR_TIMEOUT = range(6)
+W4_OK, W4_ERR_INVALID_ARG, W4_ERR_UNSUPPORTED, W4_ERR_MISALIGNED, W4_ERR_CUDA, W4_ERR_TIMEOUT, W4_ERR_NUMERIC = range(7)
 W4_PATH_AUTO, W4_PATH_SMALL_M, W4_PATH_TENSOR = 0, 1, 2
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -54,6 +56,10 @@ _SIGNATURES = {
     "w4_quantize_rtn_scaled": (ctypes.c_int, [_vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp]),
     "w4_quantize_rtn_asym": (ctypes.c_int, [_vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp]),
     "w4_zeros_bytes": (_sz, [_i64, _i64, _i32]),
+    "w4_gptq_factor_workspace_bytes": (_sz, [_i64]),
+    "w4_gptq_factor": (ctypes.c_int, [_vp, _i64, ctypes.c_double, _vp, _vp, _sz, _vp]),
+    "w4_gptq_workspace_bytes": (_sz, [_i64, _i64]),
+    "w4_gptq_quantize": (ctypes.c_int, [_vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
     "w4_gemm_affine": (ctypes.c_int, [_vp, _i64, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _i32]),
     "w4_scale_activations": (ctypes.c_int, [_vp, _i64, _i64, _vp, _vp, _vp]),
     "w4_gemm": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp]),
@@ -223,6 +229,57 @@ def w4_scale_activations(x: torch.Tensor, s: torch.Tensor, out: torch.Tensor | N
         _check(load().w4_scale_activations(x.data_ptr(), M, K, s.data_ptr(), out.data_ptr(),
                                            _stream(x.device)), "w4_scale_activations")
     return out
+
+
+def w4_gptq_factor(H: torch.Tensor, damp: float = 0.01, U: torch.Tensor | None = None,
+                   workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """U (fp64 [K, K], upper triangle) with Uᵀ U = (H + λI)⁻¹, λ = damp·mean(diag H)."""
+    _cuda_tensor(H, "H", torch.float32, 2)
+    K = H.shape[0]
+    if tuple(H.shape) != (K, K):
+        raise ValueError("H must be square")
+    if U is None:
+        U = torch.empty((K, K), dtype=torch.float64, device=H.device)
+    _cuda_tensor(U, "U", torch.float64, 2)
+    if tuple(U.shape) != (K, K):
+        raise ValueError("U must be [K, K]")
+    with torch.cuda.device(H.device):
+        need = load().w4_gptq_factor_workspace_bytes(K)
+        if need == 0:
+            raise W4Error(W4_ERR_UNSUPPORTED, "w4_gptq_factor_workspace_bytes")
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=H.device)
+        _cuda_tensor(workspace, "workspace", torch.uint8, 1)
+        _check(load().w4_gptq_factor(H.data_ptr(), K, float(damp), U.data_ptr(), workspace.data_ptr(),
+                                     workspace.numel(), _stream(H.device)), "w4_gptq_factor")
+    return U
+
+
+def w4_gptq_quantize(W: torch.Tensor, U: torch.Tensor, group: int = GROUP, packed: torch.Tensor | None = None,
+                     scales: torch.Tensor | None = None, workspace: torch.Tensor | None = None):
+    """GPTQ of W (bf16 [N, K]) given U from w4_gptq_factor -> (packed u8 [N, K/2],
+    scales bf16 [N, K/group]), the RTN storage."""
+    N, K, packed, scales = _quant_outputs(W, group, packed, scales, "w4_gptq_quantize")
+    _cuda_tensor(U, "U", torch.float64, 2)
+    if tuple(U.shape) != (K, K):
+        raise ValueError("U must be [K, K]")
+    with torch.cuda.device(W.device):
+        need = load().w4_gptq_workspace_bytes(N, K)
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=W.device)
+        _cuda_tensor(workspace, "workspace", torch.uint8, 1)
+        _check(load().w4_gptq_quantize(W.data_ptr(), N, K, group, U.data_ptr(), packed.data_ptr(),
+                                       scales.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                                       _stream(W.device)), "w4_gptq_quantize")
+    return packed, scales
+
+
+def w4_gptq_workspace_bytes(N: int, K: int) -> int:
+    return load().w4_gptq_workspace_bytes(N, K)
+
+
+def w4_gptq_factor_workspace_bytes(K: int) -> int:
+    return load().w4_gptq_factor_workspace_bytes(K)
 
 
 def w4_gemm_ex(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,

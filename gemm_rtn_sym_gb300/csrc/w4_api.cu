@@ -140,6 +140,72 @@ int w4_quantize_rtn_scaled(const void* W, int64_t N, int64_t K, int32_t group, c
     return quantize_impl(W, N, K, group, s, true, false, packed, scales, nullptr, stream);
 }
 
+size_t w4_gptq_factor_workspace_bytes(int64_t K) {
+    if (check_sizes(1, K) != W4_OK || K == 0 || K > INT32_MAX) return 0;
+    return gptq_factor_workspace_bytes(K);
+}
+
+int w4_gptq_factor(const float* H, int64_t K, double damp, double* U, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+    if (const int s = check_sizes(1, K)) return s;
+    if (K == 0) return W4_OK;
+    if (K > INT32_MAX || static_cast<double>(K) * K > 1e18) return W4_ERR_UNSUPPORTED;
+    if (!(damp >= 0.0) || damp > 1e30) return W4_ERR_INVALID_ARG;
+    if (!H || !U || !workspace) return W4_ERR_INVALID_ARG;
+    if (!aligned(H, 4) || !aligned(U, 8) || !aligned(workspace, 256)) return W4_ERR_MISALIGNED;
+    const size_t hb = static_cast<size_t>(K) * K * 4, ub = static_cast<size_t>(K) * K * 8;
+    if (overlaps(H, hb, U, ub) || overlaps(workspace, workspace_bytes, H, hb) ||
+        overlaps(workspace, workspace_bytes, U, ub))
+        return W4_ERR_INVALID_ARG;
+    cudaError_t err;
+    const DeviceInfo* dev = device_info(&err);
+    if (!dev) return W4_ERR_CUDA;
+    if (dev->cc_major < 10) return W4_ERR_UNSUPPORTED;
+    switch (launch_gptq_factor(H, K, damp, U, workspace, workspace_bytes, *dev, static_cast<cudaStream_t>(stream))) {
+        case 0: return W4_OK;
+        case 2: return W4_ERR_INVALID_ARG;
+        default: return W4_ERR_CUDA;
+    }
+}
+
+size_t w4_gptq_workspace_bytes(int64_t N, int64_t K) {
+    if (check_sizes(N, K) != W4_OK || N == 0 || K == 0 || N > INT32_MAX || K > INT32_MAX) return 0;
+    if (static_cast<double>(N) * K > 1e18) return 0;
+    return gptq_workspace_bytes(N, K);
+}
+
+int w4_gptq_quantize(const void* W, int64_t N, int64_t K, int32_t group, const double* U, void* packed,
+                     void* scales, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!valid_group(group)) return W4_ERR_UNSUPPORTED;
+    if (const int s = check_sizes(N, K)) return s;
+    if (N == 0 || K == 0) return W4_OK;
+    if (N > INT32_MAX || K > INT32_MAX) return W4_ERR_UNSUPPORTED;
+    if (!W || !U || !packed || !scales || !workspace) return W4_ERR_INVALID_ARG;
+    if (!aligned(W, 16) || !aligned(U, 8) || !aligned(packed, 16) || !aligned(scales, 2) || !aligned(workspace, 256))
+        return W4_ERR_MISALIGNED;
+    const size_t wb = static_cast<size_t>(N * K) * 2, ub = static_cast<size_t>(K) * K * 8,
+                 pb = w4_packed_bytes(N, K), sb = w4_scales_bytes(N, K, group);
+    const void* outs[2] = {packed, scales};
+    const size_t ob[2] = {pb, sb};
+    for (int i = 0; i < 2; ++i)
+        if (overlaps(outs[i], ob[i], W, wb) || overlaps(outs[i], ob[i], U, ub) ||
+            overlaps(outs[i], ob[i], workspace, workspace_bytes))
+            return W4_ERR_INVALID_ARG;
+    if (overlaps(packed, pb, scales, sb) || overlaps(workspace, workspace_bytes, W, wb) ||
+        overlaps(workspace, workspace_bytes, U, ub))
+        return W4_ERR_INVALID_ARG;
+    cudaError_t err;
+    const DeviceInfo* dev = device_info(&err);
+    if (!dev) return W4_ERR_CUDA;
+    if (dev->cc_major < 10) return W4_ERR_UNSUPPORTED;
+    switch (launch_gptq(W, N, K, group, U, packed, scales, workspace, workspace_bytes, *dev,
+                        static_cast<cudaStream_t>(stream))) {
+        case 0: return W4_OK;
+        case 2: return W4_ERR_INVALID_ARG;
+        default: return W4_ERR_CUDA;
+    }
+}
+
 int w4_scale_activations(const void* x, int64_t M, int64_t K, const float* s, void* x_out, void* stream) {
     if (M < 0) return W4_ERR_INVALID_ARG;
     if (const int st = check_sizes(M, K)) return st;
@@ -439,6 +505,7 @@ const char* w4_status_string(int status) {
         case W4_ERR_MISALIGNED: return "W4_ERR_MISALIGNED: pointer alignment";
         case W4_ERR_CUDA: return "W4_ERR_CUDA: CUDA runtime error";
         case W4_ERR_TIMEOUT: return "W4_ERR_TIMEOUT: a bounded device wait ran out";
+        case W4_ERR_NUMERIC: return "W4_ERR_NUMERIC: a factorization failed (matrix not positive definite)";
         default: return "unknown w4 status";
     }
 }

@@ -44,6 +44,16 @@ cudaError_t launch_gemv_affine(const void* x, int64_t M, int64_t N, int64_t K, i
 cudaError_t launch_gemm_tc(const void* x, int64_t M, int64_t N, int64_t K, const void* packed,
                            const void* scales, void* y, const DeviceInfo& dev, cudaStream_t stream);
 
+// GPTQ (fp64 state): the factor U of (H + λI)⁻¹ by cuSOLVER, then per matrix
+// the own sweep kernel and cuBLAS DGEMM block updates.  Return 0, 1 on a CUDA /
+// library failure, 2 when the workspace is too small.
+size_t gptq_factor_workspace_bytes(int64_t K);
+size_t gptq_workspace_bytes(int64_t N, int64_t K);
+int launch_gptq_factor(const float* H, int64_t K, double damp, double* U, void* workspace, size_t workspace_bytes,
+                       const DeviceInfo& dev, cudaStream_t stream);
+int launch_gptq(const void* W, int64_t N, int64_t K, int group, const double* U, void* packed, void* scales,
+                void* workspace, size_t workspace_bytes, const DeviceInfo& dev, cudaStream_t stream);
+
 // Tensor-core path for the affine formats (group 32/64/128, zeros or nullptr).
 cudaError_t launch_gemm_tc_affine(const void* x, int64_t M, int64_t N, int64_t K, int group, const void* packed,
                                   const void* scales, const void* zeros, void* y, const DeviceInfo& dev,

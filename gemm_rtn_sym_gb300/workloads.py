@@ -108,6 +108,22 @@ def channel_scales(K: int, seed: int, alpha: float = AWQ_ALPHA, device="cpu") ->
     return s.to(torch.float32).to(device)
 
 
+def calibration_hessian(K: int, T: int, seed: int, device="cpu") -> torch.Tensor:
+    """fp32 [K, K] H = Xᵀ X / T of synthetic calibration inputs X [T, K] for
+    the GPTQ quantiser (the study calibrates on 128 × 1,024 tokens; none are
+    available here): seeded N(0, 1) rows mixed across channels by
+    (I + 0.3·G/√K) with G seeded N(0, 1), scaled per channel by log-normal
+    magnitudes (σ = 0.5) with 1 % of the channels ×8, and symmetrised exactly."""
+    g = _gen(seed, device)
+    Z = torch.randn((T, K), generator=g, device=device, dtype=torch.float32)
+    G = torch.randn((K, K), generator=g, device=device, dtype=torch.float32)
+    m = torch.exp(torch.randn(K, generator=g, device=device, dtype=torch.float32) * CHANNEL_LOG_STD)
+    m[outlier_channels(K, seed + 1, device)] *= OUTLIER_FACTOR
+    X = (Z @ (torch.eye(K, device=device) + 0.3 * G / K ** 0.5)) * m
+    H = X.T @ X / T
+    return (H + H.T) / 2
+
+
 def workload_channel_scales(workload: str, matrix_index: int = 0, device="cpu") -> torch.Tensor:
     """The channel scales of one matrix of a workload (K of that matrix)."""
     K = SHAPES[workload][matrix_index][1]

@@ -71,7 +71,10 @@ typedef enum w4_status {
     W4_ERR_UNSUPPORTED = 2, /* group != 128, K % 128 != 0, unsupported device    */
     W4_ERR_MISALIGNED = 3,  /* pointer alignment below what is stated above     */
     W4_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed       */
-    W4_ERR_TIMEOUT = 5      /* a bounded device-side wait ran out (see below)    */
+    W4_ERR_TIMEOUT = 5,     /* a bounded device-side wait ran out (see below)    */
+    W4_ERR_NUMERIC = 6      /* a factorization failed (w4_gptq_quantize: H + λI
+                               not positive definite); reported through
+                               w4_last_device_status                             */
 } w4_status;
 
 /* Kernel choice for w4_gemm_ex. */
@@ -202,6 +205,53 @@ int w4_gemm_ex(const void* x, int64_t M, int64_t N, int64_t K,
 int w4_gemm_affine(const void* x, int64_t M, int64_t N, int64_t K, int32_t group,
                    const void* packed, const void* scales, const void* zeros,
                    void* y, void* stream, int32_t path);
+
+/*
+ * GPTQ into the same storage as RTN (§2 settings table: GPTQ with the RTN
+ * storage, damping 0.01, columns in their original order, 128-column blocks;
+ * §2 H' = H + λI with λ = damp·mean(diag H); the method table: quantise one
+ * column, then correct the remaining weights).  The correction is the
+ * published GPTQ rule (Frantar et al., 2022): with Uᵀ U = (H')⁻¹, U upper
+ * triangular, column c's error (w_c − ŵ_c) / U[c, c] moves every later column
+ * k of the row by −err·U[c, k]; each group's scale is taken at its first
+ * column from the group's current (corrected) weights with the RTN rules:
+ * d = bf16_rne(fp32(max|w| / 7)), q = clamp(round_half_even(w / d), −8, 7).
+ * All arithmetic is fp64, so the rounding decisions match an fp64 reference.
+ * Two calls: the factor once per calibration statistic (every matrix that
+ * reads the same input shares it), then the quantisation per matrix.
+ *
+ * w4_gptq_factor — U, upper triangular with Uᵀ U = (H + λI)⁻¹:
+ *   H          in : fp32 [K, K], symmetric positive semi-definite (the
+ *                   calibration statistic, e.g. Xᵀ X over calibration inputs
+ *                   X [T, K]), 4-byte aligned
+ *   damp       in : the damping fraction (the study: 0.01), ≥ 0
+ *   U          out: fp64 [K, K] row-major, 8-byte aligned; its upper triangle
+ *                   (diagonal included) is the factor, the rest unspecified
+ *   workspace  in : w4_gptq_factor_workspace_bytes(K) bytes, 256-byte aligned
+ * cuSOLVER potrf / potri / potrf on `stream`.  A failed factorization shows as
+ * W4_ERR_NUMERIC in w4_last_device_status.
+ *
+ * w4_gptq_quantize — codes and scales of W given U:
+ *   W          in : bf16 [N, K] (not modified)
+ *   group      in : 32, 64 or 128 (columns are processed in blocks of 128)
+ *   U          in : as written by w4_gptq_factor for this W's input
+ *   packed     out: u8   [N, K/2]
+ *   scales     out: bf16 [N, K/group]
+ *   workspace  in : w4_gptq_workspace_bytes(N, K) bytes (= 8·N·K + 8·N·128,
+ *                   rounded), 256-byte aligned
+ * Block updates by cuBLAS DGEMM on `stream`.
+ *
+ * Both: N, K < 2^31; workspaces owned by the caller, overlapping nothing else,
+ * contents on return unspecified; each call holds a library lock while it
+ * enqueues work.
+ */
+size_t w4_gptq_factor_workspace_bytes(int64_t K);
+int w4_gptq_factor(const float* H, int64_t K, double damp, double* U,
+                   void* workspace, size_t workspace_bytes, void* stream);
+size_t w4_gptq_workspace_bytes(int64_t N, int64_t K);
+int w4_gptq_quantize(const void* W, int64_t N, int64_t K, int32_t group,
+                     const double* U, void* packed, void* scales,
+                     void* workspace, size_t workspace_bytes, void* stream);
 
 /* The kernel W4_PATH_AUTO picks for these sizes (W4_PATH_SMALL_M or
  * W4_PATH_TENSOR), or a negative w4_status for invalid sizes. */

@@ -64,7 +64,7 @@ def test_path_choice(lib):
 
 
 def test_status_strings(lib):
-    for s in range(6):
+    for s in range(7):
         assert lib.w4_status_string(s).decode().startswith("W4_")
     assert b"unknown" in lib.w4_status_string(99)
 
@@ -141,6 +141,31 @@ def test_quantize_scaled_needs_group_128(lib):
 ])
 def test_gemm_affine_rejects(lib, args, expect):
     assert lib.w4_gemm_affine(*args) == expect
+
+
+def test_gptq_rejects_without_gpu(lib):
+    # w4_gptq_quantize(W, N, K, group, U, packed, scales, workspace, bytes, stream)
+    assert lib.w4_gptq_quantize(A16, 4, 256, 96, A16 * 8, A16 * 2, A16 * 3, A16 * 16, 4096, None) == \
+        w4.W4_ERR_UNSUPPORTED
+    assert lib.w4_gptq_quantize(A16, 4, 200, 128, A16 * 8, A16 * 2, A16 * 3, A16 * 16, 4096, None) == \
+        w4.W4_ERR_UNSUPPORTED
+    assert lib.w4_gptq_quantize(A16, 4, 256, 128, None, A16 * 2, A16 * 3, A16 * 16, 4096, None) == \
+        w4.W4_ERR_INVALID_ARG
+    assert lib.w4_gptq_quantize(A16, 4, 256, 128, A16 * 8 + 4, A16 * 2, A16 * 3, A16 * 16, 4096, None) == \
+        w4.W4_ERR_MISALIGNED
+    assert lib.w4_gptq_quantize(A16, 4, 256, 128, A16 * 8, A16 * 2, A16 * 3, A16 * 16 + 16, 4096, None) == \
+        w4.W4_ERR_MISALIGNED
+    assert lib.w4_gptq_quantize(A16, 4, 256, 128, A16 * 8, A16 * 8 + 64, A16 * 3, A16 * 16, 4096, None) == \
+        w4.W4_ERR_INVALID_ARG  # packed inside U
+    assert lib.w4_gptq_quantize(None, 0, 256, 128, None, None, None, None, 0, None) == w4.W4_OK
+    # w4_gptq_factor(H, K, damp, U, workspace, bytes, stream)
+    assert lib.w4_gptq_factor(A16, 200, 0.01, A16 * 8, A16 * 16, 4096, None) == w4.W4_ERR_UNSUPPORTED
+    assert lib.w4_gptq_factor(A16, 256, -1.0, A16 * 8, A16 * 16, 4096, None) == w4.W4_ERR_INVALID_ARG
+    assert lib.w4_gptq_factor(A16, 256, float("nan"), A16 * 8, A16 * 16, 4096, None) == w4.W4_ERR_INVALID_ARG
+    assert lib.w4_gptq_factor(A16, 256, 0.01, A16 * 8 + 4, A16 * 16, 4096, None) == w4.W4_ERR_MISALIGNED
+    assert lib.w4_gptq_factor(A16, 256, 0.01, A16 + 1024, A16 * 16, 4096, None) == w4.W4_ERR_INVALID_ARG  # U on H
+    assert lib.w4_gptq_workspace_bytes(2560, 9216) == 2560 * 9216 * 8 + 2560 * 128 * 8
+    assert lib.w4_gptq_workspace_bytes(4, 200) == 0
 
 
 def test_quantize_empty_is_noop(lib):
