@@ -7,13 +7,15 @@
     python -m gemm_rtn_sym_gb300.profile_case grouped --workload layer27b --M 1
     python -m gemm_rtn_sym_gb300.profile_case quantize --workload outlier --group 32 --asym
     python -m gemm_rtn_sym_gb300.profile_case gemm --workload outlier --M 8 --group 32 --asym
+    python -m gemm_rtn_sym_gb300.profile_case gptq --workload ffn
 
 The inputs are the seeded synthetic matrices of ``workloads``.  For ``gemm`` the
 weights are quantised first (one quantiser launch), then the matmul runs
 ``--launches`` times on the same inputs.  ``grouped`` quantises every matrix
 of the workload and runs one grouped plan over all of them.  ``--group`` and
 ``--asym`` select the affine formats (w4_quantize_rtn / w4_quantize_rtn_asym at
-that group size, w4_gemm_affine).  The case checks the device status
+that group size, w4_gemm_affine).  ``gptq`` factors a seeded synthetic
+calibration statistic once and runs the GPTQ quantiser ``--launches`` times.  The case checks the device status
 word at the end and exits non-zero if any wait timed out.  It times nothing:
 numbers taken under a profiler are not benchmark results.
 """
@@ -26,7 +28,7 @@ import torch
 
 from . import W4_PATH_AUTO, W4_PATH_SMALL_M, W4_PATH_TENSOR
 from . import load, w4_gemm_ex, w4_gemm_grouped, w4_grouped_plan, w4_last_device_status, w4_quantize_rtn
-from . import w4_gemm_affine, w4_quantize_rtn_asym, w4_quantize_rtn_scaled
+from . import w4_gemm_affine, w4_gptq_factor, w4_gptq_quantize, w4_quantize_rtn_asym, w4_quantize_rtn_scaled
 from . import workloads as wl
 
 PATHS = {"auto": W4_PATH_AUTO, "small": W4_PATH_SMALL_M, "tensor": W4_PATH_TENSOR}
@@ -34,7 +36,7 @@ PATHS = {"auto": W4_PATH_AUTO, "small": W4_PATH_SMALL_M, "tensor": W4_PATH_TENSO
 
 def main(argv=None) -> int:
     p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
-    p.add_argument("kernel", choices=["quantize", "quantize_scaled", "gemm", "grouped"])
+    p.add_argument("kernel", choices=["quantize", "quantize_scaled", "gemm", "grouped", "gptq"])
     p.add_argument("--workload", default="outlier", choices=sorted(wl.SHAPES))
     p.add_argument("--matrix", type=int, default=0, help="index into the workload's matrices")
     p.add_argument("--M", type=int, default=8, help="token rows of x (gemm)")
@@ -80,6 +82,12 @@ def main(argv=None) -> int:
         for _ in range(a.launches):
             quantize()
         what = f"quantize {a.workload}[{a.matrix}] {N}x{K}{fmt}"
+    elif a.kernel == "gptq":
+        H = wl.calibration_hessian(K, 4096, seed=wl.seed_for(a.workload, a.matrix, 4), device=dev)
+        U = w4_gptq_factor(H)
+        for _ in range(a.launches):
+            w4_gptq_quantize(W, U, a.group, packed=packed, scales=scales)
+        what = f"gptq {a.workload}[{a.matrix}] {N}x{K} g{a.group}"
     elif a.kernel == "quantize_scaled":
         s = wl.workload_channel_scales(a.workload, a.matrix, device=dev)
         for _ in range(a.launches):
