@@ -267,18 +267,28 @@ gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_cons
         }
     }
     if (split > 1) {
-        // Split-K partials: rank 0 of the cluster sums them in rank order.
+        // Split-K partials, summed in rank order.  Every rank of the cluster
+        // takes a slice of the outputs and reads that slice from all ranks
+        // through DSMEM, issuing all of an element's remote loads before the
+        // first add, so the reduction costs about one DSMEM round trip instead
+        // of one per rank and element.
         cluster_sync();
-        if (rank == 0) {
-            const uint32_t part_addr = smem_addr(part);
-            for (int e = threadIdx.x; e < kRowsCta * M; e += kThreads) {
-                const int rowc = e % kRowsCta, m = e / kRowsCta;
-                const int64_t n = n0 + rowc;
-                float v = 0.0f;
-                for (int r = 0; r < split; ++r)
-                    v += ld_cluster_f32(part_addr + static_cast<uint32_t>((m * kRowsCta + rowc) * 4), static_cast<uint32_t>(r));
-                if (n < args.N) args.y[static_cast<int64_t>(m) * args.N + n] = __float2bfloat16_rn(v);
-            }
+        const uint32_t part_addr = smem_addr(part);
+        const int total = kRowsCta * M;
+        const int per = (total + split - 1) / split;
+        const int e_end = min(total, static_cast<int>(rank + 1) * per);
+        for (int e = static_cast<int>(rank) * per + threadIdx.x; e < e_end; e += kThreads) {
+            const int rowc = e % kRowsCta, m = e / kRowsCta;
+            const int64_t n = n0 + rowc;
+            const uint32_t a = part_addr + static_cast<uint32_t>((m * kRowsCta + rowc) * 4);
+            float p[kMaxSplit];
+#pragma unroll
+            for (int r = 0; r < kMaxSplit; ++r) p[r] = r < split ? ld_cluster_f32(a, static_cast<uint32_t>(r)) : 0.0f;
+            float v = 0.0f;
+#pragma unroll
+            for (int r = 0; r < kMaxSplit; ++r)
+                if (r < split) v += p[r];
+            if (n < args.N) args.y[static_cast<int64_t>(m) * args.N + n] = __float2bfloat16_rn(v);
         }
         cluster_sync();
     }
