@@ -480,7 +480,7 @@ def gptq_set(torch, w4, wl, workload, pk, T=4096, reps=3):
     t_f = T_.time(lambda: w4.w4_gptq_factor(H, U=U, workspace=fws), reps=reps)
     t_q = T_.time(lambda: w4.w4_gptq_quantize(W, U, packed=packed, scales=scales, workspace=qws), reps=reps)
     assert w4.w4_last_device_status() == 0
-    f_f = 4.0 / 3.0 * K ** 3
+    f_f = 2.0 / 3.0 * K ** 3  # potrf K³/3 + trtri K³/3
     f_q = 2.0 * N * 128 * sum(K - i2 for i2 in range(128, K, 128)) + N * K * 128
     del W, H, U, fws, qws, packed, scales
     torch.cuda.empty_cache()

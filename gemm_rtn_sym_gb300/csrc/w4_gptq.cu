@@ -14,10 +14,14 @@
 // few codes per matrix, each flip then changing the rest of its row).
 //
 // Factor (once per calibration statistic H, shared by every matrix that reads
-// the same input):
-//  1. λ and H' = fp64(H) + λI (own kernels);
-//  2. (H')⁻¹ and its Cholesky factor by cuSOLVER (potrf, potri, potrf): plain
-//     library linear algebra, about (4/3)·K³ flops.
+// the same input).  With J the order-reversing permutation, the Cholesky
+// factor L̃ of J H' J gives H' = Ũ Ũᵀ with Ũ = J L̃ J upper triangular, so
+// U = Ũ⁻¹ = J L̃⁻¹ J is upper triangular with Uᵀ U = (H')⁻¹: one Cholesky and
+// one triangular inverse, (2/3)·K³ flops, instead of inverting H' and
+// factoring the inverse.
+//  1. λ, and J H' J = J (fp64(H) + λI) J written reversed (own kernels);
+//  2. potrf and trtri by cuSOLVER (plain library linear algebra);
+//  3. the reversal and transposition back to row-major U in place (own kernel).
 // Quantise (per matrix):
 //  3. W widened to fp64 (own kernel);
 //  4. per 128-column block: the sweep kernel (own) rounds the block's columns
@@ -46,17 +50,17 @@ constexpr unsigned kStatusNumeric = 6;   // W4_ERR_NUMERIC
 
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
-// Factor workspace: λ, cuSOLVER's info word and work space.
+// Factor workspace: λ, cuSOLVER's info word and device work space.
 struct FactorLayout {
     size_t lam, info, work, total;
 };
 
-FactorLayout factor_layout(int64_t lwork) {
+FactorLayout factor_layout(size_t work_bytes) {
     FactorLayout l;
     l.lam = 0;
     l.info = 256;
     l.work = 512;
-    l.total = align256(l.work + static_cast<size_t>(lwork) * 8);
+    l.total = align256(l.work + work_bytes);
     return l;
 }
 
@@ -88,15 +92,33 @@ __global__ void __launch_bounds__(256) diag_mean_kernel(const float* __restrict_
     if (threadIdx.x == 0) *lam = damp * part[0] / static_cast<double>(K);
 }
 
-// A = fp64(H) + λ I.
-__global__ void damp_kernel(const float* __restrict__ H, int64_t K, const double* __restrict__ lam,
-                            double* __restrict__ A) {
+// A = J (fp64(H) + λ I) J: element p of A is element K² − 1 − p of H'.
+__global__ void damp_reversed_kernel(const float* __restrict__ H, int64_t K, const double* __restrict__ lam,
+                                     double* __restrict__ A) {
     const double l = *lam;
     const int64_t n = K * K;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t r = i / K, c = i - r * K;
-        A[i] = static_cast<double>(H[i]) + (r == c ? l : 0.0);
+        A[i] = static_cast<double>(H[n - 1 - i]) + (r == c ? l : 0.0);
+    }
+}
+
+// The column-major lower triangle of A holds L̃⁻¹ (L̃⁻¹[i][j] at i + j·K).
+// Row-major U[r][c] = L̃⁻¹[K−1−r][K−1−c] sits at K² − 1 − (r + c·K): the map
+// p = r·K + c -> q = K² − 1 − (r + c·K) is an involution, so swapping each pair
+// once turns A into U in place.
+__global__ void reverse_transpose_kernel(double* __restrict__ A, int64_t K) {
+    const int64_t n = K * K;
+    for (int64_t p = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; p < n;
+         p += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = p / K, c = p - r * K;
+        const int64_t q = n - 1 - (r + c * K);
+        if (p < q) {
+            const double t = A[p];
+            A[p] = A[q];
+            A[q] = t;
+        }
     }
 }
 
@@ -209,14 +231,19 @@ Handles* handles() {
     return &h;
 }
 
-// Doubles of cuSOLVER work space for potrf and potri at order K.
-bool solver_lwork(Handles* h, int64_t K, int* lwork) {
-    int a = 0, b = 0;
+// Device bytes of cuSOLVER work space for potrf and trtri at order K (trtri
+// must need no host work space, which this library does not keep).
+bool solver_work_bytes(Handles* h, int64_t K, size_t* bytes) {
+    int a = 0;
+    size_t dev_b = 0, host_b = 0;
     const int n = static_cast<int>(K);
     if (cusolverDnDpotrf_bufferSize(h->solver, CUBLAS_FILL_MODE_LOWER, n, nullptr, n, &a) != CUSOLVER_STATUS_SUCCESS ||
-        cusolverDnDpotri_bufferSize(h->solver, CUBLAS_FILL_MODE_LOWER, n, nullptr, n, &b) != CUSOLVER_STATUS_SUCCESS)
+        cusolverDnXtrtri_bufferSize(h->solver, CUBLAS_FILL_MODE_LOWER, CUBLAS_DIAG_NON_UNIT, K, CUDA_R_64F, nullptr,
+                                    K, &dev_b, &host_b) != CUSOLVER_STATUS_SUCCESS ||
+        host_b != 0)
         return false;
-    *lwork = a > b ? a : b;
+    const size_t pa = static_cast<size_t>(a) * 8;
+    *bytes = pa > dev_b ? pa : dev_b;
     return true;
 }
 
@@ -232,9 +259,9 @@ int grid_for(int64_t n, const DeviceInfo& dev) {
 size_t gptq_factor_workspace_bytes(int64_t K) {
     std::lock_guard<std::mutex> lock(g_la_mutex);
     Handles* h = handles();
-    int lwork = 0;
-    if (!h || !solver_lwork(h, K, &lwork)) return 0;
-    return factor_layout(lwork).total;
+    size_t work = 0;
+    if (!h || !solver_work_bytes(h, K, &work)) return 0;
+    return factor_layout(work).total;
 }
 
 size_t gptq_workspace_bytes(int64_t N, int64_t K) { return quant_layout(N, K).total; }
@@ -243,32 +270,29 @@ int launch_gptq_factor(const float* H, int64_t K, double damp, double* A, void* 
                        const DeviceInfo& dev, cudaStream_t stream) {
     std::lock_guard<std::mutex> lock(g_la_mutex);
     Handles* h = handles();
-    int lwork = 0;
-    if (!h || !solver_lwork(h, K, &lwork)) return 1;
-    const FactorLayout l = factor_layout(lwork);
+    size_t work_bytes = 0;
+    if (!h || !solver_work_bytes(h, K, &work_bytes)) return 1;
+    const FactorLayout l = factor_layout(work_bytes);
     if (workspace_bytes < l.total) return 2;
     auto* base = static_cast<uint8_t*>(workspace);
     double* lam = reinterpret_cast<double*>(base + l.lam);
     int* info = reinterpret_cast<int*>(base + l.info);
     double* work = reinterpret_cast<double*>(base + l.work);
     const int n = static_cast<int>(K);
+    const int lwork = static_cast<int>(work_bytes / 8);
     if (cusolverDnSetStream(h->solver, stream) != CUSOLVER_STATUS_SUCCESS) return 1;
     diag_mean_kernel<<<1, 256, 0, stream>>>(H, K, damp, lam);
-    damp_kernel<<<grid_for(K * K, dev), 256, 0, stream>>>(H, K, lam, A);
-    // Column-major LOWER on a symmetric matrix: the factor L (H' = L Lᵀ) fills
-    // the lower triangle; potri then writes the lower triangle of (H')⁻¹, and
-    // the second potrf its factor L2 ((H')⁻¹ = L2 L2ᵀ).  Read row-major, the
-    // buffer's upper triangle is U = L2ᵀ, with Uᵀ U = (H')⁻¹: the only part
-    // the sweep and the block update read.
+    damp_reversed_kernel<<<grid_for(K * K, dev), 256, 0, stream>>>(H, K, lam, A);
+    // Column-major LOWER (the matrix is symmetric): L̃ with J H' J = L̃ L̃ᵀ
+    // fills the lower triangle, then its inverse replaces it.
     if (cusolverDnDpotrf(h->solver, CUBLAS_FILL_MODE_LOWER, n, A, n, work, lwork, info) != CUSOLVER_STATUS_SUCCESS)
         return 1;
     check_info_kernel<<<1, 1, 0, stream>>>(info, dev.status);
-    if (cusolverDnDpotri(h->solver, CUBLAS_FILL_MODE_LOWER, n, A, n, work, lwork, info) != CUSOLVER_STATUS_SUCCESS)
+    if (cusolverDnXtrtri(h->solver, CUBLAS_FILL_MODE_LOWER, CUBLAS_DIAG_NON_UNIT, K, CUDA_R_64F, A, K, work,
+                         work_bytes, nullptr, 0, info) != CUSOLVER_STATUS_SUCCESS)
         return 1;
     check_info_kernel<<<1, 1, 0, stream>>>(info, dev.status);
-    if (cusolverDnDpotrf(h->solver, CUBLAS_FILL_MODE_LOWER, n, A, n, work, lwork, info) != CUSOLVER_STATUS_SUCCESS)
-        return 1;
-    check_info_kernel<<<1, 1, 0, stream>>>(info, dev.status);
+    reverse_transpose_kernel<<<grid_for(K * K, dev), 256, 0, stream>>>(A, K);
     return cudaGetLastError() == cudaSuccess ? 0 : 1;
 }
 

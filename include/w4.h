@@ -228,8 +228,10 @@ int w4_gemm_affine(const void* x, int64_t M, int64_t N, int64_t K, int32_t group
  *   U          out: fp64 [K, K] row-major, 8-byte aligned; its upper triangle
  *                   (diagonal included) is the factor, the rest unspecified
  *   workspace  in : w4_gptq_factor_workspace_bytes(K) bytes, 256-byte aligned
- * cuSOLVER potrf / potri / potrf on `stream`.  A failed factorization shows as
- * W4_ERR_NUMERIC in w4_last_device_status.
+ * Computed as U = J L̃⁻¹ J with L̃ the Cholesky factor of J (H + λI) J (J the
+ * order-reversing permutation): cuSOLVER potrf and trtri on `stream`, (2/3)·K³
+ * flops.  A failed factorization shows as W4_ERR_NUMERIC in
+ * w4_last_device_status.
  *
  * w4_gptq_quantize — codes and scales of W given U:
  *   W          in : bf16 [N, K] (not modified)
