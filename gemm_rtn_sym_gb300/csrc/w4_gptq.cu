@@ -25,7 +25,7 @@
 // Quantise (per matrix):
 //  3. W widened to fp64 (own kernel);
 //  4. per 128-column block: the sweep kernel (own) rounds the block's columns
-//     one after another, each thread carrying one row through the block in
+//     one after another, eight threads carrying each row through the block in
 //     shared memory, writes the block's codes, scales and errors E; then the
 //     later columns get W[:, i2:] −= E·U[i1:i2, i2:] by cuBLAS DGEMM, which
 //     carries N·K² flops in total and bounds the call on GB300's fp64 rate.
@@ -43,8 +43,12 @@ namespace w4 {
 namespace {
 
 constexpr int kBlock = 128;              // columns per computation block
-constexpr int kSweepRows = 64;           // rows per CTA, one per thread
-constexpr int kPitch = kSweepRows + 1;   // doubles per shared-memory column (bank spread)
+constexpr int kSweepRows = 16;           // rows per CTA
+constexpr int kRowThreads = 8;           // threads per row (each owns 16 of the block's columns)
+constexpr int kSweepThreads = kSweepRows * kRowThreads;
+// Doubles per shared-memory column: ≡ 2 (mod 16), so the 16 lanes of a half
+// warp (two rows × eight column residues) hit distinct bank pairs.
+constexpr int kPitch = kSweepRows + 2;
 constexpr int kSweepSmem = kBlock * kPitch * 8 + kBlock * kSweepRows;
 constexpr unsigned kStatusNumeric = 6;   // W4_ERR_NUMERIC
 
@@ -132,20 +136,26 @@ __global__ void check_info_kernel(const int* __restrict__ info, unsigned* status
     if (*info != 0) record_status(status, kStatusNumeric);
 }
 
-// One 128-column block [i1, i1 + 128) for kSweepRows rows.  Thread r carries
-// row n0 + r: its block of W (fp64, current) sits in shared memory column-major
-// (W1s[k][r]) so that a fixed k is one contiguous row of 64 doubles.
-__global__ void __launch_bounds__(kSweepRows)
+// One 128-column block [i1, i1 + 128) for kSweepRows rows.  Each row has
+// kRowThreads threads: thread t of a row owns the block's columns k ≡ t (mod
+// kRowThreads).  The block sits in shared memory column-major (W1s[k][r],
+// pitch kPitch) so that one k is a contiguous run of rows.  Per column j all
+// threads of the row read w_j from shared memory (after a warp barrier, since
+// its owner updated it in the previous step), take the same rounding decision
+// and error, and each applies the correction to its own later columns.
+__global__ void __launch_bounds__(kSweepThreads)
 gptq_sweep_kernel(const double* __restrict__ Wd, const double* __restrict__ U, int64_t N, int64_t K, int64_t i1,
                   int group, uint8_t* __restrict__ packed, uint16_t* __restrict__ scales, double* __restrict__ E) {
     extern __shared__ double smem_d[];
     double* W1s = smem_d;                                                     // [kBlock][kPitch]
     int8_t* Qs = reinterpret_cast<int8_t*>(smem_d + kBlock * kPitch);         // [kBlock][kSweepRows]
-    const int r = threadIdx.x;
+    const int tid = threadIdx.x;
+    const int r = tid / kRowThreads;  // row within the CTA
+    const int t = tid % kRowThreads;  // column residue owned by this thread
     const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kSweepRows;
     const int64_t n = n0 + r;
 
-    for (int idx = r; idx < kSweepRows * kBlock; idx += kSweepRows) {
+    for (int idx = tid; idx < kSweepRows * kBlock; idx += kSweepThreads) {
         const int rr = idx / kBlock, k = idx % kBlock;
         const int64_t row = n0 + rr;
         W1s[k * kPitch + rr] = row < N ? Wd[row * K + i1 + k] : 0.0;
@@ -156,47 +166,54 @@ gptq_sweep_kernel(const double* __restrict__ Wd, const double* __restrict__ U, i
     const int64_t row_groups = K / group;
     double d = 0.0;
     for (int j = 0; j < kBlock; ++j) {
+        __syncwarp();
         if (j % group == 0) {
-            // The group's current weights: every later column of the block
-            // already carries the corrections of the columns before j.
+            // The group's current weights (every later column of the block
+            // already carries the corrections of the columns before j): max
+            // over this thread's columns of the group, then over the row.
             double a = 0.0;
-            for (int k = j; k < j + group; ++k) a = fmax(a, fabs(W1s[k * kPitch + r]));
+            for (int k = j + t; k < j + group; k += kRowThreads) a = fmax(a, fabs(W1s[k * kPitch + r]));
+#pragma unroll
+            for (int m = 1; m < kRowThreads; m <<= 1) a = fmax(a, __shfl_xor_sync(0xffffffffu, a, m));
             const __nv_bfloat16 d16 = __float2bfloat16_rn(__double2float_rn(a / 7.0));
             d = static_cast<double>(__bfloat162float(d16));
-            if (n < N) scales[n * row_groups + (i1 + j) / group] = *reinterpret_cast<const uint16_t*>(&d16);
+            if (n < N && t == 0) scales[n * row_groups + (i1 + j) / group] = *reinterpret_cast<const uint16_t*>(&d16);
         }
         const double wj = W1s[j * kPitch + r];
         const double q = d != 0.0 ? fmin(fmax(rint(wj / d), -8.0), 7.0) : 0.0;
-        Qs[j * kSweepRows + r] = static_cast<int8_t>(q);
         const double err = (wj - d * q) / __ldg(Ub + static_cast<int64_t>(j) * K + j);
-        W1s[j * kPitch + r] = err;  // column j is done: keep its error for the block update
         const double* urow = Ub + static_cast<int64_t>(j) * K;
-        for (int k = j + 1; k < kBlock; ++k) W1s[k * kPitch + r] = fma(-err, __ldg(urow + k), W1s[k * kPitch + r]);
+        // This thread's columns after j: k = j + 1 + ((t − j − 1) mod kRowThreads) + kRowThreads·i.
+        const int k0 = j + 1 + ((t - j - 1) & (kRowThreads - 1));
+#pragma unroll 4
+        for (int k = k0; k < kBlock; k += kRowThreads) W1s[k * kPitch + r] = fma(-err, __ldg(urow + k), W1s[k * kPitch + r]);
+        __syncwarp();  // every thread of the row has read w_j before its owner overwrites it
+        if (t == (j & (kRowThreads - 1))) {
+            Qs[j * kSweepRows + r] = static_cast<int8_t>(q);
+            W1s[j * kPitch + r] = err;  // column j is done: keep its error for the block update
+        }
     }
     __syncthreads();
 
     // Errors for the later blocks, row-major [N, kBlock].
-    for (int idx = r; idx < kSweepRows * kBlock; idx += kSweepRows) {
+    for (int idx = tid; idx < kSweepRows * kBlock; idx += kSweepThreads) {
         const int rr = idx / kBlock, k = idx % kBlock;
         const int64_t row = n0 + rr;
         if (row < N) E[row * kBlock + k] = W1s[k * kPitch + rr];
     }
-    // Codes of this row's block in the stored nibble order: chunk k/32, word
-    // (k mod 32)/8, slot i with offset {0,2,4,6,1,3,5,7}[i] = k mod 8.
-    if (n < N) {
-        uint32_t words[16];
+    // Codes in the stored nibble order: chunk c (k = 32c .. 32c + 31) of the
+    // block, word (k mod 32)/8, slot i with offset {0,2,4,6,1,3,5,7}[i] = k mod 8.
+    // Threads t < 4 of a row write chunk t as one 16-byte store.
+    if (n < N && t < 4) {
+        uint32_t words[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-        for (int w = 0; w < 16; ++w) words[w] = 0u;
-#pragma unroll
-        for (int k = 0; k < kBlock; ++k) {
-            const int e = k % 8;
+        for (int kk = 0; kk < 32; ++kk) {
+            const int e = kk % 8;
             const int slot = (e % 2 == 0) ? e / 2 : 4 + e / 2;
-            const uint32_t nib = static_cast<uint32_t>(Qs[k * kSweepRows + r]) & 0xFu;
-            words[(k / 32) * 4 + (k % 32) / 8] |= nib << (4 * slot);
+            const uint32_t nib = static_cast<uint32_t>(Qs[(32 * t + kk) * kSweepRows + r]) & 0xFu;
+            words[kk / 8] |= nib << (4 * slot);
         }
-        uint4* dst = reinterpret_cast<uint4*>(packed + n * (K / 2) + i1 / 2);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) dst[c] = make_uint4(words[4 * c], words[4 * c + 1], words[4 * c + 2], words[4 * c + 3]);
+        reinterpret_cast<uint4*>(packed + n * (K / 2) + i1 / 2)[t] = make_uint4(words[0], words[1], words[2], words[3]);
     }
 }
 
@@ -313,7 +330,7 @@ int launch_gptq(const void* W, int64_t N, int64_t K, int group, const double* U,
     const unsigned sweep_grid = static_cast<unsigned>((N + kSweepRows - 1) / kSweepRows);
     for (int64_t i1 = 0; i1 < K; i1 += kBlock) {
         const int64_t i2 = i1 + kBlock;
-        gptq_sweep_kernel<<<sweep_grid, kSweepRows, kSweepSmem, stream>>>(
+        gptq_sweep_kernel<<<sweep_grid, kSweepThreads, kSweepSmem, stream>>>(
             Wd, U, N, K, i1, group, static_cast<uint8_t*>(packed), static_cast<uint16_t*>(scales), E);
         if (cudaGetLastError() != cudaSuccess) return 1;
         if (i2 < K) {
