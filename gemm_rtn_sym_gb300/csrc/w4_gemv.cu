@@ -15,8 +15,9 @@
 //    tiles, so the activation fragments are loaded once per group and reused
 //    for 64 rows; the warps' fp32 partials are summed in shared memory in a
 //    fixed order at the end.  Small matrices are split along K over the CTAs
-//    of a thread-block cluster, whose partials rank 0 adds through
-//    distributed shared memory in rank order: deterministic, no global scratch.
+//    of a thread-block cluster; each rank then adds one slice of the outputs
+//    over all ranks' partials through distributed shared memory, in rank
+//    order: deterministic, no global scratch.
 //  * The stored nibble order makes every 32-bit word yield four bf16x2 pairs
 //    (136 + q) with one shift and one LOP3 each, with no shuffles; the
 //    136·Σx offset is removed by starting each group's accumulator at −136·Σx,
