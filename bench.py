@@ -229,7 +229,9 @@ def headline(torch, w4, wl, steps, warmup, pk):
         while time.time() < t_end:  # untimed soak so the clock record spans the load
             g_all.replay()
         torch.cuda.synchronize()
+        rank_barrier()
         t_step = T.time(g_all.replay) / steps
+        rank_barrier()
     t_q = T.time(g_q.replay) / steps
     t_g = T.time(g_g.replay) / steps
     torch.cuda.synchronize()
@@ -570,6 +572,35 @@ def config_block(extra=None):
     return c
 
 
+def rank_barrier() -> None:
+    """Barrier over all ranks when a process group is up (brackets the timed
+    region, with a device synchronize on both sides)."""
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.barrier()
+
+
+def max_over_ranks(t_local: float, device="cpu") -> float:
+    """The job's step time: the largest per-rank time (all-reduce MAX, then a
+    barrier).  With no process group, or one rank, the local time."""
+    import torch
+    import torch.distributed as dist
+
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return t_local
+    t = torch.tensor([t_local], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return float(t.item())
+
+
+def job_value(bytes_per_rank_step: float, world: int, t_step: float) -> float:
+    """Whole-job GB/s: every rank processes its own copy of the step's work
+    (replicas, weak scaling), timed by the slowest rank."""
+    return world * bytes_per_rank_step / t_step / 1e9
+
+
 def run_gpu(args):
     import torch
     import gemm_rtn_sym_gb300 as w4
@@ -585,16 +616,10 @@ def run_gpu(args):
     w4.load()
     pk = peaks()
     res = headline(torch, w4, wl, args.steps, args.warmup, pk)
-    t_step = res["ms_per_step"] / 1e3
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([t_step], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_step = float(t.item())
-        dist.barrier()
+    t_step = max_over_ranks(res["ms_per_step"] / 1e3, device="cuda")
     N, K = wl.SHAPES[HEADLINE][0]
     bytes_step = quant_bytes(N, K) + gemm_bytes(HEADLINE_M, N, K)
-    value = world * bytes_step / t_step / 1e9
+    value = job_value(bytes_step, world, t_step)
 
     sub = {}
     if not args.no_sub and rank == 0:
