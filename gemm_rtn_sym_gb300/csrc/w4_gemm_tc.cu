@@ -286,18 +286,30 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             const int cmid = (bm >> 5) << 4;
             const int cbeg = half == 0 ? 0 : cmid;
             const int cend = half == 0 ? cmid : bm;
-            for (int c0 = cbeg; c0 < cend; c0 += 16) {
-                uint32_t v[16];
-                tmem_ld16(lane_base + static_cast<uint32_t>(c0), v);
-                if (split > 1) {
+            // Up to four 16-column loads in flight per wait (the column range
+            // is a multiple of 16).
+            for (int c0 = cbeg; c0 < cend; c0 += 64) {
+                const int nq = min(4, (cend - c0) >> 4);  // warp-uniform
+                uint32_t v[4][16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) red[(c0 + j) * kBN + t] = __uint_as_float(v[j]);
-                } else if (ny < args.N) {
+                for (int q = 0; q < 4; ++q)
+                    if (q < nq) tmem_ld16_async(lane_base + static_cast<uint32_t>(c0 + 16 * q), v[q]);
+                tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int64_t m = m0 + c0 + j;
-                        if (m < args.M)
-                            args.y[m * args.N + ny] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                for (int q = 0; q < 4; ++q) {
+                    if (q >= nq) continue;
+                    reg_fence16(v[q]);
+                    const int cq = c0 + 16 * q;
+                    if (split > 1) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) red[(cq + j) * kBN + t] = __uint_as_float(v[q][j]);
+                    } else if (ny < args.N) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int64_t m = m0 + cq + j;
+                            if (m < args.M)
+                                args.y[m * args.N + ny] = __float2bfloat16_rn(__uint_as_float(v[q][j]));
+                        }
                     }
                 }
             }
@@ -319,9 +331,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             const int c = e / rows;
             const int64_t ny = n0 + rowt;
             const int64_t m = m0 + c;
+            // All of the element's remote loads are issued before the first add.
+            const uint32_t a = red_addr + static_cast<uint32_t>((c * kBN + rowt) * 4);
+            float p[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) p[r] = r < split ? ld_cluster_f32(a, static_cast<uint32_t>(r)) : 0.0f;
             float v = 0.0f;
-            for (int r = 0; r < split; ++r)
-                v += ld_cluster_f32(red_addr + static_cast<uint32_t>((c * kBN + rowt) * 4), static_cast<uint32_t>(r));
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+                if (r < split) v += p[r];
             if (ny < args.N && m < args.M) args.y[m * args.N + ny] = __float2bfloat16_rn(v);
         }
         cluster_sync();

@@ -178,6 +178,7 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
         const int G = pr->G;
         const int64_t N = pr->N;
         const int M = pr->M;
+        __nv_bfloat16* const y = pr->y;  // read once: stores to y could alias the record
         const int64_t row0 = static_cast<int64_t>(it.y) * kRowsCta;
         // Scale rows gid / gid+8 of each tile (clamped: rows past N have zero codes).
         const uint16_t* srow[TPW][2];
@@ -259,7 +260,7 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
                 for (int w = 0; w < kStageGroups; ++w) v += red[((w * kTiles + rt) * 4 + r) * 32 + l];
                 const int m = mt * 8 + 2 * (l & 3) + (r & 1);
                 const int64_t n = row0 + rt * 16 + (l >> 2) + (r >= 2 ? 8 : 0);
-                if (!aborted && n < N && m < M) pr->y[static_cast<int64_t>(m) * N + n] = __float2bfloat16_rn(v);
+                if (!aborted && n < N && m < M) y[static_cast<int64_t>(m) * N + n] = __float2bfloat16_rn(v);
             }
         }
     }

@@ -320,18 +320,34 @@ gemm_tc_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
                 continue;  // skip the rest; every wait from here on is skipped too
             }
             tc_fence_after();
+            // The problem's fields are read once: the stores to y below could
+            // alias the problem record for the compiler, which would otherwise
+            // reload them after every store.
+            const int64_t N = pr->N, M = pr->M;
+            __nv_bfloat16* const y = pr->y;
             const int64_t ny = n0 + t;
             const int cmid = (bm >> 5) << 4;  // the two warps of a lane quarter split the columns
             const int cbeg = half == 0 ? 0 : cmid;
             const int cend = half == 0 ? cmid : bm;
-            for (int c0 = cbeg; c0 < cend; c0 += 16) {
-                uint32_t v[16];
-                tmem_ld16(lane_base + static_cast<uint32_t>(c0), v);
-                if (ny < pr->N) {
+            // Up to four 16-column loads in flight per wait (the column range
+            // is a multiple of 16).
+            for (int c0 = cbeg; c0 < cend; c0 += 64) {
+                const int nq = min(4, (cend - c0) >> 4);  // warp-uniform
+                uint32_t v[4][16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int64_t m = m0 + c0 + j;
-                        if (m < pr->M) pr->y[m * pr->N + ny] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                for (int q = 0; q < 4; ++q)
+                    if (q < nq) tmem_ld16_async(lane_base + static_cast<uint32_t>(c0 + 16 * q), v[q]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (q >= nq) continue;
+                    reg_fence16(v[q]);
+                    if (ny < N) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int64_t m = m0 + c0 + 16 * q + j;
+                            if (m < M) y[m * N + ny] = __float2bfloat16_rn(__uint_as_float(v[q][j]));
+                        }
                     }
                 }
             }
