@@ -222,31 +222,60 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
         // (d, 136 + z') of the two 32-k chunks this thread dequantises in k
         // stage kb, as bf16x2: {d2 of chunk 2·half, of chunk 2·half + 1,
         // off2 of the first, of the second}.
+        // With groups of 32 the thread's two chunks have adjacent groups (ia,
+        // ia + 1, ia even): their scales are one 32-bit load and their zeros
+        // one 16-bit load when the buffers are aligned for it (rows of K/32
+        // entries keep that alignment).
+        const bool pair_s = QG == 32 && (reinterpret_cast<uintptr_t>(srow) & 3u) == 0;
+        const bool pair_z = QG == 32 && zrow && (reinterpret_cast<uintptr_t>(zrow) & 1u) == 0;
         auto load_dz = [&](int kb, uint32_t (&o)[4]) {
             const int64_t gk = kb_lo + kb;
-            int64_t ia = gk, ib = gk;
-            if (QG == 64) ia = ib = 2 * gk + half;
-            if (QG == 32) ia = 4 * gk + 2 * half, ib = ia + 1;
-            const uint32_t da = __ldg(srow + ia), db = QG == 32 ? __ldg(srow + ib) : da;
-            const uint32_t za = zrow ? static_cast<uint32_t>(0x4308 + __ldg(zrow + ia)) : 0x4308u;
-            const uint32_t zb = zrow && QG == 32 ? static_cast<uint32_t>(0x4308 + __ldg(zrow + ib)) : za;
+            int64_t ia = gk;
+            if (QG == 64) ia = 2 * gk + half;
+            if (QG == 32) ia = 4 * gk + 2 * half;
+            uint32_t da, db;
+            if (QG == 32 && pair_s) {
+                const uint32_t w = __ldg(reinterpret_cast<const unsigned int*>(srow + ia));
+                da = w & 0xFFFFu;
+                db = w >> 16;
+            } else {
+                da = __ldg(srow + ia);
+                db = QG == 32 ? __ldg(srow + ia + 1) : da;
+            }
+            int za = 0, zb = 0;
+            if (zrow) {
+                if (QG == 32 && pair_z) {
+                    const unsigned short w = __ldg(reinterpret_cast<const unsigned short*>(zrow + ia));
+                    za = static_cast<int8_t>(w & 0xFFu);
+                    zb = static_cast<int8_t>(w >> 8);
+                } else {
+                    za = __ldg(zrow + ia);
+                    zb = QG == 32 ? __ldg(zrow + ia + 1) : za;
+                }
+            }
+            const uint32_t oa = static_cast<uint32_t>(0x4308 + za), ob = static_cast<uint32_t>(0x4308 + zb);
             o[0] = da | (da << 16);
             o[1] = db | (db << 16);
-            o[2] = za | (za << 16);
-            o[3] = zb | (zb << 16);
+            o[2] = oa | (oa << 16);
+            o[3] = ob | (ob << 16);
         };
         // Row t of a code stage: 64 bytes per group, 16-byte chunk c at c ^ ((t >> 1) & 3).
         const uint32_t row_off = static_cast<uint32_t>(t * 64);
         const uint32_t sw = static_cast<uint32_t>((t >> 1) & 3);
-        uint32_t dz_next[4] = {0u, 0u, 0x43084308u, 0x43084308u};
-        if (nkb > 0) load_dz(0, dz_next);
+        // Scales and zeros are fetched two k stages ahead.
+        uint32_t dz1[4] = {0u, 0u, 0x43084308u, 0x43084308u};
+        uint32_t dz2[4] = {0u, 0u, 0x43084308u, 0x43084308u};
+        if (nkb > 0) load_dz(0, dz1);
+        if (nkb > 1) load_dz(1, dz2);
         for (int kb = 0; kb < nkb && ok; ++kb) {
             const int s = kb % kStages;
             const uint32_t r = static_cast<uint32_t>(kb / kStages);
             const int cst = (kb >> 1) % kCodeStages;
             const int sub = kb & 1;  // group within the code stage
-            const uint32_t dz[4] = {dz_next[0], dz_next[1], dz_next[2], dz_next[3]};
-            if (kb + 1 < nkb) load_dz(kb + 1, dz_next);
+            const uint32_t dz[4] = {dz1[0], dz1[1], dz1[2], dz1[3]};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dz1[i] = dz2[i];
+            if (kb + 2 < nkb) load_dz(kb + 2, dz2);
             const bool have = mbar_wait(code_full(cst), static_cast<uint32_t>((kb >> 1) / kCodeStages) & 1u);
             if (!__all_sync(0xffffffffu, have)) { ok = false; break; }
             const uint32_t grp = code_base + cst * kCodeStageBytes + sub * (kBN * 64) + row_off;

@@ -161,3 +161,26 @@ def test_gemm_affine_repeat_is_bit_identical(cuda_lib, group):
         ys = [cuda_lib.w4_gemm_affine(x, packed, scales, zeros, group=group) for _ in range(5)]
         torch.cuda.synchronize()
         assert all(torch.equal(ys[0].view(torch.int16), v.view(torch.int16)) for v in ys[1:])
+
+
+@pytest.mark.parametrize("group", [32, 64])
+def test_gemm_affine_unaligned_scales_and_zeros(cuda_lib, group):
+    """Scales only 2-byte aligned and zeros at an odd address take the
+    unpaired loads; the result must equal the one from aligned buffers."""
+    W = wl.random_bf16((200, 1152), 0.02, seed=31, device=DEV)
+    N, K = W.shape
+    packed, scales, zeros = quantize_gpu(cuda_lib, W, group, True)
+    sb = torch.empty(N * (K // group) + 1, dtype=torch.bfloat16, device=DEV)
+    s_odd = sb[1:].view(N, K // group)
+    s_odd.copy_(scales)
+    zb = torch.empty(N * (K // group) + 1, dtype=torch.int8, device=DEV)
+    z_odd = zb[1:].view(N, K // group)
+    z_odd.copy_(zeros)
+    assert s_odd.data_ptr() % 4 == 2 and z_odd.data_ptr() % 2 == 1
+    for M in (8, 40):
+        x = wl.random_bf16((M, K), 1.0, seed=M, device=DEV)
+        for path in (W4_PATH_SMALL_M, W4_PATH_TENSOR):
+            a = cuda_lib.w4_gemm_affine(x, packed, scales, zeros, group=group, path=path)
+            b = cuda_lib.w4_gemm_affine(x, packed, s_odd, z_odd, group=group, path=path)
+            torch.cuda.synchronize()
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16)), (M, path)
