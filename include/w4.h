@@ -39,10 +39,15 @@
  * Conventions for every entry point
  * ---------------------------------
  *  - All tensor pointers are DEVICE pointers owned by the caller.  The library
- *    allocates no device memory and keeps no per-call state.
+ *    keeps no per-call state and allocates no device memory of its own, with
+ *    two exceptions: a per-device status word and a 2 MB plan array (for
+ *    w4_gemm_grouped_noalloc) as static __device__ variables, and the cuSOLVER
+ *    and cuBLAS handles the GPTQ calls create once per device (those libraries
+ *    hold their own work memory).
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    Work is enqueued asynchronously on it; nothing synchronises, except
- *    w4_last_device_status().
+ *    w4_last_device_status(), w4_grouped_plan_init (a blocking copy of the
+ *    plan) and w4_gemm_grouped_noalloc (see there).
  *  - K must be a multiple of 128; group is 128 except where an entry point
  *    says otherwise (32, 64 or 128 for the quantisers and w4_gemm_affine);
  *    N, M, K ≥ 0.  Sizes
