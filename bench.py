@@ -392,16 +392,30 @@ def gemm_set(torch, w4, wl, workload, Ms, pk, reps=20, path=None, grouped=False)
                         w4.w4_gemm_ex(x, p, s, out=ys[j], path=path)
 
         g = capture(torch, run)
-        t = T.time(g.replay, reps=reps) / copies
         nb = sum(gemm_bytes(M, N, K) for (N, K, _, _, _) in mats) / copies
         fl = sum(2 * M * N * K for (N, K, _, _, _) in mats) / copies
         t_hbm = nb / (pk["hbm_gbs"] * 1e9)
         t_tc = fl / (tensor_peak(pk) * 1e12)
+        clocks = None
+        if t_tc > t_hbm:
+            # Tensor-bound: soak for half a second and time under the clock
+            # sampler, to record the (power-capped) SM clock the fraction uses.
+            with ClockSampler(dev.index) as clk:
+                t_end = time.time() + 0.5
+                while time.time() < t_end:
+                    g.replay()
+                torch.cuda.synchronize()
+                t = T.time(g.replay, reps=reps) / copies
+            clocks = clk.summary()
+        else:
+            t = T.time(g.replay, reps=reps) / copies
         out[f"M{M}"] = {"us": t * 1e6, "GB/s": nb / t / 1e9, "TFLOP/s": fl / t / 1e12,
                         "tok/s": M / t, "bound": "hbm" if t_hbm >= t_tc else "tensor",
                         "frac": max(t_hbm, t_tc) / t,
                         "path": "grouped" if grouped else
                         (w4.w4_gemm_path_for(M, mats[0][0], mats[0][1]) if path is None else path)}
+        if clocks is not None:
+            out[f"M{M}"]["clocks"] = clocks
         if grouped:
             out[f"M{M}"]["launches_per_set"] = 1
             del plans
