@@ -69,3 +69,39 @@ def test_reference_arm_on_two_ranks():
     for key in ("metric", "unit", "steps", "warmup", "ms_per_step", "higher_is_better", "config",
                 "cpu_baseline", "e2e"):
         assert key in d
+
+
+def test_algorithmic_bytes():
+    """Bytes the bench charges per weight and per activation: 0.5 B codes +
+    2/128 B scales per weight; bf16 x and y; the quantiser reads bf16 W."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    N, K, M = 2560, 9216, 8
+    assert bench.gemm_bytes(M, N, K) == N * K * 0.515625 + 2 * M * K + 2 * M * N
+    assert bench.quant_bytes(N, K) == N * K * (2 + 0.515625)
+    assert bench.affine_bytes(M, N, K, 128, False) == bench.gemm_bytes(M, N, K)
+    assert bench.affine_bytes(M, N, K, 32, True) == N * K // 2 + N * (K // 32) * 3 + 2 * M * K + 2 * M * N
+
+
+def test_profiles_are_reproducible_summaries():
+    """Every committed profile summary gives the command that made it and holds
+    no raw report; every traffic record parses."""
+    pdir = os.path.join(ROOT, "profiles")
+    names = sorted(os.listdir(pdir))
+    assert any(n.startswith("launches_") for n in names)
+    for n in names:
+        path = os.path.join(pdir, n)
+        assert n.endswith((".md", ".txt")), n
+        assert os.path.getsize(path) < 16 * 1024, n
+        text = open(path).read()
+        if n.endswith(".md"):
+            assert "```" in text and ("ncu " in text), n
+            assert "--clock-control none" in text, n
+    for line in open(os.path.join(pdir, "traffic.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        parts = line.split()
+        fields = dict(p.split("=", 1) for p in parts[2:])
+        assert int(fields["read"]) + int(fields["write"]) == int(fields["bytes_per_launch"])
+        assert len(fields["source"]) == 12
