@@ -48,14 +48,15 @@ def obs_route(W_bits, H, group=128, damp=0.01):
     return O.pack_p1(q), s
 
 
-def test_gptq_matches_obs_route():
+@pytest.mark.parametrize("group", [128, 64, 32])
+def test_gptq_matches_obs_route(group):
     W = wl.bits(wl.random_bf16((12, 384), 0.02, seed=5))
     H, _ = correlated_h(384, 1024, seed=6)
-    p, s = O.gptq_quantize(W, H)
-    p2, s2 = obs_route(W, H)
+    p, s = O.gptq_quantize(W, H, group)
+    p2, s2 = obs_route(W, H, group)
     assert np.array_equal(s, s2)
     assert np.array_equal(p, p2)
-    assert np.mean(p != O.quantize_rtn(W)[0]) > 0.05  # the corrections do change codes
+    assert np.mean(p != O.quantize_rtn(W, group)[0]) > 0.05  # the corrections do change codes
 
 
 def test_gptq_diagonal_h_is_rtn():

@@ -109,7 +109,8 @@ PIN_TESTS = [
     lambda: pins.test_asym_matmul_bruteforce(32),
     lambda: pins.test_asym_invariants("ffn", 64),
     pins.test_asym_special_groups,
-    gptq.test_gptq_matches_obs_route,
+    lambda: gptq.test_gptq_matches_obs_route(128),
+    lambda: gptq.test_gptq_matches_obs_route(32),
     gptq.test_gptq_diagonal_h_is_rtn,
     lambda: gptq.test_gptq_block_size_does_not_change_the_result(32),
     gptq.test_gptq_scale_invariant_in_h,
@@ -124,6 +125,13 @@ def load_mutant(old: str, new: str) -> types.ModuleType:
     mod = types.ModuleType("w4_oracle_mutant")
     exec(compile(src.replace(old, new), "w4_oracle_mutant", "exec"), mod.__dict__)
     return mod
+
+
+def test_every_pin_passes_on_the_oracle():
+    """A pin that fails (or cannot be called) on the unmutated oracle would
+    count every mutant as caught: each one must pass here first."""
+    for t in PIN_TESTS:
+        t()
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
