@@ -74,6 +74,10 @@ MUTANTS = {
     "gptq_error_unscaled": ("err = (W1[:, j] - d * qc) / U[c, c]", "err = (W1[:, j] - d * qc)"),
     "gptq_no_block_carry": ("W[:, i2:] -= E1 @ U[i1:i2, i2:]", "W[:, i2:] -= 0.0"),
     "gptq_column_not_row": ("W1[:, j:] -= np.outer(err, U[c, c:i2])", "W1[:, j:] -= np.outer(err, U[c:i2, c])"),
+    "gptq_round_unclipped": ("    return np.clip(np.rint(r), Q_MIN, Q_MAX)\n\n\ndef gptq_quantize",
+                             "    return np.rint(r)\n\n\ndef gptq_quantize"),
+    "gptq_scale_divisor_8": ("    return f32_to_bf16_bits_rne((a / DIVISOR).astype(np.float32))",
+                             "    return f32_to_bf16_bits_rne((a / 8.0).astype(np.float32))"),
     "gptq_scale_from_original": (
         "cur = W1[:, j:j + group] if j + group <= i2 - i1 else W[:, c:c + group]",
         "cur = bf16_bits_to_f32(np.asarray(W_bits, dtype=np.uint16))[:, c:c + group]"),
