@@ -74,6 +74,11 @@ MUTANTS = {
     "gptq_error_unscaled": ("err = (W1[:, j] - d * qc) / U[c, c]", "err = (W1[:, j] - d * qc)"),
     "gptq_no_block_carry": ("W[:, i2:] -= E1 @ U[i1:i2, i2:]", "W[:, i2:] -= 0.0"),
     "gptq_column_not_row": ("W1[:, j:] -= np.outer(err, U[c, c:i2])", "W1[:, j:] -= np.outer(err, U[c:i2, c])"),
+    "tolerance_10x_loose": ("TOL_REL = 4e-3", "TOL_REL = 4e-2"),
+    "tolerance_ulp_dropped": ("    return TOL_REL * s_abs + bf16_ulp(y_ref)", "    return TOL_REL * s_abs + 0.0"),
+    "tolerance_ulp_x4": ("    return TOL_REL * s_abs + bf16_ulp(y_ref)", "    return TOL_REL * s_abs + 4 * bf16_ulp(y_ref)"),
+    "tolerance_signed_error": ("    return np.abs(y - y_ref) / parity_bound(y_ref, s_abs)",
+                               "    return (y - y_ref) / parity_bound(y_ref, s_abs)"),
     "gptq_round_unclipped": ("    return np.clip(np.rint(r), Q_MIN, Q_MAX)\n\n\ndef gptq_quantize",
                              "    return np.rint(r)\n\n\ndef gptq_quantize"),
     "gptq_scale_divisor_8": ("    return f32_to_bf16_bits_rne((a / DIVISOR).astype(np.float32))",
@@ -101,6 +106,7 @@ PIN_TESTS = [
     pins.test_bf16_rne_against_exact,
     pins.test_bf16_ulp,
     pins.test_parity_bound_accepts_exact_and_rejects_offset,
+    pins.test_parity_bound_edges,
     pins.test_awq_unit_scale_is_plain_rtn,
     lambda: pins.test_awq_bruteforce_4x256(71),
     pins.test_awq_rounds_through_fp32,

@@ -627,3 +627,23 @@ def test_parity_bound_accepts_exact_and_rejects_offset():
     assert O.parity_excess(yb, y, sabs).max() <= 1
     bad = O.f32_to_bf16_bits_rne((y + 0.05 * sabs).astype(np.float32))
     assert O.parity_excess(bad, y, sabs).max() > 1
+
+
+# Hand-worked edges of the matmul tolerance |y − y_ref| ≤ 4e-3·Σ|ŵx| + ulp_bf16(y_ref):
+# (y_ref, Σ|ŵx|, bf16 bits of y, inside the bound?).
+#   y_ref = 1, Σ = 10: bound = 0.04 + 2⁻⁷ = 0.0478125; bf16 steps near 1 are 2⁻⁷ above and
+#   2⁻⁸ below, so 1 ± 6/128 (0x3F86, 0x3F74) are inside and 1 ± 7/128 (0x3F87, 0x3F72) outside.
+#   y_ref = 3, Σ = 0: ulp = 2^(1−7) = 2⁻⁶; 3 + 2⁻⁶ (0x4041) inside, 3 + 2⁻⁵ (0x4042) outside.
+#   y_ref = 0, Σ = 0: ulp = 2⁻¹³³, the smallest bf16 subnormal (0x0001) inside, 2⁻¹³² (0x0002) outside.
+BOUND_EDGES = [
+    (1.0, 10.0, 0x3F80, True), (1.0, 10.0, 0x3F86, True), (1.0, 10.0, 0x3F87, False),
+    (1.0, 10.0, 0x3F74, True), (1.0, 10.0, 0x3F72, False),
+    (3.0, 0.0, 0x4041, True), (3.0, 0.0, 0x4042, False),
+    (0.0, 0.0, 0x0001, True), (0.0, 0.0, 0x0002, False),
+]
+
+
+def test_parity_bound_edges():
+    for y_ref, sabs, bits, inside in BOUND_EDGES:
+        e = O.parity_excess(np.array([bits], dtype=np.uint16), np.array([y_ref]), np.array([sabs]))[0]
+        assert (e <= 1) == inside, (y_ref, sabs, hex(bits), e)
