@@ -213,3 +213,36 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(w4, "library_path", lambda: str(tmp_path / "libw4.so"))
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         w4.load()
+
+
+@pytest.mark.parametrize("lang", ["c", "c++"])
+def test_header_is_a_c_abi(lib, lang, tmp_path):
+    """w4.h compiles as strict C99 and as C++17, and a program that takes the
+    address of every declared entry point links against libw4.so with the
+    unmangled names (the header's extern "C" guard)."""
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip(f"no {lang} compiler")
+    names = declared_functions()
+    src = tmp_path / ("abi.c" if lang == "c" else "abi.cpp")
+    body = ",\n    ".join(f"(void (*)(void)){n}" for n in names)
+    src.write_text(
+        '#include "w4.h"\n'
+        "#include <stdio.h>\n"
+        f"void (*const entry_points[])(void) = {{\n    {body}\n}};\n"
+        "int main(void) {\n"
+        "    static w4_gemm_problem p;\n"
+        "    static w4_grouped_plan plan;\n"
+        "    (void)p; (void)plan;\n"
+        "    printf(\"%d\\n\", (int)(sizeof entry_points / sizeof entry_points[0]));\n"
+        "    return w4_status_string(W4_OK) == NULL;\n"
+        "}\n")
+    std = ["-std=c99", "-pedantic"] if lang == "c" else ["-std=c++17"]
+    lib_dir = os.path.dirname(w4.library_path())
+    cmd = [cc, *std, "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+           "-o", str(tmp_path / "abi"), "-L", lib_dir, "-lw4", "-Wl,--unresolved-symbols=ignore-in-shared-libs"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
