@@ -356,40 +356,26 @@ def w4_grouped_plan(problems) -> GroupedPlan:
     problems: sequence of (x, packed, scales, y) CUDA tensors with the shapes
     of w4_gemm, all on one device."""
     problems = list(problems)
-    if not problems:
-        raise ValueError("no problems")
-    arr = (_Problem * len(problems))()
-    tensors = []
-    device = problems[0][0].device
-    for i, (x, packed, scales, y) in enumerate(problems):
-        _cuda_tensor(x, "x", torch.bfloat16, 2)
-        _cuda_tensor(packed, "packed", torch.uint8, 2)
-        _cuda_tensor(scales, "scales", torch.bfloat16, 2)
-        _cuda_tensor(y, "y", torch.bfloat16, 2)
-        M, K = x.shape
-        N = packed.shape[0]
-        if tuple(packed.shape) != (N, K // 2) or tuple(scales.shape) != (N, K // GROUP) or tuple(y.shape) != (M, N):
-            raise ValueError(f"problem {i}: x / packed / scales / y shapes disagree")
-        if x.device != device or packed.device != device or scales.device != device or y.device != device:
-            raise ValueError("all tensors of a plan must be on one device")
-        arr[i] = _Problem(x.data_ptr(), M, N, K, packed.data_ptr(), scales.data_ptr(), y.data_ptr())
-        tensors += [x, packed, scales, y]
+    arr, n, device = _problem_array(problems)
+    tensors = [t for p in problems for t in p]
     with torch.cuda.device(device):
-        nbytes = load().w4_grouped_plan_bytes(len(problems), arr)
+        nbytes = load().w4_grouped_plan_bytes(n, arr)
         if nbytes == 0:  # some problem is invalid: let plan_init name the reason
             probe = torch.empty(256, dtype=torch.uint8, device=device)
             status = load().w4_grouped_plan_init(ctypes.byref(_Plan()), probe.data_ptr() + (-probe.data_ptr()) % 128,
-                                                 128, len(problems), arr)
+                                                 128, n, arr)
             raise W4Error(status if status != W4_OK else W4_ERR_INVALID_ARG, "w4_grouped_plan")
         memory = torch.empty(nbytes + 128, dtype=torch.uint8, device=device)
         off = (-memory.data_ptr()) % 128
         plan = _Plan()
-        _check(load().w4_grouped_plan_init(ctypes.byref(plan), memory.data_ptr() + off, nbytes, len(problems), arr),
+        _check(load().w4_grouped_plan_init(ctypes.byref(plan), memory.data_ptr() + off, nbytes, n, arr),
                "w4_grouped_plan_init")
     return GroupedPlan(memory, plan, tensors)
 
 
 def _problem_array(problems):
+    """The w4_gemm_problem array of (x, packed, scales, y) tuples, after the
+    shape, dtype and device checks; returns (array, count, device)."""
     problems = list(problems)
     if not problems:
         raise ValueError("no problems")
@@ -405,7 +391,7 @@ def _problem_array(problems):
         if tuple(packed.shape) != (N, K // 2) or tuple(scales.shape) != (N, K // GROUP) or tuple(y.shape) != (M, N):
             raise ValueError(f"problem {i}: x / packed / scales / y shapes disagree")
         if x.device != device or packed.device != device or scales.device != device or y.device != device:
-            raise ValueError("all tensors must be on one device")
+            raise ValueError("all tensors of a grouped call must be on one device")
         arr[i] = _Problem(x.data_ptr(), M, N, K, packed.data_ptr(), scales.data_ptr(), y.data_ptr())
     return arr, len(problems), device
 

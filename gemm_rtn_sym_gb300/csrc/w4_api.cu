@@ -461,9 +461,10 @@ int w4_gemm_grouped_noalloc(int32_t count, const w4_gemm_problem* problems, void
     size_t cap = 0;
     if (static_plan_memory(&mem, &cap) != cudaSuccess) return W4_ERR_CUDA;
     if (image.size() > cap) return W4_ERR_UNSUPPORTED;
-    // A pageable source: the copy waits for the stream's earlier work (so a
-    // previous call's kernels no longer read the buffer) and has been staged
-    // when it returns, so `image` may be released.
+    // Stream-ordered: the copy lands after the stream's earlier work (a
+    // previous call's kernels no longer read the array).  From pageable
+    // memory, the source has been staged when the call returns, so `image`
+    // may be released.
     if (cudaMemcpyAsync(mem, image.data(), image.size(), cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream)) !=
         cudaSuccess)
         return W4_ERR_CUDA;

@@ -333,13 +333,13 @@ int w4_gemm_grouped(const w4_grouped_plan* plan, void* stream);
  *                       (about 5000 problems, or about 250000 64-row blocks);
  *   otherwise the checks and results of w4_grouped_plan_init + w4_gemm_grouped.
  * Races: the array is shared by every call on a device.  Calls in order on
- * one stream are safe (the plan copy waits for the stream's earlier work);
- * calls that may overlap — other streams, other host threads, or a CUDA
- * graph replaying a captured call while another call runs — can overwrite a
- * plan a running kernel is reading, and give wrong results.  The host thread
- * blocks until the stream's earlier work is done (pageable-memory copy), and
- * the call cannot be captured into a CUDA graph; use w4_grouped_plan_init +
- * w4_gemm_grouped for either.
+ * one stream are safe (the plan copy is ordered after the stream's earlier
+ * work); calls that may overlap on the GPU — other streams or other host
+ * threads — can overwrite a plan a running kernel is reading, and give wrong
+ * results.  The plan is copied from pageable host memory, so the host thread
+ * may block until the stream's earlier work is done.  Callers that need
+ * overlapping calls use w4_grouped_plan_init + w4_gemm_grouped, with one plan
+ * buffer per call.
  */
 int w4_gemm_grouped_noalloc(int32_t count, const w4_gemm_problem* problems, void* stream);
 

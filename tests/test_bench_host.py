@@ -105,3 +105,49 @@ def test_profiles_are_reproducible_summaries():
         fields = dict(p.split("=", 1) for p in parts[2:])
         assert int(fields["read"]) + int(fields["write"]) == int(fields["bytes_per_launch"])
         assert len(fields["source"]) == 12
+
+
+def test_oracle_pool_splits_rows_and_runs():
+    """The CPU baseline's process pool (spawned workers, the oracle unchanged)
+    covers every row once per pass and returns a positive wall time."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+
+    import bench
+    from gemm_rtn_sym_gb300 import workloads as wl
+
+    W = wl.bits(wl.random_bf16((10, 256), 0.02, seed=3))
+    x = wl.bits(wl.random_bf16((2, 256), 1.0, seed=4))
+    pool = bench.OraclePool(3, W, x, 256)
+    try:
+        assert pool.run(1) > 0 and pool.run(2) > 0
+    finally:
+        pool.close()
+    # The row split used by run(): contiguous, disjoint, complete.
+    w = min(pool.workers, pool.rows)
+    bounds = [pool.rows * i // w for i in range(w + 1)]
+    assert bounds[0] == 0 and bounds[-1] == 10 and all(a < b for a, b in zip(bounds, bounds[1:]))
+    assert np.array_equal(np.concatenate([W[a:b] for a, b in zip(bounds, bounds[1:])]), W)
+
+
+def test_compact_configs_line_is_short():
+    """The per-workload summary printed on the result line names every
+    workload and stays short enough for a log tail."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    pk = {"hbm_gbs": 6773.9, "bf16_tflops": 1872.3, "bf16_tflops_sustained": 1705.0, "source": "measured"}
+    one = {"us": 6.6, "frac": 0.27, "bound": "hbm"}
+    tc = {"us": 283.0, "frac": 0.67, "bound": "tensor"}
+    sub = {"ffn_m1": one, "outlier_m8": one, "quant_ffn": one,
+           "layer27b": {f"M{m}": one for m in (1, 5, 7, 13)},
+           "layer27b_grouped": {f"M{m}": one for m in (1, 5, 7, 13)},
+           "layer70b": {"M208": tc}, "layer70b_grouped": {"M208": tc},
+           "stack4b": {f"M{m}": one for m in (1, 2, 4, 8, 16, 32, 64, 128)},
+           "stack4b_grouped": {f"M{m}": one for m in (1, 2, 4, 8, 16, 32, 64, 128)}}
+    c = bench.compact_configs(sub, pk)
+    for label in ("1_ffn", "2_outlier", "3_layer27b", "3_layer27b_grouped", "4_layer70b", "4_layer70b_grouped",
+                  "5_stack4b", "5_stack4b_grouped", "quant_ffn"):
+        assert label in c
+    assert c["4_layer70b_grouped"]["M208"][2] == "tc"
+    assert len(json.dumps(c, separators=(",", ":"))) < 1200

@@ -1,8 +1,12 @@
 """w4_gemm_grouped_noalloc: the grouped matmul through the library's static
-plan buffer.  Collected last (file name) so the static buffer's reuse across
-earlier tests cannot hide a stale plan.  Results must equal the plan-based
-w4_gemm_grouped bit for bit (same kernels, same schedule) on two successive
-calls with different activations, and match the oracle."""
+plan buffer, for callers that cannot allocate device memory.  Collected last
+(file name), so that a run stopping at its first failure has run every other
+test first.  Results must equal the plan-based w4_gemm_grouped bit for bit
+(same kernels, same schedule) on two successive calls with different
+activations, and match the oracle; two calls with different problem sets,
+queued back to back on one stream with no synchronisation between them,
+must each give their own problems' results (the second call's plan must not
+overwrite the first one's while its kernels still read it)."""
 import pytest
 import torch
 
@@ -58,3 +62,28 @@ def test_noalloc_rejects_a_plan_larger_than_its_buffer(cuda_lib):
     w4.w4_gemm_grouped_noalloc(probs[:8])
     torch.cuda.synchronize()
     check_gemm(W, x, ys[3:4])
+
+
+def test_noalloc_two_problem_sets_back_to_back(cuda_lib):
+    """Call A (small-M problems only) and call B (a tensor-core problem and a
+    small-M problem of other shapes) share the static plan array: queued on one
+    stream without a synchronisation, A's kernels must still see A's plan."""
+    def make(shapes_ms, seed):
+        Ws, probs = [], []
+        for i, ((N, K), M) in enumerate(shapes_ms):
+            W = wl.random_bf16((N, K), 0.02, seed=seed + i, device=DEV)
+            packed, scales = quantize_gpu(cuda_lib, W)
+            x = wl.random_bf16((M, K), 1.0, seed=seed + 50 + i, device=DEV)
+            Ws.append(W)
+            probs.append((x, packed, scales, torch.empty((M, N), dtype=torch.bfloat16, device=DEV)))
+        return Ws, probs
+
+    Wa, a = make([((4096, 2048), 1), ((640, 4608), 8), ((300, 1152), 5)], 900)
+    Wb, b = make([((1000, 1024), 40), ((512, 3072), 16)], 950)
+    torch.cuda.synchronize()
+    w4.w4_gemm_grouped_noalloc(a)
+    w4.w4_gemm_grouped_noalloc(b)
+    torch.cuda.synchronize()
+    assert w4.w4_last_device_status() == 0
+    for W, (x, _, _, y) in zip(Wa + Wb, a + b):
+        check_gemm(W, x, y)
