@@ -13,7 +13,7 @@ constexpr int kTiles = 4;                // 16-row tiles per CTA
 constexpr int kRowsCta = 16 * kTiles;    // 64 weight rows per CTA
 constexpr int kStageGroups = 4;          // groups per stage
 constexpr int kMaxSplit = 8;
-constexpr int kTpw = 2;  // row tiles per consumer warp at M <= 8 (4 at M <= 16: fewer x fragments per tile)
+constexpr int kTpw = 4;  // row tiles per consumer warp: each warp takes one group of a stage for all 64 rows
 
 // TPW: row tiles per consumer warp.  Consumer warp c takes group c % 4 of every
 // stage for tiles (c / 4)·TPW .. +TPW-1, so 16 / TPW consumer warps per CTA.
