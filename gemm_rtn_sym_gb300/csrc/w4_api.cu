@@ -25,6 +25,10 @@ std::mutex g_info_mutex;
 // Smallest M that goes to the tensor-core kernel under W4_PATH_AUTO.
 constexpr int64_t kTensorMinM = 17;
 
+// Largest N or K of the GPTQ calls: their fp64 tile products run 64-row tiles
+// on a grid at most 65535 tiles high.
+constexpr int64_t kGptqMaxDim = int64_t{65535} * 64;
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
@@ -141,7 +145,7 @@ int w4_quantize_rtn_scaled(const void* W, int64_t N, int64_t K, int32_t group, c
 }
 
 size_t w4_gptq_factor_workspace_bytes(int64_t K) {
-    if (check_sizes(1, K) != W4_OK || K == 0 || K > INT32_MAX) return 0;
+    if (check_sizes(1, K) != W4_OK || K == 0 || K > kGptqMaxDim) return 0;
     return gptq_factor_workspace_bytes(K);
 }
 
@@ -149,7 +153,7 @@ int w4_gptq_factor(const float* H, int64_t K, double damp, double* U, void* work
                    void* stream) {
     if (const int s = check_sizes(1, K)) return s;
     if (K == 0) return W4_OK;
-    if (K > INT32_MAX || static_cast<double>(K) * K > 1e18) return W4_ERR_UNSUPPORTED;
+    if (K > kGptqMaxDim || static_cast<double>(K) * K > 1e18) return W4_ERR_UNSUPPORTED;
     if (!(damp >= 0.0) || damp > 1e30) return W4_ERR_INVALID_ARG;
     if (!H || !U || !workspace) return W4_ERR_INVALID_ARG;
     if (!aligned(H, 4) || !aligned(U, 8) || !aligned(workspace, 256)) return W4_ERR_MISALIGNED;
@@ -179,7 +183,7 @@ int w4_gptq_quantize(const void* W, int64_t N, int64_t K, int32_t group, const d
     if (!valid_group(group)) return W4_ERR_UNSUPPORTED;
     if (const int s = check_sizes(N, K)) return s;
     if (N == 0 || K == 0) return W4_OK;
-    if (N > INT32_MAX || K > INT32_MAX) return W4_ERR_UNSUPPORTED;
+    if (N > kGptqMaxDim || K > kGptqMaxDim) return W4_ERR_UNSUPPORTED;
     if (!W || !U || !packed || !scales || !workspace) return W4_ERR_INVALID_ARG;
     if (!aligned(W, 16) || !aligned(U, 8) || !aligned(packed, 16) || !aligned(scales, 2) || !aligned(workspace, 256))
         return W4_ERR_MISALIGNED;

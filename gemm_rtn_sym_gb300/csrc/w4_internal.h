@@ -44,9 +44,10 @@ cudaError_t launch_gemv_affine(const void* x, int64_t M, int64_t N, int64_t K, i
 cudaError_t launch_gemm_tc(const void* x, int64_t M, int64_t N, int64_t K, const void* packed,
                            const void* scales, void* y, const DeviceInfo& dev, cudaStream_t stream);
 
-// GPTQ (fp64 state): the factor U of (H + λI)⁻¹ by cuSOLVER, then per matrix
-// the own sweep kernel and cuBLAS DGEMM block updates.  Return 0, 1 on a CUDA /
-// library failure, 2 when the workspace is too small.
+// GPTQ (fp64 state): the factor U of (H + λI)⁻¹ (own blocked Cholesky and
+// triangular inverse), then per matrix the sweep kernel and the fp64 tile
+// product for the block updates.  Return 0, 1 on a CUDA failure, 2 when the
+// workspace is too small.
 size_t gptq_factor_workspace_bytes(int64_t K);
 size_t gptq_workspace_bytes(int64_t N, int64_t K);
 int launch_gptq_factor(const float* H, int64_t K, double damp, double* U, void* workspace, size_t workspace_bytes,

@@ -39,11 +39,9 @@
  * Conventions for every entry point
  * ---------------------------------
  *  - All tensor pointers are DEVICE pointers owned by the caller.  The library
- *    keeps no per-call state and allocates no device memory of its own, with
- *    two exceptions: a per-device status word and a 2 MB plan array (for
- *    w4_gemm_grouped_noalloc) as static __device__ variables, and the cuSOLVER
- *    and cuBLAS handles the GPTQ calls create once per device (those libraries
- *    hold their own work memory).
+ *    keeps no per-call state and allocates no device memory of its own; its
+ *    only device state is a per-device status word and a 2 MB plan array (for
+ *    w4_gemm_grouped_noalloc), both static __device__ variables.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    Work is enqueued asynchronously on it; nothing synchronises, except
  *    w4_last_device_status(), w4_grouped_plan_init (a blocking copy of the
@@ -232,11 +230,13 @@ int w4_gemm_affine(const void* x, int64_t M, int64_t N, int64_t K, int32_t group
  *   damp       in : the damping fraction (the study: 0.01), ≥ 0
  *   U          out: fp64 [K, K] row-major, 8-byte aligned; its upper triangle
  *                   (diagonal included) is the factor, the rest unspecified
- *   workspace  in : w4_gptq_factor_workspace_bytes(K) bytes, 256-byte aligned
  * Computed as U = J L̃⁻¹ J with L̃ the Cholesky factor of J (H + λI) J (J the
- * order-reversing permutation): cuSOLVER potrf and trtri on `stream`, (2/3)·K³
- * flops.  A failed factorization shows as W4_ERR_NUMERIC in
- * w4_last_device_status.
+ * order-reversing permutation): the library's own blocked fp64 Cholesky and
+ * triangular inverse on `stream`, (2/3)·K³ flops.  A failed factorization (a
+ * pivot ≤ 0) shows as W4_ERR_NUMERIC in w4_last_device_status; U is then
+ * unspecified.
+ *   workspace  in : w4_gptq_factor_workspace_bytes(K) bytes (= 8·K² + 256,
+ *                   rounded), 256-byte aligned
  *
  * w4_gptq_quantize — codes and scales of W given U:
  *   W          in : bf16 [N, K] (not modified)
@@ -246,11 +246,10 @@ int w4_gemm_affine(const void* x, int64_t M, int64_t N, int64_t K, int32_t group
  *   scales     out: bf16 [N, K/group]
  *   workspace  in : w4_gptq_workspace_bytes(N, K) bytes (= 8·N·K + 8·N·128,
  *                   rounded), 256-byte aligned
- * Block updates by cuBLAS DGEMM on `stream`.
+ * Block updates by the library's own fp64 tile product on `stream`.
  *
- * Both: N, K < 2^31; workspaces owned by the caller, overlapping nothing else,
- * contents on return unspecified; each call holds a library lock while it
- * enqueues work.
+ * Both: N, K ≤ 4,194,240 (W4_ERR_UNSUPPORTED above); workspaces owned by the caller,
+ * overlapping nothing else, contents on return unspecified.
  */
 size_t w4_gptq_factor_workspace_bytes(int64_t K);
 int w4_gptq_factor(const float* H, int64_t K, double damp, double* U,
