@@ -1,5 +1,6 @@
 // C ABI of the library (declared in include/w4.h): argument checks, kernel
 // choice, launches and the per-device status word of the bounded waits.
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -22,8 +23,14 @@ DeviceInfo g_info[kMaxDevices];
 bool g_info_ready[kMaxDevices];
 std::mutex g_info_mutex;
 
-// Smallest M that goes to the tensor-core kernel under W4_PATH_AUTO.
-constexpr int64_t kTensorMinM = 17;
+// Smallest M that goes to the tensor-core kernel: under W4_PATH_AUTO for one
+// matrix, and in grouped plans.  Measured crossovers on the 4B-class stack
+// and the 27B-class layer (the small-M kernel reads the weights once per pass
+// of up to 32 token rows): one launch per matrix, small-M is faster up to
+// M = 24 and the tensor-core tile from M = 32; in one grouped launch the
+// small-M kernel stays faster up to M = 32.
+constexpr int64_t kTensorMinM = 25;
+constexpr int64_t kGroupedTensorMinM = 33;
 
 // Largest N or K of the GPTQ calls: their fp64 tile products run 64-row tiles
 // on a grid at most 65535 tiles high.
@@ -310,7 +317,7 @@ int check_grouped_problem(const w4_gemm_problem& p) {
 
 size_t out_bytes(const w4_gemm_problem& p) { return static_cast<size_t>(p.M * p.N) * 2; }
 
-bool is_tensor(const w4_gemm_problem& p) { return p.M >= kTensorMinM; }
+bool is_tensor(const w4_gemm_problem& p) { return p.M >= kGroupedTensorMinM; }
 
 size_t round128(size_t v) { return (v + 127) / 128 * 128; }
 
@@ -370,7 +377,7 @@ int grouped_prepare(const void* device_memory, size_t bytes, int32_t count, cons
             tc.push_back(sp);
         } else {
             small.push_back(sp);
-            if (p.M > 8) token_tiles = 2;
+            token_tiles = std::max(token_tiles, static_cast<int>((p.M + 7) / 8));
         }
     }
     cudaError_t err;
@@ -436,7 +443,7 @@ int w4_gemm_grouped(const w4_grouped_plan* plan, void* stream) {
     const bool has_small = plan->items > 0, has_tc = plan->tc_items > 0;
     if (!has_small && !has_tc) return W4_ERR_INVALID_ARG;
     if (has_small && (plan->ctas < 1 || plan->ctas > plan->items ||
-                      (plan->token_tiles != 1 && plan->token_tiles != 2)))
+                      plan->token_tiles < 1 || plan->token_tiles > 4))
         return W4_ERR_INVALID_ARG;
     if (has_tc && (plan->tc_ctas < 1 || plan->tc_ctas > plan->tc_items || plan->tc_max_bm < 16 ||
                    plan->tc_max_bm > 256 || plan->tc_offset % 128 != 0 || plan->tc_offset >= plan->bytes))

@@ -57,13 +57,13 @@ struct GemvArgs {
     const int8_t* zeros;  // affine variant only; nullptr: symmetric
     int64_t row_groups;   // affine variant: scales (and zeros) per row, K / group
     __nv_bfloat16* y;
-    int M;  // token rows of this pass, 1..16
+    int M;  // token rows of this pass, 1..32
     int64_t N, K;
     int split;
     unsigned* status;
 };
 
-// MT: token tiles of 8 (1: M <= 8, 2: M <= 16).  QG: 0 for the symmetric
+// MT: token tiles of 8 (1..4: M <= 8, 16, 24, 32 per pass).  QG: 0 for the symmetric
 // group-128 format (offset MMA chain, one fp32 scaling per group); 32, 64 or
 // 128 for the affine variant (group size QG, optional zero points).
 template <int MT, int TPW, int QG>
@@ -73,6 +73,9 @@ gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_cons
     using C = Cfg<MT>;
     constexpr int kConsumers = Warps<TPW>::kConsumers;
     constexpr int kThreads = Warps<TPW>::kThreads;
+    // Every weight dequantised to bf16 before its MMA (affine formats, and the
+    // symmetric format at 24 or 32 token rows).
+    constexpr bool kDeq = QG != 0 || Dequant<MT>::value;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -198,22 +201,20 @@ gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_cons
             }
             const bool active = gs + t * kStageGroups + cw < ge;  // warp-uniform
             const uint32_t st = base + s * C::kStageBytes;
-            uint32_t xw[MT][16];
-            uint4 wv[TPW][2];
-            if (active) {
-                load_x_frags<MT, C::kXRows>(xw, st + x_blk, gid, tig);
-#pragma unroll
-                for (int rt = 0; rt < TPW; ++rt) {
-                    wv[rt][0] = lds128(st + w_off + rt * 16 * 64);
-                    wv[rt][1] = lds128(st + w_off + rt * 16 * 64 + 8 * 64);
-                }
-            }
             // Release the stage only after its fragments have been used: the
             // shared-memory loads may still be pending when an arrive executes,
             // and the next TMA copy into this stage must not overtake them
             // (releasing right after the loads gave rare corrupted fragments).
             if (active) {
-                if (QG == 0) {
+                uint32_t xw[MT][16];
+                load_x_frags<MT, C::kXRows>(xw, st + x_blk, gid, tig);
+                if (!kDeq) {
+                    uint4 wv[TPW][2];
+#pragma unroll
+                    for (int rt = 0; rt < TPW; ++rt) {
+                        wv[rt][0] = lds128(st + w_off + rt * 16 * 64);
+                        wv[rt][1] = lds128(st + w_off + rt * 16 * 64 + 8 * 64);
+                    }
                     group_math<MT, TPW>(acc, xw, wv, d_cur);
                 } else {
                     uint32_t d2[TPW][2], o2[TPW][2];
@@ -222,9 +223,9 @@ gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_cons
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             d2[rt][h] = d_cur[rt][h] | (d_cur[rt][h] << 16);
-                            o2[rt][h] = z_cur[rt][h] | (z_cur[rt][h] << 16);
+                            o2[rt][h] = QG == 0 ? 0x43084308u : (z_cur[rt][h] | (z_cur[rt][h] << 16));
                         }
-                    group_math_affine<MT, TPW>(acc, xw, wv, d2, o2);
+                    group_math_affine_lds<MT, TPW>(acc, xw, st + w_off, d2, o2);
                 }
             }
             mbar_arrive(empty(s));
@@ -393,11 +394,15 @@ cudaError_t launch_gemv_q(const void* x, int64_t M, int64_t N, int64_t K, const 
     const auto* sc = static_cast<const uint16_t*>(scales);
     const auto* zp = static_cast<const int8_t*>(zeros);
     auto* yb = static_cast<__nv_bfloat16*>(y);
-    for (int64_t m0 = 0; m0 < M; m0 += 16) {
-        const int mp = static_cast<int>(M - m0 < 16 ? M - m0 : 16);
+    for (int64_t m0 = 0; m0 < M; m0 += kMaxPassRows) {
+        const int mp = static_cast<int>(M - m0 < kMaxPassRows ? M - m0 : kMaxPassRows);
+        const __nv_bfloat16* xp = xb + m0 * K;
+        __nv_bfloat16* yp = yb + m0 * N;
         const cudaError_t e =
-            mp <= 8 ? launch_mt<1, kTpw, QG>(xb + m0 * K, mp, N, K, tmap_codes, sc, zp, yb + m0 * N, dev, stream)
-                    : launch_mt<2, 4, QG>(xb + m0 * K, mp, N, K, tmap_codes, sc, zp, yb + m0 * N, dev, stream);
+            mp <= 8    ? launch_mt<1, kTpw, QG>(xp, mp, N, K, tmap_codes, sc, zp, yp, dev, stream)
+            : mp <= 16 ? launch_mt<2, kTpw, QG>(xp, mp, N, K, tmap_codes, sc, zp, yp, dev, stream)
+            : mp <= 24 ? launch_mt<3, kTpw, QG>(xp, mp, N, K, tmap_codes, sc, zp, yp, dev, stream)
+                       : launch_mt<4, kTpw, QG>(xp, mp, N, K, tmap_codes, sc, zp, yp, dev, stream);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -14,6 +14,7 @@ constexpr int kRowsCta = 16 * kTiles;    // 64 weight rows per CTA
 constexpr int kStageGroups = 4;          // groups per stage
 constexpr int kMaxSplit = 8;
 constexpr int kTpw = 4;  // row tiles per consumer warp: each warp takes one group of a stage for all 64 rows
+constexpr int kMaxPassRows = 32;  // token rows of one pass (MT = 4)
 
 // TPW: row tiles per consumer warp.  Consumer warp c takes group c % 4 of every
 // stage for tiles (c / 4)·TPW .. +TPW-1, so 16 / TPW consumer warps per CTA.
@@ -24,11 +25,13 @@ struct Warps {
 };
 constexpr int kCodeStageBytes = kStageGroups * kRowsCta * 64;  // 16 KB: [group][row][64 B]
 
+// MT: token tiles of 8 per pass (1..4, i.e. up to 32 token rows).
 template <int MT>
 struct Cfg {
     static constexpr int kXRows = 8 * MT;                               // token rows staged
     static constexpr int kXStageBytes = 2 * kStageGroups * kXRows * 128;  // [k-block][row][128 B]
-    static constexpr int kStages = MT == 1 ? 4 : 3;
+    // Ring depth: two CTAs per SM must fit (a 24 KB stage at MT = 1 up to 48 KB at MT = 4).
+    static constexpr int kStages = MT == 1 ? 4 : (MT == 2 ? 3 : 2);
     static constexpr int kStageBytes = kCodeStageBytes + kXStageBytes;
     // Two CTAs per SM, each with its own TMA producer (one issuing thread per
     // SM does not reach the HBM rate with copies of this size).
@@ -143,33 +146,62 @@ __device__ __forceinline__ uint32_t affine_pair(uint32_t biased, uint32_t off2, 
     return r;
 }
 
+// One row tile of the affine variant: wa / wb are the 16-byte chunks of rows
+// gid and gid + 8.
+template <int MT>
+__device__ __forceinline__ void tile_math_affine(float (&acc)[MT][4], const uint32_t (&xw)[MT][16], const uint4 wa4,
+                                                 const uint4 wb4, uint32_t da, uint32_t db, uint32_t oa, uint32_t ob) {
+    const uint32_t wa[4] = {wa4.x, wa4.y, wa4.z, wa4.w};
+    const uint32_t wb[4] = {wb4.x, wb4.y, wb4.z, wb4.w};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const uint32_t a0 = affine_pair(biased_pair<0>(wa[w]), oa, da);
+        const uint32_t a2 = affine_pair(biased_pair<1>(wa[w]), oa, da);
+        const uint32_t a1 = affine_pair(biased_pair<0>(wb[w]), ob, db);
+        const uint32_t a3 = affine_pair(biased_pair<1>(wb[w]), ob, db);
+        const uint32_t b0 = affine_pair(biased_pair<2>(wa[w]), oa, da);
+        const uint32_t b2 = affine_pair(biased_pair<3>(wa[w]), oa, da);
+        const uint32_t b1 = affine_pair(biased_pair<2>(wb[w]), ob, db);
+        const uint32_t b3 = affine_pair(biased_pair<3>(wb[w]), ob, db);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            mma_bf16_16816(acc[mt], a0, a1, a2, a3, xw[mt][4 * w], xw[mt][4 * w + 1]);
+            mma_bf16_16816(acc[mt], b0, b1, b2, b3, xw[mt][4 * w + 2], xw[mt][4 * w + 3]);
+        }
+    }
+}
+
 template <int MT, int TPW>
 __device__ __forceinline__ void group_math_affine(float (&acc)[TPW][MT][4], const uint32_t (&xw)[MT][16],
                                                   const uint4 (&wv)[TPW][2], const uint32_t (&d2)[TPW][2],
                                                   const uint32_t (&off2)[TPW][2]) {
 #pragma unroll
+    for (int rt = 0; rt < TPW; ++rt)
+        tile_math_affine<MT>(acc[rt], xw, wv[rt][0], wv[rt][1], d2[rt][0], d2[rt][1], off2[rt][0], off2[rt][1]);
+}
+
+// The same with each row tile's 16-byte chunks loaded from the stage just
+// before use (fewer live registers at 24 or 32 token rows).
+template <int MT, int TPW>
+__device__ __forceinline__ void group_math_affine_lds(float (&acc)[TPW][MT][4], const uint32_t (&xw)[MT][16],
+                                                      uint32_t w_addr, const uint32_t (&d2)[TPW][2],
+                                                      const uint32_t (&off2)[TPW][2]) {
+#pragma unroll
     for (int rt = 0; rt < TPW; ++rt) {
-        const uint32_t wa[4] = {wv[rt][0].x, wv[rt][0].y, wv[rt][0].z, wv[rt][0].w};
-        const uint32_t wb[4] = {wv[rt][1].x, wv[rt][1].y, wv[rt][1].z, wv[rt][1].w};
-        const uint32_t da = d2[rt][0], db = d2[rt][1], oa = off2[rt][0], ob = off2[rt][1];
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            const uint32_t a0 = affine_pair(biased_pair<0>(wa[w]), oa, da);
-            const uint32_t a2 = affine_pair(biased_pair<1>(wa[w]), oa, da);
-            const uint32_t a1 = affine_pair(biased_pair<0>(wb[w]), ob, db);
-            const uint32_t a3 = affine_pair(biased_pair<1>(wb[w]), ob, db);
-            const uint32_t b0 = affine_pair(biased_pair<2>(wa[w]), oa, da);
-            const uint32_t b2 = affine_pair(biased_pair<3>(wa[w]), oa, da);
-            const uint32_t b1 = affine_pair(biased_pair<2>(wb[w]), ob, db);
-            const uint32_t b3 = affine_pair(biased_pair<3>(wb[w]), ob, db);
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                mma_bf16_16816(acc[rt][mt], a0, a1, a2, a3, xw[mt][4 * w], xw[mt][4 * w + 1]);
-                mma_bf16_16816(acc[rt][mt], b0, b1, b2, b3, xw[mt][4 * w + 2], xw[mt][4 * w + 3]);
-            }
-        }
+        const uint4 wa = lds128(w_addr + rt * 16 * 64);
+        const uint4 wb = lds128(w_addr + rt * 16 * 64 + 8 * 64);
+        tile_math_affine<MT>(acc[rt], xw, wa, wb, d2[rt][0], d2[rt][1], off2[rt][0], off2[rt][1]);
     }
 }
+
+// Symmetric codes with 24 or 32 token rows per pass: there the legacy MMA
+// pipe, not the decode, bounds the kernel, so each weight is dequantised to
+// bf16(d·q) (the affine path with zero 0) instead of spending an offset MMA
+// chain and per-group fp32 scaling on the 136 bias.
+template <int MT>
+struct Dequant {
+    static constexpr bool value = MT >= 3;
+};
 
 }  // namespace gemv
 }  // namespace w4

@@ -53,7 +53,7 @@ static __device__ __align__(256) uint8_t g_static_plan[kStaticPlanBytes];
 struct alignas(128) GroupedHeader {
     int32_t count;
     int32_t n_items;
-    int32_t token_tiles;  // MT: 1 (all M <= 8) or 2 (some M in 9..16)
+    int32_t token_tiles;  // MT: ceil(max M / 8), 1..4
     int32_t n_ctas;       // the grid the plan was scheduled for
     int32_t reserved[28];
 };
@@ -221,19 +221,31 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
             if (!aborted) {
                 const bool active = t * kStageGroups + cw < G;  // warp-uniform
                 if (active) {
-                    const uint32_t st = base + s * C::kStageBytes;
-                    uint32_t xw[MT][16];
-                    uint4 wv[TPW][2];
-                    load_x_frags<MT, C::kXRows>(xw, st + x_blk, gid, tig);
-#pragma unroll
-                    for (int rt = 0; rt < TPW; ++rt) {
-                        wv[rt][0] = lds128(st + w_off + rt * 16 * 64);
-                        wv[rt][1] = lds128(st + w_off + rt * 16 * 64 + 8 * 64);
-                    }
                     // Release the stage only after its fragments have been used
                     // (shared-memory loads may still be pending when an arrive
                     // executes; the next TMA copy must not overtake them).
-                    group_math<MT, TPW>(acc, xw, wv, d_cur);
+                    const uint32_t st = base + s * C::kStageBytes;
+                    uint32_t xw[MT][16];
+                    load_x_frags<MT, C::kXRows>(xw, st + x_blk, gid, tig);
+                    if (!Dequant<MT>::value) {
+                        uint4 wv[TPW][2];
+#pragma unroll
+                        for (int rt = 0; rt < TPW; ++rt) {
+                            wv[rt][0] = lds128(st + w_off + rt * 16 * 64);
+                            wv[rt][1] = lds128(st + w_off + rt * 16 * 64 + 8 * 64);
+                        }
+                        group_math<MT, TPW>(acc, xw, wv, d_cur);
+                    } else {
+                        uint32_t d2[TPW][2], o2[TPW][2];
+#pragma unroll
+                        for (int rt = 0; rt < TPW; ++rt)
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                d2[rt][h] = d_cur[rt][h] | (d_cur[rt][h] << 16);
+                                o2[rt][h] = 0x43084308u;  // bf16x2 (136, 136): zero point 0
+                            }
+                        group_math_affine_lds<MT, TPW>(acc, xw, st + w_off, d2, o2);
+                    }
                 }
                 mbar_arrive(empty(s));
             }
@@ -339,7 +351,10 @@ size_t grouped_plan_bytes(int32_t count, int64_t n_items, int32_t n_ctas) {
 int grouped_ctas(int token_tiles, const DeviceInfo& dev) {
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess) return 0;
-    const int per_sm = token_tiles == 1 ? grouped_ctas_per_sm<1, kTpw>(device) : grouped_ctas_per_sm<2, 4>(device);
+    const int per_sm = token_tiles == 1   ? grouped_ctas_per_sm<1, kTpw>(device)
+                       : token_tiles == 2 ? grouped_ctas_per_sm<2, kTpw>(device)
+                       : token_tiles == 3 ? grouped_ctas_per_sm<3, kTpw>(device)
+                                          : grouped_ctas_per_sm<4, kTpw>(device);
     return per_sm * dev.sm_count;
 }
 
@@ -414,8 +429,12 @@ cudaError_t grouped_plan_build(const GroupedSpec* specs, int32_t count, int toke
 cudaError_t launch_grouped(const void* plan, int32_t n_ctas, int token_tiles, const DeviceInfo& dev,
                            cudaStream_t stream) {
     if (n_ctas < 1) return cudaSuccess;
-    return token_tiles == 1 ? launch_grouped_t<1, kTpw>(plan, n_ctas, dev, stream)
-                            : launch_grouped_t<2, 4>(plan, n_ctas, dev, stream);
+    switch (token_tiles) {
+        case 1: return launch_grouped_t<1, kTpw>(plan, n_ctas, dev, stream);
+        case 2: return launch_grouped_t<2, kTpw>(plan, n_ctas, dev, stream);
+        case 3: return launch_grouped_t<3, kTpw>(plan, n_ctas, dev, stream);
+        default: return launch_grouped_t<4, kTpw>(plan, n_ctas, dev, stream);
+    }
 }
 
 }  // namespace w4

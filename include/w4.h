@@ -84,7 +84,7 @@ typedef enum w4_status {
 typedef enum w4_gemm_path {
     W4_PATH_AUTO = 0,    /* what w4_gemm does: picked from M (w4_gemm_path_for)  */
     W4_PATH_SMALL_M = 1, /* TMA-fed GEMV: register nibble decode, legacy MMA,
-                            cluster split-K; any M (16 token rows per pass)     */
+                            cluster split-K; any M (32 token rows per pass)     */
     W4_PATH_TENSOR = 2   /* tcgen05 tile: weights dequantised into tensor
                             memory as the A operand, TMEM accumulators, cluster
                             split-K; any M ≥ 1                                  */
@@ -259,17 +259,18 @@ int w4_gptq_quantize(const void* W, int64_t N, int64_t K, int32_t group,
                      const double* U, void* packed, void* scales,
                      void* workspace, size_t workspace_bytes, void* stream);
 
-/* The kernel W4_PATH_AUTO picks for these sizes (W4_PATH_SMALL_M or
- * W4_PATH_TENSOR), or a negative w4_status for invalid sizes. */
+/* The kernel W4_PATH_AUTO picks for these sizes (W4_PATH_SMALL_M for
+ * M ≤ 24, W4_PATH_TENSOR above: the measured crossover for one launch per
+ * matrix), or a negative w4_status for invalid sizes. */
 int w4_gemm_path_for(int64_t M, int64_t N, int64_t K);
 
 /*
  * Grouped matmul — many independent problems y_i = Ŵ_i x_i in one call (the
  * matrices of a layer, or of a whole model step).  Each problem is computed
  * as by w4_gemm's kernel for its M (same per-element results contract, K not
- * split, deterministic): problems with M ≤ 16 by the small-M kernel, whose
+ * split, deterministic): problems with M ≤ 32 by the small-M kernel, whose
  * work items are (problem, 64-row block) pairs on a fixed grid of two CTAs
- * per SM; problems with M ≥ 17 by the tensor-core kernel, whose items are
+ * per SM; problems with M ≥ 33 by the tensor-core kernel, whose items are
  * (problem, 128-row tile, token tile) on one CTA per SM.  Items are assigned
  * at plan time longest first to the least-loaded CTA, and each CTA streams
  * its items back to back through its TMA pipelines.  A plan with both kinds
@@ -296,10 +297,10 @@ typedef struct w4_grouped_plan {
     size_t bytes;        /* bytes of it in use                                    */
     int32_t count;       /* problems                                              */
     int32_t device;      /* CUDA device the plan was built on                     */
-    int32_t items;       /* small-M work items (0: no problem with M ≤ 16)        */
+    int32_t items;       /* small-M work items (0: no problem with M ≤ 32)        */
     int32_t ctas;        /* CTAs they were scheduled over (the launch grid)       */
-    int32_t token_tiles; /* small-M kernel variant: 1 when every M ≤ 8, else 2    */
-    int32_t tc_items;    /* tensor-core work items (0: no problem with M ≥ 17)    */
+    int32_t token_tiles; /* small-M kernel variant: ceil(largest M / 8), 1..4     */
+    int32_t tc_items;    /* tensor-core work items (0: no problem with M ≥ 33)    */
     int32_t tc_ctas;     /* CTAs they were scheduled over                         */
     int32_t tc_max_bm;   /* widest token tile                                     */
     size_t tc_offset;    /* byte offset of the tensor-core part of the plan       */

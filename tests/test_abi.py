@@ -57,7 +57,8 @@ def test_size_helpers(lib):
 def test_path_choice(lib):
     assert lib.w4_gemm_path_for(1, 2560, 9216) == w4.W4_PATH_SMALL_M
     assert lib.w4_gemm_path_for(16, 2560, 9216) == w4.W4_PATH_SMALL_M
-    assert lib.w4_gemm_path_for(17, 2560, 9216) == w4.W4_PATH_TENSOR
+    assert lib.w4_gemm_path_for(24, 2560, 9216) == w4.W4_PATH_SMALL_M
+    assert lib.w4_gemm_path_for(25, 2560, 9216) == w4.W4_PATH_TENSOR
     assert lib.w4_gemm_path_for(208, 8192, 8192) == w4.W4_PATH_TENSOR
     assert lib.w4_gemm_path_for(-1, 2560, 9216) == -w4.W4_ERR_INVALID_ARG
     assert lib.w4_gemm_path_for(1, 2560, 100) == -w4.W4_ERR_UNSUPPORTED
