@@ -46,7 +46,7 @@ class _Problem(ctypes.Structure):
 class _Plan(ctypes.Structure):
     """w4_grouped_plan of include/w4.h."""
     _fields_ = [("device_plan", _vp), ("bytes", _sz), ("count", _i32), ("device", _i32), ("items", _i32),
-                ("ctas", _i32), ("token_tiles", _i32), ("tc_items", _i32), ("tc_ctas", _i32), ("tc_max_bm", _i32),
+                ("ctas", _i32), ("token_rows", _i32), ("tc_items", _i32), ("tc_ctas", _i32), ("tc_max_bm", _i32),
                 ("tc_offset", _sz)]
 
 _SIGNATURES = {

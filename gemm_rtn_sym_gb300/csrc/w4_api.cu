@@ -354,7 +354,7 @@ namespace {
 // of *plan except device_plan.
 int grouped_prepare(const void* device_memory, size_t bytes, int32_t count, const w4_gemm_problem* problems,
                     std::vector<uint8_t>* image, w4_grouped_plan* plan) {
-    int token_tiles = 1;
+    int64_t max_m = 1;
     std::vector<GroupedSpec> small, tc;
     for (int32_t i = 0; i < count; ++i) {
         const w4_gemm_problem& p = problems[i];
@@ -377,9 +377,10 @@ int grouped_prepare(const void* device_memory, size_t bytes, int32_t count, cons
             tc.push_back(sp);
         } else {
             small.push_back(sp);
-            token_tiles = std::max(token_tiles, static_cast<int>((p.M + 7) / 8));
+            max_m = std::max(max_m, p.M);
         }
     }
+    const int token_rows = grouped_token_rows(max_m);
     cudaError_t err;
     const DeviceInfo* dev = device_info(&err);
     if (!dev) return W4_ERR_CUDA;
@@ -389,10 +390,10 @@ int grouped_prepare(const void* device_memory, size_t bytes, int32_t count, cons
     int32_t n_ctas = 0, n_tc_ctas = 0;
     image->clear();
     if (!small.empty()) {
-        const int ctas = grouped_ctas(token_tiles, *dev);
+        const int ctas = grouped_ctas(token_rows, *dev);
         if (ctas < 1) return W4_ERR_CUDA;
-        if (grouped_plan_build(small.data(), static_cast<int32_t>(small.size()), token_tiles, ctas, image, &n_items,
-                               &n_ctas) != cudaSuccess)
+        if (grouped_plan_build(small.data(), static_cast<int32_t>(small.size()), token_rows, ctas, dev->sm_count,
+                               image, &n_items, &n_ctas) != cudaSuccess)
             return W4_ERR_CUDA;
         image->resize(round128(image->size()), 0);
     }
@@ -413,7 +414,7 @@ int grouped_prepare(const void* device_memory, size_t bytes, int32_t count, cons
     plan->device = device;
     plan->items = static_cast<int32_t>(n_items);
     plan->ctas = n_ctas;
-    plan->token_tiles = small.empty() ? 0 : token_tiles;
+    plan->token_rows = small.empty() ? 0 : token_rows;
     plan->tc_items = static_cast<int32_t>(n_tc_items);
     plan->tc_ctas = n_tc_ctas;
     plan->tc_max_bm = max_bm;
@@ -443,7 +444,7 @@ int w4_gemm_grouped(const w4_grouped_plan* plan, void* stream) {
     const bool has_small = plan->items > 0, has_tc = plan->tc_items > 0;
     if (!has_small && !has_tc) return W4_ERR_INVALID_ARG;
     if (has_small && (plan->ctas < 1 || plan->ctas > plan->items ||
-                      plan->token_tiles < 1 || plan->token_tiles > 4))
+                      grouped_token_rows(plan->token_rows) != plan->token_rows))
         return W4_ERR_INVALID_ARG;
     if (has_tc && (plan->tc_ctas < 1 || plan->tc_ctas > plan->tc_items || plan->tc_max_bm < 16 ||
                    plan->tc_max_bm > 256 || plan->tc_offset % 128 != 0 || plan->tc_offset >= plan->bytes))
@@ -456,7 +457,7 @@ int w4_gemm_grouped(const w4_grouped_plan* plan, void* stream) {
     if (!dev) return W4_ERR_CUDA;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (has_small)
-        if (const int s = to_status(launch_grouped(plan->device_plan, plan->ctas, plan->token_tiles, *dev, st))) return s;
+        if (const int s = to_status(launch_grouped(plan->device_plan, plan->ctas, plan->token_rows, *dev, st))) return s;
     if (has_tc)
         return to_status(launch_tc_grouped(static_cast<const uint8_t*>(plan->device_plan) + plan->tc_offset,
                                            plan->tc_ctas, plan->tc_max_bm, *dev, st));

@@ -124,7 +124,7 @@ gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_cons
             int issued = 0;
             for (int t = 0; t < nt; ++t) {
                 const int s = t % C::kStages;
-                if (!mbar_wait(empty(s), (static_cast<uint32_t>(t / C::kStages) & 1u) ^ 1u)) {
+                if (!mbar_wait_suspend(empty(s), (static_cast<uint32_t>(t / C::kStages) & 1u) ^ 1u)) {
                     ok = false;
                     break;
                 }

@@ -63,17 +63,26 @@ constexpr uint32_t kMinus136x2 = 0xC308C308u;  // bf16x2 (−136, −136)
 
 // Activation fragments of one stage: token rows mt·8 + gid, the 64 contiguous
 // bytes (32 k) of this lane's part of the group, from the 128-byte-swizzled
-// [k-block][row][128 B] tile.
+// [k-block][row][128 B] tile with kXRows rows per block.  The swizzle XORs the
+// 16-byte chunk index with the 128-byte line's index in its 1024-byte atom
+// (address bits 7..9; stages are 1024-byte aligned).  Rows at or past kXRows
+// are not staged and read as zeros.
 template <int MT, int kXRows>
 __device__ __forceinline__ void load_x_frags(uint32_t (&xw)[MT][16], uint32_t st_x_blk, int gid, int tig) {
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
         const int r = mt * 8 + gid;
         const uint32_t rowa = st_x_blk + r * 128;
+        if (kXRows < 8 && r >= kXRows) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) xw[mt][j] = 0u;
+            continue;
+        }
+        const uint32_t line = (rowa >> 7) & 7u;
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
             const uint32_t c = static_cast<uint32_t>(4 * (tig & 1) + v);
-            const uint4 q = lds128(rowa + ((c ^ static_cast<uint32_t>(r & 7)) << 4));
+            const uint4 q = lds128(rowa + ((c ^ line) << 4));
             xw[mt][4 * v + 0] = q.x;
             xw[mt][4 * v + 1] = q.y;
             xw[mt][4 * v + 2] = q.z;

@@ -53,14 +53,14 @@ static __device__ __align__(256) uint8_t g_static_plan[kStaticPlanBytes];
 struct alignas(128) GroupedHeader {
     int32_t count;
     int32_t n_items;
-    int32_t token_tiles;  // MT: ceil(max M / 8), 1..4
+    int32_t token_rows;   // x rows staged per 64-k block: 2, 4, 8, 16, 24 or 32
     int32_t n_ctas;       // the grid the plan was scheduled for
     int32_t reserved[28];
 };
 
 struct alignas(128) GroupedProblem {
     CUtensorMap codes;  // [G][N][64 B], boxes of 4 groups × 64 rows
-    CUtensorMap x;      // [K/64][M][64], boxes of 8 blocks × 8·MT rows, 128-byte swizzle
+    CUtensorMap x;      // [K/64][M][64], boxes of 8 blocks × token_rows rows, 128-byte swizzle
     const uint16_t* scales;
     __nv_bfloat16* y;
     int64_t N;
@@ -80,10 +80,30 @@ __device__ __forceinline__ void consumer_sync(int n_threads) {
     asm volatile("bar.sync 1, %0;" ::"r"(n_threads) : "memory");
 }
 
-template <int MT, int TPW>
-__global__ void __launch_bounds__(Warps<TPW>::kThreads, 2)
+// Geometry of the grouped kernel for MT token tiles with XR token rows staged
+// per 64-k block (XR < 8 only for one tile: a decode step of one or two tokens
+// stages one or two rows, not eight), run with CPS CTAs per SM.  The ring is
+// as deep as fits: per CTA about 227 KB / CPS of shared memory, of which the
+// reduction buffer and barriers take 9 KB.  With one token tile three CTAs
+// per SM stream faster than two (more warps to hide the decode's dependency
+// latency), unless the items balance badly over that many CTAs.
+template <int MT, int XR, int CPS>
+struct GCfg {
+    static constexpr int kXRows = XR;
+    static constexpr int kXStageBytes = 2 * kStageGroups * XR * 128;  // [k-block][row][128 B]
+    static constexpr int kStageBytes = kCodeStageBytes + kXStageBytes;
+    static constexpr int kCtasPerSm = CPS;
+    static constexpr int kBudget = (CPS == 3 ? 74 : 112) * 1024 - 9 * 1024;
+    static constexpr int kStages = kBudget / kStageBytes > 5 ? 5 : kBudget / kStageBytes;
+    static_assert(XR == 8 * MT || (MT == 1 && (XR == 2 || XR == 4)), "staged rows");
+    static_assert(kStages >= 2, "ring depth");
+};
+
+template <int MT, int XR, int CPS>
+__global__ void __launch_bounds__(Warps<kTpw>::kThreads, CPS)
 gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
-    using C = Cfg<MT>;
+    using C = GCfg<MT, XR, CPS>;
+    constexpr int TPW = kTpw;
     constexpr int kConsumers = Warps<TPW>::kConsumers;
     constexpr int kCThreads = 32 * kConsumers;
     constexpr int kRedFloats = kStageGroups * kTiles * 4 * 32;
@@ -134,7 +154,7 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
                 tensormap_acquire(&pr->x);
                 const int row = static_cast<int>(it.y) * kRowsCta;
                 for (int t = 0; t < pr->T; ++t) {
-                    if (!mbar_wait(empty(s), phase ^ 1u)) {
+                    if (!mbar_wait_suspend(empty(s), phase ^ 1u)) {
                         ok = false;
                         break;
                     }
@@ -278,25 +298,25 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
     }
 }
 
-template <int MT, int TPW>
+template <int MT, int XR, int CPS>
 constexpr int grouped_smem_bytes() {
-    return Cfg<MT>::kStages * Cfg<MT>::kStageBytes + kStageGroups * kTiles * 4 * 32 * 4 + 16 * Cfg<MT>::kStages +
-           1024;
+    using C = GCfg<MT, XR, CPS>;
+    return C::kStages * C::kStageBytes + kStageGroups * kTiles * 4 * 32 * 4 + 16 * C::kStages + 1024;
 }
 
 std::mutex g_grouped_mutex;
 
-template <int MT, int TPW>
+template <int MT, int XR, int CPS>
 int grouped_ctas_per_sm(int device) {
     static int per_device[64];
     std::lock_guard<std::mutex> lock(g_grouped_mutex);
     if (device < 0 || device >= 64) return 0;
     if (per_device[device] == 0) {
         int v = 0;
-        if (cudaFuncSetAttribute(gemv_grouped_kernel<MT, TPW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 grouped_smem_bytes<MT, TPW>()) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, gemv_grouped_kernel<MT, TPW>, Warps<TPW>::kThreads,
-                                                          grouped_smem_bytes<MT, TPW>()) != cudaSuccess ||
+        if (cudaFuncSetAttribute(gemv_grouped_kernel<MT, XR, CPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 grouped_smem_bytes<MT, XR, CPS>()) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, gemv_grouped_kernel<MT, XR, CPS>, Warps<kTpw>::kThreads,
+                                                          grouped_smem_bytes<MT, XR, CPS>()) != cudaSuccess ||
             v < 1) {
             cudaGetLastError();
             return 0;
@@ -306,23 +326,22 @@ int grouped_ctas_per_sm(int device) {
     return per_device[device];
 }
 
-template <int MT, int TPW>
+template <int MT, int XR, int CPS>
 cudaError_t launch_grouped_t(const void* plan, int32_t n_ctas, const DeviceInfo& dev, cudaStream_t stream) {
     int device = 0;
     if (cudaError_t e = cudaGetDevice(&device)) return e;
-    if (grouped_ctas_per_sm<MT, TPW>(device) < 1) return cudaErrorInvalidConfiguration;  // sets the smem attribute
+    if (grouped_ctas_per_sm<MT, XR, CPS>(device) < 1) return cudaErrorInvalidConfiguration;  // sets the smem attribute
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(n_ctas), 1, 1);
-    cfg.blockDim = dim3(Warps<TPW>::kThreads, 1, 1);
-    cfg.dynamicSmemBytes = grouped_smem_bytes<MT, TPW>();
+    cfg.blockDim = dim3(Warps<kTpw>::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = grouped_smem_bytes<MT, XR, CPS>();
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    (void)dev;
-    return cudaLaunchKernelEx(&cfg, gemv_grouped_kernel<MT, TPW>, static_cast<const uint8_t*>(plan), dev.status);
+    return cudaLaunchKernelEx(&cfg, gemv_grouped_kernel<MT, XR, CPS>, static_cast<const uint8_t*>(plan), dev.status);
 }
 
 }  // namespace
@@ -348,69 +367,111 @@ size_t grouped_plan_bytes(int32_t count, int64_t n_items, int32_t n_ctas) {
            sizeof(int32_t) * static_cast<size_t>((n_ctas + 2) & ~1) + sizeof(uint2) * static_cast<size_t>(n_items);
 }
 
-int grouped_ctas(int token_tiles, const DeviceInfo& dev) {
+int grouped_token_rows(int64_t max_m) {
+    return max_m <= 2 ? 2 : max_m <= 4 ? 4 : max_m <= 8 ? 8 : max_m <= 16 ? 16 : max_m <= 24 ? 24 : 32;
+}
+
+// Resident CTAs per SM of the grouped kernel for these token rows (three for
+// one token tile, two otherwise).
+int grouped_ctas(int token_rows, const DeviceInfo& dev) {
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess) return 0;
-    const int per_sm = token_tiles == 1   ? grouped_ctas_per_sm<1, kTpw>(device)
-                       : token_tiles == 2 ? grouped_ctas_per_sm<2, kTpw>(device)
-                       : token_tiles == 3 ? grouped_ctas_per_sm<3, kTpw>(device)
-                                          : grouped_ctas_per_sm<4, kTpw>(device);
+    int per_sm = 0;
+    switch (token_rows) {
+        case 2: per_sm = grouped_ctas_per_sm<1, 2, 3>(device); break;
+        case 4: per_sm = grouped_ctas_per_sm<1, 4, 3>(device); break;
+        case 8: per_sm = grouped_ctas_per_sm<1, 8, 3>(device); break;
+        case 16: per_sm = grouped_ctas_per_sm<2, 16, 2>(device); break;
+        case 24: per_sm = grouped_ctas_per_sm<3, 24, 2>(device); break;
+        case 32: per_sm = grouped_ctas_per_sm<4, 32, 2>(device); break;
+        default: return 0;
+    }
     return per_sm * dev.sm_count;
 }
 
-cudaError_t grouped_plan_build(const GroupedSpec* specs, int32_t count, int token_tiles, int32_t n_ctas,
-                               std::vector<uint8_t>* out, int64_t* n_items_out, int32_t* n_ctas_out) {
+namespace {
+
+struct PlanItem {
+    int32_t stages;
+    uint2 id;
+};
+
+// Longest processing time first: items by cost (stages, plus one for the
+// item's epilogue) in decreasing order, each to the least-loaded CTA (lowest
+// index among equals).  Deterministic.  Returns the largest CTA load.
+int64_t schedule_lpt(const std::vector<PlanItem>& sorted, int32_t n_ctas, std::vector<std::vector<uint2>>* per_cta) {
+    using Load = std::pair<int64_t, int32_t>;  // (work so far, CTA)
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+    for (int32_t c = 0; c < n_ctas; ++c) heap.push({0, c});
+    if (per_cta) per_cta->assign(static_cast<size_t>(n_ctas), {});
+    int64_t makespan = 0;
+    for (const PlanItem& it : sorted) {
+        Load l = heap.top();
+        heap.pop();
+        if (per_cta) (*per_cta)[static_cast<size_t>(l.second)].push_back(it.id);
+        l.first += it.stages + 1;
+        makespan = std::max(makespan, l.first);
+        heap.push(l);
+    }
+    return makespan;
+}
+
+}  // namespace
+
+cudaError_t grouped_plan_build(const GroupedSpec* specs, int32_t count, int token_rows, int32_t max_ctas,
+                               int32_t sm_count, std::vector<uint8_t>* out, int64_t* n_items_out,
+                               int32_t* n_ctas_out) {
     int64_t n_items = 0;
     for (int32_t i = 0; i < count; ++i) n_items += (specs[i].N + kRowsCta - 1) / kRowsCta;
-    if (n_items > 0x7fffffffLL || n_ctas < 1) return cudaErrorInvalidValue;
-    if (n_ctas > n_items) n_ctas = static_cast<int32_t>(n_items);
-    out->assign(grouped_plan_bytes(count, n_items, n_ctas), 0);
-    GroupedHeader hdr = {};
-    hdr.count = count;
-    hdr.n_items = static_cast<int32_t>(n_items);
-    hdr.token_tiles = token_tiles;
-    hdr.n_ctas = n_ctas;
-    std::memcpy(out->data(), &hdr, sizeof(hdr));
-    struct Item {
-        int32_t stages;
-        uint2 id;
-    };
-    std::vector<Item> list;
+    if (n_items > 0x7fffffffLL || max_ctas < 1 || sm_count < 1) return cudaErrorInvalidValue;
+    std::vector<GroupedProblem> probs(static_cast<size_t>(count));
+    std::vector<PlanItem> list;
     list.reserve(static_cast<size_t>(n_items));
     for (int32_t i = 0; i < count; ++i) {
         const GroupedSpec& sp = specs[i];
-        GroupedProblem pr;
+        GroupedProblem& pr = probs[static_cast<size_t>(i)];
         std::memset(&pr, 0, sizeof(pr));
         if (cudaError_t e = encode_codes_stage_map(&pr.codes, sp.packed, sp.N, sp.K, kRowsCta, kStageGroups,
                                                    CU_TENSOR_MAP_SWIZZLE_NONE))
             return e;
-        if (cudaError_t e = encode_x_stage_map(&pr.x, sp.x, sp.M, sp.K, 8 * token_tiles, 2 * kStageGroups)) return e;
+        if (cudaError_t e = encode_x_stage_map(&pr.x, sp.x, sp.M, sp.K, token_rows, 2 * kStageGroups)) return e;
         pr.scales = static_cast<const uint16_t*>(sp.scales);
         pr.y = static_cast<__nv_bfloat16*>(sp.y);
         pr.N = sp.N;
         pr.M = static_cast<int32_t>(sp.M);
         pr.G = static_cast<int32_t>(sp.K / 128);
         pr.T = (pr.G + kStageGroups - 1) / kStageGroups;
-        std::memcpy(out->data() + sizeof(GroupedHeader) + sizeof(GroupedProblem) * i, &pr, sizeof(pr));
         const int64_t rbs = (sp.N + kRowsCta - 1) / kRowsCta;
         for (int64_t rb = 0; rb < rbs; ++rb)
             list.push_back({pr.T, make_uint2(static_cast<unsigned>(i), static_cast<unsigned>(rb))});
     }
-    // Longest processing time first: items by cost (stages, plus one for the
-    // item's epilogue) in decreasing order, each to the least-loaded CTA
-    // (lowest index among equals).  Deterministic.
-    std::stable_sort(list.begin(), list.end(), [](const Item& a, const Item& b) { return a.stages > b.stages; });
-    using Load = std::pair<int64_t, int32_t>;  // (work so far, CTA)
-    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
-    for (int32_t c = 0; c < n_ctas; ++c) heap.push({0, c});
-    std::vector<std::vector<uint2>> per_cta(static_cast<size_t>(n_ctas));
-    for (const Item& it : list) {
-        Load l = heap.top();
-        heap.pop();
-        per_cta[static_cast<size_t>(l.second)].push_back(it.id);
-        l.first += it.stages + 1;
-        heap.push(l);
+    std::stable_sort(list.begin(), list.end(), [](const PlanItem& a, const PlanItem& b) { return a.stages > b.stages; });
+    // The grid: every resident CTA, or, where three share an SM, two per SM
+    // when that schedules better.  Three CTAs per SM stream about 5 % faster
+    // than two (3.5–6.6 % measured on the balanced 200-matrix stack at M = 1,
+    // 4, 8), so the modelled time of a grid is its largest CTA load × CTAs per
+    // SM / (1.05 with three, 1 with two).  A layer with a few long items (the
+    // 27B-class down matrix) balances better over fewer, longer-lived CTAs
+    // (there two per SM measured 4–7 % faster than three).
+    const int per_sm = std::max(1, max_ctas / sm_count);
+    int32_t n_ctas = static_cast<int32_t>(std::min<int64_t>(max_ctas, n_items));
+    if (per_sm >= 3) {
+        const int32_t fewer = static_cast<int32_t>(std::min<int64_t>(static_cast<int64_t>(per_sm - 1) * sm_count, n_items));
+        const double t_all = static_cast<double>(schedule_lpt(list, n_ctas, nullptr)) * per_sm / 1.05;
+        const double t_fewer = static_cast<double>(schedule_lpt(list, fewer, nullptr)) * (per_sm - 1);
+        if (t_fewer < t_all) n_ctas = fewer;
     }
+    std::vector<std::vector<uint2>> per_cta;
+    schedule_lpt(list, n_ctas, &per_cta);
+
+    out->assign(grouped_plan_bytes(count, n_items, n_ctas), 0);
+    GroupedHeader hdr = {};
+    hdr.count = count;
+    hdr.n_items = static_cast<int32_t>(n_items);
+    hdr.token_rows = token_rows;
+    hdr.n_ctas = n_ctas;
+    std::memcpy(out->data(), &hdr, sizeof(hdr));
+    std::memcpy(out->data() + sizeof(GroupedHeader), probs.data(), sizeof(GroupedProblem) * probs.size());
     int32_t* first = reinterpret_cast<int32_t*>(out->data() + sizeof(GroupedHeader) + sizeof(GroupedProblem) * count);
     uint2* items = reinterpret_cast<uint2*>(first + ((n_ctas + 2) & ~1));
     // The kernel loads items with 8-byte loads from a 128-byte aligned plan.
@@ -426,14 +487,23 @@ cudaError_t grouped_plan_build(const GroupedSpec* specs, int32_t count, int toke
     return cudaSuccess;
 }
 
-cudaError_t launch_grouped(const void* plan, int32_t n_ctas, int token_tiles, const DeviceInfo& dev,
+cudaError_t launch_grouped(const void* plan, int32_t n_ctas, int token_rows, const DeviceInfo& dev,
                            cudaStream_t stream) {
     if (n_ctas < 1) return cudaSuccess;
-    switch (token_tiles) {
-        case 1: return launch_grouped_t<1, kTpw>(plan, n_ctas, dev, stream);
-        case 2: return launch_grouped_t<2, kTpw>(plan, n_ctas, dev, stream);
-        case 3: return launch_grouped_t<3, kTpw>(plan, n_ctas, dev, stream);
-        default: return launch_grouped_t<4, kTpw>(plan, n_ctas, dev, stream);
+    // A one-tile plan scheduled over at most two CTAs per SM runs the
+    // two-per-SM instance (deeper ring; exactly two fit, so they spread evenly).
+    const bool two = n_ctas <= 2 * dev.sm_count;
+    switch (token_rows) {
+        case 2: return two ? launch_grouped_t<1, 2, 2>(plan, n_ctas, dev, stream)
+                           : launch_grouped_t<1, 2, 3>(plan, n_ctas, dev, stream);
+        case 4: return two ? launch_grouped_t<1, 4, 2>(plan, n_ctas, dev, stream)
+                           : launch_grouped_t<1, 4, 3>(plan, n_ctas, dev, stream);
+        case 8: return two ? launch_grouped_t<1, 8, 2>(plan, n_ctas, dev, stream)
+                           : launch_grouped_t<1, 8, 3>(plan, n_ctas, dev, stream);
+        case 16: return launch_grouped_t<2, 16, 2>(plan, n_ctas, dev, stream);
+        case 24: return launch_grouped_t<3, 24, 2>(plan, n_ctas, dev, stream);
+        case 32: return launch_grouped_t<4, 32, 2>(plan, n_ctas, dev, stream);
+        default: return cudaErrorInvalidValue;
     }
 }
 

@@ -85,17 +85,21 @@ struct GroupedSpec {
 // Plan bytes for `count` problems with `n_items` 64-row blocks in total,
 // scheduled over `n_ctas` CTAs.
 size_t grouped_plan_bytes(int32_t count, int64_t n_items, int32_t n_ctas);
+// Token rows the grouped small-M kernel stages per pass for a largest M of
+// max_m (2, 4, 8, 16, 24 or 32; max_m ≤ 32).
+int grouped_token_rows(int64_t max_m);
 // CTAs the grouped kernel runs with on this device (resident at once).
-int grouped_ctas(int token_tiles, const DeviceInfo& dev);
-// Host image of a grouped plan: tensor maps, and the items assigned to
-// min(n_ctas, items) CTAs longest first.
-cudaError_t grouped_plan_build(const GroupedSpec* specs, int32_t count, int token_tiles, int32_t n_ctas,
-                               std::vector<uint8_t>* out, int64_t* n_items, int32_t* n_ctas_used);
+int grouped_ctas(int token_rows, const DeviceInfo& dev);
+// Host image of a grouped plan: tensor maps, and the items assigned longest
+// first to a grid of at most max_ctas CTAs (sm_count SMs; see the source for
+// how the grid is chosen).
+cudaError_t grouped_plan_build(const GroupedSpec* specs, int32_t count, int token_rows, int32_t max_ctas,
+                               int32_t sm_count, std::vector<uint8_t>* out, int64_t* n_items, int32_t* n_ctas_used);
 // The device address and size of the library's static plan buffer on the
 // current device (w4_gemm_grouped_noalloc).
 cudaError_t static_plan_memory(void** ptr, size_t* bytes);
 // Runs a plan already copied to device memory.
-cudaError_t launch_grouped(const void* plan, int32_t n_ctas, int token_tiles, const DeviceInfo& dev,
+cudaError_t launch_grouped(const void* plan, int32_t n_ctas, int token_rows, const DeviceInfo& dev,
                            cudaStream_t stream);
 
 // Tensor-core grouped plan (problems with M ≥ 17): (problem, 128-row tile,

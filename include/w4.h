@@ -299,7 +299,8 @@ typedef struct w4_grouped_plan {
     int32_t device;      /* CUDA device the plan was built on                     */
     int32_t items;       /* small-M work items (0: no problem with M ≤ 32)        */
     int32_t ctas;        /* CTAs they were scheduled over (the launch grid)       */
-    int32_t token_tiles; /* small-M kernel variant: ceil(largest M / 8), 1..4     */
+    int32_t token_rows;  /* small-M kernel variant: token rows staged per pass,
+                            the smallest of 2, 4, 8, 16, 24, 32 ≥ the largest M  */
     int32_t tc_items;    /* tensor-core work items (0: no problem with M ≥ 33)    */
     int32_t tc_ctas;     /* CTAs they were scheduled over                         */
     int32_t tc_max_bm;   /* widest token tile                                     */

@@ -28,10 +28,15 @@ def make_problems(cuda_lib, shapes, Ms, seed=0):
 SHAPES = [(1, 128), (7, 256), (129, 1152), (200, 4096), (64, 384), (2560, 512), (96, 30720)]
 
 
-@pytest.mark.parametrize("Ms", [[1, 2, 3, 5, 8, 1, 4], [9, 1, 13, 16, 8, 12, 11]])
-def test_grouped_small_problems(cuda_lib, Ms):
-    Ws, probs, bufs = make_problems(cuda_lib, SHAPES, Ms, seed=len(Ms) * Ms[0])
+@pytest.mark.parametrize("Ms,rows", [([1, 2, 3, 5, 8, 1, 4], 8), ([9, 1, 13, 16, 8, 12, 11], 16),
+                                     ([1, 1, 2, 1, 2, 2, 1], 2), ([3, 1, 4, 2, 4, 1, 3], 4),
+                                     ([1, 1, 1, 1, 1, 1, 1], 2)])
+def test_grouped_small_problems(cuda_lib, Ms, rows):
+    """Plans whose largest M selects each one-tile variant of the small-M
+    kernel (2, 4 or 8 token rows staged) and the 16-row variant."""
+    Ws, probs, bufs = make_problems(cuda_lib, SHAPES, Ms, seed=len(Ms) * Ms[0] + sum(Ms))
     plan = w4.w4_grouped_plan(probs)
+    assert plan.plan.token_rows == rows
     w4.w4_gemm_grouped(plan)
     torch.cuda.synchronize()
     assert w4.w4_last_device_status() == 0
@@ -100,7 +105,7 @@ def test_grouped_rejects(cuda_lib):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("M", [1, 5, 13])
+@pytest.mark.parametrize("M", [1, 2, 4, 5, 13, 24, 32])
 def test_grouped_layer27b_sampled(cuda_lib, M):
     shapes = wl.SHAPES["layer27b"]
     Ws, probs = [], []
