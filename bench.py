@@ -341,26 +341,38 @@ def headline(torch, w4, wl, steps, warmup, pk):
     return res
 
 
-def gemm_set(torch, w4, wl, workload, Ms, pk, reps=20, path=None, grouped=False):
+def gemm_set(torch, w4, wl, workload, Ms, pk, reps=20, path=None, grouped=False, fmt=None):
     """Matmul over every matrix of a workload (one launch per matrix, or one
     grouped launch over all of them), per M.  Matrices that fit in L2 several
-    times are rotated over copies."""
+    times are rotated over copies.  fmt = (group, asym) selects an affine
+    format (grouped launches only): codes from w4_quantize_rtn_asym (asym) or
+    w4_quantize_rtn at that group size."""
     dev = torch.device("cuda", torch.cuda.current_device())
     mats = []
     shapes = wl.SHAPES[workload]
     total_packed = sum(n * k // 2 for n, k in shapes)
     copies = 1 if total_packed > 4 * 126e6 else n_copies(torch, total_packed)[0]
     cache = {}
+    zeros_of = {}
+    group, asym = fmt if fmt else (128, False)
     for i, (N, K) in enumerate(shapes):
         key = (N, K) if workload == "stack4b" else i
         if key not in cache:
             W = wl.weight(workload, i, device=dev)
-            cache[key] = w4.w4_quantize_rtn(W)
+            if asym:
+                p_, s_, z_ = w4.w4_quantize_rtn_asym(W, group)
+                cache[key] = (p_, s_)
+                zeros_of[key] = z_
+            else:
+                cache[key] = w4.w4_quantize_rtn(W, group)
             del W
         for c in range(copies):
             p, s = cache[key]
             mats.append((N, K, p.clone() if (copies > 1 or workload == "stack4b") else p,
                          s.clone() if (copies > 1 or workload == "stack4b") else s, i))
+    # every copy gets its own zeros too, so no copy reads L2-resident ones
+    zeros_list = [None if zeros_of.get((N, K) if workload == "stack4b" else i) is None
+                  else zeros_of[(N, K) if workload == "stack4b" else i].clone() for (N, K, _, _, i) in mats]
     cache.clear()
     out = {}
     T = Timer(torch)
@@ -379,9 +391,11 @@ def gemm_set(torch, w4, wl, workload, Ms, pk, reps=20, path=None, grouped=False)
             n_per = len(mats) // copies
             plans = [w4.w4_grouped_plan([(xs[(K, i if workload != "stack4b" else 0)], p, s, ys[j])
                                          for j, (N, K, p, s, i) in enumerate(mats)
-                                         if j % copies == c])
+                                         if j % copies == c], group=group,
+                                        zeros=[zeros_list[j] for j in range(len(mats)) if j % copies == c]
+                                        if asym else None)
                      for c in range(copies)]
-            assert all(len(pl.tensors) == 4 * n_per for pl in plans)
+            assert all(len(pl.tensors) == (5 if asym else 4) * n_per for pl in plans)
 
             def run():
                 for pl in plans:
@@ -396,7 +410,7 @@ def gemm_set(torch, w4, wl, workload, Ms, pk, reps=20, path=None, grouped=False)
                         w4.w4_gemm_ex(x, p, s, out=ys[j], path=path)
 
         g = capture(torch, run)
-        nb = sum(gemm_bytes(M, N, K) for (N, K, _, _, _) in mats) / copies
+        nb = sum(affine_bytes(M, N, K, group, asym) for (N, K, _, _, _) in mats) / copies
         fl = sum(2 * M * N * K for (N, K, _, _, _) in mats) / copies
         t_hbm = nb / (pk["hbm_gbs"] * 1e9)
         t_tc = fl / (tensor_peak(pk) * 1e12)
@@ -768,6 +782,11 @@ def run_gpu(args):
                                                grouped=True)
         if want("stack4b_grouped") and not args.no_sweep:
             sub["stack4b_grouped"] = gemm_set(torch, w4, wl, "stack4b", wl.ROWS["stack4b"], pk, reps=3, grouped=True)
+        if want("affine_grouped"):
+            for group, asym in ((128, True), (32, True)):
+                key = f"layer27b_grouped_g{group}_{'asym' if asym else 'sym'}"
+                sub[key] = gemm_set(torch, w4, wl, "layer27b", [1, 8, 32], pk, reps=10, grouped=True,
+                                    fmt=(group, asym))
 
     if rank != 0:
         return

@@ -47,7 +47,7 @@ class _Plan(ctypes.Structure):
     """w4_grouped_plan of include/w4.h."""
     _fields_ = [("device_plan", _vp), ("bytes", _sz), ("count", _i32), ("device", _i32), ("items", _i32),
                 ("ctas", _i32), ("token_rows", _i32), ("tc_items", _i32), ("tc_ctas", _i32), ("tc_max_bm", _i32),
-                ("tc_offset", _sz)]
+                ("tc_offset", _sz), ("format", _i32)]
 
 _SIGNATURES = {
     "w4_packed_bytes": (_sz, [_i64, _i64]),
@@ -72,6 +72,9 @@ _SIGNATURES = {
     "w4_grouped_plan_init": (ctypes.c_int, [ctypes.POINTER(_Plan), _vp, _sz, _i32, ctypes.POINTER(_Problem)]),
     "w4_gemm_grouped": (ctypes.c_int, [ctypes.POINTER(_Plan), _vp]),
     "w4_gemm_grouped_noalloc": (ctypes.c_int, [_i32, ctypes.POINTER(_Problem), _vp]),
+    "w4_grouped_plan_bytes_affine": (_sz, [_i32, ctypes.POINTER(_Problem), _i32, ctypes.POINTER(_vp)]),
+    "w4_grouped_plan_init_affine": (ctypes.c_int, [ctypes.POINTER(_Plan), _vp, _sz, _i32, ctypes.POINTER(_Problem),
+                                                   _i32, ctypes.POINTER(_vp)]),
 }
 
 
@@ -351,31 +354,54 @@ class GroupedPlan:
         return self.plan.items + self.plan.tc_items
 
 
-def w4_grouped_plan(problems) -> GroupedPlan:
+def w4_grouped_plan(problems, group: int = GROUP, zeros=None) -> GroupedPlan:
     """Plan for many matmuls y_i = Ŵ_i x_i run by one w4_gemm_grouped call.
     problems: sequence of (x, packed, scales, y) CUDA tensors with the shapes
-    of w4_gemm, all on one device."""
+    of w4_gemm, all on one device.  For the affine formats of w4_gemm_affine:
+    group (32, 64 or 128; scales [N, K/group]) and zeros, None or one entry
+    per problem (an int8 [N, K/group] tensor, or None for symmetric codes)."""
     problems = list(problems)
-    arr, n, device = _problem_array(problems)
+    arr, n, device = _problem_array(problems, group)
     tensors = [t for p in problems for t in p]
+    affine = group != GROUP or zeros is not None
+    zarr = None
+    if zeros is not None:
+        zeros = list(zeros)
+        if len(zeros) != n:
+            raise ValueError("zeros needs one entry per problem")
+        zarr = (_vp * n)()
+        for i, (z, (x, packed, _, _)) in enumerate(zip(zeros, problems)):
+            if z is None:
+                continue
+            _cuda_tensor(z, "zeros", torch.int8, 2)
+            if tuple(z.shape) != (packed.shape[0], x.shape[1] // group) or z.device != device:
+                raise ValueError(f"problem {i}: zeros must be int8 [N, K/group] on the problems' device")
+            zarr[i] = z.data_ptr()
+            tensors.append(z)
     with torch.cuda.device(device):
-        nbytes = load().w4_grouped_plan_bytes(n, arr)
-        if nbytes == 0:  # some problem is invalid: let plan_init name the reason
-            probe = torch.empty(256, dtype=torch.uint8, device=device)
-            status = load().w4_grouped_plan_init(ctypes.byref(_Plan()), probe.data_ptr() + (-probe.data_ptr()) % 128,
-                                                 128, n, arr)
-            raise W4Error(status if status != W4_OK else W4_ERR_INVALID_ARG, "w4_grouped_plan")
-        memory = torch.empty(nbytes + 128, dtype=torch.uint8, device=device)
+        if affine:
+            nbytes = load().w4_grouped_plan_bytes_affine(n, arr, int(group), zarr)
+        else:
+            nbytes = load().w4_grouped_plan_bytes(n, arr)
+        size = max(nbytes, 128)
+        memory = torch.empty(size + 128, dtype=torch.uint8, device=device)
         off = (-memory.data_ptr()) % 128
         plan = _Plan()
-        _check(load().w4_grouped_plan_init(ctypes.byref(plan), memory.data_ptr() + off, nbytes, n, arr),
-               "w4_grouped_plan_init")
+        if affine:
+            status = load().w4_grouped_plan_init_affine(ctypes.byref(plan), memory.data_ptr() + off, nbytes, n, arr,
+                                                        int(group), zarr)
+        else:
+            status = load().w4_grouped_plan_init(ctypes.byref(plan), memory.data_ptr() + off, nbytes, n, arr)
+        if status == W4_OK and nbytes == 0:
+            status = W4_ERR_INVALID_ARG
+        _check(status, "w4_grouped_plan_init")
     return GroupedPlan(memory, plan, tensors)
 
 
-def _problem_array(problems):
+def _problem_array(problems, group: int = GROUP):
     """The w4_gemm_problem array of (x, packed, scales, y) tuples, after the
-    shape, dtype and device checks; returns (array, count, device)."""
+    shape, dtype and device checks (scales [N, K/group]); returns (array,
+    count, device)."""
     problems = list(problems)
     if not problems:
         raise ValueError("no problems")
@@ -388,7 +414,7 @@ def _problem_array(problems):
         _cuda_tensor(y, "y", torch.bfloat16, 2)
         M, K = x.shape
         N = packed.shape[0]
-        if tuple(packed.shape) != (N, K // 2) or tuple(scales.shape) != (N, K // GROUP) or tuple(y.shape) != (M, N):
+        if tuple(packed.shape) != (N, K // 2) or tuple(scales.shape) != (N, K // group) or tuple(y.shape) != (M, N):
             raise ValueError(f"problem {i}: x / packed / scales / y shapes disagree")
         if x.device != device or packed.device != device or scales.device != device or y.device != device:
             raise ValueError("all tensors of a grouped call must be on one device")

@@ -323,7 +323,9 @@ size_t round128(size_t v) { return (v + 127) / 128 * 128; }
 
 }  // namespace
 
-size_t w4_grouped_plan_bytes(int32_t count, const w4_gemm_problem* problems) {
+namespace {
+
+size_t grouped_plan_bytes_impl(int32_t count, const w4_gemm_problem* problems) {
     if (count < 1 || !problems) return 0;
     int64_t small_items = 0, tc_items = 0;
     int32_t n_small = 0, n_tc = 0;
@@ -332,7 +334,7 @@ size_t w4_grouped_plan_bytes(int32_t count, const w4_gemm_problem* problems) {
         if (check_grouped_problem(p) != W4_OK) return 0;
         if (is_tensor(p)) {
             ++n_tc;
-            tc_items += tc_grouped_items(GroupedSpec{p.x, p.M, p.N, p.K, p.packed, p.scales, p.y});
+            tc_items += tc_grouped_items(GroupedSpec{p.x, p.M, p.N, p.K, p.packed, p.scales, p.y, nullptr});
         } else {
             ++n_small;
             small_items += (p.N + 63) / 64;
@@ -347,32 +349,40 @@ size_t w4_grouped_plan_bytes(int32_t count, const w4_gemm_problem* problems) {
     return bytes;
 }
 
-namespace {
-
 // Validates the problems (against each other and, when device_memory is not
 // NULL, against the plan memory), builds the plan image and fills every field
-// of *plan except device_plan.
+// of *plan except device_plan.  group: the codes' group size (32, 64, 128);
+// zeros: NULL, or count pointers (each NULL or int8 [N, K/group]).  Group 128
+// without zeros is the symmetric format's own path (format 0).
 int grouped_prepare(const void* device_memory, size_t bytes, int32_t count, const w4_gemm_problem* problems,
-                    std::vector<uint8_t>* image, w4_grouped_plan* plan) {
+                    int32_t group, const void* const* zeros, std::vector<uint8_t>* image, w4_grouped_plan* plan) {
+    if (!valid_group(group)) return W4_ERR_UNSUPPORTED;
+    bool any_zeros = false;
+    for (int32_t i = 0; zeros && i < count; ++i) any_zeros = any_zeros || zeros[i] != nullptr;
+    const int format = group == 128 && !any_zeros ? 0 : group;
     int64_t max_m = 1;
     std::vector<GroupedSpec> small, tc;
     for (int32_t i = 0; i < count; ++i) {
         const w4_gemm_problem& p = problems[i];
         if (const int s = check_grouped_problem(p)) return s;
+        if (p.K % group != 0) return W4_ERR_UNSUPPORTED;
         const size_t yb = out_bytes(p);
         for (int32_t j = 0; j < count; ++j) {
             const w4_gemm_problem& q = problems[j];
+            const void* qz = zeros ? zeros[j] : nullptr;
             const size_t xb = static_cast<size_t>(q.M * q.K) * 2, pb = w4_packed_bytes(q.N, q.K),
-                         sb = w4_scales_bytes(q.N, q.K, 128);
-            if (overlaps(p.y, yb, q.x, xb) || overlaps(p.y, yb, q.packed, pb) || overlaps(p.y, yb, q.scales, sb))
+                         sb = w4_scales_bytes(q.N, q.K, group), zb = qz ? w4_zeros_bytes(q.N, q.K, group) : 0;
+            if (overlaps(p.y, yb, q.x, xb) || overlaps(p.y, yb, q.packed, pb) || overlaps(p.y, yb, q.scales, sb) ||
+                overlaps(p.y, yb, qz, zb))
                 return W4_ERR_INVALID_ARG;
             if (j != i && overlaps(p.y, yb, q.y, out_bytes(q))) return W4_ERR_INVALID_ARG;
             if (device_memory &&
                 (overlaps(device_memory, bytes, q.x, xb) || overlaps(device_memory, bytes, q.packed, pb) ||
-                 overlaps(device_memory, bytes, q.scales, sb) || overlaps(device_memory, bytes, q.y, out_bytes(q))))
+                 overlaps(device_memory, bytes, q.scales, sb) || overlaps(device_memory, bytes, q.y, out_bytes(q)) ||
+                 overlaps(device_memory, bytes, qz, zb)))
                 return W4_ERR_INVALID_ARG;
         }
-        const GroupedSpec sp{p.x, p.M, p.N, p.K, p.packed, p.scales, p.y};
+        const GroupedSpec sp{p.x, p.M, p.N, p.K, p.packed, p.scales, p.y, zeros ? zeros[i] : nullptr};
         if (is_tensor(p)) {
             tc.push_back(sp);
         } else {
@@ -390,17 +400,17 @@ int grouped_prepare(const void* device_memory, size_t bytes, int32_t count, cons
     int32_t n_ctas = 0, n_tc_ctas = 0;
     image->clear();
     if (!small.empty()) {
-        const int ctas = grouped_ctas(token_rows, *dev);
+        const int ctas = grouped_ctas(token_rows, format, *dev);
         if (ctas < 1) return W4_ERR_CUDA;
-        if (grouped_plan_build(small.data(), static_cast<int32_t>(small.size()), token_rows, ctas, dev->sm_count,
-                               image, &n_items, &n_ctas) != cudaSuccess)
+        if (grouped_plan_build(small.data(), static_cast<int32_t>(small.size()), token_rows, format, ctas,
+                               dev->sm_count, image, &n_items, &n_ctas) != cudaSuccess)
             return W4_ERR_CUDA;
         image->resize(round128(image->size()), 0);
     }
     const size_t tc_offset = image->size();
     if (!tc.empty()) {
-        if (tc_grouped_plan_build(tc.data(), static_cast<int32_t>(tc.size()), dev->sm_count, &tc_image, &n_tc_items,
-                                  &n_tc_ctas) != cudaSuccess)
+        if (tc_grouped_plan_build(tc.data(), static_cast<int32_t>(tc.size()), format, dev->sm_count, &tc_image,
+                                  &n_tc_items, &n_tc_ctas) != cudaSuccess)
             return W4_ERR_CUDA;
         image->insert(image->end(), tc_image.begin(), tc_image.end());
     }
@@ -419,18 +429,17 @@ int grouped_prepare(const void* device_memory, size_t bytes, int32_t count, cons
     plan->tc_ctas = n_tc_ctas;
     plan->tc_max_bm = max_bm;
     plan->tc_offset = tc_offset;
+    plan->format = format;
     return W4_OK;
 }
 
-}  // namespace
-
-int w4_grouped_plan_init(w4_grouped_plan* plan, void* device_memory, size_t bytes, int32_t count,
-                         const w4_gemm_problem* problems) {
+int grouped_plan_init_impl(w4_grouped_plan* plan, void* device_memory, size_t bytes, int32_t count,
+                           const w4_gemm_problem* problems, int32_t group, const void* const* zeros) {
     if (!plan || !device_memory || count < 1 || !problems) return W4_ERR_INVALID_ARG;
     if (!aligned(device_memory, 128)) return W4_ERR_MISALIGNED;
     std::vector<uint8_t> image;
     w4_grouped_plan p;
-    if (const int s = grouped_prepare(device_memory, bytes, count, problems, &image, &p)) return s;
+    if (const int s = grouped_prepare(device_memory, bytes, count, problems, group, zeros, &image, &p)) return s;
     if (bytes < image.size()) return W4_ERR_INVALID_ARG;
     if (cudaMemcpy(device_memory, image.data(), image.size(), cudaMemcpyHostToDevice) != cudaSuccess)
         return W4_ERR_CUDA;
@@ -439,10 +448,36 @@ int w4_grouped_plan_init(w4_grouped_plan* plan, void* device_memory, size_t byte
     return W4_OK;
 }
 
+}  // namespace
+
+size_t w4_grouped_plan_bytes(int32_t count, const w4_gemm_problem* problems) {
+    return grouped_plan_bytes_impl(count, problems);
+}
+
+size_t w4_grouped_plan_bytes_affine(int32_t count, const w4_gemm_problem* problems, int32_t group,
+                                    const void* const* zeros) {
+    (void)zeros;  // the plan's size does not depend on the format
+    if (!valid_group(group)) return 0;
+    for (int32_t i = 0; problems && i < count; ++i)
+        if (problems[i].K % group != 0) return 0;
+    return grouped_plan_bytes_impl(count, problems);
+}
+
+int w4_grouped_plan_init(w4_grouped_plan* plan, void* device_memory, size_t bytes, int32_t count,
+                         const w4_gemm_problem* problems) {
+    return grouped_plan_init_impl(plan, device_memory, bytes, count, problems, 128, nullptr);
+}
+
+int w4_grouped_plan_init_affine(w4_grouped_plan* plan, void* device_memory, size_t bytes, int32_t count,
+                                const w4_gemm_problem* problems, int32_t group, const void* const* zeros) {
+    return grouped_plan_init_impl(plan, device_memory, bytes, count, problems, group, zeros);
+}
+
 int w4_gemm_grouped(const w4_grouped_plan* plan, void* stream) {
     if (!plan || !plan->device_plan) return W4_ERR_INVALID_ARG;
     const bool has_small = plan->items > 0, has_tc = plan->tc_items > 0;
     if (!has_small && !has_tc) return W4_ERR_INVALID_ARG;
+    if (plan->format != 0 && !valid_group(plan->format)) return W4_ERR_INVALID_ARG;
     if (has_small && (plan->ctas < 1 || plan->ctas > plan->items ||
                       grouped_token_rows(plan->token_rows) != plan->token_rows))
         return W4_ERR_INVALID_ARG;
@@ -457,10 +492,12 @@ int w4_gemm_grouped(const w4_grouped_plan* plan, void* stream) {
     if (!dev) return W4_ERR_CUDA;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (has_small)
-        if (const int s = to_status(launch_grouped(plan->device_plan, plan->ctas, plan->token_rows, *dev, st))) return s;
+        if (const int s = to_status(
+                launch_grouped(plan->device_plan, plan->ctas, plan->token_rows, plan->format, *dev, st)))
+            return s;
     if (has_tc)
         return to_status(launch_tc_grouped(static_cast<const uint8_t*>(plan->device_plan) + plan->tc_offset,
-                                           plan->tc_ctas, plan->tc_max_bm, *dev, st));
+                                           plan->tc_ctas, plan->tc_max_bm, plan->format, *dev, st));
     return W4_OK;
 }
 
@@ -468,7 +505,7 @@ int w4_gemm_grouped_noalloc(int32_t count, const w4_gemm_problem* problems, void
     if (count < 1 || !problems) return W4_ERR_INVALID_ARG;
     std::vector<uint8_t> image;
     w4_grouped_plan p;
-    if (const int s = grouped_prepare(nullptr, 0, count, problems, &image, &p)) return s;
+    if (const int s = grouped_prepare(nullptr, 0, count, problems, 128, nullptr, &image, &p)) return s;
     void* mem = nullptr;
     size_t cap = 0;
     if (static_plan_memory(&mem, &cap) != cudaSuccess) return W4_ERR_CUDA;

@@ -74,7 +74,7 @@ gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_cons
     constexpr int kConsumers = Warps<TPW>::kConsumers;
     constexpr int kThreads = Warps<TPW>::kThreads;
     // Every weight dequantised to bf16 before its MMA (affine formats, and the
-    // symmetric format at 24 or 32 token rows).
+    // symmetric format at 16 or more token rows).
     constexpr bool kDeq = QG != 0 || Dequant<MT>::value;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -225,7 +225,18 @@ gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_cons
                             d2[rt][h] = d_cur[rt][h] | (d_cur[rt][h] << 16);
                             o2[rt][h] = QG == 0 ? 0x43084308u : (z_cur[rt][h] | (z_cur[rt][h] << 16));
                         }
-                    group_math_affine_lds<MT, TPW>(acc, xw, st + w_off, d2, o2);
+                    if (MT <= 2) {
+                        // Registers allow every row tile's chunks in flight at once.
+                        uint4 wv[TPW][2];
+#pragma unroll
+                        for (int rt = 0; rt < TPW; ++rt) {
+                            wv[rt][0] = lds128(st + w_off + rt * 16 * 64);
+                            wv[rt][1] = lds128(st + w_off + rt * 16 * 64 + 8 * 64);
+                        }
+                        group_math_affine<MT, TPW>(acc, xw, wv, d2, o2);
+                    } else {
+                        group_math_affine_lds<MT, TPW>(acc, xw, st + w_off, d2, o2);
+                    }
                 }
             }
             mbar_arrive(empty(s));

@@ -55,7 +55,8 @@ struct alignas(128) GroupedHeader {
     int32_t n_items;
     int32_t token_rows;   // x rows staged per 64-k block: 2, 4, 8, 16, 24 or 32
     int32_t n_ctas;       // the grid the plan was scheduled for
-    int32_t reserved[28];
+    int32_t format;       // 0: symmetric group 128; 32, 64, 128: affine format of that group size
+    int32_t reserved[27];
 };
 
 struct alignas(128) GroupedProblem {
@@ -67,7 +68,10 @@ struct alignas(128) GroupedProblem {
     int32_t M;
     int32_t G;
     int32_t T;  // stages per item
-    int32_t reserved[23];
+    int32_t pad;
+    const int8_t* zeros;  // affine formats: int8 zero − 8 per group, or null
+    int64_t row_groups;   // scales (and zeros) per row: K / group
+    int32_t reserved[18];
 };
 static_assert(sizeof(GroupedHeader) == 128, "plan header");
 static_assert(sizeof(GroupedProblem) == 384, "plan problem record");
@@ -92,18 +96,24 @@ struct GCfg {
     static constexpr int kXRows = XR;
     static constexpr int kXStageBytes = 2 * kStageGroups * XR * 128;  // [k-block][row][128 B]
     static constexpr int kStageBytes = kCodeStageBytes + kXStageBytes;
-    static constexpr int kCtasPerSm = CPS;
     static constexpr int kBudget = (CPS == 3 ? 74 : 112) * 1024 - 9 * 1024;
     static constexpr int kStages = kBudget / kStageBytes > 5 ? 5 : kBudget / kStageBytes;
     static_assert(XR == 8 * MT || (MT == 1 && (XR == 2 || XR == 4)), "staged rows");
     static_assert(kStages >= 2, "ring depth");
 };
 
-template <int MT, int XR, int CPS>
+// QG: 0 for the symmetric group-128 format; 32, 64 or 128 for the affine
+// formats (group size QG, zero points where a problem has them), which
+// dequantise every weight to bf16(d·(c − z')) as the single-matrix kernel does.
+template <int MT, int XR, int CPS, int QG>
 __global__ void __launch_bounds__(Warps<kTpw>::kThreads, CPS)
 gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
     using C = GCfg<MT, XR, CPS>;
     constexpr int TPW = kTpw;
+    constexpr bool kDeq = QG != 0 || Dequant<MT>::value;
+    // The QG-group holding a thread's 32 codes of a 128-k block (k 32·tig ..
+    // 32·tig + 31) is (128/QG)·g + sub.
+    constexpr int kSub = QG == 0 ? 1 : 128 / QG;
     constexpr int kConsumers = Warps<TPW>::kConsumers;
     constexpr int kCThreads = 32 * kConsumers;
     constexpr int kRedFloats = kStageGroups * kTiles * 4 * 32;
@@ -201,14 +211,19 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
         __nv_bfloat16* const y = pr->y;  // read once: stores to y could alias the record
         const int64_t row0 = static_cast<int64_t>(it.y) * kRowsCta;
         // Scale rows gid / gid+8 of each tile (clamped: rows past N have zero codes).
+        const int sub = QG == 32 ? tig : (QG == 64 ? (tig >> 1) : 0);
+        const int64_t rg = QG == 0 ? G : pr->row_groups;
+        const int8_t* const zeros = QG == 0 ? nullptr : pr->zeros;
         const uint16_t* srow[TPW][2];
+        const int8_t* zrow[TPW][2];
 #pragma unroll
         for (int rt = 0; rt < TPW; ++rt)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 int64_t n = row0 + (tile0 + rt) * 16 + gid + 8 * h;
                 if (n >= N) n = N - 1;
-                srow[rt][h] = pr->scales + n * G;
+                srow[rt][h] = pr->scales + n * rg + sub;
+                zrow[rt][h] = zeros ? zeros + n * rg + sub : nullptr;
             }
         float acc[TPW][MT][4];
 #pragma unroll
@@ -217,21 +232,33 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
                 for (int r = 0; r < 4; ++r) acc[rt][mt][r] = 0.0f;
-        uint32_t d_nxt[TPW][2];
+        // d: scale bits; affine formats also z: bf16 bits of 136 + z'.
+        uint32_t d_nxt[TPW][2], z_nxt[TPW][2];
         auto load_scales = [&](int t) {
             const int g = t * kStageGroups + cw;
+            const bool in = t < T && g < G;
 #pragma unroll
             for (int rt = 0; rt < TPW; ++rt)
 #pragma unroll
-                for (int h = 0; h < 2; ++h) d_nxt[rt][h] = (t < T && g < G) ? __ldg(srow[rt][h] + g) : 0u;
+                for (int h = 0; h < 2; ++h) {
+                    d_nxt[rt][h] = in ? __ldg(srow[rt][h] + g * kSub) : 0u;
+                    if (QG != 0) {
+                        const int zq = in && zrow[rt][h] ? __ldg(zrow[rt][h] + g * kSub) : 0;
+                        z_nxt[rt][h] = static_cast<uint32_t>(0x4308 + zq);  // bf16(136 + z'), z' in [-8, 7]
+                    }
+                }
         };
         load_scales(0);
         for (int t = 0; t < T; ++t) {
-            uint32_t d_cur[TPW][2];
+            uint32_t d_cur[TPW][2], z_cur[TPW][2];
 #pragma unroll
             for (int rt = 0; rt < TPW; ++rt) {
                 d_cur[rt][0] = d_nxt[rt][0];
                 d_cur[rt][1] = d_nxt[rt][1];
+                if (QG != 0) {
+                    z_cur[rt][0] = z_nxt[rt][0];
+                    z_cur[rt][1] = z_nxt[rt][1];
+                }
             }
             load_scales(t + 1);
             if (!aborted) {
@@ -247,7 +274,7 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
                     const uint32_t st = base + s * C::kStageBytes;
                     uint32_t xw[MT][16];
                     load_x_frags<MT, C::kXRows>(xw, st + x_blk, gid, tig);
-                    if (!Dequant<MT>::value) {
+                    if (!kDeq) {
                         uint4 wv[TPW][2];
 #pragma unroll
                         for (int rt = 0; rt < TPW; ++rt) {
@@ -262,9 +289,21 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
 #pragma unroll
                             for (int h = 0; h < 2; ++h) {
                                 d2[rt][h] = d_cur[rt][h] | (d_cur[rt][h] << 16);
-                                o2[rt][h] = 0x43084308u;  // bf16x2 (136, 136): zero point 0
+                                // bf16x2 (136 + z', 136 + z'); z' = 0 for symmetric codes
+                                o2[rt][h] = QG == 0 ? 0x43084308u : (z_cur[rt][h] | (z_cur[rt][h] << 16));
                             }
-                        group_math_affine_lds<MT, TPW>(acc, xw, st + w_off, d2, o2);
+                        if (MT <= 2) {
+                            // Registers allow every row tile's chunks in flight at once.
+                            uint4 wv[TPW][2];
+#pragma unroll
+                            for (int rt = 0; rt < TPW; ++rt) {
+                                wv[rt][0] = lds128(st + w_off + rt * 16 * 64);
+                                wv[rt][1] = lds128(st + w_off + rt * 16 * 64 + 8 * 64);
+                            }
+                            group_math_affine<MT, TPW>(acc, xw, wv, d2, o2);
+                        } else {
+                            group_math_affine_lds<MT, TPW>(acc, xw, st + w_off, d2, o2);
+                        }
                     }
                 }
                 mbar_arrive(empty(s));
@@ -306,16 +345,16 @@ constexpr int grouped_smem_bytes() {
 
 std::mutex g_grouped_mutex;
 
-template <int MT, int XR, int CPS>
+template <int MT, int XR, int CPS, int QG>
 int grouped_ctas_per_sm(int device) {
     static int per_device[64];
     std::lock_guard<std::mutex> lock(g_grouped_mutex);
     if (device < 0 || device >= 64) return 0;
     if (per_device[device] == 0) {
         int v = 0;
-        if (cudaFuncSetAttribute(gemv_grouped_kernel<MT, XR, CPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(gemv_grouped_kernel<MT, XR, CPS, QG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  grouped_smem_bytes<MT, XR, CPS>()) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, gemv_grouped_kernel<MT, XR, CPS>, Warps<kTpw>::kThreads,
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, gemv_grouped_kernel<MT, XR, CPS, QG>, Warps<kTpw>::kThreads,
                                                           grouped_smem_bytes<MT, XR, CPS>()) != cudaSuccess ||
             v < 1) {
             cudaGetLastError();
@@ -326,11 +365,11 @@ int grouped_ctas_per_sm(int device) {
     return per_device[device];
 }
 
-template <int MT, int XR, int CPS>
+template <int MT, int XR, int CPS, int QG>
 cudaError_t launch_grouped_t(const void* plan, int32_t n_ctas, const DeviceInfo& dev, cudaStream_t stream) {
     int device = 0;
     if (cudaError_t e = cudaGetDevice(&device)) return e;
-    if (grouped_ctas_per_sm<MT, XR, CPS>(device) < 1) return cudaErrorInvalidConfiguration;  // sets the smem attribute
+    if (grouped_ctas_per_sm<MT, XR, CPS, QG>(device) < 1) return cudaErrorInvalidConfiguration;  // sets the smem attribute
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(n_ctas), 1, 1);
     cfg.blockDim = dim3(Warps<kTpw>::kThreads, 1, 1);
@@ -341,7 +380,7 @@ cudaError_t launch_grouped_t(const void* plan, int32_t n_ctas, const DeviceInfo&
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_grouped_kernel<MT, XR, CPS>, static_cast<const uint8_t*>(plan), dev.status);
+    return cudaLaunchKernelEx(&cfg, gemv_grouped_kernel<MT, XR, CPS, QG>, static_cast<const uint8_t*>(plan), dev.status);
 }
 
 }  // namespace
@@ -371,19 +410,31 @@ int grouped_token_rows(int64_t max_m) {
     return max_m <= 2 ? 2 : max_m <= 4 ? 4 : max_m <= 8 ? 8 : max_m <= 16 ? 16 : max_m <= 24 ? 24 : 32;
 }
 
-// Resident CTAs per SM of the grouped kernel for these token rows (three for
-// one token tile, two otherwise).
-int grouped_ctas(int token_rows, const DeviceInfo& dev) {
+// Resident CTAs per SM of the grouped kernel for these token rows and format
+// (three for one token tile of the symmetric format, two otherwise).
+template <int QG>
+int grouped_ctas_q(int token_rows, int device) {
+    constexpr int kOne = QG == 0 ? 3 : 2;  // the affine formats run two per SM
+    switch (token_rows) {
+        case 2: return grouped_ctas_per_sm<1, 2, kOne, QG>(device);
+        case 4: return grouped_ctas_per_sm<1, 4, kOne, QG>(device);
+        case 8: return grouped_ctas_per_sm<1, 8, kOne, QG>(device);
+        case 16: return grouped_ctas_per_sm<2, 16, 2, QG>(device);
+        case 24: return grouped_ctas_per_sm<3, 24, 2, QG>(device);
+        case 32: return grouped_ctas_per_sm<4, 32, 2, QG>(device);
+        default: return 0;
+    }
+}
+
+int grouped_ctas(int token_rows, int format, const DeviceInfo& dev) {
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess) return 0;
     int per_sm = 0;
-    switch (token_rows) {
-        case 2: per_sm = grouped_ctas_per_sm<1, 2, 3>(device); break;
-        case 4: per_sm = grouped_ctas_per_sm<1, 4, 3>(device); break;
-        case 8: per_sm = grouped_ctas_per_sm<1, 8, 3>(device); break;
-        case 16: per_sm = grouped_ctas_per_sm<2, 16, 2>(device); break;
-        case 24: per_sm = grouped_ctas_per_sm<3, 24, 2>(device); break;
-        case 32: per_sm = grouped_ctas_per_sm<4, 32, 2>(device); break;
+    switch (format) {
+        case 0: per_sm = grouped_ctas_q<0>(token_rows, device); break;
+        case 32: per_sm = grouped_ctas_q<32>(token_rows, device); break;
+        case 64: per_sm = grouped_ctas_q<64>(token_rows, device); break;
+        case 128: per_sm = grouped_ctas_q<128>(token_rows, device); break;
         default: return 0;
     }
     return per_sm * dev.sm_count;
@@ -418,7 +469,7 @@ int64_t schedule_lpt(const std::vector<PlanItem>& sorted, int32_t n_ctas, std::v
 
 }  // namespace
 
-cudaError_t grouped_plan_build(const GroupedSpec* specs, int32_t count, int token_rows, int32_t max_ctas,
+cudaError_t grouped_plan_build(const GroupedSpec* specs, int32_t count, int token_rows, int format, int32_t max_ctas,
                                int32_t sm_count, std::vector<uint8_t>* out, int64_t* n_items_out,
                                int32_t* n_ctas_out) {
     int64_t n_items = 0;
@@ -441,6 +492,8 @@ cudaError_t grouped_plan_build(const GroupedSpec* specs, int32_t count, int toke
         pr.M = static_cast<int32_t>(sp.M);
         pr.G = static_cast<int32_t>(sp.K / 128);
         pr.T = (pr.G + kStageGroups - 1) / kStageGroups;
+        pr.zeros = static_cast<const int8_t*>(sp.zeros);
+        pr.row_groups = sp.K / (format == 0 ? 128 : format);
         const int64_t rbs = (sp.N + kRowsCta - 1) / kRowsCta;
         for (int64_t rb = 0; rb < rbs; ++rb)
             list.push_back({pr.T, make_uint2(static_cast<unsigned>(i), static_cast<unsigned>(rb))});
@@ -470,6 +523,7 @@ cudaError_t grouped_plan_build(const GroupedSpec* specs, int32_t count, int toke
     hdr.n_items = static_cast<int32_t>(n_items);
     hdr.token_rows = token_rows;
     hdr.n_ctas = n_ctas;
+    hdr.format = format;
     std::memcpy(out->data(), &hdr, sizeof(hdr));
     std::memcpy(out->data() + sizeof(GroupedHeader), probs.data(), sizeof(GroupedProblem) * probs.size());
     int32_t* first = reinterpret_cast<int32_t*>(out->data() + sizeof(GroupedHeader) + sizeof(GroupedProblem) * count);
@@ -487,22 +541,40 @@ cudaError_t grouped_plan_build(const GroupedSpec* specs, int32_t count, int toke
     return cudaSuccess;
 }
 
-cudaError_t launch_grouped(const void* plan, int32_t n_ctas, int token_rows, const DeviceInfo& dev,
+namespace {
+
+template <int QG>
+cudaError_t launch_grouped_q(const void* plan, int32_t n_ctas, int token_rows, const DeviceInfo& dev,
+                             cudaStream_t stream) {
+    // A one-tile plan of the symmetric format scheduled over at most two CTAs
+    // per SM runs the two-per-SM instance (deeper ring; exactly two fit, so
+    // they spread evenly).  The affine formats always run two per SM.
+    const bool two = QG != 0 || n_ctas <= 2 * dev.sm_count;
+    constexpr int kOne = QG == 0 ? 3 : 2;
+    switch (token_rows) {
+        case 2: return two ? launch_grouped_t<1, 2, 2, QG>(plan, n_ctas, dev, stream)
+                           : launch_grouped_t<1, 2, kOne, QG>(plan, n_ctas, dev, stream);
+        case 4: return two ? launch_grouped_t<1, 4, 2, QG>(plan, n_ctas, dev, stream)
+                           : launch_grouped_t<1, 4, kOne, QG>(plan, n_ctas, dev, stream);
+        case 8: return two ? launch_grouped_t<1, 8, 2, QG>(plan, n_ctas, dev, stream)
+                           : launch_grouped_t<1, 8, kOne, QG>(plan, n_ctas, dev, stream);
+        case 16: return launch_grouped_t<2, 16, 2, QG>(plan, n_ctas, dev, stream);
+        case 24: return launch_grouped_t<3, 24, 2, QG>(plan, n_ctas, dev, stream);
+        case 32: return launch_grouped_t<4, 32, 2, QG>(plan, n_ctas, dev, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_grouped(const void* plan, int32_t n_ctas, int token_rows, int format, const DeviceInfo& dev,
                            cudaStream_t stream) {
     if (n_ctas < 1) return cudaSuccess;
-    // A one-tile plan scheduled over at most two CTAs per SM runs the
-    // two-per-SM instance (deeper ring; exactly two fit, so they spread evenly).
-    const bool two = n_ctas <= 2 * dev.sm_count;
-    switch (token_rows) {
-        case 2: return two ? launch_grouped_t<1, 2, 2>(plan, n_ctas, dev, stream)
-                           : launch_grouped_t<1, 2, 3>(plan, n_ctas, dev, stream);
-        case 4: return two ? launch_grouped_t<1, 4, 2>(plan, n_ctas, dev, stream)
-                           : launch_grouped_t<1, 4, 3>(plan, n_ctas, dev, stream);
-        case 8: return two ? launch_grouped_t<1, 8, 2>(plan, n_ctas, dev, stream)
-                           : launch_grouped_t<1, 8, 3>(plan, n_ctas, dev, stream);
-        case 16: return launch_grouped_t<2, 16, 2>(plan, n_ctas, dev, stream);
-        case 24: return launch_grouped_t<3, 24, 2>(plan, n_ctas, dev, stream);
-        case 32: return launch_grouped_t<4, 32, 2>(plan, n_ctas, dev, stream);
+    switch (format) {
+        case 0: return launch_grouped_q<0>(plan, n_ctas, token_rows, dev, stream);
+        case 32: return launch_grouped_q<32>(plan, n_ctas, token_rows, dev, stream);
+        case 64: return launch_grouped_q<64>(plan, n_ctas, token_rows, dev, stream);
+        case 128: return launch_grouped_q<128>(plan, n_ctas, token_rows, dev, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -49,7 +49,8 @@ struct alignas(128) TcHeader {
     int32_t n_items;
     int32_t n_ctas;
     int32_t max_bm;
-    int32_t reserved[28];
+    int32_t format;  // 0: symmetric group 128; 32, 64, 128: affine format of that group size
+    int32_t reserved[27];
 };
 
 struct alignas(128) TcProblem {
@@ -62,7 +63,10 @@ struct alignas(128) TcProblem {
     int32_t G;
     int32_t nkb;  // k stages (groups)
     int32_t bm;   // token rows per tile (multiple of 16, ≤ 256)
-    int32_t reserved[21];
+    int32_t pad;
+    const int8_t* zeros;  // affine formats: int8 zero − 8 per group, or null
+    int64_t row_groups;   // scales (and zeros) per row: K / group
+    int32_t reserved[16];
 };
 static_assert(sizeof(TcHeader) == 128, "plan header");
 static_assert(sizeof(TcProblem) == 384, "plan problem record");
@@ -73,10 +77,25 @@ __device__ __forceinline__ uint32_t deq_pair(uint32_t word, int i, __nv_bfloat16
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Affine formats: d·(c − z') for the pair i of a code word, as bf16x2:
+// (136 + c) − (136 + z') is exact, the product rounds once.  off2 =
+// bf16x2(136 + z'), d2 = bf16x2(d).
+__device__ __forceinline__ uint32_t deq_pair_affine(uint32_t word, int i, uint32_t off2, uint32_t d2) {
+    const uint32_t biased = ((word >> (4 * i)) & 0x000F000Fu) ^ 0x43084308u;
+    uint32_t r;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(biased), "r"(off2));
+    asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(r) : "r"(d2));
+    return r;
+}
+
 __device__ __forceinline__ void tensormap_acquire(const void* map) {
     asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
 }
 
+// QG: 0 for the symmetric group-128 format; 32, 64 or 128 for the affine
+// formats (group size QG, zero points where a problem has them).  Only the
+// dequantisers' scale (and zero) reads differ.
+template <int QG>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
     extern __shared__ uint8_t smem_raw[];
@@ -261,13 +280,34 @@ gemm_tc_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
             const int64_t n0 = static_cast<int64_t>(items[i].y) * kBN;
             const int64_t m0 = static_cast<int64_t>(items[i].z) * bm;
             const int64_t n = n0 + t < pr->N ? n0 + t : pr->N - 1;  // padding rows: zero codes, valid scale
-            const uint16_t* srow = pr->scales + n * pr->G;
+            const int64_t rg = QG == 0 ? pr->G : pr->row_groups;
+            const uint16_t* srow = pr->scales + n * rg;
+            const int8_t* zrow = QG != 0 && pr->zeros ? pr->zeros + n * rg : nullptr;
+            // The QG-group of this thread's first 32 k of group kb (its second
+            // 32 k are in the next one at QG = 32).
+            auto gidx = [&](int kb) {
+                return QG == 0 ? kb : kb * (128 / QG) + (QG == 64 ? half : (QG == 32 ? 2 * half : 0));
+            };
+            auto zbits = [&](int i) { return static_cast<uint32_t>(0x4308 + (zrow ? __ldg(zrow + i) : 0)); };
             if (ok) {
-                uint32_t d_next = __ldg(srow);
+                uint32_t d_next = __ldg(srow + gidx(0));
+                uint32_t d_next_b = QG == 32 ? __ldg(srow + gidx(0) + 1) : d_next;
+                uint32_t z_next = QG != 0 ? zbits(gidx(0)) : 0u;
+                uint32_t z_next_b = QG == 32 ? zbits(gidx(0) + 1) : z_next;
                 for (int kb = 0; kb < nkb; ++kb) {
                     const int sub = kb & 1;  // group within the code stage
-                    const uint32_t dbits = d_next;
-                    if (kb + 1 < nkb) d_next = __ldg(srow + kb + 1);
+                    const uint32_t dbits = d_next, dbits_b = d_next_b, zb0 = z_next, zb1 = z_next_b;
+                    if (kb + 1 < nkb) {
+                        const int ia = gidx(kb + 1);
+                        d_next = __ldg(srow + ia);
+                        if (QG == 32) d_next_b = __ldg(srow + ia + 1);
+                        if (QG != 0) z_next = zbits(ia);
+                        if (QG == 32) z_next_b = zbits(ia + 1);
+                        if (QG != 0 && QG != 32) {
+                            d_next_b = d_next;
+                            z_next_b = z_next;
+                        }
+                    }
                     const bool have = mbar_wait(code_full(c), cph);
                     if (!__all_sync(0xffffffffu, have)) {
                         ok = false;
@@ -277,13 +317,24 @@ gemm_tc_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
                     const uint4 q0 = lds128(grp + (((2u * half) ^ sw) << 4));
                     const uint4 q1 = lds128(grp + (((2u * half + 1u) ^ sw) << 4));
                     const uint32_t d2bits = dbits | (dbits << 16);
-                    const __nv_bfloat162 d2 = *reinterpret_cast<const __nv_bfloat162*>(&d2bits);
                     const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
                     uint32_t v[32];
+                    if (QG == 0) {
+                        const __nv_bfloat162 d2 = *reinterpret_cast<const __nv_bfloat162*>(&d2bits);
 #pragma unroll
-                    for (int w = 0; w < 8; ++w)
+                        for (int w = 0; w < 8; ++w)
 #pragma unroll
-                        for (int p = 0; p < 4; ++p) v[4 * w + p] = deq_pair(words[w], p, d2);
+                            for (int p = 0; p < 4; ++p) v[4 * w + p] = deq_pair(words[w], p, d2);
+                    } else {
+                        // words 0..3: the first 32 k (d, z of gidx), words 4..7: the next 32.
+                        const uint32_t d2b = dbits_b | (dbits_b << 16);
+                        const uint32_t o2a = zb0 | (zb0 << 16), o2b = zb1 | (zb1 << 16);
+#pragma unroll
+                        for (int w = 0; w < 8; ++w)
+#pragma unroll
+                            for (int p = 0; p < 4; ++p)
+                                v[4 * w + p] = deq_pair_affine(words[w], p, w < 4 ? o2a : o2b, w < 4 ? d2bits : d2b);
+                    }
                     // Release the code slot only after its words have been used
                     // (the shared-memory load may still be pending at an arrive).
                     mbar_arrive(code_empty(c));
@@ -372,7 +423,6 @@ int tc_grouped_smem_bytes(int max_bm) {
 }
 
 std::mutex g_tc_grouped_mutex;
-bool g_tc_attr[64];
 
 }  // namespace
 
@@ -386,8 +436,8 @@ int64_t tc_grouped_items(const GroupedSpec& sp) {
     return ((sp.N + kBN - 1) / kBN) * m_tiles;
 }
 
-cudaError_t tc_grouped_plan_build(const GroupedSpec* specs, int32_t count, int32_t n_ctas, std::vector<uint8_t>* out,
-                                  int64_t* n_items_out, int32_t* n_ctas_out) {
+cudaError_t tc_grouped_plan_build(const GroupedSpec* specs, int32_t count, int format, int32_t n_ctas,
+                                  std::vector<uint8_t>* out, int64_t* n_items_out, int32_t* n_ctas_out) {
     int64_t n_items = 0;
     for (int32_t i = 0; i < count; ++i) n_items += tc_grouped_items(specs[i]);
     if (n_items > 0x7fffffffLL || n_ctas < 1) return cudaErrorInvalidValue;
@@ -397,6 +447,7 @@ cudaError_t tc_grouped_plan_build(const GroupedSpec* specs, int32_t count, int32
     hdr.count = count;
     hdr.n_items = static_cast<int32_t>(n_items);
     hdr.n_ctas = n_ctas;
+    hdr.format = format;
     struct Item {
         int32_t cost;
         uint4 id;
@@ -422,6 +473,8 @@ cudaError_t tc_grouped_plan_build(const GroupedSpec* specs, int32_t count, int32
         pr.G = static_cast<int32_t>(sp.K / 128);
         pr.nkb = static_cast<int32_t>(sp.K / kBK);  // groups
         pr.bm = static_cast<int32_t>(bm);
+        pr.zeros = static_cast<const int8_t*>(sp.zeros);
+        pr.row_groups = sp.K / (format == 0 ? 128 : format);
         std::memcpy(out->data() + sizeof(TcHeader) + sizeof(TcProblem) * i, &pr, sizeof(pr));
         const int64_t n_tiles = (sp.N + kBN - 1) / kBN;
         // Cost of a tile: its k stages, each 8 MMAs of N = bm, plus its epilogue.
@@ -460,21 +513,25 @@ cudaError_t tc_grouped_plan_build(const GroupedSpec* specs, int32_t count, int32
     return cudaSuccess;
 }
 
-cudaError_t launch_tc_grouped(const void* plan, int32_t n_ctas, int max_bm, const DeviceInfo& dev,
-                              cudaStream_t stream) {
-    if (n_ctas < 1) return cudaSuccess;
+namespace {
+
+template <int QG>
+cudaError_t launch_tc_grouped_q(const void* plan, int32_t n_ctas, int max_bm, const DeviceInfo& dev,
+                                cudaStream_t stream) {
     const int smem = tc_grouped_smem_bytes(max_bm);
     if (smem > dev.max_smem_optin) return cudaErrorInvalidConfiguration;
     int device = 0;
     if (cudaError_t e = cudaGetDevice(&device)) return e;
     {
+        static bool attr_set[64];
         std::lock_guard<std::mutex> lock(g_tc_grouped_mutex);
         if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
-        if (!g_tc_attr[device]) {
-            if (cudaError_t e = cudaFuncSetAttribute(gemm_tc_grouped_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (!attr_set[device]) {
+            if (cudaError_t e = cudaFuncSetAttribute(gemm_tc_grouped_kernel<QG>,
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                      tc_grouped_smem_bytes(kMaxBM)))
                 return e;
-            g_tc_attr[device] = true;
+            attr_set[device] = true;
         }
     }
     cudaLaunchConfig_t cfg = {};
@@ -487,7 +544,21 @@ cudaError_t launch_tc_grouped(const void* plan, int32_t n_ctas, int max_bm, cons
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_tc_grouped_kernel, static_cast<const uint8_t*>(plan), dev.status);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_grouped_kernel<QG>, static_cast<const uint8_t*>(plan), dev.status);
+}
+
+}  // namespace
+
+cudaError_t launch_tc_grouped(const void* plan, int32_t n_ctas, int max_bm, int format, const DeviceInfo& dev,
+                              cudaStream_t stream) {
+    if (n_ctas < 1) return cudaSuccess;
+    switch (format) {
+        case 0: return launch_tc_grouped_q<0>(plan, n_ctas, max_bm, dev, stream);
+        case 32: return launch_tc_grouped_q<32>(plan, n_ctas, max_bm, dev, stream);
+        case 64: return launch_tc_grouped_q<64>(plan, n_ctas, max_bm, dev, stream);
+        case 128: return launch_tc_grouped_q<128>(plan, n_ctas, max_bm, dev, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace w4

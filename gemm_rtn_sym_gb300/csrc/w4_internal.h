@@ -74,13 +74,15 @@ cudaError_t encode_x_stage_map(CUtensorMap* map, const void* x, int64_t M, int64
 cudaError_t encode_codes_stage_map(CUtensorMap* map, const void* packed, int64_t N, int64_t K, int rows,
                                    int groups, CUtensorMapSwizzle swizzle);
 
-// One problem of a grouped matmul (validated by the C ABI layer).
+// One problem of a grouped matmul (validated by the C ABI layer).  zeros:
+// int8 zero − 8 per group of the affine formats, or null.
 struct GroupedSpec {
     const void* x;
     int64_t M, N, K;
     const void* packed;
     const void* scales;
     void* y;
+    const void* zeros;
 };
 // Plan bytes for `count` problems with `n_items` 64-row blocks in total,
 // scheduled over `n_ctas` CTAs.
@@ -89,26 +91,27 @@ size_t grouped_plan_bytes(int32_t count, int64_t n_items, int32_t n_ctas);
 // max_m (2, 4, 8, 16, 24 or 32; max_m ≤ 32).
 int grouped_token_rows(int64_t max_m);
 // CTAs the grouped kernel runs with on this device (resident at once).
-int grouped_ctas(int token_rows, const DeviceInfo& dev);
+// format: 0 for the symmetric group-128 format, else the affine group size.
+int grouped_ctas(int token_rows, int format, const DeviceInfo& dev);
 // Host image of a grouped plan: tensor maps, and the items assigned longest
 // first to a grid of at most max_ctas CTAs (sm_count SMs; see the source for
 // how the grid is chosen).
-cudaError_t grouped_plan_build(const GroupedSpec* specs, int32_t count, int token_rows, int32_t max_ctas,
+cudaError_t grouped_plan_build(const GroupedSpec* specs, int32_t count, int token_rows, int format, int32_t max_ctas,
                                int32_t sm_count, std::vector<uint8_t>* out, int64_t* n_items, int32_t* n_ctas_used);
 // The device address and size of the library's static plan buffer on the
 // current device (w4_gemm_grouped_noalloc).
 cudaError_t static_plan_memory(void** ptr, size_t* bytes);
 // Runs a plan already copied to device memory.
-cudaError_t launch_grouped(const void* plan, int32_t n_ctas, int token_rows, const DeviceInfo& dev,
+cudaError_t launch_grouped(const void* plan, int32_t n_ctas, int token_rows, int format, const DeviceInfo& dev,
                            cudaStream_t stream);
 
 // Tensor-core grouped plan (problems with M ≥ 17): (problem, 128-row tile,
 // token tile) items scheduled longest first over one CTA per SM.
 size_t tc_grouped_plan_bytes(int32_t count, int64_t n_items, int32_t n_ctas);
 int64_t tc_grouped_items(const GroupedSpec& sp);
-cudaError_t tc_grouped_plan_build(const GroupedSpec* specs, int32_t count, int32_t n_ctas, std::vector<uint8_t>* out,
-                                  int64_t* n_items, int32_t* n_ctas_used);
-cudaError_t launch_tc_grouped(const void* plan, int32_t n_ctas, int max_bm, const DeviceInfo& dev,
+cudaError_t tc_grouped_plan_build(const GroupedSpec* specs, int32_t count, int format, int32_t n_ctas,
+                                  std::vector<uint8_t>* out, int64_t* n_items, int32_t* n_ctas_used);
+cudaError_t launch_tc_grouped(const void* plan, int32_t n_ctas, int max_bm, int format, const DeviceInfo& dev,
                               cudaStream_t stream);
 
 cudaError_t launch_wait_probe(int64_t spin_limit, int arrive, const DeviceInfo& dev,

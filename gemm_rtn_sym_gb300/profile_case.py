@@ -5,6 +5,7 @@
     python -m gemm_rtn_sym_gb300.profile_case gemm --workload outlier --M 8
     python -m gemm_rtn_sym_gb300.profile_case gemm --workload layer70b --matrix 2 --M 208
     python -m gemm_rtn_sym_gb300.profile_case grouped --workload layer27b --M 1
+    python -m gemm_rtn_sym_gb300.profile_case grouped --workload layer27b --M 1 --group 128 --asym
     python -m gemm_rtn_sym_gb300.profile_case quantize --workload outlier --group 32 --asym
     python -m gemm_rtn_sym_gb300.profile_case gemm --workload outlier --M 8 --group 32 --asym
     python -m gemm_rtn_sym_gb300.profile_case gptq --workload ffn
@@ -50,14 +51,18 @@ def main(argv=None) -> int:
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     if a.kernel == "grouped":
-        problems = []
+        problems, zeros = [], []
         for i, (N, K) in enumerate(wl.SHAPES[a.workload]):
             W = wl.weight(a.workload, i, device=dev)
-            packed, scales = w4_quantize_rtn(W)
+            if a.asym:
+                packed, scales, z = w4_quantize_rtn_asym(W, a.group)
+                zeros.append(z)
+            else:
+                packed, scales = w4_quantize_rtn(W, a.group)
             del W
             x = wl.activations(a.workload, a.M, K, i, device=dev)
             problems.append((x, packed, scales, torch.empty((a.M, N), dtype=torch.bfloat16, device=dev)))
-        plan = w4_grouped_plan(problems)
+        plan = w4_grouped_plan(problems, group=a.group, zeros=zeros if a.asym else None)
         for _ in range(a.launches):
             w4_gemm_grouped(plan)
         torch.cuda.synchronize()

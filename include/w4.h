@@ -305,6 +305,8 @@ typedef struct w4_grouped_plan {
     int32_t tc_ctas;     /* CTAs they were scheduled over                         */
     int32_t tc_max_bm;   /* widest token tile                                     */
     size_t tc_offset;    /* byte offset of the tensor-core part of the plan       */
+    int32_t format;      /* 0: symmetric group 128 (w4_gemm); 32, 64, 128: the
+                            affine formats of w4_gemm_affine at that group size   */
 } w4_grouped_plan;
 
 /* Device bytes a plan for these problems needs (0 if any problem is invalid);
@@ -318,6 +320,26 @@ size_t w4_grouped_plan_bytes(int32_t count, const w4_gemm_problem* problems);
  * library keeps no reference to `problems` afterwards. */
 int w4_grouped_plan_init(w4_grouped_plan* plan, void* device_memory, size_t bytes,
                          int32_t count, const w4_gemm_problem* problems);
+
+/*
+ * Grouped matmul over the affine formats of w4_gemm_affine (study §1 equation
+ * with a free zero point; §2 settings table: smaller groups): every problem of
+ * the plan stores its codes at one group size.
+ *   group  in : 32, 64 or 128 (each problem's scales are bf16 [N, K/group])
+ *   zeros  in : NULL (no problem has zero points), or `count` pointers, each
+ *               NULL (symmetric codes) or problem i's int8 [N, K/group] zeros
+ *               from w4_quantize_rtn_asym (any alignment)
+ * Each problem is computed as by w4_gemm_affine's kernel for its M (M ≤ 32:
+ * the small-M kernel, M ≥ 33: the tensor-core kernel), within the same
+ * bound; group 128 without zeros is exactly w4_grouped_plan_init.  The plan
+ * runs with w4_gemm_grouped; sizes, checks and errors as above (zeros must
+ * not overlap any output).
+ */
+size_t w4_grouped_plan_bytes_affine(int32_t count, const w4_gemm_problem* problems,
+                                    int32_t group, const void* const* zeros);
+int w4_grouped_plan_init_affine(w4_grouped_plan* plan, void* device_memory, size_t bytes,
+                                int32_t count, const w4_gemm_problem* problems,
+                                int32_t group, const void* const* zeros);
 
 /* Runs every problem of the plan on `stream` (the device must be the one the
  * plan was built on).  Asynchronous; no allocation. */

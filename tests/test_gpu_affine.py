@@ -184,3 +184,64 @@ def test_gemm_affine_unaligned_scales_and_zeros(cuda_lib, group):
             b = cuda_lib.w4_gemm_affine(x, packed, s_odd, z_odd, group=group, path=path)
             torch.cuda.synchronize()
             assert torch.equal(a.view(torch.int16), b.view(torch.int16)), (M, path)
+
+
+GROUPED_SHAPES = [(300, 1152), (7, 256), (129, 2560), (64, 384), (1000, 512)]
+
+
+@pytest.mark.parametrize("group,asym", FORMATS)
+@pytest.mark.parametrize("Ms", [[1, 2, 1, 2, 1], [8, 3, 5, 1, 7], [16, 9, 13, 4, 2], [24, 32, 17, 1, 30],
+                                [40, 208, 33, 8, 1]])
+def test_grouped_affine_parity(cuda_lib, group, asym, Ms):
+    """The grouped matmul over the affine formats (w4_grouped_plan_init_affine):
+    every problem within the parity bound of the oracle's dequantised matmul
+    with its zeros, on plans that select every small-M variant (2 to 32 token
+    rows staged) and mix in the tensor-core kernel (M ≥ 33); repeat runs
+    bit-identical."""
+    probs, refs, zs = [], [], []
+    for i, ((N, K), M) in enumerate(zip(GROUPED_SHAPES, Ms)):
+        W = wl.random_bf16((N, K), 0.02, seed=40 + 7 * i + group, device=DEV)
+        x = wl.random_bf16((M, K), 1.0, seed=90 + M + i, device=DEV)
+        packed, scales, zeros = quantize_gpu(cuda_lib, W, group, asym)
+        # one problem without zeros in an asymmetric plan: symmetric codes there
+        if asym and i == 3:
+            packed, scales, zeros = quantize_gpu(cuda_lib, W, group, False)
+        y, ybuf = guarded((M, N), torch.bfloat16, DEV)
+        probs.append((x, packed, scales, y))
+        zs.append(zeros)
+        Wb = wl.bits(W)
+        if zeros is not None:
+            p_ref, s_ref, z_ref = O.quantize_rtn_asym(Wb, group)
+        else:
+            (p_ref, s_ref), z_ref = O.quantize_rtn(Wb, group), None
+        refs.append((O.gemm_reference(wl.bits(x), p_ref, s_ref, K, group, z_ref), ybuf))
+    plan = cuda_lib.w4_grouped_plan(probs, group=group, zeros=zs if asym else None)
+    assert plan.plan.format == group
+    cuda_lib.w4_gemm_grouped(plan)
+    torch.cuda.synchronize()
+    assert cuda_lib.w4_last_device_status() == 0
+    first = []
+    for (x, _, _, y), ((y_ref, s_abs), ybuf) in zip(probs, refs):
+        assert guards_intact(ybuf), "grouped matmul wrote outside an output"
+        excess = O.parity_excess(wl.bits(y), y_ref, s_abs)
+        assert float(excess.max()) <= 1.0, float(excess.max())
+        first.append(y.clone())
+    cuda_lib.w4_gemm_grouped(plan)
+    torch.cuda.synchronize()
+    for f, (_, _, _, y) in zip(first, probs):
+        assert torch.equal(f.view(torch.int16), y.view(torch.int16))
+
+
+def test_grouped_affine_group128_without_zeros_is_the_symmetric_plan(cuda_lib):
+    W = wl.random_bf16((500, 2048), 0.02, seed=3, device=DEV)
+    x = wl.random_bf16((5, 2048), 1.0, seed=4, device=DEV)
+    packed, scales, _ = quantize_gpu(cuda_lib, W, 128, False)
+    y0 = torch.empty((5, 500), dtype=torch.bfloat16, device=DEV)
+    y1 = torch.empty_like(y0)
+    p0 = cuda_lib.w4_grouped_plan([(x, packed, scales, y0)])
+    p1 = cuda_lib.w4_grouped_plan([(x, packed, scales, y1)], group=128, zeros=[None])
+    assert p0.plan.format == 0 and p1.plan.format == 0
+    cuda_lib.w4_gemm_grouped(p0)
+    cuda_lib.w4_gemm_grouped(p1)
+    torch.cuda.synchronize()
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
