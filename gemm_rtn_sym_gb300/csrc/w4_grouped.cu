@@ -102,14 +102,24 @@ struct GCfg {
     static_assert(kStages >= 2, "ring depth");
 };
 
+// Row tiles per consumer warp: four, except for the affine formats up to 16
+// token rows, whose per-tile (d, z') pairs and dequantising arithmetic run
+// better over eight warps of two tiles (as in the single-matrix kernel: on the
+// 27B-class layer asymmetric group 128 took 62 against 95 µs at M = 1 and 94
+// against 122 µs at M = 16).
+template <int MT, int QG>
+struct GTpw {
+    static constexpr int value = QG != 0 && MT <= 2 ? 2 : kTpw;
+};
+
 // QG: 0 for the symmetric group-128 format; 32, 64 or 128 for the affine
 // formats (group size QG, zero points where a problem has them), which
 // dequantise every weight to bf16(d·(c − z')) as the single-matrix kernel does.
 template <int MT, int XR, int CPS, int QG>
-__global__ void __launch_bounds__(Warps<kTpw>::kThreads, CPS)
+__global__ void __launch_bounds__(Warps<GTpw<MT, QG>::value>::kThreads, CPS)
 gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
     using C = GCfg<MT, XR, CPS>;
-    constexpr int TPW = kTpw;
+    constexpr int TPW = GTpw<MT, QG>::value;
     constexpr bool kDeq = QG != 0 || Dequant<MT>::value;
     // The QG-group holding a thread's 32 codes of a 128-k block (k 32·tig ..
     // 32·tig + 31) is (128/QG)·g + sub.
@@ -354,7 +364,8 @@ int grouped_ctas_per_sm(int device) {
         int v = 0;
         if (cudaFuncSetAttribute(gemv_grouped_kernel<MT, XR, CPS, QG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  grouped_smem_bytes<MT, XR, CPS>()) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, gemv_grouped_kernel<MT, XR, CPS, QG>, Warps<kTpw>::kThreads,
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, gemv_grouped_kernel<MT, XR, CPS, QG>,
+                                                          Warps<GTpw<MT, QG>::value>::kThreads,
                                                           grouped_smem_bytes<MT, XR, CPS>()) != cudaSuccess ||
             v < 1) {
             cudaGetLastError();
@@ -372,7 +383,7 @@ cudaError_t launch_grouped_t(const void* plan, int32_t n_ctas, const DeviceInfo&
     if (grouped_ctas_per_sm<MT, XR, CPS, QG>(device) < 1) return cudaErrorInvalidConfiguration;  // sets the smem attribute
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(n_ctas), 1, 1);
-    cfg.blockDim = dim3(Warps<kTpw>::kThreads, 1, 1);
+    cfg.blockDim = dim3(Warps<GTpw<MT, QG>::value>::kThreads, 1, 1);
     cfg.dynamicSmemBytes = grouped_smem_bytes<MT, XR, CPS>();
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
