@@ -91,51 +91,69 @@ __device__ __forceinline__ void load_x_frags(uint32_t (&xw)[MT][16], uint32_t st
     }
 }
 
+// Word w (0..3) of a 16-byte chunk.
+__device__ __forceinline__ uint32_t word_of(const uint4 v, int w) {
+    return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
+}
+
+// The biased A fragment of k-step 2w + H from word w of rows gid (wa) and
+// gid + 8 (wb): pairs 2H and 2H + 1 of each word.
+template <int H>
+__device__ __forceinline__ void biased_frag(uint32_t wa, uint32_t wb, uint32_t (&f)[4]) {
+    f[0] = biased_pair<2 * H>(wa);
+    f[1] = biased_pair<2 * H>(wb);
+    f[2] = biased_pair<2 * H + 1>(wa);
+    f[3] = biased_pair<2 * H + 1>(wb);
+}
+
 // One group of one stage for TPW row tiles: acc += d · (Σ (136 + q)·x − 136·Σx).
+// The k-steps run outermost and the row tiles inside them, so an MMA's
+// accumulator was last written TPW MMAs earlier (tile-by-tile order chained
+// eight dependent MMAs; this order measured 2–5 % faster on the grouped
+// layers), and the −136·Σx chain is added at the end instead of seeding
+// every tile.
 template <int MT, int TPW>
 __device__ __forceinline__ void group_math(float (&acc)[TPW][MT][4], const uint32_t (&xw)[MT][16],
                                            const uint4 (&wv)[TPW][2], const uint32_t (&dbits)[TPW][2]) {
-    // −136·Σ_k x[m, k] over this group, identical for every row.
-    float corr[MT][4];
+    float corr[MT][4];  // −136·Σ_k x[m, k] over this group, identical for every row
+    float cg[TPW][MT][4];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
+    for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-        for (int r = 0; r < 4; ++r) corr[mt][r] = 0.0f;
+        for (int r = 0; r < 4; ++r) {
+            corr[mt][r] = 0.0f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-            mma_bf16_16816(corr[mt], kMinus136x2, kMinus136x2, kMinus136x2, kMinus136x2, xw[mt][2 * k],
-                           xw[mt][2 * k + 1]);
+            for (int rt = 0; rt < TPW; ++rt) cg[rt][mt][r] = 0.0f;
+        }
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+        const int w = ks >> 1;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+            mma_bf16_16816(corr[mt], kMinus136x2, kMinus136x2, kMinus136x2, kMinus136x2, xw[mt][2 * ks],
+                           xw[mt][2 * ks + 1]);
+#pragma unroll
+        for (int rt = 0; rt < TPW; ++rt) {
+            uint32_t f[4];
+            if (ks & 1)
+                biased_frag<1>(word_of(wv[rt][0], w), word_of(wv[rt][1], w), f);
+            else
+                biased_frag<0>(word_of(wv[rt][0], w), word_of(wv[rt][1], w), f);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+                mma_bf16_16816(cg[rt][mt], f[0], f[1], f[2], f[3], xw[mt][2 * ks], xw[mt][2 * ks + 1]);
+        }
     }
 #pragma unroll
     for (int rt = 0; rt < TPW; ++rt) {
-        float cg[MT][4];
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) cg[mt][r] = corr[mt][r];
-        const uint32_t wa[4] = {wv[rt][0].x, wv[rt][0].y, wv[rt][0].z, wv[rt][0].w};
-        const uint32_t wb[4] = {wv[rt][1].x, wv[rt][1].y, wv[rt][1].z, wv[rt][1].w};
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            // k-steps 2w (pairs 0, 1 of word w) and 2w+1 (pairs 2, 3).
-            const uint32_t a0 = biased_pair<0>(wa[w]), a2 = biased_pair<1>(wa[w]);
-            const uint32_t a1 = biased_pair<0>(wb[w]), a3 = biased_pair<1>(wb[w]);
-            const uint32_t b0 = biased_pair<2>(wa[w]), b2 = biased_pair<3>(wa[w]);
-            const uint32_t b1 = biased_pair<2>(wb[w]), b3 = biased_pair<3>(wb[w]);
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                mma_bf16_16816(cg[mt], a0, a1, a2, a3, xw[mt][4 * w], xw[mt][4 * w + 1]);
-                mma_bf16_16816(cg[mt], b0, b1, b2, b3, xw[mt][4 * w + 2], xw[mt][4 * w + 3]);
-            }
-        }
         const float da = bf16_lo(dbits[rt][0]);
         const float db = bf16_lo(dbits[rt][1]);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-            acc[rt][mt][0] = fmaf(da, cg[mt][0], acc[rt][mt][0]);
-            acc[rt][mt][1] = fmaf(da, cg[mt][1], acc[rt][mt][1]);
-            acc[rt][mt][2] = fmaf(db, cg[mt][2], acc[rt][mt][2]);
-            acc[rt][mt][3] = fmaf(db, cg[mt][3], acc[rt][mt][3]);
+            acc[rt][mt][0] = fmaf(da, cg[rt][mt][0] + corr[mt][0], acc[rt][mt][0]);
+            acc[rt][mt][1] = fmaf(da, cg[rt][mt][1] + corr[mt][1], acc[rt][mt][1]);
+            acc[rt][mt][2] = fmaf(db, cg[rt][mt][2] + corr[mt][2], acc[rt][mt][2]);
+            acc[rt][mt][3] = fmaf(db, cg[rt][mt][3] + corr[mt][3], acc[rt][mt][3]);
         }
     }
 }
@@ -184,9 +202,28 @@ template <int MT, int TPW>
 __device__ __forceinline__ void group_math_affine(float (&acc)[TPW][MT][4], const uint32_t (&xw)[MT][16],
                                                   const uint4 (&wv)[TPW][2], const uint32_t (&d2)[TPW][2],
                                                   const uint32_t (&off2)[TPW][2]) {
+    // k-steps outermost, row tiles inside (as in group_math): consecutive MMAs
+    // update different tiles' accumulators (10 % faster for the affine
+    // formats at 16 token rows, 1.5 % for the symmetric grouped stack).
 #pragma unroll
-    for (int rt = 0; rt < TPW; ++rt)
-        tile_math_affine<MT>(acc[rt], xw, wv[rt][0], wv[rt][1], d2[rt][0], d2[rt][1], off2[rt][0], off2[rt][1]);
+    for (int ks = 0; ks < 8; ++ks) {
+        const int w = ks >> 1;
+#pragma unroll
+        for (int rt = 0; rt < TPW; ++rt) {
+            uint32_t f[4];
+            if (ks & 1)
+                biased_frag<1>(word_of(wv[rt][0], w), word_of(wv[rt][1], w), f);
+            else
+                biased_frag<0>(word_of(wv[rt][0], w), word_of(wv[rt][1], w), f);
+            f[0] = affine_pair(f[0], off2[rt][0], d2[rt][0]);
+            f[1] = affine_pair(f[1], off2[rt][1], d2[rt][1]);
+            f[2] = affine_pair(f[2], off2[rt][0], d2[rt][0]);
+            f[3] = affine_pair(f[3], off2[rt][1], d2[rt][1]);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+                mma_bf16_16816(acc[rt][mt], f[0], f[1], f[2], f[3], xw[mt][2 * ks], xw[mt][2 * ks + 1]);
+        }
+    }
 }
 
 // The same with each row tile's 16-byte chunks loaded from the stage just
