@@ -146,15 +146,4 @@ __device__ __forceinline__ void pdl_start() {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
-// Pair i (0..3) of a stored 32-bit code word: nibble slots i and i+4 hold the
-// codes of two consecutive k.  XOR with 0x4308 turns nibble c = q & 0xF into
-// the bf16 pattern of 128 + (c ^ 8) = 136 + q; subtracting 136 (exact) leaves q.
-__device__ __forceinline__ uint32_t code_pair_bf16x2(uint32_t word, int i) {
-    const uint32_t biased = ((word >> (4 * i)) & 0x000F000Fu) ^ 0x43084308u;
-    __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&biased);
-    const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
-    __nv_bfloat162 q = __hsub2(v, off);
-    return *reinterpret_cast<uint32_t*>(&q);
-}
-
 }  // namespace w4

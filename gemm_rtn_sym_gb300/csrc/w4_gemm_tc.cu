@@ -14,11 +14,12 @@
 // a cluster of up to 8 CTAs may split K (whole groups each) and sum its fp32
 // partials over distributed shared memory.
 //   warp 0      : TMA loads of x tiles (128-byte swizzle) into the ring;
-//   warp 1      : allocates TMEM, one lane issues 8 MMAs (K = 16 each) per
-//                 stage with A read from TMEM, B from shared memory, and
-//                 commits each stage back to its "empty" barrier (a 64-k stage
-//                 left the issuing thread's barrier and commit overhead per
-//                 stage as large as the MMAs' own time at N ≈ 200);
+//   warp 1      : allocates TMEM; the whole warp runs the stage loop and
+//                 one elected lane issues 8 MMAs (K = 16 each) per stage with
+//                 A read from TMEM, B from shared memory, and commits each
+//                 stage back to its "empty" barrier (a 64-k stage left the
+//                 barrier and commit overhead per stage as large as the MMAs'
+//                 own time at N ≈ 200);
 //   warps 2..9  : one weight row and 64 k per thread — read 32 bytes of codes
 //                 from the code ring, decode nibble pairs to bf16 q, multiply
 //                 by d (bf16, round-to-nearest) and store the 32 columns into
@@ -190,15 +191,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issue
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16(bm);
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int s = kb % kStages;
-                const uint32_t par = static_cast<uint32_t>(kb / kStages) & 1u;
-                if (!mbar_wait(full_b(s), par) || !mbar_wait(full_a(s), par)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t a_s = tmem_d + kColA + 64u * s;
-                const uint32_t b_s = b_base + s * b_tile_bytes;
+        // The whole warp runs the loop, so its control flow and the MMA
+        // operands are warp-uniform (kept in uniform registers); one elected
+        // lane issues the MMAs and the commits.  Issued from one lane's
+        // divergent branch, each MMA cost about 100 cycles of issue on its
+        // own, which bounded the tile at every token count.
+        const uint32_t idesc = idesc_bf16(bm);
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int s = kb % kStages;
+            const uint32_t par = static_cast<uint32_t>(kb / kStages) & 1u;
+            ok = __all_sync(0xffffffffu, mbar_wait(full_b(s), par) && mbar_wait(full_a(s), par));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t a_s = tmem_d + kColA + 64u * s;
+            const uint32_t b_s = b_base + s * b_tile_bytes;
+            if (elect_one()) {
 #pragma unroll
                 for (int ks = 0; ks < kBK / 16; ++ks)
                     mma_bf16_tmem_a(tmem_d, a_s + 8u * ks,
@@ -206,9 +213,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
                                     (kb | ks) != 0 ? 1u : 0u);
                 mma_commit(empty(s));
             }
-            mma_commit(accum_bar);  // also tracks MMAs issued before an abort
-            if (!ok) record_status(args.status, kStatusTimeout);
+            __syncwarp();
         }
+        if (elect_one()) mma_commit(accum_bar);  // also tracks MMAs issued before an abort
+        __syncwarp();
+        if (!ok && lane == 0) record_status(args.status, kStatusTimeout);
     } else {
         // ------------------------------------------------ dequantisers
         const int quarter = warp & 3;               // TMEM lane quarter this warp may access

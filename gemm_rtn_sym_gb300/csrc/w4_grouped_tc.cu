@@ -1,4 +1,4 @@
-// Grouped tensor-core W4A16 matmul: many independent problems with M ≥ 17
+// Grouped tensor-core W4A16 matmul: many independent problems with M ≥ 33
 // (for example the four matrices of a 70B-class layer in a speculative-verify
 // pass) in one persistent launch.
 //
@@ -71,15 +71,11 @@ struct alignas(128) TcProblem {
 static_assert(sizeof(TcHeader) == 128, "plan header");
 static_assert(sizeof(TcProblem) == 384, "plan problem record");
 
-__device__ __forceinline__ uint32_t deq_pair(uint32_t word, int i, __nv_bfloat162 d2) {
-    const uint32_t q = code_pair_bf16x2(word, i);
-    __nv_bfloat162 v = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&q), d2);
-    return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// Affine formats: d·(c − z') for the pair i of a code word, as bf16x2:
-// (136 + c) − (136 + z') is exact, the product rounds once.  off2 =
-// bf16x2(136 + z'), d2 = bf16x2(d).
+// d·(c − z') for the pair i of a code word, as bf16x2: (136 + c) − (136 + z')
+// is exact, the product rounds once.  off2 = bf16x2(136 + z') (136 for the
+// symmetric format), d2 = bf16x2(d).  One shift, one LOP3, one subtract and
+// one multiply per pair, written out in PTX (the bf16x2 arithmetic
+// intrinsics cost about twice as many instructions here).
 __device__ __forceinline__ uint32_t deq_pair_affine(uint32_t word, int i, uint32_t off2, uint32_t d2) {
     const uint32_t biased = ((word >> (4 * i)) & 0x000F000Fu) ^ 0x43084308u;
     uint32_t r;
@@ -218,47 +214,53 @@ gemm_tc_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issue
-        if (lane == 0) {
-            int s = 0;
-            uint32_t ph = 0;
-            uint32_t acc_ph = 0;
-            bool ok = true;
-            for (int i = i_begin; i < i_end && ok; ++i) {
-                const TcProblem* pr = probs + items[i].x;
-                const uint32_t idesc = idesc_bf16(pr->bm);
-                const uint32_t half_bytes = static_cast<uint32_t>(pr->bm) * 128u;
-                // The previous item's accumulator must have been read out.
-                if (!mbar_wait(acc_empty, acc_ph ^ 1u)) {
-                    ok = false;
-                    break;
-                }
-                acc_ph ^= 1u;
+        // The whole warp runs the loop, so its control flow and the MMA
+        // operands are warp-uniform (kept in uniform registers); one elected
+        // lane issues the MMAs and the commits.  Issued from one lane's
+        // divergent branch, each MMA cost about 100 cycles of issue on its
+        // own (measured with clock64 stamps: 840 cycles per 8-MMA stage at
+        // every token count), which bounded the tile.
+        int s = 0;
+        uint32_t ph = 0;
+        uint32_t acc_ph = 0;
+        bool ok = true;
+        for (int i = i_begin; i < i_end && ok; ++i) {
+            const TcProblem* pr = probs + items[i].x;
+            const uint32_t idesc = idesc_bf16(pr->bm);
+            const uint32_t half_bytes = static_cast<uint32_t>(pr->bm) * 128u;
+            const int nkb = pr->nkb;
+            // The previous item's accumulator must have been read out.
+            ok = __all_sync(0xffffffffu, mbar_wait(acc_empty, acc_ph ^ 1u));
+            if (!ok) break;
+            acc_ph ^= 1u;
+            tc_fence_after();
+            for (int kb = 0; kb < nkb; ++kb) {
+                ok = __all_sync(0xffffffffu, mbar_wait(full_b(s), ph) && mbar_wait(full_a(s), ph));
+                if (!ok) break;
                 tc_fence_after();
-                for (int kb = 0; kb < pr->nkb; ++kb) {
-                    if (!mbar_wait(full_b(s), ph) || !mbar_wait(full_a(s), ph)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t a_s = tmem_d + kColA + 64u * s;
-                    const uint32_t b_s = b_base + s * b_slot;
+                const uint32_t a_s = tmem_d + kColA + 64u * s;
+                const uint32_t b_s = b_base + s * b_slot;
+                if (elect_one()) {
 #pragma unroll
                     for (int ks = 0; ks < kBK / 16; ++ks)
                         mma_bf16_tmem_a(tmem_d, a_s + 8u * ks, sw128_desc(b_s + (ks >> 2) * half_bytes + (ks & 3) * 32),
                                         idesc, (kb | ks) != 0 ? 1u : 0u);
                     mma_commit(empty(s));
-                    if (++s == kStages) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
                 }
-                if (ok) mma_commit(accum_bar);
+                __syncwarp();
+                if (++s == kStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
-            if (!ok) record_status(status, kStatusTimeout);
-            // Every MMA issued has completed once this commit arrives.
-            mma_commit(drain_bar);
-            mbar_wait(drain_bar, 0);
+            if (ok && elect_one()) mma_commit(accum_bar);
+            __syncwarp();
         }
+        if (!ok && lane == 0) record_status(status, kStatusTimeout);
+        // Every MMA issued has completed once this commit arrives.
+        if (elect_one()) mma_commit(drain_bar);
+        __syncwarp();
+        mbar_wait(drain_bar, 0);
     } else {
         // ------------------------------------------------ dequantisers + epilogue
         const int quarter = warp & 3;
@@ -320,11 +322,10 @@ gemm_tc_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
                     const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
                     uint32_t v[32];
                     if (QG == 0) {
-                        const __nv_bfloat162 d2 = *reinterpret_cast<const __nv_bfloat162*>(&d2bits);
 #pragma unroll
                         for (int w = 0; w < 8; ++w)
 #pragma unroll
-                            for (int p = 0; p < 4; ++p) v[4 * w + p] = deq_pair(words[w], p, d2);
+                            for (int p = 0; p < 4; ++p) v[4 * w + p] = deq_pair_affine(words[w], p, 0x43084308u, d2bits);
                     } else {
                         // words 0..3: the first 32 k (d, z of gidx), words 4..7: the next 32.
                         const uint32_t d2b = dbits_b | (dbits_b << 16);
