@@ -20,12 +20,17 @@
 //                 stage back to its "empty" barrier (a 64-k stage left the
 //                 barrier and commit overhead per stage as large as the MMAs'
 //                 own time at N ≈ 200);
-//   warps 2..9  : one weight row and 64 k per thread — read 32 bytes of codes
-//                 from the code ring, decode nibble pairs to bf16 q, multiply
-//                 by d (bf16, round-to-nearest) and store the 32 columns into
-//                 the stage's A slot with tcgen05.st; after the last stage,
-//                 read the accumulator back and store y (or the partial);
-//   warp 10     : TMA loads of codes, two groups × 128 rows per copy.
+//   warp 2      : TMA loads of codes, two groups × 128 rows per copy;
+//   warps 4..19 : one weight row and 32 k per thread (four warps per TMEM
+//                 lane quarter) — read 16 bytes of codes from the code ring,
+//                 decode nibble pairs to bf16 q, multiply by d (bf16,
+//                 round-to-nearest) and store the 16 columns into the stage's
+//                 A slot with tcgen05.st; after the last stage, read the
+//                 accumulator back and store y (or the partial).  Sixteen
+//                 dequantising warps rather than eight of 64 k each: the
+//                 decode is latency-bound per warp, and with eight it set the
+//                 stage time (on the grouped 27B-class layer at M = 64, 91 ->
+//                 80 µs).
 // Keeping A out of shared memory leaves the shared-memory port to the MMA's
 // B reads and the code ring, which at 200+ tokens is what bounds the tile.
 // Every mbarrier wait is bounded; a wait that runs out records a timeout in
@@ -48,12 +53,12 @@ constexpr int kBK = 128;            // k per stage: one group
 constexpr int kStages = 3;          // A (decoded, in TMEM) + B (activation, shared memory) stages
 constexpr int kCodeStages = 2;      // code stages of two groups (two k stages) each
 constexpr int kCodeStageBytes = 2 * kBN * 64;  // 16 KB: [group][row][64 B], 64-byte swizzle
-// Warps: 0 activation TMA, 1 TMEM + MMA, 2..9 dequantise + epilogue (two per
-// TMEM lane quarter, each one half of the k-block), 10 code TMA.
-constexpr int kDequantWarp0 = 2;
-constexpr int kDequantWarps = 8;
-constexpr int kCodeWarp = kDequantWarp0 + kDequantWarps;
-constexpr int kThreads = 32 * (kCodeWarp + 1);
+// Warps: 0 activation TMA, 1 TMEM + MMA, 2 code TMA, 3 idle, 4..19 dequantise
+// + epilogue (four per TMEM lane quarter, each 32 k of the k-block).
+constexpr int kCodeWarp = 2;
+constexpr int kDequantWarp0 = 4;
+constexpr int kDequantWarps = 16;
+constexpr int kThreads = 32 * (kDequantWarp0 + kDequantWarps);
 constexpr int kMaxBM = 256;
 // Tensor memory: accumulator in columns [0, 256), decoded A stages of 64
 // columns (128 k of bf16 pairs) from column 256.  The whole 512 columns are
@@ -218,62 +223,31 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
         if (elect_one()) mma_commit(accum_bar);  // also tracks MMAs issued before an abort
         __syncwarp();
         if (!ok && lane == 0) record_status(args.status, kStatusTimeout);
-    } else {
+    } else if (warp >= kDequantWarp0) {
         // ------------------------------------------------ dequantisers
-        const int quarter = warp & 3;               // TMEM lane quarter this warp may access
-        const int half = (warp - kDequantWarp0) >> 2;  // which 64 k of each group
-        const int t = quarter * 32 + lane;          // weight row within the tile
+        const int quarter = warp & 3;                  // TMEM lane quarter this warp may access
+        const int part = (warp - kDequantWarp0) >> 2;  // which 32 k of each group
+        const int t = quarter * 32 + lane;             // weight row within the tile
         const uint32_t lane_base = tmem_d + (static_cast<uint32_t>(quarter * 32) << 16);
         const int64_t n = n0 + t < args.N ? n0 + t : args.N - 1;  // padding rows: zero codes, valid scale
         const int64_t rg = QG == 0 ? G : args.row_groups;
         const uint16_t* srow = args.scales + n * rg;
         const int8_t* zrow = QG != 0 && args.zeros ? args.zeros + n * rg : nullptr;
-        // (d, 136 + z') of the two 32-k chunks this thread dequantises in k
-        // stage kb, as bf16x2: {d2 of chunk 2·half, of chunk 2·half + 1,
-        // off2 of the first, of the second}.
-        // With groups of 32 the thread's two chunks have adjacent groups (ia,
-        // ia + 1, ia even): their scales are one 32-bit load and their zeros
-        // one 16-bit load when the buffers are aligned for it (rows of K/32
-        // entries keep that alignment).
-        const bool pair_s = QG == 32 && (reinterpret_cast<uintptr_t>(srow) & 3u) == 0;
-        const bool pair_z = QG == 32 && zrow && (reinterpret_cast<uintptr_t>(zrow) & 1u) == 0;
-        auto load_dz = [&](int kb, uint32_t (&o)[4]) {
+        // (d, 136 + z') of the 32-k chunk this thread dequantises in k stage
+        // kb, as bf16x2: {d2, off2}.
+        auto load_dz = [&](int kb, uint32_t (&o)[2]) {
             const int64_t gk = kb_lo + kb;
-            int64_t ia = gk;
-            if (QG == 64) ia = 2 * gk + half;
-            if (QG == 32) ia = 4 * gk + 2 * half;
-            uint32_t da, db;
-            if (QG == 32 && pair_s) {
-                const uint32_t w = __ldg(reinterpret_cast<const unsigned int*>(srow + ia));
-                da = w & 0xFFFFu;
-                db = w >> 16;
-            } else {
-                da = __ldg(srow + ia);
-                db = QG == 32 ? __ldg(srow + ia + 1) : da;
-            }
-            int za = 0, zb = 0;
-            if (zrow) {
-                if (QG == 32 && pair_z) {
-                    const unsigned short w = __ldg(reinterpret_cast<const unsigned short*>(zrow + ia));
-                    za = static_cast<int8_t>(w & 0xFFu);
-                    zb = static_cast<int8_t>(w >> 8);
-                } else {
-                    za = __ldg(zrow + ia);
-                    zb = QG == 32 ? __ldg(zrow + ia + 1) : za;
-                }
-            }
-            const uint32_t oa = static_cast<uint32_t>(0x4308 + za), ob = static_cast<uint32_t>(0x4308 + zb);
-            o[0] = da | (da << 16);
-            o[1] = db | (db << 16);
-            o[2] = oa | (oa << 16);
-            o[3] = ob | (ob << 16);
+            const int64_t ia = QG == 64 ? 2 * gk + (part >> 1) : (QG == 32 ? 4 * gk + part : gk);
+            const uint32_t d = __ldg(srow + ia);
+            const uint32_t z = static_cast<uint32_t>(0x4308 + (zrow ? __ldg(zrow + ia) : 0));
+            o[0] = d | (d << 16);
+            o[1] = z | (z << 16);
         };
-        // Row t of a code stage: 64 bytes per group, 16-byte chunk c at c ^ ((t >> 1) & 3).
-        const uint32_t row_off = static_cast<uint32_t>(t * 64);
-        const uint32_t sw = static_cast<uint32_t>((t >> 1) & 3);
+        // Row t of a code stage: 64 bytes per group, 16-byte chunk j at j ^ ((t >> 1) & 3).
+        const uint32_t row_chunk = static_cast<uint32_t>(t * 64) + (static_cast<uint32_t>(part ^ ((t >> 1) & 3)) << 4);
         // Scales and zeros are fetched two k stages ahead.
-        uint32_t dz1[4] = {0u, 0u, 0x43084308u, 0x43084308u};
-        uint32_t dz2[4] = {0u, 0u, 0x43084308u, 0x43084308u};
+        uint32_t dz1[2] = {0u, 0x43084308u};
+        uint32_t dz2[2] = {0u, 0x43084308u};
         if (nkb > 0) load_dz(0, dz1);
         if (nkb > 1) load_dz(1, dz2);
         for (int kb = 0; kb < nkb && ok; ++kb) {
@@ -281,21 +255,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             const uint32_t r = static_cast<uint32_t>(kb / kStages);
             const int cst = (kb >> 1) % kCodeStages;
             const int sub = kb & 1;  // group within the code stage
-            const uint32_t dz[4] = {dz1[0], dz1[1], dz1[2], dz1[3]};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dz1[i] = dz2[i];
+            const uint32_t d2 = dz1[0], o2 = dz1[1];
+            dz1[0] = dz2[0];
+            dz1[1] = dz2[1];
             if (kb + 2 < nkb) load_dz(kb + 2, dz2);
             const bool have = mbar_wait(code_full(cst), static_cast<uint32_t>((kb >> 1) / kCodeStages) & 1u);
             if (!__all_sync(0xffffffffu, have)) { ok = false; break; }
-            const uint32_t grp = code_base + cst * kCodeStageBytes + sub * (kBN * 64) + row_off;
-            const uint4 q0 = lds128(grp + (((2u * half) ^ sw) << 4));
-            const uint4 q1 = lds128(grp + (((2u * half + 1u) ^ sw) << 4));
-            const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-            uint32_t v[32];  // column 4w + i of this thread's 32: pair i of word w
+            const uint4 q = lds128(code_base + cst * kCodeStageBytes + sub * (kBN * 64) + row_chunk);
+            const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+            uint32_t v[16];  // column 4w + i of this thread's 16: pair i of word w
 #pragma unroll
-            for (int w = 0; w < 8; ++w)
+            for (int w = 0; w < 4; ++w)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) v[4 * w + i] = deq_pair(words[w], i, dz[2 + (w >> 2)], dz[w >> 2]);
+                for (int i = 0; i < 4; ++i) v[4 * w + i] = deq_pair(words[w], i, o2, d2);
             // The code slot is released only once its words have been used: the
             // shared-memory load may still be pending when an arrive executes,
             // and the next TMA copy into the slot must not overtake it.
@@ -303,7 +275,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             const bool free_stage = mbar_wait(empty(s), (r & 1u) ^ 1u);
             if (!__all_sync(0xffffffffu, free_stage)) { ok = false; break; }
             tc_fence_after();
-            tmem_st32(lane_base + kColA + 64u * s + 32u * half, v);
+            tmem_st16(lane_base + kColA + 64u * s + 16u * part, v);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(full_a(s));
@@ -320,21 +292,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             // With a split, the fp32 partial goes to shared memory (the rings
             // are idle now) as red[column][row], for the cluster reduction below.
             float* red = reinterpret_cast<float*>(gbase);
-            // The two warps of a lane quarter take the columns below / from cmid.
-            const int cmid = (bm >> 5) << 4;
-            const int cbeg = half == 0 ? 0 : cmid;
-            const int cend = half == 0 ? cmid : bm;
-            // Up to four 16-column loads in flight per wait (the column range
-            // is a multiple of 16).
-            for (int c0 = cbeg; c0 < cend; c0 += 64) {
-                const int nq = min(4, (cend - c0) >> 4);  // warp-uniform
-                uint32_t v[4][16];
+            // The four warps of a lane quarter split the 16-column blocks.
+            const int nb = bm >> 4;
+            const int cbeg = ((part * nb) >> 2) << 4;
+            const int cend = (((part + 1) * nb) >> 2) << 4;
+            // Up to two 16-column loads in flight per wait.
+            for (int c0 = cbeg; c0 < cend; c0 += 32) {
+                const int nq = min(2, (cend - c0) >> 4);  // warp-uniform
+                uint32_t v[2][16];
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
+                for (int q = 0; q < 2; ++q)
                     if (q < nq) tmem_ld16_async(lane_base + static_cast<uint32_t>(c0 + 16 * q), v[q]);
                 tmem_wait_ld();
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < 2; ++q) {
                     if (q >= nq) continue;
                     reg_fence16(v[q]);
                     const int cq = c0 + 16 * q;

@@ -33,10 +33,12 @@ constexpr int kBK = 128;            // k per stage: one group
 constexpr int kStages = 3;          // A (TMEM) + B (shared memory) stages
 constexpr int kCodeStages = 2;      // code stages of two groups (two k stages) each
 constexpr int kCodeStageBytes = 2 * kBN * 64;
-constexpr int kDequantWarp0 = 2;
-constexpr int kDequantWarps = 8;
-constexpr int kCodeWarp = kDequantWarp0 + kDequantWarps;
-constexpr int kThreads = 32 * (kCodeWarp + 1);
+// Warps: 0 activation TMA, 1 TMEM + MMA, 2 code TMA, 3 idle, 4..19 dequantise
+// + epilogue (warp w takes TMEM lane quarter w % 4 and 32 k of each group).
+constexpr int kCodeWarp = 2;
+constexpr int kDequantWarp0 = 4;
+constexpr int kDequantWarps = 16;
+constexpr int kThreads = 32 * (kDequantWarp0 + kDequantWarps);
 constexpr int kMaxBM = 256;
 constexpr uint32_t kColA = 256;
 constexpr uint32_t kTmemCols = 512;
@@ -261,14 +263,14 @@ gemm_tc_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
         if (elect_one()) mma_commit(drain_bar);
         __syncwarp();
         mbar_wait(drain_bar, 0);
-    } else {
+    } else if (warp >= kDequantWarp0) {
         // ------------------------------------------------ dequantisers + epilogue
-        const int quarter = warp & 3;
-        const int half = (warp - kDequantWarp0) >> 2;
-        const int t = quarter * 32 + lane;  // weight row within the tile
+        const int quarter = warp & 3;                  // TMEM lane quarter this warp may access
+        const int part = (warp - kDequantWarp0) >> 2;  // which 32 k of each group
+        const int t = quarter * 32 + lane;             // weight row within the tile
         const uint32_t lane_base = tmem_d + (static_cast<uint32_t>(quarter * 32) << 16);
-        const uint32_t row_off = static_cast<uint32_t>(t * 64);
-        const uint32_t sw = static_cast<uint32_t>((t >> 1) & 3);
+        // Row t of a code stage: 64 bytes per group, 16-byte chunk j at j ^ ((t >> 1) & 3).
+        const uint32_t row_chunk = static_cast<uint32_t>(t * 64) + (static_cast<uint32_t>(part ^ ((t >> 1) & 3)) << 4);
         int s = 0;
         uint32_t ph = 0;
         int c = 0;
@@ -285,57 +287,34 @@ gemm_tc_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
             const int64_t rg = QG == 0 ? pr->G : pr->row_groups;
             const uint16_t* srow = pr->scales + n * rg;
             const int8_t* zrow = QG != 0 && pr->zeros ? pr->zeros + n * rg : nullptr;
-            // The QG-group of this thread's first 32 k of group kb (its second
-            // 32 k are in the next one at QG = 32).
+            // The QG-group holding this thread's 32 k of group kb.
             auto gidx = [&](int kb) {
-                return QG == 0 ? kb : kb * (128 / QG) + (QG == 64 ? half : (QG == 32 ? 2 * half : 0));
+                return QG == 0 ? kb : kb * (128 / QG) + (QG == 64 ? (part >> 1) : (QG == 32 ? part : 0));
             };
-            auto zbits = [&](int i) { return static_cast<uint32_t>(0x4308 + (zrow ? __ldg(zrow + i) : 0)); };
+            auto zbits = [&](int g) { return static_cast<uint32_t>(0x4308 + (zrow ? __ldg(zrow + g) : 0)); };
             if (ok) {
                 uint32_t d_next = __ldg(srow + gidx(0));
-                uint32_t d_next_b = QG == 32 ? __ldg(srow + gidx(0) + 1) : d_next;
-                uint32_t z_next = QG != 0 ? zbits(gidx(0)) : 0u;
-                uint32_t z_next_b = QG == 32 ? zbits(gidx(0) + 1) : z_next;
+                uint32_t z_next = QG != 0 ? zbits(gidx(0)) : 0x4308u;
                 for (int kb = 0; kb < nkb; ++kb) {
                     const int sub = kb & 1;  // group within the code stage
-                    const uint32_t dbits = d_next, dbits_b = d_next_b, zb0 = z_next, zb1 = z_next_b;
+                    const uint32_t dbits = d_next, zb = z_next;
                     if (kb + 1 < nkb) {
-                        const int ia = gidx(kb + 1);
-                        d_next = __ldg(srow + ia);
-                        if (QG == 32) d_next_b = __ldg(srow + ia + 1);
-                        if (QG != 0) z_next = zbits(ia);
-                        if (QG == 32) z_next_b = zbits(ia + 1);
-                        if (QG != 0 && QG != 32) {
-                            d_next_b = d_next;
-                            z_next_b = z_next;
-                        }
+                        d_next = __ldg(srow + gidx(kb + 1));
+                        if (QG != 0) z_next = zbits(gidx(kb + 1));
                     }
                     const bool have = mbar_wait(code_full(c), cph);
                     if (!__all_sync(0xffffffffu, have)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t grp = code_base + c * kCodeStageBytes + sub * (kBN * 64) + row_off;
-                    const uint4 q0 = lds128(grp + (((2u * half) ^ sw) << 4));
-                    const uint4 q1 = lds128(grp + (((2u * half + 1u) ^ sw) << 4));
-                    const uint32_t d2bits = dbits | (dbits << 16);
-                    const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                    uint32_t v[32];
-                    if (QG == 0) {
+                    const uint4 q = lds128(code_base + c * kCodeStageBytes + sub * (kBN * 64) + row_chunk);
+                    const uint32_t d2 = dbits | (dbits << 16), o2 = zb | (zb << 16);
+                    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+                    uint32_t v[16];  // column 4w + i of this thread's 16: pair i of word w
 #pragma unroll
-                        for (int w = 0; w < 8; ++w)
+                    for (int w = 0; w < 4; ++w)
 #pragma unroll
-                            for (int p = 0; p < 4; ++p) v[4 * w + p] = deq_pair_affine(words[w], p, 0x43084308u, d2bits);
-                    } else {
-                        // words 0..3: the first 32 k (d, z of gidx), words 4..7: the next 32.
-                        const uint32_t d2b = dbits_b | (dbits_b << 16);
-                        const uint32_t o2a = zb0 | (zb0 << 16), o2b = zb1 | (zb1 << 16);
-#pragma unroll
-                        for (int w = 0; w < 8; ++w)
-#pragma unroll
-                            for (int p = 0; p < 4; ++p)
-                                v[4 * w + p] = deq_pair_affine(words[w], p, w < 4 ? o2a : o2b, w < 4 ? d2bits : d2b);
-                    }
+                        for (int p = 0; p < 4; ++p) v[4 * w + p] = deq_pair_affine(words[w], p, o2, d2);
                     // Release the code slot only after its words have been used
                     // (the shared-memory load may still be pending at an arrive).
                     mbar_arrive(code_empty(c));
@@ -353,7 +332,7 @@ gemm_tc_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
                         break;
                     }
                     tc_fence_after();
-                    tmem_st32(lane_base + kColA + 64u * s + 32u * half, v);
+                    tmem_st16(lane_base + kColA + 64u * s + 16u * part, v);
                     tmem_wait_st();
                     tc_fence_before();
                     mbar_arrive(full_a(s));
@@ -378,27 +357,26 @@ gemm_tc_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
             const int64_t N = pr->N, M = pr->M;
             __nv_bfloat16* const y = pr->y;
             const int64_t ny = n0 + t;
-            const int cmid = (bm >> 5) << 4;  // the two warps of a lane quarter split the columns
-            const int cbeg = half == 0 ? 0 : cmid;
-            const int cend = half == 0 ? cmid : bm;
-            // Up to four 16-column loads in flight per wait (the column range
-            // is a multiple of 16).
-            for (int c0 = cbeg; c0 < cend; c0 += 64) {
-                const int nq = min(4, (cend - c0) >> 4);  // warp-uniform
-                uint32_t v[4][16];
+            // The four warps of a lane quarter split the 16-column blocks.
+            const int nb = bm >> 4;
+            const int cbeg = ((part * nb) >> 2) << 4;
+            const int cend = (((part + 1) * nb) >> 2) << 4;
+            for (int c0 = cbeg; c0 < cend; c0 += 32) {
+                const int nq = min(2, (cend - c0) >> 4);  // warp-uniform
+                uint32_t v[2][16];
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    if (q < nq) tmem_ld16_async(lane_base + static_cast<uint32_t>(c0 + 16 * q), v[q]);
+                for (int qq = 0; qq < 2; ++qq)
+                    if (qq < nq) tmem_ld16_async(lane_base + static_cast<uint32_t>(c0 + 16 * qq), v[qq]);
                 tmem_wait_ld();
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    if (q >= nq) continue;
-                    reg_fence16(v[q]);
+                for (int qq = 0; qq < 2; ++qq) {
+                    if (qq >= nq) continue;
+                    reg_fence16(v[qq]);
                     if (ny < N) {
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
-                            const int64_t m = m0 + c0 + 16 * q + j;
-                            if (m < M) y[m * N + ny] = __float2bfloat16_rn(__uint_as_float(v[q][j]));
+                            const int64_t m = m0 + c0 + 16 * qq + j;
+                            if (m < M) y[m * N + ny] = __float2bfloat16_rn(__uint_as_float(v[qq][j]));
                         }
                     }
                 }
