@@ -81,7 +81,11 @@ struct TcArgs {
 // d·(c − z') for the pair i of a code word, as bf16x2: (136 + c) − (136 + z') is
 // exact, the product rounds once.  off2 = bf16x2(136 + z'), d2 = bf16x2(d).
 __device__ __forceinline__ uint32_t deq_pair(uint32_t word, int i, uint32_t off2, uint32_t d2) {
-    const uint32_t biased = ((word >> (4 * i)) & 0x000F000Fu) ^ 0x43084308u;
+    // (t & 0x000F000F) ^ 0x43084308 as one three-input logic op (LUT 0x6A),
+    // written out: as plain C it compiled to about two LOP3s per pair.
+    uint32_t t = word, biased;
+    if (i != 0) asm("shr.b32 %0, %1, %2;" : "=r"(t) : "r"(word), "r"(4 * i));
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(biased) : "r"(t), "n"(0x000F000F), "r"(0x43084308u));
     uint32_t r;
     asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(biased), "r"(off2));
     asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(r) : "r"(d2));
@@ -268,9 +272,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             for (int w = 0; w < 4; ++w)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) v[4 * w + i] = deq_pair(words[w], i, o2, d2);
-            // The code slot is released only once its words have been used: the
-            // shared-memory load may still be pending when an arrive executes,
-            // and the next TMA copy into the slot must not overtake it.
+            // Release the code slot only after a proxy fence: the words were read
+            // through the generic proxy and the next TMA copy into the slot writes
+            // through the async proxy, so without the fence the copy could overtake
+            // a read still in flight (nothing keeps the decode that consumes the
+            // words ahead of the arrive).  A 40-run repeat test changed output
+            // elements in every attempt without it.
+            fence_async_smem();
             mbar_arrive(code_empty(cst));
             const bool free_stage = mbar_wait(empty(s), (r & 1u) ^ 1u);
             if (!__all_sync(0xffffffffu, free_stage)) { ok = false; break; }

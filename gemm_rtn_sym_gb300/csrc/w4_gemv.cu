@@ -239,6 +239,9 @@ gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_cons
                     }
                 }
             }
+            // Generic-proxy reads of the slot before the async-proxy TMA copy that
+            // reuses it: formally ordered only by a proxy fence (about 0.5 % here).
+            fence_async_smem();
             mbar_arrive(empty(s));
         }
         if (!ok) record_status(args.status, kStatusTimeout);

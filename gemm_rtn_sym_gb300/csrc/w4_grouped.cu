@@ -316,6 +316,9 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
                         }
                     }
                 }
+                // Generic-proxy reads of the slot before the async-proxy TMA copy that
+                // reuses it: formally ordered only by a proxy fence (about 0.5 % here).
+                fence_async_smem();
                 mbar_arrive(empty(s));
             }
             if (++s == C::kStages) {

@@ -79,7 +79,11 @@ static_assert(sizeof(TcProblem) == 384, "plan problem record");
 // one multiply per pair, written out in PTX (the bf16x2 arithmetic
 // intrinsics cost about twice as many instructions here).
 __device__ __forceinline__ uint32_t deq_pair_affine(uint32_t word, int i, uint32_t off2, uint32_t d2) {
-    const uint32_t biased = ((word >> (4 * i)) & 0x000F000Fu) ^ 0x43084308u;
+    // (t & 0x000F000F) ^ 0x43084308 as one three-input logic op (LUT 0x6A),
+    // written out: as plain C it compiled to about two LOP3s per pair.
+    uint32_t t = word, biased;
+    if (i != 0) asm("shr.b32 %0, %1, %2;" : "=r"(t) : "r"(word), "r"(4 * i));
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(biased) : "r"(t), "n"(0x000F000F), "r"(0x43084308u));
     uint32_t r;
     asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(biased), "r"(off2));
     asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(r) : "r"(d2));
@@ -315,8 +319,13 @@ gemm_tc_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
                     for (int w = 0; w < 4; ++w)
 #pragma unroll
                         for (int p = 0; p < 4; ++p) v[4 * w + p] = deq_pair_affine(words[w], p, o2, d2);
-                    // Release the code slot only after its words have been used
-                    // (the shared-memory load may still be pending at an arrive).
+                    // Release the code slot only after a proxy fence: the words were read
+                    // through the generic proxy and the next TMA copy into the slot writes
+                    // through the async proxy, so without the fence the copy could overtake
+                    // a read still in flight (nothing keeps the decode that consumes the
+                    // words ahead of the arrive).  A 40-run repeat test changed output
+                    // elements in every attempt without it.
+                    fence_async_smem();
                     mbar_arrive(code_empty(c));
                     if (sub == 1 || kb + 1 == nkb) {
                         // A last stage holding one group still owes one arrival.
