@@ -24,13 +24,14 @@ bool g_info_ready[kMaxDevices];
 std::mutex g_info_mutex;
 
 // Smallest M that goes to the tensor-core kernel: under W4_PATH_AUTO for one
-// matrix, and in grouped plans.  Measured crossovers on the 4B-class stack
-// and the 27B-class layer (the small-M kernel reads the weights once per pass
-// of up to 32 token rows): one launch per matrix, small-M is faster up to
-// M = 24 and the tensor-core tile from M = 32; in one grouped launch the
-// small-M kernel stays faster up to M = 32.
+// matrix, and in grouped plans.  Measured crossovers on the 4B-class stack,
+// the 27B-class layer and the 2560×9216 matrix (M = 17, 20, 24, 28, 32): the
+// small-M kernel is faster up to M = 24 (three token tiles per pass; e.g.
+// grouped stack 621 against 665 µs at M = 24), the tensor-core tile from
+// M = 28 (grouped stack 665 against 815 µs; 2560×9216 alone 10.5 against
+// 11.5 µs), in one launch per matrix and in grouped launches alike.
 constexpr int64_t kTensorMinM = 25;
-constexpr int64_t kGroupedTensorMinM = 33;
+constexpr int64_t kGroupedTensorMinM = 25;
 
 // Largest N or K of the GPTQ calls: their fp64 tile products run 64-row tiles
 // on a grid at most 65535 tiles high.

@@ -53,7 +53,7 @@ static __device__ __align__(256) uint8_t g_static_plan[kStaticPlanBytes];
 struct alignas(128) GroupedHeader {
     int32_t count;
     int32_t n_items;
-    int32_t token_rows;   // x rows staged per 64-k block: 2, 4, 8, 16, 24 or 32
+    int32_t token_rows;   // x rows staged per 64-k block: 2, 4, 8, 16 or 24
     int32_t n_ctas;       // the grid the plan was scheduled for
     int32_t format;       // 0: symmetric group 128; 32, 64, 128: affine format of that group size
     int32_t reserved[27];
@@ -421,7 +421,7 @@ size_t grouped_plan_bytes(int32_t count, int64_t n_items, int32_t n_ctas) {
 }
 
 int grouped_token_rows(int64_t max_m) {
-    return max_m <= 2 ? 2 : max_m <= 4 ? 4 : max_m <= 8 ? 8 : max_m <= 16 ? 16 : max_m <= 24 ? 24 : 32;
+    return max_m <= 2 ? 2 : max_m <= 4 ? 4 : max_m <= 8 ? 8 : max_m <= 16 ? 16 : 24;
 }
 
 // Resident CTAs per SM of the grouped kernel for these token rows and format
@@ -435,7 +435,6 @@ int grouped_ctas_q(int token_rows, int device) {
         case 8: return grouped_ctas_per_sm<1, 8, kOne, QG>(device);
         case 16: return grouped_ctas_per_sm<2, 16, 2, QG>(device);
         case 24: return grouped_ctas_per_sm<3, 24, 2, QG>(device);
-        case 32: return grouped_ctas_per_sm<4, 32, 2, QG>(device);
         default: return 0;
     }
 }
@@ -574,7 +573,6 @@ cudaError_t launch_grouped_q(const void* plan, int32_t n_ctas, int token_rows, c
                            : launch_grouped_t<1, 8, kOne, QG>(plan, n_ctas, dev, stream);
         case 16: return launch_grouped_t<2, 16, 2, QG>(plan, n_ctas, dev, stream);
         case 24: return launch_grouped_t<3, 24, 2, QG>(plan, n_ctas, dev, stream);
-        case 32: return launch_grouped_t<4, 32, 2, QG>(plan, n_ctas, dev, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -1,4 +1,4 @@
-// Grouped tensor-core W4A16 matmul: many independent problems with M ≥ 33
+// Grouped tensor-core W4A16 matmul: many independent problems with M ≥ 25
 // (for example the four matrices of a 70B-class layer in a speculative-verify
 // pass) in one persistent launch.
 //

@@ -88,7 +88,7 @@ struct GroupedSpec {
 // scheduled over `n_ctas` CTAs.
 size_t grouped_plan_bytes(int32_t count, int64_t n_items, int32_t n_ctas);
 // Token rows the grouped small-M kernel stages per pass for a largest M of
-// max_m (2, 4, 8, 16, 24 or 32; max_m ≤ 32).
+// max_m (2, 4, 8, 16 or 24; max_m ≤ 24).
 int grouped_token_rows(int64_t max_m);
 // CTAs the grouped kernel runs with on this device (resident at once).
 // format: 0 for the symmetric group-128 format, else the affine group size.
@@ -105,7 +105,7 @@ cudaError_t static_plan_memory(void** ptr, size_t* bytes);
 cudaError_t launch_grouped(const void* plan, int32_t n_ctas, int token_rows, int format, const DeviceInfo& dev,
                            cudaStream_t stream);
 
-// Tensor-core grouped plan (problems with M ≥ 17): (problem, 128-row tile,
+// Tensor-core grouped plan (problems with M ≥ 25): (problem, 128-row tile,
 // token tile) items scheduled longest first over one CTA per SM.
 size_t tc_grouped_plan_bytes(int32_t count, int64_t n_items, int32_t n_ctas);
 int64_t tc_grouped_items(const GroupedSpec& sp);

@@ -268,9 +268,10 @@ int w4_gemm_path_for(int64_t M, int64_t N, int64_t K);
  * Grouped matmul — many independent problems y_i = Ŵ_i x_i in one call (the
  * matrices of a layer, or of a whole model step).  Each problem is computed
  * as by w4_gemm's kernel for its M (same per-element results contract, K not
- * split, deterministic): problems with M ≤ 32 by the small-M kernel, whose
- * work items are (problem, 64-row block) pairs on a fixed grid of two CTAs
- * per SM; problems with M ≥ 33 by the tensor-core kernel, whose items are
+ * split, deterministic): problems with M ≤ 24 by the small-M kernel, whose
+ * work items are (problem, 64-row block) pairs on a fixed grid of two or
+ * three CTAs per SM; problems with M ≥ 25 by the tensor-core kernel (the
+ * measured crossover, as for w4_gemm), whose items are
  * (problem, 128-row tile, token tile) on one CTA per SM.  Items are assigned
  * at plan time longest first to the least-loaded CTA, and each CTA streams
  * its items back to back through its TMA pipelines.  A plan with both kinds
@@ -297,11 +298,11 @@ typedef struct w4_grouped_plan {
     size_t bytes;        /* bytes of it in use                                    */
     int32_t count;       /* problems                                              */
     int32_t device;      /* CUDA device the plan was built on                     */
-    int32_t items;       /* small-M work items (0: no problem with M ≤ 32)        */
+    int32_t items;       /* small-M work items (0: no problem with M ≤ 24)        */
     int32_t ctas;        /* CTAs they were scheduled over (the launch grid)       */
     int32_t token_rows;  /* small-M kernel variant: token rows staged per pass,
-                            the smallest of 2, 4, 8, 16, 24, 32 ≥ the largest M  */
-    int32_t tc_items;    /* tensor-core work items (0: no problem with M ≥ 33)    */
+                            the smallest of 2, 4, 8, 16, 24 ≥ the largest M      */
+    int32_t tc_items;    /* tensor-core work items (0: no problem with M ≥ 25)    */
     int32_t tc_ctas;     /* CTAs they were scheduled over                         */
     int32_t tc_max_bm;   /* widest token tile                                     */
     size_t tc_offset;    /* byte offset of the tensor-core part of the plan       */
@@ -329,8 +330,8 @@ int w4_grouped_plan_init(w4_grouped_plan* plan, void* device_memory, size_t byte
  *   zeros  in : NULL (no problem has zero points), or `count` pointers, each
  *               NULL (symmetric codes) or problem i's int8 [N, K/group] zeros
  *               from w4_quantize_rtn_asym (any alignment)
- * Each problem is computed as by w4_gemm_affine's kernel for its M (M ≤ 32:
- * the small-M kernel, M ≥ 33: the tensor-core kernel), within the same
+ * Each problem is computed as by w4_gemm_affine's kernel for its M (M ≤ 24:
+ * the small-M kernel, M ≥ 25: the tensor-core kernel), within the same
  * bound; group 128 without zeros is exactly w4_grouped_plan_init.  The plan
  * runs with w4_gemm_grouped; sizes, checks and errors as above (zeros must
  * not overlap any output).

@@ -195,8 +195,8 @@ GROUPED_SHAPES = [(300, 1152), (7, 256), (129, 2560), (64, 384), (1000, 512)]
 def test_grouped_affine_parity(cuda_lib, group, asym, Ms):
     """The grouped matmul over the affine formats (w4_grouped_plan_init_affine):
     every problem within the parity bound of the oracle's dequantised matmul
-    with its zeros, on plans that select every small-M variant (2 to 32 token
-    rows staged) and mix in the tensor-core kernel (M ≥ 33); repeat runs
+    with its zeros, on plans that select every small-M variant (2 to 24 token
+    rows staged) and mix in the tensor-core kernel (M ≥ 25); repeat runs
     bit-identical."""
     probs, refs, zs = [], [], []
     for i, ((N, K), M) in enumerate(zip(GROUPED_SHAPES, Ms)):

@@ -72,9 +72,9 @@ def test_grouped_new_inputs_and_graph_replay(cuda_lib):
 @pytest.mark.parametrize("Ms", [[17, 33, 64, 208, 100, 257, 19], [1, 40, 13, 208, 8, 24, 2],
                                 [32, 28, 1, 5, 64, 25, 33]])
 def test_grouped_tensor_and_mixed(cuda_lib, Ms):
-    """Problems with M ≥ 33 take the tensor-core grouped kernel, the others the
-    small-M kernel at the token width of the largest (24 or 32 rows here); a
-    plan mixing both kinds runs both kernels."""
+    """Problems with M ≥ 25 take the tensor-core grouped kernel, the others the
+    small-M kernel at the token width of the largest (24 rows in the second
+    set); a plan mixing both kinds runs both kernels."""
     Ws, probs, bufs = make_problems(cuda_lib, SHAPES, Ms, seed=3 + Ms[1])
     plan = w4.w4_grouped_plan(probs)
     assert plan.plan.tc_items > 0
