@@ -104,6 +104,27 @@ def test_repeat_is_bit_identical_mid_m(cuda_lib):
             assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("N,K,M", [(57344, 8192, 208), (2560, 9216, 64), (10240, 2048, 33)])
+def test_tensor_repeat_is_bit_identical(cuda_lib, N, K, M):
+    """Many repeats of the tensor-core tile: persistent over more tiles than
+    SMs (57344 rows at M = 208), split-K over a cluster (2560 rows), one
+    token tile of 48 (M = 33).  A code slot handed back to TMA before its read
+    completed would show up as an occasional difference; the first run is
+    checked against the oracle on sampled rows."""
+    W = wl.random_bf16((N, K), 0.02, seed=N + M, device=DEV)
+    packed, scales = quantize_gpu(cuda_lib, W)
+    x = wl.random_bf16((M, K), 1.0, seed=M, device=DEV)
+    ref = w4.w4_gemm_ex(x, packed, scales, path=w4.W4_PATH_TENSOR)
+    ys = [w4.w4_gemm_ex(x, packed, scales, path=w4.W4_PATH_TENSOR) for _ in range(30)]
+    torch.cuda.synchronize()
+    assert w4.w4_last_device_status() == 0
+    rows = torch.from_numpy(sample_rows(N, 16, seed=N)).to(DEV)
+    check_gemm(W[rows].cpu(), x, ref[:, rows])
+    for y in ys:
+        assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
+
+
 def test_empty_and_degenerate(cuda_lib):
     packed = torch.empty((4, 0), dtype=torch.uint8, device=DEV)
     scales = torch.empty((4, 0), dtype=torch.bfloat16, device=DEV)
