@@ -107,9 +107,9 @@ def test_repeat_is_bit_identical_mid_m(cuda_lib):
 @pytest.mark.slow
 @pytest.mark.parametrize("N,K,M", [(57344, 8192, 208), (2560, 9216, 64), (10240, 2048, 33)])
 def test_tensor_repeat_is_bit_identical(cuda_lib, N, K, M):
-    """Many repeats of the tensor-core tile: persistent over more tiles than
-    SMs (57344 rows at M = 208), split-K over a cluster (2560 rows), one
-    token tile of 48 (M = 33).  A code slot handed back to TMA before its read
+    """Many repeats of the tensor-core tile: more tiles than SMs (57344 rows
+    at M = 208, three waves), split-K over a cluster (2560 rows), one token
+    tile of 48 (M = 33).  A code slot handed back to TMA before its read
     completed would show up as an occasional difference; the first run is
     checked against the oracle on sampled rows."""
     W = wl.random_bf16((N, K), 0.02, seed=N + M, device=DEV)
