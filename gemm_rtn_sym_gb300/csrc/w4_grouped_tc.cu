@@ -295,13 +295,15 @@ gemm_tc_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
             auto gidx = [&](int kb) {
                 return QG == 0 ? kb : kb * (128 / QG) + (QG == 64 ? (part >> 1) : (QG == 32 ? part : 0));
             };
-            auto zbits = [&](int g) { return static_cast<uint32_t>(0x4308 + (zrow ? __ldg(zrow + g) : 0)); };
+            // Zeros as loaded (z', sign-extended); 136 + z' is formed where it is
+            // used, so that the load issued a stage ahead is not waited for at once.
+            auto zbits = [&](int g) { return static_cast<uint32_t>(zrow ? static_cast<int>(__ldg(zrow + g)) : 0); };
             if (ok) {
                 uint32_t d_next = __ldg(srow + gidx(0));
-                uint32_t z_next = QG != 0 ? zbits(gidx(0)) : 0x4308u;
+                uint32_t z_next = QG != 0 ? zbits(gidx(0)) : 0u;
                 for (int kb = 0; kb < nkb; ++kb) {
                     const int sub = kb & 1;  // group within the code stage
-                    const uint32_t dbits = d_next, zb = z_next;
+                    const uint32_t dbits = d_next, zb = 0x4308u + z_next;  // bf16(136 + z')
                     if (kb + 1 < nkb) {
                         d_next = __ldg(srow + gidx(kb + 1));
                         if (QG != 0) z_next = zbits(gidx(kb + 1));
