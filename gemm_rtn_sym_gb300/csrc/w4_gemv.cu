@@ -173,7 +173,7 @@ gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_cons
                     d[rt][h] = in ? __ldg(srow[rt][h] + g * kSub) : 0u;
                     if (QG != 0) {
                         const int zq = in && zrow[rt][h] ? __ldg(zrow[rt][h] + g * kSub) : 0;
-                        z[rt][h] = static_cast<uint32_t>(0x4308 + zq);  // bf16(136 + z'), z' in [-8, 7]
+                        z[rt][h] = static_cast<uint32_t>(zq);  // z' in [-8, 7], as loaded: 136 + z' is formed at use
                     }
                 }
         };
@@ -223,7 +223,7 @@ gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_cons
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             d2[rt][h] = d_cur[rt][h] | (d_cur[rt][h] << 16);
-                            o2[rt][h] = QG == 0 ? 0x43084308u : (z_cur[rt][h] | (z_cur[rt][h] << 16));
+                            o2[rt][h] = QG == 0 ? 0x43084308u : ((0x4308u + z_cur[rt][h]) | ((0x4308u + z_cur[rt][h]) << 16));
                         }
                     if (MT <= 2) {
                         // Registers allow every row tile's chunks in flight at once.

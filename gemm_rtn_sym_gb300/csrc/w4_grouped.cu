@@ -254,7 +254,7 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
                     d_nxt[rt][h] = in ? __ldg(srow[rt][h] + g * kSub) : 0u;
                     if (QG != 0) {
                         const int zq = in && zrow[rt][h] ? __ldg(zrow[rt][h] + g * kSub) : 0;
-                        z_nxt[rt][h] = static_cast<uint32_t>(0x4308 + zq);  // bf16(136 + z'), z' in [-8, 7]
+                        z_nxt[rt][h] = static_cast<uint32_t>(zq);  // z' in [-8, 7], as loaded: 136 + z' is formed at use
                     }
                 }
         };
@@ -300,7 +300,7 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
                             for (int h = 0; h < 2; ++h) {
                                 d2[rt][h] = d_cur[rt][h] | (d_cur[rt][h] << 16);
                                 // bf16x2 (136 + z', 136 + z'); z' = 0 for symmetric codes
-                                o2[rt][h] = QG == 0 ? 0x43084308u : (z_cur[rt][h] | (z_cur[rt][h] << 16));
+                                o2[rt][h] = QG == 0 ? 0x43084308u : ((0x4308u + z_cur[rt][h]) | ((0x4308u + z_cur[rt][h]) << 16));
                             }
                         if (MT <= 2) {
                             // Registers allow every row tile's chunks in flight at once.
