@@ -188,51 +188,4 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
     return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
-
-
-// A dequantising thread's running window over its weight row's scale (and
-// zero) entries: eight consecutive entries from an 8-aligned index, loaded as
-// one 16-byte (and one 8-byte) load, with the next eight requested as soon as
-// the window moves onto the current ones.  Per k stage a thread needs one
-// entry (its 32-k chunk's group); loaded one by one, the scale and the zero
-// are two scattered load instructions per thread and stage (32 sectors per
-// warp load).  Usable when a row holds a multiple of 8 entries and the scale
-// (zero) row is 16- (8-) byte aligned; entries are read only inside the row.
-struct ScaleWindow {
-    const uint16_t* srow;
-    const int8_t* zrow;  // null: no zeros (z' = 0)
-    int64_t rg;          // entries per row
-    int64_t base;        // index of s_cur's first entry
-    uint4 s_cur, s_nxt;
-    uint2 z_cur, z_nxt;
-
-    __device__ __forceinline__ void load(int64_t at, uint4& s, uint2& z) const {
-        if (at < rg) {
-            s = __ldg(reinterpret_cast<const uint4*>(srow + at));
-            z = zrow ? __ldg(reinterpret_cast<const uint2*>(zrow + at)) : make_uint2(0u, 0u);
-        }
-    }
-    __device__ __forceinline__ void start(int64_t ia) {
-        base = ia & ~int64_t{7};
-        s_cur = s_nxt = make_uint4(0u, 0u, 0u, 0u);
-        z_cur = z_nxt = make_uint2(0u, 0u);
-        load(base, s_cur, z_cur);
-        load(base + 8, s_nxt, z_nxt);
-    }
-    // Entry ia (≥ the previous call's, by at most 8): scale bits d and zero z'.
-    __device__ __forceinline__ void get(int64_t ia, uint32_t& d, int& z) {
-        if (ia >= base + 8) {
-            s_cur = s_nxt;
-            z_cur = z_nxt;
-            base += 8;
-            load(base + 8, s_nxt, z_nxt);
-        }
-        const int j = static_cast<int>(ia - base);
-        const uint32_t w = j < 4 ? (j < 2 ? s_cur.x : s_cur.y) : (j < 6 ? s_cur.z : s_cur.w);
-        d = (j & 1) ? (w >> 16) : (w & 0xFFFFu);
-        const uint32_t zw = j < 4 ? z_cur.x : z_cur.y;
-        z = static_cast<int>(static_cast<int8_t>((zw >> (8 * (j & 3))) & 0xFFu));
-    }
-};
-
 }  // namespace w4
