@@ -215,7 +215,13 @@ gemv_w4_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_cons
                         wv[rt][0] = lds128(st + w_off + rt * 16 * 64);
                         wv[rt][1] = lds128(st + w_off + rt * 16 * 64 + 8 * 64);
                     }
-                    group_math<MT, TPW>(acc, xw, wv, d_cur);
+                    float dv[TPW][2];
+#pragma unroll
+                    for (int rt = 0; rt < TPW; ++rt) {
+                        dv[rt][0] = bf16_lo(d_cur[rt][0]);
+                        dv[rt][1] = bf16_lo(d_cur[rt][1]);
+                    }
+                    group_math<MT, TPW>(acc, xw, wv, dv);
                 } else {
                     uint32_t d2[TPW][2], o2[TPW][2];
 #pragma unroll
@@ -401,11 +407,13 @@ cudaError_t launch_mt(const __nv_bfloat16* x, int mp, int64_t N, int64_t K, cons
 template <int QG>
 cudaError_t launch_gemv_q(const void* x, int64_t M, int64_t N, int64_t K, const void* packed, const void* scales,
                           const void* zeros, void* y, const DeviceInfo& dev, cudaStream_t stream) {
-    // Row tiles per consumer warp up to 16 token rows: four for the symmetric
+    // Row tiles per consumer warp up to 8 token rows: four for the symmetric
     // format; two (eight consumer warps) for the affine formats, whose
     // per-tile (d, z') pairs and dequantising arithmetic leave four tiles per
     // warp latency-bound (on 2560×9216, asymmetric group 128: 11.3 against
-    // 8.2 µs at M = 1, 14.4 against 10.8 µs at M = 16).
+    // 8.2 µs at M = 1).  From 9 to 16 token rows two tiles per warp for every
+    // format (affine: 14.4 against 10.8 µs at M = 16; symmetric: 8.17
+    // against 7.92 µs at M = 16, 70.9 against 70.5 µs for a 27B layer).
     constexpr int kAffineTpw = QG == 0 ? kTpw : 2;
     CUtensorMap tmap_codes;
     if (cudaError_t e = encode_codes_stage_map(&tmap_codes, packed, N, K, kRowsCta, kStageGroups, CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -420,7 +428,7 @@ cudaError_t launch_gemv_q(const void* x, int64_t M, int64_t N, int64_t K, const 
         __nv_bfloat16* yp = yb + m0 * N;
         const cudaError_t e =
             mp <= 8    ? launch_mt<1, kAffineTpw, QG>(xp, mp, N, K, tmap_codes, sc, zp, yp, dev, stream)
-            : mp <= 16 ? launch_mt<2, kAffineTpw, QG>(xp, mp, N, K, tmap_codes, sc, zp, yp, dev, stream)
+            : mp <= 16 ? launch_mt<2, 2, QG>(xp, mp, N, K, tmap_codes, sc, zp, yp, dev, stream)
             : mp <= 24 ? launch_mt<3, kTpw, QG>(xp, mp, N, K, tmap_codes, sc, zp, yp, dev, stream)
                        : launch_mt<4, kTpw, QG>(xp, mp, N, K, tmap_codes, sc, zp, yp, dev, stream);
         if (e != cudaSuccess) return e;

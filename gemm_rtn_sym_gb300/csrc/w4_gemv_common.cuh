@@ -114,7 +114,7 @@ __device__ __forceinline__ void biased_frag(uint32_t wa, uint32_t wb, uint32_t (
 // every tile.
 template <int MT, int TPW>
 __device__ __forceinline__ void group_math(float (&acc)[TPW][MT][4], const uint32_t (&xw)[MT][16],
-                                           const uint4 (&wv)[TPW][2], const uint32_t (&dbits)[TPW][2]) {
+                                           const uint4 (&wv)[TPW][2], const float (&d)[TPW][2]) {
     float corr[MT][4];  // −136·Σ_k x[m, k] over this group, identical for every row
     float cg[TPW][MT][4];
 #pragma unroll
@@ -146,8 +146,8 @@ __device__ __forceinline__ void group_math(float (&acc)[TPW][MT][4], const uint3
     }
 #pragma unroll
     for (int rt = 0; rt < TPW; ++rt) {
-        const float da = bf16_lo(dbits[rt][0]);
-        const float db = bf16_lo(dbits[rt][1]);
+        const float da = d[rt][0];  // rows gid and gid + 8 of the tile
+        const float db = d[rt][1];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
             acc[rt][mt][0] = fmaf(da, cg[rt][mt][0] + corr[mt][0], acc[rt][mt][0]);

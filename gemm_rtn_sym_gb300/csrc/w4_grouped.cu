@@ -91,13 +91,18 @@ __device__ __forceinline__ void consumer_sync(int n_threads) {
 // reduction buffer and barriers take 9 KB.  With one token tile three CTAs
 // per SM stream faster than two (more warps to hide the decode's dependency
 // latency), unless the items balance badly over that many CTAs.
+// Scales of one stage (symmetric format), staged in shared memory by a warp
+// of their own: 4 groups × 64 rows of bf16.
+constexpr int kScaleStageBytes = kStageGroups * kRowsCta * 2;
+
 template <int MT, int XR, int CPS>
 struct GCfg {
     static constexpr int kXRows = XR;
     static constexpr int kXStageBytes = 2 * kStageGroups * XR * 128;  // [k-block][row][128 B]
     static constexpr int kStageBytes = kCodeStageBytes + kXStageBytes;
     static constexpr int kBudget = (CPS == 3 ? 74 : 112) * 1024 - 9 * 1024;
-    static constexpr int kStages = kBudget / kStageBytes > 5 ? 5 : kBudget / kStageBytes;
+    static constexpr int kPerStage = kStageBytes + kScaleStageBytes;
+    static constexpr int kStages = kBudget / kPerStage > 5 ? 5 : kBudget / kPerStage;
     static_assert(XR == 8 * MT || (MT == 1 && (XR == 2 || XR == 4)), "staged rows");
     static_assert(kStages >= 2, "ring depth");
 };
@@ -111,6 +116,7 @@ template <int MT, int QG>
 struct GTpw {
     static constexpr int value = QG != 0 && MT <= 2 ? 2 : kTpw;
 };
+
 
 // QG: 0 for the symmetric group-128 format; 32, 64 or 128 for the affine
 // formats (group size QG, zero points where a problem has them), which
@@ -127,14 +133,22 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
     constexpr int kConsumers = Warps<TPW>::kConsumers;
     constexpr int kCThreads = 32 * kConsumers;
     constexpr int kRedFloats = kStageGroups * kTiles * 4 * 32;
+    // Symmetric format: the producer warp also stages each stage's scales in
+    // shared memory, so that a consumer lane reads its eight with one 16-byte
+    // load instead of eight scattered global loads (those loads, their
+    // pointers and registers measured 12–14 % of the kernel's time on the
+    // 200-matrix stack).
+    constexpr bool kSmemScales = QG == 0;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
     float* red = reinterpret_cast<float*>(gbase + C::kStages * C::kStageBytes);
-    const uint32_t bar_base = base + C::kStages * C::kStageBytes + kRedFloats * 4;
+    const uint32_t sc_base = base + C::kStages * C::kStageBytes + kRedFloats * 4;
+    const uint32_t bar_base = sc_base + C::kStages * kScaleStageBytes;
     auto full = [&](int s) { return bar_base + 8u * s; };
     auto empty = [&](int s) { return bar_base + 8u * (C::kStages + s); };
+    auto sfull = [&](int s) { return bar_base + 8u * (2 * C::kStages + s); };  // the stage's scales are stored
 
     const GroupedHeader* hdr = reinterpret_cast<const GroupedHeader*>(plan);
     const GroupedProblem* probs = reinterpret_cast<const GroupedProblem*>(plan + sizeof(GroupedHeader));
@@ -153,6 +167,7 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(full(s), 1);
             mbar_init(empty(s), 32 * kConsumers);
+            if (kSmemScales) mbar_init(sfull(s), 32);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_async_smem();
@@ -162,39 +177,112 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
 
     if (warp == 0) {
         // -------------------------------------------------- producer: stages of every item, back to back
-        if (lane == 0) {
-            int s = 0;
-            uint32_t phase = 0;
-            int issued = 0;  // stages issued
-            bool ok = true;
-            for (int i = i_begin; i < i_end && ok; ++i) {
-                const uint2 it = items[i];
-                const GroupedProblem* pr = probs + it.x;
+        // Lane 0 issues the TMA copies of each stage.  With the symmetric
+        // format every lane then stores its share of the stage's scales: stage
+        // t of an item uses the scales of groups 4t .. 4t + 3 of its 64 rows;
+        // the consumer warp taking group cw reads, in lane (gid, tig), the
+        // scales of rows 8j + gid, j = 0..7 (row tile j / 2, row half j % 2),
+        // as the 16 bytes at byte (cw·8 + gid)·16 of the stage's slot.  Lane l
+        // stages rows l and l + 32 (j = l / 8 and 4 + l / 8), its global loads
+        // two stages ahead of its stores.  Rows past N repeat row N − 1 (their
+        // codes are zero); groups past G stage zeros (no consumer takes them).
+        const uint32_t row_off = static_cast<uint32_t>(((lane & 7) * 8 + (lane >> 3)) * 2);
+        int li = i_begin - 1, lt = 0, lT = 0;  // next (item, stage) whose scales to fetch; its stages
+        int lG = 0;
+        bool lvec = false;
+        const uint16_t* lp[2] = {nullptr, nullptr};  // scales of rows l and l + 32 of item li
+        auto fetch = [&](uint2 (&o)[2]) {
+            if (lt == lT) {  // next item with stages
+                lt = 0;
+                lT = 0;
+                while (lT <= 0 && ++li < i_end) lT = probs[items[li].x].T;
+                if (li >= i_end) {
+                    lT = -1;  // fetches past the end stage zeros
+                } else {
+                    const uint2 it = items[li];
+                    const GroupedProblem* pr = probs + it.x;
+                    lG = pr->G;
+                    // One 8-byte load per row where every row's and stage's start is 8-byte aligned.
+                    lvec = (lG & 3) == 0 && (reinterpret_cast<uintptr_t>(pr->scales) & 7u) == 0;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        int64_t n = static_cast<int64_t>(it.y) * kRowsCta + lane + 32 * h;
+                        if (n >= pr->N) n = pr->N - 1;
+                        lp[h] = pr->scales + n * lG;
+                    }
+                }
+            }
+            o[0] = o[1] = make_uint2(0u, 0u);
+            if (lT < 0) return;
+            const int g0 = lt * kStageGroups;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (lvec) {
+                    o[h] = __ldg(reinterpret_cast<const uint2*>(lp[h] + g0));
+                } else {
+                    uint32_t q[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) q[c] = g0 + c < lG ? static_cast<uint32_t>(__ldg(lp[h] + g0 + c)) : 0u;
+                    o[h] = make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+                }
+            }
+            ++lt;
+        };
+        uint2 a[2], b[2], c[2];  // scales of stages k, k + 1, k + 2
+        if (kSmemScales) {
+            fetch(a);
+            fetch(b);
+        }
+        int s = 0;
+        uint32_t phase = 0;
+        int issued = 0;  // stages issued
+        bool ok = true;
+        for (int i = i_begin; i < i_end && ok; ++i) {
+            const uint2 it = items[i];
+            const GroupedProblem* pr = probs + it.x;
+            if (lane == 0) {
                 tensormap_acquire(&pr->codes);
                 tensormap_acquire(&pr->x);
-                const int row = static_cast<int>(it.y) * kRowsCta;
-                for (int t = 0; t < pr->T; ++t) {
-                    if (!mbar_wait_suspend(empty(s), phase ^ 1u)) {
-                        ok = false;
-                        break;
-                    }
+            }
+            const int row = static_cast<int>(it.y) * kRowsCta;
+            for (int t = 0; t < pr->T; ++t) {
+                if (kSmemScales) fetch(c);
+                ok = __all_sync(0xffffffffu, mbar_wait_suspend(empty(s), phase ^ 1u));
+                if (!ok) break;
+                if (lane == 0) {
                     const uint32_t st = base + s * C::kStageBytes;
                     mbar_arrive_expect_tx(full(s), C::kStageBytes);
                     tma_load_3d(st, &pr->codes, 0, row, t * kStageGroups, full(s));
                     tma_load_3d(st + kCodeStageBytes, &pr->x, 0, 0, 2 * kStageGroups * t, full(s));
-                    ++issued;
-                    if (++s == C::kStages) {
-                        s = 0;
-                        phase ^= 1u;
+                }
+                if (kSmemScales) {
+                    const uint32_t slot = sc_base + s * kScaleStageBytes;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t o = slot + row_off + 8u * h;  // j + 4h
+                        sts16(o, a[h].x);
+                        sts16(o + 128u, a[h].x >> 16);
+                        sts16(o + 256u, a[h].y);
+                        sts16(o + 384u, a[h].y >> 16);
                     }
+                    mbar_arrive(sfull(s));
+                    a[0] = b[0];
+                    a[1] = b[1];
+                    b[0] = c[0];
+                    b[1] = c[1];
+                }
+                ++issued;
+                if (++s == C::kStages) {
+                    s = 0;
+                    phase ^= 1u;
                 }
             }
-            if (!ok) {
-                record_status(status, kStatusTimeout);
-                // Drain: every issued copy lands before the CTA may exit.
-                for (int j = issued > C::kStages ? issued - C::kStages : 0; j < issued; ++j)
-                    mbar_wait(full(j % C::kStages), static_cast<uint32_t>(j / C::kStages) & 1u);
-            }
+        }
+        if (!ok && lane == 0) {
+            record_status(status, kStatusTimeout);
+            // Drain: every issued copy lands before the CTA may exit.
+            for (int j = issued > C::kStages ? issued - C::kStages : 0; j < issued; ++j)
+                mbar_wait(full(j % C::kStages), static_cast<uint32_t>(j / C::kStages) & 1u);
         }
         return;
     }
@@ -258,26 +346,40 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
                     }
                 }
         };
-        load_scales(0);
+        if (!kSmemScales) load_scales(0);
         for (int t = 0; t < T; ++t) {
             uint32_t d_cur[TPW][2], z_cur[TPW][2];
+            if (!kSmemScales) {
 #pragma unroll
-            for (int rt = 0; rt < TPW; ++rt) {
-                d_cur[rt][0] = d_nxt[rt][0];
-                d_cur[rt][1] = d_nxt[rt][1];
-                if (QG != 0) {
-                    z_cur[rt][0] = z_nxt[rt][0];
-                    z_cur[rt][1] = z_nxt[rt][1];
+                for (int rt = 0; rt < TPW; ++rt) {
+                    d_cur[rt][0] = d_nxt[rt][0];
+                    d_cur[rt][1] = d_nxt[rt][1];
+                    if (QG != 0) {
+                        z_cur[rt][0] = z_nxt[rt][0];
+                        z_cur[rt][1] = z_nxt[rt][1];
+                    }
                 }
+                load_scales(t + 1);
             }
-            load_scales(t + 1);
             if (!aborted) {
-                aborted = !__all_sync(0xffffffffu, mbar_wait(full(s), phase));
+                aborted = !__all_sync(0xffffffffu,
+                                      mbar_wait(full(s), phase) && (!kSmemScales || mbar_wait(sfull(s), phase)));
                 if (aborted && lane == 0) record_status(status, kStatusTimeout);
             }
             if (!aborted) {
                 const bool active = t * kStageGroups + cw < G;  // warp-uniform
                 if (active) {
+                    if (kSmemScales) {
+                        // Word rt: (row half 0, row half 1) of tile rt (TPW = 4, tile0 = 0).
+                        static_assert(!kSmemScales || TPW == kTiles, "one consumer warp per group");
+                        const uint4 q = lds128(sc_base + s * kScaleStageBytes + static_cast<uint32_t>((cw * 8 + gid) * 16));
+                        const uint32_t wds[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                        for (int rt = 0; rt < TPW; ++rt) {
+                            d_cur[rt][0] = wds[rt] & 0xFFFFu;
+                            d_cur[rt][1] = wds[rt] >> 16;
+                        }
+                    }
                     // Release the stage only after its fragments have been used
                     // (shared-memory loads may still be pending when an arrive
                     // executes; the next TMA copy must not overtake them).
@@ -291,7 +393,13 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
                             wv[rt][0] = lds128(st + w_off + rt * 16 * 64);
                             wv[rt][1] = lds128(st + w_off + rt * 16 * 64 + 8 * 64);
                         }
-                        group_math<MT, TPW>(acc, xw, wv, d_cur);
+                        float dv[TPW][2];
+#pragma unroll
+                        for (int rt = 0; rt < TPW; ++rt) {
+                            dv[rt][0] = bf16_lo(d_cur[rt][0]);
+                            dv[rt][1] = bf16_lo(d_cur[rt][1]);
+                        }
+                        group_math<MT, TPW>(acc, xw, wv, dv);
                     } else {
                         uint32_t d2[TPW][2], o2[TPW][2];
 #pragma unroll
@@ -353,7 +461,8 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
 template <int MT, int XR, int CPS>
 constexpr int grouped_smem_bytes() {
     using C = GCfg<MT, XR, CPS>;
-    return C::kStages * C::kStageBytes + kStageGroups * kTiles * 4 * 32 * 4 + 16 * C::kStages + 1024;
+    return C::kStages * (C::kStageBytes + kScaleStageBytes) + kStageGroups * kTiles * 4 * 32 * 4 + 24 * C::kStages +
+           1024;
 }
 
 std::mutex g_grouped_mutex;

@@ -69,6 +69,29 @@ def test_grouped_new_inputs_and_graph_replay(cuda_lib):
             check_gemm(W, x, y)
 
 
+def test_grouped_unaligned_scales(cuda_lib):
+    """Scales at an address that is 2-byte but not 8-byte aligned are staged
+    one element at a time (otherwise four groups of a row per 8-byte load):
+    the outputs are bit-identical to those of the same problems with aligned
+    scales."""
+    shapes = [(200, 4096), (2560, 512), (96, 30720)]
+    Ws, probs, _ = make_problems(cuda_lib, shapes, [1, 3, 2], seed=11)
+    w4.w4_gemm_grouped(w4.w4_grouped_plan(probs))
+    moved = []
+    for x, p, s, y in probs:
+        buf = torch.empty(s.numel() + 4, dtype=s.dtype, device=DEV)
+        s2 = buf[1:1 + s.numel()].view(s.shape)
+        s2.copy_(s)
+        assert s2.data_ptr() % 8 == 2
+        moved.append((x, p, s2, torch.empty_like(y)))
+    w4.w4_gemm_grouped(w4.w4_grouped_plan(moved))
+    torch.cuda.synchronize()
+    assert w4.w4_last_device_status() == 0
+    for W, (x, _, _, y), (_, _, _, y2) in zip(Ws, probs, moved):
+        check_gemm(W, x, y)
+        assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+
+
 @pytest.mark.parametrize("Ms", [[17, 33, 64, 208, 100, 257, 19], [1, 40, 13, 208, 8, 24, 2],
                                 [32, 28, 1, 5, 64, 25, 33]])
 def test_grouped_tensor_and_mixed(cuda_lib, Ms):
