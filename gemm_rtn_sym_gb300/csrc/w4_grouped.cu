@@ -95,13 +95,18 @@ __device__ __forceinline__ void consumer_sync(int n_threads) {
 // of their own: 4 groups × 64 rows of bf16.
 constexpr int kScaleStageBytes = kStageGroups * kRowsCta * 2;
 
-template <int MT, int XR, int CPS>
+template <int MT, int XR, int CPS, int QG>
 struct GCfg {
     static constexpr int kXRows = XR;
     static constexpr int kXStageBytes = 2 * kStageGroups * XR * 128;  // [k-block][row][128 B]
     static constexpr int kStageBytes = kCodeStageBytes + kXStageBytes;
+    // Scale slot of a stage: the symmetric format's 4 groups × 64 rows of
+    // bf16; the affine formats' kE (d, z') entries per row (d bf16 as
+    // [row][kE], then z' int8 as [row][kE]), kE = the stage's 512 k / QG.
+    static constexpr int kE = QG == 0 ? kStageGroups : kStageGroups * 128 / QG;
+    static constexpr int kScaleSlotBytes = QG == 0 ? kScaleStageBytes : kRowsCta * kE * 3;
     static constexpr int kBudget = (CPS == 3 ? 74 : 112) * 1024 - 9 * 1024;
-    static constexpr int kPerStage = kStageBytes + kScaleStageBytes;
+    static constexpr int kPerStage = kStageBytes + kScaleSlotBytes;
     static constexpr int kStages = kBudget / kPerStage > 5 ? 5 : kBudget / kPerStage;
     static_assert(XR == 8 * MT || (MT == 1 && (XR == 2 || XR == 4)), "staged rows");
     static_assert(kStages >= 2, "ring depth");
@@ -117,35 +122,45 @@ struct GTpw {
     static constexpr int value = QG != 0 && MT <= 2 ? 2 : kTpw;
 };
 
+// Threads of a CTA: the TMA producer warp, the consumer warps and, for the
+// affine formats, a warp that stages the scales and zero points.
+template <int MT, int QG>
+struct GThreads {
+    static constexpr int value = Warps<GTpw<MT, QG>::value>::kThreads + (QG != 0 ? 32 : 0);
+};
+
 
 // QG: 0 for the symmetric group-128 format; 32, 64 or 128 for the affine
 // formats (group size QG, zero points where a problem has them), which
 // dequantise every weight to bf16(d·(c − z')) as the single-matrix kernel does.
 template <int MT, int XR, int CPS, int QG>
-__global__ void __launch_bounds__(Warps<GTpw<MT, QG>::value>::kThreads, CPS)
+__global__ void __launch_bounds__(GThreads<MT, QG>::value, CPS)
 gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
-    using C = GCfg<MT, XR, CPS>;
+    using C = GCfg<MT, XR, CPS, QG>;
     constexpr int TPW = GTpw<MT, QG>::value;
     constexpr bool kDeq = QG != 0 || Dequant<MT>::value;
-    // The QG-group holding a thread's 32 codes of a 128-k block (k 32·tig ..
-    // 32·tig + 31) is (128/QG)·g + sub.
-    constexpr int kSub = QG == 0 ? 1 : 128 / QG;
     constexpr int kConsumers = Warps<TPW>::kConsumers;
     constexpr int kCThreads = 32 * kConsumers;
     constexpr int kRedFloats = kStageGroups * kTiles * 4 * 32;
-    // Symmetric format: the producer warp also stages each stage's scales in
-    // shared memory, so that a consumer lane reads its eight with one 16-byte
-    // load instead of eight scattered global loads (those loads, their
-    // pointers and registers measured 12–14 % of the kernel's time on the
-    // 200-matrix stack).
+    // Each stage's scales (and zero points) are staged in shared memory,
+    // replacing the consumers' scattered global loads of them (those loads,
+    // their pointers and registers measured 12–14 % of the kernel's time on
+    // the 200-matrix stack, 22–26 % with zero points on the 27B-class layer).
+    // Symmetric format: the producer warp stores a transposed slot, read with
+    // one 16-byte load per consumer lane.  Affine formats: a warp of its own
+    // copies the rows as stored with cp.async (done by the producer warp, the
+    // copies or loads of these small rows delayed its TMA issue and every
+    // stage behind it).
     constexpr bool kSmemScales = QG == 0;
+    constexpr int kE = C::kE;
+    constexpr int kStagerWarp = 1 + kConsumers;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
     float* red = reinterpret_cast<float*>(gbase + C::kStages * C::kStageBytes);
     const uint32_t sc_base = base + C::kStages * C::kStageBytes + kRedFloats * 4;
-    const uint32_t bar_base = sc_base + C::kStages * kScaleStageBytes;
+    const uint32_t bar_base = sc_base + C::kStages * C::kScaleSlotBytes;
     auto full = [&](int s) { return bar_base + 8u * s; };
     auto empty = [&](int s) { return bar_base + 8u * (C::kStages + s); };
     auto sfull = [&](int s) { return bar_base + 8u * (2 * C::kStages + s); };  // the stage's scales are stored
@@ -167,7 +182,7 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(full(s), 1);
             mbar_init(empty(s), 32 * kConsumers);
-            if (kSmemScales) mbar_init(sfull(s), 32);
+            mbar_init(sfull(s), 32);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_async_smem();
@@ -256,7 +271,7 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
                     tma_load_3d(st + kCodeStageBytes, &pr->x, 0, 0, 2 * kStageGroups * t, full(s));
                 }
                 if (kSmemScales) {
-                    const uint32_t slot = sc_base + s * kScaleStageBytes;
+                    const uint32_t slot = sc_base + s * C::kScaleSlotBytes;
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const uint32_t o = slot + row_off + 8u * h;  // j + 4h
@@ -287,6 +302,85 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
         return;
     }
 
+    if (!kSmemScales && warp == kStagerWarp) {
+        // -------------------------------------------------- affine stager
+        // Stage t of an item: the kE (d, z') entries t·kE .. of rows l and
+        // l + 32 (rows past N repeat row N − 1, whose codes are zero) into the
+        // stage's slot, d as [row][kE] bf16 then z' as [row][kE] int8, with
+        // cp.async in the largest chunks (16, 8 or 4 bytes) that the row
+        // stride, the base and a stage's entries allow, else element by
+        // element; the lane's arrival on the stage's barrier is made when its
+        // copies have landed.  Entries past the end of a row are not written
+        // (no consumer takes them).
+        auto chunk = [](int64_t stride, uintptr_t addr, int per_stage) {
+            for (int c = 16; c >= 4; c >>= 1)
+                if (stride % c == 0 && addr % c == 0 && per_stage % c == 0) return c;
+            return 0;
+        };
+        int s = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int i = i_begin; i < i_end && ok; ++i) {
+            const uint2 it = items[i];
+            const GroupedProblem* pr = probs + it.x;
+            const int64_t arg = pr->row_groups;
+            const uint16_t* drow[2];
+            const int8_t* zrow[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                int64_t n = static_cast<int64_t>(it.y) * kRowsCta + lane + 32 * h;
+                if (n >= pr->N) n = pr->N - 1;
+                drow[h] = pr->scales + n * arg;
+                zrow[h] = pr->zeros ? pr->zeros + n * arg : nullptr;
+            }
+            const int cd = chunk(2 * arg, reinterpret_cast<uintptr_t>(pr->scales), 2 * kE);
+            const int cz = pr->zeros ? chunk(arg, reinterpret_cast<uintptr_t>(pr->zeros), kE) : 0;
+            for (int t = 0; t < pr->T; ++t) {
+                ok = __all_sync(0xffffffffu, mbar_wait_suspend(empty(s), phase ^ 1u));
+                if (!ok) break;
+                const uint32_t slot = sc_base + s * C::kScaleSlotBytes;
+                const int64_t e0 = static_cast<int64_t>(t) * kE;
+                const int ne = static_cast<int>(arg - e0 < kE ? arg - e0 : kE);  // entries inside the row
+                bool plain = false;  // some entries stored with plain stores
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t r = static_cast<uint32_t>(lane + 32 * h);
+                    const uint32_t dd = slot + r * (2 * kE);
+                    const uint16_t* ds = drow[h] + e0;
+                    if (cd) {
+                        for (int b = 0; b < 2 * ne; b += cd) cp_async_n(dd + b, reinterpret_cast<const uint8_t*>(ds) + b, cd);
+                    } else {
+                        for (int e = 0; e < ne; ++e) sts16(dd + 2 * e, __ldg(ds + e));
+                        plain = true;
+                    }
+                    if (zrow[h]) {
+                        const uint32_t zd = slot + kRowsCta * 2 * kE + r * kE;
+                        const int8_t* zs = zrow[h] + e0;
+                        if (cz) {
+                            for (int b = 0; b < ne; b += cz) cp_async_n(zd + b, zs + b, cz);
+                        } else {
+                            for (int e = 0; e < ne; ++e) sts8(zd + e, static_cast<uint32_t>(__ldg(zs + e)));
+                            plain = true;
+                        }
+                    }
+                }
+                if (plain) {
+                    cp_async_wait_all();
+                    mbar_arrive(sfull(s));
+                } else {
+                    cp_async_arrive(sfull(s));
+                }
+                if (++s == C::kStages) {
+                    s = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok && lane == 0) record_status(status, kStatusTimeout);
+        cp_async_wait_all();  // no copy of this thread outlives it
+        return;
+    }
+
     // ------------------------------------------------------ consumers
     // Every consumer warp runs the same sequence of items, stages and named
     // barriers; after a timed-out wait a warp only skips work.
@@ -308,21 +402,11 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
         const int M = pr->M;
         __nv_bfloat16* const y = pr->y;  // read once: stores to y could alias the record
         const int64_t row0 = static_cast<int64_t>(it.y) * kRowsCta;
-        // Scale rows gid / gid+8 of each tile (clamped: rows past N have zero codes).
+        // Affine formats: this lane's entry of each staged row, the QG-group
+        // holding its 32 codes of the warp's 128-k group (k 32·tig .. +31).
         const int sub = QG == 32 ? tig : (QG == 64 ? (tig >> 1) : 0);
-        const int64_t rg = QG == 0 ? G : pr->row_groups;
-        const int8_t* const zeros = QG == 0 ? nullptr : pr->zeros;
-        const uint16_t* srow[TPW][2];
-        const int8_t* zrow[TPW][2];
-#pragma unroll
-        for (int rt = 0; rt < TPW; ++rt)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                int64_t n = row0 + (tile0 + rt) * 16 + gid + 8 * h;
-                if (n >= N) n = N - 1;
-                srow[rt][h] = pr->scales + n * rg + sub;
-                zrow[rt][h] = zeros ? zeros + n * rg + sub : nullptr;
-            }
+        const bool has_z = QG != 0 && pr->zeros != nullptr;
+        const uint32_t a_off = static_cast<uint32_t>((tile0 * 16 + gid) * kE + cw * (kE / kStageGroups) + sub);
         float acc[TPW][MT][4];
 #pragma unroll
         for (int rt = 0; rt < TPW; ++rt)
@@ -330,55 +414,37 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
                 for (int r = 0; r < 4; ++r) acc[rt][mt][r] = 0.0f;
-        // d: scale bits; affine formats also z: bf16 bits of 136 + z'.
-        uint32_t d_nxt[TPW][2], z_nxt[TPW][2];
-        auto load_scales = [&](int t) {
-            const int g = t * kStageGroups + cw;
-            const bool in = t < T && g < G;
-#pragma unroll
-            for (int rt = 0; rt < TPW; ++rt)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    d_nxt[rt][h] = in ? __ldg(srow[rt][h] + g * kSub) : 0u;
-                    if (QG != 0) {
-                        const int zq = in && zrow[rt][h] ? __ldg(zrow[rt][h] + g * kSub) : 0;
-                        z_nxt[rt][h] = static_cast<uint32_t>(zq);  // z' in [-8, 7], as loaded: 136 + z' is formed at use
-                    }
-                }
-        };
-        if (!kSmemScales) load_scales(0);
         for (int t = 0; t < T; ++t) {
+            // d: scale bits; affine formats also z': the zero as stored (136 + z' is formed at use).
             uint32_t d_cur[TPW][2], z_cur[TPW][2];
-            if (!kSmemScales) {
-#pragma unroll
-                for (int rt = 0; rt < TPW; ++rt) {
-                    d_cur[rt][0] = d_nxt[rt][0];
-                    d_cur[rt][1] = d_nxt[rt][1];
-                    if (QG != 0) {
-                        z_cur[rt][0] = z_nxt[rt][0];
-                        z_cur[rt][1] = z_nxt[rt][1];
-                    }
-                }
-                load_scales(t + 1);
-            }
             if (!aborted) {
-                aborted = !__all_sync(0xffffffffu,
-                                      mbar_wait(full(s), phase) && (!kSmemScales || mbar_wait(sfull(s), phase)));
+                aborted = !__all_sync(0xffffffffu, mbar_wait(full(s), phase) && mbar_wait(sfull(s), phase));
                 if (aborted && lane == 0) record_status(status, kStatusTimeout);
             }
             if (!aborted) {
                 const bool active = t * kStageGroups + cw < G;  // warp-uniform
                 if (active) {
+                    const uint32_t slot = sc_base + s * C::kScaleSlotBytes;
                     if (kSmemScales) {
                         // Word rt: (row half 0, row half 1) of tile rt (TPW = 4, tile0 = 0).
                         static_assert(!kSmemScales || TPW == kTiles, "one consumer warp per group");
-                        const uint4 q = lds128(sc_base + s * kScaleStageBytes + static_cast<uint32_t>((cw * 8 + gid) * 16));
+                        const uint4 q = lds128(slot + static_cast<uint32_t>((cw * 8 + gid) * 16));
                         const uint32_t wds[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
                         for (int rt = 0; rt < TPW; ++rt) {
                             d_cur[rt][0] = wds[rt] & 0xFFFFu;
                             d_cur[rt][1] = wds[rt] >> 16;
                         }
+                    } else {
+                        // Row (tile0 + rt)·16 + gid + 8h of the slot: entry a_off + (16·rt + 8h)·kE.
+#pragma unroll
+                        for (int rt = 0; rt < TPW; ++rt)
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const uint32_t e = a_off + static_cast<uint32_t>((16 * rt + 8 * h) * kE);
+                                d_cur[rt][h] = lds_u16(slot + 2 * e);
+                                z_cur[rt][h] = has_z ? static_cast<uint32_t>(lds_s8(slot + kRowsCta * 2 * kE + e)) : 0u;
+                            }
                     }
                     // Release the stage only after its fragments have been used
                     // (shared-memory loads may still be pending when an arrive
@@ -458,11 +524,11 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
     }
 }
 
-template <int MT, int XR, int CPS>
+template <int MT, int XR, int CPS, int QG>
 constexpr int grouped_smem_bytes() {
-    using C = GCfg<MT, XR, CPS>;
-    return C::kStages * (C::kStageBytes + kScaleStageBytes) + kStageGroups * kTiles * 4 * 32 * 4 + 24 * C::kStages +
-           1024;
+    using C = GCfg<MT, XR, CPS, QG>;
+    return C::kStages * (C::kStageBytes + C::kScaleSlotBytes) + kStageGroups * kTiles * 4 * 32 * 4 +
+           24 * C::kStages + 1024;
 }
 
 std::mutex g_grouped_mutex;
@@ -475,10 +541,10 @@ int grouped_ctas_per_sm(int device) {
     if (per_device[device] == 0) {
         int v = 0;
         if (cudaFuncSetAttribute(gemv_grouped_kernel<MT, XR, CPS, QG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 grouped_smem_bytes<MT, XR, CPS>()) != cudaSuccess ||
+                                 grouped_smem_bytes<MT, XR, CPS, QG>()) != cudaSuccess ||
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, gemv_grouped_kernel<MT, XR, CPS, QG>,
-                                                          Warps<GTpw<MT, QG>::value>::kThreads,
-                                                          grouped_smem_bytes<MT, XR, CPS>()) != cudaSuccess ||
+                                                          GThreads<MT, QG>::value,
+                                                          grouped_smem_bytes<MT, XR, CPS, QG>()) != cudaSuccess ||
             v < 1) {
             cudaGetLastError();
             return 0;
@@ -495,8 +561,8 @@ cudaError_t launch_grouped_t(const void* plan, int32_t n_ctas, const DeviceInfo&
     if (grouped_ctas_per_sm<MT, XR, CPS, QG>(device) < 1) return cudaErrorInvalidConfiguration;  // sets the smem attribute
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(n_ctas), 1, 1);
-    cfg.blockDim = dim3(Warps<GTpw<MT, QG>::value>::kThreads, 1, 1);
-    cfg.dynamicSmemBytes = grouped_smem_bytes<MT, XR, CPS>();
+    cfg.blockDim = dim3(GThreads<MT, QG>::value, 1, 1);
+    cfg.dynamicSmemBytes = grouped_smem_bytes<MT, XR, CPS, QG>();
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
