@@ -122,11 +122,13 @@ struct GTpw {
     static constexpr int value = QG != 0 && MT <= 2 ? 2 : kTpw;
 };
 
-// Threads of a CTA: the TMA producer warp, the consumer warps and, for the
-// affine formats, a warp that stages the scales and zero points.
-template <int MT, int QG>
+// Threads of a CTA: the TMA producer warp, the consumer warps and, except
+// for the symmetric format at three CTAs per SM (where a sixth warp would
+// leave 96 registers a thread), a warp that stages the scales (and zero points).
+template <int MT, int QG, int CPS>
 struct GThreads {
-    static constexpr int value = Warps<GTpw<MT, QG>::value>::kThreads + (QG != 0 ? 32 : 0);
+    static constexpr bool kStager = QG != 0 || CPS != 3;
+    static constexpr int value = Warps<GTpw<MT, QG>::value>::kThreads + (kStager ? 32 : 0);
 };
 
 
@@ -134,7 +136,7 @@ struct GThreads {
 // formats (group size QG, zero points where a problem has them), which
 // dequantise every weight to bf16(d·(c − z')) as the single-matrix kernel does.
 template <int MT, int XR, int CPS, int QG>
-__global__ void __launch_bounds__(GThreads<MT, QG>::value, CPS)
+__global__ void __launch_bounds__(GThreads<MT, QG, CPS>::value, CPS)
 gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
     using C = GCfg<MT, XR, CPS, QG>;
     constexpr int TPW = GTpw<MT, QG>::value;
@@ -146,13 +148,16 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
     // replacing the consumers' scattered global loads of them (those loads,
     // their pointers and registers measured 12–14 % of the kernel's time on
     // the 200-matrix stack, 22–26 % with zero points on the 27B-class layer).
-    // Symmetric format: the producer warp stores a transposed slot, read with
-    // one 16-byte load per consumer lane.  Affine formats: a warp of its own
-    // copies the rows as stored with cp.async (done by the producer warp, the
-    // copies or loads of these small rows delayed its TMA issue and every
-    // stage behind it).
+    // Symmetric format: a transposed slot, read with one 16-byte load per
+    // consumer lane.  Affine formats: the rows as stored, copied with
+    // cp.async.  A warp of its own stages them (done by the producer warp, the
+    // loads or copies of these small rows delay its TMA issue and every stage
+    // behind it), except for the symmetric format at three CTAs per SM, where
+    // the producer warp does.
     constexpr bool kSmemScales = QG == 0;
     constexpr int kE = C::kE;
+    constexpr bool kStager = GThreads<MT, QG, CPS>::kStager;
+    constexpr bool kProducerScales = kSmemScales && !kStager;  // the producer warp stages them
     constexpr int kStagerWarp = 1 + kConsumers;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -190,61 +195,72 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
     __syncthreads();
     pdl_start();
 
+    // Symmetric format: stage t of an item uses the scales of groups
+    // 4t .. 4t + 3 of its 64 rows; the consumer warp taking group cw reads, in
+    // lane (gid, tig), the scales of rows 8j + gid, j = 0..7 (row tile j / 2,
+    // row half j % 2), as the 16 bytes at byte (cw·8 + gid)·16 of the stage's
+    // slot.  Lane l of the staging warp stages rows l and l + 32 (j = l / 8
+    // and 4 + l / 8), its global loads two stages ahead of its stores.  Rows
+    // past N repeat row N − 1 (their codes are zero); groups past G stage zeros
+    // (no consumer takes them).
+    const uint32_t row_off = static_cast<uint32_t>(((lane & 7) * 8 + (lane >> 3)) * 2);
+    int li = i_begin - 1, lt = 0, lT = 0;  // next (item, stage) whose scales to fetch; its stages
+    int lG = 0;
+    bool lvec = false;
+    const uint16_t* lp[2] = {nullptr, nullptr};  // scales of rows l and l + 32 of item li
+    auto fetch = [&](uint2 (&o)[2]) {
+        if (lt == lT) {  // next item with stages
+            lt = 0;
+            lT = 0;
+            while (lT <= 0 && ++li < i_end) lT = probs[items[li].x].T;
+            if (li >= i_end) {
+                lT = -1;  // fetches past the end stage zeros
+            } else {
+                const uint2 it = items[li];
+                const GroupedProblem* pr = probs + it.x;
+                lG = pr->G;
+                // One 8-byte load per row where every row's and stage's start is 8-byte aligned.
+                lvec = (lG & 3) == 0 && (reinterpret_cast<uintptr_t>(pr->scales) & 7u) == 0;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    int64_t n = static_cast<int64_t>(it.y) * kRowsCta + lane + 32 * h;
+                    if (n >= pr->N) n = pr->N - 1;
+                    lp[h] = pr->scales + n * lG;
+                }
+            }
+        }
+        o[0] = o[1] = make_uint2(0u, 0u);
+        if (lT < 0) return;
+        const int g0 = lt * kStageGroups;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (lvec) {
+                o[h] = __ldg(reinterpret_cast<const uint2*>(lp[h] + g0));
+            } else {
+                uint32_t q[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) q[c] = g0 + c < lG ? static_cast<uint32_t>(__ldg(lp[h] + g0 + c)) : 0u;
+                o[h] = make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+            }
+        }
+        ++lt;
+    };
+    auto store_sym = [&](uint32_t slot, const uint2 (&v)[2]) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t o = slot + row_off + 8u * h;  // j + 4h
+            sts16(o, v[h].x);
+            sts16(o + 128u, v[h].x >> 16);
+            sts16(o + 256u, v[h].y);
+            sts16(o + 384u, v[h].y >> 16);
+        }
+    };
     if (warp == 0) {
         // -------------------------------------------------- producer: stages of every item, back to back
-        // Lane 0 issues the TMA copies of each stage.  With the symmetric
-        // format every lane then stores its share of the stage's scales: stage
-        // t of an item uses the scales of groups 4t .. 4t + 3 of its 64 rows;
-        // the consumer warp taking group cw reads, in lane (gid, tig), the
-        // scales of rows 8j + gid, j = 0..7 (row tile j / 2, row half j % 2),
-        // as the 16 bytes at byte (cw·8 + gid)·16 of the stage's slot.  Lane l
-        // stages rows l and l + 32 (j = l / 8 and 4 + l / 8), its global loads
-        // two stages ahead of its stores.  Rows past N repeat row N − 1 (their
-        // codes are zero); groups past G stage zeros (no consumer takes them).
-        const uint32_t row_off = static_cast<uint32_t>(((lane & 7) * 8 + (lane >> 3)) * 2);
-        int li = i_begin - 1, lt = 0, lT = 0;  // next (item, stage) whose scales to fetch; its stages
-        int lG = 0;
-        bool lvec = false;
-        const uint16_t* lp[2] = {nullptr, nullptr};  // scales of rows l and l + 32 of item li
-        auto fetch = [&](uint2 (&o)[2]) {
-            if (lt == lT) {  // next item with stages
-                lt = 0;
-                lT = 0;
-                while (lT <= 0 && ++li < i_end) lT = probs[items[li].x].T;
-                if (li >= i_end) {
-                    lT = -1;  // fetches past the end stage zeros
-                } else {
-                    const uint2 it = items[li];
-                    const GroupedProblem* pr = probs + it.x;
-                    lG = pr->G;
-                    // One 8-byte load per row where every row's and stage's start is 8-byte aligned.
-                    lvec = (lG & 3) == 0 && (reinterpret_cast<uintptr_t>(pr->scales) & 7u) == 0;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        int64_t n = static_cast<int64_t>(it.y) * kRowsCta + lane + 32 * h;
-                        if (n >= pr->N) n = pr->N - 1;
-                        lp[h] = pr->scales + n * lG;
-                    }
-                }
-            }
-            o[0] = o[1] = make_uint2(0u, 0u);
-            if (lT < 0) return;
-            const int g0 = lt * kStageGroups;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                if (lvec) {
-                    o[h] = __ldg(reinterpret_cast<const uint2*>(lp[h] + g0));
-                } else {
-                    uint32_t q[4];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) q[c] = g0 + c < lG ? static_cast<uint32_t>(__ldg(lp[h] + g0 + c)) : 0u;
-                    o[h] = make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
-                }
-            }
-            ++lt;
-        };
+        // Lane 0 issues the TMA copies of each stage; where the producer warp
+        // stages the symmetric scales, every lane then stores its share.
         uint2 a[2], b[2], c[2];  // scales of stages k, k + 1, k + 2
-        if (kSmemScales) {
+        if (kProducerScales) {
             fetch(a);
             fetch(b);
         }
@@ -261,7 +277,7 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
             }
             const int row = static_cast<int>(it.y) * kRowsCta;
             for (int t = 0; t < pr->T; ++t) {
-                if (kSmemScales) fetch(c);
+                if (kProducerScales) fetch(c);
                 ok = __all_sync(0xffffffffu, mbar_wait_suspend(empty(s), phase ^ 1u));
                 if (!ok) break;
                 if (lane == 0) {
@@ -270,16 +286,8 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
                     tma_load_3d(st, &pr->codes, 0, row, t * kStageGroups, full(s));
                     tma_load_3d(st + kCodeStageBytes, &pr->x, 0, 0, 2 * kStageGroups * t, full(s));
                 }
-                if (kSmemScales) {
-                    const uint32_t slot = sc_base + s * C::kScaleSlotBytes;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint32_t o = slot + row_off + 8u * h;  // j + 4h
-                        sts16(o, a[h].x);
-                        sts16(o + 128u, a[h].x >> 16);
-                        sts16(o + 256u, a[h].y);
-                        sts16(o + 384u, a[h].y >> 16);
-                    }
+                if (kProducerScales) {
+                    store_sym(sc_base + s * C::kScaleSlotBytes, a);
                     mbar_arrive(sfull(s));
                     a[0] = b[0];
                     a[1] = b[1];
@@ -299,6 +307,36 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
             for (int j = issued > C::kStages ? issued - C::kStages : 0; j < issued; ++j)
                 mbar_wait(full(j % C::kStages), static_cast<uint32_t>(j / C::kStages) & 1u);
         }
+        return;
+    }
+
+    if (kStager && kSmemScales && warp == kStagerWarp) {
+        // -------------------------------------------------- symmetric stager
+        uint2 a[2], b[2], c[2];  // scales of stages k, k + 1, k + 2
+        fetch(a);
+        fetch(b);
+        int s = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int i = i_begin; i < i_end && ok; ++i) {
+            const int T = probs[items[i].x].T;
+            for (int t = 0; t < T; ++t) {
+                fetch(c);
+                ok = __all_sync(0xffffffffu, mbar_wait_suspend(empty(s), phase ^ 1u));
+                if (!ok) break;
+                store_sym(sc_base + s * C::kScaleSlotBytes, a);
+                mbar_arrive(sfull(s));
+                a[0] = b[0];
+                a[1] = b[1];
+                b[0] = c[0];
+                b[1] = c[1];
+                if (++s == C::kStages) {
+                    s = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok && lane == 0) record_status(status, kStatusTimeout);
         return;
     }
 
@@ -543,7 +581,7 @@ int grouped_ctas_per_sm(int device) {
         if (cudaFuncSetAttribute(gemv_grouped_kernel<MT, XR, CPS, QG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  grouped_smem_bytes<MT, XR, CPS, QG>()) != cudaSuccess ||
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, gemv_grouped_kernel<MT, XR, CPS, QG>,
-                                                          GThreads<MT, QG>::value,
+                                                          GThreads<MT, QG, CPS>::value,
                                                           grouped_smem_bytes<MT, XR, CPS, QG>()) != cudaSuccess ||
             v < 1) {
             cudaGetLastError();
@@ -561,7 +599,7 @@ cudaError_t launch_grouped_t(const void* plan, int32_t n_ctas, const DeviceInfo&
     if (grouped_ctas_per_sm<MT, XR, CPS, QG>(device) < 1) return cudaErrorInvalidConfiguration;  // sets the smem attribute
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(n_ctas), 1, 1);
-    cfg.blockDim = dim3(GThreads<MT, QG>::value, 1, 1);
+    cfg.blockDim = dim3(GThreads<MT, QG, CPS>::value, 1, 1);
     cfg.dynamicSmemBytes = grouped_smem_bytes<MT, XR, CPS, QG>();
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
