@@ -232,6 +232,36 @@ def test_grouped_affine_parity(cuda_lib, group, asym, Ms):
         assert torch.equal(f.view(torch.int16), y.view(torch.int16))
 
 
+@pytest.mark.parametrize("group", [32, 64, 128])
+def test_grouped_affine_unaligned_scales_and_zeros(cuda_lib, group):
+    """Scales at a 2-byte and zero points at a 1-byte aligned address are
+    staged element by element instead of in 4- to 16-byte copies: outputs
+    bit-identical to those of the same problems with aligned ones."""
+    shapes = [(200, 4096), (96, 2560), (64, 1152)]
+    probs, zs, moved, zs2 = [], [], [], []
+    for i, (N, K) in enumerate(shapes):
+        W = wl.random_bf16((N, K), 0.02, seed=70 + i + group, device=DEV)
+        x = wl.random_bf16((1 + 3 * i, K), 1.0, seed=80 + i, device=DEV)
+        packed, scales, zeros = quantize_gpu(cuda_lib, W, group, True)
+        probs.append((x, packed, scales, torch.empty((x.shape[0], N), dtype=torch.bfloat16, device=DEV)))
+        zs.append(zeros)
+        sbuf = torch.empty(scales.numel() + 8, dtype=scales.dtype, device=DEV)
+        s2 = sbuf[1:1 + scales.numel()].view(scales.shape)
+        s2.copy_(scales)
+        zbuf = torch.empty(zeros.numel() + 16, dtype=zeros.dtype, device=DEV)
+        z2 = zbuf[1:1 + zeros.numel()].view(zeros.shape)
+        z2.copy_(zeros)
+        assert s2.data_ptr() % 4 == 2 and z2.data_ptr() % 2 == 1
+        moved.append((x, packed, s2, torch.empty_like(probs[-1][3])))
+        zs2.append(z2)
+    cuda_lib.w4_gemm_grouped(cuda_lib.w4_grouped_plan(probs, group=group, zeros=zs))
+    cuda_lib.w4_gemm_grouped(cuda_lib.w4_grouped_plan(moved, group=group, zeros=zs2))
+    torch.cuda.synchronize()
+    assert cuda_lib.w4_last_device_status() == 0
+    for (_, _, _, y), (_, _, _, y2) in zip(probs, moved):
+        assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+
+
 def test_grouped_affine_group128_without_zeros_is_the_symmetric_plan(cuda_lib):
     W = wl.random_bf16((500, 2048), 0.02, seed=3, device=DEV)
     x = wl.random_bf16((5, 2048), 1.0, seed=4, device=DEV)
