@@ -84,6 +84,10 @@ __device__ __forceinline__ void consumer_sync(int n_threads) {
     asm volatile("bar.sync 1, %0;" ::"r"(n_threads) : "memory");
 }
 
+// Scales of one stage of the symmetric format in shared memory: 4 groups × 64
+// rows of bf16.
+constexpr int kScaleStageBytes = kStageGroups * kRowsCta * 2;
+
 // Geometry of the grouped kernel for MT token tiles with XR token rows staged
 // per 64-k block (XR < 8 only for one tile: a decode step of one or two tokens
 // stages one or two rows, not eight), run with CPS CTAs per SM.  The ring is
@@ -91,10 +95,6 @@ __device__ __forceinline__ void consumer_sync(int n_threads) {
 // reduction buffer and barriers take 9 KB.  With one token tile three CTAs
 // per SM stream faster than two (more warps to hide the decode's dependency
 // latency), unless the items balance badly over that many CTAs.
-// Scales of one stage (symmetric format), staged in shared memory by a warp
-// of their own: 4 groups × 64 rows of bf16.
-constexpr int kScaleStageBytes = kStageGroups * kRowsCta * 2;
-
 template <int MT, int XR, int CPS, int QG>
 struct GCfg {
     static constexpr int kXRows = XR;
