@@ -542,21 +542,47 @@ gemv_grouped_kernel(const uint8_t* __restrict__ plan, unsigned* status) {
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
             consumer_sync(kCThreads);  // the previous readers of red are done
+            if constexpr (TPW == kTiles && MT <= 2) {
+                // Four warps, one per group of a stage, each holding every tile:
+                // warp cw sums, for every tile, the elements acc[.][mt][cw] whose
+                // own partial it holds, and writes only the other three (1–2 %
+                // faster up to 16 token rows; at 24, 6 % slower).
 #pragma unroll
-            for (int rt = 0; rt < TPW; ++rt)
+                for (int rt = 0; rt < TPW; ++rt)
 #pragma unroll
-                for (int r = 0; r < 4; ++r) red[((cw * kTiles + tile0 + rt) * 4 + r) * 32 + lane] = acc[rt][mt][r];
-            consumer_sync(kCThreads);
-            for (int e = ctid; e < kTiles * 4 * 32; e += kCThreads) {
-                const int l = e & 31;
-                const int r = (e >> 5) & 3;
-                const int rt = e >> 7;
-                float v = 0.0f;
+                    for (int r = 0; r < 4; ++r)
+                        if (r != cw) red[((cw * kTiles + rt) * 4 + r) * 32 + lane] = acc[rt][mt][r];
+                consumer_sync(kCThreads);
+                const int m = mt * 8 + 2 * (lane & 3) + (cw & 1);
 #pragma unroll
-                for (int w = 0; w < kStageGroups; ++w) v += red[((w * kTiles + rt) * 4 + r) * 32 + l];
-                const int m = mt * 8 + 2 * (l & 3) + (r & 1);
-                const int64_t n = row0 + rt * 16 + (l >> 2) + (r >= 2 ? 8 : 0);
-                if (!aborted && n < N && m < M) y[static_cast<int64_t>(m) * N + n] = __float2bfloat16_rn(v);
+                for (int rt = 0; rt < TPW; ++rt) {
+                    const float own = cw == 0 ? acc[rt][mt][0]
+                                    : cw == 1 ? acc[rt][mt][1]
+                                    : cw == 2 ? acc[rt][mt][2]
+                                              : acc[rt][mt][3];
+                    float v = 0.0f;
+#pragma unroll
+                    for (int w = 0; w < kStageGroups; ++w) v += w == cw ? own : red[((w * kTiles + rt) * 4 + cw) * 32 + lane];
+                    const int64_t n = row0 + rt * 16 + (lane >> 2) + (cw >= 2 ? 8 : 0);
+                    if (!aborted && n < N && m < M) y[static_cast<int64_t>(m) * N + n] = __float2bfloat16_rn(v);
+                }
+            } else {
+#pragma unroll
+                for (int rt = 0; rt < TPW; ++rt)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) red[((cw * kTiles + tile0 + rt) * 4 + r) * 32 + lane] = acc[rt][mt][r];
+                consumer_sync(kCThreads);
+                for (int e = ctid; e < kTiles * 4 * 32; e += kCThreads) {
+                    const int l = e & 31;
+                    const int r = (e >> 5) & 3;
+                    const int rt = e >> 7;
+                    float v = 0.0f;
+#pragma unroll
+                    for (int w = 0; w < kStageGroups; ++w) v += red[((w * kTiles + rt) * 4 + r) * 32 + l];
+                    const int m = mt * 8 + 2 * (l & 3) + (r & 1);
+                    const int64_t n = row0 + rt * 16 + (l >> 2) + (r >= 2 ? 8 : 0);
+                    if (!aborted && n < N && m < M) y[static_cast<int64_t>(m) * N + n] = __float2bfloat16_rn(v);
+                }
             }
         }
     }
