@@ -92,6 +92,24 @@ def test_grouped_unaligned_scales(cuda_lib):
         assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
 
 
+def test_grouped_three_ctas_per_sm_ragged_groups(cuda_lib):
+    """A plan of many equal items (64 problems × 5 row blocks) runs three CTAs
+    per SM, where the producer warp stages the scales; K = 128·(9..12) gives
+    rows whose scales are loaded element by element (groups not a multiple of
+    four) as well as in 8-byte loads. Every problem within the parity bound."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    shapes = [(320, 128 * (9 + i % 4)) for i in range(64)]
+    Ws, probs, bufs = make_problems(cuda_lib, shapes, [1 + i % 2 for i in range(64)], seed=21)
+    plan = w4.w4_grouped_plan(probs)
+    assert plan.plan.ctas > 2 * sms, plan.plan.ctas
+    w4.w4_gemm_grouped(plan)
+    torch.cuda.synchronize()
+    assert w4.w4_last_device_status() == 0
+    for W, (x, _, _, y), b in zip(Ws, probs, bufs):
+        assert guards_intact(b), "grouped matmul wrote outside an output"
+        check_gemm(W, x, y)
+
+
 @pytest.mark.parametrize("Ms", [[17, 33, 64, 208, 100, 257, 19], [1, 40, 13, 208, 8, 24, 2],
                                 [32, 28, 1, 5, 64, 25, 33]])
 def test_grouped_tensor_and_mixed(cuda_lib, Ms):
